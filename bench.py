@@ -1,0 +1,411 @@
+"""Throughput of the Engram layer on GB300, one JSON line on stdout.
+
+Workload: prefill, B=1 sequence of T=4096 tokens through two independent
+Engram layers (layer ids 1 and 15): N=3 (orders 2, 3), K=8 heads per order,
+64-dim bf16 rows (d_mem = 1024), 16 prime-sized tables of ~646400 rows per
+layer (10344164 rows, 1.32 GB per layer), hidden d = 1024, conv w=4 dilation 3.
+It mirrors the demo run of the Ascend RecSDK Engram blog (seq 4096, max n-gram
+3, 8 heads, 512 per n-gram, layers 1 and 15).  Inputs are seeded synthetic
+(Zipf(1.1) ids over 129280 with 5% repeated 16-token spans).
+
+A step is one pass of the whole layer path (hash, gather, K/V projection,
+gate, conv + residual) over the batch, for both layers.  ``value`` is
+token-layers per second (tokens x layers / step time) with inputs resident in
+HBM; the L2 is flushed (a 256 MiB write) between timed steps.  ``e2e`` is the
+same metric through the public API with the ids and H copied from pinned host
+memory and H copied back every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer needs no exchange between GPUs); value = all ranks' tokens / the
+slowest rank's time.  ``--impl reference`` times the CPU oracle on the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Engram-layer tokens/s at B=1,T=4096; gather HBM GB/s and % of peak"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def workload_desc(w) -> dict:
+    return {"workload": f"{w.name}: B={w.B} T={w.T}, {len(w.layers)} independent Engram layers "
+                        f"(ids {', '.join(map(str, w.layers))}), N={w.N} K={w.K}, {w.row_dim}-dim {w.table_dtype} rows, "
+                        f"d={w.d}, conv w={w.conv_w} dilation {w.conv_dil}",
+            "tokens_per_step": w.ntok, "layers": len(w.layers), "global_batch": w.B, "seq_len": w.T,
+            "parallelism": "replicas", "l2": "flushed between timed steps (256 MiB write)"}
+
+
+# --------------------------------------------------------------------------- #
+# distributed helpers (replicas)
+# --------------------------------------------------------------------------- #
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Slowest rank's value (a host timing reduction, not a data-path collective)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region
+# --------------------------------------------------------------------------- #
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_uuid: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_uuid, "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- #
+# algorithmic work per token per layer (bytes or flops), per kernel
+# --------------------------------------------------------------------------- #
+def per_token_work(w) -> dict:
+    act = 2 if w.act_dtype == "bf16" else 4
+    row_bytes = w.row_dim * {"f32": 4, "bf16": 2, "i8": 1}[w.table_dtype]
+    nc = (w.M + 1) * w.d
+    return {
+        "hash": ("bytes", 4 + 4 + 4 * w.R),                                  # id, P[id], R indices out
+        "gather": ("bytes", w.R * row_bytes + 4 * w.R + act * w.d_mem),      # rows in, idx in, e out
+        "kv_projection": ("flops", 2 * w.d_mem * nc),                        # one GEMM, all branches
+        "fusion": ("bytes", act * nc + act * w.M * w.d                        # gate: kv + H in, scalars out
+                   + 8 * w.M + act * w.d + 2 * act * w.M * w.d + 8 * w.M),    # conv: v + H in, H out, scalars
+    }
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+def run_ours(args) -> None:
+    import numpy as np
+    import torch
+    import workloads as W
+    from hashed_gram_embedding_engram_gb300 import EngramLayer
+    from tests.gpu_helpers import make_layer, to_torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.PREFILL_BF16
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    tc_peak = peaks.get("bf16_tflops", 1900.0)
+    peak_src = "measured" if peaks else "fallback"
+
+    ids_np = W.token_stream(w, key="tokens" if rank == 0 else f"tokens-rank{rank}")
+    P = W.projection_map(w)
+    layers = []
+    for lid in w.layers:
+        L = W.layer_inputs(w, lid)
+        plan, weights, proj, H = make_layer(w, L, P, w.ntok)
+        layers.append({"plan": plan, "weights": weights, "proj": proj, "H0": H, "H": H.clone(),
+                       "ws": plan.new_workspace(w.ntok), "H_host": to_torch(L.H, "bf16", "cpu", pin=True)})
+        del L
+    ids = torch.from_numpy(ids_np).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for ly in layers:
+            ly["plan"].forward(ids, ly["proj"], ly["weights"], ly["H"], None, ly["ws"])
+
+    def restore():
+        for ly in layers:
+            ly["H"].copy_(ly["H0"])
+
+    # ---- warm-up (also sets kernel attributes before capture) ----
+    for _ in range(max(1, args.warmup)):
+        restore()
+        step()
+    torch.cuda.synchronize()
+    for ly in layers:
+        st, flags = ly["plan"].get_error()
+        assert st == 0, f"device error flags {flags}"
+
+    # ---- capture one step in a CUDA graph ----
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, L2 flushed (untimed) between them ----
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        restore()
+        flush.zero_()
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_per_step = max_over_ranks(sum(step_ms) / K, world, dev)
+    tokens_per_step = w.ntok * len(w.layers)
+    value = world * tokens_per_step / (ms_per_step / 1e3)
+    for ly in layers:
+        st, flags = ly["plan"].get_error()
+        assert st == 0, f"device error flags {flags}"
+
+    # ---- per-kernel durations, same work, component entry points on the same stream ----
+    Kb = min(K, 200)
+    names = ["hash", "gather", "kv_projection", "fusion"]
+    dur = {n: [] for n in names}
+    for i in range(Kb):
+        restore()
+        flush.zero_()
+        for ly in layers:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            plan, wts = ly["plan"], ly["weights"]
+            ws = ly["ws"]
+            e[0].record(stream)
+            idx = plan.hash(ids, ly["proj"], out=ly.setdefault("idx", torch.empty(w.ntok, w.R, dtype=torch.int32,
+                                                                               device=dev)))
+            e[1].record(stream)
+            ebuf = plan.gather(idx, wts.table, wts.scales, out=ly.setdefault(
+                "e", torch.empty(w.ntok, w.d_mem, dtype=torch.bfloat16, device=dev)))
+            e[2].record(stream)
+            kv = plan.kv_projection(ebuf, wts.w_kv, out=ly.setdefault(
+                "kv", torch.empty(w.ntok, (w.M + 1) * w.d, dtype=torch.bfloat16, device=dev)))
+            e[3].record(stream)
+            plan.fusion(kv, wts, ly["H"], ws)
+            e[4].record(stream)
+            ly.setdefault("events", []).append(e)
+    torch.cuda.synchronize()
+    for ly in layers:
+        for e in ly.pop("events"):
+            for j, n in enumerate(names):
+                dur[n].append(e[j].elapsed_time(e[j + 1]))
+    work = per_token_work(w)
+    kernels = {}
+    for n in names:
+        ms = sum(dur[n]) / len(dur[n])
+        kind, per_tok = work[n]
+        amount = per_tok * w.ntok
+        if kind == "flops":
+            ach = amount / (ms / 1e3) / 1e12
+            kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 2), "unit": "TFLOP/s",
+                          "peak": tc_peak, "frac": round(ach / tc_peak, 4), "bound": "tensor"}
+        else:
+            ach = amount / (ms / 1e3) / 1e9
+            kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 1), "unit": "GB/s",
+                          "peak": hbm_peak, "frac": round(ach / hbm_peak, 4), "bound": "hbm"}
+    top = max(names, key=lambda n: kernels[n]["ms"])
+    kt = kernels[top]
+    roofline = {"kernel": top, "bound": kt["bound"], "achieved": kt["achieved"], "peak": kt["peak"],
+                "unit": kt["unit"], "frac": kt["frac"], "traffic": None,
+                "peak_source": f"{peak_src} ({'bf16_tflops burst' if kt['bound'] == 'tensor' else 'hbm_gbs'})",
+                "algorithmic_per_token": work[top][1], "units_per_launch": w.ntok}
+
+    # ---- end to end through the public API: pinned host in, pinned host out ----
+    e2e_layers = [EngramLayer(ly["plan"], ly["weights"], ly["proj"]) for ly in layers]
+    ids_host = torch.from_numpy(ids_np).pin_memory()
+    H_out = [ly["H_host"].clone().pin_memory() for ly in layers]
+    Ke = min(K, 200)
+    for _ in range(3):
+        for lay, ly, ho in zip(e2e_layers, layers, H_out):
+            ho.copy_(ly["H_host"])
+            lay(ids_host, ho)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(Ke):
+        for ly, ho in zip(layers, H_out):
+            ho.copy_(ly["H_host"])                     # fresh input, host side, untimed
+        flush.zero_()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for lay, ho in zip(e2e_layers, H_out):
+            lay(ids_host, ho)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_step = max_over_ranks(sum(e2e_ms) / Ke, world, dev)
+    h2d = len(layers) * (ids_host.numel() * 4 + layers[0]["H_host"].numel() * 2)
+    d2h = len(layers) * layers[0]["H_host"].numel() * 2
+    e2e = {"value": round(world * tokens_per_step / (e2e_step / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_step, 5),
+           "path": "EngramLayer.__call__ (pinned host ids/H -> device -> engram_forward -> host)"}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_subprocess(w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": dict(workload_desc(w), cuda_graph=True), "roofline": roofline, "kernels": kernels,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * 5 * len(layers), "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- #
+# the CPU oracle: baseline leg and reference arm
+# --------------------------------------------------------------------------- #
+def oracle_sample_seconds(T_sample: int, repeats: int = 1):
+    """Time the oracle on the first T_sample tokens of the workload, both layers.
+
+    Input generation is excluded; returns (seconds per pass, token-layers per pass)."""
+    import copy
+    import workloads as W
+    from oracle import engram_oracle as O
+    w = W.PREFILL_BF16
+    ids = W.token_stream(w)[:, :T_sample]
+    P = W.projection_map(w)
+    Ls = []
+    for lid in w.layers:
+        L = W.layer_inputs(w, lid)
+        Lc = copy.copy(L)
+        Lc.H = L.H[:, :T_sample]
+        Ls.append(Lc)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        for L in Ls:
+            O.forward(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype)
+        times.append(time.perf_counter() - t0)
+    return times, T_sample * len(w.layers)
+
+
+def cpu_baseline_subprocess(w) -> dict:
+    """Run the oracle in a child process with a known BLAS thread count."""
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads), CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "t, n = bench.oracle_sample_seconds(%d, 5); print(json.dumps({'t': t, 'n': n}))") % (ROOT, w.T)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # the baseline must never sink the GPU line
+        return {"value": None, "unit": UNIT, "cores": threads, "kind": "oracle", "error": str(exc)[:200]}
+    best = min(res["t"])
+    return {"value": round(res["n"] / best, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full workload ({w.T} tokens x {len(w.layers)} layers), float64 numpy oracle, "
+                      f"best of 5 passes ({best:.2f} s each), BLAS threads = {threads}, input generation excluded"}
+
+
+def run_reference(args) -> None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    w = W.PREFILL_BF16
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    # size each step's sample so that warm-up + steps take ~2 minutes
+    calib, n_cal = oracle_sample_seconds(256, 1)
+    per_tl = calib[0] / n_cal
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    T_s = int(max(16, min(w.T, budget / per_tl / len(w.layers))))
+    for _ in range(args.warmup):
+        oracle_sample_seconds(T_s, 1)
+    total, tl = 0.0, 0
+    for _ in range(args.steps):
+        t, n = oracle_sample_seconds(T_s, 1)
+        total += t[0]
+        tl += n
+    value = tl / total
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": dict(workload_desc(w), sample_tokens_per_layer=T_s),
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"first {T_s} tokens of the workload per step, both layers"},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

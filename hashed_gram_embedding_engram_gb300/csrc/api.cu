@@ -1,0 +1,330 @@
+// Host side of the C ABI: argument checks, the plan, workspace layout, dispatch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "engram_internal.h"
+
+using engram::PlanDev;
+
+namespace {
+
+constexpr uint64_t kU64Max = ~0ull;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+size_t act_bytes(engram_dtype_t t) { return t == ENGRAM_F32 ? 4 : 2; }
+
+size_t table_elem_bytes(engram_dtype_t t) {
+  switch (t) {
+    case ENGRAM_F32: return 4;
+    case ENGRAM_BF16: return 2;
+    default: return 1;
+  }
+}
+
+engram_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA; }
+
+// Resolve a pointer the kernels will dereference.  Device and managed memory
+// are used as is; pinned or registered host memory through its device alias;
+// pageable host memory is refused.
+engram_status_t device_view(const void* ptr, const void** out) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ENGRAM_ERR_NOT_MAPPED;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      *out = ptr;
+      return ENGRAM_OK;
+    case cudaMemoryTypeHost:
+      if (a.devicePointer == nullptr) return ENGRAM_ERR_NOT_MAPPED;
+      *out = a.devicePointer;
+      return ENGRAM_OK;
+    default:
+      return ENGRAM_ERR_NOT_MAPPED;
+  }
+}
+
+engram_status_t check_tokens(const engram_plan* p, int B, int T) {
+  if (B < 0 || T < 0) return ENGRAM_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * T > p->max_tokens) return ENGRAM_ERR_INVALID_ARG;
+  return ENGRAM_OK;
+}
+
+engram_status_t check_weights(const engram_plan* p, const engram_weights_t* w, bool need_table) {
+  if (!w) return ENGRAM_ERR_INVALID_ARG;
+  if (!w->w_kv || !w->g_h || !w->g_k || !w->g_c || !w->conv) return ENGRAM_ERR_INVALID_ARG;
+  if (!aligned16(w->w_kv) || !aligned16(w->g_h) || !aligned16(w->g_k) || !aligned16(w->g_c) ||
+      !aligned16(w->conv))
+    return ENGRAM_ERR_INVALID_ARG;
+  if (need_table) {
+    if (!w->table) return ENGRAM_ERR_INVALID_ARG;
+    if ((p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16) != (w->scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
+  }
+  return ENGRAM_OK;
+}
+
+engram_status_t check_state(const engram_plan* p, const engram_state_t* st) {
+  if (!st) return ENGRAM_OK;
+  if (!st->prev_ids || !st->u_ring || !st->pos) return ENGRAM_ERR_INVALID_ARG;
+  if (!aligned16(st->u_ring)) return ENGRAM_ERR_INVALID_ARG;
+  (void)p;
+  return ENGRAM_OK;
+}
+
+}  // namespace
+
+namespace engram {
+
+Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
+  Workspace w{};
+  const size_t ab = act_bytes(p->cfg.act_dtype);
+  const size_t M = p->cfg.M, d = p->cfg.d;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align_up(off + bytes, 256);
+    return base ? static_cast<char*>(base) + at : nullptr;
+  };
+  w.idx = reinterpret_cast<int32_t*>(take(static_cast<size_t>(ntok) * p->R * 4));
+  w.e = take(static_cast<size_t>(ntok) * p->d_mem * ab);
+  w.kv = take(static_cast<size_t>(ntok) * (M + 1) * d * ab);
+  w.alpha = reinterpret_cast<float*>(take(static_cast<size_t>(ntok) * M * 4));
+  w.rinv = reinterpret_cast<float*>(take(static_cast<size_t>(ntok) * M * 4));
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace engram
+
+extern "C" {
+
+const char* engram_status_string(engram_status_t s) {
+  switch (s) {
+    case ENGRAM_OK: return "ok";
+    case ENGRAM_ERR_INVALID_ARG: return "invalid argument";
+    case ENGRAM_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case ENGRAM_ERR_NOT_MAPPED: return "host pointer not mapped for device access (pin or register it)";
+    case ENGRAM_ERR_INDEX_RANGE: return "index out of range (row zero-filled)";
+    case ENGRAM_ERR_CUDA: return "CUDA runtime error";
+    case ENGRAM_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case ENGRAM_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_tokens, engram_plan_t** out) {
+  if (!cfg || !out) return ENGRAM_ERR_INVALID_ARG;
+  *out = nullptr;
+  const engram_config_t& c = *cfg;
+  if (c.N < 2 || c.N > engram::kMaxN || c.K < 1) return ENGRAM_ERR_INVALID_ARG;
+  const int R = (c.N - 1) * c.K;
+  if (R > engram::kMaxR) return ENGRAM_ERR_INVALID_ARG;
+  if (c.M < 1 || c.M > engram::kMaxM || c.d < 8 || c.d % 8) return ENGRAM_ERR_INVALID_ARG;
+  if (c.conv_w < 1 || c.conv_w > engram::kMaxConvW || c.conv_dilation < 1) return ENGRAM_ERR_INVALID_ARG;
+  if (!(c.eps > 0.f) || !std::isfinite(c.eps)) return ENGRAM_ERR_INVALID_ARG;
+  if (!c.primes || !c.multipliers) return ENGRAM_ERR_INVALID_ARG;
+  if (max_tokens <= 0 || max_tokens > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
+  if (c.row_dim < 1 || (static_cast<size_t>(c.row_dim) * table_elem_bytes(c.table_dtype)) % 16)
+    return ENGRAM_ERR_INVALID_ARG;
+  // table / activation pairs: copy f32->f32, bf16->bf16, dequant int8->bf16
+  const bool pair_ok = (c.table_dtype == ENGRAM_F32 && c.act_dtype == ENGRAM_F32) ||
+                       (c.table_dtype == ENGRAM_BF16 && c.act_dtype == ENGRAM_BF16) ||
+                       (c.table_dtype == ENGRAM_I8_ROWSCALE_F16 && c.act_dtype == ENGRAM_BF16);
+  if (!pair_ok) return ENGRAM_ERR_UNSUPPORTED;
+  const int d_mem = R * c.row_dim;
+  if (c.act_dtype == ENGRAM_BF16 && (d_mem % 64 || c.d % 32)) return ENGRAM_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(c.M + 1) * c.d > INT32_MAX / 2) return ENGRAM_ERR_INVALID_ARG;
+
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (major != 10 || minor != 3) return ENGRAM_ERR_UNSUPPORTED;   // built for sm_103a only
+
+  engram_plan* p = new (std::nothrow) engram_plan();
+  if (!p) return ENGRAM_ERR_CUDA;
+  p->cfg = c;
+  p->cfg.primes = nullptr;
+  p->cfg.multipliers = nullptr;
+  p->R = R;
+  p->d_mem = d_mem;
+  p->L_ring = (c.conv_w - 1) * c.conv_dilation;
+  p->max_tokens = max_tokens;
+  p->device = dev;
+  p->num_sms = sms;
+
+  PlanDev h{};
+  h.R = R;
+  h.N = c.N;
+  h.K = c.K;
+  int64_t rows = 0;
+  for (int r = 0; r < R; ++r) {
+    const uint32_t prime = c.primes[r];
+    if (prime < 2 || prime > static_cast<uint32_t>(INT32_MAX)) {
+      delete p;
+      return ENGRAM_ERR_INVALID_ARG;
+    }
+    h.primes[r] = prime;
+    h.mu[r] = kU64Max / prime;    // floor((2^64-1)/p): Barrett reciprocal (see hash.cu)
+    h.offsets[r] = rows;
+    rows += prime;
+    p->primes.push_back(prime);
+    p->offsets.push_back(h.offsets[r]);
+  }
+  p->total_rows = rows;
+  int base = 0;
+  for (int n = 2; n <= c.N; ++n) {
+    h.mult_base[n] = base;
+    base += c.K * n;
+  }
+  for (int i = 0; i < base; ++i) {
+    h.mults[i] = c.multipliers[i];
+    p->mults.push_back(c.multipliers[i]);
+  }
+  if (cudaMalloc(&p->dev, sizeof(PlanDev)) != cudaSuccess) {
+    delete p;
+    return ENGRAM_ERR_CUDA;
+  }
+  if (cudaMemcpy(p->dev, &h, sizeof(PlanDev), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(p->dev);
+    delete p;
+    return ENGRAM_ERR_CUDA;
+  }
+  *out = p;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_plan_destroy(engram_plan_t* plan) {
+  if (!plan) return ENGRAM_OK;
+  cudaError_t e = cudaFree(plan->dev);
+  delete plan;
+  return cuda_status(e);
+}
+
+engram_status_t engram_plan_workspace_bytes(const engram_plan_t* plan, int64_t ntok, size_t* bytes) {
+  if (!plan || !bytes || ntok < 0) return ENGRAM_ERR_INVALID_ARG;
+  *bytes = engram::carve_workspace(plan, ntok, nullptr).bytes;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_hash(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
+                            int V, const int32_t* prev_ids, int32_t* idx_out, engram_stream_t stream) {
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
+  if (!ids || !proj || !idx_out || V <= 0) return ENGRAM_ERR_INVALID_ARG;
+  return cuda_status(engram::launch_hash(plan, ids, B, T, proj, V, prev_ids, idx_out, (cudaStream_t)stream));
+}
+
+engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int64_t ntok, const void* table,
+                              const uint16_t* scales, void* e_out, engram_stream_t stream) {
+  if (!plan || ntok < 0 || ntok > plan->max_tokens) return ENGRAM_ERR_INVALID_ARG;
+  if (ntok == 0) return ENGRAM_OK;
+  if (!idx || !table || !e_out || !aligned16(e_out)) return ENGRAM_ERR_INVALID_ARG;
+  const bool i8 = plan->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
+  if (i8 != (scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
+  const void* tab = nullptr;
+  if (engram_status_t s = device_view(table, &tab)) return s;
+  if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
+  const void* sc = nullptr;
+  if (i8) {
+    if (engram_status_t s = device_view(scales, &sc)) return s;
+  }
+  return cuda_status(engram::launch_gather(plan, idx, ntok, tab, static_cast<const uint16_t*>(sc), e_out,
+                                           (cudaStream_t)stream));
+}
+
+engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok, const void* w_kv,
+                                     void* kv_out, engram_stream_t stream) {
+  if (!plan || ntok < 0 || ntok > plan->max_tokens) return ENGRAM_ERR_INVALID_ARG;
+  if (ntok == 0) return ENGRAM_OK;
+  if (!e || !w_kv || !kv_out || !aligned16(e) || !aligned16(w_kv) || !aligned16(kv_out))
+    return ENGRAM_ERR_INVALID_ARG;
+  return cuda_status(engram::launch_kv_projection(plan, e, ntok, w_kv, kv_out, (cudaStream_t)stream));
+}
+
+static engram_status_t run_fusion(const engram_plan_t* plan, const engram::Workspace& ws, const void* kv,
+                                  const int32_t* ids, const int32_t* proj, int V, int B, int T,
+                                  const engram_weights_t* w, void* H, engram_state_t* state, cudaStream_t s) {
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  cudaError_t e = engram::launch_gate(plan, kv, H, ntok, w->g_h, w->g_k, ws.alpha, ws.rinv, s);
+  if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+  e = engram::launch_conv_residual(plan, kv, ws.alpha, ws.rinv, B, T, w->g_c, w->conv, H, state, s);
+  if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (state) {
+    e = engram::launch_state_update(plan, ids, proj, V, kv, ws.alpha, ws.rinv, B, T, w->g_c, state, s);
+    if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+  }
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_fusion(const engram_plan_t* plan, const void* kv, int B, int T, const engram_weights_t* w,
+                              void* H, void* workspace, size_t workspace_bytes, engram_stream_t stream) {
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  if (ntok == 0) return ENGRAM_OK;
+  if (!kv || !H || !aligned16(kv) || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_weights(plan, w, false)) return s;
+  engram::Workspace ws = engram::carve_workspace(plan, ntok, workspace);
+  if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ENGRAM_ERR_WORKSPACE;
+  return run_fusion(plan, ws, kv, nullptr, nullptr, 0, B, T, w, H, nullptr, (cudaStream_t)stream);
+}
+
+engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
+                               int V, const engram_weights_t* w, void* H, engram_state_t* state, void* workspace,
+                               size_t workspace_bytes, engram_stream_t stream) {
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  if (ntok == 0) return ENGRAM_OK;
+  if (!ids || !proj || V <= 0 || !H || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_weights(plan, w, true)) return s;
+  if (engram_status_t s = check_state(plan, state)) return s;
+  engram::Workspace ws = engram::carve_workspace(plan, ntok, workspace);
+  if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ENGRAM_ERR_WORKSPACE;
+  const void* tab = nullptr;
+  if (engram_status_t s = device_view(w->table, &tab)) return s;
+  if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
+  const void* sc = nullptr;
+  if (w->scales) {
+    if (engram_status_t s = device_view(w->scales, &sc)) return s;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t* prev = state ? state->prev_ids : nullptr;
+  if (engram::launch_hash(plan, ids, B, T, proj, V, prev, ws.idx, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (engram::launch_gather(plan, ws.idx, ntok, tab, static_cast<const uint16_t*>(sc), ws.e, s) != cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  if (engram::launch_kv_projection(plan, ws.e, ntok, w->w_kv, ws.kv, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  return run_fusion(plan, ws, ws.kv, ids, proj, V, B, T, w, H, state, s);
+}
+
+engram_status_t engram_get_error(const engram_plan_t* plan, engram_stream_t stream, uint32_t* flags_out) {
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, &plan->dev->err, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(&plan->dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  if (flags_out) *flags_out = bits;
+  if (bits & engram::kErrTimeout) return ENGRAM_ERR_TIMEOUT;
+  if (bits & engram::kErrIndexRange) return ENGRAM_ERR_INDEX_RANGE;
+  return ENGRAM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Internal declarations shared by the host API and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/engram.h"
+
+namespace engram {
+
+constexpr int kMaxR = 64;          // (N-1)*K
+constexpr int kMaxMults = 320;     // sum_{n=2..N} K*n with (N-1)*K <= 64, N <= 8
+constexpr int kMaxN = 8;
+constexpr int kMaxConvW = 8;
+constexpr int kMaxM = 8;
+
+// bits of the device error word
+constexpr uint32_t kErrIndexRange = 1u;
+constexpr uint32_t kErrTimeout = 2u;
+
+// Device-resident parameter block of a plan.  Kernels copy what they need into
+// shared memory at start.
+struct PlanDev {
+  uint32_t err;                    // error word (atomicOr from kernels)
+  int32_t R;
+  int32_t N;
+  int32_t K;
+  uint32_t primes[kMaxR];          // rows of table r = (n-2)*K + k
+  uint64_t mu[kMaxR];              // floor(2^64 / p_r) for the Barrett remainder
+  int64_t offsets[kMaxR];          // first row of table r in the concatenated table
+  int32_t mult_base[kMaxN + 1];    // index of m_{n,0,0} in mults, per order n
+  uint64_t mults[kMaxMults];
+};
+
+}  // namespace engram
+
+struct engram_plan {
+  engram_config_t cfg;             // host copy; the two array pointers are cleared
+  int R;
+  int d_mem;
+  int L_ring;                      // (conv_w - 1) * conv_dilation
+  int64_t max_tokens;
+  int64_t total_rows;
+  int device;
+  int num_sms;
+  std::vector<uint32_t> primes;
+  std::vector<uint64_t> mults;
+  std::vector<int64_t> offsets;
+  engram::PlanDev* dev;            // device copy of the parameter block
+};
+
+namespace engram {
+
+// Workspace carve-up for engram_forward / engram_fusion, 256-byte aligned parts.
+struct Workspace {
+  int32_t* idx;      // [ntok, R]
+  void* e;           // [ntok, d_mem] act dtype
+  void* kv;          // [ntok, (M+1)d] act dtype
+  float* alpha;      // [ntok, M]
+  float* rinv;       // [ntok, M]   1/sqrt(mean(v~^2)+eps) of each gated row
+  size_t bytes;
+};
+Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base);
+
+// ---- launchers (each returns cudaGetLastError() after the launch) ----
+cudaError_t launch_hash(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                        const int32_t* prev_ids, int32_t* idx, cudaStream_t s);
+cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
+                          const uint16_t* scales, void* e, cudaStream_t s);
+cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
+                                 cudaStream_t s);
+cudaError_t launch_gate(const engram_plan* p, const void* kv, const void* H, int64_t ntok, const float* g_h,
+                        const float* g_k, float* alpha, float* rinv, cudaStream_t s);
+cudaError_t launch_conv_residual(const engram_plan* p, const void* kv, const float* alpha, const float* rinv,
+                                 int B, int T, const float* g_c, const float* conv, void* H,
+                                 const engram_state_t* state, cudaStream_t s);
+cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V,
+                                const void* kv, const float* alpha, const float* rinv, int B, int T,
+                                const float* g_c, const engram_state_t* state, cudaStream_t s);
+
+// bf16 GEMM on tcgen05: C[Mr, Nc] = A[Mr, Kd] . B[Nc, Kd]^T, all row-major bf16.
+cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,
+                              uint32_t* err, cudaStream_t s);
+// fp32 GEMM on the CUDA cores, same shapes.
+cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);
+
+}  // namespace engram

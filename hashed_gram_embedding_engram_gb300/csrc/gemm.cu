@@ -1,0 +1,356 @@
+// Step 5 of "DeepSeek Engram 系列导读", section "Engram 工作原理", Stage B:
+// k_t = W_K e_t, v_t = W_V e_t, computed for all branches as ONE GEMM
+//   kv[Mr, Nc] = e[Mr, Kd] . W_kv[Nc, Kd]^T,  Nc = (M+1)*d,  W_kv = [W_V; W_K^(1..M)],
+// the fusion that the page's section "多分支 backbone 上的变体" suggests for the
+// hyper-connection variant (it names FP8; this kernel runs bf16 -> fp32).
+//
+// sm_103a design (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: 128x64 A and BNx64 B tiles, 128-byte swizzle,
+//               into a kStages-deep shared-memory ring (mbarrier full/empty).
+//   warp 1      allocates TMEM (2 x BN fp32 columns: two accumulators) and one
+//               elected lane issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide
+//               K slice; tcgen05.commit frees ring stages and publishes tiles.
+//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, round
+//               to bf16, store; overlaps the MMA of the next tile (the
+//               accumulators ping-pong).
+// Every mbarrier wait is bounded in time: on expiry the kernel records
+// kErrTimeout, drains its own TMA loads and MMAs (again bounded), frees TMEM
+// and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "engram_internal.h"
+#include "ptx.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                        // one 128-byte swizzle atom of bf16
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: a healthy stage turns over in < 1 us
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN);
+};
+
+struct Bars {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* b, uint32_t* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&b->abort)) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrTimeout);
+      *reinterpret_cast<volatile int*>(&b->abort) = 1;
+      return false;
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     __nv_bfloat16* __restrict__ C, int Mr, int Nc, int Kd, uint32_t* __restrict__ err) {
+  using G = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + G::kStages * G::kStageBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (Mr + kBM - 1) / kBM;
+  const int n_tiles = (Nc + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int k_blocks = (Kd + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::kStages; ++s) {
+      ptx::mbar_init(&bars->full[s], 1);
+      ptx::mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&bars->tfull[a], 1);
+      ptx::mbar_init(&bars->tempty[a], 4);     // one arrive per epilogue warp
+    }
+    ptx::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&bars->tmem_base, G::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      const uint64_t keep = ptx::policy_evict_last();    // W_kv is re-read by every row tile
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;               // per stage: armed at least once / parity
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles) * kBM;
+        const int n0 = (tile % n_tiles) * BN;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!wait_or_abort(&bars->empty[stage], phase ^ 1, bars, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * G::kStageBytes;
+          ptx::mbar_arrive_expect_tx(&bars->full[stage], G::kStageBytes);
+          ptx::tma_load_2d_nohint(sa, &tmA, &bars->full[stage], kb * kBK, m0);
+          ptx::tma_load_2d(sa + G::kABytes, &tmB, &bars->full[stage], kb * kBK, n0, keep);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == G::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // our own copies in flight must land before the CTA can exit
+      for (int s = 0; s < G::kStages; ++s)
+        if (armed & (1u << s)) ptx::mbar_wait_bounded(&bars->full[s], (armed_parity >> s) & 1u, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!wait_or_abort(&bars->tempty[acc], acc_phase ^ 1, bars, err)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!wait_or_abort(&bars->full[stage], phase, bars, err)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(smem + stage * G::kStageBytes);
+          const uint32_t b_addr = a_addr + G::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + k * 32), ptx::sdesc_kmajor_sw128(b_addr + k * 32),
+                          G::kIdesc, (kb | k) != 0);
+          }
+          ptx::mma_commit(&bars->empty[stage]);
+          if (++stage == G::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&bars->tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // every MMA this thread issued has finished before TMEM is freed
+      ptx::mma_commit(&bars->drain);
+      ptx::mbar_wait_bounded(&bars->drain, 0, kWaitLimitNs);
+    }
+  } else {
+    // -------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile / n_tiles) * kBM;
+      const int n0 = (tile % n_tiles) * BN;
+      if (!wait_or_abort(&bars->tfull[acc], acc_phase, bars, err)) break;
+      ptx::tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(t_row + c, r);
+        ptx::tmem_ld_wait();
+        if (row < Mr && n0 + c < Nc) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            packed[j] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(C + static_cast<int64_t>(row) * Nc + n0 + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, G::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 [rows, cols] -> 2D map with a box of box_rows x 64 elements, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms, uint32_t* err,
+                cudaStream_t s) {
+  using G = Cfg<BN>;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, Mr, Kd, kBM) || !make_map(&tb, B, Nc, Kd, BN)) return cudaErrorInvalidValue;
+  static bool attr_set = false;   // per template instance; idempotent if raced
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t tiles = ((Mr + kBM - 1) / kBM) * ((Nc + BN - 1) / BN);
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  gemm_bf16_kernel<BN><<<grid, kThreads, G::kSmem, s>>>(ta, tb, static_cast<__nv_bfloat16*>(C), static_cast<int>(Mr),
+                                                       Nc, Kd, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fp32 (CUDA cores)
+constexpr int kFT = 64;   // output tile
+constexpr int kFK = 16;   // K step
+
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                                                       float* __restrict__ C, int Mr, int Nc, int Kd) {
+  __shared__ float sA[kFK][kFT + 1];
+  __shared__ float sB[kFK][kFT + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * kFT, n0 = blockIdx.x * kFT;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < Kd; k0 += kFK) {
+    for (int i = threadIdx.x; i < kFT * kFK; i += 256) {
+      const int rr = i / kFK, kk = i % kFK;
+      const int am = m0 + rr, bn = n0 + rr, k = k0 + kk;
+      sA[kk][rr] = (am < Mr && k < Kd) ? A[static_cast<int64_t>(am) * Kd + k] : 0.f;
+      sB[kk][rr] = (bn < Nc && k < Kd) ? B[static_cast<int64_t>(bn) * Kd + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kFK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = sA[kk][ty * 4 + i];
+        b[i] = sB[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+      if (m < Mr && n < Nc) C[static_cast<int64_t>(m) * Nc + n] = acc[i][j];
+    }
+}
+
+}  // namespace
+
+cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,
+                              uint32_t* err, cudaStream_t s) {
+  if (Nc % 32 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
+  const int64_t m_tiles = (Mr + kBM - 1) / kBM;
+  // widest tile that still gives every SM work
+  if (Nc % 256 == 0 && m_tiles * (Nc / 256) >= num_sms) return run<256>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
+  if (Nc % 128 == 0 && m_tiles * (Nc / 128) >= num_sms) return run<128>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
+  if (Nc % 64 == 0) return run<64>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
+  return run<128>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
+}
+
+cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s) {
+  dim3 grid((Nc + kFT - 1) / kFT, static_cast<unsigned>((Mr + kFT - 1) / kFT));
+  gemm_f32_kernel<<<grid, 256, 0, s>>>(A, B, C, static_cast<int>(Mr), Nc, Kd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
+                                 cudaStream_t s) {
+  const int Nc = (p->cfg.M + 1) * p->cfg.d;
+  if (p->cfg.act_dtype == ENGRAM_F32)
+    return gemm_f32_simt(static_cast<const float*>(e), static_cast<const float*>(w_kv), static_cast<float*>(kv), ntok,
+                         Nc, p->d_mem, s);
+  return gemm_bf16_tcgen05(e, w_kv, kv, ntok, Nc, p->d_mem, p->num_sms, &p->dev->err, s);
+}
+
+}  // namespace engram

@@ -1,0 +1,261 @@
+"""Python front end of the Engram C ABI: argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels (libengram_gb300.so);
+torch provides device memory and the current stream.  Tensors are passed by
+pointer; no tensor is copied or converted here except where a method says so
+(``EngramLayer.__call__`` moves host inputs to the device and back).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import _lib
+
+_TABLE_DTYPES = {"f32": (_lib.F32, torch.float32), "bf16": (_lib.BF16, torch.bfloat16),
+                 "i8": (_lib.I8_ROWSCALE_F16, torch.int8)}
+_ACT_DTYPES = {"f32": (_lib.F32, torch.float32), "bf16": (_lib.BF16, torch.bfloat16)}
+
+
+def _stream() -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype) -> int:
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name}: host tables must be pinned (read by the GPU over UVA)")
+    return t.data_ptr()
+
+
+@dataclass
+class EngramWeights:
+    """One layer's parameters (see engram_weights_t).  ``table`` / ``scales`` may be
+    pinned host tensors; everything else lives on the device."""
+    table: torch.Tensor            # [sum primes, row_dim]
+    w_kv: torch.Tensor             # [(M+1)d, d_mem]: W_V then W_K^(1..M)
+    g_h: torch.Tensor              # float32 [M, d]
+    g_k: torch.Tensor              # float32 [M, d]
+    g_c: torch.Tensor              # float32 [d]
+    conv: torch.Tensor             # float32 [d, w]
+    scales: Optional[torch.Tensor] = None   # float16 [sum primes] for int8 tables
+
+    def struct(self, plan: "EngramPlan", need_table: bool = True) -> _lib.Weights:
+        c = plan
+        tdt = _TABLE_DTYPES[c.table_dtype][1]
+        adt = _ACT_DTYPES[c.act_dtype][1]
+        w = _lib.Weights()
+        if need_table:
+            w.table = _dev_or_pinned(self.table, "table", tdt)
+            if self.table.shape != (c.total_rows, c.row_dim):
+                raise ValueError(f"table: shape {tuple(self.table.shape)}, expected {(c.total_rows, c.row_dim)}")
+            if c.table_dtype == "i8":
+                if self.scales is None:
+                    raise ValueError("int8 tables need fp16 row scales")
+                w.scales = _dev_or_pinned(self.scales, "scales", torch.float16)
+        w.w_kv = _dev(self.w_kv, "w_kv", adt, ((c.M + 1) * c.d, c.d_mem))
+        w.g_h = _dev(self.g_h, "g_h", torch.float32, (c.M, c.d))
+        w.g_k = _dev(self.g_k, "g_k", torch.float32, (c.M, c.d))
+        w.g_c = _dev(self.g_c, "g_c", torch.float32, (c.d,))
+        w.conv = _dev(self.conv, "conv", torch.float32, (c.d, c.conv_w))
+        return w
+
+
+@dataclass
+class EngramState:
+    """Streaming state of B sequences (see engram_state_t); zeros = fresh."""
+    prev_ids: torch.Tensor         # int32 [B, N-1]
+    u_ring: torch.Tensor           # float32 [B, L, M, d]
+    pos: torch.Tensor              # int32 [B]
+
+    @classmethod
+    def zeros(cls, plan: "EngramPlan", B: int, device="cuda") -> "EngramState":
+        L = max(1, (plan.conv_w - 1) * plan.conv_dilation)
+        return cls(torch.zeros(B, plan.N - 1, dtype=torch.int32, device=device),
+                   torch.zeros(B, L, plan.M, plan.d, dtype=torch.float32, device=device),
+                   torch.zeros(B, dtype=torch.int32, device=device))
+
+    def struct(self, plan: "EngramPlan", B: int) -> _lib.State:
+        L = max(1, (plan.conv_w - 1) * plan.conv_dilation)
+        s = _lib.State()
+        s.prev_ids = _dev(self.prev_ids, "prev_ids", torch.int32, (B, plan.N - 1))
+        s.u_ring = _dev(self.u_ring, "u_ring", torch.float32, (B, L, plan.M, plan.d))
+        s.pos = _dev(self.pos, "pos", torch.int32, (B,))
+        return s
+
+    def clone(self) -> "EngramState":
+        return EngramState(self.prev_ids.clone(), self.u_ring.clone(), self.pos.clone())
+
+
+class EngramPlan:
+    """A validated layer configuration bound to the current CUDA device."""
+
+    def __init__(self, *, N: int, K: int, row_dim: int, d: int, M: int = 1, conv_w: int = 4,
+                 conv_dilation: Optional[int] = None, table_dtype: str = "bf16", act_dtype: str = "bf16",
+                 eps: float = 1e-6, primes: Sequence[int], multipliers: Sequence[int], max_tokens: int):
+        self.N, self.K, self.row_dim, self.d, self.M = N, K, row_dim, d, M
+        self.conv_w = conv_w
+        self.conv_dilation = N if conv_dilation is None else conv_dilation
+        self.table_dtype, self.act_dtype, self.eps = table_dtype, act_dtype, eps
+        self.R = (N - 1) * K
+        self.d_mem = self.R * row_dim
+        self.primes = [int(p) for p in primes]
+        self.total_rows = sum(self.primes)
+        self.max_tokens = int(max_tokens)
+        if len(self.primes) != self.R:
+            raise ValueError(f"need {self.R} primes, got {len(self.primes)}")
+        n_mult = sum(K * n for n in range(2, N + 1))
+        mults = [int(m) for m in multipliers]
+        if len(mults) != n_mult:
+            raise ValueError(f"need {n_mult} multipliers, got {len(mults)}")
+        self._primes_c = (ctypes.c_uint32 * self.R)(*self.primes)
+        self._mults_c = (ctypes.c_uint64 * n_mult)(*mults)
+        cfg = _lib.Config(N, K, row_dim, d, M, conv_w, self.conv_dilation, _TABLE_DTYPES[table_dtype][0],
+                          _ACT_DTYPES[act_dtype][0], eps, self._primes_c, self._mults_c)
+        self._lib = _lib._lib()
+        self._h = ctypes.c_void_p()
+        torch.cuda.current_device()   # make sure a context exists on the current device
+        _lib.check(self._lib.engram_plan_create(ctypes.byref(cfg), self.max_tokens, ctypes.byref(self._h)),
+                   "engram_plan_create")
+
+    # ------------------------------------------------------------ helpers
+    @property
+    def act_torch_dtype(self) -> torch.dtype:
+        return _ACT_DTYPES[self.act_dtype][1]
+
+    def workspace_bytes(self, ntok: int) -> int:
+        n = ctypes.c_size_t()
+        _lib.check(self._lib.engram_plan_workspace_bytes(self._h, ntok, ctypes.byref(n)), "workspace_bytes")
+        return n.value
+
+    def new_workspace(self, ntok: int, device="cuda") -> torch.Tensor:
+        return torch.empty(max(1, self.workspace_bytes(ntok)), dtype=torch.uint8, device=device)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) and self._h.value:
+            self._lib.engram_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------ entry points
+    def hash(self, ids: torch.Tensor, proj: torch.Tensor, prev_ids: Optional[torch.Tensor] = None,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Steps 1-3: int32 ids [B, T] -> int32 indices [B*T, R]."""
+        B, T = ids.shape
+        if out is None:
+            out = torch.empty(B * T, self.R, dtype=torch.int32, device=ids.device)
+        prev = 0 if prev_ids is None else _dev(prev_ids, "prev_ids", torch.int32, (B, self.N - 1))
+        _lib.check(self._lib.engram_hash(self._h, _dev(ids, "ids", torch.int32), B, T,
+                                         _dev(proj, "proj", torch.int32), proj.numel(), prev,
+                                         _dev(out, "idx_out", torch.int32, (B * T, self.R)), _stream()),
+                   "engram_hash")
+        return out
+
+    def gather(self, idx: torch.Tensor, table: torch.Tensor, scales: Optional[torch.Tensor] = None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Step 4: int32 indices [ntok, R] -> e [ntok, d_mem] (act dtype)."""
+        ntok = idx.shape[0]
+        if out is None:
+            out = torch.empty(ntok, self.d_mem, dtype=self.act_torch_dtype, device=idx.device)
+        tab = _dev_or_pinned(table, "table", _TABLE_DTYPES[self.table_dtype][1])
+        sc = 0 if scales is None else _dev_or_pinned(scales, "scales", torch.float16)
+        _lib.check(self._lib.engram_gather(self._h, _dev(idx, "idx", torch.int32, (ntok, self.R)), ntok, tab, sc,
+                                           _dev(out, "e_out", self.act_torch_dtype, (ntok, self.d_mem)), _stream()),
+                   "engram_gather")
+        return out
+
+    def kv_projection(self, e: torch.Tensor, w_kv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Step 5: e [ntok, d_mem] -> kv [ntok, (M+1)d] = e . w_kv^T."""
+        ntok = e.shape[0]
+        nc = (self.M + 1) * self.d
+        if out is None:
+            out = torch.empty(ntok, nc, dtype=self.act_torch_dtype, device=e.device)
+        _lib.check(self._lib.engram_kv_projection(
+            self._h, _dev(e, "e", self.act_torch_dtype, (ntok, self.d_mem)), ntok,
+            _dev(w_kv, "w_kv", self.act_torch_dtype, (nc, self.d_mem)),
+            _dev(out, "kv_out", self.act_torch_dtype, (ntok, nc)), _stream()), "engram_kv_projection")
+        return out
+
+    def fusion(self, kv: torch.Tensor, weights: EngramWeights, H: torch.Tensor,
+               workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Steps 6-8 in place on H [B, T, M, d] from kv [B*T, (M+1)d]."""
+        B, T = H.shape[0], H.shape[1]
+        ws = self.new_workspace(B * T, H.device) if workspace is None else workspace
+        w = weights.struct(self, need_table=False)
+        _lib.check(self._lib.engram_fusion(
+            self._h, _dev(kv, "kv", self.act_torch_dtype, (B * T, (self.M + 1) * self.d)), B, T, ctypes.byref(w),
+            _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), _dev(ws, "workspace"), ws.numel(),
+            _stream()), "engram_fusion")
+        return H
+
+    def forward(self, ids: torch.Tensor, proj: torch.Tensor, weights: EngramWeights, H: torch.Tensor,
+                state: Optional[EngramState] = None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Steps 1-8 in place on H [B, T, M, d]; ``state`` continues sequences."""
+        B, T = ids.shape
+        ws = self.new_workspace(B * T, H.device) if workspace is None else workspace
+        w = weights.struct(self)
+        st = None if state is None else ctypes.byref(state.struct(self, B))
+        _lib.check(self._lib.engram_forward(
+            self._h, _dev(ids, "ids", torch.int32), B, T, _dev(proj, "proj", torch.int32), proj.numel(),
+            ctypes.byref(w), _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), st,
+            _dev(ws, "workspace"), ws.numel(), _stream()), "engram_forward")
+        return H
+
+    def get_error(self) -> Tuple[int, int]:
+        """Synchronise the current stream; return (status, raw flag bits) and clear them."""
+        flags = ctypes.c_uint32()
+        st = self._lib.engram_get_error(self._h, _stream(), ctypes.byref(flags))
+        return st, flags.value
+
+
+class EngramLayer:
+    """A plan, its weights, the projection map and a reusable workspace.
+
+    Calling it runs the whole layer; inputs on the host are copied to the
+    device on the current stream and H is copied back into the caller's host
+    tensor (use pinned host tensors for asynchronous copies)."""
+
+    def __init__(self, plan: EngramPlan, weights: EngramWeights, proj: torch.Tensor):
+        self.plan, self.weights, self.proj = plan, weights, proj
+        self._ws = None
+
+    def workspace(self, ntok: int, device) -> torch.Tensor:
+        need = self.plan.workspace_bytes(ntok)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(1, need), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, ids: torch.Tensor, H: torch.Tensor, state: Optional[EngramState] = None) -> torch.Tensor:
+        dev = self.proj.device
+        ids_d = ids if ids.is_cuda else ids.to(dev, non_blocking=True)
+        H_d = H if H.is_cuda else H.to(dev, non_blocking=True)
+        self.plan.forward(ids_d, self.proj, self.weights, H_d, state, self.workspace(ids.numel(), dev))
+        if not H.is_cuda:
+            H.copy_(H_d, non_blocking=True)
+            return H
+        return H_d

@@ -1,0 +1,192 @@
+/*
+ * engram.h -- C ABI of the GB300 (sm_103a) Engram conditional-memory forward path.
+ *
+ * The operation is the one described in "DeepSeek Engram 系列导读"
+ * (foosynaptic.github.io, deepseek-tech-notes, chapter 07-Engram), section
+ * "Engram 工作原理":
+ *   Stage A (deterministic retrieval)
+ *     Step 1  x'_t = P(x_t)                               vocabulary projection
+ *     Step 2  g_{t,n} = (x'_{t-n+1}, ..., x'_t), n=2..N   suffix n-grams
+ *     Step 3  z_{t,n,k} = phi_{n,k}(g_{t,n})              K multiplicative-XOR heads per order
+ *     Step 4  e_t = concat_{n,k} E_{n,k}[z_{t,n,k}]       row gather + concat
+ *   Stage B (context-aware gating and fusion)
+ *     Step 5  k_t = W_K e_t,  v_t = W_V e_t
+ *     Step 6  alpha_t = sigma(RMSNorm(h_t) . RMSNorm(k_t) / sqrt(d)),  v~_t = alpha_t v_t
+ *     Step 7  Y = SiLU(Conv1D_{w, dilation N}(RMSNorm(V~))) + V~   (depthwise, causal)
+ *     Step 8  H <- H + Y
+ * and, for M hyper-connection branches, its section "多分支 backbone 上的变体":
+ * a gate per branch from h^(m) and W_K^(m) e_t, a value W_V e_t shared by all.
+ * Int8 tables with a per-row scale, read from HBM or from pinned host memory
+ * by the same gather kernel, follow "Engram 嵌入扩展：面向高效 DRAM/SSD 卸载的
+ * 协同设计" (web.reeddaily.com), section "AgentX Engram DRAM卸载提升性能".
+ *
+ * Concrete choices the pages leave open (hash form, window order, pad id,
+ * RMSNorm form, conv layout):
+ *   h = XOR_{i=0}^{n-1} (x'_{t-i} * m_{n,k,i})  (mod 2^64, unsigned)
+ *   z = h mod p_{n,k}                            (p_{n,k} the table's row count)
+ *   x'_{t-i} = 0 (pad) before the first token of a sequence
+ *   RMSNorm(x) = x / sqrt(mean(x^2) + eps) * g   (one weight vector per use)
+ *   conv tap j multiplies the input at lag (w-1-j)*dilation (PyTorch depthwise
+ *   Conv1d layout), no bias, zeros before the sequence start.
+ *
+ * Conventions for every entry point
+ *   - Every call is asynchronous and stream-ordered on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream).  Argument checks run on
+ *     the host before any launch; a failed check launches nothing.
+ *   - The caller owns every buffer and the stream.  The library owns only the
+ *     plan: its small device parameter block and a device error word.
+ *   - Arrays are dense, row-major, and (unless stated) in device memory.  Device
+ *     pointers handed to the 16-byte vector paths must be 16-byte aligned.
+ *   - No exception crosses the ABI.  A status code is returned; errors found
+ *     inside kernels (an index out of range, a wait that timed out) are
+ *     recorded in the plan's error word and reported by engram_get_error.
+ *   - Indices are int32: every table has fewer than 2^31 rows.
+ *   - Calls on one plan may run concurrently on different streams only if they
+ *     write disjoint buffers.
+ */
+#ifndef ENGRAM_GB300_H
+#define ENGRAM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* engram_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  ENGRAM_OK = 0,
+  ENGRAM_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad config */
+  ENGRAM_ERR_UNSUPPORTED = 2,   /* valid but outside what this build implements */
+  ENGRAM_ERR_NOT_MAPPED = 3,    /* a host pointer the GPU cannot address (not pinned/registered) */
+  ENGRAM_ERR_INDEX_RANGE = 4,   /* a gather index >= its table's row count (row zero-filled) */
+  ENGRAM_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  ENGRAM_ERR_TIMEOUT = 6,       /* a bounded in-kernel wait gave up (results invalid) */
+  ENGRAM_ERR_WORKSPACE = 7      /* workspace missing or smaller than engram_plan_workspace_bytes */
+} engram_status_t;
+
+typedef enum {
+  ENGRAM_F32 = 0,               /* IEEE binary32 */
+  ENGRAM_BF16 = 1,              /* bfloat16 */
+  ENGRAM_I8_ROWSCALE_F16 = 2    /* table only: int8 rows + one fp16 scale per row */
+} engram_dtype_t;
+
+/* Layer configuration.  The two host arrays are copied by engram_plan_create. */
+typedef struct {
+  int N;                        /* max n-gram order; orders 2..N.  2 <= N <= 8 */
+  int K;                        /* hash heads per order.  1 <= K, (N-1)*K <= 64 */
+  int row_dim;                  /* elements per table row; row bytes a multiple of 16 */
+  int d;                        /* hidden size; multiple of 8 (bf16) / 4 (f32) */
+  int M;                        /* hyper-connection branches, 1 <= M <= 8 */
+  int conv_w;                   /* conv taps, 1 <= conv_w <= 8 */
+  int conv_dilation;            /* >= 1 (the pages use the max order N) */
+  engram_dtype_t table_dtype;   /* F32, BF16 or I8_ROWSCALE_F16 */
+  engram_dtype_t act_dtype;     /* F32 or BF16: H, W_kv, e and the k/v buffer */
+  float eps;                    /* RMSNorm epsilon, > 0 */
+  const uint32_t* primes;       /* host [R = (N-1)*K]: rows of E_{n,k}, index (n-2)*K + k */
+  const uint64_t* multipliers;  /* host [sum_{n=2..N} K*n]: m_{n,k,i} at
+                                   sum_{n'<n} K*n' + k*n + i; any 64-bit values */
+} engram_config_t;
+
+typedef struct engram_plan engram_plan_t;
+
+/* Per-layer parameters.  `table` is the concatenation of the R tables E_{n,k}
+ * in (n, k) n-major order: table r starts at row sum_{r'<r} primes[r'].
+ * `table` (and `scales`) may be device memory or pinned/registered host memory
+ * (read over UVA: NVLink-C2C on Grace-Blackwell).  All others are device. */
+typedef struct {
+  const void* table;            /* [sum primes, row_dim] in table_dtype */
+  const uint16_t* scales;       /* fp16 [sum primes] for I8 tables, else NULL */
+  const void* w_kv;             /* act_dtype [(M+1)*d, d_mem], d_mem = R*row_dim:
+                                   rows [0,d) = W_V, rows [(1+m)d, (2+m)d) = W_K^(m) */
+  const float* g_h;             /* [M, d] RMSNorm weight on h, per branch */
+  const float* g_k;             /* [M, d] RMSNorm weight on k, per branch */
+  const float* g_c;             /* [d]    RMSNorm weight on v~ before the conv (shared) */
+  const float* conv;            /* [d, conv_w] depthwise taps (shared by branches) */
+} engram_weights_t;
+
+/* Streaming state of B sequences (decode, chunked prefill).  Owned by the
+ * caller, zero-initialised for fresh sequences, updated in place by
+ * engram_forward after the chunk.  L = (conv_w - 1) * conv_dilation. */
+typedef struct {
+  int32_t* prev_ids;            /* [B, N-1] projected ids before the chunk, oldest first (0 = pad) */
+  float* u_ring;                /* [B, L, M, d] conv inputs RMSNorm(v~)*g_c of the last L
+                                   positions; position p lives in slot p mod L */
+  int32_t* pos;                 /* [B] tokens already processed per sequence */
+} engram_state_t;
+
+/* Human-readable name of a status code (static string). */
+const char* engram_status_string(engram_status_t s);
+
+/* Validate `cfg`, copy its primes/multipliers, precompute per-table reduction
+ * constants and row offsets, and allocate the plan's device block on the
+ * current device.  `max_tokens` bounds B*T of later calls (> 0). */
+engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_tokens, engram_plan_t** out);
+
+/* Free the plan (after all its work has finished).  NULL is accepted. */
+engram_status_t engram_plan_destroy(engram_plan_t* plan);
+
+/* Bytes of device workspace engram_forward needs for `ntok` = B*T tokens. */
+engram_status_t engram_plan_workspace_bytes(const engram_plan_t* plan, int64_t ntok, size_t* bytes);
+
+/* Steps 1-3.  ids: int32 [B, T] raw token ids in [0, V); proj: int32 [V]
+ * canonical ids P; prev_ids: int32 [B, N-1] projected ids that precede
+ * position 0 of each sequence, oldest first, or NULL for fresh sequences (pad 0).
+ * idx_out: int32 [B*T, R], head (n,k) in column (n-2)*K + k, value in [0, p_{n,k}).
+ * Raw ids outside [0, V) are an argument error the kernel cannot see; they are
+ * clamped to 0 and flagged as ENGRAM_ERR_INDEX_RANGE. */
+engram_status_t engram_hash(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                            const int32_t* proj, int V, const int32_t* prev_ids,
+                            int32_t* idx_out, engram_stream_t stream);
+
+/* Step 4.  idx: int32 [ntok, R] from engram_hash.  e_out: [ntok, d_mem] in
+ * act_dtype, segment (n,k) at columns [r*row_dim, (r+1)*row_dim), r=(n-2)K+k.
+ * Copies rows (F32 -> F32, BF16 -> BF16), or dequantises I8 rows as
+ * bf16(q * scale) with one rounding (the product is exact in binary32).
+ * An index >= p_r writes a zero row and flags ENGRAM_ERR_INDEX_RANGE.
+ * Host tables must be cudaHostAlloc'd or cudaHostRegister'd: otherwise
+ * ENGRAM_ERR_NOT_MAPPED. */
+engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int64_t ntok,
+                              const void* table, const uint16_t* scales, void* e_out,
+                              engram_stream_t stream);
+
+/* Step 5.  e: [ntok, d_mem] act_dtype; w_kv as in engram_weights_t;
+ * kv_out: [ntok, (M+1)*d] act_dtype = e . w_kv^T (fp32 accumulation), columns
+ * [0,d) = v, [(1+m)d, (2+m)d) = k^(m).  BF16 runs on the tcgen05 tensor cores. */
+engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok,
+                                     const void* w_kv, void* kv_out, engram_stream_t stream);
+
+/* Steps 6-8 from a k/v buffer, for fresh sequences (streaming continuation
+ * goes through engram_forward, which also has the token ids the state needs).
+ * kv: [B*T, (M+1)*d] as from engram_kv_projection; w: only w_kv is ignored
+ * and table/scales may be NULL; H: [B, T, M, d] act_dtype, updated in place.
+ * The per-token gate scalars are kept in `workspace`
+ * (engram_plan_workspace_bytes(plan, B*T) bytes, 256-B aligned, suffice). */
+engram_status_t engram_fusion(const engram_plan_t* plan, const void* kv, int B, int T,
+                              const engram_weights_t* w, void* H,
+                              void* workspace, size_t workspace_bytes, engram_stream_t stream);
+
+/* Steps 1-8: the whole layer for B sequences of T new tokens each.
+ * ids/proj/V as in engram_hash; w as in engram_weights_t; H: [B, T, M, d]
+ * act_dtype, updated in place; state: NULL or engram_state_t (prev_ids is then
+ * used instead of the pad, and u_ring/pos supply the convolution's history).
+ * workspace: device, >= engram_plan_workspace_bytes(plan, B*T), 256-B aligned.
+ * Capturable in a CUDA graph (no allocation, no synchronisation). */
+engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                               const int32_t* proj, int V, const engram_weights_t* w,
+                               void* H, engram_state_t* state,
+                               void* workspace, size_t workspace_bytes, engram_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the plan's device error word.
+ * Returns ENGRAM_OK, ENGRAM_ERR_INDEX_RANGE or ENGRAM_ERR_TIMEOUT (the first
+ * set, in that order of precedence reversed: TIMEOUT wins).  `flags_out`
+ * (optional) receives the raw bits: 1 = index range, 2 = timeout. */
+engram_status_t engram_get_error(const engram_plan_t* plan, engram_stream_t stream, uint32_t* flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_GB300_H */

@@ -1,0 +1,243 @@
+"""GPU path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Indices and gathered rows: bit-exact.  Layer outputs: max-abs 2e-2 and
+relative L2 5e-3 for bf16 (fp32 accumulation), tighter for the fp32 workload.
+Small cases span several 128-row GEMM tiles with ragged tails and run the
+oracle in full; the full-size workloads are checked in full for the integer
+work and on sampled positions (every sequence start included) for the layer
+output, via the oracle's windowed evaluator.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import engram_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from tests.gpu_helpers import act_to_f64, assert_close, bf16_bits, make_layer, to_torch  # noqa: E402
+
+
+SMALL = {
+    "tiny_f32": W.TINY_F32,
+    "small_bf16": W.PREFILL_BF16.scaled(B=3, T=333, V=5000, V_proj=3850, prime_target=4001, d=256),
+    "small_i8": W.INT8_HOST.scaled(B=2, T=300, V=5000, V_proj=3850, prime_target=3001, d=256, span_copies=3),
+    "small_multibranch": W.MULTIBRANCH_N4.scaled(B=2, T=257, V=5000, V_proj=3850, prime_target=2003, d=256,
+                                                 span_copies=3),
+}
+
+
+def oracle_forward(w, ids, P, L, state=None):
+    return O.forward(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype, state)
+
+
+def expected_e_bits(w, z, L):
+    """What the gather must write, exactly: the stored rows (copy) or bf16(q*s)."""
+    e = O.gather_concat(z, L.tables(), w.table_dtype, L.table_scales())
+    if w.table_dtype == "f32":
+        return e.astype(np.float32)
+    if w.table_dtype == "bf16":
+        return O.f64_to_bf16_bits(e)
+    return O.f64_to_bf16_bits(e)
+
+
+def gpu_e_bits(w, e):
+    return e.cpu().numpy() if w.table_dtype == "f32" else bf16_bits(e)
+
+
+@pytest.fixture(scope="module", params=list(SMALL))
+def small(request):
+    w = SMALL[request.param]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, w.layers[0])
+    ref = oracle_forward(w, ids, P, L)
+    return request.param, w, ids, P, L, ref
+
+
+def test_small_hash_bitexact(small):
+    name, w, ids, P, L, ref = small
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    idx = plan.hash(torch.from_numpy(ids).cuda(), proj)
+    assert np.array_equal(idx.cpu().numpy(), ref["z"].reshape(-1, w.R))
+
+
+def test_small_gather_bitexact(small):
+    name, w, ids, P, L, ref = small
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    z = torch.from_numpy(ref["z"].reshape(-1, w.R).astype(np.int32)).cuda()
+    e = plan.gather(z, weights.table, weights.scales)
+    assert np.array_equal(gpu_e_bits(w, e), expected_e_bits(w, ref["z"].reshape(-1, w.R), L).reshape(e.shape))
+
+
+def test_small_kv_projection(small):
+    name, w, ids, P, L, ref = small
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    # exact e as the GPU stores it, then the GEMM alone
+    e_bits = expected_e_bits(w, ref["z"].reshape(-1, w.R), L)
+    e = to_torch(e_bits, "f32" if w.table_dtype == "f32" else "bf16")
+    kv = plan.kv_projection(e, weights.w_kv)
+    e64 = O.widen(e_bits, w.act_dtype)
+    Wm = O.widen(L.W_kv, w.act_dtype)
+    exp = e64 @ Wm.T
+    got = act_to_f64(kv)
+    rms = np.sqrt(np.mean(exp ** 2))
+    if w.act_dtype == "bf16":
+        # one bf16 rounding of an fp32 accumulation: |err| <= 2^-8 |x| plus accumulation noise
+        assert np.all(np.abs(got - exp) <= 2.0 ** -8 * np.abs(exp) + 1e-3 * rms)
+    else:
+        assert np.all(np.abs(got - exp) <= 1e-5 * rms + 1e-6 * np.abs(exp))
+
+
+def test_small_forward_matches_oracle(small):
+    name, w, ids, P, L, ref = small
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    plan.forward(torch.from_numpy(ids).cuda(), proj, weights, H)
+    st, flags = plan.get_error()
+    assert st == 0 and flags == 0
+    assert_close(act_to_f64(H), ref["H_new"], w.act_dtype, name)
+
+
+def test_small_fusion_entry_matches_forward(small):
+    name, w, ids, P, L, ref = small
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    idx = plan.hash(ids_d, proj)
+    e = plan.gather(idx, weights.table, weights.scales)
+    kv = plan.kv_projection(e, weights.w_kv)
+    H2 = H.clone()
+    plan.fusion(kv, weights, H2)
+    plan.forward(ids_d, proj, weights, H)
+    assert torch.equal(H, H2)
+
+
+def test_zero_table_leaves_H_bit_unchanged():
+    w = SMALL["small_bf16"]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    L.table[:] = 0
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    H0 = H.clone()
+    plan.forward(torch.from_numpy(ids).cuda(), proj, weights, H)
+    assert torch.equal(H.view(torch.int16), H0.view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 129])
+def test_short_and_ragged_sequences(T):
+    w = SMALL["small_bf16"].scaled(B=5, T=T)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    ref = oracle_forward(w, ids, P, L)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    idx = plan.hash(torch.from_numpy(ids).cuda(), proj)
+    assert np.array_equal(idx.cpu().numpy(), ref["z"].reshape(-1, w.R))
+    plan.forward(torch.from_numpy(ids).cuda(), proj, weights, H)
+    assert_close(act_to_f64(H), ref["H_new"], "bf16", f"T={T}")
+
+
+def test_empty_input_is_a_no_op():
+    w = SMALL["small_bf16"]
+    L = W.layer_inputs(w, 1)
+    P = W.projection_map(w)
+    plan, weights, proj, H = make_layer(w, L, P, 16)
+    ids = torch.zeros(0, 7, dtype=torch.int32, device="cuda")
+    Hz = torch.zeros(0, 7, 1, w.d, dtype=torch.bfloat16, device="cuda")
+    plan.forward(ids, proj, weights, Hz)
+    assert plan.get_error() == (0, 0)
+
+
+def test_causality_on_gpu():
+    w = SMALL["small_bf16"].scaled(B=1, T=200)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    H1 = H.clone()
+    plan.forward(torch.from_numpy(ids).cuda(), proj, weights, H1)
+    ids2 = ids.copy()
+    ids2[0, 120:] = (ids2[0, 120:] + 7) % w.V
+    H2 = H.clone()
+    H2[0, 150:] += 1.0
+    plan.forward(torch.from_numpy(ids2).cuda(), proj, weights, H2)
+    assert torch.equal(H1[0, :120], H2[0, :120])
+    assert not torch.equal(H1[0, 120:132], H2[0, 120:132])
+
+
+# --------------------------------------------------------------------------- #
+# streaming: chunked prefill and decode
+# --------------------------------------------------------------------------- #
+def test_decode_steps_match_prefill_and_oracle():
+    from hashed_gram_embedding_engram_gb300 import EngramState
+    w = SMALL["small_bf16"].scaled(B=6, T=40)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    ref = oracle_forward(w, ids, P, L)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    full = H.clone()
+    plan.forward(torch.from_numpy(ids).cuda(), proj, weights, full)
+    st = EngramState.zeros(plan, w.B)
+    ids_d = torch.from_numpy(ids).cuda()
+    out = H.clone()
+    prefix = 17
+    chunk = out[:, :prefix].contiguous()
+    plan.forward(ids_d[:, :prefix].contiguous(), proj, weights, chunk, st)
+    out[:, :prefix] = chunk
+    for t in range(prefix, w.T):
+        step = out[:, t:t + 1].contiguous()
+        plan.forward(ids_d[:, t:t + 1].contiguous(), proj, weights, step, st)
+        out[:, t:t + 1] = step
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(st.pos.cpu(), torch.full((w.B,), w.T, dtype=torch.int32))
+    # the streamed result equals one-shot prefill bit for bit, and the oracle within tolerance
+    assert torch.equal(out.view(torch.int16), full.view(torch.int16))
+    assert_close(act_to_f64(out), ref["H_new"], "bf16", "streamed")
+    # prev ids hold the last N-1 projected ids
+    assert np.array_equal(st.prev_ids.cpu().numpy(), ref["state"]["prev"])
+
+
+def test_chunked_prefill_with_ragged_chunks():
+    from hashed_gram_embedding_engram_gb300 import EngramState
+    w = SMALL["small_multibranch"].scaled(B=2, T=61)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    full = H.clone()
+    ids_d = torch.from_numpy(ids).cuda()
+    plan.forward(ids_d, proj, weights, full)
+    st = EngramState.zeros(plan, w.B)
+    out = H.clone()
+    t0 = 0
+    for n in (1, 2, 3, 13, 5, 37):
+        seg = out[:, t0:t0 + n].contiguous()
+        plan.forward(ids_d[:, t0:t0 + n].contiguous(), proj, weights, seg, st)
+        out[:, t0:t0 + n] = seg
+        t0 += n
+    assert t0 == w.T
+    assert torch.equal(out.view(torch.int16), full.view(torch.int16))
+
+
+# --------------------------------------------------------------------------- #
+# UVA: host-resident tables
+# --------------------------------------------------------------------------- #
+def test_uva_gather_equals_hbm_gather():
+    w = SMALL["small_i8"]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, wd, proj, H = make_layer(w, L, P, ids.size)
+    table_host = to_torch(L.table, "i8", "cpu", pin=True)
+    scales_host = to_torch(L.scales, "f16", "cpu", pin=True)
+    idx = plan.hash(torch.from_numpy(ids).cuda(), proj)
+    e_dev = plan.gather(idx, wd.table, wd.scales)
+    e_host = plan.gather(idx, table_host, scales_host)
+    e_mix = plan.gather(idx, table_host, wd.scales)
+    assert torch.equal(e_dev.view(torch.int16), e_host.view(torch.int16))
+    assert torch.equal(e_dev.view(torch.int16), e_mix.view(torch.int16))
