@@ -121,16 +121,18 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 # algorithmic work per token per layer (bytes or flops), per kernel
 # --------------------------------------------------------------------------- #
-def per_token_work(w) -> dict:
+def per_token_work(w, bn: int = 256) -> dict:
+    """Algorithmic bytes (or flops) per token per layer of each kernel engram_forward launches."""
     act = 2 if w.act_dtype == "bf16" else 4
     row_bytes = w.row_dim * {"f32": 4, "bf16": 2, "i8": 1}[w.table_dtype]
     nc = (w.M + 1) * w.d
+    n_part = (w.d // bn) * (1 + 3 * w.M)
     return {
-        "hash": ("bytes", 4 + 4 + 4 * w.R),                                  # id, P[id], R indices out
-        "gather": ("bytes", w.R * row_bytes + 4 * w.R + act * w.d_mem),      # rows in, idx in, e out
-        "kv_projection": ("flops", 2 * w.d_mem * nc),                        # one GEMM, all branches
-        "fusion": ("bytes", act * nc + act * w.M * w.d                        # gate: kv + H in, scalars out
-                   + 8 * w.M + act * w.d + 2 * act * w.M * w.d + 8 * w.M),    # conv: v + H in, H out, scalars
+        "hash": ("bytes", 4 + 4 + 4 * w.R),                                   # id, P[id] in; R indices out
+        "gather": ("bytes", w.R * row_bytes + 4 * w.R + act * w.d_mem),       # rows + idx in; e out
+        "kv_gemm": ("flops", 2 * w.d_mem * nc),                               # e . [W_V; W_K]^T
+        "finalize": ("bytes", 4 * n_part + 8 * w.M),                          # partials in; alpha, rinv out
+        "conv": ("bytes", 4 * w.d + 8 * w.M + 2 * act * w.M * w.d),           # v, scalars, H in; H out
     }
 
 
@@ -218,35 +220,23 @@ def run_ours(args) -> None:
         st, flags = ly["plan"].get_error()
         assert st == 0, f"device error flags {flags}"
 
-    # ---- per-kernel durations, same work, component entry points on the same stream ----
+    # ---- per-kernel durations: the plan's tracing events around each kernel of engram_forward ----
     Kb = min(K, 200)
-    names = ["hash", "gather", "kv_projection", "fusion"]
+    names = ["hash", "gather", "kv_gemm", "finalize", "conv"]
     dur = {n: [] for n in names}
+    for ly in layers:
+        ly["plan"].set_timing(True)
     for i in range(Kb):
         restore()
-        flush.zero_()
         for ly in layers:
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-            plan, wts = ly["plan"], ly["weights"]
-            ws = ly["ws"]
-            e[0].record(stream)
-            idx = plan.hash(ids, ly["proj"], out=ly.setdefault("idx", torch.empty(w.ntok, w.R, dtype=torch.int32,
-                                                                               device=dev)))
-            e[1].record(stream)
-            ebuf = plan.gather(idx, wts.table, wts.scales, out=ly.setdefault(
-                "e", torch.empty(w.ntok, w.d_mem, dtype=torch.bfloat16, device=dev)))
-            e[2].record(stream)
-            kv = plan.kv_projection(ebuf, wts.w_kv, out=ly.setdefault(
-                "kv", torch.empty(w.ntok, (w.M + 1) * w.d, dtype=torch.bfloat16, device=dev)))
-            e[3].record(stream)
-            plan.fusion(kv, wts, ly["H"], ws)
-            e[4].record(stream)
-            ly.setdefault("events", []).append(e)
-    torch.cuda.synchronize()
+            flush.zero_()
+            ly["plan"].forward(ids, ly["proj"], ly["weights"], ly["H"], None, ly["ws"])
+            t = ly["plan"].kernel_times()
+            assert len(t) == len(names), t
+            for n, x in zip(names, t):
+                dur[n].append(x)
     for ly in layers:
-        for e in ly.pop("events"):
-            for j, n in enumerate(names):
-                dur[n].append(e[j].elapsed_time(e[j + 1]))
+        ly["plan"].set_timing(False)
     work = per_token_work(w)
     kernels = {}
     for n in names:
@@ -261,6 +251,9 @@ def run_ours(args) -> None:
             ach = amount / (ms / 1e3) / 1e9
             kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 1), "unit": "GB/s",
                           "peak": hbm_peak, "frac": round(ach / hbm_peak, 4), "bound": "hbm"}
+    total_k = sum(kernels[n]["ms"] for n in names)
+    for n in names:
+        kernels[n]["share"] = round(kernels[n]["ms"] / total_k, 4)
     top = max(names, key=lambda n: kernels[n]["ms"])
     kt = kernels[top]
     roofline = {"kernel": top, "bound": kt["bound"], "achieved": kt["achieved"], "peak": kt["peak"],
@@ -308,7 +301,7 @@ def run_ours(args) -> None:
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": dict(workload_desc(w), cuda_graph=True), "roofline": roofline, "kernels": kernels,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * 5 * len(layers), "clocks": clocks}
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * len(names) * len(layers), "clocks": clocks}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

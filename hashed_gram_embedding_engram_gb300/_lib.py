@@ -17,8 +17,8 @@ STATUS_NAMES = ["OK", "INVALID_ARG", "UNSUPPORTED", "NOT_MAPPED", "INDEX_RANGE",
 F32, BF16, I8_ROWSCALE_F16 = 0, 1, 2
 
 EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes",
-           "engram_hash", "engram_gather", "engram_kv_projection", "engram_fusion", "engram_forward",
-           "engram_get_error")
+           "engram_hash", "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward",
+           "engram_get_error", "engram_plan_set_timing", "engram_plan_kernel_times")
 
 
 class Config(ctypes.Structure):
@@ -65,10 +65,13 @@ def _lib() -> ctypes.CDLL:
         lib.engram_hash.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp]
         lib.engram_gather.argtypes = [vp, vp, i64, vp, vp, vp, vp]
         lib.engram_kv_projection.argtypes = [vp, vp, i64, vp, vp, vp]
-        lib.engram_fusion.argtypes = [vp, vp, i32, i32, ctypes.POINTER(Weights), vp, vp, sz, vp]
+        lib.engram_stage_b.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.POINTER(Weights), vp,
+                                       ctypes.POINTER(State), vp, sz, vp]
         lib.engram_forward.argtypes = [vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
                                        ctypes.POINTER(State), vp, sz, vp]
         lib.engram_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.engram_plan_set_timing.argtypes = [vp, i32]
+        lib.engram_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
         for name in EXPORTS:
             if name != "engram_status_string":
                 getattr(lib, name).restype = i32

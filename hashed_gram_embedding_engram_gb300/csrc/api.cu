@@ -54,6 +54,11 @@ engram_status_t device_view(const void* ptr, const void** out) {
   }
 }
 
+// Tracing: record the plan's next event on `s` (no-op unless timing is on).
+void mark(const engram_plan* p, cudaStream_t s) {
+  if (p->timing && p->n_marks < engram_plan::kMaxMarks) cudaEventRecord(p->marks[p->n_marks++], s);
+}
+
 engram_status_t check_tokens(const engram_plan* p, int B, int T) {
   if (B < 0 || T < 0) return ENGRAM_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * T > p->max_tokens) return ENGRAM_ERR_INVALID_ARG;
@@ -89,17 +94,23 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
   Workspace w{};
   const size_t ab = act_bytes(p->cfg.act_dtype);
   const size_t M = p->cfg.M, d = p->cfg.d;
+  const size_t n = static_cast<size_t>(ntok);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t at = off;
     off = align_up(off + bytes, 256);
     return base ? static_cast<char*>(base) + at : nullptr;
   };
-  w.idx = reinterpret_cast<int32_t*>(take(static_cast<size_t>(ntok) * p->R * 4));
-  w.e = take(static_cast<size_t>(ntok) * p->d_mem * ab);
-  w.kv = take(static_cast<size_t>(ntok) * (M + 1) * d * ab);
-  w.alpha = reinterpret_cast<float*>(take(static_cast<size_t>(ntok) * M * 4));
-  w.rinv = reinterpret_cast<float*>(take(static_cast<size_t>(ntok) * M * 4));
+  w.idx = reinterpret_cast<int32_t*>(take(n * p->R * 4));
+  w.e = take(n * p->d_mem * ab);
+  if (p->cfg.act_dtype == ENGRAM_F32) {
+    w.kv = reinterpret_cast<float*>(take(n * (M + 1) * d * 4));
+  } else {
+    w.v32 = reinterpret_cast<float*>(take(n * d * 4));
+    w.part = reinterpret_cast<float*>(take(n * (d / 64) * (1 + 3 * M) * 4));   // widest case: 64-column tiles
+  }
+  w.alpha = reinterpret_cast<float*>(take(n * M * 4));
+  w.rinv = reinterpret_cast<float*>(take(n * M * 4));
   w.bytes = off;
   return w;
 }
@@ -142,7 +153,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
                        (c.table_dtype == ENGRAM_I8_ROWSCALE_F16 && c.act_dtype == ENGRAM_BF16);
   if (!pair_ok) return ENGRAM_ERR_UNSUPPORTED;
   const int d_mem = R * c.row_dim;
-  if (c.act_dtype == ENGRAM_BF16 && (d_mem % 64 || c.d % 32)) return ENGRAM_ERR_UNSUPPORTED;
+  if (c.act_dtype == ENGRAM_BF16 && (d_mem % 64 || c.d % 64)) return ENGRAM_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(c.M + 1) * c.d > INT32_MAX / 2) return ENGRAM_ERR_INVALID_ARG;
 
   int dev = 0, sms = 0, major = 0, minor = 0;
@@ -207,6 +218,8 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
 
 engram_status_t engram_plan_destroy(engram_plan_t* plan) {
   if (!plan) return ENGRAM_OK;
+  if (plan->timing)
+    for (int i = 0; i < engram_plan::kMaxMarks; ++i) cudaEventDestroy(plan->marks[i]);
   cudaError_t e = cudaFree(plan->dev);
   delete plan;
   return cuda_status(e);
@@ -254,33 +267,66 @@ engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, i
   return cuda_status(engram::launch_kv_projection(plan, e, ntok, w_kv, kv_out, (cudaStream_t)stream));
 }
 
-static engram_status_t run_fusion(const engram_plan_t* plan, const engram::Workspace& ws, const void* kv,
-                                  const int32_t* ids, const int32_t* proj, int V, int B, int T,
-                                  const engram_weights_t* w, void* H, engram_state_t* state, cudaStream_t s) {
+// Steps 5-8 from e (already gathered into ws.e or the caller's buffer).
+static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Workspace& ws, const void* e,
+                                   const int32_t* ids, const int32_t* proj, int V, int B, int T,
+                                   const engram_weights_t* w, void* H, engram_state_t* state, cudaStream_t s) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
-  cudaError_t e = engram::launch_gate(plan, kv, H, ntok, w->g_h, w->g_k, ws.alpha, ws.rinv, s);
-  if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
-  e = engram::launch_conv_residual(plan, kv, ws.alpha, ws.rinv, B, T, w->g_c, w->conv, H, state, s);
-  if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+  const int d = plan->cfg.d, M = plan->cfg.M;
+  const float* v = nullptr;
+  int64_t sv = 0;
+  mark(plan, s);
+  if (plan->cfg.act_dtype == ENGRAM_F32) {
+    if (engram::gemm_f32_simt(static_cast<const float*>(e), static_cast<const float*>(w->w_kv), ws.kv, ntok,
+                              (M + 1) * d, plan->d_mem, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    mark(plan, s);
+    if (engram::launch_gate_f32(plan, ws.kv, static_cast<const float*>(H), ntok, w->g_h, w->g_k, ws.alpha, ws.rinv,
+                                s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    v = ws.kv;
+    sv = static_cast<int64_t>(M + 1) * d;
+  } else {
+    if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
+                                 plan->num_sms, &plan->dev->err, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    mark(plan, s);
+    const int n_vt = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
+    if (engram::launch_finalize(plan, ws.part, n_vt, ntok, ws.alpha, ws.rinv, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    v = ws.v32;
+    sv = d;
+  }
+  mark(plan, s);
+  if (engram::launch_conv_residual(plan, v, sv, ws.alpha, ws.rinv, B, T, w->g_c, w->conv, H, state, s) !=
+      cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  mark(plan, s);
   if (state) {
-    e = engram::launch_state_update(plan, ids, proj, V, kv, ws.alpha, ws.rinv, B, T, w->g_c, state, s);
-    if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+    if (engram::launch_state_update(plan, ids, proj, V, v, sv, ws.alpha, ws.rinv, B, T, w->g_c, state, s) !=
+        cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    mark(plan, s);
   }
   return ENGRAM_OK;
 }
 
-engram_status_t engram_fusion(const engram_plan_t* plan, const void* kv, int B, int T, const engram_weights_t* w,
-                              void* H, void* workspace, size_t workspace_bytes, engram_stream_t stream) {
+engram_status_t engram_stage_b(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
+                               int V, const void* e, const engram_weights_t* w, void* H, engram_state_t* state,
+                               void* workspace, size_t workspace_bytes, engram_stream_t stream) {
   if (!plan) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_tokens(plan, B, T)) return s;
   const int64_t ntok = static_cast<int64_t>(B) * T;
   if (ntok == 0) return ENGRAM_OK;
-  if (!kv || !H || !aligned16(kv) || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
+  if (!e || !H || !aligned16(e) || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
+  if (state && (!ids || !proj || V <= 0)) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_weights(plan, w, false)) return s;
+  if (engram_status_t s = check_state(plan, state)) return s;
   engram::Workspace ws = engram::carve_workspace(plan, ntok, workspace);
   if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ENGRAM_ERR_WORKSPACE;
-  return run_fusion(plan, ws, kv, nullptr, nullptr, 0, B, T, w, H, nullptr, (cudaStream_t)stream);
+  plan->n_marks = 0;
+  return run_stage_b(plan, ws, e, ids, proj, V, B, T, w, H, state, (cudaStream_t)stream);
 }
 
 engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
@@ -305,11 +351,44 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   }
   cudaStream_t s = (cudaStream_t)stream;
   const int32_t* prev = state ? state->prev_ids : nullptr;
+  plan->n_marks = 0;
+  mark(plan, s);
   if (engram::launch_hash(plan, ids, B, T, proj, V, prev, ws.idx, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  mark(plan, s);
   if (engram::launch_gather(plan, ws.idx, ntok, tab, static_cast<const uint16_t*>(sc), ws.e, s) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
-  if (engram::launch_kv_projection(plan, ws.e, ntok, w->w_kv, ws.kv, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
-  return run_fusion(plan, ws, ws.kv, ids, proj, V, B, T, w, H, state, s);
+  return run_stage_b(plan, ws, ws.e, ids, proj, V, B, T, w, H, state, s);
+}
+
+engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable) {
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (enable && !plan->timing) {
+    for (int i = 0; i < engram_plan::kMaxMarks; ++i) {
+      if (cudaEventCreate(&plan->marks[i]) != cudaSuccess) {
+        for (int j = 0; j < i; ++j) cudaEventDestroy(plan->marks[j]);
+        return ENGRAM_ERR_CUDA;
+      }
+    }
+    plan->timing = true;
+  } else if (!enable && plan->timing) {
+    for (int i = 0; i < engram_plan::kMaxMarks; ++i) cudaEventDestroy(plan->marks[i]);
+    plan->timing = false;
+  }
+  plan->n_marks = 0;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_plan_kernel_times(const engram_plan_t* plan, float* ms_out, int max_out, int* count) {
+  if (!plan || !count || (max_out > 0 && !ms_out)) return ENGRAM_ERR_INVALID_ARG;
+  *count = 0;
+  if (!plan->timing || plan->n_marks < 2) return ENGRAM_OK;
+  if (cudaEventSynchronize(plan->marks[plan->n_marks - 1]) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  const int n = plan->n_marks - 1;
+  for (int i = 0; i < n && i < max_out; ++i) {
+    if (cudaEventElapsedTime(&ms_out[i], plan->marks[i], plan->marks[i + 1]) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  }
+  *count = n < max_out ? n : max_out;
+  return ENGRAM_OK;
 }
 
 engram_status_t engram_get_error(const engram_plan_t* plan, engram_stream_t stream, uint32_t* flags_out) {

@@ -49,15 +49,22 @@ struct engram_plan {
   std::vector<uint64_t> mults;
   std::vector<int64_t> offsets;
   engram::PlanDev* dev;            // device copy of the parameter block
+  // tracing: events recorded around each kernel of the last engram_forward
+  static constexpr int kMaxMarks = 8;
+  cudaEvent_t marks[kMaxMarks];
+  bool timing;
+  mutable int n_marks;
 };
 
 namespace engram {
 
-// Workspace carve-up for engram_forward / engram_fusion, 256-byte aligned parts.
+// Workspace carve-up for engram_forward / engram_stage_b, 256-byte aligned parts.
 struct Workspace {
   int32_t* idx;      // [ntok, R]
   void* e;           // [ntok, d_mem] act dtype
-  void* kv;          // [ntok, (M+1)d] act dtype
+  float* kv;         // f32 layers: [ntok, (M+1)d] = [v | k^(1..M)]
+  float* v32;        // bf16 layers: [ntok, d] v in fp32 (fused K/V epilogue)
+  float* part;       // bf16 layers: [ntok, (d/64)(1+3M)] gate partial sums
   float* alpha;      // [ntok, M]
   float* rinv;       // [ntok, M]   1/sqrt(mean(v~^2)+eps) of each gated row
   size_t bytes;
@@ -71,18 +78,27 @@ cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok
                           const uint16_t* scales, void* e, cudaStream_t s);
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
                                  cudaStream_t s);
-cudaError_t launch_gate(const engram_plan* p, const void* kv, const void* H, int64_t ntok, const float* g_h,
-                        const float* g_k, float* alpha, float* rinv, cudaStream_t s);
-cudaError_t launch_conv_residual(const engram_plan* p, const void* kv, const float* alpha, const float* rinv,
-                                 int B, int T, const float* g_c, const float* conv, void* H,
+cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
+                            const float* g_k, float* alpha, float* rinv, cudaStream_t s);
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_vt, int64_t ntok, float* alpha,
+                            float* rinv, cudaStream_t s);
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
+                                 const float* rinv, int B, int T, const float* g_c, const float* conv, void* H,
                                  const engram_state_t* state, cudaStream_t s);
-cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V,
-                                const void* kv, const float* alpha, const float* rinv, int B, int T,
-                                const float* g_c, const engram_state_t* state, cudaStream_t s);
+cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
+                                int64_t sv, const float* alpha, const float* rinv, int B, int T, const float* g_c,
+                                const engram_state_t* state, cudaStream_t s);
 
 // bf16 GEMM on tcgen05: C[Mr, Nc] = A[Mr, Kd] . B[Nc, Kd]^T, all row-major bf16.
 cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,
                               uint32_t* err, cudaStream_t s);
+// The same GEMM with the Engram epilogue: v (columns [0,d)) to v32 in fp32,
+// gate partial sums of every tile to part; k is never stored.
+cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
+                             const float* g_h, const float* g_k, float* v32, float* part, int num_sms, uint32_t* err,
+                             cudaStream_t s);
+// Partials per token gemm_bf16_engram writes for this shape: (d / BN) * (1 + 3M).
+int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms);
 // fp32 GEMM on the CUDA cores, same shapes.
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);
 

@@ -4,16 +4,19 @@
 //   Y^(m) = SiLU(Conv1D_{w, dilation}(RMSNorm(V~^(m)))) + V~^(m),       H^(m) <- H^(m) + Y^(m)
 //
 // Kernel split (all HBM-bound, fp32 arithmetic):
-//   gate_kernel   one warp per token: reads h^(1..M), k^(1..M), v once and
-//                 writes two scalars per (token, branch): alpha and
-//                 rinv = 1/sqrt(mean((alpha v)^2) + eps).  Since
-//                 RMSNorm(v~) = (alpha v) * rinv * g_c, the convolution needs
-//                 only v and these scalars -- no full-row reduction per lag.
-//   conv_kernel   one thread per (token, 16-byte channel group): the causal
-//                 dilated taps read v rows at t - j*dilation (neighbouring
-//                 threads' rows: served by L1/L2), the history before a chunk
-//                 from the caller's ring, then SiLU, skip and the residual
-//                 update of all M branches in place.
+//   bf16 layers: the K/V GEMM's epilogue (gemm.cu) already reduced every k tile
+//   to partial sums and wrote v in fp32.
+//     finalize_kernel  one thread per (token, branch): partials -> alpha and
+//                      rinv = 1/sqrt(mean((alpha v)^2) + eps).  Since
+//                      RMSNorm(v~) = (alpha v) * rinv * g_c, the convolution
+//                      needs only v and these two scalars.
+//   fp32 layers (CUDA-core GEMM, [v | k] buffer in fp32):
+//     gate_kernel      one warp per token: the same scalars from h, k and v.
+//   conv_kernel   one thread per (token, 16-byte group of H channels): the
+//                 causal dilated taps read v rows at t - j*dilation (rows of
+//                 neighbouring tokens, served by L1/L2), the history before a
+//                 chunk from the caller's ring, then SiLU, skip and the
+//                 residual update of all M branches in place.
 //   state_kernel  after the chunk: writes the last (w-1)*dilation conv inputs
 //                 into the ring, rolls the last N-1 projected ids, advances pos.
 #include <cuda_bf16.h>
@@ -125,18 +128,59 @@ __global__ void __launch_bounds__(256) gate_kernel(const T* __restrict__ kv, con
   }
 }
 
+// ------------------------------------------------------------------ finalize the gate
+// partials from the fused GEMM epilogue -> alpha and rinv per (token, branch)
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int64_t ntok, int M, int d,
+                                                       int n_vt, float eps, float* __restrict__ alpha,
+                                                       float* __restrict__ rinv) {
+  const int P = n_vt * (1 + 3 * M);
+  const float inv_d = 1.f / static_cast<float>(d);
+  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < ntok * M;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tok = i / M;
+    const int m = static_cast<int>(i - tok * M);
+    const float* p = part + tok * P;
+    float sv = 0.f, dot = 0.f, sk = 0.f, sh = 0.f;
+    for (int j = 0; j < n_vt; ++j) {
+      sv += p[j];
+      const float* q = p + n_vt + (m * n_vt + j) * 3;
+      dot += q[0];
+      sk += q[1];
+      sh += q[2];
+    }
+    const float rh = 1.f / sqrtf(sh * inv_d + eps);
+    const float rk = 1.f / sqrtf(sk * inv_d + eps);
+    const float a = sigmoidf(dot * rh * rk * inv_sqrt_d);
+    alpha[i] = a;
+    rinv[i] = 1.f / sqrtf(a * a * (sv * inv_d) + eps);
+  }
+}
+
+template <int VN>
+__device__ __forceinline__ void load_v(const float* p, float* out) {
+#pragma unroll
+  for (int i = 0; i < VN; i += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p + i);
+    out[i] = q.x;
+    out[i + 1] = q.y;
+    out[i + 2] = q.z;
+    out[i + 3] = q.w;
+  }
+}
+
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
-template <typename T, int W>
-__global__ void __launch_bounds__(256) conv_kernel(const T* __restrict__ kv, const float* __restrict__ alpha,
-                                                   const float* __restrict__ rinv, int B, int Tn, int M, int d,
-                                                   int dil, const float* __restrict__ g_c,
-                                                   const float* __restrict__ conv, T* __restrict__ H,
+// v rows are fp32 with row stride sv (the fused path's v buffer, or the fp32 kv buffer).
+template <typename TH, int W>
+__global__ void __launch_bounds__(256) conv_kernel(const float* __restrict__ v_base, int64_t sv,
+                                                   const float* __restrict__ alpha, const float* __restrict__ rinv,
+                                                   int B, int Tn, int M, int d, int dil, const float* __restrict__ g_c,
+                                                   const float* __restrict__ conv, TH* __restrict__ H,
                                                    const float* __restrict__ ring, const int32_t* __restrict__ pos,
                                                    int L) {
-  constexpr int V = Vec<T>::kN;
+  constexpr int V = Vec<TH>::kN;
   const int groups = d / V;
   const int64_t total = static_cast<int64_t>(B) * Tn * groups;
-  const int64_t stride_kv = static_cast<int64_t>(M + 1) * d;
   for (int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; item < total;
        item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t tok = item / groups;
@@ -157,10 +201,10 @@ __global__ void __launch_bounds__(256) conv_kernel(const T* __restrict__ kv, con
     bool in_chunk[W];
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      const int tl = t - (W - 1 - j) * dil;
-      in_chunk[j] = tl >= 0;
+      const int lag = (W - 1 - j) * dil;
+      in_chunk[j] = t - lag >= 0;
       if (in_chunk[j]) {
-        Vec<T>::load(kv + (tok - (t - tl)) * stride_kv + c, v[j]);
+        load_v<V>(v_base + (tok - lag) * sv + c, v[j]);
       } else {
 #pragma unroll
         for (int i = 0; i < V; ++i) v[j][i] = 0.f;
@@ -182,15 +226,7 @@ __global__ void __launch_bounds__(256) conv_kernel(const T* __restrict__ kv, con
         } else {
           const int abs_pos = p0 + t - lag;
           if (ring != nullptr && abs_pos >= 0) {
-            const float* src = ring + ((static_cast<int64_t>(b) * L + abs_pos % L) * M + m) * d + c;
-#pragma unroll
-            for (int i = 0; i < V; i += 4) {
-              const float4 q = *reinterpret_cast<const float4*>(src + i);
-              u[i] = q.x;
-              u[i + 1] = q.y;
-              u[i + 2] = q.z;
-              u[i + 3] = q.w;
-            }
+            load_v<V>(ring + ((static_cast<int64_t>(b) * L + abs_pos % L) * M + m) * d + c, u);
           } else {
 #pragma unroll
             for (int i = 0; i < V; ++i) u[i] = 0.f;
@@ -200,34 +236,32 @@ __global__ void __launch_bounds__(256) conv_kernel(const T* __restrict__ kv, con
         for (int i = 0; i < V; ++i) acc[i] = fmaf(w[i][j], u[i], acc[i]);
       }
       const float a_t = alpha[tok * M + m];
-      T* hp = H + (tok * M + m) * static_cast<int64_t>(d) + c;
+      TH* hp = H + (tok * M + m) * static_cast<int64_t>(d) + c;
       float h[V];
-      Vec<T>::load(hp, h);
+      Vec<TH>::load(hp, h);
 #pragma unroll
       for (int i = 0; i < V; ++i) {
         const float y = acc[i] * sigmoidf(acc[i]) + a_t * v[W - 1][i];
         h[i] = h[i] + y;
       }
-      Vec<T>::store(hp, h);
+      Vec<TH>::store(hp, h);
     }
   }
 }
 
 // ------------------------------------------------------------------ streaming state
-template <typename T>
-__global__ void __launch_bounds__(256) state_kernel(const T* __restrict__ kv, const float* __restrict__ alpha,
-                                                    const float* __restrict__ rinv, int Tn, int M, int d,
-                                                    const float* __restrict__ g_c, float* __restrict__ ring,
-                                                    int32_t* __restrict__ pos, int L,
+__global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_base, int64_t sv,
+                                                    const float* __restrict__ alpha, const float* __restrict__ rinv,
+                                                    int Tn, int M, int d, const float* __restrict__ g_c,
+                                                    float* __restrict__ ring, int32_t* __restrict__ pos, int L,
                                                     const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ proj, int V,
                                                     int32_t* __restrict__ prev, int N, uint32_t* __restrict__ err) {
-  constexpr int VN = Vec<T>::kN;
+  constexpr int VN = 4;
   const int b = blockIdx.x;
   const int keep = Tn < L ? Tn : L;            // chunk positions that stay in the ring
   const int p0 = pos[b];
   const int groups = d / VN;
-  const int64_t stride_kv = static_cast<int64_t>(M + 1) * d;
   const int items = keep * M * groups;
   for (int it = threadIdx.x; it < items; it += blockDim.x) {
     const int g = it % groups;
@@ -236,7 +270,7 @@ __global__ void __launch_bounds__(256) state_kernel(const T* __restrict__ kv, co
     const int64_t tok = static_cast<int64_t>(b) * Tn + t;
     const int c = g * VN;
     float v[VN];
-    Vec<T>::load(kv + tok * stride_kv + c, v);
+    load_v<VN>(v_base + tok * sv + c, v);
     const float a = alpha[tok * M + m], ri = rinv[tok * M + m];
     float* dst = ring + ((static_cast<int64_t>(b) * L + (p0 + t) % L) * M + m) * d + c;
 #pragma unroll
@@ -275,28 +309,29 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-template <typename T, int W>
-void conv_launch(const engram_plan* p, const void* kv, const float* alpha, const float* rinv, int B, int Tn,
-                 const float* g_c, const float* conv, void* H, const engram_state_t* st, cudaStream_t s) {
+template <typename TH, int W>
+void conv_launch(const engram_plan* p, const float* v, int64_t sv, const float* alpha, const float* rinv, int B,
+                 int Tn, const float* g_c, const float* conv, void* H, const engram_state_t* st, cudaStream_t s) {
   const int d = p->cfg.d;
-  const int64_t items = static_cast<int64_t>(B) * Tn * (d / Vec<T>::kN);
-  conv_kernel<T, W><<<grid_for(items, 256, p->num_sms), 256, 0, s>>>(
-      static_cast<const T*>(kv), alpha, rinv, B, Tn, p->cfg.M, d, p->cfg.conv_dilation, g_c, conv,
-      static_cast<T*>(H), st ? st->u_ring : nullptr, st ? st->pos : nullptr, p->L_ring);
+  const int64_t items = static_cast<int64_t>(B) * Tn * (d / Vec<TH>::kN);
+  conv_kernel<TH, W><<<grid_for(items, 256, p->num_sms), 256, 0, s>>>(
+      v, sv, alpha, rinv, B, Tn, p->cfg.M, d, p->cfg.conv_dilation, g_c, conv, static_cast<TH*>(H),
+      st ? st->u_ring : nullptr, st ? st->pos : nullptr, p->L_ring);
 }
 
-template <typename T>
-cudaError_t conv_dispatch(const engram_plan* p, const void* kv, const float* alpha, const float* rinv, int B, int Tn,
-                          const float* g_c, const float* conv, void* H, const engram_state_t* st, cudaStream_t s) {
+template <typename TH>
+cudaError_t conv_dispatch(const engram_plan* p, const float* v, int64_t sv, const float* alpha, const float* rinv,
+                          int B, int Tn, const float* g_c, const float* conv, void* H, const engram_state_t* st,
+                          cudaStream_t s) {
   switch (p->cfg.conv_w) {
-    case 1: conv_launch<T, 1>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 2: conv_launch<T, 2>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 3: conv_launch<T, 3>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 4: conv_launch<T, 4>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 5: conv_launch<T, 5>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 6: conv_launch<T, 6>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 7: conv_launch<T, 7>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
-    case 8: conv_launch<T, 8>(p, kv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 1: conv_launch<TH, 1>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 2: conv_launch<TH, 2>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 3: conv_launch<TH, 3>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 4: conv_launch<TH, 4>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 5: conv_launch<TH, 5>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 6: conv_launch<TH, 6>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 7: conv_launch<TH, 7>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
+    case 8: conv_launch<TH, 8>(p, v, sv, alpha, rinv, B, Tn, g_c, conv, H, st, s); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -304,37 +339,33 @@ cudaError_t conv_dispatch(const engram_plan* p, const void* kv, const float* alp
 
 }  // namespace
 
-cudaError_t launch_gate(const engram_plan* p, const void* kv, const void* H, int64_t ntok, const float* g_h,
-                        const float* g_k, float* alpha, float* rinv, cudaStream_t s) {
+cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
+                            const float* g_k, float* alpha, float* rinv, cudaStream_t s) {
   const int grid = grid_for(ntok * 32, 256, p->num_sms);
-  if (p->cfg.act_dtype == ENGRAM_F32)
-    gate_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(kv), static_cast<const float*>(H), ntok,
-                                            p->cfg.M, p->cfg.d, p->cfg.eps, g_h, g_k, alpha, rinv);
-  else
-    gate_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(kv),
-                                                    static_cast<const __nv_bfloat16*>(H), ntok, p->cfg.M, p->cfg.d,
-                                                    p->cfg.eps, g_h, g_k, alpha, rinv);
+  gate_kernel<float><<<grid, 256, 0, s>>>(kv, H, ntok, p->cfg.M, p->cfg.d, p->cfg.eps, g_h, g_k, alpha, rinv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_conv_residual(const engram_plan* p, const void* kv, const float* alpha, const float* rinv, int B,
-                                 int T, const float* g_c, const float* conv, void* H, const engram_state_t* state,
-                                 cudaStream_t s) {
-  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, kv, alpha, rinv, B, T, g_c, conv, H, state, s);
-  return conv_dispatch<__nv_bfloat16>(p, kv, alpha, rinv, B, T, g_c, conv, H, state, s);
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_vt, int64_t ntok, float* alpha,
+                            float* rinv, cudaStream_t s) {
+  finalize_kernel<<<grid_for(ntok * p->cfg.M, 256, p->num_sms), 256, 0, s>>>(part, ntok, p->cfg.M, p->cfg.d, n_vt,
+                                                                            p->cfg.eps, alpha, rinv);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const void* kv,
-                                const float* alpha, const float* rinv, int B, int T, const float* g_c,
-                                const engram_state_t* st, cudaStream_t s) {
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
+                                 const float* rinv, int B, int T, const float* g_c, const float* conv, void* H,
+                                 const engram_state_t* state, cudaStream_t s) {
   if (p->cfg.act_dtype == ENGRAM_F32)
-    state_kernel<float><<<B, 256, 0, s>>>(static_cast<const float*>(kv), alpha, rinv, T, p->cfg.M, p->cfg.d, g_c,
-                                          st->u_ring, st->pos, p->L_ring, ids, proj, V, st->prev_ids, p->cfg.N,
-                                          &p->dev->err);
-  else
-    state_kernel<__nv_bfloat16><<<B, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(kv), alpha, rinv, T, p->cfg.M,
-                                                  p->cfg.d, g_c, st->u_ring, st->pos, p->L_ring, ids, proj, V,
-                                                  st->prev_ids, p->cfg.N, &p->dev->err);
+    return conv_dispatch<float>(p, v, sv, alpha, rinv, B, T, g_c, conv, H, state, s);
+  return conv_dispatch<__nv_bfloat16>(p, v, sv, alpha, rinv, B, T, g_c, conv, H, state, s);
+}
+
+cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
+                                int64_t sv, const float* alpha, const float* rinv, int B, int T, const float* g_c,
+                                const engram_state_t* st, cudaStream_t s) {
+  state_kernel<<<B, 256, 0, s>>>(v, sv, alpha, rinv, T, p->cfg.M, p->cfg.d, g_c, st->u_ring, st->pos, p->L_ring, ids,
+                                 proj, V, st->prev_ids, p->cfg.N, &p->dev->err);
   return cudaGetLastError();
 }
 

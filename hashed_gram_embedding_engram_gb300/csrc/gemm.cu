@@ -45,6 +45,17 @@ struct Cfg {
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN);
 };
 
+struct EngramEpilogue {
+  float* v32;                     // [Mr, d]
+  float* part;                    // [Mr, n_vt * (1 + 3M)]
+  const __nv_bfloat16* H;         // [Mr, M, d]
+  const float* g_h;               // [M, d]
+  const float* g_k;               // [M, d]
+  int d;
+  int M;
+  int n_vt;                       // d / BN
+};
+
 struct Bars {
   uint64_t full[8];
   uint64_t empty[8];
@@ -70,10 +81,84 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
+// Engram epilogue of the K/V projection (Steps 5-6 fused).  Output columns
+// [0, d) are v: stored in fp32 with a per-tile partial of sum(v^2).  Columns
+// [(1+m)d, (2+m)d) are k^(m): never stored; each tile contributes the partial
+// sums the gate needs, taken from the fp32 accumulators and H^(m):
+//   dot = sum h*g_h*g_k*k,  sk = sum k^2,  sh = sum h^2   (over the tile's columns).
+// Partials of token t: part[t*P + j] = sum v^2 of v tile j (j < n_vt), and
+// part[t*P + n_vt + (m*n_vt + j)*3 + {0,1,2}] = (dot, sk, sh) of k^(m) tile j.
 template <int BN>
+__device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0) {
+  const int d = epi.d;
+  const int P = epi.n_vt * (1 + 3 * epi.M);
+  if (n0 < d) {
+    float sv = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(t_row + c, r);
+      ptx::tmem_ld_wait();
+      if (row < Mr) {
+        float4* dst = reinterpret_cast<float4*>(epi.v32 + static_cast<int64_t>(row) * d + n0 + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 q = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          dst[j] = q;
+          sv = fmaf(q.x, q.x, sv);
+          sv = fmaf(q.y, q.y, sv);
+          sv = fmaf(q.z, q.z, sv);
+          sv = fmaf(q.w, q.w, sv);
+        }
+      }
+    }
+    if (row < Mr) epi.part[static_cast<int64_t>(row) * P + n0 / BN] = sv;
+  } else {
+    const int m = (n0 - d) / d;
+    const int col = n0 - d - m * d;
+    const int j = col / BN;
+    const __nv_bfloat16* hrow = epi.H + (static_cast<int64_t>(row) * epi.M + m) * d + col;
+    const float* gh = epi.g_h + static_cast<int64_t>(m) * d + col;
+    const float* gk = epi.g_k + static_cast<int64_t>(m) * d + col;
+    float dot = 0.f, sk = 0.f, sh = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(t_row + c, r);
+      ptx::tmem_ld_wait();
+      if (row < Mr) {
+        const uint4* hp = reinterpret_cast<const uint4*>(hrow + c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 hv = __ldg(hp + q4);
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int cc = q4 * 8 + i;
+            const float h = __uint_as_float(i & 1 ? (hw[i >> 1] & 0xFFFF0000u) : (hw[i >> 1] << 16));
+            const float k = __uint_as_float(r[cc]);
+            dot = fmaf(h * __ldg(gh + c + cc), k * __ldg(gk + c + cc), dot);
+            sk = fmaf(k, k, sk);
+            sh = fmaf(h, h, sh);
+          }
+        }
+      }
+    }
+    if (row < Mr) {
+      float* dst = epi.part + static_cast<int64_t>(row) * P + epi.n_vt + (m * epi.n_vt + j) * 3;
+      dst[0] = dot;
+      dst[1] = sk;
+      dst[2] = sh;
+    }
+  }
+}
+
+template <int BN, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     __nv_bfloat16* __restrict__ C, int Mr, int Nc, int Kd, uint32_t* __restrict__ err) {
+                     __nv_bfloat16* __restrict__ C, int Mr, int Nc, int Kd, uint32_t* __restrict__ err,
+                     const EngramEpilogue epi) {
   using G = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -196,23 +281,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const int row = m0 + q * 32 + lane;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (!kFused) {
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(t_row + c, r);
-        ptx::tmem_ld_wait();
-        if (row < Mr && n0 + c < Nc) {
-          uint32_t packed[16];
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c, r);
+          ptx::tmem_ld_wait();
+          if (row < Mr && n0 + c < Nc) {
+            uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            packed[j] = *reinterpret_cast<uint32_t*>(&v);
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              packed[j] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(C + static_cast<int64_t>(row) * Nc + n0 + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(C + static_cast<int64_t>(row) * Nc + n0 + c);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
         }
+      } else {
+        fused_epilogue<BN>(epi, t_row, row, Mr, n0);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -263,23 +352,35 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int cols, int bo
   return r == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool kFused>
 cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms, uint32_t* err,
-                cudaStream_t s) {
+                EngramEpilogue epi, cudaStream_t s) {
   using G = Cfg<BN>;
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, Mr, Kd, kBM) || !make_map(&tb, B, Nc, Kd, BN)) return cudaErrorInvalidValue;
   static bool attr_set = false;   // per template instance; idempotent if raced
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_bf16_kernel<BN, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int64_t tiles = ((Mr + kBM - 1) / kBM) * ((Nc + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  gemm_bf16_kernel<BN><<<grid, kThreads, G::kSmem, s>>>(ta, tb, static_cast<__nv_bfloat16*>(C), static_cast<int>(Mr),
-                                                       Nc, Kd, err);
+  if constexpr (kFused) epi.n_vt = epi.d / BN;
+  gemm_bf16_kernel<BN, kFused><<<grid, kThreads, G::kSmem, s>>>(ta, tb, static_cast<__nv_bfloat16*>(C),
+                                                                static_cast<int>(Mr), Nc, Kd, err, epi);
   return cudaGetLastError();
+}
+
+// Widest N tile (256, 128, 64) that divides `div` and still gives every SM a tile.
+int pick_bn(int64_t Mr, int Nc, int div, int num_sms) {
+  const int64_t m_tiles = (Mr + kBM - 1) / kBM;
+  for (int bn : {256, 128}) {
+    if (div % bn == 0 && m_tiles * (Nc / bn) >= num_sms) return bn;
+  }
+  if (div % 64 == 0) return 64;
+  return div % 128 == 0 ? 128 : 0;
 }
 
 // ---------------------------------------------------------------- fp32 (CUDA cores)
@@ -330,12 +431,30 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
 cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,
                               uint32_t* err, cudaStream_t s) {
   if (Nc % 32 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
-  const int64_t m_tiles = (Mr + kBM - 1) / kBM;
-  // widest tile that still gives every SM work
-  if (Nc % 256 == 0 && m_tiles * (Nc / 256) >= num_sms) return run<256>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
-  if (Nc % 128 == 0 && m_tiles * (Nc / 128) >= num_sms) return run<128>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
-  if (Nc % 64 == 0) return run<64>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
-  return run<128>(A, B, C, Mr, Nc, Kd, num_sms, err, s);
+  EngramEpilogue none{};
+  switch (pick_bn(Mr, Nc, Nc % 64 == 0 ? Nc : 32, num_sms)) {
+    case 256: return run<256, false>(A, B, C, Mr, Nc, Kd, num_sms, err, none, s);
+    case 64: return run<64, false>(A, B, C, Mr, Nc, Kd, num_sms, err, none, s);
+    default: return run<128, false>(A, B, C, Mr, Nc, Kd, num_sms, err, none, s);
+  }
+}
+
+cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
+                             const float* g_h, const float* g_k, float* v32, float* part, int num_sms, uint32_t* err,
+                             cudaStream_t s) {
+  const int Nc = (M + 1) * d;
+  if (d % 64 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
+  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0};
+  switch (pick_bn(Mr, Nc, d, num_sms)) {
+    case 256: return run<256, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
+    case 128: return run<128, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
+    default: return run<64, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
+  }
+}
+
+int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms) {
+  const int bn = pick_bn(Mr, (M + 1) * d, d, num_sms);
+  return (d / bn) * (1 + 3 * M);
 }
 
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s) {

@@ -201,16 +201,22 @@ class EngramPlan:
             _dev(out, "kv_out", self.act_torch_dtype, (ntok, nc)), _stream()), "engram_kv_projection")
         return out
 
-    def fusion(self, kv: torch.Tensor, weights: EngramWeights, H: torch.Tensor,
-               workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-        """Steps 6-8 in place on H [B, T, M, d] from kv [B*T, (M+1)d]."""
+    def stage_b(self, e: torch.Tensor, weights: EngramWeights, H: torch.Tensor, state: Optional[EngramState] = None,
+                ids: Optional[torch.Tensor] = None, proj: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Steps 5-8 in place on H [B, T, M, d] from gathered rows e [B*T, d_mem].
+
+        With a ``state``, ``ids`` [B, T] and ``proj`` are needed too."""
         B, T = H.shape[0], H.shape[1]
         ws = self.new_workspace(B * T, H.device) if workspace is None else workspace
         w = weights.struct(self, need_table=False)
-        _lib.check(self._lib.engram_fusion(
-            self._h, _dev(kv, "kv", self.act_torch_dtype, (B * T, (self.M + 1) * self.d)), B, T, ctypes.byref(w),
-            _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), _dev(ws, "workspace"), ws.numel(),
-            _stream()), "engram_fusion")
+        st = None if state is None else ctypes.byref(state.struct(self, B))
+        ids_p = 0 if ids is None else _dev(ids, "ids", torch.int32, (B, T))
+        proj_p, V = (0, 0) if proj is None else (_dev(proj, "proj", torch.int32), proj.numel())
+        _lib.check(self._lib.engram_stage_b(
+            self._h, ids_p, B, T, proj_p, V, _dev(e, "e", self.act_torch_dtype, (B * T, self.d_mem)),
+            ctypes.byref(w), _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), st,
+            _dev(ws, "workspace"), ws.numel(), _stream()), "engram_stage_b")
         return H
 
     def forward(self, ids: torch.Tensor, proj: torch.Tensor, weights: EngramWeights, H: torch.Tensor,
@@ -225,6 +231,17 @@ class EngramPlan:
             ctypes.byref(w), _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), st,
             _dev(ws, "workspace"), ws.numel(), _stream()), "engram_forward")
         return H
+
+    def set_timing(self, enable: bool) -> None:
+        """Record CUDA events around each kernel of later forward / stage_b calls."""
+        _lib.check(self._lib.engram_plan_set_timing(self._h, int(bool(enable))), "engram_plan_set_timing")
+
+    def kernel_times(self) -> list:
+        """Device milliseconds of each kernel of the last call (waits for it)."""
+        buf = (ctypes.c_float * 8)()
+        n = ctypes.c_int()
+        _lib.check(self._lib.engram_plan_kernel_times(self._h, buf, 8, ctypes.byref(n)), "engram_plan_kernel_times")
+        return [buf[i] for i in range(n.value)]
 
     def get_error(self) -> Tuple[int, int]:
         """Synchronise the current stream; return (status, raw flag bits) and clear them."""

@@ -152,21 +152,28 @@ engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int
                               const void* table, const uint16_t* scales, void* e_out,
                               engram_stream_t stream);
 
-/* Step 5.  e: [ntok, d_mem] act_dtype; w_kv as in engram_weights_t;
- * kv_out: [ntok, (M+1)*d] act_dtype = e . w_kv^T (fp32 accumulation), columns
- * [0,d) = v, [(1+m)d, (2+m)d) = k^(m).  BF16 runs on the tcgen05 tensor cores. */
+/* Step 5 alone (inspection / reuse of k and v).  e: [ntok, d_mem] act_dtype;
+ * w_kv as in engram_weights_t; kv_out: [ntok, (M+1)*d] act_dtype =
+ * e . w_kv^T (fp32 accumulation, one rounding to act_dtype), columns [0,d) = v,
+ * [(1+m)d, (2+m)d) = k^(m).  BF16 runs on the tcgen05 tensor cores. */
 engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok,
                                      const void* w_kv, void* kv_out, engram_stream_t stream);
 
-/* Steps 6-8 from a k/v buffer, for fresh sequences (streaming continuation
- * goes through engram_forward, which also has the token ids the state needs).
- * kv: [B*T, (M+1)*d] as from engram_kv_projection; w: only w_kv is ignored
- * and table/scales may be NULL; H: [B, T, M, d] act_dtype, updated in place.
- * The per-token gate scalars are kept in `workspace`
- * (engram_plan_workspace_bytes(plan, B*T) bytes, 256-B aligned, suffice). */
-engram_status_t engram_fusion(const engram_plan_t* plan, const void* kv, int B, int T,
-                              const engram_weights_t* w, void* H,
-                              void* workspace, size_t workspace_bytes, engram_stream_t stream);
+/* Steps 5-8 from gathered rows (Stage B): for a caller that ran Stage A
+ * (engram_hash + engram_gather) ahead of time, e.g. on a side stream while
+ * earlier layers computed -- the indices depend on the tokens only.
+ * e: [B*T, d_mem] act_dtype as written by engram_gather; w: table/scales are
+ * not read (may be NULL); H: [B, T, M, d] act_dtype, updated in place;
+ * state: NULL or as in engram_forward, which then also needs ids/proj/V (the
+ * chunk's raw ids, for the rolling n-gram state); with state == NULL, ids
+ * and proj may be NULL.  workspace: device, >= engram_plan_workspace_bytes(
+ * plan, B*T), 256-B aligned.  BF16 layers run the K/V projection on the
+ * tcgen05 tensor cores with a fused epilogue that keeps v in fp32 and turns
+ * the k tiles into gate partial sums (k itself is never stored). */
+engram_status_t engram_stage_b(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                               const int32_t* proj, int V, const void* e,
+                               const engram_weights_t* w, void* H, engram_state_t* state,
+                               void* workspace, size_t workspace_bytes, engram_stream_t stream);
 
 /* Steps 1-8: the whole layer for B sequences of T new tokens each.
  * ids/proj/V as in engram_hash; w as in engram_weights_t; H: [B, T, M, d]
@@ -178,6 +185,17 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
                                const int32_t* proj, int V, const engram_weights_t* w,
                                void* H, engram_state_t* state,
                                void* workspace, size_t workspace_bytes, engram_stream_t stream);
+
+/* Tracing.  With timing on, engram_forward / engram_stage_b record one of
+ * the plan's CUDA events on `stream` before the first kernel and after every
+ * kernel they launch: hash, gather, K/V projection, gate (finalize for BF16),
+ * conv + residual, and the state update when a state is given.  For use on
+ * one stream at a time, outside CUDA-graph capture.  enable: 0 or 1. */
+engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable);
+
+/* Wait for the last call's events and write the device time of each kernel it
+ * launched, in launch order, in milliseconds: ms_out[0..*count-1]. */
+engram_status_t engram_plan_kernel_times(const engram_plan_t* plan, float* ms_out, int max_out, int* count);
 
 /* Synchronise `stream`, then read and clear the plan's device error word.
  * Returns ENGRAM_OK, ENGRAM_ERR_INDEX_RANGE or ENGRAM_ERR_TIMEOUT (the first

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes", "engram_hash",
-              "engram_gather", "engram_kv_projection", "engram_fusion", "engram_forward", "engram_get_error",
+              "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward", "engram_get_error",
               "engram_status_string"):
         assert n in names
 
@@ -95,7 +95,7 @@ def test_null_plan_is_refused_everywhere(lib):
     assert lib.engram_hash(None, None, 1, 1, None, 1, None, None, None) == _lib.ERR_INVALID_ARG
     assert lib.engram_gather(None, None, 1, None, None, None, None) == _lib.ERR_INVALID_ARG
     assert lib.engram_kv_projection(None, None, 1, None, None, None) == _lib.ERR_INVALID_ARG
-    assert lib.engram_fusion(None, None, 1, 1, None, None, None, 0, None) == _lib.ERR_INVALID_ARG
+    assert lib.engram_stage_b(None, None, 1, 1, None, 1, None, None, None, None, None, 0, None) == _lib.ERR_INVALID_ARG
     assert lib.engram_forward(None, None, 1, 1, None, 1, None, None, None, None, 0, None) == _lib.ERR_INVALID_ARG
     assert lib.engram_get_error(None, None, None) == _lib.ERR_INVALID_ARG
 

@@ -102,15 +102,14 @@ def test_small_forward_matches_oracle(small):
     assert_close(act_to_f64(H), ref["H_new"], w.act_dtype, name)
 
 
-def test_small_fusion_entry_matches_forward(small):
+def test_small_stage_a_then_stage_b_matches_forward(small):
     name, w, ids, P, L, ref = small
     plan, weights, proj, H = make_layer(w, L, P, ids.size)
     ids_d = torch.from_numpy(ids).cuda()
     idx = plan.hash(ids_d, proj)
     e = plan.gather(idx, weights.table, weights.scales)
-    kv = plan.kv_projection(e, weights.w_kv)
     H2 = H.clone()
-    plan.fusion(kv, weights, H2)
+    plan.stage_b(e, weights, H2)
     plan.forward(ids_d, proj, weights, H)
     assert torch.equal(H, H2)
 
