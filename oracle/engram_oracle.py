@@ -14,11 +14,14 @@ deepseek-tech-notes, chapter 07-Engram), section "Engram 工作原理":
   and the section "多分支 backbone 上的变体" for M hyper-connection branches.
 The int8 row dequantisation follows "Engram 嵌入扩展：面向高效 DRAM/SSD 卸载的
 协同设计" (web.reeddaily.com), section "AgentX Engram DRAM卸载提升性能": one
-kernel selects and dequantises rows, from HBM or pinned host memory.
+kernel selects and dequantises rows, from HBM or pinned host memory; the page
+gives no output precision, and the dequantised row is read as a bf16 row (it is
+the input of the bf16 K/V projection).
 
 Arithmetic: integers exactly (64-bit unsigned, wrap-around multiply); floating
-point in float64, after exact widening of the stored inputs (fp32, bf16, int8
-times fp16 scale).  The pages fix no precision, so nothing is rounded inside.
+point in float64, after exact widening of the stored inputs (fp32, bf16, and
+int8 rows dequantised to bf16).  The pages fix no precision; apart from that
+dequantised row nothing is rounded inside.
 
 Readings where the pages leave a step open (each one is listed in the design
 notes of the repository):
@@ -129,13 +132,15 @@ def gather_concat(z: np.ndarray, tables: Sequence[np.ndarray], table_kind: str,
     """Step 4: e_t = concat over n = 2..N, k = 1..K of E_{n,k}[z_{t,n,k}].
 
     table_kind: 'f32', 'bf16' (uint16 bits) or 'i8' (int8 rows, each times its
-    fp16 row scale).  Returns float64 [..., R * row_dim]."""
+    fp16 row scale, dequantised to a bf16 row: the rows feed the bf16 K/V
+    projection; the product is exact in binary32, so bf16(q*s) is one rounding).
+    Returns float64 [..., R * row_dim]."""
     parts = []
     for r, E in enumerate(tables):
         rows = E[z[..., r]]
         if table_kind == "i8":
             s = np.asarray(scales[r], dtype=np.float16).astype(np.float64)[z[..., r]]
-            parts.append(rows.astype(np.float64) * s[..., None])
+            parts.append(bf16_to_f64(f64_to_bf16_bits(rows.astype(np.float64) * s[..., None])))
         else:
             parts.append(widen(rows, table_kind))
     return np.concatenate(parts, axis=-1)

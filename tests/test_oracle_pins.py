@@ -207,13 +207,17 @@ def test_bf16_widening_and_rounding_agree_with_torch():
     assert O.f64_to_bf16_bits(np.array([1 + 3 * 2.0 ** -8]))[0] == 0x3F82
 
 
-def test_int8_dequant_is_exact_product():
-    q = np.array([[-127, -1, 0, 1, 127]], dtype=np.int8)
-    s = np.array([np.float16(0.00015735)], dtype=np.float16)
-    e = O.gather_concat(np.array([[0]]), [q], "i8", [s])
-    assert e[0].tolist() == [float(v) * float(s[0]) for v in (-127, -1, 0, 1, 127)]
-    # int8 (8 bits) times fp16 (11 bits) fits binary32's 24 bits: no rounding before bf16
-    assert np.array_equal(e.astype(np.float32).astype(np.float64), e)
+def test_int8_dequant_is_one_bf16_rounding_of_the_exact_product():
+    rng = np.random.default_rng(18)
+    q = rng.integers(-127, 128, size=(50, 64)).astype(np.int8)
+    s = (rng.random(50) * 1e-3 + 1e-4).astype(np.float16)
+    e = O.gather_concat(np.arange(50)[:, None], [q], "i8", [s])
+    # int8 (8 bits) times fp16 (11 bits) fits binary32's 24 bits: the product is exact there
+    prod32 = torch.from_numpy(q.astype(np.float32)) * torch.from_numpy(s.astype(np.float32))[:, None]
+    assert np.array_equal(prod32.double().numpy(), q.astype(np.float64) * s.astype(np.float64)[:, None])
+    # and the row the gather produces is torch's bf16 rounding of it
+    assert np.array_equal(e, prod32.to(torch.bfloat16).double().numpy())
+    assert e[0, 0] == O.bf16_to_f64(O.f64_to_bf16_bits(np.array([float(q[0, 0]) * float(s[0])])))[0]
 
 
 # --------------------------------------------------------------------------- #
