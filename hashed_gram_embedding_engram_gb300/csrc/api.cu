@@ -107,7 +107,7 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
     w.kv = reinterpret_cast<float*>(take(n * (M + 1) * d * 4));
   } else {
     w.v32 = reinterpret_cast<float*>(take(n * d * 4));
-    w.part = reinterpret_cast<float*>(take(n * (d / 64) * (1 + 3 * M) * 4));   // widest case: 64-column tiles
+    w.part = reinterpret_cast<float*>(take(n * (d / 32) * (1 + 3 * M) * 4));   // widest case: 32-column slices
   }
   w.alpha = reinterpret_cast<float*>(take(n * M * 4));
   w.rinv = reinterpret_cast<float*>(take(n * M * 4));

@@ -64,7 +64,7 @@ struct Workspace {
   void* e;           // [ntok, d_mem] act dtype
   float* kv;         // f32 layers: [ntok, (M+1)d] = [v | k^(1..M)]
   float* v32;        // bf16 layers: [ntok, d] v in fp32 (fused K/V epilogue)
-  float* part;       // bf16 layers: [ntok, (d/64)(1+3M)] gate partial sums
+  float* part;       // bf16 layers: [ntok, (d/32)(1+3M)] gate partial sums (at most)
   float* alpha;      // [ntok, M]
   float* rinv;       // [ntok, M]   1/sqrt(mean(v~^2)+eps) of each gated row
   size_t bytes;
@@ -97,7 +97,7 @@ cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr,
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
                              const float* g_h, const float* g_k, float* v32, float* part, int num_sms, uint32_t* err,
                              cudaStream_t s);
-// Partials per token gemm_bf16_engram writes for this shape: (d / BN) * (1 + 3M).
+// Partials per token gemm_bf16_engram writes for this shape: (d / (BN/2)) * (1 + 3M).
 int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms);
 // fp32 GEMM on the CUDA cores, same shapes.
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);

@@ -12,7 +12,7 @@
 //                      needs only v and these two scalars.
 //   fp32 layers (CUDA-core GEMM, [v | k] buffer in fp32):
 //     gate_kernel      one warp per token: the same scalars from h, k and v.
-//   conv_kernel   one thread per (token, 16-byte group of H channels): the
+//   conv_kernel   one thread per (token, 4 channels of H): the
 //                 causal dilated taps read v rows at t - j*dilation (rows of
 //                 neighbouring tokens, served by L1/L2), the history before a
 //                 chunk from the caller's ring, then SiLU, skip and the
@@ -170,15 +170,42 @@ __device__ __forceinline__ void load_v(const float* p, float* out) {
 }
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
+// 4 channels per thread (8-byte bf16 / 16-byte fp32 H accesses), register use
+// capped so that 3 blocks of 256 threads stay resident per SM: the kernel is
+// latency-bound unless many tokens are in flight.
+template <typename T>
+struct Vec4;
+template <>
+struct Vec4<__nv_bfloat16> {
+  __device__ static void load(const __nv_bfloat16* p, float* out) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    out[0] = __uint_as_float(u.x << 16);
+    out[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    out[2] = __uint_as_float(u.y << 16);
+    out[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* in) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(in[2], in[3]);
+    *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+};
+template <>
+struct Vec4<float> {
+  __device__ static void load(const float* p, float* out) { Vec<float>::load(p, out); }
+  __device__ static void store(float* p, const float* in) { Vec<float>::store(p, in); }
+};
+
 // v rows are fp32 with row stride sv (the fused path's v buffer, or the fp32 kv buffer).
 template <typename TH, int W>
-__global__ void __launch_bounds__(256) conv_kernel(const float* __restrict__ v_base, int64_t sv,
-                                                   const float* __restrict__ alpha, const float* __restrict__ rinv,
-                                                   int B, int Tn, int M, int d, int dil, const float* __restrict__ g_c,
-                                                   const float* __restrict__ conv, TH* __restrict__ H,
-                                                   const float* __restrict__ ring, const int32_t* __restrict__ pos,
-                                                   int L) {
-  constexpr int V = Vec<TH>::kN;
+__global__ void __launch_bounds__(256, 3) conv_kernel(const float* __restrict__ v_base, int64_t sv,
+                                                      const float* __restrict__ alpha,
+                                                      const float* __restrict__ rinv, int B, int Tn, int M, int d,
+                                                      int dil, const float* __restrict__ g_c,
+                                                      const float* __restrict__ conv, TH* __restrict__ H,
+                                                      const float* __restrict__ ring,
+                                                      const int32_t* __restrict__ pos, int L) {
+  constexpr int V = 4;
   const int groups = d / V;
   const int64_t total = static_cast<int64_t>(B) * Tn * groups;
   for (int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; item < total;
@@ -187,29 +214,33 @@ __global__ void __launch_bounds__(256) conv_kernel(const float* __restrict__ v_b
     const int c = static_cast<int>(item - tok * groups) * V;
     const int b = static_cast<int>(tok / Tn);
     const int t = static_cast<int>(tok - static_cast<int64_t>(b) * Tn);
-    const int p0 = ring ? pos[b] : 0;
 
-    float w[V][W], gc[V];
+    // taps of the 4 channels: conv[c+i][j]
+    float w[V][W];
+    if constexpr (W == 4) {
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      gc[i] = g_c[c + i];
+      for (int i = 0; i < V; ++i) Vec<float>::load(conv + static_cast<int64_t>(c + i) * W, w[i]);
+    } else {
 #pragma unroll
-      for (int j = 0; j < W; ++j) w[i][j] = conv[static_cast<int64_t>(c + i) * W + j];
+      for (int i = 0; i < V; ++i)
+#pragma unroll
+        for (int j = 0; j < W; ++j) w[i][j] = __ldg(conv + static_cast<int64_t>(c + i) * W + j);
     }
+    float gc[V];
+    Vec<float>::load(g_c + c, gc);
     // v rows at the taps' positions inside this chunk
     float v[W][V];
-    bool in_chunk[W];
 #pragma unroll
     for (int j = 0; j < W; ++j) {
       const int lag = (W - 1 - j) * dil;
-      in_chunk[j] = t - lag >= 0;
-      if (in_chunk[j]) {
-        load_v<V>(v_base + (tok - lag) * sv + c, v[j]);
+      if (t - lag >= 0) {
+        Vec<float>::load(v_base + (tok - lag) * sv + c, v[j]);
       } else {
 #pragma unroll
         for (int i = 0; i < V; ++i) v[j][i] = 0.f;
       }
     }
+    const int p0 = ring ? pos[b] : 0;
     for (int m = 0; m < M; ++m) {
       float acc[V];
 #pragma unroll
@@ -218,7 +249,7 @@ __global__ void __launch_bounds__(256) conv_kernel(const float* __restrict__ v_b
       for (int j = 0; j < W; ++j) {
         const int lag = (W - 1 - j) * dil;
         float u[V];
-        if (in_chunk[j]) {
+        if (t - lag >= 0) {
           const int64_t tj = tok - lag;
           const float a = alpha[tj * M + m], ri = rinv[tj * M + m];
 #pragma unroll
@@ -226,7 +257,7 @@ __global__ void __launch_bounds__(256) conv_kernel(const float* __restrict__ v_b
         } else {
           const int abs_pos = p0 + t - lag;
           if (ring != nullptr && abs_pos >= 0) {
-            load_v<V>(ring + ((static_cast<int64_t>(b) * L + abs_pos % L) * M + m) * d + c, u);
+            Vec<float>::load(ring + ((static_cast<int64_t>(b) * L + abs_pos % L) * M + m) * d + c, u);
           } else {
 #pragma unroll
             for (int i = 0; i < V; ++i) u[i] = 0.f;
@@ -238,13 +269,10 @@ __global__ void __launch_bounds__(256) conv_kernel(const float* __restrict__ v_b
       const float a_t = alpha[tok * M + m];
       TH* hp = H + (tok * M + m) * static_cast<int64_t>(d) + c;
       float h[V];
-      Vec<TH>::load(hp, h);
+      Vec4<TH>::load(hp, h);
 #pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const float y = acc[i] * sigmoidf(acc[i]) + a_t * v[W - 1][i];
-        h[i] = h[i] + y;
-      }
-      Vec<TH>::store(hp, h);
+      for (int i = 0; i < V; ++i) h[i] += acc[i] * sigmoidf(acc[i]) + a_t * v[W - 1][i];
+      Vec4<TH>::store(hp, h);
     }
   }
 }
@@ -313,7 +341,7 @@ template <typename TH, int W>
 void conv_launch(const engram_plan* p, const float* v, int64_t sv, const float* alpha, const float* rinv, int B,
                  int Tn, const float* g_c, const float* conv, void* H, const engram_state_t* st, cudaStream_t s) {
   const int d = p->cfg.d;
-  const int64_t items = static_cast<int64_t>(B) * Tn * (d / Vec<TH>::kN);
+  const int64_t items = static_cast<int64_t>(B) * Tn * (d / 4);
   conv_kernel<TH, W><<<grid_for(items, 256, p->num_sms), 256, 0, s>>>(
       v, sv, alpha, rinv, B, Tn, p->cfg.M, d, p->cfg.conv_dilation, g_c, conv, static_cast<TH*>(H),
       st ? st->u_ring : nullptr, st ? st->pos : nullptr, p->L_ring);

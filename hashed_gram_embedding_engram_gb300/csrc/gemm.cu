@@ -10,9 +10,10 @@
 //   warp 1      allocates TMEM (2 x BN fp32 columns: two accumulators) and one
 //               elected lane issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide
 //               K slice; tcgen05.commit frees ring stages and publishes tiles.
-//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, round
-//               to bf16, store; overlaps the MMA of the next tile (the
-//               accumulators ping-pong).
+//   warps 2-9   epilogue: two warps per TMEM lane quadrant, each taking half
+//               of the tile's columns; tcgen05.ld 32 lanes x 32 columns at a
+//               time, round to bf16 and store (or the Engram epilogue below);
+//               overlaps the MMA of the next tile (the accumulators ping-pong).
 // Every mbarrier wait is bounded in time: on expiry the kernel records
 // kErrTimeout, drains its own TMA loads and MMAs (again bounded), frees TMEM
 // and returns.
@@ -30,7 +31,7 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;                        // one 128-byte swizzle atom of bf16
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: a healthy stage turns over in < 1 us
 
 template <int BN>
@@ -47,13 +48,13 @@ struct Cfg {
 
 struct EngramEpilogue {
   float* v32;                     // [Mr, d]
-  float* part;                    // [Mr, n_vt * (1 + 3M)]
+  float* part;                    // [Mr, n_sl * (1 + 3M)]
   const __nv_bfloat16* H;         // [Mr, M, d]
   const float* g_h;               // [M, d]
   const float* g_k;               // [M, d]
   int d;
   int M;
-  int n_vt;                       // d / BN
+  int n_sl;                       // d / (BN / 2): column slices per row of v
 };
 
 struct Bars {
@@ -82,20 +83,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 }
 
 // Engram epilogue of the K/V projection (Steps 5-6 fused).  Output columns
-// [0, d) are v: stored in fp32 with a per-tile partial of sum(v^2).  Columns
-// [(1+m)d, (2+m)d) are k^(m): never stored; each tile contributes the partial
+// [0, d) are v: stored in fp32 with a per-slice partial of sum(v^2).  Columns
+// [(1+m)d, (2+m)d) are k^(m): never stored; each slice contributes the partial
 // sums the gate needs, taken from the fp32 accumulators and H^(m):
-//   dot = sum h*g_h*g_k*k,  sk = sum k^2,  sh = sum h^2   (over the tile's columns).
-// Partials of token t: part[t*P + j] = sum v^2 of v tile j (j < n_vt), and
-// part[t*P + n_vt + (m*n_vt + j)*3 + {0,1,2}] = (dot, sk, sh) of k^(m) tile j.
+//   dot = sum h*g_h*g_k*k,  sk = sum k^2,  sh = sum h^2   (over the slice's columns).
+// A slice is the half tile (BN/2 columns) one epilogue warp handles; with
+// n_sl = d / (BN/2) slices per row of v (and of each k^(m)), token t has
+// part[t*P + j] = sum v^2 of v slice j, and
+// part[t*P + n_sl + (m*n_sl + j)*3 + {0,1,2}] = (dot, sk, sh) of k^(m) slice j.
 template <int BN>
-__device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0) {
+__device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0,
+                                               int c_lo) {
+  constexpr int SW = BN / 2;
   const int d = epi.d;
-  const int P = epi.n_vt * (1 + 3 * epi.M);
+  const int P = epi.n_sl * (1 + 3 * epi.M);
   if (n0 < d) {
     float sv = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c_lo; c < c_lo + SW; c += 32) {
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
@@ -113,32 +118,37 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32
         }
       }
     }
-    if (row < Mr) epi.part[static_cast<int64_t>(row) * P + n0 / BN] = sv;
+    if (row < Mr) epi.part[static_cast<int64_t>(row) * P + (n0 + c_lo) / SW] = sv;
   } else {
     const int m = (n0 - d) / d;
     const int col = n0 - d - m * d;
-    const int j = col / BN;
+    const int j = (col + c_lo) / SW;
     const __nv_bfloat16* hrow = epi.H + (static_cast<int64_t>(row) * epi.M + m) * d + col;
     const float* gh = epi.g_h + static_cast<int64_t>(m) * d + col;
     const float* gk = epi.g_k + static_cast<int64_t>(m) * d + col;
     float dot = 0.f, sk = 0.f, sh = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c_lo; c < c_lo + SW; c += 32) {
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
       if (row < Mr) {
         const uint4* hp = reinterpret_cast<const uint4*>(hrow + c);
+        const float4* gh4 = reinterpret_cast<const float4*>(gh + c);
+        const float4* gk4 = reinterpret_cast<const float4*>(gk + c);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const uint4 hv = __ldg(hp + q4);
           const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+          const float4 ga = __ldg(gh4 + 2 * q4), gb = __ldg(gh4 + 2 * q4 + 1);
+          const float4 ka = __ldg(gk4 + 2 * q4), kb = __ldg(gk4 + 2 * q4 + 1);
+          const float g[8] = {ga.x * ka.x, ga.y * ka.y, ga.z * ka.z, ga.w * ka.w,
+                              gb.x * kb.x, gb.y * kb.y, gb.z * kb.z, gb.w * kb.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int cc = q4 * 8 + i;
             const float h = __uint_as_float(i & 1 ? (hw[i >> 1] & 0xFFFF0000u) : (hw[i >> 1] << 16));
-            const float k = __uint_as_float(r[cc]);
-            dot = fmaf(h * __ldg(gh + c + cc), k * __ldg(gk + c + cc), dot);
+            const float k = __uint_as_float(r[q4 * 8 + i]);
+            dot = fmaf(h * g[i], k, dot);
             sk = fmaf(k, k, sk);
             sh = fmaf(h, h, sh);
           }
@@ -146,7 +156,7 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32
       }
     }
     if (row < Mr) {
-      float* dst = epi.part + static_cast<int64_t>(row) * P + epi.n_vt + (m * epi.n_vt + j) * 3;
+      float* dst = epi.part + static_cast<int64_t>(row) * P + epi.n_sl + (m * epi.n_sl + j) * 3;
       dst[0] = dot;
       dst[1] = sk;
       dst[2] = sh;
@@ -178,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&bars->tfull[a], 1);
-      ptx::mbar_init(&bars->tempty[a], 4);     // one arrive per epilogue warp
+      ptx::mbar_init(&bars->tempty[a], 8);     // one arrive per epilogue warp
     }
     ptx::mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -270,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_wait_bounded(&bars->drain, 0, kWaitLimitNs);
     }
   } else {
-    // -------------------------------------------------- epilogue (warps 2..5)
+    // -------------------------------------------------- epilogue (warps 2..9)
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int c_lo = ((warp - 2) >> 2) * (BN / 2);   // half of the tile's columns
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -283,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       if constexpr (!kFused) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
           uint32_t r[32];
           ptx::tmem_ld_32x32b_x32(t_row + c, r);
           ptx::tmem_ld_wait();
@@ -301,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        fused_epilogue<BN>(epi, t_row, row, Mr, n0);
+        fused_epilogue<BN>(epi, t_row, row, Mr, n0, c_lo);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -367,7 +378,7 @@ cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int K
   }
   const int64_t tiles = ((Mr + kBM - 1) / kBM) * ((Nc + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  if constexpr (kFused) epi.n_vt = epi.d / BN;
+  if constexpr (kFused) epi.n_sl = epi.d / (BN / 2);
   gemm_bf16_kernel<BN, kFused><<<grid, kThreads, G::kSmem, s>>>(ta, tb, static_cast<__nv_bfloat16*>(C),
                                                                 static_cast<int>(Mr), Nc, Kd, err, epi);
   return cudaGetLastError();
@@ -454,7 +465,7 @@ cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d,
 
 int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms) {
   const int bn = pick_bn(Mr, (M + 1) * d, d, num_sms);
-  return (d / bn) * (1 + 3 * M);
+  return (d / (bn / 2)) * (1 + 3 * M);
 }
 
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s) {
