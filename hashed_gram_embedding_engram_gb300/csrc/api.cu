@@ -141,7 +141,8 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   const int R = (c.N - 1) * c.K;
   if (R > engram::kMaxR) return ENGRAM_ERR_INVALID_ARG;
   if (c.M < 1 || c.M > engram::kMaxM || c.d < 8 || c.d % 8) return ENGRAM_ERR_INVALID_ARG;
-  if (c.conv_w < 1 || c.conv_w > engram::kMaxConvW || c.conv_dilation < 1) return ENGRAM_ERR_INVALID_ARG;
+  if (c.conv_w < 1 || c.conv_w > engram::kMaxConvW || c.conv_dilation < 1 || c.conv_dilation > 64)
+    return ENGRAM_ERR_INVALID_ARG;
   if (!(c.eps > 0.f) || !std::isfinite(c.eps)) return ENGRAM_ERR_INVALID_ARG;
   if (!c.primes || !c.multipliers) return ENGRAM_ERR_INVALID_ARG;
   if (max_tokens <= 0 || max_tokens > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
@@ -203,6 +204,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
     h.mults[i] = c.multipliers[i];
     p->mults.push_back(c.multipliers[i]);
   }
+  p->host = h;
   if (cudaMalloc(&p->dev, sizeof(PlanDev)) != cudaSuccess) {
     delete p;
     return ENGRAM_ERR_CUDA;
@@ -276,6 +278,8 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
   const float* v = nullptr;
   int64_t sv = 0;
   mark(plan, s);
+  const float* part = nullptr;
+  int n_sl = 0;
   if (plan->cfg.act_dtype == ENGRAM_F32) {
     if (engram::gemm_f32_simt(static_cast<const float*>(e), static_cast<const float*>(w->w_kv), ws.kv, ntok,
                               (M + 1) * d, plan->d_mem, s) != cudaSuccess)
@@ -290,16 +294,14 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
                                  plan->num_sms, &plan->dev->err, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
-    mark(plan, s);
-    const int n_vt = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
-    if (engram::launch_finalize(plan, ws.part, n_vt, ntok, ws.alpha, ws.rinv, s) != cudaSuccess)
-      return ENGRAM_ERR_CUDA;
+    part = ws.part;
+    n_sl = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
     v = ws.v32;
     sv = d;
   }
   mark(plan, s);
-  if (engram::launch_conv_residual(plan, v, sv, ws.alpha, ws.rinv, B, T, w->g_c, w->conv, H, state, s) !=
-      cudaSuccess)
+  if (engram::launch_conv_residual(plan, v, sv, part, n_sl, ws.alpha, ws.rinv, B, T, w->g_c, w->conv, H, state,
+                                   s) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
   mark(plan, s);
   if (state) {
@@ -353,9 +355,8 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   const int32_t* prev = state ? state->prev_ids : nullptr;
   plan->n_marks = 0;
   mark(plan, s);
-  if (engram::launch_hash(plan, ids, B, T, proj, V, prev, ws.idx, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
-  mark(plan, s);
-  if (engram::launch_gather(plan, ws.idx, ntok, tab, static_cast<const uint16_t*>(sc), ws.e, s) != cudaSuccess)
+  if (engram::launch_hash_gather(plan, ids, B, T, proj, V, prev, tab, static_cast<const uint16_t*>(sc), ws.e, s) !=
+      cudaSuccess)
     return ENGRAM_ERR_CUDA;
   return run_stage_b(plan, ws, ws.e, ids, proj, V, B, T, w, H, state, s);
 }

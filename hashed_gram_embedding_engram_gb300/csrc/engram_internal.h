@@ -20,8 +20,9 @@ constexpr int kMaxM = 8;
 constexpr uint32_t kErrIndexRange = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 
-// Device-resident parameter block of a plan.  Kernels copy what they need into
-// shared memory at start.
+// Parameter block of a plan.  A device copy holds the error word; kernels get
+// the parameters by value (a __grid_constant__ argument, read from the
+// constant bank), so no block starts with a dependent global load.
 struct PlanDev {
   uint32_t err;                    // error word (atomicOr from kernels)
   int32_t R;
@@ -48,7 +49,8 @@ struct engram_plan {
   std::vector<uint32_t> primes;
   std::vector<uint64_t> mults;
   std::vector<int64_t> offsets;
-  engram::PlanDev* dev;            // device copy of the parameter block
+  engram::PlanDev* dev;            // device copy of the parameter block (its err word is live)
+  engram::PlanDev host;            // host copy, passed to kernels by value
   // tracing: events recorded around each kernel of the last engram_forward
   static constexpr int kMaxMarks = 8;
   cudaEvent_t marks[kMaxMarks];
@@ -76,15 +78,20 @@ cudaError_t launch_hash(const engram_plan* p, const int32_t* ids, int B, int T, 
                         const int32_t* prev_ids, int32_t* idx, cudaStream_t s);
 cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
                           const uint16_t* scales, void* e, cudaStream_t s);
+// Steps 1-4 fused: indices computed per row inside the gather, never stored.
+cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                               const int32_t* prev_ids, const void* table, const uint16_t* scales, void* e,
+                               cudaStream_t s);
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
                                  cudaStream_t s);
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
                             const float* g_k, float* alpha, float* rinv, cudaStream_t s);
-cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_vt, int64_t ntok, float* alpha,
-                            float* rinv, cudaStream_t s);
-cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
-                                 const float* rinv, int B, int T, const float* g_c, const float* conv, void* H,
-                                 const engram_state_t* state, cudaStream_t s);
+// Conv + SiLU + skip + residual over B sequences of T positions.  With `part`
+// (bf16 layers) alpha/rinv are computed from the gate partials (n_sl slices)
+// and written; without it they are read.
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* part, int n_sl,
+                                 float* alpha, float* rinv, int B, int T, const float* g_c, const float* conv,
+                                 void* H, const engram_state_t* state, cudaStream_t s);
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
                                 int64_t sv, const float* alpha, const float* rinv, int B, int T, const float* g_c,
                                 const engram_state_t* state, cudaStream_t s);

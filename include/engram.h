@@ -81,7 +81,7 @@ typedef struct {
   int d;                        /* hidden size; multiple of 8 (bf16) / 4 (f32) */
   int M;                        /* hyper-connection branches, 1 <= M <= 8 */
   int conv_w;                   /* conv taps, 1 <= conv_w <= 8 */
-  int conv_dilation;            /* >= 1 (the pages use the max order N) */
+  int conv_dilation;            /* 1..64 (the pages use the max order N) */
   engram_dtype_t table_dtype;   /* F32, BF16 or I8_ROWSCALE_F16 */
   engram_dtype_t act_dtype;     /* F32 or BF16: H, W_kv, e and the k/v buffer */
   float eps;                    /* RMSNorm epsilon, > 0 */
@@ -188,8 +188,11 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
 
 /* Tracing.  With timing on, engram_forward / engram_stage_b record one of
  * the plan's CUDA events on `stream` before the first kernel and after every
- * kernel they launch: hash, gather, K/V projection, gate (finalize for BF16),
- * conv + residual, and the state update when a state is given.  For use on
+ * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps
+ * 1-4 in one kernel), K/V projection with the gate reductions, conv +
+ * residual with the gate; on F32 layers: hash + gather, K/V projection, gate,
+ * conv + residual; then the state update when a state is given.
+ * engram_stage_b records the same list without the first kernel.  For use on
  * one stream at a time, outside CUDA-graph capture.  enable: 0 or 1. */
 engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable);
 
