@@ -16,12 +16,14 @@
 //                     sequence: first the scalars of the tile and its causal
 //                     halo of (w-1)*dilation positions into shared memory, then
 //                     one thread per 4 channels walks the tile's positions with
-//                     its taps and g_c in registers; the v rows of the taps come
+//                     its taps (times g_c) in registers; the v rows of the taps come
 //                     from L1/L2 (the thread itself read them a few positions
 //                     earlier), the history before a chunk from the caller's
 //                     ring; SiLU, skip and H += Y for all M branches in place.
 //   state_kernel      after the chunk: writes the last (w-1)*dilation conv
-//                     inputs into the ring, rolls the last N-1 projected ids,
+//                     inputs RMSNorm(v~) (before the weight g_c, which the conv
+//                     folds into its taps) into the ring, rolls the last N-1
+//                     projected ids,
 //                     advances pos (a separate launch: the ring slots it
 //                     writes are slots the conv still reads).
 #include <cuda_bf16.h>
@@ -146,13 +148,16 @@ struct ConvArgs {
   int L;
 };
 
+// SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
 template <typename TH, int W>
 __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __restrict__ H) {
-  extern __shared__ float s_sc[];                  // [2][(TT + halo) * M]: alpha, rinv
+  extern __shared__ float s_sc[];                  // [2][(TT + halo) * M]: s = alpha * rinv, alpha
   const int halo = (W - 1) * a.dil;
   const int span = (a.TT + halo) * a.M;
-  float* s_a = s_sc;
-  float* s_r = s_sc + span;
+  float* s_s = s_sc;
+  float* s_a = s_sc + span;
   const int M = a.M, d = a.d;
   const int groups = d / 4;
   const int tiles_per_seq = (a.Tn + a.TT - 1) / a.TT;
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
   const float inv_d = 1.f / static_cast<float>(d);
   const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
   const int P = a.n_sl * (1 + 3 * M);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
 
   for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     const int b = tile / tiles_per_seq;
@@ -167,37 +173,45 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
     const int tn = min(a.TT, a.Tn - t0);
     const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
 
-    // ---- scalars of positions [t0 - halo, t0 + tn) of this chunk
-    for (int i = threadIdx.x; i < (tn + halo) * M; i += blockDim.x) {
-      const int tl = t0 - halo + i / M;
-      const int m = i - (i / M) * M;
+    // ---- scalars of positions [t0 - halo, t0 + tn) of this chunk, one warp per position
+    for (int pi = warp; pi < tn + halo; pi += n_warps) {
+      const int tl = t0 - halo + pi;
       if (tl < 0) continue;
       const int64_t tok = tok_b + tl;
-      float al, ri;
       if (a.part != nullptr) {
         const float* p = a.part + tok * P;
-        float sv = 0.f, dot = 0.f, sk = 0.f, sh = 0.f;
-        for (int j = 0; j < a.n_sl; ++j) {
-          sv += p[j];
-          const float* q = p + a.n_sl + (m * a.n_sl + j) * 3;
-          dot += q[0];
-          sk += q[1];
-          sh += q[2];
+        float sv = 0.f;
+        for (int j = lane; j < a.n_sl; j += 32) sv += p[j];
+        sv = warp_sum(sv);
+        for (int m = 0; m < M; ++m) {
+          float dot = 0.f, sk = 0.f, sh = 0.f;
+          for (int j = lane; j < a.n_sl; j += 32) {
+            const float* q = p + a.n_sl + (m * a.n_sl + j) * 3;
+            dot += q[0];
+            sk += q[1];
+            sh += q[2];
+          }
+          dot = warp_sum(dot);
+          sk = warp_sum(sk);
+          sh = warp_sum(sh);
+          if (lane == 0) {
+            const float rh = 1.f / sqrtf(sh * inv_d + a.eps);
+            const float rk = 1.f / sqrtf(sk * inv_d + a.eps);
+            const float al = sigmoidf(dot * rh * rk * inv_sqrt_d);
+            const float ri = 1.f / sqrtf(al * al * (sv * inv_d) + a.eps);
+            s_s[pi * M + m] = al * ri;
+            s_a[pi * M + m] = al;
+            if (tl >= t0) {                        // the tile that owns the position records it
+              a.alpha[tok * M + m] = al;
+              a.rinv[tok * M + m] = ri;
+            }
+          }
         }
-        const float rh = 1.f / sqrtf(sh * inv_d + a.eps);
-        const float rk = 1.f / sqrtf(sk * inv_d + a.eps);
-        al = sigmoidf(dot * rh * rk * inv_sqrt_d);
-        ri = 1.f / sqrtf(al * al * (sv * inv_d) + a.eps);
-        if (tl >= t0) {                            // the tile that owns the position records it
-          a.alpha[tok * M + m] = al;
-          a.rinv[tok * M + m] = ri;
-        }
-      } else {
-        al = a.alpha[tok * M + m];
-        ri = a.rinv[tok * M + m];
+      } else if (lane < M) {
+        const float al = a.alpha[tok * M + lane], ri = a.rinv[tok * M + lane];
+        s_s[pi * M + lane] = al * ri;
+        s_a[pi * M + lane] = al;
       }
-      s_a[i] = al;
-      s_r[i] = ri;
     }
     __syncthreads();
 
@@ -205,27 +219,30 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
     const int p0 = a.ring ? a.pos[b] : 0;
     for (int g = threadIdx.x; g < groups; g += blockDim.x) {
       const int c = g * 4;
-      float w[4][W];
+      float wq[4][W];                               // taps times the RMSNorm weight g_c
+      float gc[4];
+      ld4(a.g_c + c, gc);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if constexpr (W == 4) {
-          ld4(a.conv + static_cast<int64_t>(c + i) * W, w[i]);
+          ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
         } else {
 #pragma unroll
-          for (int j = 0; j < W; ++j) w[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
+          for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
         }
+#pragma unroll
+        for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
       }
-      float gc[4];
-      ld4(a.g_c + c, gc);
-      for (int ti = 0; ti < tn; ++ti) {
+      const float* vp = a.v + (tok_b + t0) * a.sv + c;
+      TH* hp = H + ((tok_b + t0) * M) * static_cast<int64_t>(d) + c;
+      for (int ti = 0; ti < tn; ++ti, vp += a.sv, hp += static_cast<int64_t>(M) * d) {
         const int t = t0 + ti;
-        const int64_t tok = tok_b + t;
         float v[W][4];
 #pragma unroll
         for (int j = 0; j < W; ++j) {
           const int lag = (W - 1 - j) * a.dil;
           if (t - lag >= 0) {
-            ld4(a.v + (tok - lag) * a.sv + c, v[j]);
+            ld4(vp - lag * a.sv, v[j]);
           } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[j][i] = 0.f;
@@ -236,12 +253,11 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
 #pragma unroll
           for (int j = 0; j < W; ++j) {
             const int lag = (W - 1 - j) * a.dil;
-            float u[4];
+            float u[4];                             // RMSNorm(v~) before its weight
             if (t - lag >= 0) {
-              const int si = (ti + halo - lag) * M + m;
-              const float al = s_a[si], ri = s_r[si];
+              const float sj = s_s[(ti + halo - lag) * M + m];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) u[i] = ((al * v[j][i]) * ri) * gc[i];
+              for (int i = 0; i < 4; ++i) u[i] = sj * v[j][i];
             } else {
               const int abs_pos = p0 + t - lag;
               if (a.ring != nullptr && abs_pos >= 0) {
@@ -252,15 +268,14 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
               }
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(w[i][j], u[i], acc[i]);
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
           }
           const float a_t = s_a[(ti + halo) * M + m];
-          TH* hp = H + (tok * M + m) * static_cast<int64_t>(d) + c;
           float h[4];
-          H4<TH>::load(hp, h);
+          H4<TH>::load(hp + static_cast<int64_t>(m) * d, h);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) h[i] += acc[i] * sigmoidf(acc[i]) + a_t * v[W - 1][i];
-          H4<TH>::store(hp, h);
+          for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + a_t * v[W - 1][i];
+          H4<TH>::store(hp + static_cast<int64_t>(m) * d, h);
         }
       }
     }
@@ -289,10 +304,10 @@ __global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_
     const int c = g * 4;
     float v[4];
     ld4(v_base + tok * sv + c, v);
-    const float al = alpha[tok * M + m], ri = rinv[tok * M + m];
+    const float sc = alpha[tok * M + m] * rinv[tok * M + m];
     float* dst = ring + ((static_cast<int64_t>(b) * L + (p0 + t) % L) * M + m) * d + c;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = ((al * v[i]) * ri) * g_c[c + i];
+    for (int i = 0; i < 4; ++i) dst[i] = sc * v[i];
   }
   __syncthreads();                              // every thread has read pos[b]
   if (threadIdx.x == 0) {

@@ -5,19 +5,20 @@
 // or in pinned host memory reached over UVA (NVLink-C2C on Grace-Blackwell).
 //
 // Layout trick: because the R rows of one token are concatenated in (n,k)
-// order, the 16-byte chunk number f of the flattened work list
-//   f = (token*R + r) * chunks_per_row + c
-// is also the 16-byte slot of the output (copy) or 32-byte slot (int8 -> bf16).
-// Consecutive threads therefore read consecutive chunks of one row (one
-// 64/128-byte transaction per row) and write perfectly contiguous output;
-// no shared-memory staging is needed for coalescing.  Each thread keeps
-// kItems independent 16-byte loads in flight before it stores anything.
+// order, the 16-byte chunk f = r * chunks_per_row + c of a token's rows is
+// also the 16-byte slot of its output (copy) or 32-byte slot (int8 -> bf16).
+// A warp owns one token: consecutive lanes read consecutive chunks of a row
+// (one 64/128-byte transaction per row) and write contiguous output, so no
+// shared-memory staging is needed for coalescing; each lane keeps several
+// independent 16-byte loads in flight before it stores anything.
 //
-// Two entry kernels share this body: gather_kernel reads the indices from
-// memory (engram_gather), hash_gather_kernel computes them (Steps 1-3, in
-// hashing.cuh) for the row it is about to read (engram_forward), so the
-// indices never travel through HBM.  All lanes of a row compute the same index
-// in the same instructions, which costs no extra issue slots.
+// The same kernel serves engram_gather (indices read from memory) and
+// engram_forward (indices computed from the token ids for the rows about to
+// be read, Steps 1-3 -- the arithmetic of hashing.cuh -- so they never
+// travel through HBM).  There the warp first loads the token's n-gram window
+// (lane i holds x'_{t-i}) and broadcasts it by shuffle; each lane computes the
+// index of its chunk's row from per-row constants in shared memory (the lanes
+// of one row compute the same index in the same instructions).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -29,7 +30,7 @@ namespace engram {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kItems = 8;
+constexpr int kWarpItems = 4;    // 16-byte chunks per lane per round
 
 __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
   uint4 v;
@@ -61,73 +62,107 @@ __device__ __forceinline__ void dequant16(uint4 q, float s, uint4& o0, uint4& o1
   o1 = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
-// Where the indices come from.
-struct IdxFromMemory {
-  const int32_t* idx;        // [ntok, R]
-  __device__ uint32_t operator()(const PlanDev&, int64_t row_item, int, bool&) const {
-    return static_cast<uint32_t>(__ldg(idx + row_item));
+template <int kCpr, bool kInt8, bool kHash>
+__global__ void __launch_bounds__(kThreads)
+    row_gather_kernel(const __grid_constant__ PlanDev pd, uint32_t* __restrict__ err,
+                      const int32_t* __restrict__ idx, const int32_t* __restrict__ ids, int T,
+                      const int32_t* __restrict__ proj, int V, const int32_t* __restrict__ prev, int64_t ntok,
+                      const uint8_t* __restrict__ table, const __half* __restrict__ scales,
+                      uint4* __restrict__ out) {
+  __shared__ uint64_t s_mult[kMaxMults];
+  __shared__ uint64_t s_mu[kMaxR];
+  __shared__ int64_t s_off[kMaxR];
+  __shared__ uint32_t s_p[kMaxR];
+  __shared__ int32_t s_mo[kMaxR];      // index of m_{n,k,0} in s_mult for row r
+  __shared__ int32_t s_n[kMaxR];       // order n of row r
+  const int R = pd.R, N = pd.N, K = pd.K;
+  for (int i = threadIdx.x; i < pd.mult_base[N] + K * N; i += blockDim.x) s_mult[i] = pd.mults[i];
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    const int n = 2 + r / K, k = r - (r / K) * K;
+    s_mu[r] = pd.mu[r];
+    s_off[r] = pd.offsets[r];
+    s_p[r] = pd.primes[r];
+    s_n[r] = n;
+    s_mo[r] = pd.mult_base[n] + k * n;
   }
-};
-struct IdxFromHash {
-  const int32_t* ids;        // [B, T] raw ids
-  const int32_t* proj;       // [V]
-  const int32_t* prev;       // [B, N-1] or nullptr
-  int T;
-  int V;
-  __device__ uint32_t operator()(const PlanDev& pd, int64_t row_item, int r, bool& bad) const {
-    const int64_t tok = row_item / pd.R;
-    const int b = static_cast<int>(tok / T);
-    const int t = static_cast<int>(tok - static_cast<int64_t>(b) * T);
-    return hash_index(pd, ids, T, b, t, r, proj, V, prev, bad);
-  }
-};
+  __syncthreads();
 
-template <int kCpr, bool kInt8, typename Src>
-__device__ __forceinline__ void gather_body(const PlanDev& pd, uint32_t* err, const Src& src, int64_t ntok,
-                                            const uint8_t* __restrict__ table, const __half* __restrict__ scales,
-                                            uint4* __restrict__ out) {
   constexpr int kRowBytes = kCpr * 16;
-  const int R = pd.R;
-  const int64_t total = ntok * R * kCpr;
-  const int64_t span = static_cast<int64_t>(kThreads) * kItems;
+  const int lane = threadIdx.x & 31;
+  const int per_tok = R * kCpr;
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   bool bad = false;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * span; base < total;
-       base += static_cast<int64_t>(gridDim.x) * span) {
-    uint4 v[kItems];
-    float sc[kItems];
-    bool ok[kItems];
-#pragma unroll
-    for (int j = 0; j < kItems; ++j) {
-      const int64_t f = base + j * kThreads + threadIdx.x;
-      ok[j] = false;
-      v[j] = make_uint4(0, 0, 0, 0);
-      sc[j] = 0.f;
-      if (f < total) {
-        const int64_t row_item = f / kCpr;          // token*R + r
-        const int c = static_cast<int>(f % kCpr);
-        const int r = static_cast<int>(row_item % R);
-        const uint32_t z = src(pd, row_item, r, bad);
-        if (z < pd.primes[r]) {
-          const int64_t row = pd.offsets[r] + z;
-          v[j] = ld_stream_16(table + row * kRowBytes + c * 16);
-          if constexpr (kInt8) sc[j] = __half2float(scales[row]);
-          ok[j] = true;
-        } else {
-          bad = true;
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
+       tok += n_warps) {
+    uint64_t xp[kMaxN];
+    if constexpr (kHash) {
+      const int b = static_cast<int>(tok / T);
+      const int t = static_cast<int>(tok - static_cast<int64_t>(b) * T);
+      int64_t x = 0;                                   // lane i: x'_{t-i}, pad 0 before the start
+      if (lane < N) {
+        const int tt = t - lane;
+        if (tt >= 0) {
+          int raw = __ldg(ids + static_cast<int64_t>(b) * T + tt);
+          if (static_cast<unsigned>(raw) >= static_cast<unsigned>(V)) {
+            bad = true;
+            raw = 0;
+          }
+          x = __ldg(proj + raw);
+        } else if (prev != nullptr) {
+          x = __ldg(prev + static_cast<int64_t>(b) * (N - 1) + (N - 1) + tt);
         }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < kItems; ++j) {
-      const int64_t f = base + j * kThreads + threadIdx.x;
-      if (f < total) {
-        if constexpr (kInt8) {
-          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-          if (ok[j]) dequant16(v[j], sc[j], o0, o1);
-          out[2 * f] = o0;
-          out[2 * f + 1] = o1;
-        } else {
-          out[f] = v[j];
+      for (int i = 0; i < kMaxN; ++i) xp[i] = static_cast<uint64_t>(__shfl_sync(0xFFFFFFFFu, x, i));
+    }
+    uint4* dst = out + (kInt8 ? 2 : 1) * tok * per_tok;
+    for (int f0 = 0; f0 < per_tok; f0 += 32 * kWarpItems) {
+      uint4 v[kWarpItems];
+      float sc[kWarpItems];
+      bool ok[kWarpItems];
+#pragma unroll
+      for (int j = 0; j < kWarpItems; ++j) {
+        const int f = f0 + j * 32 + lane;
+        ok[j] = false;
+        v[j] = make_uint4(0, 0, 0, 0);
+        sc[j] = 0.f;
+        if (f < per_tok) {
+          const int r = f / kCpr;
+          const int c = f % kCpr;
+          uint32_t z;
+          if constexpr (kHash) {
+            const uint64_t* m = s_mult + s_mo[r];
+            const int n = s_n[r];
+            uint64_t h = 0;
+#pragma unroll
+            for (int i = 0; i < kMaxN; ++i)
+              if (i < n) h ^= xp[i] * m[i];
+            z = barrett_mod(h, s_p[r], s_mu[r]);
+          } else {
+            z = static_cast<uint32_t>(__ldg(idx + tok * R + r));
+          }
+          if (z < s_p[r]) {
+            const int64_t row = s_off[r] + z;
+            v[j] = ld_stream_16(table + row * kRowBytes + c * 16);
+            if constexpr (kInt8) sc[j] = __half2float(scales[row]);
+            ok[j] = true;
+          } else {
+            bad = true;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kWarpItems; ++j) {
+        const int f = f0 + j * 32 + lane;
+        if (f < per_tok) {
+          if constexpr (kInt8) {
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (ok[j]) dequant16(v[j], sc[j], o0, o1);
+            dst[2 * f] = o0;
+            dst[2 * f + 1] = o1;
+          } else {
+            dst[f] = v[j];
+          }
         }
       }
     }
@@ -135,29 +170,10 @@ __device__ __forceinline__ void gather_body(const PlanDev& pd, uint32_t* err, co
   if (bad) atomicOr(err, kErrIndexRange);
 }
 
-template <int kCpr, bool kInt8>
-__global__ void __launch_bounds__(kThreads) gather_kernel(const __grid_constant__ PlanDev pd, uint32_t* __restrict__ err,
-                                                          const int32_t* __restrict__ idx, int64_t ntok,
-                                                          const uint8_t* __restrict__ table,
-                                                          const __half* __restrict__ scales,
-                                                          uint4* __restrict__ out) {
-  gather_body<kCpr, kInt8>(pd, err, IdxFromMemory{idx}, ntok, table, scales, out);
-}
-
-template <int kCpr, bool kInt8>
-__global__ void __launch_bounds__(kThreads)
-    hash_gather_kernel(const __grid_constant__ PlanDev pd, uint32_t* __restrict__ err,
-                       const int32_t* __restrict__ ids, int B, int T, const int32_t* __restrict__ proj, int V,
-                       const int32_t* __restrict__ prev, const uint8_t* __restrict__ table,
-                       const __half* __restrict__ scales, uint4* __restrict__ out) {
-  gather_body<kCpr, kInt8>(pd, err, IdxFromHash{ids, proj, prev, T, V}, static_cast<int64_t>(B) * T, table, scales,
-                           out);
-}
-
-int grid_blocks(const engram_plan* p, int64_t total) {
-  const int64_t span = static_cast<int64_t>(kThreads) * kItems;
-  int64_t blocks = (total + span - 1) / span;
-  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;   // 8 x 256 threads resident per SM
+int grid_for_tokens(const engram_plan* p, int64_t ntok) {
+  const int64_t warps_per_block = kThreads / 32;
+  int64_t blocks = (ntok + warps_per_block - 1) / warps_per_block;
+  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
   if (blocks > cap) blocks = cap;
   return static_cast<int>(blocks);
 }
@@ -165,9 +181,9 @@ int grid_blocks(const engram_plan* p, int64_t total) {
 template <int kCpr, bool kInt8>
 cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
                        const uint16_t* scales, void* e, cudaStream_t s) {
-  gather_kernel<kCpr, kInt8><<<grid_blocks(p, ntok * p->R * kCpr), kThreads, 0, s>>>(
-      p->host, &p->dev->err, idx, ntok, static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
-      static_cast<uint4*>(e));
+  row_gather_kernel<kCpr, kInt8, false><<<grid_for_tokens(p, ntok), kThreads, 0, s>>>(
+      p->host, &p->dev->err, idx, nullptr, 1, nullptr, 0, nullptr, ntok, static_cast<const uint8_t*>(table),
+      reinterpret_cast<const __half*>(scales), static_cast<uint4*>(e));
   return cudaGetLastError();
 }
 
@@ -175,8 +191,8 @@ template <int kCpr, bool kInt8>
 cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                          const int32_t* prev, const void* table, const uint16_t* scales, void* e, cudaStream_t s) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
-  hash_gather_kernel<kCpr, kInt8><<<grid_blocks(p, ntok * p->R * kCpr), kThreads, 0, s>>>(
-      p->host, &p->dev->err, ids, B, T, proj, V, prev, static_cast<const uint8_t*>(table),
+  row_gather_kernel<kCpr, kInt8, true><<<grid_for_tokens(p, ntok), kThreads, 0, s>>>(
+      p->host, &p->dev->err, nullptr, ids, T, proj, V, prev, ntok, static_cast<const uint8_t*>(table),
       reinterpret_cast<const __half*>(scales), static_cast<uint4*>(e));
   return cudaGetLastError();
 }

@@ -112,8 +112,8 @@ typedef struct {
  * engram_forward after the chunk.  L = (conv_w - 1) * conv_dilation. */
 typedef struct {
   int32_t* prev_ids;            /* [B, N-1] projected ids before the chunk, oldest first (0 = pad) */
-  float* u_ring;                /* [B, L, M, d] conv inputs RMSNorm(v~)*g_c of the last L
-                                   positions; position p lives in slot p mod L */
+  float* u_ring;                /* [B, L, M, d] RMSNorm(v~) (before its weight g_c) of the
+                                   last L positions; position p lives in slot p mod L */
   int32_t* pos;                 /* [B] tokens already processed per sequence */
 } engram_state_t;
 
