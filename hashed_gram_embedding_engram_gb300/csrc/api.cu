@@ -141,7 +141,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   const int R = (c.N - 1) * c.K;
   if (R > engram::kMaxR) return ENGRAM_ERR_INVALID_ARG;
   if (c.M < 1 || c.M > engram::kMaxM || c.d < 8 || c.d % 8) return ENGRAM_ERR_INVALID_ARG;
-  if (c.conv_w < 1 || c.conv_w > engram::kMaxConvW || c.conv_dilation < 1 || c.conv_dilation > 64)
+  if (c.conv_w < 1 || c.conv_w > engram::kMaxConvW || c.conv_dilation < 1 || (c.conv_w - 1) * c.conv_dilation > 192)
     return ENGRAM_ERR_INVALID_ARG;
   if (!(c.eps > 0.f) || !std::isfinite(c.eps)) return ENGRAM_ERR_INVALID_ARG;
   if (!c.primes || !c.multipliers) return ENGRAM_ERR_INVALID_ARG;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the host API and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -106,6 +107,10 @@ cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d,
                              cudaStream_t s);
 // Partials per token gemm_bf16_engram writes for this shape: (d / (BN/2)) * (1 + 3M).
 int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms);
+// 2-D tiled TMA descriptor of a row-major [rows, inner] array (fp32 or bf16),
+// rows row_stride_bytes apart, box of box_rows x box_inner elements.
+bool make_tensor_map_2d(CUtensorMap* map, const void* base, bool is_f32, uint64_t inner, uint64_t rows,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 // fp32 GEMM on the CUDA cores, same shapes.
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);
 

@@ -12,14 +12,14 @@
 //   fp32 layers: gate_kernel (one warp per token) computes alpha and rinv from
 //   the fp32 [v | k] buffer; conv_tile_kernel reads them.
 //
-//   conv_tile_kernel  one block per tile of TT consecutive positions of one
-//                     sequence: first the scalars of the tile and its causal
-//                     halo of (w-1)*dilation positions into shared memory, then
-//                     one thread per 4 channels walks the tile's positions with
-//                     its taps (times g_c) in registers; the v rows of the taps come
-//                     from L1/L2 (the thread itself read them a few positions
-//                     earlier), the history before a chunk from the caller's
-//                     ring; SiLU, skip and H += Y for all M branches in place.
+//   conv_tma_kernel   one block per (tile of TT consecutive positions of one
+//                     sequence, slice of up to 256 channels): TMA stages the
+//                     slice's v rows of the tile plus its causal halo of
+//                     (w-1)*dilation positions, and its H rows, in shared
+//                     memory while the block computes the gate scalars of the
+//                     tile and halo; then 4 channels per thread, taps (times
+//                     g_c) in registers, history before a chunk from the
+//                     caller's ring; SiLU, skip and H += Y for all M branches.
 //   state_kernel      after the chunk: writes the last (w-1)*dilation conv
 //                     inputs RMSNorm(v~) (before the weight g_c, which the conv
 //                     folds into its taps) into the ring, rolls the last N-1
@@ -29,7 +29,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "engram_internal.h"
+#include "ptx.cuh"
 
 namespace engram {
 namespace {
@@ -146,34 +149,76 @@ struct ConvArgs {
   const float* ring;     // [B, L, M, d] or nullptr
   const int32_t* pos;    // [B] or nullptr
   int L;
+  int CS;                // channels per slice (one block per tile x slice)
+  int halo_eff;          // largest lag that can land inside a chunk: min((W-1)*dil, T-1)
+  uint32_t* err;
 };
 
 // SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
+constexpr uint64_t kTmaWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
+
+// One block per (tile of TT positions of one sequence, slice of CS channels).
+// Thread 0 starts two TMA copies -- the slice's v rows of the tile and its
+// causal halo, and the slice's H rows of the tile -- and the block computes
+// the tile's gate scalars (one warp per position) while they land.  Then
+// CS/4 threads per position row read v and H from shared memory, convolve,
+// and write H back.
 template <typename TH, int W>
-__global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __restrict__ H) {
-  extern __shared__ float s_sc[];                  // [2][(TT + halo) * M]: s = alpha * rinv, alpha
+__global__ void __launch_bounds__(256) conv_tma_kernel(const __grid_constant__ CUtensorMap tm_v,
+                                                       const __grid_constant__ CUtensorMap tm_h, const ConvArgs a,
+                                                       TH* __restrict__ H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int M = a.M, d = a.d, CS = a.CS, TT = a.TT;
   const int halo = (W - 1) * a.dil;
-  const int span = (a.TT + halo) * a.M;
-  float* s_s = s_sc;
-  float* s_a = s_sc + span;
-  const int M = a.M, d = a.d;
-  const int groups = d / 4;
-  const int tiles_per_seq = (a.Tn + a.TT - 1) / a.TT;
-  const int n_tiles = a.B * tiles_per_seq;
+  const int box_v = TT + a.halo_eff;
+  // TMA destinations start on 128-byte boundaries
+  const size_t v_bytes = (static_cast<size_t>(box_v) * CS * 4 + 127) & ~size_t(127);
+  const size_t h_bytes = (static_cast<size_t>(TT) * M * CS * sizeof(TH) + 127) & ~size_t(127);
+  float* s_v = reinterpret_cast<float*>(smem);                          // [box_v][CS]
+  TH* s_h = reinterpret_cast<TH*>(smem + v_bytes);                      // [TT*M][CS]
+  float* s_s = reinterpret_cast<float*>(smem + v_bytes + h_bytes);      // [(TT+halo)*M]
+  float* s_a = s_s + (TT + halo) * M;
+  uint64_t* bar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(s_a + (TT + halo) * M) + 7) & ~uintptr_t(7));
+  const uint32_t tx_bytes = static_cast<uint32_t>(box_v) * CS * 4 + static_cast<uint32_t>(TT) * M * CS * sizeof(TH);
+
+  const int n_slices = d / CS;
+  const int tiles_per_seq = (a.Tn + TT - 1) / TT;
+  const int n_tiles = a.B * tiles_per_seq * n_slices;
   const float inv_d = 1.f / static_cast<float>(d);
   const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
   const int P = a.n_sl * (1 + 3 * M);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  const int tpr = CS / 4;                        // threads per position row
+  const int g = threadIdx.x % tpr, ty = threadIdx.x / tpr, rows_par = blockDim.x / tpr;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
 
   for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int b = tile / tiles_per_seq;
-    const int t0 = (tile - b * tiles_per_seq) * a.TT;
-    const int tn = min(a.TT, a.Tn - t0);
+    const int slice = tile % n_slices;
+    const int q = tile / n_slices;
+    const int b = q / tiles_per_seq;
+    const int t0 = (q - b * tiles_per_seq) * TT;
+    const int tn = min(TT, a.Tn - t0);
+    const int h0 = min(a.halo_eff, t0);            // in-chunk rows staged before t0
+    const int c0 = slice * CS;
     const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
 
-    // ---- scalars of positions [t0 - halo, t0 + tn) of this chunk, one warp per position
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // prior generic reads before async writes
+      ptx::mbar_arrive_expect_tx(bar, tx_bytes);
+      ptx::tma_load_2d_nohint(s_v, &tm_v, bar, c0, static_cast<int32_t>(tok_b + t0 - h0));
+      ptx::tma_load_2d_nohint(s_h, &tm_h, bar, c0, static_cast<int32_t>((tok_b + t0) * M));
+    }
+
+    // ---- gate scalars of positions [t0 - halo, t0 + tn), one warp per position
     for (int pi = warp; pi < tn + halo; pi += n_warps) {
       const int tl = t0 - halo + pi;
       if (tl < 0) continue;
@@ -186,10 +231,10 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
         for (int m = 0; m < M; ++m) {
           float dot = 0.f, sk = 0.f, sh = 0.f;
           for (int j = lane; j < a.n_sl; j += 32) {
-            const float* q = p + a.n_sl + (m * a.n_sl + j) * 3;
-            dot += q[0];
-            sk += q[1];
-            sh += q[2];
+            const float* qq = p + a.n_sl + (m * a.n_sl + j) * 3;
+            dot += qq[0];
+            sk += qq[1];
+            sh += qq[2];
           }
           dot = warp_sum(dot);
           sk = warp_sum(sk);
@@ -201,7 +246,7 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
             const float ri = 1.f / sqrtf(al * al * (sv * inv_d) + a.eps);
             s_s[pi * M + m] = al * ri;
             s_a[pi * M + m] = al;
-            if (tl >= t0) {                        // the tile that owns the position records it
+            if (tl >= t0 && slice == 0) {          // one block records each position
               a.alpha[tok * M + m] = al;
               a.rinv[tok * M + m] = ri;
             }
@@ -214,12 +259,17 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
       }
     }
     __syncthreads();
+    if (!ptx::mbar_wait_bounded(bar, phase, kTmaWaitNs)) {
+      atomicOr(a.err, kErrTimeout);
+      ptx::mbar_wait_bounded(bar, phase, kTmaWaitNs);   // our copies must land before the block can leave
+      break;
+    }
+    phase ^= 1;
 
-    // ---- one thread per 4 channels, walking the tile's positions
-    const int p0 = a.ring ? a.pos[b] : 0;
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-      const int c = g * 4;
-      float wq[4][W];                               // taps times the RMSNorm weight g_c
+    // ---- CS/4 threads per position row, 4 channels each
+    const int c = c0 + 4 * g;
+    float wq[4][W];                                // taps times the RMSNorm weight g_c
+    {
       float gc[4];
       ld4(a.g_c + c, gc);
 #pragma unroll
@@ -233,53 +283,52 @@ __global__ void __launch_bounds__(256) conv_tile_kernel(const ConvArgs a, TH* __
 #pragma unroll
         for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
       }
-      const float* vp = a.v + (tok_b + t0) * a.sv + c;
-      TH* hp = H + ((tok_b + t0) * M) * static_cast<int64_t>(d) + c;
-      for (int ti = 0; ti < tn; ++ti, vp += a.sv, hp += static_cast<int64_t>(M) * d) {
-        const int t = t0 + ti;
-        float v[W][4];
+    }
+    const int p0 = a.ring ? a.pos[b] : 0;
+    for (int ti = ty; ti < tn; ti += rows_par) {
+      const int t = t0 + ti;
+      float v[W][4];
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const int lag = (W - 1 - j) * a.dil;
+        if (t - lag >= 0) {
+          ld4(s_v + (ti + h0 - lag) * CS + 4 * g, v[j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[j][i] = 0.f;
+        }
+      }
+      for (int m = 0; m < M; ++m) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < W; ++j) {
           const int lag = (W - 1 - j) * a.dil;
+          float u[4];                              // RMSNorm(v~) before its weight
           if (t - lag >= 0) {
-            ld4(vp - lag * a.sv, v[j]);
+            const float sj = s_s[(ti + halo - lag) * M + m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[i] = sj * v[j][i];
           } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[j][i] = 0.f;
-          }
-        }
-        for (int m = 0; m < M; ++m) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < W; ++j) {
-            const int lag = (W - 1 - j) * a.dil;
-            float u[4];                             // RMSNorm(v~) before its weight
-            if (t - lag >= 0) {
-              const float sj = s_s[(ti + halo - lag) * M + m];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[i] = sj * v[j][i];
+            const int abs_pos = p0 + t - lag;
+            if (a.ring != nullptr && abs_pos >= 0) {
+              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + abs_pos % a.L) * M + m) * d + c, u);
             } else {
-              const int abs_pos = p0 + t - lag;
-              if (a.ring != nullptr && abs_pos >= 0) {
-                ld4(a.ring + ((static_cast<int64_t>(b) * a.L + abs_pos % a.L) * M + m) * d + c, u);
-              } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) u[i] = 0.f;
-              }
+              for (int i = 0; i < 4; ++i) u[i] = 0.f;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
           }
-          const float a_t = s_a[(ti + halo) * M + m];
-          float h[4];
-          H4<TH>::load(hp + static_cast<int64_t>(m) * d, h);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + a_t * v[W - 1][i];
-          H4<TH>::store(hp + static_cast<int64_t>(m) * d, h);
+          for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
         }
+        const float a_t = s_a[(ti + halo) * M + m];
+        float h[4];
+        H4<TH>::load(s_h + (ti * M + m) * CS + 4 * g, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + a_t * v[W - 1][i];
+        H4<TH>::store(H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c, h);
       }
     }
-    __syncthreads();                                // shared scalars are reused by the next tile
+    __syncthreads();                                // shared tiles are reused by the next tile
   }
 }
 
@@ -342,12 +391,55 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
+size_t conv_smem_bytes(const ConvArgs& a, int W, size_t esize) {
+  const int halo = (W - 1) * a.dil;
+  return 128 + (static_cast<size_t>(a.TT + a.halo_eff) * a.CS * 4 + 127) / 128 * 128 +
+         (static_cast<size_t>(a.TT) * a.M * a.CS * esize + 127) / 128 * 128 + 2 * static_cast<size_t>(a.TT + halo) * a.M * 4 +
+         16;
+}
+
 template <typename TH, int W>
-cudaError_t conv_launch(const engram_plan* p, const ConvArgs& a, void* H, cudaStream_t s) {
-  const int tiles = a.B * ((a.Tn + a.TT - 1) / a.TT);
-  const size_t smem = 2 * static_cast<size_t>(a.TT + (W - 1) * a.dil) * a.M * sizeof(float);
-  const int grid = tiles < p->num_sms * 8 ? tiles : p->num_sms * 8;
-  conv_tile_kernel<TH, W><<<grid, 256, smem, s>>>(a, static_cast<TH*>(H));
+cudaError_t conv_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
+  const size_t esize = sizeof(TH);
+  // channels per slice: the widest of 256/128/64/32/16/8 dividing d
+  a.CS = 8;
+  for (int cs : {256, 128, 64, 32, 16})
+    if (a.d % cs == 0) {
+      a.CS = cs;
+      break;
+    }
+  a.halo_eff = std::min((W - 1) * a.dil, a.Tn - 1);
+  const int64_t ntok = static_cast<int64_t>(a.B) * a.Tn;
+  const int n_slices = a.d / a.CS;
+  // positions per tile: at most 32 (and 256/M rows of H per copy), shared memory within
+  // 100 KB, and at least two blocks per SM when the batch allows it
+  int tt = std::min(32, a.Tn);
+  tt = std::min(tt, 256 / a.M);
+  while (tt > 1) {
+    a.TT = tt;
+    const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + tt - 1) / tt) * n_slices;
+    if (conv_smem_bytes(a, W, esize) <= 100 * 1024 && tiles >= 2LL * p->num_sms) break;
+    if (conv_smem_bytes(a, W, esize) <= 100 * 1024 && ntok * n_slices < 2LL * p->num_sms) break;
+    tt = tt > 8 ? tt - 4 : tt - 1;
+  }
+  a.TT = std::max(tt, 1);
+  const size_t smem = conv_smem_bytes(a, W, esize);
+  CUtensorMap tv, th;
+  if (!make_tensor_map_2d(&tv, a.v, true, a.d, ntok, a.sv * 4, a.CS, a.TT + a.halo_eff, false) ||
+      !make_tensor_map_2d(&th, H, esize == 4, a.d, ntok * a.M, static_cast<uint64_t>(a.d) * esize, a.CS,
+                          a.TT * a.M, false))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(conv_tma_kernel<TH, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024 + 512);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT) * n_slices;
+  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
+  conv_tma_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(tv, th, a,
+                                                                                       static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
@@ -396,13 +488,7 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.ring = state ? state->u_ring : nullptr;
   a.pos = state ? state->pos : nullptr;
   a.L = p->L_ring;
-  // positions per tile: about 3 tiles per SM, at most 32 positions
-  const int64_t ntok = static_cast<int64_t>(B) * T;
-  int64_t tt = (ntok + 3LL * p->num_sms - 1) / (3LL * p->num_sms);
-  if (tt < 1) tt = 1;
-  if (tt > 32) tt = 32;
-  if (tt > T) tt = T;
-  a.TT = static_cast<int>(tt);
+  a.err = &p->dev->err;
   if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, H, s);
   return conv_dispatch<__nv_bfloat16>(p, a, H, s);
 }

@@ -81,7 +81,7 @@ typedef struct {
   int d;                        /* hidden size; multiple of 8 (bf16) / 4 (f32) */
   int M;                        /* hyper-connection branches, 1 <= M <= 8 */
   int conv_w;                   /* conv taps, 1 <= conv_w <= 8 */
-  int conv_dilation;            /* 1..64 (the pages use the max order N) */
+  int conv_dilation;            /* >= 1, (conv_w-1)*conv_dilation <= 192 (the pages use N) */
   engram_dtype_t table_dtype;   /* F32, BF16 or I8_ROWSCALE_F16 */
   engram_dtype_t act_dtype;     /* F32 or BF16: H, W_kv, e and the k/v buffer */
   float eps;                    /* RMSNorm epsilon, > 0 */
