@@ -12,14 +12,16 @@
 //   fp32 layers: gate_kernel (one warp per token) computes alpha and rinv from
 //   the fp32 [v | k] buffer; conv_tile_kernel reads them.
 //
-//   conv_tma_kernel   one block per (tile of TT consecutive positions of one
-//                     sequence, slice of up to 256 channels): TMA stages the
-//                     slice's v rows of the tile plus its causal halo of
-//                     (w-1)*dilation positions, and its H rows, in shared
-//                     memory while the block computes the gate scalars of the
-//                     tile and halo; then 4 channels per thread, taps (times
-//                     g_c) in registers, history before a chunk from the
-//                     caller's ring; SiLU, skip and H += Y for all M branches.
+//   conv_window_kernel  one block per tile of 16 consecutive positions of one
+//                     sequence: the gate scalars of the tile and its causal
+//                     halo of (w-1)*dilation positions go to shared memory
+//                     (one warp per position), then one thread per 4 channels
+//                     walks the tile with its taps (times g_c) and a sliding
+//                     register window of RMSNorm(v~), so each v row is read
+//                     once; history before a chunk comes from the caller's
+//                     ring; SiLU, skip and H += Y for all M branches.  w = 4
+//                     with dilation 1..8 is compiled per case; other shapes use
+//                     conv_generic_kernel (the same arithmetic, taps re-read).
 //   state_kernel      after the chunk: writes the last (w-1)*dilation conv
 //                     inputs RMSNorm(v~) (before the weight g_c, which the conv
 //                     folds into its taps) into the ring, rolls the last N-1
@@ -32,7 +34,6 @@
 #include <algorithm>
 
 #include "engram_internal.h"
-#include "ptx.cuh"
 
 namespace engram {
 namespace {
@@ -149,186 +150,212 @@ struct ConvArgs {
   const float* ring;     // [B, L, M, d] or nullptr
   const int32_t* pos;    // [B] or nullptr
   int L;
-  int CS;                // channels per slice (one block per tile x slice)
-  int halo_eff;          // largest lag that can land inside a chunk: min((W-1)*dil, T-1)
-  uint32_t* err;
 };
 
 // SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
-constexpr uint64_t kTmaWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
-
-// One block per (tile of TT positions of one sequence, slice of CS channels).
-// Thread 0 starts two TMA copies -- the slice's v rows of the tile and its
-// causal halo, and the slice's H rows of the tile -- and the block computes
-// the tile's gate scalars (one warp per position) while they land.  Then
-// CS/4 threads per position row read v and H from shared memory, convolve,
-// and write H back.
-template <typename TH, int W>
-__global__ void __launch_bounds__(256) conv_tma_kernel(const __grid_constant__ CUtensorMap tm_v,
-                                                       const __grid_constant__ CUtensorMap tm_h, const ConvArgs a,
-                                                       TH* __restrict__ H) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const int M = a.M, d = a.d, CS = a.CS, TT = a.TT;
-  const int halo = (W - 1) * a.dil;
-  const int box_v = TT + a.halo_eff;
-  // TMA destinations start on 128-byte boundaries
-  const size_t v_bytes = (static_cast<size_t>(box_v) * CS * 4 + 127) & ~size_t(127);
-  const size_t h_bytes = (static_cast<size_t>(TT) * M * CS * sizeof(TH) + 127) & ~size_t(127);
-  float* s_v = reinterpret_cast<float*>(smem);                          // [box_v][CS]
-  TH* s_h = reinterpret_cast<TH*>(smem + v_bytes);                      // [TT*M][CS]
-  float* s_s = reinterpret_cast<float*>(smem + v_bytes + h_bytes);      // [(TT+halo)*M]
-  float* s_a = s_s + (TT + halo) * M;
-  uint64_t* bar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(s_a + (TT + halo) * M) + 7) & ~uintptr_t(7));
-  const uint32_t tx_bytes = static_cast<uint32_t>(box_v) * CS * 4 + static_cast<uint32_t>(TT) * M * CS * sizeof(TH);
-
-  const int n_slices = d / CS;
-  const int tiles_per_seq = (a.Tn + TT - 1) / TT;
-  const int n_tiles = a.B * tiles_per_seq * n_slices;
-  const float inv_d = 1.f / static_cast<float>(d);
-  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
-  const int P = a.n_sl * (1 + 3 * M);
+// Gate scalars of positions [t0 - halo, t0 + tn) of sequence b, one warp per
+// position: s = alpha * rinv (the scale that turns v into RMSNorm(v~) before
+// its weight) and alpha.  The block that owns a position records alpha and
+// rinv for the state update.
+__device__ void tile_scalars(const ConvArgs& a, int b, int t0, int tn, int halo, float* s_s, float* s_a) {
+  const int M = a.M;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  const int tpr = CS / 4;                        // threads per position row
-  const int g = threadIdx.x % tpr, ty = threadIdx.x / tpr, rows_par = blockDim.x / tpr;
-
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(bar, 1);
-    ptx::fence_mbar_init();
-  }
-  __syncthreads();
-  uint32_t phase = 0;
-
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int slice = tile % n_slices;
-    const int q = tile / n_slices;
-    const int b = q / tiles_per_seq;
-    const int t0 = (q - b * tiles_per_seq) * TT;
-    const int tn = min(TT, a.Tn - t0);
-    const int h0 = min(a.halo_eff, t0);            // in-chunk rows staged before t0
-    const int c0 = slice * CS;
-    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-
-    if (threadIdx.x == 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // prior generic reads before async writes
-      ptx::mbar_arrive_expect_tx(bar, tx_bytes);
-      ptx::tma_load_2d_nohint(s_v, &tm_v, bar, c0, static_cast<int32_t>(tok_b + t0 - h0));
-      ptx::tma_load_2d_nohint(s_h, &tm_h, bar, c0, static_cast<int32_t>((tok_b + t0) * M));
-    }
-
-    // ---- gate scalars of positions [t0 - halo, t0 + tn), one warp per position
-    for (int pi = warp; pi < tn + halo; pi += n_warps) {
-      const int tl = t0 - halo + pi;
-      if (tl < 0) continue;
-      const int64_t tok = tok_b + tl;
-      if (a.part != nullptr) {
-        const float* p = a.part + tok * P;
-        float sv = 0.f;
-        for (int j = lane; j < a.n_sl; j += 32) sv += p[j];
-        sv = warp_sum(sv);
-        for (int m = 0; m < M; ++m) {
-          float dot = 0.f, sk = 0.f, sh = 0.f;
-          for (int j = lane; j < a.n_sl; j += 32) {
-            const float* qq = p + a.n_sl + (m * a.n_sl + j) * 3;
-            dot += qq[0];
-            sk += qq[1];
-            sh += qq[2];
-          }
-          dot = warp_sum(dot);
-          sk = warp_sum(sk);
-          sh = warp_sum(sh);
-          if (lane == 0) {
-            const float rh = 1.f / sqrtf(sh * inv_d + a.eps);
-            const float rk = 1.f / sqrtf(sk * inv_d + a.eps);
-            const float al = sigmoidf(dot * rh * rk * inv_sqrt_d);
-            const float ri = 1.f / sqrtf(al * al * (sv * inv_d) + a.eps);
-            s_s[pi * M + m] = al * ri;
-            s_a[pi * M + m] = al;
-            if (tl >= t0 && slice == 0) {          // one block records each position
-              a.alpha[tok * M + m] = al;
-              a.rinv[tok * M + m] = ri;
-            }
-          }
-        }
-      } else if (lane < M) {
-        const float al = a.alpha[tok * M + lane], ri = a.rinv[tok * M + lane];
-        s_s[pi * M + lane] = al * ri;
-        s_a[pi * M + lane] = al;
-      }
-    }
-    __syncthreads();
-    if (!ptx::mbar_wait_bounded(bar, phase, kTmaWaitNs)) {
-      atomicOr(a.err, kErrTimeout);
-      ptx::mbar_wait_bounded(bar, phase, kTmaWaitNs);   // our copies must land before the block can leave
-      break;
-    }
-    phase ^= 1;
-
-    // ---- CS/4 threads per position row, 4 channels each
-    const int c = c0 + 4 * g;
-    float wq[4][W];                                // taps times the RMSNorm weight g_c
-    {
-      float gc[4];
-      ld4(a.g_c + c, gc);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if constexpr (W == 4) {
-          ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
-        }
-#pragma unroll
-        for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
-      }
-    }
-    const int p0 = a.ring ? a.pos[b] : 0;
-    for (int ti = ty; ti < tn; ti += rows_par) {
-      const int t = t0 + ti;
-      float v[W][4];
-#pragma unroll
-      for (int j = 0; j < W; ++j) {
-        const int lag = (W - 1 - j) * a.dil;
-        if (t - lag >= 0) {
-          ld4(s_v + (ti + h0 - lag) * CS + 4 * g, v[j]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) v[j][i] = 0.f;
-        }
-      }
+  const float inv_d = 1.f / static_cast<float>(a.d);
+  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(a.d));
+  const int P = a.n_sl * (1 + 3 * M);
+  const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
+  for (int pi = warp; pi < tn + halo; pi += n_warps) {
+    const int tl = t0 - halo + pi;
+    if (tl < 0) continue;
+    const int64_t tok = tok_b + tl;
+    if (a.part != nullptr) {
+      const float* p = a.part + tok * P;
+      float sv = 0.f;
+      for (int j = lane; j < a.n_sl; j += 32) sv += p[j];
+      sv = warp_sum(sv);
       for (int m = 0; m < M; ++m) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float dot = 0.f, sk = 0.f, sh = 0.f;
+        for (int j = lane; j < a.n_sl; j += 32) {
+          const float* q = p + a.n_sl + (m * a.n_sl + j) * 3;
+          dot += q[0];
+          sk += q[1];
+          sh += q[2];
+        }
+        dot = warp_sum(dot);
+        sk = warp_sum(sk);
+        sh = warp_sum(sh);
+        if (lane == 0) {
+          const float rh = 1.f / sqrtf(sh * inv_d + a.eps);
+          const float rk = 1.f / sqrtf(sk * inv_d + a.eps);
+          const float al = sigmoidf(dot * rh * rk * inv_sqrt_d);
+          const float ri = 1.f / sqrtf(al * al * (sv * inv_d) + a.eps);
+          s_s[pi * M + m] = al * ri;
+          s_a[pi * M + m] = al;
+          if (tl >= t0) {
+            a.alpha[tok * M + m] = al;
+            a.rinv[tok * M + m] = ri;
+          }
+        }
+      }
+    } else if (lane < M) {
+      const float al = a.alpha[tok * M + lane], ri = a.rinv[tok * M + lane];
+      s_s[pi * M + lane] = al * ri;
+      s_a[pi * M + lane] = al;
+    }
+  }
+}
+
+// Taps of channels c..c+3 times the conv-input RMSNorm weight g_c.
+template <int W>
+__device__ __forceinline__ void load_taps(const ConvArgs& a, int c, float (&wq)[4][W]) {
+  float gc[4];
+  ld4(a.g_c + c, gc);
 #pragma unroll
-        for (int j = 0; j < W; ++j) {
-          const int lag = (W - 1 - j) * a.dil;
-          float u[4];                              // RMSNorm(v~) before its weight
-          if (t - lag >= 0) {
-            const float sj = s_s[(ti + halo - lag) * M + m];
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (W == 4) {
+      ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
+    } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) u[i] = sj * v[j][i];
+      for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
+    }
+#pragma unroll
+    for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
+  }
+}
+
+// One block per tile of TT positions of one sequence, all channels; one
+// thread per 4 channels walks the tile with a sliding register window of
+// u = s * v (RMSNorm(v~) before its weight) over the last (W-1)*DIL + 1
+// positions, so every v row is read once.  W, DIL and TT are compile-time:
+// the window indices are static after unrolling.
+template <typename TH, int W, int DIL, int TT>
+__global__ void __launch_bounds__(256, 2) conv_window_kernel(const ConvArgs a, TH* __restrict__ H) {
+  constexpr int HALO = (W - 1) * DIL;
+  __shared__ float s_s[(TT + HALO) * kMaxM];
+  __shared__ float s_a[(TT + HALO) * kMaxM];
+  const int M = a.M, d = a.d, groups = d / 4;
+  const int tiles_per_seq = (a.Tn + TT - 1) / TT;
+  const int n_tiles = a.B * tiles_per_seq;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int b = tile / tiles_per_seq;
+    const int t0 = (tile - b * tiles_per_seq) * TT;
+    const int tn = min(TT, a.Tn - t0);
+    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
+    tile_scalars(a, b, t0, tn, HALO, s_s, s_a);
+    __syncthreads();
+    const int p0 = a.ring ? a.pos[b] : 0;
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+      const int c = 4 * g;
+      float wq[4][W];
+      load_taps<W>(a, c, wq);
+      const float* vrow = a.v + (tok_b + t0) * a.sv + c;       // v of position t0
+      for (int m = 0; m < M; ++m) {
+        float u[HALO + TT][4];                                // u[k]: position t0 - HALO + k
+#pragma unroll
+        for (int k = 0; k < HALO; ++k) {
+          const int tl = t0 - HALO + k;
+          if (tl >= 0) {
+            float v[4];
+            ld4(vrow + static_cast<int64_t>(k - HALO) * a.sv, v);
+            const float sk = s_s[k * M + m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[k][i] = sk * v[i];
+          } else if (a.ring != nullptr && p0 + tl >= 0) {
+            ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + tl) % a.L) * M + m) * d + c, u[k]);
           } else {
-            const int abs_pos = p0 + t - lag;
-            if (a.ring != nullptr && abs_pos >= 0) {
-              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + abs_pos % a.L) * M + m) * d + c, u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[k][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int ti = 0; ti < TT; ++ti) {
+          if (ti < tn) {
+            float v[4];
+            ld4(vrow + static_cast<int64_t>(ti) * a.sv, v);
+            const float st = s_s[(ti + HALO) * M + m], at = s_a[(ti + HALO) * M + m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[ti + HALO][i] = st * v[i];
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < W; ++j)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[ti + HALO - (W - 1 - j) * DIL][i], acc[i]);
+            TH* hp = H + ((tok_b + t0 + ti) * M + m) * static_cast<int64_t>(d) + c;
+            float h[4];
+            H4<TH>::load(hp, h);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * v[i];
+            H4<TH>::store(hp, h);
+          }
+        }
+      }
+    }
+    __syncthreads();                                // shared scalars are reused by the next tile
+  }
+}
+
+// Any (W, dilation): the same arithmetic with the v rows of every tap read
+// for every position (L1/L2 serve the repeats).
+template <typename TH, int W>
+__global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, TH* __restrict__ H) {
+  extern __shared__ float s_sc[];                  // [2][(TT + halo) * M]
+  const int halo = (W - 1) * a.dil;
+  float* s_s = s_sc;
+  float* s_a = s_sc + (a.TT + halo) * a.M;
+  const int M = a.M, d = a.d, groups = d / 4;
+  const int tiles_per_seq = (a.Tn + a.TT - 1) / a.TT;
+  const int n_tiles = a.B * tiles_per_seq;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int b = tile / tiles_per_seq;
+    const int t0 = (tile - b * tiles_per_seq) * a.TT;
+    const int tn = min(a.TT, a.Tn - t0);
+    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
+    tile_scalars(a, b, t0, tn, halo, s_s, s_a);
+    __syncthreads();
+    const int p0 = a.ring ? a.pos[b] : 0;
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+      const int c = 4 * g;
+      float wq[4][W];
+      load_taps<W>(a, c, wq);
+      for (int ti = 0; ti < tn; ++ti) {
+        const int t = t0 + ti;
+        const float* vp = a.v + (tok_b + t) * a.sv + c;
+        float v0[4];
+        ld4(vp, v0);
+        for (int m = 0; m < M; ++m) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < W; ++j) {
+            const int lag = (W - 1 - j) * a.dil;
+            float u[4];
+            if (t - lag >= 0) {
+              float v[4];
+              ld4(vp - static_cast<int64_t>(lag) * a.sv, v);
+              const float sj = s_s[(ti + halo - lag) * M + m];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) u[i] = sj * v[i];
+            } else if (a.ring != nullptr && p0 + t - lag >= 0) {
+              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
             } else {
 #pragma unroll
               for (int i = 0; i < 4; ++i) u[i] = 0.f;
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
           }
+          const float at = s_a[(ti + halo) * M + m];
+          TH* hp = H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c;
+          float h[4];
+          H4<TH>::load(hp, h);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+          for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * v0[i];
+          H4<TH>::store(hp, h);
         }
-        const float a_t = s_a[(ti + halo) * M + m];
-        float h[4];
-        H4<TH>::load(s_h + (ti * M + m) * CS + 4 * g, h);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + a_t * v[W - 1][i];
-        H4<TH>::store(H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c, h);
       }
     }
-    __syncthreads();                                // shared tiles are reused by the next tile
+    __syncthreads();
   }
 }
 
@@ -391,69 +418,52 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-size_t conv_smem_bytes(const ConvArgs& a, int W, size_t esize) {
-  const int halo = (W - 1) * a.dil;
-  return 128 + (static_cast<size_t>(a.TT + a.halo_eff) * a.CS * 4 + 127) / 128 * 128 +
-         (static_cast<size_t>(a.TT) * a.M * a.CS * esize + 127) / 128 * 128 + 2 * static_cast<size_t>(a.TT + halo) * a.M * 4 +
-         16;
+constexpr int kWindowTT = 16;
+
+template <typename TH, int W, int DIL>
+cudaError_t conv_window_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
+  a.TT = kWindowTT;
+  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + kWindowTT - 1) / kWindowTT);
+  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
+  conv_window_kernel<TH, W, DIL, kWindowTT><<<static_cast<int>(tiles < cap ? tiles : cap), 256, 0, s>>>(
+      a, static_cast<TH*>(H));
+  return cudaGetLastError();
 }
 
 template <typename TH, int W>
-cudaError_t conv_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
-  const size_t esize = sizeof(TH);
-  // channels per slice: the widest of 256/128/64/32/16/8 dividing d
-  a.CS = 8;
-  for (int cs : {256, 128, 64, 32, 16})
-    if (a.d % cs == 0) {
-      a.CS = cs;
-      break;
-    }
-  a.halo_eff = std::min((W - 1) * a.dil, a.Tn - 1);
-  const int64_t ntok = static_cast<int64_t>(a.B) * a.Tn;
-  const int n_slices = a.d / a.CS;
-  // positions per tile: at most 32 (and 256/M rows of H per copy), shared memory within
-  // 100 KB, and at least two blocks per SM when the batch allows it
-  int tt = std::min(32, a.Tn);
-  tt = std::min(tt, 256 / a.M);
-  while (tt > 1) {
-    a.TT = tt;
-    const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + tt - 1) / tt) * n_slices;
-    if (conv_smem_bytes(a, W, esize) <= 100 * 1024 && tiles >= 2LL * p->num_sms) break;
-    if (conv_smem_bytes(a, W, esize) <= 100 * 1024 && ntok * n_slices < 2LL * p->num_sms) break;
-    tt = tt > 8 ? tt - 4 : tt - 1;
-  }
-  a.TT = std::max(tt, 1);
-  const size_t smem = conv_smem_bytes(a, W, esize);
-  CUtensorMap tv, th;
-  if (!make_tensor_map_2d(&tv, a.v, true, a.d, ntok, a.sv * 4, a.CS, a.TT + a.halo_eff, false) ||
-      !make_tensor_map_2d(&th, H, esize == 4, a.d, ntok * a.M, static_cast<uint64_t>(a.d) * esize, a.CS,
-                          a.TT * a.M, false))
-    return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(conv_tma_kernel<TH, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024 + 512);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT) * n_slices;
+cudaError_t conv_generic_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
+  a.TT = std::min(16, a.Tn);
+  const size_t smem = 2 * static_cast<size_t>(a.TT + (W - 1) * a.dil) * a.M * sizeof(float);
+  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT);
   const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
-  conv_tma_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(tv, th, a,
-                                                                                       static_cast<TH*>(H));
+  conv_generic_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(a, static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
 template <typename TH>
 cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, void* H, cudaStream_t s) {
+  if (p->cfg.conv_w == 4) {
+    switch (a.dil) {   // the pages' short conv: w = 4, dilation = max n-gram order
+      case 1: return conv_window_launch<TH, 4, 1>(p, a, H, s);
+      case 2: return conv_window_launch<TH, 4, 2>(p, a, H, s);
+      case 3: return conv_window_launch<TH, 4, 3>(p, a, H, s);
+      case 4: return conv_window_launch<TH, 4, 4>(p, a, H, s);
+      case 5: return conv_window_launch<TH, 4, 5>(p, a, H, s);
+      case 6: return conv_window_launch<TH, 4, 6>(p, a, H, s);
+      case 7: return conv_window_launch<TH, 4, 7>(p, a, H, s);
+      case 8: return conv_window_launch<TH, 4, 8>(p, a, H, s);
+      default: break;
+    }
+  }
   switch (p->cfg.conv_w) {
-    case 1: return conv_launch<TH, 1>(p, a, H, s);
-    case 2: return conv_launch<TH, 2>(p, a, H, s);
-    case 3: return conv_launch<TH, 3>(p, a, H, s);
-    case 4: return conv_launch<TH, 4>(p, a, H, s);
-    case 5: return conv_launch<TH, 5>(p, a, H, s);
-    case 6: return conv_launch<TH, 6>(p, a, H, s);
-    case 7: return conv_launch<TH, 7>(p, a, H, s);
-    case 8: return conv_launch<TH, 8>(p, a, H, s);
+    case 1: return conv_generic_launch<TH, 1>(p, a, H, s);
+    case 2: return conv_generic_launch<TH, 2>(p, a, H, s);
+    case 3: return conv_generic_launch<TH, 3>(p, a, H, s);
+    case 4: return conv_generic_launch<TH, 4>(p, a, H, s);
+    case 5: return conv_generic_launch<TH, 5>(p, a, H, s);
+    case 6: return conv_generic_launch<TH, 6>(p, a, H, s);
+    case 7: return conv_generic_launch<TH, 7>(p, a, H, s);
+    case 8: return conv_generic_launch<TH, 8>(p, a, H, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -488,7 +498,6 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.ring = state ? state->u_ring : nullptr;
   a.pos = state ? state->pos : nullptr;
   a.L = p->L_ring;
-  a.err = &p->dev->err;
   if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, H, s);
   return conv_dispatch<__nv_bfloat16>(p, a, H, s);
 }
