@@ -168,7 +168,10 @@ __device__ void tile_scalars(const ConvArgs& a, int b, int t0, int tn, int halo,
   const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
   for (int pi = warp; pi < tn + halo; pi += n_warps) {
     const int tl = t0 - halo + pi;
-    if (tl < 0) continue;
+    if (tl < 0) {                       // history before the chunk: values used as they are
+      if (lane < M) s_s[pi * M + lane] = 1.f;
+      continue;
+    }
     const int64_t tok = tok_b + tl;
     if (a.part != nullptr) {
       const float* p = a.part + tok * P;
@@ -226,12 +229,17 @@ __device__ __forceinline__ void load_taps(const ConvArgs& a, int c, float (&wq)[
 }
 
 // One block per tile of TT positions of one sequence, all channels; one
-// thread per 4 channels walks the tile with a sliding register window of
-// u = s * v (RMSNorm(v~) before its weight) over the last (W-1)*DIL + 1
-// positions, so every v row is read once.  W, DIL and TT are compile-time:
-// the window indices are static after unrolling.
+// thread per 4 channels.  Each thread first issues every load it needs for
+// the tile -- the v rows of the tile and its causal halo (a register window,
+// static indices after unrolling), the H values, the ring history when the
+// tile starts a chunk -- and only then computes and stores, so the loads of
+// all positions are in flight together (v, ring and H are restrict-qualified
+// kernel arguments: the stores cannot alias the loads).  W, DIL and TT are
+// compile-time.
 template <typename TH, int W, int DIL, int TT>
-__global__ void __launch_bounds__(256, 2) conv_window_kernel(const ConvArgs a, TH* __restrict__ H) {
+__global__ void __launch_bounds__(256, 1)
+    conv_window_kernel(const ConvArgs a, const float* __restrict__ v, const float* __restrict__ ring,
+                       TH* __restrict__ H) {
   constexpr int HALO = (W - 1) * DIL;
   __shared__ float s_s[(TT + HALO) * kMaxM];
   __shared__ float s_a[(TT + HALO) * kMaxM];
@@ -245,49 +253,61 @@ __global__ void __launch_bounds__(256, 2) conv_window_kernel(const ConvArgs a, T
     const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
     tile_scalars(a, b, t0, tn, HALO, s_s, s_a);
     __syncthreads();
-    const int p0 = a.ring ? a.pos[b] : 0;
+    const int p0 = ring != nullptr ? a.pos[b] : 0;
     for (int g = threadIdx.x; g < groups; g += blockDim.x) {
       const int c = 4 * g;
       float wq[4][W];
       load_taps<W>(a, c, wq);
-      const float* vrow = a.v + (tok_b + t0) * a.sv + c;       // v of position t0
+      // v rows of positions t0 - HALO .. t0 + TT - 1 (zero outside the chunk)
+      const float* vrow = v + (tok_b + t0) * a.sv + c;
+      float vw[HALO + TT][4];
+#pragma unroll
+      for (int k = 0; k < HALO + TT; ++k) {
+        const int tl = t0 - HALO + k;
+        if (tl >= 0 && k - HALO < tn) {
+          ld4(vrow + static_cast<int64_t>(k - HALO) * a.sv, vw[k]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vw[k][i] = 0.f;
+        }
+      }
       for (int m = 0; m < M; ++m) {
-        float u[HALO + TT][4];                                // u[k]: position t0 - HALO + k
+        // positions before the chunk: the ring holds RMSNorm(v~) itself, and
+        // their scale in shared memory is 1 (x * 1 is exact)
+        if (t0 < HALO) {
 #pragma unroll
-        for (int k = 0; k < HALO; ++k) {
-          const int tl = t0 - HALO + k;
-          if (tl >= 0) {
-            float v[4];
-            ld4(vrow + static_cast<int64_t>(k - HALO) * a.sv, v);
-            const float sk = s_s[k * M + m];
+          for (int k = 0; k < HALO; ++k) {
+            const int tl = t0 - HALO + k;
+            if (tl < 0) {
+              if (ring != nullptr && p0 + tl >= 0) {
+                ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + tl) % a.L) * M + m) * d + c, vw[k]);
+              } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) u[k][i] = sk * v[i];
-          } else if (a.ring != nullptr && p0 + tl >= 0) {
-            ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + tl) % a.L) * M + m) * d + c, u[k]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) u[k][i] = 0.f;
+                for (int i = 0; i < 4; ++i) vw[k][i] = 0.f;
+              }
+            }
           }
         }
+        float hv[TT][4];
+        TH* hp = H + ((tok_b + t0) * M + m) * static_cast<int64_t>(d) + c;
+#pragma unroll
+        for (int ti = 0; ti < TT; ++ti)
+          if (ti < tn) H4<TH>::load(hp + static_cast<int64_t>(ti) * M * d, hv[ti]);
 #pragma unroll
         for (int ti = 0; ti < TT; ++ti) {
           if (ti < tn) {
-            float v[4];
-            ld4(vrow + static_cast<int64_t>(ti) * a.sv, v);
-            const float st = s_s[(ti + HALO) * M + m], at = s_a[(ti + HALO) * M + m];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) u[ti + HALO][i] = st * v[i];
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < W; ++j)
+            for (int j = 0; j < W; ++j) {
+              const int k = ti + HALO - (W - 1 - j) * DIL;   // window index of the tap's position
+              const float sk = s_s[k * M + m];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[ti + HALO - (W - 1 - j) * DIL][i], acc[i]);
-            TH* hp = H + ((tok_b + t0 + ti) * M + m) * static_cast<int64_t>(d) + c;
-            float h[4];
-            H4<TH>::load(hp, h);
+              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sk * vw[k][i], acc[i]);
+            }
+            const float at = s_a[(ti + HALO) * M + m];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * v[i];
-            H4<TH>::store(hp, h);
+            for (int i = 0; i < 4; ++i) hv[ti][i] += silu_fast(acc[i]) + at * vw[ti + HALO][i];
+            H4<TH>::store(hp + static_cast<int64_t>(ti) * M * d, hv[ti]);
           }
         }
       }
@@ -418,7 +438,7 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-constexpr int kWindowTT = 16;
+constexpr int kWindowTT = 8;
 
 template <typename TH, int W, int DIL>
 cudaError_t conv_window_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
@@ -426,7 +446,7 @@ cudaError_t conv_window_launch(const engram_plan* p, ConvArgs a, void* H, cudaSt
   const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + kWindowTT - 1) / kWindowTT);
   const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
   conv_window_kernel<TH, W, DIL, kWindowTT><<<static_cast<int>(tiles < cap ? tiles : cap), 256, 0, s>>>(
-      a, static_cast<TH*>(H));
+      a, a.v, a.ring, static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
