@@ -110,7 +110,7 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
     w.part = reinterpret_cast<float*>(take(n * (d / 32) * (1 + 3 * M) * 4));   // widest case: 32-column slices
   }
   w.alpha = reinterpret_cast<float*>(take(n * M * 4));
-  w.rinv = reinterpret_cast<float*>(take(n * M * 4));
+  w.scale = reinterpret_cast<float*>(take(n * M * 4));
   w.bytes = off;
   return w;
 }
@@ -278,14 +278,12 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
   const float* v = nullptr;
   int64_t sv = 0;
   mark(plan, s);
-  const float* part = nullptr;
-  int n_sl = 0;
   if (plan->cfg.act_dtype == ENGRAM_F32) {
     if (engram::gemm_f32_simt(static_cast<const float*>(e), static_cast<const float*>(w->w_kv), ws.kv, ntok,
                               (M + 1) * d, plan->d_mem, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     mark(plan, s);
-    if (engram::launch_gate_f32(plan, ws.kv, static_cast<const float*>(H), ntok, w->g_h, w->g_k, ws.alpha, ws.rinv,
+    if (engram::launch_gate_f32(plan, ws.kv, static_cast<const float*>(H), ntok, w->g_h, w->g_k, ws.alpha, ws.scale,
                                 s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     v = ws.kv;
@@ -294,19 +292,20 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
                                  plan->num_sms, &plan->dev->err, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
-    part = ws.part;
-    n_sl = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
+    mark(plan, s);
+    const int n_sl = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
+    if (engram::launch_finalize(plan, ws.part, n_sl, ntok, ws.alpha, ws.scale, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
     v = ws.v32;
     sv = d;
   }
   mark(plan, s);
-  if (engram::launch_conv_residual(plan, v, sv, part, n_sl, ws.alpha, ws.rinv, B, T, w->g_c, w->conv, H, state,
-                                   s) != cudaSuccess)
+  if (engram::launch_conv_residual(plan, v, sv, ws.alpha, ws.scale, B, T, w->g_c, w->conv, H, state, s) !=
+      cudaSuccess)
     return ENGRAM_ERR_CUDA;
   mark(plan, s);
   if (state) {
-    if (engram::launch_state_update(plan, ids, proj, V, v, sv, ws.alpha, ws.rinv, B, T, w->g_c, state, s) !=
-        cudaSuccess)
+    if (engram::launch_state_update(plan, ids, proj, V, v, sv, ws.scale, B, T, state, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     mark(plan, s);
   }

@@ -69,7 +69,7 @@ struct Workspace {
   float* v32;        // bf16 layers: [ntok, d] v in fp32 (fused K/V epilogue)
   float* part;       // bf16 layers: [ntok, (d/32)(1+3M)] gate partial sums (at most)
   float* alpha;      // [ntok, M]
-  float* rinv;       // [ntok, M]   1/sqrt(mean(v~^2)+eps) of each gated row
+  float* scale;      // [ntok, M]   alpha * 1/sqrt(mean(v~^2)+eps): RMSNorm(v~) = scale * v * g_c
   size_t bytes;
 };
 Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base);
@@ -86,16 +86,17 @@ cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, 
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
                                  cudaStream_t s);
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
-                            const float* g_k, float* alpha, float* rinv, cudaStream_t s);
-// Conv + SiLU + skip + residual over B sequences of T positions.  With `part`
-// (bf16 layers) alpha/rinv are computed from the gate partials (n_sl slices)
-// and written; without it they are read.
-cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* part, int n_sl,
-                                 float* alpha, float* rinv, int B, int T, const float* g_c, const float* conv,
-                                 void* H, const engram_state_t* state, cudaStream_t s);
+                            const float* g_k, float* alpha, float* scale, cudaStream_t s);
+// Gate partials of the fused K/V epilogue (n_sl slices) -> alpha, scale.
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* alpha,
+                            float* scale, cudaStream_t s);
+// Conv + SiLU + skip + residual over B sequences of T positions (v fp32 with row stride sv).
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
+                                 const float* scale, int B, int T, const float* g_c, const float* conv, void* H,
+                                 const engram_state_t* state, cudaStream_t s);
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
-                                int64_t sv, const float* alpha, const float* rinv, int B, int T, const float* g_c,
-                                const engram_state_t* state, cudaStream_t s);
+                                int64_t sv, const float* scale, int B, int T, const engram_state_t* state,
+                                cudaStream_t s);
 
 // bf16 GEMM on tcgen05: C[Mr, Nc] = A[Mr, Kd] . B[Nc, Kd]^T, all row-major bf16.
 cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,

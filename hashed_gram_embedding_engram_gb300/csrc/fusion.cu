@@ -3,31 +3,33 @@
 //   alpha^(m)_t = sigma(RMSNorm(h^(m)_t) . RMSNorm(k^(m)_t) / sqrt(d)),  v~^(m)_t = alpha^(m)_t v_t
 //   Y^(m) = SiLU(Conv1D_{w, dilation}(RMSNorm(V~^(m)))) + V~^(m),       H^(m) <- H^(m) + Y^(m)
 //
-// Since RMSNorm(v~) = (alpha v) * rinv * g_c with rinv = 1/sqrt(alpha^2 mean(v^2) + eps),
-// the convolution needs only the v rows and two scalars per (token, branch).
+// RMSNorm(v~) = s * v * g_c with the per-(token, branch) scale
+//   s = alpha * rinv,  rinv = 1/sqrt(alpha^2 mean(v^2) + eps),
+// so after the gate the convolution needs only the v rows and two scalars
+// (alpha for the skip term, s for the normalised input).
 //
-//   bf16 layers: the K/V GEMM's epilogue (gemm.cu) has reduced every k slice to
-//   partial sums and written v in fp32; conv_tile_kernel turns the partials
-//   into alpha and rinv itself.
-//   fp32 layers: gate_kernel (one warp per token) computes alpha and rinv from
-//   the fp32 [v | k] buffer; conv_tile_kernel reads them.
-//
-//   conv_window_kernel  one block per tile of 16 consecutive positions of one
-//                     sequence: the gate scalars of the tile and its causal
-//                     halo of (w-1)*dilation positions go to shared memory
-//                     (one warp per position), then one thread per 4 channels
-//                     walks the tile with its taps (times g_c) and a sliding
-//                     register window of RMSNorm(v~), so each v row is read
-//                     once; history before a chunk comes from the caller's
-//                     ring; SiLU, skip and H += Y for all M branches.  w = 4
-//                     with dilation 1..8 is compiled per case; other shapes use
+//   finalize_kernel   bf16 layers: one warp per token turns the gate partial
+//                     sums written by the K/V GEMM's epilogue (gemm.cu) into
+//                     alpha and s for every branch.
+//   gate_kernel       fp32 layers: one warp per token computes alpha and s from
+//                     the fp32 [v | k] buffer of the CUDA-core GEMM.
+//   conv_window_kernel  one block per tile of 8 consecutive positions of one
+//                     sequence, one thread per 4 channels: the thread issues
+//                     every load of the tile first -- the v rows of the tile
+//                     and its causal halo of (w-1)*dilation positions (a
+//                     register window with static indices), the ring history
+//                     when the tile starts a chunk, the H values -- then
+//                     convolves with its taps (times g_c) in registers, applies
+//                     SiLU, the skip and H += Y for all M branches.  w = 4 with
+//                     dilation 1..8 is compiled per case; other shapes use
 //                     conv_generic_kernel (the same arithmetic, taps re-read).
-//   state_kernel      after the chunk: writes the last (w-1)*dilation conv
-//                     inputs RMSNorm(v~) (before the weight g_c, which the conv
-//                     folds into its taps) into the ring, rolls the last N-1
-//                     projected ids,
-//                     advances pos (a separate launch: the ring slots it
-//                     writes are slots the conv still reads).
+//   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
+//                     (s * v) of the last (w-1)*dilation positions into the
+//                     ring, rolls the last N-1 projected ids, advances pos (a
+//                     separate launch: the ring slots it writes are slots the
+//                     conv still reads).  The ring values are the same float
+//                     products the conv forms inside a chunk, so streaming a
+//                     sequence reproduces one-shot prefill bit for bit.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -81,11 +83,54 @@ __device__ __forceinline__ float warp_sum(float x) {
 // logistic function; __frcp_rn is the correctly rounded reciprocal (same value as 1.f / x)
 __device__ __forceinline__ float sigmoidf(float x) { return __frcp_rn(1.f + expf(-x)); }
 
+// SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
+// alpha and s from the four sums of one (token, branch)
+__device__ __forceinline__ void gate_scalars(float sv, float dot, float sk, float sh, float inv_d, float inv_sqrt_d,
+                                             float eps, float& alpha, float& scale) {
+  const float rh = 1.f / sqrtf(sh * inv_d + eps);
+  const float rk = 1.f / sqrtf(sk * inv_d + eps);
+  alpha = sigmoidf(dot * rh * rk * inv_sqrt_d);
+  scale = alpha * (1.f / sqrtf(alpha * alpha * (sv * inv_d) + eps));
+}
+
+// ------------------------------------------------------------------ gate (bf16 layers: from partials)
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int n_sl, int64_t ntok, int M,
+                                                       int d, float eps, float* __restrict__ alpha,
+                                                       float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int P = n_sl * (1 + 3 * M);
+  const float inv_d = 1.f / static_cast<float>(d);
+  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
+       tok += n_warps) {
+    const float* p = part + tok * P;
+    float sv = 0.f;
+    for (int j = lane; j < n_sl; j += 32) sv += p[j];
+    sv = warp_sum(sv);
+    for (int m = 0; m < M; ++m) {
+      float dot = 0.f, sk = 0.f, sh = 0.f;
+      for (int j = lane; j < n_sl; j += 32) {
+        const float* q = p + n_sl + (m * n_sl + j) * 3;
+        dot += q[0];
+        sk += q[1];
+        sh += q[2];
+      }
+      dot = warp_sum(dot);
+      sk = warp_sum(sk);
+      sh = warp_sum(sh);
+      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, alpha[tok * M + m], scale[tok * M + m]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ gate (fp32 layers)
 __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv, const float* __restrict__ H,
                                                    int64_t ntok, int M, int d, float eps,
                                                    const float* __restrict__ g_h, const float* __restrict__ g_k,
-                                                   float* __restrict__ alpha, float* __restrict__ rinv) {
+                                                   float* __restrict__ alpha, float* __restrict__ scale) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const float inv_d = 1.f / static_cast<float>(d);
@@ -101,7 +146,6 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
       for (int i = 0; i < 4; ++i) sv = fmaf(v[i], v[i], sv);
     }
     sv = warp_sum(sv);
-    const float ms_v = sv * inv_d;
     for (int m = 0; m < M; ++m) {
       const float* k = row + static_cast<int64_t>(1 + m) * d;
       const float* h = H + (tok * M + m) * static_cast<int64_t>(d);
@@ -124,88 +168,37 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
       sh = warp_sum(sh);
       sk = warp_sum(sk);
       dot = warp_sum(dot);
-      const float rh = 1.f / sqrtf(sh * inv_d + eps);
-      const float rk = 1.f / sqrtf(sk * inv_d + eps);
-      const float a = sigmoidf(dot * rh * rk * inv_sqrt_d);
-      if (lane == 0) {
-        alpha[tok * M + m] = a;
-        rinv[tok * M + m] = 1.f / sqrtf(a * a * ms_v + eps);
-      }
+      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, alpha[tok * M + m], scale[tok * M + m]);
     }
   }
 }
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
 struct ConvArgs {
-  const float* v;        // fp32 v rows, row stride sv
-  int64_t sv;
-  const float* part;     // bf16 layers: gate partials [ntok, n_sl(1+3M)]; else nullptr
-  int n_sl;
-  float* alpha;          // [ntok, M]: written (from partials) or read
-  float* rinv;           // [ntok, M]
+  int64_t sv;            // row stride of v (elements)
+  const float* alpha;    // [ntok, M]
+  const float* scale;    // [ntok, M]  s = alpha * rinv
   int B, Tn, M, d, dil, TT;
-  float eps;
   const float* g_c;      // [d]
   const float* conv;     // [d, W]
-  const float* ring;     // [B, L, M, d] or nullptr
-  const int32_t* pos;    // [B] or nullptr
+  const int32_t* pos;    // [B] (with a ring)
   int L;
 };
 
-// SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
-
-// Gate scalars of positions [t0 - halo, t0 + tn) of sequence b, one warp per
-// position: s = alpha * rinv (the scale that turns v into RMSNorm(v~) before
-// its weight) and alpha.  The block that owns a position records alpha and
-// rinv for the state update.
-__device__ void tile_scalars(const ConvArgs& a, int b, int t0, int tn, int halo, float* s_s, float* s_a) {
+// s and alpha of positions [t0 - halo, t0 + tn) of sequence b into shared memory;
+// history positions before the chunk get s = 1 (the ring holds RMSNorm(v~) itself).
+__device__ __forceinline__ void stage_scalars(const ConvArgs& a, int64_t tok_b, int t0, int tn, int halo, float* s_s,
+                                              float* s_a) {
   const int M = a.M;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  const float inv_d = 1.f / static_cast<float>(a.d);
-  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(a.d));
-  const int P = a.n_sl * (1 + 3 * M);
-  const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-  for (int pi = warp; pi < tn + halo; pi += n_warps) {
-    const int tl = t0 - halo + pi;
-    if (tl < 0) {                       // history before the chunk: values used as they are
-      if (lane < M) s_s[pi * M + lane] = 1.f;
-      continue;
-    }
-    const int64_t tok = tok_b + tl;
-    if (a.part != nullptr) {
-      const float* p = a.part + tok * P;
-      float sv = 0.f;
-      for (int j = lane; j < a.n_sl; j += 32) sv += p[j];
-      sv = warp_sum(sv);
-      for (int m = 0; m < M; ++m) {
-        float dot = 0.f, sk = 0.f, sh = 0.f;
-        for (int j = lane; j < a.n_sl; j += 32) {
-          const float* q = p + a.n_sl + (m * a.n_sl + j) * 3;
-          dot += q[0];
-          sk += q[1];
-          sh += q[2];
-        }
-        dot = warp_sum(dot);
-        sk = warp_sum(sk);
-        sh = warp_sum(sh);
-        if (lane == 0) {
-          const float rh = 1.f / sqrtf(sh * inv_d + a.eps);
-          const float rk = 1.f / sqrtf(sk * inv_d + a.eps);
-          const float al = sigmoidf(dot * rh * rk * inv_sqrt_d);
-          const float ri = 1.f / sqrtf(al * al * (sv * inv_d) + a.eps);
-          s_s[pi * M + m] = al * ri;
-          s_a[pi * M + m] = al;
-          if (tl >= t0) {
-            a.alpha[tok * M + m] = al;
-            a.rinv[tok * M + m] = ri;
-          }
-        }
-      }
-    } else if (lane < M) {
-      const float al = a.alpha[tok * M + lane], ri = a.rinv[tok * M + lane];
-      s_s[pi * M + lane] = al * ri;
-      s_a[pi * M + lane] = al;
+  for (int i = threadIdx.x; i < (tn + halo) * M; i += blockDim.x) {
+    const int tl = t0 - halo + i / M;
+    if (tl < 0) {
+      s_s[i] = 1.f;
+      s_a[i] = 0.f;
+    } else {
+      const int64_t q = (tok_b + tl) * M + (i - (i / M) * M);
+      s_s[i] = __ldg(a.scale + q);
+      s_a[i] = __ldg(a.alpha + q);
     }
   }
 }
@@ -228,14 +221,6 @@ __device__ __forceinline__ void load_taps(const ConvArgs& a, int c, float (&wq)[
   }
 }
 
-// One block per tile of TT positions of one sequence, all channels; one
-// thread per 4 channels.  Each thread first issues every load it needs for
-// the tile -- the v rows of the tile and its causal halo (a register window,
-// static indices after unrolling), the H values, the ring history when the
-// tile starts a chunk -- and only then computes and stores, so the loads of
-// all positions are in flight together (v, ring and H are restrict-qualified
-// kernel arguments: the stores cannot alias the loads).  W, DIL and TT are
-// compile-time.
 template <typename TH, int W, int DIL, int TT>
 __global__ void __launch_bounds__(256, 1)
     conv_window_kernel(const ConvArgs a, const float* __restrict__ v, const float* __restrict__ ring,
@@ -251,7 +236,7 @@ __global__ void __launch_bounds__(256, 1)
     const int t0 = (tile - b * tiles_per_seq) * TT;
     const int tn = min(TT, a.Tn - t0);
     const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-    tile_scalars(a, b, t0, tn, HALO, s_s, s_a);
+    stage_scalars(a, tok_b, t0, tn, HALO, s_s, s_a);
     __syncthreads();
     const int p0 = ring != nullptr ? a.pos[b] : 0;
     for (int g = threadIdx.x; g < groups; g += blockDim.x) {
@@ -272,8 +257,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       for (int m = 0; m < M; ++m) {
-        // positions before the chunk: the ring holds RMSNorm(v~) itself, and
-        // their scale in shared memory is 1 (x * 1 is exact)
+        // positions before the chunk: RMSNorm(v~) straight from the ring (scale 1)
         if (t0 < HALO) {
 #pragma unroll
           for (int k = 0; k < HALO; ++k) {
@@ -316,10 +300,11 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-// Any (W, dilation): the same arithmetic with the v rows of every tap read
-// for every position (L1/L2 serve the repeats).
+// Any (W, dilation): the same arithmetic with the v rows of every tap read for
+// every position (L1/L2 serve the repeats).
 template <typename TH, int W>
-__global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, TH* __restrict__ H) {
+__global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, const float* __restrict__ v,
+                                                           const float* __restrict__ ring, TH* __restrict__ H) {
   extern __shared__ float s_sc[];                  // [2][(TT + halo) * M]
   const int halo = (W - 1) * a.dil;
   float* s_s = s_sc;
@@ -332,16 +317,16 @@ __global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, TH*
     const int t0 = (tile - b * tiles_per_seq) * a.TT;
     const int tn = min(a.TT, a.Tn - t0);
     const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-    tile_scalars(a, b, t0, tn, halo, s_s, s_a);
+    stage_scalars(a, tok_b, t0, tn, halo, s_s, s_a);
     __syncthreads();
-    const int p0 = a.ring ? a.pos[b] : 0;
+    const int p0 = ring != nullptr ? a.pos[b] : 0;
     for (int g = threadIdx.x; g < groups; g += blockDim.x) {
       const int c = 4 * g;
       float wq[4][W];
       load_taps<W>(a, c, wq);
       for (int ti = 0; ti < tn; ++ti) {
         const int t = t0 + ti;
-        const float* vp = a.v + (tok_b + t) * a.sv + c;
+        const float* vp = v + (tok_b + t) * a.sv + c;
         float v0[4];
         ld4(vp, v0);
         for (int m = 0; m < M; ++m) {
@@ -349,21 +334,18 @@ __global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, TH*
 #pragma unroll
           for (int j = 0; j < W; ++j) {
             const int lag = (W - 1 - j) * a.dil;
+            const float sj = s_s[(ti + halo - lag) * M + m];
             float u[4];
             if (t - lag >= 0) {
-              float v[4];
-              ld4(vp - static_cast<int64_t>(lag) * a.sv, v);
-              const float sj = s_s[(ti + halo - lag) * M + m];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[i] = sj * v[i];
-            } else if (a.ring != nullptr && p0 + t - lag >= 0) {
-              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
+              ld4(vp - static_cast<int64_t>(lag) * a.sv, u);
+            } else if (ring != nullptr && p0 + t - lag >= 0) {
+              ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
             } else {
 #pragma unroll
               for (int i = 0; i < 4; ++i) u[i] = 0.f;
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * u[i], acc[i]);
           }
           const float at = s_a[(ti + halo) * M + m];
           TH* hp = H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c;
@@ -381,8 +363,7 @@ __global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, TH*
 
 // ------------------------------------------------------------------ streaming state
 __global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_base, int64_t sv,
-                                                    const float* __restrict__ alpha, const float* __restrict__ rinv,
-                                                    int Tn, int M, int d, const float* __restrict__ g_c,
+                                                    const float* __restrict__ scale, int Tn, int M, int d,
                                                     float* __restrict__ ring, int32_t* __restrict__ pos, int L,
                                                     const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ proj, int V,
@@ -400,7 +381,7 @@ __global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_
     const int c = g * 4;
     float v[4];
     ld4(v_base + tok * sv + c, v);
-    const float sc = alpha[tok * M + m] * rinv[tok * M + m];
+    const float sc = scale[tok * M + m];
     float* dst = ring + ((static_cast<int64_t>(b) * L + (p0 + t) % L) * M + m) * d + c;
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = sc * v[i];
@@ -441,92 +422,99 @@ int grid_for(int64_t items, int threads, int num_sms) {
 constexpr int kWindowTT = 8;
 
 template <typename TH, int W, int DIL>
-cudaError_t conv_window_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
+cudaError_t conv_window_launch(const engram_plan* p, ConvArgs a, const float* v, const float* ring, void* H,
+                               cudaStream_t s) {
   a.TT = kWindowTT;
   const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + kWindowTT - 1) / kWindowTT);
   const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
   conv_window_kernel<TH, W, DIL, kWindowTT><<<static_cast<int>(tiles < cap ? tiles : cap), 256, 0, s>>>(
-      a, a.v, a.ring, static_cast<TH*>(H));
+      a, v, ring, static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
 template <typename TH, int W>
-cudaError_t conv_generic_launch(const engram_plan* p, ConvArgs a, void* H, cudaStream_t s) {
+cudaError_t conv_generic_launch(const engram_plan* p, ConvArgs a, const float* v, const float* ring, void* H,
+                                cudaStream_t s) {
   a.TT = std::min(16, a.Tn);
   const size_t smem = 2 * static_cast<size_t>(a.TT + (W - 1) * a.dil) * a.M * sizeof(float);
   const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT);
   const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
-  conv_generic_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(a, static_cast<TH*>(H));
+  conv_generic_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(a, v, ring,
+                                                                                          static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
 template <typename TH>
-cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, void* H, cudaStream_t s) {
+cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, const float* v, const float* ring, void* H,
+                          cudaStream_t s) {
   if (p->cfg.conv_w == 4) {
     switch (a.dil) {   // the pages' short conv: w = 4, dilation = max n-gram order
-      case 1: return conv_window_launch<TH, 4, 1>(p, a, H, s);
-      case 2: return conv_window_launch<TH, 4, 2>(p, a, H, s);
-      case 3: return conv_window_launch<TH, 4, 3>(p, a, H, s);
-      case 4: return conv_window_launch<TH, 4, 4>(p, a, H, s);
-      case 5: return conv_window_launch<TH, 4, 5>(p, a, H, s);
-      case 6: return conv_window_launch<TH, 4, 6>(p, a, H, s);
-      case 7: return conv_window_launch<TH, 4, 7>(p, a, H, s);
-      case 8: return conv_window_launch<TH, 4, 8>(p, a, H, s);
+      case 1: return conv_window_launch<TH, 4, 1>(p, a, v, ring, H, s);
+      case 2: return conv_window_launch<TH, 4, 2>(p, a, v, ring, H, s);
+      case 3: return conv_window_launch<TH, 4, 3>(p, a, v, ring, H, s);
+      case 4: return conv_window_launch<TH, 4, 4>(p, a, v, ring, H, s);
+      case 5: return conv_window_launch<TH, 4, 5>(p, a, v, ring, H, s);
+      case 6: return conv_window_launch<TH, 4, 6>(p, a, v, ring, H, s);
+      case 7: return conv_window_launch<TH, 4, 7>(p, a, v, ring, H, s);
+      case 8: return conv_window_launch<TH, 4, 8>(p, a, v, ring, H, s);
       default: break;
     }
   }
   switch (p->cfg.conv_w) {
-    case 1: return conv_generic_launch<TH, 1>(p, a, H, s);
-    case 2: return conv_generic_launch<TH, 2>(p, a, H, s);
-    case 3: return conv_generic_launch<TH, 3>(p, a, H, s);
-    case 4: return conv_generic_launch<TH, 4>(p, a, H, s);
-    case 5: return conv_generic_launch<TH, 5>(p, a, H, s);
-    case 6: return conv_generic_launch<TH, 6>(p, a, H, s);
-    case 7: return conv_generic_launch<TH, 7>(p, a, H, s);
-    case 8: return conv_generic_launch<TH, 8>(p, a, H, s);
+    case 1: return conv_generic_launch<TH, 1>(p, a, v, ring, H, s);
+    case 2: return conv_generic_launch<TH, 2>(p, a, v, ring, H, s);
+    case 3: return conv_generic_launch<TH, 3>(p, a, v, ring, H, s);
+    case 4: return conv_generic_launch<TH, 4>(p, a, v, ring, H, s);
+    case 5: return conv_generic_launch<TH, 5>(p, a, v, ring, H, s);
+    case 6: return conv_generic_launch<TH, 6>(p, a, v, ring, H, s);
+    case 7: return conv_generic_launch<TH, 7>(p, a, v, ring, H, s);
+    case 8: return conv_generic_launch<TH, 8>(p, a, v, ring, H, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
-                            const float* g_k, float* alpha, float* rinv, cudaStream_t s) {
-  gate_kernel<<<grid_for(ntok * 32, 256, p->num_sms), 256, 0, s>>>(kv, H, ntok, p->cfg.M, p->cfg.d, p->cfg.eps, g_h,
-                                                                   g_k, alpha, rinv);
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* alpha,
+                            float* scale, cudaStream_t s) {
+  finalize_kernel<<<grid_for(ntok * 32, 256, p->num_sms), 256, 0, s>>>(part, n_sl, ntok, p->cfg.M, p->cfg.d,
+                                                                       p->cfg.eps, alpha, scale);
   return cudaGetLastError();
 }
 
-cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* part, int n_sl,
-                                 float* alpha, float* rinv, int B, int T, const float* g_c, const float* conv,
-                                 void* H, const engram_state_t* state, cudaStream_t s) {
+cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
+                            const float* g_k, float* alpha, float* scale, cudaStream_t s) {
+  gate_kernel<<<grid_for(ntok * 32, 256, p->num_sms), 256, 0, s>>>(kv, H, ntok, p->cfg.M, p->cfg.d, p->cfg.eps, g_h,
+                                                                   g_k, alpha, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
+                                 const float* scale, int B, int T, const float* g_c, const float* conv, void* H,
+                                 const engram_state_t* state, cudaStream_t s) {
   ConvArgs a{};
-  a.v = v;
   a.sv = sv;
-  a.part = part;
-  a.n_sl = n_sl;
   a.alpha = alpha;
-  a.rinv = rinv;
+  a.scale = scale;
   a.B = B;
   a.Tn = T;
   a.M = p->cfg.M;
   a.d = p->cfg.d;
   a.dil = p->cfg.conv_dilation;
-  a.eps = p->cfg.eps;
   a.g_c = g_c;
   a.conv = conv;
-  a.ring = state ? state->u_ring : nullptr;
   a.pos = state ? state->pos : nullptr;
   a.L = p->L_ring;
-  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, H, s);
-  return conv_dispatch<__nv_bfloat16>(p, a, H, s);
+  const float* ring = state ? state->u_ring : nullptr;
+  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, v, ring, H, s);
+  return conv_dispatch<__nv_bfloat16>(p, a, v, ring, H, s);
 }
 
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
-                                int64_t sv, const float* alpha, const float* rinv, int B, int T, const float* g_c,
-                                const engram_state_t* st, cudaStream_t s) {
-  state_kernel<<<B, 256, 0, s>>>(v, sv, alpha, rinv, T, p->cfg.M, p->cfg.d, g_c, st->u_ring, st->pos, p->L_ring, ids,
-                                 proj, V, st->prev_ids, p->cfg.N, &p->dev->err);
+                                int64_t sv, const float* scale, int B, int T, const engram_state_t* st,
+                                cudaStream_t s) {
+  state_kernel<<<B, 256, 0, s>>>(v, sv, scale, T, p->cfg.M, p->cfg.d, st->u_ring, st->pos, p->L_ring, ids, proj, V,
+                                 st->prev_ids, p->cfg.N, &p->dev->err);
   return cudaGetLastError();
 }
 

@@ -189,9 +189,9 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
 /* Tracing.  With timing on, engram_forward / engram_stage_b record one of
  * the plan's CUDA events on `stream` before the first kernel and after every
  * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps
- * 1-4 in one kernel), K/V projection with the gate reductions, conv +
- * residual with the gate; on F32 layers: hash + gather, K/V projection, gate,
- * conv + residual; then the state update when a state is given.
+ * 1-4 in one kernel), K/V projection with the gate reductions, gate
+ * (finalize), conv + residual; on F32 layers: hash + gather, K/V projection,
+ * gate, conv + residual; then the state update when a state is given.
  * engram_stage_b records the same list without the first kernel.  For use on
  * one stream at a time, outside CUDA-graph capture.  enable: 0 or 1. */
 engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable);
