@@ -13,16 +13,12 @@
 //                     alpha and s for every branch.
 //   gate_kernel       fp32 layers: one warp per token computes alpha and s from
 //                     the fp32 [v | k] buffer of the CUDA-core GEMM.
-//   conv_window_kernel  one block per tile of 8 consecutive positions of one
-//                     sequence, one thread per 4 channels: the thread issues
-//                     every load of the tile first -- the v rows of the tile
-//                     and its causal halo of (w-1)*dilation positions (a
-//                     register window with static indices), the ring history
-//                     when the tile starts a chunk, the H values -- then
-//                     convolves with its taps (times g_c) in registers, applies
-//                     SiLU, the skip and H += Y for all M branches.  w = 4 with
-//                     dilation 1..8 is compiled per case; other shapes use
-//                     conv_generic_kernel (the same arithmetic, taps re-read).
+//   conv_kernel       one thread per (token, 4 channels): the v rows of the W
+//                     taps (the rows a token shares with its neighbours come
+//                     from L1/L2), the ring history before a chunk, the
+//                     scalars and H are all loaded together; taps (times g_c)
+//                     in registers; SiLU, the skip and H += Y for all M
+//                     branches.
 //   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
 //                     (s * v) of the last (w-1)*dilation positions into the
 //                     ring, rolls the last N-1 projected ids, advances pos (a
@@ -32,8 +28,6 @@
 //                     sequence reproduces one-shot prefill bit for bit.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-
-#include <algorithm>
 
 #include "engram_internal.h"
 
@@ -178,30 +172,12 @@ struct ConvArgs {
   int64_t sv;            // row stride of v (elements)
   const float* alpha;    // [ntok, M]
   const float* scale;    // [ntok, M]  s = alpha * rinv
-  int B, Tn, M, d, dil, TT;
+  int B, Tn, M, d, dil;
   const float* g_c;      // [d]
   const float* conv;     // [d, W]
   const int32_t* pos;    // [B] (with a ring)
   int L;
 };
-
-// s and alpha of positions [t0 - halo, t0 + tn) of sequence b into shared memory;
-// history positions before the chunk get s = 1 (the ring holds RMSNorm(v~) itself).
-__device__ __forceinline__ void stage_scalars(const ConvArgs& a, int64_t tok_b, int t0, int tn, int halo, float* s_s,
-                                              float* s_a) {
-  const int M = a.M;
-  for (int i = threadIdx.x; i < (tn + halo) * M; i += blockDim.x) {
-    const int tl = t0 - halo + i / M;
-    if (tl < 0) {
-      s_s[i] = 1.f;
-      s_a[i] = 0.f;
-    } else {
-      const int64_t q = (tok_b + tl) * M + (i - (i / M) * M);
-      s_s[i] = __ldg(a.scale + q);
-      s_a[i] = __ldg(a.alpha + q);
-    }
-  }
-}
 
 // Taps of channels c..c+3 times the conv-input RMSNorm weight g_c.
 template <int W>
@@ -221,143 +197,58 @@ __device__ __forceinline__ void load_taps(const ConvArgs& a, int c, float (&wq)[
   }
 }
 
-template <typename TH, int W, int DIL, int TT>
-__global__ void __launch_bounds__(256, 1)
-    conv_window_kernel(const ConvArgs a, const float* __restrict__ v, const float* __restrict__ ring,
-                       TH* __restrict__ H) {
-  constexpr int HALO = (W - 1) * DIL;
-  __shared__ float s_s[(TT + HALO) * kMaxM];
-  __shared__ float s_a[(TT + HALO) * kMaxM];
-  const int M = a.M, d = a.d, groups = d / 4;
-  const int tiles_per_seq = (a.Tn + TT - 1) / TT;
-  const int n_tiles = a.B * tiles_per_seq;
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int b = tile / tiles_per_seq;
-    const int t0 = (tile - b * tiles_per_seq) * TT;
-    const int tn = min(TT, a.Tn - t0);
-    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-    stage_scalars(a, tok_b, t0, tn, HALO, s_s, s_a);
-    __syncthreads();
-    const int p0 = ring != nullptr ? a.pos[b] : 0;
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-      const int c = 4 * g;
-      float wq[4][W];
-      load_taps<W>(a, c, wq);
-      // v rows of positions t0 - HALO .. t0 + TT - 1 (zero outside the chunk)
-      const float* vrow = v + (tok_b + t0) * a.sv + c;
-      float vw[HALO + TT][4];
-#pragma unroll
-      for (int k = 0; k < HALO + TT; ++k) {
-        const int tl = t0 - HALO + k;
-        if (tl >= 0 && k - HALO < tn) {
-          ld4(vrow + static_cast<int64_t>(k - HALO) * a.sv, vw[k]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) vw[k][i] = 0.f;
-        }
-      }
-      for (int m = 0; m < M; ++m) {
-        // positions before the chunk: RMSNorm(v~) straight from the ring (scale 1)
-        if (t0 < HALO) {
-#pragma unroll
-          for (int k = 0; k < HALO; ++k) {
-            const int tl = t0 - HALO + k;
-            if (tl < 0) {
-              if (ring != nullptr && p0 + tl >= 0) {
-                ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + tl) % a.L) * M + m) * d + c, vw[k]);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) vw[k][i] = 0.f;
-              }
-            }
-          }
-        }
-        float hv[TT][4];
-        TH* hp = H + ((tok_b + t0) * M + m) * static_cast<int64_t>(d) + c;
-#pragma unroll
-        for (int ti = 0; ti < TT; ++ti)
-          if (ti < tn) H4<TH>::load(hp + static_cast<int64_t>(ti) * M * d, hv[ti]);
-#pragma unroll
-        for (int ti = 0; ti < TT; ++ti) {
-          if (ti < tn) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < W; ++j) {
-              const int k = ti + HALO - (W - 1 - j) * DIL;   // window index of the tap's position
-              const float sk = s_s[k * M + m];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sk * vw[k][i], acc[i]);
-            }
-            const float at = s_a[(ti + HALO) * M + m];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) hv[ti][i] += silu_fast(acc[i]) + at * vw[ti + HALO][i];
-            H4<TH>::store(hp + static_cast<int64_t>(ti) * M * d, hv[ti]);
-          }
-        }
-      }
-    }
-    __syncthreads();                                // shared scalars are reused by the next tile
-  }
-}
-
-// Any (W, dilation): the same arithmetic with the v rows of every tap read for
-// every position (L1/L2 serve the repeats).
+// One thread per (token, 4 channels): grid x = token, grid y = block of 256
+// channel groups.  Every load a thread needs (the v rows of its W taps, the
+// ring history before a chunk, the scalars of the tap positions, H) is
+// independent of the others and issued together; the v rows a token shares
+// with its neighbours' taps come from L1/L2.  No loop over positions, no
+// barrier, few registers: many tokens are in flight per SM.
 template <typename TH, int W>
-__global__ void __launch_bounds__(256) conv_generic_kernel(const ConvArgs a, const float* __restrict__ v,
-                                                           const float* __restrict__ ring, TH* __restrict__ H) {
-  extern __shared__ float s_sc[];                  // [2][(TT + halo) * M]
-  const int halo = (W - 1) * a.dil;
-  float* s_s = s_sc;
-  float* s_a = s_sc + (a.TT + halo) * a.M;
-  const int M = a.M, d = a.d, groups = d / 4;
-  const int tiles_per_seq = (a.Tn + a.TT - 1) / a.TT;
-  const int n_tiles = a.B * tiles_per_seq;
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-    const int b = tile / tiles_per_seq;
-    const int t0 = (tile - b * tiles_per_seq) * a.TT;
-    const int tn = min(a.TT, a.Tn - t0);
-    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-    stage_scalars(a, tok_b, t0, tn, halo, s_s, s_a);
-    __syncthreads();
-    const int p0 = ring != nullptr ? a.pos[b] : 0;
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-      const int c = 4 * g;
-      float wq[4][W];
-      load_taps<W>(a, c, wq);
-      for (int ti = 0; ti < tn; ++ti) {
-        const int t = t0 + ti;
-        const float* vp = v + (tok_b + t) * a.sv + c;
-        float v0[4];
-        ld4(vp, v0);
-        for (int m = 0; m < M; ++m) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+__global__ void __launch_bounds__(256) conv_kernel(const ConvArgs a, const float* __restrict__ v,
+                                                   const float* __restrict__ ring, TH* __restrict__ H) {
+  const int g = blockIdx.y * blockDim.x + threadIdx.x;
+  if (g >= a.d / 4) return;
+  const int64_t tok = blockIdx.x;
+  const int b = static_cast<int>(static_cast<uint32_t>(blockIdx.x) / static_cast<uint32_t>(a.Tn));
+  const int t = static_cast<int>(blockIdx.x) - b * a.Tn;
+  const int M = a.M, d = a.d, c = 4 * g;
+  float wq[4][W];
+  load_taps<W>(a, c, wq);
+  float vt[W][4];                                   // v rows of the tap positions in the chunk
 #pragma unroll
-          for (int j = 0; j < W; ++j) {
-            const int lag = (W - 1 - j) * a.dil;
-            const float sj = s_s[(ti + halo - lag) * M + m];
-            float u[4];
-            if (t - lag >= 0) {
-              ld4(vp - static_cast<int64_t>(lag) * a.sv, u);
-            } else if (ring != nullptr && p0 + t - lag >= 0) {
-              ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
-            } else {
+  for (int j = 0; j < W; ++j) {
+    const int lag = (W - 1 - j) * a.dil;
+    if (t - lag >= 0) {
+      ld4(v + (tok - lag) * a.sv + c, vt[j]);
+    } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) u[i] = 0.f;
-            }
+      for (int i = 0; i < 4; ++i) vt[j][i] = 0.f;
+    }
+  }
+  const int p0 = ring != nullptr ? a.pos[b] : 0;
+  for (int m = 0; m < M; ++m) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * u[i], acc[i]);
-          }
-          const float at = s_a[(ti + halo) * M + m];
-          TH* hp = H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c;
-          float h[4];
-          H4<TH>::load(hp, h);
+    for (int j = 0; j < W; ++j) {
+      const int lag = (W - 1 - j) * a.dil;
+      if (t - lag >= 0) {
+        const float sj = __ldg(a.scale + (tok - lag) * M + m);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * v0[i];
-          H4<TH>::store(hp, h);
-        }
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
+      } else if (ring != nullptr && p0 + t - lag >= 0) {
+        float u[4];                                 // the ring holds RMSNorm(v~) before its weight
+        ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
       }
     }
-    __syncthreads();
+    const float at = __ldg(a.alpha + tok * M + m);
+    TH* hp = H + (tok * M + m) * static_cast<int64_t>(d) + c;
+    float h[4];
+    H4<TH>::load(hp, h);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
+    H4<TH>::store(hp, h);
   }
 }
 
@@ -419,56 +310,26 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-constexpr int kWindowTT = 8;
-
-template <typename TH, int W, int DIL>
-cudaError_t conv_window_launch(const engram_plan* p, ConvArgs a, const float* v, const float* ring, void* H,
-                               cudaStream_t s) {
-  a.TT = kWindowTT;
-  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + kWindowTT - 1) / kWindowTT);
-  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
-  conv_window_kernel<TH, W, DIL, kWindowTT><<<static_cast<int>(tiles < cap ? tiles : cap), 256, 0, s>>>(
-      a, v, ring, static_cast<TH*>(H));
-  return cudaGetLastError();
-}
-
 template <typename TH, int W>
-cudaError_t conv_generic_launch(const engram_plan* p, ConvArgs a, const float* v, const float* ring, void* H,
-                                cudaStream_t s) {
-  a.TT = std::min(16, a.Tn);
-  const size_t smem = 2 * static_cast<size_t>(a.TT + (W - 1) * a.dil) * a.M * sizeof(float);
-  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT);
-  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
-  conv_generic_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(a, v, ring,
-                                                                                          static_cast<TH*>(H));
+cudaError_t conv_launch(const ConvArgs& a, const float* v, const float* ring, void* H, cudaStream_t s) {
+  const int groups = a.d / 4;
+  const dim3 grid(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Tn), (groups + 255) / 256);
+  conv_kernel<TH, W><<<grid, 256, 0, s>>>(a, v, ring, static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
 template <typename TH>
 cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, const float* v, const float* ring, void* H,
                           cudaStream_t s) {
-  if (p->cfg.conv_w == 4) {
-    switch (a.dil) {   // the pages' short conv: w = 4, dilation = max n-gram order
-      case 1: return conv_window_launch<TH, 4, 1>(p, a, v, ring, H, s);
-      case 2: return conv_window_launch<TH, 4, 2>(p, a, v, ring, H, s);
-      case 3: return conv_window_launch<TH, 4, 3>(p, a, v, ring, H, s);
-      case 4: return conv_window_launch<TH, 4, 4>(p, a, v, ring, H, s);
-      case 5: return conv_window_launch<TH, 4, 5>(p, a, v, ring, H, s);
-      case 6: return conv_window_launch<TH, 4, 6>(p, a, v, ring, H, s);
-      case 7: return conv_window_launch<TH, 4, 7>(p, a, v, ring, H, s);
-      case 8: return conv_window_launch<TH, 4, 8>(p, a, v, ring, H, s);
-      default: break;
-    }
-  }
   switch (p->cfg.conv_w) {
-    case 1: return conv_generic_launch<TH, 1>(p, a, v, ring, H, s);
-    case 2: return conv_generic_launch<TH, 2>(p, a, v, ring, H, s);
-    case 3: return conv_generic_launch<TH, 3>(p, a, v, ring, H, s);
-    case 4: return conv_generic_launch<TH, 4>(p, a, v, ring, H, s);
-    case 5: return conv_generic_launch<TH, 5>(p, a, v, ring, H, s);
-    case 6: return conv_generic_launch<TH, 6>(p, a, v, ring, H, s);
-    case 7: return conv_generic_launch<TH, 7>(p, a, v, ring, H, s);
-    case 8: return conv_generic_launch<TH, 8>(p, a, v, ring, H, s);
+    case 1: return conv_launch<TH, 1>(a, v, ring, H, s);
+    case 2: return conv_launch<TH, 2>(a, v, ring, H, s);
+    case 3: return conv_launch<TH, 3>(a, v, ring, H, s);
+    case 4: return conv_launch<TH, 4>(a, v, ring, H, s);
+    case 5: return conv_launch<TH, 5>(a, v, ring, H, s);
+    case 6: return conv_launch<TH, 6>(a, v, ring, H, s);
+    case 7: return conv_launch<TH, 7>(a, v, ring, H, s);
+    case 8: return conv_launch<TH, 8>(a, v, ring, H, s);
     default: return cudaErrorInvalidValue;
   }
 }
