@@ -18,7 +18,8 @@ F32, BF16, I8_ROWSCALE_F16 = 0, 1, 2
 
 EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes",
            "engram_hash", "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward",
-           "engram_get_error", "engram_plan_set_timing", "engram_plan_kernel_times")
+           "engram_get_error", "engram_plan_set_timing", "engram_plan_kernel_times",
+           "engram_forward_static_scratch")
 
 
 class Config(ctypes.Structure):
@@ -70,6 +71,8 @@ def _lib() -> ctypes.CDLL:
         lib.engram_forward.argtypes = [vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
                                        ctypes.POINTER(State), vp, sz, vp]
         lib.engram_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.engram_forward_static_scratch.argtypes = [vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
+                                                      ctypes.POINTER(State), vp]
         lib.engram_plan_set_timing.argtypes = [vp, i32]
         lib.engram_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
         for name in EXPORTS:

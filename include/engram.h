@@ -186,6 +186,28 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
                                void* H, engram_state_t* state,
                                void* workspace, size_t workspace_bytes, engram_stream_t stream);
 
+/* engram_forward without a workspace argument.  No page describes this: it
+ * exists for callers that cannot allocate device memory -- a host framework
+ * that owns the device allocator and exposes none of it, a plugin host that
+ * accepts only plain calls, a latency-critical path where cudaMalloc (which
+ * may synchronise the device) is not allowed.  The scratch lives in a
+ * file-scope __device__ array of 32 MiB inside the library image: every GPU
+ * that loads the library holds it until the process exits, and this call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call).
+ * Limit: engram_plan_workspace_bytes(plan, B*T) must not exceed 32 MiB (about
+ * 4900 tokens of a d = 1024, d_mem = 1024 layer); larger calls return
+ * ENGRAM_ERR_WORKSPACE before any launch.  The current device must be the
+ * plan's.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  All calls in the process share the one array and it keeps
+ * the last call's contents (nothing in it needs to start at zero: the forward
+ * writes every scratch byte before reading it), so calls that overlap on the
+ * GPU -- on different streams, or from different threads -- race; serialise
+ * them.  Other arguments and behaviour as in engram_forward. */
+engram_status_t engram_forward_static_scratch(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                                              const int32_t* proj, int V, const engram_weights_t* w,
+                                              void* H, engram_state_t* state, engram_stream_t stream);
+
 /* Tracing.  With timing on, engram_forward / engram_stage_b record one of
  * the plan's CUDA events on `stream` before the first kernel and after every
  * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps
