@@ -109,8 +109,7 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
     w.v32 = reinterpret_cast<float*>(take(n * d * 4));
     w.part = reinterpret_cast<float*>(take(n * (d / 32) * (1 + 3 * M) * 4));   // widest case: 32-column slices
   }
-  w.alpha = reinterpret_cast<float*>(take(n * M * 4));
-  w.scale = reinterpret_cast<float*>(take(n * M * 4));
+  w.sa = reinterpret_cast<float*>(take(n * engram::sa_row_floats(static_cast<int>(M)) * 4));
   w.bytes = off;
   return w;
 }
@@ -283,8 +282,8 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
                               (M + 1) * d, plan->d_mem, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     mark(plan, s);
-    if (engram::launch_gate_f32(plan, ws.kv, static_cast<const float*>(H), ntok, w->g_h, w->g_k, ws.alpha, ws.scale,
-                                s) != cudaSuccess)
+    if (engram::launch_gate_f32(plan, ws.kv, static_cast<const float*>(H), ntok, w->g_h, w->g_k, ws.sa, s) !=
+        cudaSuccess)
       return ENGRAM_ERR_CUDA;
     v = ws.kv;
     sv = static_cast<int64_t>(M + 1) * d;
@@ -294,18 +293,18 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
       return ENGRAM_ERR_CUDA;
     mark(plan, s);
     const int n_sl = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
-    if (engram::launch_finalize(plan, ws.part, n_sl, ntok, ws.alpha, ws.scale, s) != cudaSuccess)
+    if (engram::launch_finalize(plan, ws.part, n_sl, ntok, ws.sa, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     v = ws.v32;
     sv = d;
   }
   mark(plan, s);
-  if (engram::launch_conv_residual(plan, v, sv, ws.alpha, ws.scale, B, T, w->g_c, w->conv, H, state, s) !=
+  if (engram::launch_conv_residual(plan, v, sv, ws.sa, B, T, w->g_c, w->conv, H, state, s) !=
       cudaSuccess)
     return ENGRAM_ERR_CUDA;
   mark(plan, s);
   if (state) {
-    if (engram::launch_state_update(plan, ids, proj, V, v, sv, ws.scale, B, T, state, s) != cudaSuccess)
+    if (engram::launch_state_update(plan, ids, proj, V, v, sv, ws.sa, B, T, state, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     mark(plan, s);
   }

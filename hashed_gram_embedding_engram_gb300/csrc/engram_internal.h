@@ -68,8 +68,7 @@ struct Workspace {
   float* kv;         // f32 layers: [ntok, (M+1)d] = [v | k^(1..M)]
   float* v32;        // bf16 layers: [ntok, d] v in fp32 (fused K/V epilogue)
   float* part;       // bf16 layers: [ntok, (d/32)(1+3M)] gate partial sums (at most)
-  float* alpha;      // [ntok, M]
-  float* scale;      // [ntok, M]   alpha * 1/sqrt(mean(v~^2)+eps): RMSNorm(v~) = scale * v * g_c
+  float* sa;         // [ntok, sa_row_floats(M)]: s^(1..M) = alpha/sqrt(mean(v~^2)+eps), then alpha^(1..M)
   size_t bytes;
 };
 Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base);
@@ -85,17 +84,19 @@ cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, 
                                cudaStream_t s);
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
                                  cudaStream_t s);
+// Floats per row of the per-token gate scalars: [s^(1..M), alpha^(1..M)] padded to 16 bytes.
+int sa_row_floats(int M);
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
-                            const float* g_k, float* alpha, float* scale, cudaStream_t s);
-// Gate partials of the fused K/V epilogue (n_sl slices) -> alpha, scale.
-cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* alpha,
-                            float* scale, cudaStream_t s);
+                            const float* g_k, float* sa, cudaStream_t s);
+// Gate partials of the fused K/V epilogue (n_sl slices) -> sa rows.
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* sa,
+                            cudaStream_t s);
 // Conv + SiLU + skip + residual over B sequences of T positions (v fp32 with row stride sv).
-cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
-                                 const float* scale, int B, int T, const float* g_c, const float* conv, void* H,
-                                 const engram_state_t* state, cudaStream_t s);
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
+                                 const float* g_c, const float* conv, void* H, const engram_state_t* state,
+                                 cudaStream_t s);
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
-                                int64_t sv, const float* scale, int B, int T, const engram_state_t* state,
+                                int64_t sv, const float* sa, int B, int T, const engram_state_t* state,
                                 cudaStream_t s);
 
 // bf16 GEMM on tcgen05: C[Mr, Nc] = A[Mr, Kd] . B[Nc, Kd]^T, all row-major bf16.

@@ -6,19 +6,24 @@
 // RMSNorm(v~) = s * v * g_c with the per-(token, branch) scale
 //   s = alpha * rinv,  rinv = 1/sqrt(alpha^2 mean(v^2) + eps),
 // so after the gate the convolution needs only the v rows and two scalars
-// (alpha for the skip term, s for the normalised input).
+// (alpha for the skip term, s for the normalised input).  They are kept as one
+// row per token, sa[t] = [s^(1..M), alpha^(1..M), pad] of saw = 4*ceil(2M/4)
+// floats: 16-byte rows that a TMA copy can move.
 //
 //   finalize_kernel   bf16 layers: one warp per token turns the gate partial
 //                     sums written by the K/V GEMM's epilogue (gemm.cu) into
-//                     alpha and s for every branch.
-//   gate_kernel       fp32 layers: one warp per token computes alpha and s from
+//                     the token's sa row.
+//   gate_kernel       fp32 layers: one warp per token computes the sa row from
 //                     the fp32 [v | k] buffer of the CUDA-core GEMM.
-//   conv_kernel       one thread per (token, 4 channels): the v rows of the W
-//                     taps (the rows a token shares with its neighbours come
-//                     from L1/L2), the ring history before a chunk, the
-//                     scalars and H are all loaded together; taps (times g_c)
-//                     in registers; SiLU, the skip and H += Y for all M
-//                     branches.
+//   conv_pipe_kernel  persistent blocks over tiles of (TT positions of one
+//                     sequence, CS channels); two shared-memory stages: while a
+//                     block computes tile i, TMA brings tile i+1 -- the v rows
+//                     of the tile and its causal halo of (w-1)*dilation
+//                     positions, the H rows, the sa rows -- so the loads of
+//                     the next tile overlap the arithmetic of this one and no
+//                     data waits in registers.  Four channels per thread, taps
+//                     (times g_c) in registers; history before a chunk from the
+//                     caller's ring; SiLU, the skip and H += Y for every branch.
 //   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
 //                     (s * v) of the last (w-1)*dilation positions into the
 //                     ring, rolls the last N-1 projected ids, advances pos (a
@@ -29,10 +34,15 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "engram_internal.h"
+#include "ptx.cuh"
 
 namespace engram {
 namespace {
+
+constexpr uint64_t kTmaWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
 
 __device__ __forceinline__ void ld4(const float* p, float* out) {
   const float4 u = *reinterpret_cast<const float4*>(p);
@@ -80,19 +90,19 @@ __device__ __forceinline__ float sigmoidf(float x) { return __frcp_rn(1.f + expf
 // SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
-// alpha and s from the four sums of one (token, branch)
+// s and alpha from the four sums of one (token, branch), into the token's sa row
 __device__ __forceinline__ void gate_scalars(float sv, float dot, float sk, float sh, float inv_d, float inv_sqrt_d,
-                                             float eps, float& alpha, float& scale) {
+                                             float eps, float* sa_row, int M, int m) {
   const float rh = 1.f / sqrtf(sh * inv_d + eps);
   const float rk = 1.f / sqrtf(sk * inv_d + eps);
-  alpha = sigmoidf(dot * rh * rk * inv_sqrt_d);
-  scale = alpha * (1.f / sqrtf(alpha * alpha * (sv * inv_d) + eps));
+  const float alpha = sigmoidf(dot * rh * rk * inv_sqrt_d);
+  sa_row[m] = alpha * (1.f / sqrtf(alpha * alpha * (sv * inv_d) + eps));
+  sa_row[M + m] = alpha;
 }
 
 // ------------------------------------------------------------------ gate (bf16 layers: from partials)
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int n_sl, int64_t ntok, int M,
-                                                       int d, float eps, float* __restrict__ alpha,
-                                                       float* __restrict__ scale) {
+                                                       int d, float eps, float* __restrict__ sa, int saw) {
   const int lane = threadIdx.x & 31;
   const int P = n_sl * (1 + 3 * M);
   const float inv_d = 1.f / static_cast<float>(d);
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
       dot = warp_sum(dot);
       sk = warp_sum(sk);
       sh = warp_sum(sh);
-      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, alpha[tok * M + m], scale[tok * M + m]);
+      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, sa + tok * saw, M, m);
     }
   }
 }
@@ -124,7 +134,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
 __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv, const float* __restrict__ H,
                                                    int64_t ntok, int M, int d, float eps,
                                                    const float* __restrict__ g_h, const float* __restrict__ g_k,
-                                                   float* __restrict__ alpha, float* __restrict__ scale) {
+                                                   float* __restrict__ sa, int saw) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const float inv_d = 1.f / static_cast<float>(d);
@@ -162,99 +172,163 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
       sh = warp_sum(sh);
       sk = warp_sum(sk);
       dot = warp_sum(dot);
-      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, alpha[tok * M + m], scale[tok * M + m]);
+      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, sa + tok * saw, M, m);
     }
   }
 }
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
 struct ConvArgs {
-  int64_t sv;            // row stride of v (elements)
-  const float* alpha;    // [ntok, M]
-  const float* scale;    // [ntok, M]  s = alpha * rinv
   int B, Tn, M, d, dil;
+  int TT;                // positions per tile
+  int CS;                // channels per tile
+  int halo_eff;          // rows staged before the first position: min((w-1)*dil, T-1)
+  int saw;               // floats per sa row
+  uint32_t v_off, h_off, sa_off, stage_bytes, tx_bytes;   // shared-memory layout of one stage
   const float* g_c;      // [d]
   const float* conv;     // [d, W]
   const int32_t* pos;    // [B] (with a ring)
   int L;
+  uint32_t* err;
 };
 
-// Taps of channels c..c+3 times the conv-input RMSNorm weight g_c.
-template <int W>
-__device__ __forceinline__ void load_taps(const ConvArgs& a, int c, float (&wq)[4][W]) {
-  float gc[4];
-  ld4(a.g_c + c, gc);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (W == 4) {
-      ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
-    }
-#pragma unroll
-    for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
-  }
-}
-
-// One thread per (token, 4 channels): grid x = token, grid y = block of 256
-// channel groups.  Every load a thread needs (the v rows of its W taps, the
-// ring history before a chunk, the scalars of the tap positions, H) is
-// independent of the others and issued together; the v rows a token shares
-// with its neighbours' taps come from L1/L2.  No loop over positions, no
-// barrier, few registers: many tokens are in flight per SM.
 template <typename TH, int W>
-__global__ void __launch_bounds__(256) conv_kernel(const ConvArgs a, const float* __restrict__ v,
-                                                   const float* __restrict__ ring, TH* __restrict__ H) {
-  const int g = blockIdx.y * blockDim.x + threadIdx.x;
-  if (g >= a.d / 4) return;
-  const int64_t tok = blockIdx.x;
-  const int b = static_cast<int>(static_cast<uint32_t>(blockIdx.x) / static_cast<uint32_t>(a.Tn));
-  const int t = static_cast<int>(blockIdx.x) - b * a.Tn;
-  const int M = a.M, d = a.d, c = 4 * g;
-  float wq[4][W];
-  load_taps<W>(a, c, wq);
-  float vt[W][4];                                   // v rows of the tap positions in the chunk
-#pragma unroll
-  for (int j = 0; j < W; ++j) {
-    const int lag = (W - 1 - j) * a.dil;
-    if (t - lag >= 0) {
-      ld4(v + (tok - lag) * a.sv + c, vt[j]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vt[j][i] = 0.f;
-    }
+__global__ void __launch_bounds__(256) conv_pipe_kernel(const __grid_constant__ CUtensorMap tm_v,
+                                                        const __grid_constant__ CUtensorMap tm_h,
+                                                        const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a,
+                                                        const float* __restrict__ ring, TH* __restrict__ H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full[2];
+  const int M = a.M, d = a.d, CS = a.CS, TT = a.TT, saw = a.saw;
+  const int n_slices = d / CS;
+  const int tiles_per_seq = (a.Tn + TT - 1) / TT;
+  const int n_tiles = a.B * tiles_per_seq * n_slices;
+  const int tpr = CS / 4;                          // threads per position row
+  const int g = threadIdx.x % tpr, ty = threadIdx.x / tpr, rows_par = blockDim.x / tpr;
+
+  // tile -> (sequence, first position, first channel, rows staged before it)
+  auto coords = [&](int tile, int& b, int& t0, int& c0, int& h0) {
+    const int slice = tile % n_slices;
+    const int q = tile / n_slices;
+    b = q / tiles_per_seq;
+    t0 = (q - b * tiles_per_seq) * TT;
+    c0 = slice * CS;
+    h0 = min(a.halo_eff, t0);
+  };
+  auto issue = [&](int tile, int stage) {
+    int b, t0, c0, h0;
+    coords(tile, b, t0, c0, h0);
+    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
+    uint8_t* base = smem + stage * a.stage_bytes;
+    const int32_t row0 = static_cast<int32_t>(tok_b + t0 - h0);
+    ptx::mbar_arrive_expect_tx(&full[stage], a.tx_bytes);
+    ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[stage], c0, row0);
+    ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[stage], c0, static_cast<int32_t>((tok_b + t0) * M));
+    ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[stage], 0, row0);
+  };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&full[0], 1);
+    ptx::mbar_init(&full[1], 1);
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tm_v);
+    ptx::tma_prefetch_desc(&tm_h);
+    ptx::tma_prefetch_desc(&tm_sa);
+    if (blockIdx.x < n_tiles) issue(blockIdx.x, 0);
+    if (blockIdx.x + gridDim.x < n_tiles) issue(blockIdx.x + gridDim.x, 1);
   }
-  const int p0 = ring != nullptr ? a.pos[b] : 0;
-  for (int m = 0; m < M; ++m) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  __syncthreads();
+
+  uint32_t phase[2] = {0, 0};
+  int k = 0;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++k) {
+    const int stage = k & 1;
+    const bool ok = ptx::mbar_wait_bounded(&full[stage], phase[stage], kTmaWaitNs);
+    if (__syncthreads_or(!ok)) {                   // every thread leaves together
+      if (threadIdx.x == 0) {
+        atomicOr(a.err, kErrTimeout);
+        ptx::mbar_wait_bounded(&full[stage ^ 1], phase[stage ^ 1], kTmaWaitNs);   // let our copies land
+      }
+      break;
+    }
+    phase[stage] ^= 1;
+
+    int b, t0, c0, h0;
+    coords(tile, b, t0, c0, h0);
+    const int tn = min(TT, a.Tn - t0);
+    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
+    const uint8_t* base = smem + stage * a.stage_bytes;
+    const float* s_v = reinterpret_cast<const float*>(base + a.v_off);      // [TT + halo_eff][CS]
+    const TH* s_h = reinterpret_cast<const TH*>(base + a.h_off);            // [TT * M][CS]
+    const float* s_sa = reinterpret_cast<const float*>(base + a.sa_off);    // [TT + halo_eff][saw]
+    const int c = c0 + 4 * g;
+    float wq[4][W];                                 // taps times the RMSNorm weight g_c
+    {
+      float gc[4];
+      ld4(a.g_c + c, gc);
 #pragma unroll
-    for (int j = 0; j < W; ++j) {
-      const int lag = (W - 1 - j) * a.dil;
-      if (t - lag >= 0) {
-        const float sj = __ldg(a.scale + (tok - lag) * M + m);
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (W == 4) {
+          ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
-      } else if (ring != nullptr && p0 + t - lag >= 0) {
-        float u[4];                                 // the ring holds RMSNorm(v~) before its weight
-        ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
+          for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
+        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+        for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
       }
     }
-    const float at = __ldg(a.alpha + tok * M + m);
-    TH* hp = H + (tok * M + m) * static_cast<int64_t>(d) + c;
-    float h[4];
-    H4<TH>::load(hp, h);
+    const int p0 = ring != nullptr ? a.pos[b] : 0;
+    for (int ti = ty; ti < tn; ti += rows_par) {
+      const int t = t0 + ti;
+      const int r = ti + h0;                        // staged row of position t
+      float vt[W][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
-    H4<TH>::store(hp, h);
+      for (int j = 0; j < W; ++j) {
+        const int lag = (W - 1 - j) * a.dil;
+        if (t - lag >= 0) {
+          ld4(s_v + (r - lag) * CS + 4 * g, vt[j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vt[j][i] = 0.f;
+        }
+      }
+      for (int m = 0; m < M; ++m) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+          const int lag = (W - 1 - j) * a.dil;
+          if (t - lag >= 0) {
+            const float sj = s_sa[(r - lag) * saw + m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
+          } else if (ring != nullptr && p0 + t - lag >= 0) {
+            float u[4];                             // the ring holds RMSNorm(v~) before its weight
+            ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+          }
+        }
+        const float at = s_sa[r * saw + M + m];
+        float h[4];
+        H4<TH>::load(s_h + (ti * M + m) * CS + 4 * g, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
+        H4<TH>::store(H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c, h);
+      }
+    }
+    __syncthreads();                                // this stage has been read
+    if (threadIdx.x == 0 && tile + 2 * gridDim.x < n_tiles) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(tile + 2 * gridDim.x, stage);
+    }
   }
 }
 
 // ------------------------------------------------------------------ streaming state
 __global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_base, int64_t sv,
-                                                    const float* __restrict__ scale, int Tn, int M, int d,
+                                                    const float* __restrict__ sa, int saw, int Tn, int M, int d,
                                                     float* __restrict__ ring, int32_t* __restrict__ pos, int L,
                                                     const int32_t* __restrict__ ids,
                                                     const int32_t* __restrict__ proj, int V,
@@ -272,7 +346,7 @@ __global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_
     const int c = g * 4;
     float v[4];
     ld4(v_base + tok * sv + c, v);
-    const float sc = scale[tok * M + m];
+    const float sc = sa[tok * saw + m];
     float* dst = ring + ((static_cast<int64_t>(b) * L + (p0 + t) % L) * M + m) * d + c;
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = sc * v[i];
@@ -310,72 +384,111 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
+uint32_t align128(size_t x) { return static_cast<uint32_t>((x + 127) / 128 * 128); }
+
 template <typename TH, int W>
-cudaError_t conv_launch(const ConvArgs& a, const float* v, const float* ring, void* H, cudaStream_t s) {
-  const int groups = a.d / 4;
-  const dim3 grid(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Tn), (groups + 255) / 256);
-  conv_kernel<TH, W><<<grid, 256, 0, s>>>(a, v, ring, static_cast<TH*>(H));
+cudaError_t conv_launch(const engram_plan* p, ConvArgs a, const float* v, int64_t sv, const float* sa,
+                        const float* ring, void* H, cudaStream_t s) {
+  const size_t esize = sizeof(TH);
+  a.CS = 8;
+  for (int cs : {256, 128, 64, 32, 16})
+    if (a.d % cs == 0) {
+      a.CS = cs;
+      break;
+    }
+  a.halo_eff = std::min((W - 1) * a.dil, a.Tn - 1);
+  a.TT = std::min(a.Tn, a.M <= 2 ? 16 : (a.M <= 4 ? 8 : 4));
+  const int rows_v = a.TT + a.halo_eff;
+  a.v_off = 0;
+  a.h_off = align128(static_cast<size_t>(rows_v) * a.CS * 4);
+  a.sa_off = a.h_off + align128(static_cast<size_t>(a.TT) * a.M * a.CS * esize);
+  a.stage_bytes = a.sa_off + align128(static_cast<size_t>(rows_v) * a.saw * 4);
+  a.tx_bytes = static_cast<uint32_t>(static_cast<size_t>(rows_v) * a.CS * 4 +
+                                     static_cast<size_t>(a.TT) * a.M * a.CS * esize +
+                                     static_cast<size_t>(rows_v) * a.saw * 4);
+  const size_t smem = 128 + 2 * static_cast<size_t>(a.stage_bytes);
+  const int64_t ntok = static_cast<int64_t>(a.B) * a.Tn;
+  CUtensorMap tv, th, tsa;
+  if (!make_tensor_map_2d(&tv, v, true, a.d, ntok, sv * 4, a.CS, rows_v, false) ||
+      !make_tensor_map_2d(&th, H, esize == 4, a.d, ntok * a.M, static_cast<uint64_t>(a.d) * esize, a.CS,
+                          a.TT * a.M, false) ||
+      !make_tensor_map_2d(&tsa, sa, true, a.saw, ntok, static_cast<uint64_t>(a.saw) * 4, a.saw, rows_v, false))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(conv_pipe_kernel<TH, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT) * (a.d / a.CS);
+  const int per_sm = std::max(1, static_cast<int>((220 * 1024) / smem));
+  const int64_t cap = static_cast<int64_t>(p->num_sms) * std::min(per_sm, 4);
+  conv_pipe_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(tv, th, tsa, a, ring,
+                                                                                        static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
 template <typename TH>
-cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, const float* v, const float* ring, void* H,
-                          cudaStream_t s) {
+cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, const float* v, int64_t sv, const float* sa,
+                          const float* ring, void* H, cudaStream_t s) {
   switch (p->cfg.conv_w) {
-    case 1: return conv_launch<TH, 1>(a, v, ring, H, s);
-    case 2: return conv_launch<TH, 2>(a, v, ring, H, s);
-    case 3: return conv_launch<TH, 3>(a, v, ring, H, s);
-    case 4: return conv_launch<TH, 4>(a, v, ring, H, s);
-    case 5: return conv_launch<TH, 5>(a, v, ring, H, s);
-    case 6: return conv_launch<TH, 6>(a, v, ring, H, s);
-    case 7: return conv_launch<TH, 7>(a, v, ring, H, s);
-    case 8: return conv_launch<TH, 8>(a, v, ring, H, s);
+    case 1: return conv_launch<TH, 1>(p, a, v, sv, sa, ring, H, s);
+    case 2: return conv_launch<TH, 2>(p, a, v, sv, sa, ring, H, s);
+    case 3: return conv_launch<TH, 3>(p, a, v, sv, sa, ring, H, s);
+    case 4: return conv_launch<TH, 4>(p, a, v, sv, sa, ring, H, s);
+    case 5: return conv_launch<TH, 5>(p, a, v, sv, sa, ring, H, s);
+    case 6: return conv_launch<TH, 6>(p, a, v, sv, sa, ring, H, s);
+    case 7: return conv_launch<TH, 7>(p, a, v, sv, sa, ring, H, s);
+    case 8: return conv_launch<TH, 8>(p, a, v, sv, sa, ring, H, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* alpha,
-                            float* scale, cudaStream_t s) {
+int sa_row_floats(int M) { return (2 * M + 3) / 4 * 4; }
+
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* sa,
+                            cudaStream_t s) {
   finalize_kernel<<<grid_for(ntok * 32, 256, p->num_sms), 256, 0, s>>>(part, n_sl, ntok, p->cfg.M, p->cfg.d,
-                                                                       p->cfg.eps, alpha, scale);
+                                                                       p->cfg.eps, sa, sa_row_floats(p->cfg.M));
   return cudaGetLastError();
 }
 
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
-                            const float* g_k, float* alpha, float* scale, cudaStream_t s) {
+                            const float* g_k, float* sa, cudaStream_t s) {
   gate_kernel<<<grid_for(ntok * 32, 256, p->num_sms), 256, 0, s>>>(kv, H, ntok, p->cfg.M, p->cfg.d, p->cfg.eps, g_h,
-                                                                   g_k, alpha, scale);
+                                                                   g_k, sa, sa_row_floats(p->cfg.M));
   return cudaGetLastError();
 }
 
-cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* alpha,
-                                 const float* scale, int B, int T, const float* g_c, const float* conv, void* H,
-                                 const engram_state_t* state, cudaStream_t s) {
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
+                                 const float* g_c, const float* conv, void* H, const engram_state_t* state,
+                                 cudaStream_t s) {
   ConvArgs a{};
-  a.sv = sv;
-  a.alpha = alpha;
-  a.scale = scale;
   a.B = B;
   a.Tn = T;
   a.M = p->cfg.M;
   a.d = p->cfg.d;
   a.dil = p->cfg.conv_dilation;
+  a.saw = sa_row_floats(p->cfg.M);
   a.g_c = g_c;
   a.conv = conv;
   a.pos = state ? state->pos : nullptr;
   a.L = p->L_ring;
+  a.err = &p->dev->err;
   const float* ring = state ? state->u_ring : nullptr;
-  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, v, ring, H, s);
-  return conv_dispatch<__nv_bfloat16>(p, a, v, ring, H, s);
+  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, v, sv, sa, ring, H, s);
+  return conv_dispatch<__nv_bfloat16>(p, a, v, sv, sa, ring, H, s);
 }
 
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
-                                int64_t sv, const float* scale, int B, int T, const engram_state_t* st,
+                                int64_t sv, const float* sa, int B, int T, const engram_state_t* st,
                                 cudaStream_t s) {
-  state_kernel<<<B, 256, 0, s>>>(v, sv, scale, T, p->cfg.M, p->cfg.d, st->u_ring, st->pos, p->L_ring, ids, proj, V,
-                                 st->prev_ids, p->cfg.N, &p->dev->err);
+  state_kernel<<<B, 256, 0, s>>>(v, sv, sa, sa_row_floats(p->cfg.M), T, p->cfg.M, p->cfg.d, st->u_ring, st->pos,
+                                 p->L_ring, ids, proj, V, st->prev_ids, p->cfg.N, &p->dev->err);
   return cudaGetLastError();
 }
 
