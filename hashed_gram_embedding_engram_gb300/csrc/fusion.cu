@@ -21,9 +21,11 @@
 //                     of the tile and its causal halo of (w-1)*dilation
 //                     positions, the H rows, the sa rows -- so the loads of
 //                     the next tile overlap the arithmetic of this one and no
-//                     data waits in registers.  Four channels per thread, taps
-//                     (times g_c) in registers; history before a chunk from the
-//                     caller's ring; SiLU, the skip and H += Y for every branch.
+//                     data waits in registers.  Eight channels per thread, taps
+//                     (times g_c) in registers, compile-time taps and dilation
+//                     for w = 4 (the pages' conv) with no per-tap bounds checks
+//                     away from a sequence start; history before a chunk from
+//                     the caller's ring; SiLU, the skip and H += Y per branch.
 //   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
 //                     (s * v) of the last (w-1)*dilation positions into the
 //                     ring, rolls the last N-1 projected ids, advances pos (a
@@ -192,7 +194,60 @@ struct ConvArgs {
   uint32_t* err;
 };
 
-template <typename TH, int W>
+// 8 channels of H as floats (16-byte bf16 / 2 x 16-byte fp32 accesses)
+template <typename T>
+struct H8;
+template <>
+struct H8<__nv_bfloat16> {
+  __device__ static void load(const __nv_bfloat16* p, float* out) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* in) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct H8<float> {
+  __device__ static void load(const float* p, float* out) {
+    ld4(p, out);
+    ld4(p + 4, out + 4);
+  }
+  __device__ static void store(float* p, const float* in) {
+    *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(in[4], in[5], in[6], in[7]);
+  }
+};
+
+// Tile -> (sequence b, first position t0, first channel c0, staged rows h0 before t0).
+struct TileCoords {
+  int b, t0, c0, h0;
+};
+__device__ __forceinline__ TileCoords tile_coords(const ConvArgs& a, int tile) {
+  const int n_slices = a.d / a.CS;
+  const int tiles_per_seq = (a.Tn + a.TT - 1) / a.TT;
+  TileCoords tc;
+  const int q = tile / n_slices;
+  tc.c0 = (tile - q * n_slices) * a.CS;
+  tc.b = q / tiles_per_seq;
+  tc.t0 = (q - tc.b * tiles_per_seq) * a.TT;
+  tc.h0 = min(a.halo_eff, tc.t0);
+  return tc;
+}
+
+// DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
+template <typename TH, int W, int DIL>
 __global__ void __launch_bounds__(256) conv_pipe_kernel(const __grid_constant__ CUtensorMap tm_v,
                                                         const __grid_constant__ CUtensorMap tm_h,
                                                         const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a,
@@ -200,31 +255,21 @@ __global__ void __launch_bounds__(256) conv_pipe_kernel(const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[2];
-  const int M = a.M, d = a.d, CS = a.CS, TT = a.TT, saw = a.saw;
-  const int n_slices = d / CS;
-  const int tiles_per_seq = (a.Tn + TT - 1) / TT;
-  const int n_tiles = a.B * tiles_per_seq * n_slices;
-  const int tpr = CS / 4;                          // threads per position row
+  const int dil = DIL > 0 ? DIL : a.dil;
+  const int halo = (W - 1) * dil;
+  const int M = a.M, d = a.d, CS = a.CS, saw = a.saw;
+  const int n_tiles = a.B * ((a.Tn + a.TT - 1) / a.TT) * (d / CS);
+  const int tpr = CS / 8;                          // threads per position row, 8 channels each
   const int g = threadIdx.x % tpr, ty = threadIdx.x / tpr, rows_par = blockDim.x / tpr;
 
-  // tile -> (sequence, first position, first channel, rows staged before it)
-  auto coords = [&](int tile, int& b, int& t0, int& c0, int& h0) {
-    const int slice = tile % n_slices;
-    const int q = tile / n_slices;
-    b = q / tiles_per_seq;
-    t0 = (q - b * tiles_per_seq) * TT;
-    c0 = slice * CS;
-    h0 = min(a.halo_eff, t0);
-  };
   auto issue = [&](int tile, int stage) {
-    int b, t0, c0, h0;
-    coords(tile, b, t0, c0, h0);
-    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
+    const TileCoords tc = tile_coords(a, tile);
+    const int64_t tok_b = static_cast<int64_t>(tc.b) * a.Tn;
     uint8_t* base = smem + stage * a.stage_bytes;
-    const int32_t row0 = static_cast<int32_t>(tok_b + t0 - h0);
+    const int32_t row0 = static_cast<int32_t>(tok_b + tc.t0 - tc.h0);
     ptx::mbar_arrive_expect_tx(&full[stage], a.tx_bytes);
-    ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[stage], c0, row0);
-    ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[stage], c0, static_cast<int32_t>((tok_b + t0) * M));
+    ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[stage], tc.c0, row0);
+    ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[stage], tc.c0, static_cast<int32_t>((tok_b + tc.t0) * M));
     ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[stage], 0, row0);
   };
 
@@ -244,31 +289,16 @@ __global__ void __launch_bounds__(256) conv_pipe_kernel(const __grid_constant__ 
   int k = 0;
   for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++k) {
     const int stage = k & 1;
-    const bool ok = ptx::mbar_wait_bounded(&full[stage], phase[stage], kTmaWaitNs);
-    if (__syncthreads_or(!ok)) {                   // every thread leaves together
-      if (threadIdx.x == 0) {
-        atomicOr(a.err, kErrTimeout);
-        ptx::mbar_wait_bounded(&full[stage ^ 1], phase[stage ^ 1], kTmaWaitNs);   // let our copies land
-      }
-      break;
-    }
-    phase[stage] ^= 1;
-
-    int b, t0, c0, h0;
-    coords(tile, b, t0, c0, h0);
-    const int tn = min(TT, a.Tn - t0);
-    const int64_t tok_b = static_cast<int64_t>(b) * a.Tn;
-    const uint8_t* base = smem + stage * a.stage_bytes;
-    const float* s_v = reinterpret_cast<const float*>(base + a.v_off);      // [TT + halo_eff][CS]
-    const TH* s_h = reinterpret_cast<const TH*>(base + a.h_off);            // [TT * M][CS]
-    const float* s_sa = reinterpret_cast<const float*>(base + a.sa_off);    // [TT + halo_eff][saw]
-    const int c = c0 + 4 * g;
-    float wq[4][W];                                 // taps times the RMSNorm weight g_c
+    const TileCoords tc = tile_coords(a, tile);   // overlaps the wait
+    const int tn = min(a.TT, a.Tn - tc.t0);
+    const int c = tc.c0 + 8 * g;
+    float wq[8][W];                                // taps times the RMSNorm weight g_c
     {
-      float gc[4];
+      float gc[8];
       ld4(a.g_c + c, gc);
+      ld4(a.g_c + c + 4, gc + 4);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         if constexpr (W == 4) {
           ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
         } else {
@@ -279,43 +309,63 @@ __global__ void __launch_bounds__(256) conv_pipe_kernel(const __grid_constant__ 
         for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
       }
     }
-    const int p0 = ring != nullptr ? a.pos[b] : 0;
+    const bool ok = ptx::mbar_wait_bounded(&full[stage], phase[stage], kTmaWaitNs);
+    if (__syncthreads_or(!ok)) {                   // every thread leaves together
+      if (threadIdx.x == 0) {
+        atomicOr(a.err, kErrTimeout);
+        ptx::mbar_wait_bounded(&full[stage ^ 1], phase[stage ^ 1], kTmaWaitNs);   // let our copies land
+      }
+      break;
+    }
+    phase[stage] ^= 1;
+
+    const int64_t tok_b = static_cast<int64_t>(tc.b) * a.Tn;
+    const uint8_t* base = smem + stage * a.stage_bytes;
+    const float* s_v = reinterpret_cast<const float*>(base + a.v_off) + 8 * g;   // [TT + halo_eff][CS]
+    const TH* s_h = reinterpret_cast<const TH*>(base + a.h_off) + 8 * g;         // [TT * M][CS]
+    const float* s_sa = reinterpret_cast<const float*>(base + a.sa_off);         // [TT + halo_eff][saw]
+    const bool interior = tc.t0 >= halo;           // every tap of the tile lies inside the chunk
+    const int p0 = ring != nullptr ? a.pos[tc.b] : 0;
     for (int ti = ty; ti < tn; ti += rows_par) {
-      const int t = t0 + ti;
-      const int r = ti + h0;                        // staged row of position t
-      float vt[W][4];
+      const int t = tc.t0 + ti;
+      const int r = ti + tc.h0;                    // staged row of position t
+      float vt[W][8];
 #pragma unroll
       for (int j = 0; j < W; ++j) {
-        const int lag = (W - 1 - j) * a.dil;
-        if (t - lag >= 0) {
-          ld4(s_v + (r - lag) * CS + 4 * g, vt[j]);
+        const int lag = (W - 1 - j) * dil;
+        if (interior || t - lag >= 0) {
+          ld4(s_v + (r - lag) * CS, vt[j]);
+          ld4(s_v + (r - lag) * CS + 4, vt[j] + 4);
         } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) vt[j][i] = 0.f;
+          for (int i = 0; i < 8; ++i) vt[j][i] = 0.f;
         }
       }
+      TH* hout = H + (tok_b + t) * M * static_cast<int64_t>(d) + c;
       for (int m = 0; m < M; ++m) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < W; ++j) {
-          const int lag = (W - 1 - j) * a.dil;
-          if (t - lag >= 0) {
+          const int lag = (W - 1 - j) * dil;
+          if (interior || t - lag >= 0) {
             const float sj = s_sa[(r - lag) * saw + m];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
           } else if (ring != nullptr && p0 + t - lag >= 0) {
-            float u[4];                             // the ring holds RMSNorm(v~) before its weight
-            ld4(ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c, u);
+            float u[8];                             // the ring holds RMSNorm(v~) before its weight
+            const float* rp = ring + ((static_cast<int64_t>(tc.b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c;
+            ld4(rp, u);
+            ld4(rp + 4, u + 4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
           }
         }
         const float at = s_sa[r * saw + M + m];
-        float h[4];
-        H4<TH>::load(s_h + (ti * M + m) * CS + 4 * g, h);
+        float h[8];
+        H8<TH>::load(s_h + (ti * M + m) * CS, h);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
-        H4<TH>::store(H + ((tok_b + t) * M + m) * static_cast<int64_t>(d) + c, h);
+        for (int i = 0; i < 8; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
+        H8<TH>::store(hout + static_cast<int64_t>(m) * d, h);
       }
     }
     __syncthreads();                                // this stage has been read
@@ -386,7 +436,7 @@ int grid_for(int64_t items, int threads, int num_sms) {
 
 uint32_t align128(size_t x) { return static_cast<uint32_t>((x + 127) / 128 * 128); }
 
-template <typename TH, int W>
+template <typename TH, int W, int DIL>
 cudaError_t conv_launch(const engram_plan* p, ConvArgs a, const float* v, int64_t sv, const float* sa,
                         const float* ring, void* H, cudaStream_t s) {
   const size_t esize = sizeof(TH);
@@ -416,7 +466,7 @@ cudaError_t conv_launch(const engram_plan* p, ConvArgs a, const float* v, int64_
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(conv_pipe_kernel<TH, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(conv_pipe_kernel<TH, W, DIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          200 * 1024);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -425,23 +475,36 @@ cudaError_t conv_launch(const engram_plan* p, ConvArgs a, const float* v, int64_
   const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT) * (a.d / a.CS);
   const int per_sm = std::max(1, static_cast<int>((220 * 1024) / smem));
   const int64_t cap = static_cast<int64_t>(p->num_sms) * std::min(per_sm, 4);
-  conv_pipe_kernel<TH, W><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(tv, th, tsa, a, ring,
-                                                                                        static_cast<TH*>(H));
+  conv_pipe_kernel<TH, W, DIL><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(
+      tv, th, tsa, a, ring, static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
 template <typename TH>
 cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, const float* v, int64_t sv, const float* sa,
                           const float* ring, void* H, cudaStream_t s) {
+  if (p->cfg.conv_w == 4) {
+    switch (a.dil) {   // the pages' short conv: w = 4, dilation = max n-gram order
+      case 1: return conv_launch<TH, 4, 1>(p, a, v, sv, sa, ring, H, s);
+      case 2: return conv_launch<TH, 4, 2>(p, a, v, sv, sa, ring, H, s);
+      case 3: return conv_launch<TH, 4, 3>(p, a, v, sv, sa, ring, H, s);
+      case 4: return conv_launch<TH, 4, 4>(p, a, v, sv, sa, ring, H, s);
+      case 5: return conv_launch<TH, 4, 5>(p, a, v, sv, sa, ring, H, s);
+      case 6: return conv_launch<TH, 4, 6>(p, a, v, sv, sa, ring, H, s);
+      case 7: return conv_launch<TH, 4, 7>(p, a, v, sv, sa, ring, H, s);
+      case 8: return conv_launch<TH, 4, 8>(p, a, v, sv, sa, ring, H, s);
+      default: break;
+    }
+  }
   switch (p->cfg.conv_w) {
-    case 1: return conv_launch<TH, 1>(p, a, v, sv, sa, ring, H, s);
-    case 2: return conv_launch<TH, 2>(p, a, v, sv, sa, ring, H, s);
-    case 3: return conv_launch<TH, 3>(p, a, v, sv, sa, ring, H, s);
-    case 4: return conv_launch<TH, 4>(p, a, v, sv, sa, ring, H, s);
-    case 5: return conv_launch<TH, 5>(p, a, v, sv, sa, ring, H, s);
-    case 6: return conv_launch<TH, 6>(p, a, v, sv, sa, ring, H, s);
-    case 7: return conv_launch<TH, 7>(p, a, v, sv, sa, ring, H, s);
-    case 8: return conv_launch<TH, 8>(p, a, v, sv, sa, ring, H, s);
+    case 1: return conv_launch<TH, 1, 0>(p, a, v, sv, sa, ring, H, s);
+    case 2: return conv_launch<TH, 2, 0>(p, a, v, sv, sa, ring, H, s);
+    case 3: return conv_launch<TH, 3, 0>(p, a, v, sv, sa, ring, H, s);
+    case 4: return conv_launch<TH, 4, 0>(p, a, v, sv, sa, ring, H, s);
+    case 5: return conv_launch<TH, 5, 0>(p, a, v, sv, sa, ring, H, s);
+    case 6: return conv_launch<TH, 6, 0>(p, a, v, sv, sa, ring, H, s);
+    case 7: return conv_launch<TH, 7, 0>(p, a, v, sv, sa, ring, H, s);
+    case 8: return conv_launch<TH, 8, 0>(p, a, v, sv, sa, ring, H, s);
     default: return cudaErrorInvalidValue;
   }
 }
