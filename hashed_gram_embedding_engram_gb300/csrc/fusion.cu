@@ -15,17 +15,12 @@
 //                     the token's sa row.
 //   gate_kernel       fp32 layers: one warp per token computes the sa row from
 //                     the fp32 [v | k] buffer of the CUDA-core GEMM.
-//   conv_pipe_kernel  persistent blocks over tiles of (TT positions of one
-//                     sequence, CS channels); two shared-memory stages: while a
-//                     block computes tile i, TMA brings tile i+1 -- the v rows
-//                     of the tile and its causal halo of (w-1)*dilation
-//                     positions, the H rows, the sa rows -- so the loads of
-//                     the next tile overlap the arithmetic of this one and no
-//                     data waits in registers.  Eight channels per thread, taps
-//                     (times g_c) in registers, compile-time taps and dilation
-//                     for w = 4 (the pages' conv) with no per-tap bounds checks
-//                     away from a sequence start; history before a chunk from
-//                     the caller's ring; SiLU, the skip and H += Y per branch.
+//   conv_kernel       one thread per (token, 8 channels): the v rows of the W
+//                     taps (rows a token shares with its neighbours' taps come
+//                     from L1/L2), the ring history before a chunk, the scalar
+//                     rows and H are all loaded together; taps (times g_c) in
+//                     registers, compile-time dilation for w = 4 (the pages'
+//                     conv); SiLU, the skip and H += Y for every branch.
 //   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
 //                     (s * v) of the last (w-1)*dilation positions into the
 //                     ring, rolls the last N-1 projected ids, advances pos (a
@@ -36,15 +31,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <algorithm>
-
 #include "engram_internal.h"
-#include "ptx.cuh"
 
 namespace engram {
 namespace {
-
-constexpr uint64_t kTmaWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
 
 __device__ __forceinline__ void ld4(const float* p, float* out) {
   const float4 u = *reinterpret_cast<const float4*>(p);
@@ -53,32 +43,6 @@ __device__ __forceinline__ void ld4(const float* p, float* out) {
   out[2] = u.z;
   out[3] = u.w;
 }
-
-// 4 channels of H as floats (8-byte bf16 / 16-byte fp32 accesses)
-template <typename T>
-struct H4;
-template <>
-struct H4<__nv_bfloat16> {
-  __device__ static void load(const __nv_bfloat16* p, float* out) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    out[0] = __uint_as_float(u.x << 16);
-    out[1] = __uint_as_float(u.x & 0xFFFF0000u);
-    out[2] = __uint_as_float(u.y << 16);
-    out[3] = __uint_as_float(u.y & 0xFFFF0000u);
-  }
-  __device__ static void store(__nv_bfloat16* p, const float* in) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
-    __nv_bfloat162 b = __floats2bfloat162_rn(in[2], in[3]);
-    *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
-  }
-};
-template <>
-struct H4<float> {
-  __device__ static void load(const float* p, float* out) { ld4(p, out); }
-  __device__ static void store(float* p, const float* in) {
-    *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
-  }
-};
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -181,17 +145,13 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
 struct ConvArgs {
+  int64_t sv;            // row stride of v (elements)
   int B, Tn, M, d, dil;
-  int TT;                // positions per tile
-  int CS;                // channels per tile
-  int halo_eff;          // rows staged before the first position: min((w-1)*dil, T-1)
   int saw;               // floats per sa row
-  uint32_t v_off, h_off, sa_off, stage_bytes, tx_bytes;   // shared-memory layout of one stage
   const float* g_c;      // [d]
   const float* conv;     // [d, W]
   const int32_t* pos;    // [B] (with a ring)
   int L;
-  uint32_t* err;
 };
 
 // 8 channels of H as floats (16-byte bf16 / 2 x 16-byte fp32 accesses)
@@ -230,149 +190,79 @@ struct H8<float> {
   }
 };
 
-// Tile -> (sequence b, first position t0, first channel c0, staged rows h0 before t0).
-struct TileCoords {
-  int b, t0, c0, h0;
-};
-__device__ __forceinline__ TileCoords tile_coords(const ConvArgs& a, int tile) {
-  const int n_slices = a.d / a.CS;
-  const int tiles_per_seq = (a.Tn + a.TT - 1) / a.TT;
-  TileCoords tc;
-  const int q = tile / n_slices;
-  tc.c0 = (tile - q * n_slices) * a.CS;
-  tc.b = q / tiles_per_seq;
-  tc.t0 = (q - tc.b * tiles_per_seq) * a.TT;
-  tc.h0 = min(a.halo_eff, tc.t0);
-  return tc;
-}
-
-// DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
+// One thread per (token, 8 channels): grid x = token, grid y = block of 256
+// channel groups.  Every load a thread needs -- the v rows of its W taps (the
+// rows a token shares with its neighbours' taps come from L1/L2), the ring
+// history before a chunk, the scalars of the tap positions, H -- is
+// independent of the others and issued together.  DIL > 0: compile-time
+// dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
 template <typename TH, int W, int DIL>
-__global__ void __launch_bounds__(256) conv_pipe_kernel(const __grid_constant__ CUtensorMap tm_v,
-                                                        const __grid_constant__ CUtensorMap tm_h,
-                                                        const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a,
-                                                        const float* __restrict__ ring, TH* __restrict__ H) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  __shared__ uint64_t full[2];
+__global__ void __launch_bounds__(256, 3) conv_kernel(const ConvArgs a, const float* __restrict__ v,
+                                                   const float* __restrict__ sa, const float* __restrict__ ring,
+                                                   TH* __restrict__ H) {
+  const int g = blockIdx.y * blockDim.x + threadIdx.x;
+  if (g >= a.d / 8) return;
   const int dil = DIL > 0 ? DIL : a.dil;
-  const int halo = (W - 1) * dil;
-  const int M = a.M, d = a.d, CS = a.CS, saw = a.saw;
-  const int n_tiles = a.B * ((a.Tn + a.TT - 1) / a.TT) * (d / CS);
-  const int tpr = CS / 8;                          // threads per position row, 8 channels each
-  const int g = threadIdx.x % tpr, ty = threadIdx.x / tpr, rows_par = blockDim.x / tpr;
-
-  auto issue = [&](int tile, int stage) {
-    const TileCoords tc = tile_coords(a, tile);
-    const int64_t tok_b = static_cast<int64_t>(tc.b) * a.Tn;
-    uint8_t* base = smem + stage * a.stage_bytes;
-    const int32_t row0 = static_cast<int32_t>(tok_b + tc.t0 - tc.h0);
-    ptx::mbar_arrive_expect_tx(&full[stage], a.tx_bytes);
-    ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[stage], tc.c0, row0);
-    ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[stage], tc.c0, static_cast<int32_t>((tok_b + tc.t0) * M));
-    ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[stage], 0, row0);
-  };
-
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(&full[0], 1);
-    ptx::mbar_init(&full[1], 1);
-    ptx::fence_mbar_init();
-    ptx::tma_prefetch_desc(&tm_v);
-    ptx::tma_prefetch_desc(&tm_h);
-    ptx::tma_prefetch_desc(&tm_sa);
-    if (blockIdx.x < n_tiles) issue(blockIdx.x, 0);
-    if (blockIdx.x + gridDim.x < n_tiles) issue(blockIdx.x + gridDim.x, 1);
+  const int64_t tok = blockIdx.x;
+  const int b = static_cast<int>(static_cast<uint32_t>(blockIdx.x) / static_cast<uint32_t>(a.Tn));
+  const int t = static_cast<int>(blockIdx.x) - b * a.Tn;
+  const int M = a.M, d = a.d, c = 8 * g, saw = a.saw;
+  float vt[W][8];                                   // v rows of the tap positions inside the chunk
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    const int lag = (W - 1 - j) * dil;
+    if (t - lag >= 0) {
+      const float* vp = v + (tok - lag) * a.sv + c;
+      ld4(vp, vt[j]);
+      ld4(vp + 4, vt[j] + 4);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vt[j][i] = 0.f;
+    }
   }
-  __syncthreads();
-
-  uint32_t phase[2] = {0, 0};
-  int k = 0;
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++k) {
-    const int stage = k & 1;
-    const TileCoords tc = tile_coords(a, tile);   // overlaps the wait
-    const int tn = min(a.TT, a.Tn - tc.t0);
-    const int c = tc.c0 + 8 * g;
-    float wq[8][W];                                // taps times the RMSNorm weight g_c
-    {
-      float gc[8];
-      ld4(a.g_c + c, gc);
-      ld4(a.g_c + c + 4, gc + 4);
+  float wq[8][W];                                   // taps times the RMSNorm weight g_c
+  {
+    float gc[8];
+    ld4(a.g_c + c, gc);
+    ld4(a.g_c + c + 4, gc + 4);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if constexpr (W == 4) {
-          ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
-        } else {
+    for (int i = 0; i < 8; ++i) {
+      if constexpr (W == 4) {
+        ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
+      } else {
 #pragma unroll
-          for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
-        }
+        for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
+      }
 #pragma unroll
-        for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
+      for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
+    }
+  }
+  const int p0 = ring != nullptr ? a.pos[b] : 0;
+  TH* hp = H + tok * M * static_cast<int64_t>(d) + c;
+  for (int m = 0; m < M; ++m) {
+    float h[8];
+    H8<TH>::load(hp + static_cast<int64_t>(m) * d, h);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      const int lag = (W - 1 - j) * dil;
+      if (t - lag >= 0) {
+        const float sj = __ldg(sa + (tok - lag) * saw + m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
+      } else if (ring != nullptr && p0 + t - lag >= 0) {
+        float u[8];                                 // the ring holds RMSNorm(v~) before its weight
+        const float* rp = ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c;
+        ld4(rp, u);
+        ld4(rp + 4, u + 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
       }
     }
-    const bool ok = ptx::mbar_wait_bounded(&full[stage], phase[stage], kTmaWaitNs);
-    if (__syncthreads_or(!ok)) {                   // every thread leaves together
-      if (threadIdx.x == 0) {
-        atomicOr(a.err, kErrTimeout);
-        ptx::mbar_wait_bounded(&full[stage ^ 1], phase[stage ^ 1], kTmaWaitNs);   // let our copies land
-      }
-      break;
-    }
-    phase[stage] ^= 1;
-
-    const int64_t tok_b = static_cast<int64_t>(tc.b) * a.Tn;
-    const uint8_t* base = smem + stage * a.stage_bytes;
-    const float* s_v = reinterpret_cast<const float*>(base + a.v_off) + 8 * g;   // [TT + halo_eff][CS]
-    const TH* s_h = reinterpret_cast<const TH*>(base + a.h_off) + 8 * g;         // [TT * M][CS]
-    const float* s_sa = reinterpret_cast<const float*>(base + a.sa_off);         // [TT + halo_eff][saw]
-    const bool interior = tc.t0 >= halo;           // every tap of the tile lies inside the chunk
-    const int p0 = ring != nullptr ? a.pos[tc.b] : 0;
-    for (int ti = ty; ti < tn; ti += rows_par) {
-      const int t = tc.t0 + ti;
-      const int r = ti + tc.h0;                    // staged row of position t
-      float vt[W][8];
+    const float at = __ldg(sa + tok * saw + M + m);
 #pragma unroll
-      for (int j = 0; j < W; ++j) {
-        const int lag = (W - 1 - j) * dil;
-        if (interior || t - lag >= 0) {
-          ld4(s_v + (r - lag) * CS, vt[j]);
-          ld4(s_v + (r - lag) * CS + 4, vt[j] + 4);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) vt[j][i] = 0.f;
-        }
-      }
-      TH* hout = H + (tok_b + t) * M * static_cast<int64_t>(d) + c;
-      for (int m = 0; m < M; ++m) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < W; ++j) {
-          const int lag = (W - 1 - j) * dil;
-          if (interior || t - lag >= 0) {
-            const float sj = s_sa[(r - lag) * saw + m];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
-          } else if (ring != nullptr && p0 + t - lag >= 0) {
-            float u[8];                             // the ring holds RMSNorm(v~) before its weight
-            const float* rp = ring + ((static_cast<int64_t>(tc.b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c;
-            ld4(rp, u);
-            ld4(rp + 4, u + 4);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
-          }
-        }
-        const float at = s_sa[r * saw + M + m];
-        float h[8];
-        H8<TH>::load(s_h + (ti * M + m) * CS, h);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
-        H8<TH>::store(hout + static_cast<int64_t>(m) * d, h);
-      }
-    }
-    __syncthreads();                                // this stage has been read
-    if (threadIdx.x == 0 && tile + 2 * gridDim.x < n_tiles) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(tile + 2 * gridDim.x, stage);
-    }
+    for (int i = 0; i < 8; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
+    H8<TH>::store(hp + static_cast<int64_t>(m) * d, h);
   }
 }
 
@@ -434,49 +324,14 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-uint32_t align128(size_t x) { return static_cast<uint32_t>((x + 127) / 128 * 128); }
-
 template <typename TH, int W, int DIL>
 cudaError_t conv_launch(const engram_plan* p, ConvArgs a, const float* v, int64_t sv, const float* sa,
                         const float* ring, void* H, cudaStream_t s) {
-  const size_t esize = sizeof(TH);
-  a.CS = 8;
-  for (int cs : {256, 128, 64, 32, 16})
-    if (a.d % cs == 0) {
-      a.CS = cs;
-      break;
-    }
-  a.halo_eff = std::min((W - 1) * a.dil, a.Tn - 1);
-  a.TT = std::min(a.Tn, a.M <= 2 ? 16 : (a.M <= 4 ? 8 : 4));
-  const int rows_v = a.TT + a.halo_eff;
-  a.v_off = 0;
-  a.h_off = align128(static_cast<size_t>(rows_v) * a.CS * 4);
-  a.sa_off = a.h_off + align128(static_cast<size_t>(a.TT) * a.M * a.CS * esize);
-  a.stage_bytes = a.sa_off + align128(static_cast<size_t>(rows_v) * a.saw * 4);
-  a.tx_bytes = static_cast<uint32_t>(static_cast<size_t>(rows_v) * a.CS * 4 +
-                                     static_cast<size_t>(a.TT) * a.M * a.CS * esize +
-                                     static_cast<size_t>(rows_v) * a.saw * 4);
-  const size_t smem = 128 + 2 * static_cast<size_t>(a.stage_bytes);
-  const int64_t ntok = static_cast<int64_t>(a.B) * a.Tn;
-  CUtensorMap tv, th, tsa;
-  if (!make_tensor_map_2d(&tv, v, true, a.d, ntok, sv * 4, a.CS, rows_v, false) ||
-      !make_tensor_map_2d(&th, H, esize == 4, a.d, ntok * a.M, static_cast<uint64_t>(a.d) * esize, a.CS,
-                          a.TT * a.M, false) ||
-      !make_tensor_map_2d(&tsa, sa, true, a.saw, ntok, static_cast<uint64_t>(a.saw) * 4, a.saw, rows_v, false))
-    return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(conv_pipe_kernel<TH, W, DIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  const int64_t tiles = static_cast<int64_t>(a.B) * ((a.Tn + a.TT - 1) / a.TT) * (a.d / a.CS);
-  const int per_sm = std::max(1, static_cast<int>((220 * 1024) / smem));
-  const int64_t cap = static_cast<int64_t>(p->num_sms) * std::min(per_sm, 4);
-  conv_pipe_kernel<TH, W, DIL><<<static_cast<int>(tiles < cap ? tiles : cap), 256, smem, s>>>(
-      tv, th, tsa, a, ring, static_cast<TH*>(H));
+  (void)p;
+  a.sv = sv;
+  const int groups = a.d / 8;
+  const dim3 grid(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Tn), (groups + 255) / 256);
+  conv_kernel<TH, W, DIL><<<grid, 256, 0, s>>>(a, v, sa, ring, static_cast<TH*>(H));
   return cudaGetLastError();
 }
 
@@ -541,7 +396,6 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.conv = conv;
   a.pos = state ? state->pos : nullptr;
   a.L = p->L_ring;
-  a.err = &p->dev->err;
   const float* ring = state ? state->u_ring : nullptr;
   if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, v, sv, sa, ring, H, s);
   return conv_dispatch<__nv_bfloat16>(p, a, v, sv, sa, ring, H, s);
