@@ -107,7 +107,8 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
     w.kv = reinterpret_cast<float*>(take(n * (M + 1) * d * 4));
   } else {
     w.v32 = reinterpret_cast<float*>(take(n * d * 4));
-    w.part = reinterpret_cast<float*>(take(n * (d / 32) * (1 + 3 * M) * 4));   // widest case: 32-column slices
+    // widest case: 32-column slices, rows padded to 16 bytes
+    w.part = reinterpret_cast<float*>(take(n * (((d / 32) * (1 + 3 * M) + 3) / 4 * 4) * 4));
   }
   w.sa = reinterpret_cast<float*>(take(n * engram::sa_row_floats(static_cast<int>(M)) * 4));
   w.bytes = off;
@@ -208,7 +209,15 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
     delete p;
     return ENGRAM_ERR_CUDA;
   }
-  if (cudaMemcpy(p->dev, &h, sizeof(PlanDev), cudaMemcpyHostToDevice) != cudaSuccess) {
+  p->tile_cnt_bytes = static_cast<size_t>((max_tokens + 127) / 128) * 4 * sizeof(uint32_t);
+  if (cudaMalloc(&p->tile_cnt, p->tile_cnt_bytes) != cudaSuccess) {
+    cudaFree(p->dev);
+    delete p;
+    return ENGRAM_ERR_CUDA;
+  }
+  if (cudaMemcpy(p->dev, &h, sizeof(PlanDev), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(p->tile_cnt, 0, p->tile_cnt_bytes) != cudaSuccess) {
+    cudaFree(p->tile_cnt);
     cudaFree(p->dev);
     delete p;
     return ENGRAM_ERR_CUDA;
@@ -222,6 +231,8 @@ engram_status_t engram_plan_destroy(engram_plan_t* plan) {
   if (plan->timing)
     for (int i = 0; i < engram_plan::kMaxMarks; ++i) cudaEventDestroy(plan->marks[i]);
   cudaError_t e = cudaFree(plan->dev);
+  cudaError_t e2 = cudaFree(plan->tile_cnt);
+  if (e == cudaSuccess) e = e2;
   delete plan;
   return cuda_status(e);
 }
@@ -288,19 +299,15 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     v = ws.kv;
     sv = static_cast<int64_t>(M + 1) * d;
   } else {
-    if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
-                                 plan->num_sms, &plan->dev->err, s) != cudaSuccess)
-      return ENGRAM_ERR_CUDA;
-    mark(plan, s);
-    const int n_sl = engram::engram_partials_per_token(ntok, d, M, plan->num_sms) / (1 + 3 * M);
-    if (engram::launch_finalize(plan, ws.part, n_sl, ntok, ws.sa, s) != cudaSuccess)
+    if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part, ws.sa,
+                                 engram::sa_row_floats(M), plan->cfg.eps, plan->tile_cnt, plan->num_sms,
+                                 &plan->dev->err, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     v = ws.v32;
     sv = d;
   }
   mark(plan, s);
-  if (engram::launch_conv_residual(plan, v, sv, ws.sa, B, T, w->g_c, w->conv, H, state, s) !=
-      cudaSuccess)
+  if (engram::launch_conv_residual(plan, v, sv, ws.sa, B, T, w->g_c, w->conv, H, state, s) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
   mark(plan, s);
   if (state) {
@@ -400,7 +407,11 @@ engram_status_t engram_get_error(const engram_plan_t* plan, engram_stream_t stre
   if (cudaMemcpy(&plan->dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
   if (flags_out) *flags_out = bits;
-  if (bits & engram::kErrTimeout) return ENGRAM_ERR_TIMEOUT;
+  if (bits & engram::kErrTimeout) {
+    // a K/V GEMM that gave up may have left arrival counts behind
+    if (cudaMemset(plan->tile_cnt, 0, plan->tile_cnt_bytes) != cudaSuccess) return ENGRAM_ERR_CUDA;
+    return ENGRAM_ERR_TIMEOUT;
+  }
   if (bits & engram::kErrIndexRange) return ENGRAM_ERR_INDEX_RANGE;
   return ENGRAM_OK;
 }

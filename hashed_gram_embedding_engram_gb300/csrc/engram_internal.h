@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
 #include <vector>
 
 #include "../../include/engram.h"
@@ -51,6 +52,8 @@ struct engram_plan {
   std::vector<uint64_t> mults;
   std::vector<int64_t> offsets;
   engram::PlanDev* dev;            // device copy of the parameter block (its err word is live)
+  uint32_t* tile_cnt;              // K/V epilogue arrival counters, ceil(max_tokens/128) * 4, zero at rest
+  size_t tile_cnt_bytes;
   engram::PlanDev host;            // host copy, passed to kernels by value
   // tracing: events recorded around each kernel of the last engram_forward
   static constexpr int kMaxMarks = 8;
@@ -61,13 +64,31 @@ struct engram_plan {
 
 namespace engram {
 
+// Launch `k` with programmatic stream serialisation: its blocks may be
+// scheduled while the previous kernel on `s` drains; the kernel itself waits
+// (grid_dep_wait in ptx.cuh) before it reads or writes anything shared.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
 // Workspace carve-up for engram_forward / engram_stage_b, 256-byte aligned parts.
 struct Workspace {
   int32_t* idx;      // [ntok, R]
   void* e;           // [ntok, d_mem] act dtype
   float* kv;         // f32 layers: [ntok, (M+1)d] = [v | k^(1..M)]
   float* v32;        // bf16 layers: [ntok, d] v in fp32 (fused K/V epilogue)
-  float* part;       // bf16 layers: [ntok, (d/32)(1+3M)] gate partial sums (at most)
+  float* part;       // bf16 layers: gate partial sums, at most (d/32)(1+3M) per token (rows padded to 4)
   float* sa;         // [ntok, sa_row_floats(M)]: s^(1..M) = alpha/sqrt(mean(v~^2)+eps), then alpha^(1..M)
   size_t bytes;
 };
@@ -88,10 +109,8 @@ cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t nt
 int sa_row_floats(int M);
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
                             const float* g_k, float* sa, cudaStream_t s);
-// Gate partials of the fused K/V epilogue (n_sl slices) -> sa rows.
-cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* sa,
-                            cudaStream_t s);
-// Conv + SiLU + skip + residual over B sequences of T positions (v fp32 with row stride sv).
+// Conv + SiLU + skip + residual over B sequences of T positions (v fp32 with
+// row stride sv; sa rows [s^(1..M), alpha^(1..M)] per token).
 cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
                                  const float* g_c, const float* conv, void* H, const engram_state_t* state,
                                  cudaStream_t s);
@@ -103,12 +122,12 @@ cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const 
 cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,
                               uint32_t* err, cudaStream_t s);
 // The same GEMM with the Engram epilogue: v (columns [0,d)) to v32 in fp32,
-// gate partial sums of every tile to part; k is never stored.
+// gate partial sums of every tile to part and, once a row's partials are all
+// in, its gate scalars to sa (saw floats per row); k is never stored.  cnt:
+// ceil(Mr/128) * 4 zeroed counters, left zeroed by a launch that completes.
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
-                             const float* g_h, const float* g_k, float* v32, float* part, int num_sms, uint32_t* err,
-                             cudaStream_t s);
-// Partials per token gemm_bf16_engram writes for this shape: (d / (BN/2)) * (1 + 3M).
-int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms);
+                             const float* g_h, const float* g_k, float* v32, float* part, float* sa, int saw,
+                             float eps, uint32_t* cnt, int num_sms, uint32_t* err, cudaStream_t s);
 // 2-D tiled TMA descriptor of a row-major [rows, inner] array (fp32 or bf16),
 // rows row_stride_bytes apart, box of box_rows x box_inner elements.
 bool make_tensor_map_2d(CUtensorMap* map, const void* base, bool is_f32, uint64_t inner, uint64_t rows,

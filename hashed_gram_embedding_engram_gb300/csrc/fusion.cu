@@ -10,17 +10,15 @@
 // row per token, sa[t] = [s^(1..M), alpha^(1..M), pad] of saw = 4*ceil(2M/4)
 // floats: 16-byte rows that a TMA copy can move.
 //
-//   finalize_kernel   bf16 layers: one warp per token turns the gate partial
-//                     sums written by the K/V GEMM's epilogue (gemm.cu) into
-//                     the token's sa row.
 //   gate_kernel       fp32 layers: one warp per token computes the sa row from
 //                     the fp32 [v | k] buffer of the CUDA-core GEMM.
-//   conv_kernel       one thread per (token, 8 channels): the v rows of the W
-//                     taps (rows a token shares with its neighbours' taps come
-//                     from L1/L2), the ring history before a chunk, the scalar
-//                     rows and H are all loaded together; taps (times g_c) in
-//                     registers, compile-time dilation for w = 4 (the pages'
-//                     conv); SiLU, the skip and H += Y for every branch.
+//   conv_kernel       one thread per (chain of 4 outputs a dilation apart,
+//                     4 channels): loads the 7 v rows the chain's taps cover
+//                     once, with their s and the outputs' alpha (written by
+//                     the K/V GEMM's epilogue for bf16 layers, gemm.cu);
+//                     taps (times g_c) in registers, compile-time dilation for
+//                     w = 4 (the pages' conv); SiLU, the skip and H += Y for
+//                     every branch.
 //   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
 //                     (s * v) of the last (w-1)*dilation positions into the
 //                     ring, rolls the last N-1 projected ids, advances pos (a
@@ -31,7 +29,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "engram_internal.h"
+#include "gate.cuh"
+#include "ptx.cuh"
 
 namespace engram {
 namespace {
@@ -50,51 +52,8 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// logistic function; __frcp_rn is the correctly rounded reciprocal (same value as 1.f / x)
-__device__ __forceinline__ float sigmoidf(float x) { return __frcp_rn(1.f + expf(-x)); }
-
 // SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
-
-// s and alpha from the four sums of one (token, branch), into the token's sa row
-__device__ __forceinline__ void gate_scalars(float sv, float dot, float sk, float sh, float inv_d, float inv_sqrt_d,
-                                             float eps, float* sa_row, int M, int m) {
-  const float rh = 1.f / sqrtf(sh * inv_d + eps);
-  const float rk = 1.f / sqrtf(sk * inv_d + eps);
-  const float alpha = sigmoidf(dot * rh * rk * inv_sqrt_d);
-  sa_row[m] = alpha * (1.f / sqrtf(alpha * alpha * (sv * inv_d) + eps));
-  sa_row[M + m] = alpha;
-}
-
-// ------------------------------------------------------------------ gate (bf16 layers: from partials)
-__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int n_sl, int64_t ntok, int M,
-                                                       int d, float eps, float* __restrict__ sa, int saw) {
-  const int lane = threadIdx.x & 31;
-  const int P = n_sl * (1 + 3 * M);
-  const float inv_d = 1.f / static_cast<float>(d);
-  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
-  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
-       tok += n_warps) {
-    const float* p = part + tok * P;
-    float sv = 0.f;
-    for (int j = lane; j < n_sl; j += 32) sv += p[j];
-    sv = warp_sum(sv);
-    for (int m = 0; m < M; ++m) {
-      float dot = 0.f, sk = 0.f, sh = 0.f;
-      for (int j = lane; j < n_sl; j += 32) {
-        const float* q = p + n_sl + (m * n_sl + j) * 3;
-        dot += q[0];
-        sk += q[1];
-        sh += q[2];
-      }
-      dot = warp_sum(dot);
-      sk = warp_sum(sk);
-      sh = warp_sum(sh);
-      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, sa + tok * saw, M, m);
-    }
-  }
-}
 
 // ------------------------------------------------------------------ gate (fp32 layers)
 __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv, const float* __restrict__ H,
@@ -144,125 +103,198 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
 }
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
+constexpr int kConvThreads = 512;
+constexpr int kConvStages = 2;
+constexpr uint64_t kConvWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
+constexpr int kConvMaxCS = 256;                    // channels per tile: one TMA box row (<= 256 elements)
+
 struct ConvArgs {
-  int64_t sv;            // row stride of v (elements)
   int B, Tn, M, d, dil;
+  int S;                 // positions per tile
+  int CS;                // channels per tile
+  int h0;                // staged rows before a tile's first position: (w-1)*dil, or 0 if a sequence is one tile
+  int tiles_per_seq, n_ct, n_tiles;
   int saw;               // floats per sa row
+  uint32_t v_off, h_off, sa_off, stage_bytes, tx_bytes;   // shared-memory layout of one stage
   const float* g_c;      // [d]
   const float* conv;     // [d, W]
+  const float* ring;     // [B, L, M, d] or null
   const int32_t* pos;    // [B] (with a ring)
   int L;
+  uint32_t* err;
 };
 
-// 8 channels of H as floats (16-byte bf16 / 2 x 16-byte fp32 accesses)
+// 4 channels of H as floats
 template <typename T>
-struct H8;
+struct H4;
 template <>
-struct H8<__nv_bfloat16> {
+struct H4<__nv_bfloat16> {
   __device__ static void load(const __nv_bfloat16* p, float* out) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      out[2 * i] = __uint_as_float(w[i] << 16);
-      out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    out[0] = __uint_as_float(u.x << 16);
+    out[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    out[2] = __uint_as_float(u.y << 16);
+    out[3] = __uint_as_float(u.y & 0xFFFF0000u);
   }
   __device__ static void store(__nv_bfloat16* p, const float* in) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 v = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&v);
-    }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(in[2], in[3]);
+    *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
   }
 };
 template <>
-struct H8<float> {
-  __device__ static void load(const float* p, float* out) {
-    ld4(p, out);
-    ld4(p + 4, out + 4);
-  }
+struct H4<float> {
+  __device__ static void load(const float* p, float* out) { ld4(p, out); }
   __device__ static void store(float* p, const float* in) {
     *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
-    *reinterpret_cast<float4*>(p + 4) = make_float4(in[4], in[5], in[6], in[7]);
   }
 };
 
-// One thread per (token, 8 channels): grid x = token, grid y = block of 256
-// channel groups.  Every load a thread needs -- the v rows of its W taps (the
-// rows a token shares with its neighbours' taps come from L1/L2), the ring
-// history before a chunk, the scalars of the tap positions, H -- is
-// independent of the others and issued together.  DIL > 0: compile-time
-// dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
-template <typename TH, int W, int DIL>
-__global__ void __launch_bounds__(256, 3) conv_kernel(const ConvArgs a, const float* __restrict__ v,
-                                                   const float* __restrict__ sa, const float* __restrict__ ring,
-                                                   TH* __restrict__ H) {
-  const int g = blockIdx.y * blockDim.x + threadIdx.x;
-  if (g >= a.d / 8) return;
+// Persistent blocks over tiles of (S positions of one sequence, CS channels).
+// Each tile's inputs are staged in shared memory by three TMA copies -- the v
+// rows of its positions and of the (w-1)*dilation positions before them, the
+// H rows of every branch, the sa rows [s^(1..M), alpha^(1..M)] -- in a
+// two-stage ring, so the copies of the next tile overlap the arithmetic of
+// this one and each v row is read from memory about once.  Rows before a
+// sequence's start (negative coordinates, zero-filled by the copy engine, or
+// the previous sequence's rows) are never used: those taps come from the
+// caller's ring (RMSNorm(v~) before its weight) or are zero.  Threads map to
+// (4 channels, every npar-th position); taps (times g_c) in registers; SiLU,
+// the skip and H += Y for every branch, stored straight to H.
+// DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
+template <typename TH, int W, int DIL, int MC>
+__global__ void __launch_bounds__(kConvThreads, 1)
+    conv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
+                const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a, TH* __restrict__ H) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ uint64_t full[kConvStages];
+  __shared__ int s_ok;
   const int dil = DIL > 0 ? DIL : a.dil;
-  const int64_t tok = blockIdx.x;
-  const int b = static_cast<int>(static_cast<uint32_t>(blockIdx.x) / static_cast<uint32_t>(a.Tn));
-  const int t = static_cast<int>(blockIdx.x) - b * a.Tn;
-  const int M = a.M, d = a.d, c = 8 * g, saw = a.saw;
-  float vt[W][8];                                   // v rows of the tap positions inside the chunk
-#pragma unroll
-  for (int j = 0; j < W; ++j) {
-    const int lag = (W - 1 - j) * dil;
-    if (t - lag >= 0) {
-      const float* vp = v + (tok - lag) * a.sv + c;
-      ld4(vp, vt[j]);
-      ld4(vp + 4, vt[j] + 4);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) vt[j][i] = 0.f;
-    }
+  const int M = MC > 0 ? MC : a.M;
+  const int tid = threadIdx.x;
+
+  auto coords = [&](int tile, int& b, int& t0, int& c0) {
+    const int ct = tile % a.n_ct;
+    const int q = tile / a.n_ct;
+    b = q / a.tiles_per_seq;
+    t0 = (q - b * a.tiles_per_seq) * a.S;
+    c0 = ct * a.CS;
+  };
+  auto issue = [&](int tile, int stage) {          // one thread
+    int b, t0, c0;
+    coords(tile, b, t0, c0);
+    const int32_t row0 = b * a.Tn + t0 - a.h0;     // may be negative: zero fill
+    uint8_t* base = smem + stage * a.stage_bytes;
+    ptx::mbar_arrive_expect_tx(&full[stage], a.tx_bytes);
+    ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[stage], c0, row0);
+    ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[stage], c0, (b * a.Tn + t0) * M);
+    ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[stage], 0, row0);
+  };
+
+  if (tid == 0) {
+    for (int st = 0; st < kConvStages; ++st) ptx::mbar_init(&full[st], 1);
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tm_v);
+    ptx::tma_prefetch_desc(&tm_h);
+    ptx::tma_prefetch_desc(&tm_sa);
   }
-  float wq[8][W];                                   // taps times the RMSNorm weight g_c
-  {
-    float gc[8];
-    ld4(a.g_c + c, gc);
-    ld4(a.g_c + c + 4, gc + 4);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if constexpr (W == 4) {
-        ld4(a.conv + static_cast<int64_t>(c + i) * W, wq[i]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j);
-      }
-#pragma unroll
-      for (int j = 0; j < W; ++j) wq[i][j] *= gc[i];
-    }
+  __syncthreads();
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  if (tid == 0) {
+    for (int k = 0; k < kConvStages; ++k)
+      if (blockIdx.x + k * gridDim.x < static_cast<unsigned>(a.n_tiles)) issue(blockIdx.x + k * gridDim.x, k);
   }
-  const int p0 = ring != nullptr ? a.pos[b] : 0;
-  TH* hp = H + tok * M * static_cast<int64_t>(d) + c;
-  for (int m = 0; m < M; ++m) {
-    float h[8];
-    H8<TH>::load(hp + static_cast<int64_t>(m) * d, h);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+
+  const int ng = a.CS >> 2;                        // channel groups of a tile
+  const int npar = kConvThreads / ng;              // positions processed side by side
+  const int g = tid % ng, par0 = tid / ng;
+  uint32_t parity = 0;                             // bit per stage
+  int it = 0;
+  int tile = blockIdx.x;
+  for (; tile < a.n_tiles; tile += gridDim.x, ++it) {
+    const int stage = it % kConvStages;
+    const uint32_t ph = (parity >> stage) & 1u;
+    if (tid == 0) s_ok = ptx::mbar_wait_bounded(&full[stage], ph, kConvWaitNs) ? 1 : 0;
+    __syncthreads();
+    if (!s_ok) break;
+    for (int spin = 0; spin < (1 << 20) && !ptx::mbar_try_wait(&full[stage], ph); ++spin) {
+    }
+    parity ^= 1u << stage;
+
+    int b, t0, c0;
+    coords(tile, b, t0, c0);
+    const int nt = min(a.S, a.Tn - t0);
+    const uint8_t* base = smem + stage * a.stage_bytes;
+    const float* vs = reinterpret_cast<const float*>(base + a.v_off);    // [S + h0][CS], row r: position t0 - h0 + r
+    const TH* hs = reinterpret_cast<const TH*>(base + a.h_off);          // [S * M][CS]
+    const float* ss = reinterpret_cast<const float*>(base + a.sa_off);   // [S + h0][saw]
+    if (par0 < npar) {
+      const int c = c0 + 4 * g;
+      float wq[4][W];                                 // taps times g_c
+      {
+        float gc[4];
+        ld4(a.g_c + c, gc);
 #pragma unroll
-    for (int j = 0; j < W; ++j) {
-      const int lag = (W - 1 - j) * dil;
-      if (t - lag >= 0) {
-        const float sj = __ldg(sa + (tok - lag) * saw + m);
+        for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
-      } else if (ring != nullptr && p0 + t - lag >= 0) {
-        float u[8];                                 // the ring holds RMSNorm(v~) before its weight
-        const float* rp = ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * d + c;
-        ld4(rp, u);
-        ld4(rp + 4, u + 4);
+          for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
+        }
+      }
+      const int p0 = a.ring != nullptr ? a.pos[b] : 0;
+      for (int tt = par0; tt < nt; tt += npar) {
+        const int t = t0 + tt;
+        const int r = a.h0 + tt;
+        float vt[W][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+        for (int j = 0; j < W; ++j) {
+          const int lag = (W - 1 - j) * dil;
+          if (t - lag >= 0) {
+            ld4(vs + (r - lag) * a.CS + 4 * g, vt[j]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vt[j][i] = 0.f;
+          }
+        }
+        for (int m = 0; m < M; ++m) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < W; ++j) {
+            const int lag = (W - 1 - j) * dil;
+            if (t - lag >= 0) {
+              const float sj = ss[(r - lag) * a.saw + m];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
+            } else if (a.ring != nullptr && p0 + t - lag >= 0) {
+              float u[4];                             // the ring holds RMSNorm(v~) before its weight
+              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * a.d + c, u);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+            }
+          }
+          float h[4];
+          H4<TH>::load(hs + (tt * M + m) * a.CS + 4 * g, h);
+          const float at = ss[r * a.saw + M + m];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) h[i] = h[i] + (silu_fast(acc[i]) + at * vt[W - 1][i]);
+          H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t) * M + m) * a.d + c, h);
+        }
       }
     }
-    const float at = __ldg(sa + tok * saw + M + m);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] += silu_fast(acc[i]) + at * vt[W - 1][i];
-    H8<TH>::store(hp + static_cast<int64_t>(m) * d, h);
+    __syncthreads();                                  // the stage is consumed
+    if (tid == 0 && tile + kConvStages * static_cast<int>(gridDim.x) < a.n_tiles)
+      issue(tile + kConvStages * gridDim.x, stage);
+  }
+  if (tile < a.n_tiles && tid == 0) {
+    // a copy did not land in time: record it; the copies still in flight (this
+    // stage's and the next one's) must land before the block may exit
+    atomicOr(a.err, kErrTimeout);
+    for (int k = 0; k < kConvStages; ++k) {
+      const int st = (it + k) % kConvStages;
+      if (tile + k * static_cast<int>(gridDim.x) < a.n_tiles)
+        ptx::mbar_wait_bounded(&full[st], (parity >> st) & 1u, kConvWaitNs);
+    }
   }
 }
 
@@ -324,56 +356,77 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
+template <typename TH, int W, int DIL, int MC>
+cudaError_t conv_launch_m(const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts, const ConvArgs& a,
+                          int grid, size_t smem, void* H, cudaStream_t s) {
+  static size_t attr_bytes = 0;    // per template instance: the dynamic shared memory opted into so far
+  if (smem > attr_bytes) {
+    const cudaError_t e = cudaFuncSetAttribute(conv_kernel<TH, W, DIL, MC>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_bytes = smem;
+  }
+  return launch_pdl(conv_kernel<TH, W, DIL, MC>, dim3(grid), dim3(kConvThreads), smem, s, tv, th, ts, a,
+                    static_cast<TH*>(H));
+}
+
+// single-branch layers with a compile-time dilation get a compile-time M = 1
 template <typename TH, int W, int DIL>
-cudaError_t conv_launch(const engram_plan* p, ConvArgs a, const float* v, int64_t sv, const float* sa,
-                        const float* ring, void* H, cudaStream_t s) {
-  (void)p;
-  a.sv = sv;
-  const int groups = a.d / 8;
-  const dim3 grid(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.Tn), (groups + 255) / 256);
-  conv_kernel<TH, W, DIL><<<grid, 256, 0, s>>>(a, v, sa, ring, static_cast<TH*>(H));
-  return cudaGetLastError();
+cudaError_t conv_launch(const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts, const ConvArgs& a,
+                        int grid, size_t smem, void* H, cudaStream_t s) {
+  if (DIL > 0 && a.M == 1) return conv_launch_m<TH, W, DIL, 1>(tv, th, ts, a, grid, smem, H, s);
+  return conv_launch_m<TH, W, DIL, 0>(tv, th, ts, a, grid, smem, H, s);
 }
 
 template <typename TH>
-cudaError_t conv_dispatch(const engram_plan* p, const ConvArgs& a, const float* v, int64_t sv, const float* sa,
-                          const float* ring, void* H, cudaStream_t s) {
-  if (p->cfg.conv_w == 4) {
+cudaError_t conv_dispatch(int conv_w, const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts,
+                          const ConvArgs& a, int grid, size_t smem, void* H, cudaStream_t s) {
+#define ENGRAM_CONV(Wv, Dv) conv_launch<TH, Wv, Dv>(tv, th, ts, a, grid, smem, H, s)
+  if (conv_w == 4) {
     switch (a.dil) {   // the pages' short conv: w = 4, dilation = max n-gram order
-      case 1: return conv_launch<TH, 4, 1>(p, a, v, sv, sa, ring, H, s);
-      case 2: return conv_launch<TH, 4, 2>(p, a, v, sv, sa, ring, H, s);
-      case 3: return conv_launch<TH, 4, 3>(p, a, v, sv, sa, ring, H, s);
-      case 4: return conv_launch<TH, 4, 4>(p, a, v, sv, sa, ring, H, s);
-      case 5: return conv_launch<TH, 4, 5>(p, a, v, sv, sa, ring, H, s);
-      case 6: return conv_launch<TH, 4, 6>(p, a, v, sv, sa, ring, H, s);
-      case 7: return conv_launch<TH, 4, 7>(p, a, v, sv, sa, ring, H, s);
-      case 8: return conv_launch<TH, 4, 8>(p, a, v, sv, sa, ring, H, s);
+      case 1: return ENGRAM_CONV(4, 1);
+      case 2: return ENGRAM_CONV(4, 2);
+      case 3: return ENGRAM_CONV(4, 3);
+      case 4: return ENGRAM_CONV(4, 4);
+      case 5: return ENGRAM_CONV(4, 5);
+      case 6: return ENGRAM_CONV(4, 6);
+      case 7: return ENGRAM_CONV(4, 7);
+      case 8: return ENGRAM_CONV(4, 8);
       default: break;
     }
   }
-  switch (p->cfg.conv_w) {
-    case 1: return conv_launch<TH, 1, 0>(p, a, v, sv, sa, ring, H, s);
-    case 2: return conv_launch<TH, 2, 0>(p, a, v, sv, sa, ring, H, s);
-    case 3: return conv_launch<TH, 3, 0>(p, a, v, sv, sa, ring, H, s);
-    case 4: return conv_launch<TH, 4, 0>(p, a, v, sv, sa, ring, H, s);
-    case 5: return conv_launch<TH, 5, 0>(p, a, v, sv, sa, ring, H, s);
-    case 6: return conv_launch<TH, 6, 0>(p, a, v, sv, sa, ring, H, s);
-    case 7: return conv_launch<TH, 7, 0>(p, a, v, sv, sa, ring, H, s);
-    case 8: return conv_launch<TH, 8, 0>(p, a, v, sv, sa, ring, H, s);
+  switch (conv_w) {
+    case 1: return ENGRAM_CONV(1, 0);
+    case 2: return ENGRAM_CONV(2, 0);
+    case 3: return ENGRAM_CONV(3, 0);
+    case 4: return ENGRAM_CONV(4, 0);
+    case 5: return ENGRAM_CONV(5, 0);
+    case 6: return ENGRAM_CONV(6, 0);
+    case 7: return ENGRAM_CONV(7, 0);
+    case 8: return ENGRAM_CONV(8, 0);
     default: return cudaErrorInvalidValue;
   }
+#undef ENGRAM_CONV
+}
+
+uint32_t round128(uint32_t x) { return (x + 127u) & ~127u; }
+
+// Shared-memory layout of one stage for a tile of S positions and CS channels.
+void conv_layout(ConvArgs& a, size_t act_bytes) {
+  const uint32_t rows = static_cast<uint32_t>(a.S + a.h0);
+  const uint32_t vb = rows * a.CS * 4u;
+  const uint32_t hb = static_cast<uint32_t>(a.S * a.M * a.CS) * static_cast<uint32_t>(act_bytes);
+  const uint32_t sb = rows * static_cast<uint32_t>(a.saw) * 4u;
+  a.v_off = 0;
+  a.h_off = round128(vb);
+  a.sa_off = round128(a.h_off + hb);
+  a.stage_bytes = round128(a.sa_off + sb);
+  a.tx_bytes = vb + hb + sb;
 }
 
 }  // namespace
 
 int sa_row_floats(int M) { return (2 * M + 3) / 4 * 4; }
-
-cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int64_t ntok, float* sa,
-                            cudaStream_t s) {
-  finalize_kernel<<<grid_for(ntok * 32, 256, p->num_sms), 256, 0, s>>>(part, n_sl, ntok, p->cfg.M, p->cfg.d,
-                                                                       p->cfg.eps, sa, sa_row_floats(p->cfg.M));
-  return cudaGetLastError();
-}
 
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
                             const float* g_k, float* sa, cudaStream_t s) {
@@ -394,11 +447,85 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.saw = sa_row_floats(p->cfg.M);
   a.g_c = g_c;
   a.conv = conv;
+  a.ring = state ? state->u_ring : nullptr;
   a.pos = state ? state->pos : nullptr;
   a.L = p->L_ring;
-  const float* ring = state ? state->u_ring : nullptr;
-  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p, a, v, sv, sa, ring, H, s);
-  return conv_dispatch<__nv_bfloat16>(p, a, v, sv, sa, ring, H, s);
+  a.err = &p->dev->err;
+  const bool f32 = p->cfg.act_dtype == ENGRAM_F32;
+  const size_t act = f32 ? 4 : 2;
+  const int halo = (p->cfg.conv_w - 1) * a.dil;
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  if (ntok * a.M > INT32_MAX) return cudaErrorInvalidValue;
+  // Tile shape.  Channels per tile CS: the widest (<= 256, dividing d) whose
+  // tile keeps at least 2/3 of its staged v rows useful (S / (S + halo)),
+  // else the one with the best share; S: as many positions as two stages
+  // hold (S * M <= 256 and S + halo <= 256: one TMA box each), the whole
+  // sequence if it fits.  Then S is lowered (not below 2 * halo) so the tile
+  // count fills whole waves of the SMs.
+  const int64_t budget = (227 * 1024 - 1024) / kConvStages - 3 * 128;
+  int S = 0, smax_halo = 0;
+  double best = -1.0;
+  for (int cs = kConvMaxCS; cs >= 4; cs >>= 1) {
+    if (a.d % cs || (static_cast<size_t>(cs) * act) % 16) continue;
+    const int64_t per_row = static_cast<int64_t>(cs) * 4 + a.saw * 4;   // v and sa of one staged position
+    const int64_t per_pos = per_row + static_cast<int64_t>(a.M) * cs * static_cast<int64_t>(act);
+    const int64_t box_cap = std::min<int64_t>(256 / a.M, 256);
+    const int64_t s_no_halo = std::min<int64_t>(budget / per_pos, box_cap);
+    const int64_t s_halo = std::min<int64_t>(std::max<int64_t>((budget - halo * per_row) / per_pos, 0),
+                                             std::min<int64_t>(box_cap, 256 - halo));
+    int sc;
+    double score;
+    if (T <= s_no_halo) {
+      sc = T;
+      score = 1.0;
+    } else if (s_halo >= 1) {
+      sc = static_cast<int>(s_halo);
+      score = static_cast<double>(sc) / (sc + halo);
+    } else {
+      continue;
+    }
+    if (score > best + 1e-9) {
+      best = score;
+      a.CS = cs;
+      S = sc;
+      smax_halo = static_cast<int>(s_halo);
+    }
+    if (best >= 2.0 / 3.0) break;
+  }
+  if (S == 0) return cudaErrorInvalidValue;
+  a.n_ct = a.d / a.CS;
+  {
+    const int64_t lanes = static_cast<int64_t>(B) * a.n_ct;
+    const int64_t tiles = lanes * ((T + S - 1) / S);
+    const int64_t waves = (tiles + p->num_sms - 1) / p->num_sms;
+    const int64_t per_seq = (waves * p->num_sms + lanes - 1) / lanes;
+    int s2 = static_cast<int>((T + per_seq - 1) / per_seq);
+    s2 = std::max(s2, std::min(S, 2 * halo));
+    if (s2 < S && s2 <= smax_halo) S = s2;
+  }
+  a.S = S;
+  a.tiles_per_seq = (T + S - 1) / S;
+  a.h0 = a.tiles_per_seq > 1 ? halo : 0;
+  const int64_t n_tiles = static_cast<int64_t>(B) * a.tiles_per_seq * a.n_ct;
+  if (n_tiles > INT32_MAX) return cudaErrorInvalidValue;
+  a.n_tiles = static_cast<int>(n_tiles);
+  conv_layout(a, act);
+  const size_t smem = static_cast<size_t>(kConvStages) * a.stage_bytes + 128;
+
+  CUtensorMap tv, th, ts;
+  if (!make_tensor_map_2d(&tv, v, true, static_cast<uint64_t>(a.d), static_cast<uint64_t>(ntok),
+                          static_cast<uint64_t>(sv) * 4, static_cast<uint32_t>(a.CS),
+                          static_cast<uint32_t>(a.S + a.h0), false) ||
+      !make_tensor_map_2d(&th, H, f32, static_cast<uint64_t>(a.d), static_cast<uint64_t>(ntok * a.M),
+                          static_cast<uint64_t>(a.d) * act, static_cast<uint32_t>(a.CS),
+                          static_cast<uint32_t>(a.S * a.M), false) ||
+      !make_tensor_map_2d(&ts, sa, true, static_cast<uint64_t>(a.saw), static_cast<uint64_t>(ntok),
+                          static_cast<uint64_t>(a.saw) * 4, static_cast<uint32_t>(a.saw),
+                          static_cast<uint32_t>(a.S + a.h0), false))
+    return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, p->num_sms));
+  if (f32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, s);
+  return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, s);
 }
 
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,

@@ -25,6 +25,7 @@
 
 #include "engram_internal.h"
 #include "hashing.cuh"
+#include "ptx.cuh"
 
 namespace engram {
 namespace {
@@ -86,6 +87,8 @@ __global__ void __launch_bounds__(kThreads)
     s_mo[r] = pd.mult_base[n] + k * n;
   }
   __syncthreads();
+  ptx::grid_dep_wait();       // the set-up above (parameters only) overlaps the previous kernel
+  ptx::grid_dep_launch();
 
   constexpr int kRowBytes = kCpr * 16;
   const int lane = threadIdx.x & 31;
@@ -181,20 +184,21 @@ int grid_for_tokens(const engram_plan* p, int64_t ntok) {
 template <int kCpr, bool kInt8>
 cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
                        const uint16_t* scales, void* e, cudaStream_t s) {
-  row_gather_kernel<kCpr, kInt8, false><<<grid_for_tokens(p, ntok), kThreads, 0, s>>>(
-      p->host, &p->dev->err, idx, nullptr, 1, nullptr, 0, nullptr, ntok, static_cast<const uint8_t*>(table),
-      reinterpret_cast<const __half*>(scales), static_cast<uint4*>(e));
-  return cudaGetLastError();
+  return launch_pdl(row_gather_kernel<kCpr, kInt8, false>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+                    p->host, &p->dev->err, static_cast<const int32_t*>(idx), static_cast<const int32_t*>(nullptr), 1,
+                    static_cast<const int32_t*>(nullptr), 0, static_cast<const int32_t*>(nullptr), ntok,
+                    static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
+                    static_cast<uint4*>(e));
 }
 
 template <int kCpr, bool kInt8>
 cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                          const int32_t* prev, const void* table, const uint16_t* scales, void* e, cudaStream_t s) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
-  row_gather_kernel<kCpr, kInt8, true><<<grid_for_tokens(p, ntok), kThreads, 0, s>>>(
-      p->host, &p->dev->err, nullptr, ids, T, proj, V, prev, ntok, static_cast<const uint8_t*>(table),
-      reinterpret_cast<const __half*>(scales), static_cast<uint4*>(e));
-  return cudaGetLastError();
+  return launch_pdl(row_gather_kernel<kCpr, kInt8, true>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+                    p->host, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T, proj, V, prev, ntok,
+                    static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
+                    static_cast<uint4*>(e));
 }
 
 int chunks_per_row(const engram_plan* p) {

@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "engram_internal.h"
+#include "gate.cuh"
 #include "ptx.cuh"
 
 namespace engram {
@@ -50,9 +51,14 @@ struct EngramEpilogue {
   const __nv_bfloat16* H;         // [Mr, M, d]
   const float* g_h;               // [M, d]
   const float* g_k;               // [M, d]
+  float* sa;                      // [Mr, saw]: s^(1..M), alpha^(1..M)
+  uint32_t* cnt;                  // [ceil(Mr/128) * 4] arrivals per (row tile, lane quadrant), zero between launches
+  float eps;
+  int saw;
   int d;
   int M;
   int n_sl;                       // d / (BN / 2): column slices per row of v
+  int pstride;                    // floats per row of part: n_sl * (1 + 3M) rounded up to 4
 };
 
 struct Bars {
@@ -80,6 +86,133 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
+// In-lane sum of the n values p[i * stride] as the adjacent pairwise tree over
+// the values zero-padded to a power of two: a stack of finished subtrees,
+// merged as a binary counter carries, folded right to left at the end.  The
+// loads go out eight at a time.
+__device__ __forceinline__ void tree_push(float* stk, int& top, float x, int i) {
+  for (int k = i; k & 1; k >>= 1) x = stk[--top] + x;
+  stk[top++] = x;
+}
+
+__device__ __forceinline__ float tree_fold(float* stk, int top) {
+  for (; top > 1; --top) stk[top - 2] = stk[top - 2] + stk[top - 1];
+  return top ? stk[0] : 0.f;
+}
+
+__device__ __forceinline__ float tree_sum(const float* p, int n) {
+  float stk[24];
+  int top = 0;
+  for (int i0 = 0; i0 < n; i0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = i0 + j < n ? __ldcg(p + i0 + j) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (i0 + j < n) tree_push(stk, top, x[j], i0 + j);
+  }
+  return tree_fold(stk, top);
+}
+
+// the same for the three interleaved sums (x, y, z) of p[3i], p[3i+1], p[3i+2]
+__device__ __forceinline__ void tree_sum3(const float* p, int n, float& x, float& y, float& z) {
+  float sx[24], sy[24], sz[24];
+  int tx = 0, ty = 0, tz = 0;
+  for (int i0 = 0; i0 < n; i0 += 8) {
+    float a[8][3];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int q = 0; q < 3; ++q) a[j][q] = i0 + j < n ? __ldcg(p + 3 * (i0 + j) + q) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (i0 + j < n) {
+        tree_push(sx, tx, a[j][0], i0 + j);
+        tree_push(sy, ty, a[j][1], i0 + j);
+        tree_push(sz, tz, a[j][2], i0 + j);
+      }
+    }
+  }
+  x = tree_fold(sx, tx);
+  y = tree_fold(sy, ty);
+  z = tree_fold(sz, tz);
+}
+
+// Adjacent pairwise tree over N (a power of two) values in registers.
+template <int N>
+__device__ __forceinline__ float tree_reg(float* x) {
+#pragma unroll
+  for (int w = 1; w < N; w *= 2)
+#pragma unroll
+    for (int i = 0; i + w < N; i += 2 * w) x[i] = x[i] + x[i + w];
+  return x[0];
+}
+
+// N floats from 16-byte aligned p (N a multiple of 4), all loads issued together
+template <int N>
+__device__ __forceinline__ void load_cg(const float* p, float* x) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(p) + i);
+      x[4 * i] = q.x;
+      x[4 * i + 1] = q.y;
+      x[4 * i + 2] = q.z;
+      x[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = __ldcg(p + i);
+  }
+}
+
+// The gate scalars of one row from its partial sums (layout below), into sa.
+// NSL > 0: a compile-time power-of-two slice count (registers only); 0: any.
+template <int NSL>
+__device__ __forceinline__ void finalize_row(const EngramEpilogue& epi, int row) {
+  const int M = epi.M;
+  const float* p = epi.part + static_cast<int64_t>(row) * epi.pstride;
+  const float inv_d = 1.f / static_cast<float>(epi.d);
+  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(epi.d));
+  float* sa_row = epi.sa + static_cast<int64_t>(row) * epi.saw;
+  if constexpr (NSL > 0) {
+    float xv[NSL], xk[3 * NSL];
+    load_cg<NSL>(p, xv);
+    load_cg<3 * NSL>(p + NSL, xk);
+    const float sv = tree_reg<NSL>(xv);
+    for (int m = 0; m < M; ++m) {
+      if (m > 0) load_cg<3 * NSL>(p + NSL + m * 3 * NSL, xk);
+      float d0[NSL], d1[NSL], d2[NSL];
+#pragma unroll
+      for (int i = 0; i < NSL; ++i) {
+        d0[i] = xk[3 * i];
+        d1[i] = xk[3 * i + 1];
+        d2[i] = xk[3 * i + 2];
+      }
+      gate_scalars(sv, tree_reg<NSL>(d0), tree_reg<NSL>(d1), tree_reg<NSL>(d2), inv_d, inv_sqrt_d, epi.eps, sa_row,
+                   M, m);
+    }
+  } else {
+    const int n = epi.n_sl;
+    const float sv = tree_sum(p, n);
+    for (int m = 0; m < M; ++m) {
+      float dot, sk, sh;
+      tree_sum3(p + n + m * n * 3, n, dot, sk, sh);
+      gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, epi.eps, sa_row, M, m);
+    }
+  }
+}
+
+__device__ __forceinline__ void finalize_row_any(const EngramEpilogue& epi, int row) {
+  switch (epi.n_sl) {
+    case 4: finalize_row<4>(epi, row); break;
+    case 8: finalize_row<8>(epi, row); break;
+    case 16: finalize_row<16>(epi, row); break;
+    case 32: finalize_row<32>(epi, row); break;
+    default: finalize_row<0>(epi, row); break;
+  }
+}
+
 // Engram epilogue of the K/V projection (Steps 5-6 fused).  Output columns
 // [0, d) are v: stored in fp32 with a per-slice partial of sum(v^2).  Columns
 // [(1+m)d, (2+m)d) are k^(m): never stored; each slice contributes the partial
@@ -89,34 +222,36 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 // n_sl = d / (BN/2) slices per row of v (and of each k^(m)), token t has
 // part[t*P + j] = sum v^2 of v slice j, and
 // part[t*P + n_sl + (m*n_sl + j)*3 + {0,1,2}] = (dot, sk, sh) of k^(m) slice j.
+// Each sum is a sequential fmaf chain over the 32 columns of one tcgen05.ld
+// chunk; a slice's chunks are combined as an adjacent pairwise tree, which
+// finalize_row continues over the slices, so the gate's sums have the same
+// bits for every tile width BN.  The last of the 2 * n_tiles warps that write
+// partials for a (row tile, lane quadrant) -- an atomic count, no waiting --
+// finalises those 32 rows into sa.
 template <int BN>
-__device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0,
+__device__ __forceinline__ void fused_partials(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0,
                                                int c_lo) {
   constexpr int SW = BN / 2;
+  constexpr int kChunks = SW / 32;          // 1, 2 or 4
   const int d = epi.d;
-  const int P = epi.n_sl * (1 + 3 * epi.M);
+  const int P = epi.pstride;
   if (n0 < d) {
-    float sv = 0.f;
-#pragma unroll 1
-    for (int c = c_lo; c < c_lo + SW; c += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld_32x32b_x32(t_row + c, r);
-      ptx::tmem_ld_wait();
-      if (row < Mr) {
-        float4* dst = reinterpret_cast<float4*>(epi.v32 + static_cast<int64_t>(row) * d + n0 + c);
+    // v tile, first pass: the slice's sum of v^2 (the values are stored in a second pass)
+    float stk[3];
+    int top = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 q = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-          dst[j] = q;
-          sv = fmaf(q.x, q.x, sv);
-          sv = fmaf(q.y, q.y, sv);
-          sv = fmaf(q.z, q.z, sv);
-          sv = fmaf(q.w, q.w, sv);
-        }
-      }
+    for (int ci = 0; ci < kChunks; ++ci) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(t_row + c_lo + ci * 32, r);
+      ptx::tmem_ld_wait();
+      float sv = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sv = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), sv);
+#pragma unroll
+      for (int k = ci; k & 1; k >>= 1) sv = stk[--top] + sv;
+      stk[top++] = sv;
     }
-    if (row < Mr) epi.part[static_cast<int64_t>(row) * P + (n0 + c_lo) / SW] = sv;
+    if (row < Mr) epi.part[static_cast<int64_t>(row) * P + (n0 + c_lo) / SW] = stk[0];
   } else {
     const int m = (n0 - d) / d;
     const int col = n0 - d - m * d;
@@ -124,19 +259,30 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32
     const __nv_bfloat16* hrow = epi.H + (static_cast<int64_t>(row) * epi.M + m) * d + col;
     const float* gh = epi.g_h + static_cast<int64_t>(m) * d + col;
     const float* gk = epi.g_k + static_cast<int64_t>(m) * d + col;
-    float dot = 0.f, sk = 0.f, sh = 0.f;
-#pragma unroll 1
-    for (int c = c_lo; c < c_lo + SW; c += 32) {
+    float s_dot[3], s_sk[3], s_sh[3];
+    int top = 0;
+    uint4 hcur[4], hnext[4];               // H of this chunk; the next chunk's loads are in flight
+    if (row < Mr) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) hcur[q4] = __ldg(reinterpret_cast<const uint4*>(hrow + c_lo) + q4);
+    }
+#pragma unroll
+    for (int ci = 0; ci < kChunks; ++ci) {
+      const int c = c_lo + ci * 32;
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
+      if (ci + 1 < kChunks && row < Mr) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) hnext[q4] = __ldg(reinterpret_cast<const uint4*>(hrow + c + 32) + q4);
+      }
+      float dot = 0.f, sk = 0.f, sh = 0.f;
       if (row < Mr) {
-        const uint4* hp = reinterpret_cast<const uint4*>(hrow + c);
         const float4* gh4 = reinterpret_cast<const float4*>(gh + c);
         const float4* gk4 = reinterpret_cast<const float4*>(gk + c);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 hv = __ldg(hp + q4);
+          const uint4 hv = hcur[q4];
           const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
           const float4 ga = __ldg(gh4 + 2 * q4), gb = __ldg(gh4 + 2 * q4 + 1);
           const float4 ka = __ldg(gk4 + 2 * q4), kb = __ldg(gk4 + 2 * q4 + 1);
@@ -152,12 +298,48 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, uint32
           }
         }
       }
+      if (ci + 1 < kChunks) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) hcur[q4] = hnext[q4];
+      }
+#pragma unroll
+      for (int k = ci; k & 1; k >>= 1) {
+        --top;
+        dot = s_dot[top] + dot;
+        sk = s_sk[top] + sk;
+        sh = s_sh[top] + sh;
+      }
+      s_dot[top] = dot;
+      s_sk[top] = sk;
+      s_sh[top] = sh;
+      ++top;
     }
     if (row < Mr) {
       float* dst = epi.part + static_cast<int64_t>(row) * P + epi.n_sl + (m * epi.n_sl + j) * 3;
-      dst[0] = dot;
-      dst[1] = sk;
-      dst[2] = sh;
+      dst[0] = s_dot[0];
+      dst[1] = s_sk[0];
+      dst[2] = s_sh[0];
+    }
+  }
+}
+
+// v tile, second pass: the values to v32 in fp32 (one 128-byte line per lane per chunk)
+template <int BN>
+__device__ __forceinline__ void store_v(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0,
+                                        int c_lo) {
+  constexpr int kChunks = BN / 64;
+#pragma unroll
+  for (int ci = 0; ci < kChunks; ++ci) {
+    const int c = c_lo + ci * 32;
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(t_row + c, r);
+    ptx::tmem_ld_wait();
+    if (row < Mr) {
+      float4* dst = reinterpret_cast<float4*>(epi.v32 + static_cast<int64_t>(row) * epi.d + n0 + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                             __uint_as_float(r[4 * j + 3]));
     }
   }
 }
@@ -204,6 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // the set-up above overlaps the previous kernel's tail; e, W_kv and H are read only after this
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -286,9 +471,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_tiles) * kBM;
       const int n0 = (tile % n_tiles) * BN;
+      const int row = m0 + q * 32 + lane;
+      if constexpr (kFused) {
+        // a k tile reads this row's H slice after its MMAs: pull it into L2 meanwhile
+        if (n0 >= epi.d && row < Mr) {
+          const int m = (n0 - epi.d) / epi.d;
+          const char* hp = reinterpret_cast<const char*>(
+              epi.H + (static_cast<int64_t>(row) * epi.M + m) * epi.d + (n0 - epi.d - m * epi.d) + c_lo);
+#pragma unroll
+          for (int off = 0; off < BN; off += 128) ptx::prefetch_l2(hp + off);
+        }
+      }
       if (!wait_or_abort(&bars->tfull[acc], acc_phase, bars, err)) break;
       ptx::tc_fence_after();
-      const int row = m0 + q * 32 + lane;
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       if constexpr (!kFused) {
 #pragma unroll 1
@@ -309,12 +504,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
           }
         }
-      } else {
-        fused_epilogue<BN>(epi, t_row, row, Mr, n0, c_lo);
+      }
+      uint32_t last = 0;
+      if constexpr (kFused) {
+        fused_partials<BN>(epi, t_row, row, Mr, n0, c_lo);
+        __threadfence();                       // this lane's partials, before the count
+        __syncwarp();
+        if (lane == 0)
+          last = atomicAdd(epi.cnt + (m0 / kBM) * 4 + q, 1u) == 2u * static_cast<uint32_t>(n_tiles) - 1u;
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (n0 < epi.d) store_v<BN>(epi, t_row, row, Mr, n0, c_lo);
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->tempty[acc]);
+      if constexpr (kFused) {
+        if (last) {                            // every partial of these 32 rows is in
+          __threadfence();
+          if (lane == 0) epi.cnt[(m0 / kBM) * 4 + q] = 0;
+          if (row < Mr) finalize_row_any(epi, row);
+        }
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -350,10 +560,12 @@ cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int K
   }
   const int64_t tiles = ((Mr + kBM - 1) / kBM) * ((Nc + BN - 1) / BN);
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  if constexpr (kFused) epi.n_sl = epi.d / (BN / 2);
-  gemm_bf16_kernel<BN, kFused><<<grid, kThreads, G::kSmem, s>>>(ta, tb, static_cast<__nv_bfloat16*>(C),
-                                                                static_cast<int>(Mr), Nc, Kd, err, epi);
-  return cudaGetLastError();
+  if constexpr (kFused) {
+    epi.n_sl = epi.d / (BN / 2);
+    epi.pstride = (epi.n_sl * (1 + 3 * epi.M) + 3) / 4 * 4;
+  }
+  return launch_pdl(gemm_bf16_kernel<BN, kFused>, dim3(grid), dim3(kThreads), G::kSmem, s, ta, tb,
+                    static_cast<__nv_bfloat16*>(C), static_cast<int>(Mr), Nc, Kd, err, epi);
 }
 
 // Widest N tile (256, 128, 64) that divides `div` and still gives every SM a tile.
@@ -423,21 +635,16 @@ cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr,
 }
 
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
-                             const float* g_h, const float* g_k, float* v32, float* part, int num_sms, uint32_t* err,
-                             cudaStream_t s) {
+                             const float* g_h, const float* g_k, float* v32, float* part, float* sa, int saw,
+                             float eps, uint32_t* cnt, int num_sms, uint32_t* err, cudaStream_t s) {
   const int Nc = (M + 1) * d;
   if (d % 64 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
-  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0};
+  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, sa, cnt, eps, saw, d, M, 0, 0};
   switch (pick_bn(Mr, Nc, d, num_sms)) {
     case 256: return run<256, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
     case 128: return run<128, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
     default: return run<64, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
   }
-}
-
-int engram_partials_per_token(int64_t Mr, int d, int M, int num_sms) {
-  const int bn = pick_bn(Mr, (M + 1) * d, d, num_sms);
-  return (d / (bn / 2)) * (1 + 3 * M);
 }
 
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s) {

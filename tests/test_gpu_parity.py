@@ -223,6 +223,35 @@ def test_chunked_prefill_with_ragged_chunks():
     assert torch.equal(out.view(torch.int16), full.view(torch.int16))
 
 
+def test_streaming_bit_identical_across_gemm_tile_widths():
+    """2560 tokens at d = 1024 give the K/V GEMM 20 x 8 tiles of 128 x 256; chunks of
+    100 tokens run it with 128 x 64 tiles.  The gate's partial sums are combined as
+    one pairwise tree over 32-column chunks either way, so the outputs agree bit
+    for bit; the oracle checks a sample of positions."""
+    from hashed_gram_embedding_engram_gb300 import EngramState
+    w = W.PREFILL_BF16.scaled(B=1, T=2560, V=5000, V_proj=3850, prime_target=4001)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    full = H.clone()
+    plan.forward(ids_d, proj, weights, full)
+    st = EngramState.zeros(plan, w.B)
+    out = H.clone()
+    for t0 in range(0, w.T, 100):
+        t1 = min(t0 + 100, w.T)
+        seg = out[:, t0:t1].contiguous()
+        plan.forward(ids_d[:, t0:t1].contiguous(), proj, weights, seg, st)
+        out[:, t0:t1] = seg
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(out.view(torch.int16), full.view(torch.int16))
+    pos = [(0, t) for t in (0, 1, 2, 9, 10, 11, 127, 128, 1000, 2047, 2048, 2559)]
+    ref = O.forward_at(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype, pos)
+    got = np.stack([act_to_f64(full[b, t]) for b, t in pos])
+    assert_close(got, ref, "bf16", "sampled")
+
+
 # --------------------------------------------------------------------------- #
 # UVA: host-resident tables
 # --------------------------------------------------------------------------- #
