@@ -132,8 +132,10 @@ def per_token_work(w, bn: int = 256) -> dict:
         "hash_gather": ("bytes", 4 + 4 + w.R * row_bytes + act * w.d_mem),
         # e . [W_V; W_K^(1..M)]^T
         "kv_gemm": ("flops", 2 * w.d_mem * nc),
-        # v (fp32), the gate partials, H in; H and the (alpha, scale) row out
-        "conv": ("bytes", 4 * w.d + 4 * n_part + 8 * w.M + 2 * act * w.M * w.d),
+        # gate partials in; the (scale, alpha) row out
+        "finalize": ("bytes", 4 * n_part + 8 * w.M),
+        # v (fp32), the (scale, alpha) row, H in; H out
+        "conv": ("bytes", 4 * w.d + 8 * w.M + 2 * act * w.M * w.d),
     }
 
 
@@ -223,7 +225,7 @@ def run_ours(args) -> None:
 
     # ---- per-kernel durations: the plan's tracing events around each kernel of engram_forward ----
     Kb = min(K, 200)
-    names = ["hash_gather", "kv_gemm", "conv"]
+    names = ["hash_gather", "kv_gemm", "finalize", "conv"]
     dur = {n: [] for n in names}
     for ly in layers:
         ly["plan"].set_timing(True)

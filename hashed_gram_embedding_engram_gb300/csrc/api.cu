@@ -209,15 +209,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
     delete p;
     return ENGRAM_ERR_CUDA;
   }
-  p->tile_cnt_bytes = static_cast<size_t>((max_tokens + 127) / 128) * 4 * sizeof(uint32_t);
-  if (cudaMalloc(&p->tile_cnt, p->tile_cnt_bytes) != cudaSuccess) {
-    cudaFree(p->dev);
-    delete p;
-    return ENGRAM_ERR_CUDA;
-  }
-  if (cudaMemcpy(p->dev, &h, sizeof(PlanDev), cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(p->tile_cnt, 0, p->tile_cnt_bytes) != cudaSuccess) {
-    cudaFree(p->tile_cnt);
+  if (cudaMemcpy(p->dev, &h, sizeof(PlanDev), cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaFree(p->dev);
     delete p;
     return ENGRAM_ERR_CUDA;
@@ -231,8 +223,6 @@ engram_status_t engram_plan_destroy(engram_plan_t* plan) {
   if (plan->timing)
     for (int i = 0; i < engram_plan::kMaxMarks; ++i) cudaEventDestroy(plan->marks[i]);
   cudaError_t e = cudaFree(plan->dev);
-  cudaError_t e2 = cudaFree(plan->tile_cnt);
-  if (e == cudaSuccess) e = e2;
   delete plan;
   return cuda_status(e);
 }
@@ -299,10 +289,12 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     v = ws.kv;
     sv = static_cast<int64_t>(M + 1) * d;
   } else {
-    if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part, ws.sa,
-                                 engram::sa_row_floats(M), plan->cfg.eps, plan->tile_cnt, plan->num_sms,
-                                 &plan->dev->err, s) != cudaSuccess)
+    int n_sl = 0, pstride = 0;
+    if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part, &n_sl,
+                                 &pstride, plan->num_sms, &plan->dev->err, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
+    mark(plan, s);
+    if (engram::launch_finalize(plan, ws.part, n_sl, pstride, ntok, ws.sa, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
     v = ws.v32;
     sv = d;
   }
@@ -407,11 +399,7 @@ engram_status_t engram_get_error(const engram_plan_t* plan, engram_stream_t stre
   if (cudaMemcpy(&plan->dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
   if (flags_out) *flags_out = bits;
-  if (bits & engram::kErrTimeout) {
-    // a K/V GEMM that gave up may have left arrival counts behind
-    if (cudaMemset(plan->tile_cnt, 0, plan->tile_cnt_bytes) != cudaSuccess) return ENGRAM_ERR_CUDA;
-    return ENGRAM_ERR_TIMEOUT;
-  }
+  if (bits & engram::kErrTimeout) return ENGRAM_ERR_TIMEOUT;
   if (bits & engram::kErrIndexRange) return ENGRAM_ERR_INDEX_RANGE;
   return ENGRAM_OK;
 }

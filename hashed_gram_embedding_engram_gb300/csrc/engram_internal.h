@@ -52,8 +52,6 @@ struct engram_plan {
   std::vector<uint64_t> mults;
   std::vector<int64_t> offsets;
   engram::PlanDev* dev;            // device copy of the parameter block (its err word is live)
-  uint32_t* tile_cnt;              // K/V epilogue arrival counters, ceil(max_tokens/128) * 4, zero at rest
-  size_t tile_cnt_bytes;
   engram::PlanDev host;            // host copy, passed to kernels by value
   // tracing: events recorded around each kernel of the last engram_forward
   static constexpr int kMaxMarks = 8;
@@ -109,6 +107,10 @@ cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t nt
 int sa_row_floats(int M);
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
                             const float* g_k, float* sa, cudaStream_t s);
+// bf16 layers: the K/V epilogue's partial sums (n_sl nodes per quantity, rows
+// pstride floats apart) -> sa rows.
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int pstride, int64_t ntok, float* sa,
+                            cudaStream_t s);
 // Conv + SiLU + skip + residual over B sequences of T positions (v fp32 with
 // row stride sv; sa rows [s^(1..M), alpha^(1..M)] per token).
 cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
@@ -122,16 +124,20 @@ cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const 
 cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms,
                               uint32_t* err, cudaStream_t s);
 // The same GEMM with the Engram epilogue: v (columns [0,d)) to v32 in fp32,
-// gate partial sums of every tile to part and, once a row's partials are all
-// in, its gate scalars to sa (saw floats per row); k is never stored.  cnt:
-// ceil(Mr/128) * 4 zeroed counters, left zeroed by a launch that completes.
+// gate partial sums of every tile to part (n_sl nodes per quantity, rows
+// pstride floats apart; both returned); k is never stored.
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
-                             const float* g_h, const float* g_k, float* v32, float* part, float* sa, int saw,
-                             float eps, uint32_t* cnt, int num_sms, uint32_t* err, cudaStream_t s);
+                             const float* g_h, const float* g_k, float* v32, float* part, int* n_sl, int* pstride,
+                             int num_sms, uint32_t* err, cudaStream_t s);
 // 2-D tiled TMA descriptor of a row-major [rows, inner] array (fp32 or bf16),
 // rows row_stride_bytes apart, box of box_rows x box_inner elements.
 bool make_tensor_map_2d(CUtensorMap* map, const void* base, bool is_f32, uint64_t inner, uint64_t rows,
                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+// 3-D tiled TMA descriptor of a bf16 array with dims d0 (contiguous), d1, d2 and
+// byte strides stride1, stride2 between consecutive indices of d1 and d2.
+bool make_tensor_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                             uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                             uint32_t box2, bool swizzle128);
 // fp32 GEMM on the CUDA cores, same shapes.
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);
 

@@ -10,15 +10,18 @@
 // row per token, sa[t] = [s^(1..M), alpha^(1..M), pad] of saw = 4*ceil(2M/4)
 // floats: 16-byte rows that a TMA copy can move.
 //
+//   finalize_kernel   bf16 layers: one warp per token turns the gate partial
+//                     sums written by the K/V GEMM's epilogue (gemm.cu) into
+//                     the token's sa row.
 //   gate_kernel       fp32 layers: one warp per token computes the sa row from
 //                     the fp32 [v | k] buffer of the CUDA-core GEMM.
-//   conv_kernel       one thread per (chain of 4 outputs a dilation apart,
-//                     4 channels): loads the 7 v rows the chain's taps cover
-//                     once, with their s and the outputs' alpha (written by
-//                     the K/V GEMM's epilogue for bf16 layers, gemm.cu);
-//                     taps (times g_c) in registers, compile-time dilation for
-//                     w = 4 (the pages' conv); SiLU, the skip and H += Y for
-//                     every branch.
+//   conv_kernel       persistent blocks over tiles of (positions, channels):
+//                     TMA stages each tile's v rows (with the causal halo), H
+//                     rows and sa rows in a two-stage shared-memory ring; a
+//                     thread takes chains of 4 outputs a dilation apart, whose
+//                     taps cover 7 rows; taps (times g_c) in registers,
+//                     compile-time dilation for w = 4 (the pages' conv); SiLU,
+//                     the skip and H += Y for every branch.
 //   state_kernel      after the chunk: writes RMSNorm(v~) before its weight
 //                     (s * v) of the last (w-1)*dilation positions into the
 //                     ring, rolls the last N-1 projected ids, advances pos (a
@@ -54,6 +57,82 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
+
+// ------------------------------------------------------------------ gate (bf16 layers: from partials)
+// Sum over a warp of the n values p[i * stride], i < n, as the adjacent
+// pairwise tree: lane l sums its aligned block [l*q, l*q + q) pairwise (zeros
+// past n), then the butterfly pairs lanes at distances 1, 2, ..., 16.  With
+// q a power of two the result is the tree sum over the values zero-padded to
+// a power of two, whatever q is -- so slices that are themselves pairwise
+// sums of aligned 32-column chunks (gemm.cu) give the same bits for every
+// GEMM tile width.  Every lane returns the same value.
+__device__ __forceinline__ float pairwise_warp_sum(const float* p, int stride, int n, int q, int lane) {
+  float x;
+  if (q == 1) {
+    x = lane < n ? __ldg(p + static_cast<int64_t>(lane) * stride) : 0.f;
+  } else {
+    float stk[12];
+    int top = 0;
+    for (int i = 0; i < q; ++i) {
+      const int j = lane * q + i;
+      float y = j < n ? __ldg(p + static_cast<int64_t>(j) * stride) : 0.f;
+      for (int k = i; k & 1; k >>= 1) y = stk[--top] + y;
+      stk[top++] = y;
+    }
+    x = stk[0];
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+
+// One warp per token: part[0, n_sl) = sum v^2 nodes, part[n_sl + (m*n_sl + j)*3
+// + {0,1,2}] = (h.g_h.g_k.k, k^2, h^2) nodes of branch m -> the sa row.  Up to
+// 32 nodes (one per lane) the four sums of a branch are loaded together.
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int n_sl, int pstride,
+                                                       int64_t ntok, int M, int d, float eps, float* __restrict__ sa,
+                                                       int saw) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int lane = threadIdx.x & 31;
+  const float inv_d = 1.f / static_cast<float>(d);
+  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
+  int q = 1;
+  while (q * 32 < n_sl) q <<= 1;
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
+       tok += n_warps) {
+    const float* p = part + tok * pstride;
+    float* out = sa + tok * saw;
+    if (q == 1) {
+      const bool has = lane < n_sl;
+      float sv = has ? __ldg(p + lane) : 0.f;
+      for (int m = 0; m < M; ++m) {
+        const float* pm = p + n_sl + (m * n_sl + lane) * 3;
+        float dot = has ? __ldg(pm) : 0.f;
+        float sk = has ? __ldg(pm + 1) : 0.f;
+        float sh = has ? __ldg(pm + 2) : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          if (m == 0) sv += __shfl_xor_sync(0xFFFFFFFFu, sv, o);
+          dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+          sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
+          sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
+        }
+        if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
+      }
+    } else {
+      const float sv = pairwise_warp_sum(p, 1, n_sl, q, lane);
+      for (int m = 0; m < M; ++m) {
+        const float* pm = p + n_sl + m * n_sl * 3;
+        const float dot = pairwise_warp_sum(pm, 3, n_sl, q, lane);
+        const float sk = pairwise_warp_sum(pm + 1, 3, n_sl, q, lane);
+        const float sh = pairwise_warp_sum(pm + 2, 3, n_sl, q, lane);
+        if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
+      }
+    }
+  }
+}
 
 // ------------------------------------------------------------------ gate (fp32 layers)
 __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv, const float* __restrict__ H,
@@ -104,6 +183,7 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
 constexpr int kConvThreads = 512;
+constexpr int kChain = 4;                          // outputs per thread, a dilation apart
 constexpr int kConvStages = 2;
 constexpr uint64_t kConvWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
 constexpr int kConvMaxCS = 256;                    // channels per tile: one TMA box row (<= 256 elements)
@@ -159,13 +239,16 @@ struct H4<float> {
 // sequence's start (negative coordinates, zero-filled by the copy engine, or
 // the previous sequence's rows) are never used: those taps come from the
 // caller's ring (RMSNorm(v~) before its weight) or are zero.  Threads map to
-// (4 channels, every npar-th position); taps (times g_c) in registers; SiLU,
-// the skip and H += Y for every branch, stored straight to H.
+// (4 channels, every npar-th chain of kChain outputs a dilation apart): the
+// kChain + w - 1 rows a chain's taps cover are read from shared memory once
+// and scaled once; taps (times g_c) in registers; SiLU, the skip and H += Y
+// for every branch, stored straight to H.
 // DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
 template <typename TH, int W, int DIL, int MC>
 __global__ void __launch_bounds__(kConvThreads, 1)
     conv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
                 const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a, TH* __restrict__ H) {
+  constexpr int kRows = kChain + W - 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   __shared__ uint64_t full[kConvStages];
@@ -243,42 +326,95 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         }
       }
       const int p0 = a.ring != nullptr ? a.pos[b] : 0;
-      for (int tt = par0; tt < nt; tt += npar) {
-        const int t = t0 + tt;
-        const int r = a.h0 + tt;
-        float vt[W][4];
+      // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
+      const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
+      const int rstride = dil * a.CS;                  // floats between tap rows in the staged v
+      for (int ch = par0; ch < n_chains; ch += npar) {
+        const int tb = (ch / dil) * (kChain * dil) + ch % dil;
+        if (tb >= nt) continue;
+        if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
+          // interior chain: every row staged, every output in the tile -- no branches, all loads first
+          const int r0 = a.h0 + tb - (W - 1) * dil;
+          const float* vp = vs + r0 * a.CS + 4 * g;
+          const float* sp = ss + r0 * a.saw;
+          float vr[kRows][4];
 #pragma unroll
-        for (int j = 0; j < W; ++j) {
-          const int lag = (W - 1 - j) * dil;
-          if (t - lag >= 0) {
-            ld4(vs + (r - lag) * a.CS + 4 * g, vt[j]);
+          for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
+          for (int m = 0; m < M; ++m) {
+            float u[kRows][4], h[kChain][4], at[kChain];
+#pragma unroll
+            for (int o = 0; o < kChain; ++o) {
+              H4<TH>::load(hs + ((tb + o * dil) * M + m) * a.CS + 4 * g, h[o]);
+              at[o] = sp[(o + W - 1) * dil * a.saw + M + m];
+            }
+#pragma unroll
+            for (int j = 0; j < kRows; ++j) {
+              const float sj = sp[j * dil * a.saw + m];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
+            }
+#pragma unroll
+            for (int o = 0; o < kChain; ++o) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
+                h[o][i] = h[o][i] + (silu_fast(acc) + at[o] * vr[o + W - 1][i]);
+              }
+            }
+            TH* hp = H + ((static_cast<int64_t>(b) * a.Tn + t0 + tb) * M + m) * a.d + c;
+#pragma unroll
+            for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o) * dil * M * a.d, h[o]);
+          }
+          continue;
+        }
+        float vr[kRows][4];                           // v of rows tb + (j - (W-1))*dil, tile-relative
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const int tr = tb + (j - (W - 1)) * dil;
+          if (t0 + tr >= 0 && tr < nt) {
+            ld4(vs + (a.h0 + tr) * a.CS + 4 * g, vr[j]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) vt[j][i] = 0.f;
+            for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
           }
         }
         for (int m = 0; m < M; ++m) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          float u[kRows][4];                          // conv input RMSNorm(v~) before g_c: s * v, or the ring
 #pragma unroll
-          for (int j = 0; j < W; ++j) {
-            const int lag = (W - 1 - j) * dil;
-            if (t - lag >= 0) {
-              const float sj = ss[(r - lag) * a.saw + m];
+          for (int j = 0; j < kRows; ++j) {
+            const int tr = tb + (j - (W - 1)) * dil;
+            if (tr >= nt) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sj * vt[j][i], acc[i]);
-            } else if (a.ring != nullptr && p0 + t - lag >= 0) {
-              float u[4];                             // the ring holds RMSNorm(v~) before its weight
-              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t - lag) % a.L) * M + m) * a.d + c, u);
+              for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
+            } else if (t0 + tr >= 0) {
+              const float sj = ss[(a.h0 + tr) * a.saw + m];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+              for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
+            } else if (a.ring != nullptr && p0 + t0 + tr >= 0) {
+              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t0 + tr) % a.L) * M + m) * a.d + c, u[j]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
             }
           }
-          float h[4];
-          H4<TH>::load(hs + (tt * M + m) * a.CS + 4 * g, h);
-          const float at = ss[r * a.saw + M + m];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) h[i] = h[i] + (silu_fast(acc[i]) + at * vt[W - 1][i]);
-          H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t) * M + m) * a.d + c, h);
+          for (int o = 0; o < kChain; ++o) {
+            const int tt = tb + o * dil;
+            if (tt >= nt) break;
+            float h[4];
+            H4<TH>::load(hs + (tt * M + m) * a.CS + 4 * g, h);
+            const float at = ss[(a.h0 + tt) * a.saw + M + m];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float acc = 0.f;
+#pragma unroll
+              for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
+              h[i] = h[i] + (silu_fast(acc) + at * vr[o + W - 1][i]);
+            }
+            H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t0 + tt) * M + m) * a.d + c, h);
+          }
         }
       }
     }
@@ -427,6 +563,12 @@ void conv_layout(ConvArgs& a, size_t act_bytes) {
 }  // namespace
 
 int sa_row_floats(int M) { return (2 * M + 3) / 4 * 4; }
+
+cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int pstride, int64_t ntok, float* sa,
+                            cudaStream_t s) {
+  return launch_pdl(finalize_kernel, dim3(grid_for(ntok * 32, 256, p->num_sms)), dim3(256), 0, s, part, n_sl, pstride,
+                    ntok, p->cfg.M, p->cfg.d, p->cfg.eps, sa, sa_row_floats(p->cfg.M));
+}
 
 cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* H, int64_t ntok, const float* g_h,
                             const float* g_k, float* sa, cudaStream_t s) {

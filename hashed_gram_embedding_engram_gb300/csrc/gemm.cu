@@ -22,7 +22,6 @@
 #include <cuda_runtime.h>
 
 #include "engram_internal.h"
-#include "gate.cuh"
 #include "ptx.cuh"
 
 namespace engram {
@@ -33,16 +32,20 @@ constexpr int kBK = 64;                        // one 128-byte swizzle atom of b
 constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: a healthy stage turns over in < 1 us
 
-template <int BN>
+constexpr int kEpiWarpBytes = 8192;            // fused epilogue: per-warp staging of v chunks / the H slice
+
+template <int BN, bool kFused>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kStages = kFused ? (BN == 256 ? 3 : (BN == 128 ? 4 : 6)) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kEpiBytes = kFused ? 8 * kEpiWarpBytes : 0;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN);
+  static constexpr int kHBoxes = BN / 2 > 64 ? BN / 128 : 1;   // 64-column H boxes per warp slice
 };
 
 struct EngramEpilogue {
@@ -51,10 +54,6 @@ struct EngramEpilogue {
   const __nv_bfloat16* H;         // [Mr, M, d]
   const float* g_h;               // [M, d]
   const float* g_k;               // [M, d]
-  float* sa;                      // [Mr, saw]: s^(1..M), alpha^(1..M)
-  uint32_t* cnt;                  // [ceil(Mr/128) * 4] arrivals per (row tile, lane quadrant), zero between launches
-  float eps;
-  int saw;
   int d;
   int M;
   int n_sl;                       // d / (BN / 2): column slices per row of v
@@ -66,6 +65,7 @@ struct Bars {
   uint64_t empty[8];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t hbar[8];               // fused epilogue: H slice of each epilogue warp landed
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -86,133 +86,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
   }
 }
 
-// In-lane sum of the n values p[i * stride] as the adjacent pairwise tree over
-// the values zero-padded to a power of two: a stack of finished subtrees,
-// merged as a binary counter carries, folded right to left at the end.  The
-// loads go out eight at a time.
-__device__ __forceinline__ void tree_push(float* stk, int& top, float x, int i) {
-  for (int k = i; k & 1; k >>= 1) x = stk[--top] + x;
-  stk[top++] = x;
-}
-
-__device__ __forceinline__ float tree_fold(float* stk, int top) {
-  for (; top > 1; --top) stk[top - 2] = stk[top - 2] + stk[top - 1];
-  return top ? stk[0] : 0.f;
-}
-
-__device__ __forceinline__ float tree_sum(const float* p, int n) {
-  float stk[24];
-  int top = 0;
-  for (int i0 = 0; i0 < n; i0 += 8) {
-    float x[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = i0 + j < n ? __ldcg(p + i0 + j) : 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (i0 + j < n) tree_push(stk, top, x[j], i0 + j);
-  }
-  return tree_fold(stk, top);
-}
-
-// the same for the three interleaved sums (x, y, z) of p[3i], p[3i+1], p[3i+2]
-__device__ __forceinline__ void tree_sum3(const float* p, int n, float& x, float& y, float& z) {
-  float sx[24], sy[24], sz[24];
-  int tx = 0, ty = 0, tz = 0;
-  for (int i0 = 0; i0 < n; i0 += 8) {
-    float a[8][3];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int q = 0; q < 3; ++q) a[j][q] = i0 + j < n ? __ldcg(p + 3 * (i0 + j) + q) : 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (i0 + j < n) {
-        tree_push(sx, tx, a[j][0], i0 + j);
-        tree_push(sy, ty, a[j][1], i0 + j);
-        tree_push(sz, tz, a[j][2], i0 + j);
-      }
-    }
-  }
-  x = tree_fold(sx, tx);
-  y = tree_fold(sy, ty);
-  z = tree_fold(sz, tz);
-}
-
-// Adjacent pairwise tree over N (a power of two) values in registers.
-template <int N>
-__device__ __forceinline__ float tree_reg(float* x) {
-#pragma unroll
-  for (int w = 1; w < N; w *= 2)
-#pragma unroll
-    for (int i = 0; i + w < N; i += 2 * w) x[i] = x[i] + x[i + w];
-  return x[0];
-}
-
-// N floats from 16-byte aligned p (N a multiple of 4), all loads issued together
-template <int N>
-__device__ __forceinline__ void load_cg(const float* p, float* x) {
-  if constexpr (N % 4 == 0) {
-#pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-      const float4 q = __ldcg(reinterpret_cast<const float4*>(p) + i);
-      x[4 * i] = q.x;
-      x[4 * i + 1] = q.y;
-      x[4 * i + 2] = q.z;
-      x[4 * i + 3] = q.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < N; ++i) x[i] = __ldcg(p + i);
-  }
-}
-
-// The gate scalars of one row from its partial sums (layout below), into sa.
-// NSL > 0: a compile-time power-of-two slice count (registers only); 0: any.
-template <int NSL>
-__device__ __forceinline__ void finalize_row(const EngramEpilogue& epi, int row) {
-  const int M = epi.M;
-  const float* p = epi.part + static_cast<int64_t>(row) * epi.pstride;
-  const float inv_d = 1.f / static_cast<float>(epi.d);
-  const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(epi.d));
-  float* sa_row = epi.sa + static_cast<int64_t>(row) * epi.saw;
-  if constexpr (NSL > 0) {
-    float xv[NSL], xk[3 * NSL];
-    load_cg<NSL>(p, xv);
-    load_cg<3 * NSL>(p + NSL, xk);
-    const float sv = tree_reg<NSL>(xv);
-    for (int m = 0; m < M; ++m) {
-      if (m > 0) load_cg<3 * NSL>(p + NSL + m * 3 * NSL, xk);
-      float d0[NSL], d1[NSL], d2[NSL];
-#pragma unroll
-      for (int i = 0; i < NSL; ++i) {
-        d0[i] = xk[3 * i];
-        d1[i] = xk[3 * i + 1];
-        d2[i] = xk[3 * i + 2];
-      }
-      gate_scalars(sv, tree_reg<NSL>(d0), tree_reg<NSL>(d1), tree_reg<NSL>(d2), inv_d, inv_sqrt_d, epi.eps, sa_row,
-                   M, m);
-    }
-  } else {
-    const int n = epi.n_sl;
-    const float sv = tree_sum(p, n);
-    for (int m = 0; m < M; ++m) {
-      float dot, sk, sh;
-      tree_sum3(p + n + m * n * 3, n, dot, sk, sh);
-      gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, epi.eps, sa_row, M, m);
-    }
-  }
-}
-
-__device__ __forceinline__ void finalize_row_any(const EngramEpilogue& epi, int row) {
-  switch (epi.n_sl) {
-    case 4: finalize_row<4>(epi, row); break;
-    case 8: finalize_row<8>(epi, row); break;
-    case 16: finalize_row<16>(epi, row); break;
-    case 32: finalize_row<32>(epi, row); break;
-    default: finalize_row<0>(epi, row); break;
-  }
-}
-
 // Engram epilogue of the K/V projection (Steps 5-6 fused).  Output columns
 // [0, d) are v: stored in fp32 with a per-slice partial of sum(v^2).  Columns
 // [(1+m)d, (2+m)d) are k^(m): never stored; each slice contributes the partial
@@ -222,27 +95,34 @@ __device__ __forceinline__ void finalize_row_any(const EngramEpilogue& epi, int 
 // n_sl = d / (BN/2) slices per row of v (and of each k^(m)), token t has
 // part[t*P + j] = sum v^2 of v slice j, and
 // part[t*P + n_sl + (m*n_sl + j)*3 + {0,1,2}] = (dot, sk, sh) of k^(m) slice j.
-// Each sum is a sequential fmaf chain over the 32 columns of one tcgen05.ld
-// chunk; a slice's chunks are combined as an adjacent pairwise tree, which
-// finalize_row continues over the slices, so the gate's sums have the same
-// bits for every tile width BN.  The last of the 2 * n_tiles warps that write
-// partials for a (row tile, lane quadrant) -- an atomic count, no waiting --
-// finalises those 32 rows into sa.
+// Rows of part are pstride floats apart (padded to 16 bytes).  Each sum is a
+// sequential fmaf chain over the 32 columns of one tcgen05.ld chunk; a
+// slice's chunks are combined as an adjacent pairwise tree, which the gate
+// finalisation continues over the slices (fusion.cu), so the gate's sums have
+// the same bits for every tile width BN.
+//
+// TMEM gives each lane one row, so global accesses lane by lane would touch 32
+// cache lines per instruction.  Both directions go through the warp's 8 KB of
+// shared memory in the 128-byte swizzled layout instead (16-byte chunk j of
+// row r at r*128 + 16*(j ^ (r % 8)), conflict-free for row-per-lane access):
+// v chunks of 32 x 32 fp32 leave by TMA tensor stores, and the warp's H slice
+// (32 rows x BN/2 columns) arrives by TMA while the tile's MMAs run.
 template <int BN>
-__device__ __forceinline__ void fused_partials(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0,
-                                               int c_lo) {
+__device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const CUtensorMap* tmV, uint8_t* eb,
+                                               uint32_t t_row, int row, int row0, int Mr, int n0, int c_lo, int lane) {
   constexpr int SW = BN / 2;
   constexpr int kChunks = SW / 32;          // 1, 2 or 4
   const int d = epi.d;
   const int P = epi.pstride;
+  const int swz = lane & 7;
   if (n0 < d) {
-    // v tile, first pass: the slice's sum of v^2 (the values are stored in a second pass)
     float stk[3];
     int top = 0;
 #pragma unroll
     for (int ci = 0; ci < kChunks; ++ci) {
+      const int c = c_lo + ci * 32;
       uint32_t r[32];
-      ptx::tmem_ld_32x32b_x32(t_row + c_lo + ci * 32, r);
+      ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
       float sv = 0.f;
 #pragma unroll
@@ -250,57 +130,58 @@ __device__ __forceinline__ void fused_partials(const EngramEpilogue& epi, uint32
 #pragma unroll
       for (int k = ci; k & 1; k >>= 1) sv = stk[--top] + sv;
       stk[top++] = sv;
+      uint8_t* sb = eb + (ci & 1) * 4096;
+      if (lane == 0) {
+        if (ci == 0) ptx::bulk_wait_read<0>();     // earlier tiles' stores have left both buffers
+        else if (ci >= 2) ptx::bulk_wait_read<1>();  // the store from this buffer two chunks ago
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ swz) << 4)) =
+            make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(tmV, sb, n0 + c, row0);
+        ptx::bulk_commit();
+      }
     }
     if (row < Mr) epi.part[static_cast<int64_t>(row) * P + (n0 + c_lo) / SW] = stk[0];
   } else {
     const int m = (n0 - d) / d;
     const int col = n0 - d - m * d;
     const int j = (col + c_lo) / SW;
-    const __nv_bfloat16* hrow = epi.H + (static_cast<int64_t>(row) * epi.M + m) * d + col;
     const float* gh = epi.g_h + static_cast<int64_t>(m) * d + col;
     const float* gk = epi.g_k + static_cast<int64_t>(m) * d + col;
     float s_dot[3], s_sk[3], s_sh[3];
     int top = 0;
-    uint4 hcur[4], hnext[4];               // H of this chunk; the next chunk's loads are in flight
-    if (row < Mr) {
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) hcur[q4] = __ldg(reinterpret_cast<const uint4*>(hrow + c_lo) + q4);
-    }
 #pragma unroll
     for (int ci = 0; ci < kChunks; ++ci) {
       const int c = c_lo + ci * 32;
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
-      if (ci + 1 < kChunks && row < Mr) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) hnext[q4] = __ldg(reinterpret_cast<const uint4*>(hrow + c + 32) + q4);
-      }
       float dot = 0.f, sk = 0.f, sh = 0.f;
-      if (row < Mr) {
-        const float4* gh4 = reinterpret_cast<const float4*>(gh + c);
-        const float4* gk4 = reinterpret_cast<const float4*>(gk + c);
+      const uint8_t* hb = eb + (ci >> 1) * 4096 + lane * 128;     // this row of the chunk's 64-column box
+      const float4* gh4 = reinterpret_cast<const float4*>(gh + c);
+      const float4* gk4 = reinterpret_cast<const float4*>(gk + c);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 hv = hcur[q4];
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-          const float4 ga = __ldg(gh4 + 2 * q4), gb = __ldg(gh4 + 2 * q4 + 1);
-          const float4 ka = __ldg(gk4 + 2 * q4), kb = __ldg(gk4 + 2 * q4 + 1);
-          const float g[8] = {ga.x * ka.x, ga.y * ka.y, ga.z * ka.z, ga.w * ka.w,
-                              gb.x * kb.x, gb.y * kb.y, gb.z * kb.z, gb.w * kb.w};
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 hv = *reinterpret_cast<const uint4*>(hb + ((((ci & 1) * 4 + q4) ^ swz) << 4));
+        const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+        const float4 ga = __ldg(gh4 + 2 * q4), gb = __ldg(gh4 + 2 * q4 + 1);
+        const float4 ka = __ldg(gk4 + 2 * q4), kb = __ldg(gk4 + 2 * q4 + 1);
+        const float g[8] = {ga.x * ka.x, ga.y * ka.y, ga.z * ka.z, ga.w * ka.w,
+                            gb.x * kb.x, gb.y * kb.y, gb.z * kb.z, gb.w * kb.w};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float h = __uint_as_float(i & 1 ? (hw[i >> 1] & 0xFFFF0000u) : (hw[i >> 1] << 16));
-            const float k = __uint_as_float(r[q4 * 8 + i]);
-            dot = fmaf(h * g[i], k, dot);
-            sk = fmaf(k, k, sk);
-            sh = fmaf(h, h, sh);
-          }
+        for (int i = 0; i < 8; ++i) {
+          const float h = __uint_as_float(i & 1 ? (hw[i >> 1] & 0xFFFF0000u) : (hw[i >> 1] << 16));
+          const float k = __uint_as_float(r[q4 * 8 + i]);
+          dot = fmaf(h * g[i], k, dot);
+          sk = fmaf(k, k, sk);
+          sh = fmaf(h, h, sh);
         }
-      }
-      if (ci + 1 < kChunks) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) hcur[q4] = hnext[q4];
       }
 #pragma unroll
       for (int k = ci; k & 1; k >>= 1) {
@@ -323,36 +204,17 @@ __device__ __forceinline__ void fused_partials(const EngramEpilogue& epi, uint32
   }
 }
 
-// v tile, second pass: the values to v32 in fp32 (one 128-byte line per lane per chunk)
-template <int BN>
-__device__ __forceinline__ void store_v(const EngramEpilogue& epi, uint32_t t_row, int row, int Mr, int n0,
-                                        int c_lo) {
-  constexpr int kChunks = BN / 64;
-#pragma unroll
-  for (int ci = 0; ci < kChunks; ++ci) {
-    const int c = c_lo + ci * 32;
-    uint32_t r[32];
-    ptx::tmem_ld_32x32b_x32(t_row + c, r);
-    ptx::tmem_ld_wait();
-    if (row < Mr) {
-      float4* dst = reinterpret_cast<float4*>(epi.v32 + static_cast<int64_t>(row) * epi.d + n0 + c);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
-                             __uint_as_float(r[4 * j + 3]));
-    }
-  }
-}
-
 template <int BN, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmH,
                      __nv_bfloat16* __restrict__ C, int Mr, int Nc, int Kd, uint32_t* __restrict__ err,
                      const EngramEpilogue epi) {
-  using G = Cfg<BN>;
+  using G = Cfg<BN, kFused>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + G::kStages * G::kStageBytes);
+  uint8_t* epi_smem = smem + G::kStages * G::kStageBytes;          // 1024-byte aligned
+  Bars* bars = reinterpret_cast<Bars*>(epi_smem + G::kEpiBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -370,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bars->tfull[a], 1);
       ptx::mbar_init(&bars->tempty[a], 8);     // one arrive per epilogue warp
     }
+    for (int w = 0; w < 8; ++w) ptx::mbar_init(&bars->hbar[w], 1);
     ptx::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     ptx::fence_mbar_init();
@@ -377,6 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if constexpr (kFused) {
+      ptx::tma_prefetch_desc(&tmV);
+      ptx::tma_prefetch_desc(&tmH);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(&bars->tmem_base, G::kTmemCols);
@@ -465,25 +332,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------- epilogue (warps 2..9)
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int c_lo = ((warp - 2) >> 2) * (BN / 2);   // half of the tile's columns
+    const int ew = warp - 2;
+    const int c_lo = (ew >> 2) * (BN / 2);  // half of the tile's columns
+    uint8_t* eb = epi_smem + ew * kEpiWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t h_phase = 0;
+    bool h_pending = false;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_tiles) * kBM;
       const int n0 = (tile % n_tiles) * BN;
       const int row = m0 + q * 32 + lane;
-      if constexpr (kFused) {
-        // a k tile reads this row's H slice after its MMAs: pull it into L2 meanwhile
-        if (n0 >= epi.d && row < Mr) {
+      const bool ktile = kFused && n0 >= epi.d;
+      if (ktile) {
+        // this warp's H slice (32 rows x BN/2 columns) lands while the tile's MMAs run
+        if (lane == 0) {
+          ptx::bulk_wait_read<0>();            // staged v of an earlier tile has left this buffer
+          ptx::fence_proxy_async_smem();
           const int m = (n0 - epi.d) / epi.d;
-          const char* hp = reinterpret_cast<const char*>(
-              epi.H + (static_cast<int64_t>(row) * epi.M + m) * epi.d + (n0 - epi.d - m * epi.d) + c_lo);
+          const int col = n0 - epi.d - m * epi.d + c_lo;
+          ptx::mbar_arrive_expect_tx(&bars->hbar[ew], G::kHBoxes * 4096);
 #pragma unroll
-          for (int off = 0; off < BN; off += 128) ptx::prefetch_l2(hp + off);
+          for (int bx = 0; bx < G::kHBoxes; ++bx)
+            ptx::tma_load_3d(eb + bx * 4096, &tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32);
         }
+        h_pending = true;
       }
       if (!wait_or_abort(&bars->tfull[acc], acc_phase, bars, err)) break;
       ptx::tc_fence_after();
+      if (ktile) {
+        if (!wait_or_abort(&bars->hbar[ew], h_phase, bars, err)) break;
+        h_phase ^= 1;
+        h_pending = false;
+      }
       const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       if constexpr (!kFused) {
 #pragma unroll 1
@@ -504,29 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
           }
         }
-      }
-      uint32_t last = 0;
-      if constexpr (kFused) {
-        fused_partials<BN>(epi, t_row, row, Mr, n0, c_lo);
-        __threadfence();                       // this lane's partials, before the count
-        __syncwarp();
-        if (lane == 0)
-          last = atomicAdd(epi.cnt + (m0 / kBM) * 4 + q, 1u) == 2u * static_cast<uint32_t>(n_tiles) - 1u;
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (n0 < epi.d) store_v<BN>(epi, t_row, row, Mr, n0, c_lo);
+      } else {
+        fused_epilogue<BN>(epi, &tmV, eb, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->tempty[acc]);
-      if constexpr (kFused) {
-        if (last) {                            // every partial of these 32 rows is in
-          __threadfence();
-          if (lane == 0) epi.cnt[(m0 / kBM) * 4 + q] = 0;
-          if (row < Mr) finalize_row_any(epi, row);
-        }
-      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+    }
+    if constexpr (kFused) {
+      if (lane == 0) {
+        // an H load that a timeout left in flight lands before the block exits; v stores complete
+        if (h_pending) ptx::mbar_wait_bounded(&bars->hbar[ew], h_phase, kWaitLimitNs);
+        ptx::bulk_wait_all();
+      }
     }
   }
 
@@ -548,9 +421,21 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int cols, int bo
 template <int BN, bool kFused>
 cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int Kd, int num_sms, uint32_t* err,
                 EngramEpilogue epi, cudaStream_t s) {
-  using G = Cfg<BN>;
-  CUtensorMap ta, tb;
+  using G = Cfg<BN, kFused>;
+  CUtensorMap ta, tb, tv, th;
   if (!make_map(&ta, A, Mr, Kd, kBM) || !make_map(&tb, B, Nc, Kd, BN)) return cudaErrorInvalidValue;
+  if constexpr (kFused) {
+    // v32 [Mr, d] fp32 in 32 x 32 boxes; H [Mr, M, d] bf16 in (64 columns, 1 branch, 32 rows) boxes
+    if (!make_tensor_map_2d(&tv, epi.v32, true, static_cast<uint64_t>(epi.d), static_cast<uint64_t>(Mr),
+                            static_cast<uint64_t>(epi.d) * 4, 32, 32, true) ||
+        !make_tensor_map_3d_bf16(&th, epi.H, static_cast<uint64_t>(epi.d), static_cast<uint64_t>(epi.M),
+                                 static_cast<uint64_t>(Mr), static_cast<uint64_t>(epi.d) * 2,
+                                 static_cast<uint64_t>(epi.d) * epi.M * 2, 64, 1, 32, true))
+      return cudaErrorInvalidValue;
+  } else {
+    tv = ta;
+    th = ta;
+  }
   static bool attr_set = false;   // per template instance; idempotent if raced
   if (!attr_set) {
     cudaError_t e =
@@ -564,7 +449,7 @@ cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int K
     epi.n_sl = epi.d / (BN / 2);
     epi.pstride = (epi.n_sl * (1 + 3 * epi.M) + 3) / 4 * 4;
   }
-  return launch_pdl(gemm_bf16_kernel<BN, kFused>, dim3(grid), dim3(kThreads), G::kSmem, s, ta, tb,
+  return launch_pdl(gemm_bf16_kernel<BN, kFused>, dim3(grid), dim3(kThreads), G::kSmem, s, ta, tb, tv, th,
                     static_cast<__nv_bfloat16*>(C), static_cast<int>(Mr), Nc, Kd, err, epi);
 }
 
@@ -635,12 +520,15 @@ cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr,
 }
 
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
-                             const float* g_h, const float* g_k, float* v32, float* part, float* sa, int saw,
-                             float eps, uint32_t* cnt, int num_sms, uint32_t* err, cudaStream_t s) {
+                             const float* g_h, const float* g_k, float* v32, float* part, int* n_sl, int* pstride,
+                             int num_sms, uint32_t* err, cudaStream_t s) {
   const int Nc = (M + 1) * d;
   if (d % 64 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
-  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, sa, cnt, eps, saw, d, M, 0, 0};
-  switch (pick_bn(Mr, Nc, d, num_sms)) {
+  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0, 0};
+  const int bn = pick_bn(Mr, Nc, d, num_sms);
+  *n_sl = d / (bn / 2);
+  *pstride = (*n_sl * (1 + 3 * M) + 3) / 4 * 4;
+  switch (bn) {
     case 256: return run<256, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
     case 128: return run<128, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
     default: return run<64, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
