@@ -182,9 +182,9 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
 }
 
 // ------------------------------------------------------------------ conv + SiLU + skip + residual
-constexpr int kConvThreads = 512;
+constexpr int kConvThreads = 448;                 // compute threads (14 warps); one producer warp more
 constexpr int kChain = 4;                          // outputs per thread, a dilation apart
-constexpr int kConvStages = 2;
+constexpr int kConvStages = 3;
 constexpr uint64_t kConvWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
 constexpr int kConvMaxCS = 256;                    // channels per tile: one TMA box row (<= 256 elements)
 
@@ -233,26 +233,29 @@ struct H4<float> {
 // Persistent blocks over tiles of (S positions of one sequence, CS channels).
 // Each tile's inputs are staged in shared memory by three TMA copies -- the v
 // rows of its positions and of the (w-1)*dilation positions before them, the
-// H rows of every branch, the sa rows [s^(1..M), alpha^(1..M)] -- in a
-// two-stage ring, so the copies of the next tile overlap the arithmetic of
-// this one and each v row is read from memory about once.  Rows before a
-// sequence's start (negative coordinates, zero-filled by the copy engine, or
-// the previous sequence's rows) are never used: those taps come from the
-// caller's ring (RMSNorm(v~) before its weight) or are zero.  Threads map to
-// (4 channels, every npar-th chain of kChain outputs a dilation apart): the
-// kChain + w - 1 rows a chain's taps cover are read from shared memory once
-// and scaled once; taps (times g_c) in registers; SiLU, the skip and H += Y
-// for every branch, stored straight to H.
+// H rows of every branch, the sa rows [s^(1..M), alpha^(1..M)] -- in a ring of
+// kConvStages stages.  A producer warp refills a stage as soon as all compute
+// warps have released it (an "empty" mbarrier), and each compute warp moves
+// on to the next tile on its own, so no block-wide barrier separates tiles.
+// Rows before a sequence's start (negative coordinates, zero-filled by the
+// copy engine, or the previous sequence's rows) are never used: those taps
+// come from the caller's ring (RMSNorm(v~) before its weight) or are zero.
+// Compute threads map to (4 channels, every npar-th chain of kChain outputs a
+// dilation apart, rotated from tile to tile): the kChain + w - 1 rows a
+// chain's taps cover are read from shared memory once and scaled once; taps
+// (times g_c) in registers; SiLU, the skip and H += Y for every branch,
+// stored straight to H.
 // DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
 template <typename TH, int W, int DIL, int MC>
-__global__ void __launch_bounds__(kConvThreads, 1)
+__global__ void __launch_bounds__(kConvThreads + 32, 1)
     conv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
                 const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a, TH* __restrict__ H) {
   constexpr int kRows = kChain + W - 1;
+  constexpr int kWarps = kConvThreads / 32;          // compute warps
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  __shared__ uint64_t full[kConvStages];
-  __shared__ int s_ok;
+  __shared__ uint64_t full[kConvStages], empty[kConvStages];
+  __shared__ int s_abort;
   const int dil = DIL > 0 ? DIL : a.dil;
   const int M = MC > 0 ? MC : a.M;
   const int tid = threadIdx.x;
@@ -264,72 +267,103 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     t0 = (q - b * a.tiles_per_seq) * a.S;
     c0 = ct * a.CS;
   };
-  auto issue = [&](int tile, int stage) {          // one thread
-    int b, t0, c0;
-    coords(tile, b, t0, c0);
-    const int32_t row0 = b * a.Tn + t0 - a.h0;     // may be negative: zero fill
-    uint8_t* base = smem + stage * a.stage_bytes;
-    ptx::mbar_arrive_expect_tx(&full[stage], a.tx_bytes);
-    ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[stage], c0, row0);
-    ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[stage], c0, (b * a.Tn + t0) * M);
-    ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[stage], 0, row0);
-  };
 
   if (tid == 0) {
-    for (int st = 0; st < kConvStages; ++st) ptx::mbar_init(&full[st], 1);
+    for (int st = 0; st < kConvStages; ++st) {
+      ptx::mbar_init(&full[st], 1);
+      ptx::mbar_init(&empty[st], kWarps);
+    }
+    s_abort = 0;
     ptx::fence_mbar_init();
-    ptx::tma_prefetch_desc(&tm_v);
-    ptx::tma_prefetch_desc(&tm_h);
-    ptx::tma_prefetch_desc(&tm_sa);
   }
   __syncthreads();
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  if (tid == 0) {
-    for (int k = 0; k < kConvStages; ++k)
-      if (blockIdx.x + k * gridDim.x < static_cast<unsigned>(a.n_tiles)) issue(blockIdx.x + k * gridDim.x, k);
+
+  if (tid >= kConvThreads) {
+    // ---------------------------------------------------------------- producer warp
+    if (tid == kConvThreads) {
+      ptx::tma_prefetch_desc(&tm_v);
+      ptx::tma_prefetch_desc(&tm_h);
+      ptx::tma_prefetch_desc(&tm_sa);
+      uint32_t armed = 0;                            // stages with a copy issued and not yet seen complete
+      int k = 0;
+      for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+        const int st = k % kConvStages;
+        const uint32_t round = static_cast<uint32_t>(k / kConvStages);
+        if (round > 0 && !ptx::mbar_wait_bounded(&empty[st], (round - 1) & 1u, kConvWaitNs)) {
+          atomicOr(a.err, kErrTimeout);
+          *reinterpret_cast<volatile int*>(&s_abort) = 1;
+          break;
+        }
+        int b, t0, c0;
+        coords(tile, b, t0, c0);
+        const int32_t row0 = b * a.Tn + t0 - a.h0;   // may be negative: zero fill
+        uint8_t* base = smem + st * a.stage_bytes;
+        ptx::mbar_arrive_expect_tx(&full[st], a.tx_bytes);
+        ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[st], c0, row0);
+        ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[st], c0, (b * a.Tn + t0) * M);
+        ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[st], 0, row0);
+        armed |= 1u << st;
+      }
+      // copies still in flight land before the block may exit
+      const int issued = k;
+      for (int j = issued - kConvStages; j < issued; ++j) {
+        if (j < 0) continue;
+        const int st = j % kConvStages;
+        if (armed & (1u << st)) ptx::mbar_wait_bounded(&full[st], static_cast<uint32_t>(j / kConvStages) & 1u,
+                                                       kConvWaitNs);
+      }
+    }
+    return;
   }
 
+  // -------------------------------------------------------------------- compute warps
+  const int lane = tid & 31;
   const int ng = a.CS >> 2;                        // channel groups of a tile
-  const int npar = kConvThreads / ng;              // positions processed side by side
+  const int npar = kConvThreads / ng;              // chains processed side by side
   const int g = tid % ng, par0 = tid / ng;
-  uint32_t parity = 0;                             // bit per stage
-  int it = 0;
-  int tile = blockIdx.x;
-  for (; tile < a.n_tiles; tile += gridDim.x, ++it) {
-    const int stage = it % kConvStages;
-    const uint32_t ph = (parity >> stage) & 1u;
-    if (tid == 0) s_ok = ptx::mbar_wait_bounded(&full[stage], ph, kConvWaitNs) ? 1 : 0;
-    __syncthreads();
-    if (!s_ok) break;
-    for (int spin = 0; spin < (1 << 20) && !ptx::mbar_try_wait(&full[stage], ph); ++spin) {
+  int c_cached = -1;
+  float wq[4][W];                                  // taps times g_c for channels c .. c+3
+  auto load_taps = [&](int c) {
+    float gc[4];
+    ld4(a.g_c + c, gc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
     }
-    parity ^= 1u << stage;
-
+    c_cached = c;
+  };
+  if (blockIdx.x < static_cast<unsigned>(a.n_tiles) && par0 < npar) {
+    // the first tile's taps, while its copies are in flight
+    int b, t0, c0;
+    coords(blockIdx.x, b, t0, c0);
+    load_taps(c0 + 4 * g);
+  }
+  int k = 0;
+  for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+    const int st = k % kConvStages;
+    if (!ptx::mbar_wait_bounded(&full[st], static_cast<uint32_t>(k / kConvStages) & 1u, kConvWaitNs)) {
+      if (lane == 0) atomicOr(a.err, kErrTimeout);
+      break;
+    }
+    if (*reinterpret_cast<volatile int*>(&s_abort)) break;
     int b, t0, c0;
     coords(tile, b, t0, c0);
     const int nt = min(a.S, a.Tn - t0);
-    const uint8_t* base = smem + stage * a.stage_bytes;
+    const uint8_t* base = smem + st * a.stage_bytes;
     const float* vs = reinterpret_cast<const float*>(base + a.v_off);    // [S + h0][CS], row r: position t0 - h0 + r
     const TH* hs = reinterpret_cast<const TH*>(base + a.h_off);          // [S * M][CS]
     const float* ss = reinterpret_cast<const float*>(base + a.sa_off);   // [S + h0][saw]
     if (par0 < npar) {
       const int c = c0 + 4 * g;
-      float wq[4][W];                                 // taps times g_c
-      {
-        float gc[4];
-        ld4(a.g_c + c, gc);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
-        }
-      }
+      if (c != c_cached) load_taps(c);
       const int p0 = a.ring != nullptr ? a.pos[b] : 0;
+      const int rstride = dil * a.CS;                  // floats between tap rows in the staged v
       // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
       const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
-      const int rstride = dil * a.CS;                  // floats between tap rows in the staged v
-      for (int ch = par0; ch < n_chains; ch += npar) {
+      for (int ch = (par0 + k) % npar; ch < n_chains; ch += npar) {
         const int tb = (ch / dil) * (kChain * dil) + ch % dil;
         if (tb >= nt) continue;
         if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
@@ -418,19 +452,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         }
       }
     }
-    __syncthreads();                                  // the stage is consumed
-    if (tid == 0 && tile + kConvStages * static_cast<int>(gridDim.x) < a.n_tiles)
-      issue(tile + kConvStages * gridDim.x, stage);
-  }
-  if (tile < a.n_tiles && tid == 0) {
-    // a copy did not land in time: record it; the copies still in flight (this
-    // stage's and the next one's) must land before the block may exit
-    atomicOr(a.err, kErrTimeout);
-    for (int k = 0; k < kConvStages; ++k) {
-      const int st = (it + k) % kConvStages;
-      if (tile + k * static_cast<int>(gridDim.x) < a.n_tiles)
-        ptx::mbar_wait_bounded(&full[st], (parity >> st) & 1u, kConvWaitNs);
-    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&empty[st]);    // this warp is done with the stage
   }
 }
 
@@ -502,7 +525,7 @@ cudaError_t conv_launch_m(const CUtensorMap& tv, const CUtensorMap& th, const CU
     if (e != cudaSuccess) return e;
     attr_bytes = smem;
   }
-  return launch_pdl(conv_kernel<TH, W, DIL, MC>, dim3(grid), dim3(kConvThreads), smem, s, tv, th, ts, a,
+  return launch_pdl(conv_kernel<TH, W, DIL, MC>, dim3(grid), dim3(kConvThreads + 32), smem, s, tv, th, ts, a,
                     static_cast<TH*>(H));
 }
 
@@ -600,10 +623,11 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   if (ntok * a.M > INT32_MAX) return cudaErrorInvalidValue;
   // Tile shape.  Channels per tile CS: the widest (<= 256, dividing d) whose
   // tile keeps at least 2/3 of its staged v rows useful (S / (S + halo)),
-  // else the one with the best share; S: as many positions as two stages
-  // hold (S * M <= 256 and S + halo <= 256: one TMA box each), the whole
-  // sequence if it fits.  Then S is lowered (not below 2 * halo) so the tile
-  // count fills whole waves of the SMs.
+  // else the one with the best share; S: at most what kConvStages stages hold
+  // (S * M <= 256 and S + halo <= 256: one TMA box each), the whole sequence
+  // if it fits.  Among multiples of 4 * dilation (whole chains) up to that
+  // bound, S then minimises waves-of-tiles x (S + halo + 8): the staged rows
+  // of the slowest block plus a per-tile overhead.
   const int64_t budget = (227 * 1024 - 1024) / kConvStages - 3 * 128;
   int S = 0, smax_halo = 0;
   double best = -1.0;
@@ -638,12 +662,22 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.n_ct = a.d / a.CS;
   {
     const int64_t lanes = static_cast<int64_t>(B) * a.n_ct;
-    const int64_t tiles = lanes * ((T + S - 1) / S);
-    const int64_t waves = (tiles + p->num_sms - 1) / p->num_sms;
-    const int64_t per_seq = (waves * p->num_sms + lanes - 1) / lanes;
-    int s2 = static_cast<int>((T + per_seq - 1) / per_seq);
-    s2 = std::max(s2, std::min(S, 2 * halo));
-    if (s2 < S && s2 <= smax_halo) S = s2;
+    auto cost = [&](int sc) {
+      const int64_t tiles = lanes * ((T + sc - 1) / sc);
+      const int64_t waves = (tiles + p->num_sms - 1) / p->num_sms;
+      return waves * (sc + (sc < T ? halo : 0) + 8);
+    };
+    int best_s = S;
+    int64_t best_cost = cost(S);
+    const int step = 4 * a.dil;
+    for (int sc = std::min(smax_halo, T - 1) / step * step; sc >= step; sc -= step) {
+      const int64_t c = cost(sc);
+      if (c < best_cost) {
+        best_cost = c;
+        best_s = sc;
+      }
+    }
+    S = best_s;
   }
   a.S = S;
   a.tiles_per_seq = (T + S - 1) / S;
