@@ -260,6 +260,26 @@ engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int
                                            (cudaStream_t)stream));
 }
 
+engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
+                               int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,
+                               void* e_out, engram_stream_t stream) {
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
+  if (!ids || !proj || V <= 0 || !table || !e_out || !aligned16(e_out)) return ENGRAM_ERR_INVALID_ARG;
+  const bool i8 = plan->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
+  if (i8 != (scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
+  const void* tab = nullptr;
+  if (engram_status_t s = device_view(table, &tab)) return s;
+  if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
+  const void* sc = nullptr;
+  if (i8) {
+    if (engram_status_t s = device_view(scales, &sc)) return s;
+  }
+  return cuda_status(engram::launch_hash_gather(plan, ids, B, T, proj, V, prev_ids, tab,
+                                                static_cast<const uint16_t*>(sc), e_out, (cudaStream_t)stream));
+}
+
 engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok, const void* w_kv,
                                      void* kv_out, engram_stream_t stream) {
   if (!plan || ntok < 0 || ntok > plan->max_tokens) return ENGRAM_ERR_INVALID_ARG;

@@ -30,7 +30,7 @@
 namespace engram {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarpItems = 4;    // 16-byte chunks per lane per round
 
 __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
@@ -64,30 +64,17 @@ __device__ __forceinline__ void dequant16(uint4 q, float s, uint4& o0, uint4& o1
 }
 
 template <int kCpr, bool kInt8, bool kHash>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
     row_gather_kernel(const __grid_constant__ PlanDev pd, uint32_t* __restrict__ err,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ ids, int T,
                       const int32_t* __restrict__ proj, int V, const int32_t* __restrict__ prev, int64_t ntok,
                       const uint8_t* __restrict__ table, const __half* __restrict__ scales,
                       uint4* __restrict__ out) {
-  __shared__ uint64_t s_mult[kMaxMults];
-  __shared__ uint64_t s_mu[kMaxR];
-  __shared__ int64_t s_off[kMaxR];
-  __shared__ uint32_t s_p[kMaxR];
-  __shared__ int32_t s_mo[kMaxR];      // index of m_{n,k,0} in s_mult for row r
-  __shared__ int32_t s_n[kMaxR];       // order n of row r
+  // The per-row constants are read from the parameter block itself (constant
+  // bank): no shared memory, so blocks start at once and fit beside the K/V
+  // GEMM's blocks on an SM (Stage A of a later layer prefetched on a side stream).
   const int R = pd.R, N = pd.N, K = pd.K;
-  for (int i = threadIdx.x; i < pd.mult_base[N] + K * N; i += blockDim.x) s_mult[i] = pd.mults[i];
-  for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    const int n = 2 + r / K, k = r - (r / K) * K;
-    s_mu[r] = pd.mu[r];
-    s_off[r] = pd.offsets[r];
-    s_p[r] = pd.primes[r];
-    s_n[r] = n;
-    s_mo[r] = pd.mult_base[n] + k * n;
-  }
-  __syncthreads();
-  ptx::grid_dep_wait();       // the set-up above (parameters only) overlaps the previous kernel
+  ptx::grid_dep_wait();
   ptx::grid_dep_launch();
 
   constexpr int kRowBytes = kCpr * 16;
@@ -133,19 +120,19 @@ __global__ void __launch_bounds__(kThreads)
           const int r = f / kCpr;
           const int c = f % kCpr;
           uint32_t z;
+          const int n = 2 + r / K;
           if constexpr (kHash) {
-            const uint64_t* m = s_mult + s_mo[r];
-            const int n = s_n[r];
+            const uint64_t* m = pd.mults + pd.mult_base[n] + (r - (n - 2) * K) * n;
             uint64_t h = 0;
 #pragma unroll
             for (int i = 0; i < kMaxN; ++i)
               if (i < n) h ^= xp[i] * m[i];
-            z = barrett_mod(h, s_p[r], s_mu[r]);
+            z = barrett_mod(h, pd.primes[r], pd.mu[r]);
           } else {
             z = static_cast<uint32_t>(__ldg(idx + tok * R + r));
           }
-          if (z < s_p[r]) {
-            const int64_t row = s_off[r] + z;
+          if (z < pd.primes[r]) {
+            const int64_t row = pd.offsets[r] + z;
             v[j] = ld_stream_16(table + row * kRowBytes + c * 16);
             if constexpr (kInt8) sc[j] = __half2float(scales[row]);
             ok[j] = true;

@@ -189,6 +189,22 @@ class EngramPlan:
                    "engram_gather")
         return out
 
+    def stage_a(self, ids: torch.Tensor, proj: torch.Tensor, table: torch.Tensor,
+                scales: Optional[torch.Tensor] = None, prev_ids: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Steps 1-4 in one kernel: int32 ids [B, T] -> e [B*T, d_mem] (act dtype)."""
+        B, T = ids.shape
+        if out is None:
+            out = torch.empty(B * T, self.d_mem, dtype=self.act_torch_dtype, device=ids.device)
+        prev = 0 if prev_ids is None else _dev(prev_ids, "prev_ids", torch.int32, (B, self.N - 1))
+        tab = _dev_or_pinned(table, "table", _TABLE_DTYPES[self.table_dtype][1])
+        sc = 0 if scales is None else _dev_or_pinned(scales, "scales", torch.float16)
+        _lib.check(self._lib.engram_stage_a(self._h, _dev(ids, "ids", torch.int32), B, T,
+                                            _dev(proj, "proj", torch.int32), proj.numel(), prev, tab, sc,
+                                            _dev(out, "e_out", self.act_torch_dtype, (B * T, self.d_mem)),
+                                            _stream()), "engram_stage_a")
+        return out
+
     def kv_projection(self, e: torch.Tensor, w_kv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Step 5: e [ntok, d_mem] -> kv [ntok, (M+1)d] = e . w_kv^T."""
         ntok = e.shape[0]

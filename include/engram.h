@@ -152,6 +152,21 @@ engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int
                               const void* table, const uint16_t* scales, void* e_out,
                               engram_stream_t stream);
 
+/* Steps 1-4 in one kernel (Stage A of "DeepSeek Engram 系列导读", section
+ * "Engram 工作原理"): the hash of each row is computed inside the gather as the
+ * row is read, so the indices never reach memory.  ids/proj/V/prev_ids as in
+ * engram_hash; table/scales as in engram_gather; e_out: [B*T, d_mem] act_dtype
+ * exactly as engram_gather writes it (16-byte aligned).  Stage A depends on
+ * the tokens only, so a caller can run it for a later layer on another stream
+ * while earlier layers compute (prefetch), then call engram_stage_b.  For a
+ * continued sequence prev_ids must already hold the ids before this chunk
+ * (the state as the previous chunk's Stage B left it).  Errors as in
+ * engram_hash and engram_gather. */
+engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                               const int32_t* proj, int V, const int32_t* prev_ids,
+                               const void* table, const uint16_t* scales, void* e_out,
+                               engram_stream_t stream);
+
 /* Step 5 alone (inspection / reuse of k and v).  e: [ntok, d_mem] act_dtype;
  * w_kv as in engram_weights_t; kv_out: [ntok, (M+1)*d] act_dtype =
  * e . w_kv^T (fp32 accumulation, one rounding to act_dtype), columns [0,d) = v,
@@ -160,7 +175,7 @@ engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, i
                                      const void* w_kv, void* kv_out, engram_stream_t stream);
 
 /* Steps 5-8 from gathered rows (Stage B): for a caller that ran Stage A
- * (engram_hash + engram_gather) ahead of time, e.g. on a side stream while
+ * (engram_stage_a, or engram_hash + engram_gather) ahead of time, e.g. on a side stream while
  * earlier layers computed -- the indices depend on the tokens only.
  * e: [B*T, d_mem] act_dtype as written by engram_gather; w: table/scales are
  * not read (may be NULL); H: [B, T, M, d] act_dtype, updated in place;

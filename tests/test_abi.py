@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes", "engram_hash",
-              "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward", "engram_get_error",
+              "engram_gather", "engram_stage_a", "engram_kv_projection", "engram_stage_b", "engram_forward",
+              "engram_get_error",
               "engram_status_string"):
         assert n in names
 

@@ -114,6 +114,53 @@ def test_small_stage_a_then_stage_b_matches_forward(small):
     assert torch.equal(H, H2)
 
 
+def test_small_stage_a_equals_hash_then_gather(small):
+    name, w, ids, P, L, ref = small
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    e_fused = plan.stage_a(ids_d, proj, weights.table, weights.scales)
+    e_split = plan.gather(plan.hash(ids_d, proj), weights.table, weights.scales)
+    assert torch.equal(e_fused.view(torch.int8), e_split.view(torch.int8))
+    H2 = H.clone()
+    plan.stage_b(e_fused, weights, H2)
+    plan.forward(ids_d, proj, weights, H)
+    assert torch.equal(H, H2)
+
+
+def test_prefetched_stage_a_on_a_side_stream_matches_forward():
+    """Stage A of the second layer runs on another stream while the first layer's
+    Stage B runs; the results equal two sequential forwards bit for bit."""
+    w = SMALL["small_bf16"]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    layers = [W.layer_inputs(w, lid) for lid in (1, 15)]
+    built = [make_layer(w, L, P, ids.size) for L in layers]
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = []
+    for plan, weights, proj, H in built:
+        Hr = H.clone()
+        plan.forward(ids_d, proj, weights, Hr)
+        ref.append(Hr)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    outs = [H.clone() for _, _, _, H in built]
+    es = [torch.empty(ids.size, w.d_mem, dtype=torch.bfloat16, device="cuda") for _ in built]
+    side.wait_stream(main)
+    done = []
+    with torch.cuda.stream(side):
+        for (plan, weights, proj, _), e in zip(built, es):
+            plan.stage_a(ids_d, proj, weights.table, weights.scales, out=e)
+            ev = torch.cuda.Event()
+            ev.record(side)
+            done.append(ev)
+    for (plan, weights, proj, _), e, ev, Ho in zip(built, es, done, outs):
+        main.wait_event(ev)
+        plan.stage_b(e, weights, Ho)
+    torch.cuda.synchronize()
+    for Ho, Hr in zip(outs, ref):
+        assert torch.equal(Ho.view(torch.int16), Hr.view(torch.int16))
+
+
 def test_zero_table_leaves_H_bit_unchanged():
     w = SMALL["small_bf16"]
     ids = W.token_stream(w)
