@@ -284,34 +284,64 @@ def run_ours(args) -> None:
                 "algorithmic_per_token": work[top][1], "units_per_launch": w.ntok}
 
     # ---- end to end through the public API: pinned host in, pinned host out ----
-    e2e_layers = [EngramLayer(ly["plan"], ly["weights"], ly["proj"]) for ly in layers]
+    # EngramLayer.__call__ with H and ids in pinned host memory: the layer runs in
+    # pieces whose copies in and out overlap the computation.  One step (both
+    # layers) is captured in a CUDA graph, as a serving loop would; every replay
+    # copies the step's inputs from the host and the result back.  The piece
+    # count is the API's parameter: the fastest of 1, 2, 4, 8 on a short trial.
     ids_host = torch.from_numpy(ids_np).pin_memory()
     H_out = [ly["H_host"].clone().pin_memory() for ly in layers]
-    Ke = min(K, 200)
-    for _ in range(3):
-        for lay, ly, ho in zip(e2e_layers, layers, H_out):
-            ho.copy_(ly["H_host"])
-            lay(ids_host, ho)
-    torch.cuda.synchronize()
-    e2e_ms = []
-    for i in range(Ke):
-        for ly, ho in zip(layers, H_out):
-            ho.copy_(ly["H_host"])                     # fresh input, host side, untimed
-        flush.zero_()
+
+    def e2e_graph(chunks):
+        e2e_layers = [EngramLayer(ly["plan"], ly["weights"], ly["proj"], chunks=chunks) for ly in layers]
+        for _ in range(3):
+            for lay, ly, ho in zip(e2e_layers, layers, H_out):
+                ho.copy_(ly["H_host"])
+                lay(ids_host, ho)
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for lay, ho in zip(e2e_layers, H_out):
-            lay(ids_host, ho)
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e_step = max_over_ranks(sum(e2e_ms) / Ke, world, dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for lay, ho in zip(e2e_layers, H_out):
+                lay(ids_host, ho)
+        torch.cuda.synchronize()
+        return g
+
+    def e2e_time(g, reps):
+        ms = []
+        for _ in range(reps):
+            for ly, ho in zip(layers, H_out):
+                ho.copy_(ly["H_host"])                 # fresh input, host side, untimed
+            flush.zero_()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return sum(ms) / len(ms)
+
+    trial = {c: e2e_time(e2e_graph(c), 10) for c in (1, 2, 4, 8)}
+    chunks = min(trial, key=trial.get)
+    g_e2e = e2e_graph(chunks)
+    e2e_step = max_over_ranks(e2e_time(g_e2e, min(K, 200)), world, dev)
+    for ly, ho in zip(layers, H_out):                  # the pipelined result is the layer's result
+        ref = ly["H_host"].cuda()
+        ly["plan"].forward(ids, ly["proj"], ly["weights"], ref, None, ly["ws"])
+        ho.copy_(ly["H_host"])
+    g_e2e.replay()
+    torch.cuda.synchronize()
+    for ly, ho in zip(layers, H_out):
+        ref = ly["H_host"].cuda()
+        ly["plan"].forward(ids, ly["proj"], ly["weights"], ref, None, ly["ws"])
+        assert torch.equal(ho.view(torch.int16), ref.cpu().view(torch.int16)), "e2e result differs"
     h2d = len(layers) * (ids_host.numel() * 4 + layers[0]["H_host"].numel() * 2)
     d2h = len(layers) * layers[0]["H_host"].numel() * 2
     e2e = {"value": round(world * tokens_per_step / (e2e_step / 1e3), 1), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_step, 5),
-           "path": "EngramLayer.__call__ (pinned host ids/H -> device -> engram_forward -> host)"}
+           "path": f"EngramLayer.__call__ per layer, CUDA graph of the step: pinned host ids/H copied in, the "
+                   f"layer, H copied back, in {chunks} overlapped pieces",
+           "pieces_trial_ms": {str(c): round(v, 5) for c, v in trial.items()}}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
@@ -335,10 +365,11 @@ def run_ours(args) -> None:
 # --------------------------------------------------------------------------- #
 # the CPU oracle: baseline leg and reference arm
 # --------------------------------------------------------------------------- #
-def oracle_sample_seconds(T_sample: int, repeats: int = 1):
+def oracle_sample_seconds(T_sample: int, repeats: int = 1, min_seconds: float = 0.0):
     """Time the oracle on the first T_sample tokens of the workload, both layers.
 
-    Input generation is excluded; returns (seconds per pass, token-layers per pass)."""
+    Runs ``repeats`` passes, and more until ``min_seconds`` have elapsed.  Input
+    generation is excluded; returns (seconds per pass, token-layers per pass)."""
     import copy
     import workloads as W
     from oracle import engram_oracle as O
@@ -352,7 +383,7 @@ def oracle_sample_seconds(T_sample: int, repeats: int = 1):
         Lc.H = L.H[:, :T_sample]
         Ls.append(Lc)
     times = []
-    for _ in range(repeats):
+    while len(times) < repeats or sum(times) < min_seconds:
         t0 = time.perf_counter()
         for L in Ls:
             O.forward(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype)
@@ -366,16 +397,18 @@ def cpu_baseline_subprocess(w) -> dict:
     env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
                MKL_NUM_THREADS=str(threads), CUDA_VISIBLE_DEVICES="")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "t, n = bench.oracle_sample_seconds(%d, 5); print(json.dumps({'t': t, 'n': n}))") % (ROOT, w.T)
+            "t, n = bench.oracle_sample_seconds(%d, 3, 12.0); print(json.dumps({'t': t, 'n': n}))") % (ROOT, w.T)
     try:
         r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
         res = json.loads(r.stdout.strip().splitlines()[-1])
     except Exception as exc:  # the baseline must never sink the GPU line
         return {"value": None, "unit": UNIT, "cores": threads, "kind": "oracle", "error": str(exc)[:200]}
-    best = min(res["t"])
-    return {"value": round(res["n"] / best, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"full workload ({w.T} tokens x {len(w.layers)} layers), float64 numpy oracle, "
-                      f"best of 5 passes ({best:.2f} s each), BLAS threads = {threads}, input generation excluded"}
+    total = sum(res["t"])
+    passes = len(res["t"])
+    return {"value": round(res["n"] * passes / total, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full workload ({w.T} tokens x {len(w.layers)} layers) repeated {passes} times "
+                      f"({total:.1f} s of CPU time, mean rate), float64 numpy oracle, BLAS threads = {threads}, "
+                      f"input generation excluded"}
 
 
 def run_reference(args) -> None:
@@ -408,6 +441,150 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- #
+# the other workloads (not the headline line): decode, int8 host tables, multi-branch
+# --------------------------------------------------------------------------- #
+def run_workload(args) -> None:
+    """One JSON line for a non-default workload: its tokens x layers per second
+    through the same Stage A (side stream) + Stage B step, plus what that
+    workload is about -- decode: us and table rows per step; int8_host: the
+    UVA run (rows in pinned host memory, the workload's definition) beside the
+    HBM copy of the same table, the gather's achieved host-link GB/s and a
+    pinned-host-to-device copy rate measured in the same run."""
+    import torch
+    import workloads as W
+    from hashed_gram_embedding_engram_gb300 import EngramState
+    from tests.gpu_helpers import make_layer, to_torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.BY_NAME[args.workload]
+    decode = w.prefix_len > 0
+    T_all = w.prefix_len + w.T
+    ids_np = W.token_stream(w, T=T_all) if decode else W.token_stream(w)
+    P = W.projection_map(w)
+    layers = []
+    for lid in w.layers:
+        L = W.layer_inputs(w, lid, T=T_all) if decode else W.layer_inputs(w, lid)
+        plan, weights, proj, H = make_layer(w, L, P, w.B * T_all)
+        ly = {"plan": plan, "weights": weights, "proj": proj, "ws": plan.new_workspace(w.B * T_all),
+              "e": torch.empty(w.ntok, w.d_mem, dtype=plan.act_torch_dtype, device=dev)}
+        if w.table_in_host:
+            ly["table_host"] = to_torch(L.table, w.table_dtype, "cpu", pin=True)
+            ly["table_dev"] = weights.table
+        if decode:
+            ly["state"] = EngramState.zeros(plan, w.B)
+            pre = H[:, :w.prefix_len].contiguous()
+            plan.forward(torch.from_numpy(ids_np[:, :w.prefix_len].copy()).to(dev), proj, weights, pre, ly["state"])
+            ly["H0"] = H[:, w.prefix_len:].contiguous()
+        else:
+            ly["H0"] = H
+        ly["H"] = ly["H0"].clone()
+        layers.append(ly)
+        del L
+    ids = torch.from_numpy(ids_np[:, w.prefix_len:].copy()).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+
+    def step(table_key=None):
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        ready = []
+        with torch.cuda.stream(side):
+            for ly in layers:
+                st = ly.get("state")
+                table = ly[table_key] if table_key else ly["weights"].table
+                ly["plan"].stage_a(ids, ly["proj"], table, ly["weights"].scales,
+                                   prev_ids=None if st is None else st.prev_ids, out=ly["e"])
+                ev = torch.cuda.Event()
+                ev.record(side)
+                ready.append(ev)
+        for ly, ev in zip(layers, ready):
+            main.wait_event(ev)
+            ly["plan"].stage_b(ly["e"], ly["weights"], ly["H"], ly.get("state"), ids=ids, proj=ly["proj"],
+                               workspace=ly["ws"])
+
+    def restore():
+        for ly in layers:
+            ly["H"].copy_(ly["H0"])
+
+    def timed(table_key=None, K=args.steps):
+        for _ in range(max(3, args.warmup)):
+            restore()
+            step(table_key)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            step(table_key)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            restore()
+            flush.zero_()
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        for ly in layers:
+            st_, flags = ly["plan"].get_error()
+            assert st_ == 0, f"device error flags {flags}"
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    key = "table_host" if w.table_in_host else None
+    ms = timed(key)
+    clocks = sampler.stop()
+    tokens_per_step = w.ntok * len(w.layers)
+    value = tokens_per_step / (ms / 1e3)
+    extra = {}
+    if decode:
+        rows = w.B * w.R * len(w.layers)
+        extra["decode"] = {"us_per_step": round(ms * 1e3, 2), "table_rows_per_step": rows,
+                           "table_rows_per_s": round(rows / (ms / 1e3), 1),
+                           "note": f"{w.B} sequences, one new token each after a {w.prefix_len}-token prefix, "
+                                   f"state carried between steps"}
+    if w.table_in_host:
+        ms_hbm = timed("table_dev")
+        # the gather alone over UVA: the host link carries the rows, the scales stay in HBM
+        ly = layers[0]
+        Kg = min(args.steps, 50)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            ly["plan"].stage_a(ids, ly["proj"], ly["table_host"], ly["weights"].scales, out=ly["e"])
+        g0.record()
+        for _ in range(Kg):
+            ly["plan"].stage_a(ids, ly["proj"], ly["table_host"], ly["weights"].scales, out=ly["e"])
+        g1.record()
+        g1.synchronize()
+        g_ms = g0.elapsed_time(g1) / Kg
+        row_bytes = w.row_dim  # int8 rows
+        host = torch.empty(1 << 28, dtype=torch.uint8).pin_memory()
+        devb = torch.empty(1 << 28, dtype=torch.uint8, device=dev)
+        devb.copy_(host, non_blocking=True)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(5):
+            devb.copy_(host, non_blocking=True)
+        c1.record()
+        c1.synchronize()
+        h2d = 5 * (1 << 28) / (c0.elapsed_time(c1) / 1e3) / 1e9
+        extra["uva"] = {"tables": "int8 rows in pinned host memory read over UVA (C2C), fp16 scales in HBM",
+                        "ms_per_step": round(ms, 5), "hbm_table_ms_per_step": round(ms_hbm, 5),
+                        "hbm_table_value": round(tokens_per_step / (ms_hbm / 1e3), 1),
+                        "gather_ms": round(g_ms, 5),
+                        "gather_host_link_gbs": round(w.ntok * w.R * row_bytes / (g_ms / 1e3) / 1e9, 1),
+                        "h2d_copy_gbs": round(h2d, 1)}
+    line = {"metric": f"Engram-layer tokens/s, {w.name} workload", "value": round(value, 1), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.act_dtype, "data": "synthetic",
+            "config": dict(workload_desc(w), cuda_graph=True,
+                           stage_a="every layer's hash+gather on a side stream, ahead of its Stage B"),
+            "clocks": clocks, **extra}
+    print(json.dumps(line), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,11 +592,16 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="prefill_bf16",
+                    help="prefill_bf16 (the headline line); decode_bf16, int8_host or multibranch_n4 print "
+                         "that workload's own line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "prefill_bf16":
+        run_workload(args)
     else:
         run_ours(args)
 

@@ -269,13 +269,21 @@ class EngramPlan:
 class EngramLayer:
     """A plan, its weights, the projection map and a reusable workspace.
 
-    Calling it runs the whole layer; inputs on the host are copied to the
-    device on the current stream and H is copied back into the caller's host
-    tensor (use pinned host tensors for asynchronous copies)."""
+    Calling it runs the whole layer.  With H on the device it is one
+    engram_forward.  With H (and ids) in host memory the layer is pipelined
+    in ``chunks`` pieces over three streams: the copy of piece i+1 to the
+    device, the layer on piece i and the copy of piece i-1 back to the host
+    overlap (use pinned host tensors, or the copies serialise).  Pieces split
+    the batch when B >= chunks (sequences are independent), else the
+    positions of a single-sequence batch with a streaming state carried from
+    piece to piece; both give the bits of one whole-batch call."""
 
-    def __init__(self, plan: EngramPlan, weights: EngramWeights, proj: torch.Tensor):
+    def __init__(self, plan: EngramPlan, weights: EngramWeights, proj: torch.Tensor, chunks: int = 4):
         self.plan, self.weights, self.proj = plan, weights, proj
+        self.chunks = max(1, int(chunks))
         self._ws = None
+        self._dev_buf = None
+        self._streams = None
 
     def workspace(self, ntok: int, device) -> torch.Tensor:
         need = self.plan.workspace_bytes(ntok)
@@ -283,12 +291,57 @@ class EngramLayer:
             self._ws = torch.empty(max(1, need), dtype=torch.uint8, device=device)
         return self._ws
 
+    def _buffers(self, ids: torch.Tensor, H: torch.Tensor, dev):
+        key = (tuple(ids.shape), tuple(H.shape), H.dtype)
+        if self._dev_buf is None or self._dev_buf[0] != key:
+            self._dev_buf = (key, torch.empty(ids.shape, dtype=ids.dtype, device=dev),
+                             torch.empty(H.shape, dtype=H.dtype, device=dev))
+        if self._streams is None:
+            self._streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        return self._dev_buf[1], self._dev_buf[2]
+
     def __call__(self, ids: torch.Tensor, H: torch.Tensor, state: Optional[EngramState] = None) -> torch.Tensor:
         dev = self.proj.device
-        ids_d = ids if ids.is_cuda else ids.to(dev, non_blocking=True)
-        H_d = H if H.is_cuda else H.to(dev, non_blocking=True)
-        self.plan.forward(ids_d, self.proj, self.weights, H_d, state, self.workspace(ids.numel(), dev))
-        if not H.is_cuda:
-            H.copy_(H_d, non_blocking=True)
+        if H.is_cuda:
+            ids_d = ids if ids.is_cuda else ids.to(dev, non_blocking=True)
+            self.plan.forward(ids_d, self.proj, self.weights, H, state, self.workspace(ids.numel(), dev))
             return H
-        return H_d
+        B, T = ids.shape
+        if B >= self.chunks and self.chunks > 1:
+            cuts = [(B * i // self.chunks, B * (i + 1) // self.chunks) for i in range(self.chunks)]
+            along_b = True
+        elif B == 1 and state is None and self.chunks > 1 and T >= self.chunks:
+            cuts = [(T * i // self.chunks, T * (i + 1) // self.chunks) for i in range(self.chunks)]
+            along_b = False
+        else:
+            cuts = [(0, B)]
+            along_b = True
+        ids_h = ids if not ids.is_cuda else ids.cpu()
+        ids_d, H_d = self._buffers(ids_h, H, dev)
+        s_in, s_out = self._streams
+        main = torch.cuda.current_stream(dev)
+        s_in.wait_stream(main)                    # device buffers free: the previous call joined main
+        st = None if along_b else EngramState.zeros(self.plan, 1, dev)
+        ws = self.workspace(max(hi - lo for lo, hi in cuts) * (T if along_b else 1), dev)
+        last_out = None
+        for lo, hi in cuts:
+            sl = (slice(lo, hi), slice(None)) if along_b else (slice(None), slice(lo, hi))
+            i_h, i_d = ids_h[sl], ids_d[sl]
+            h_h, h_d = H[sl], H_d[sl]
+            with torch.cuda.stream(s_in):
+                i_d.copy_(i_h, non_blocking=True)
+                h_d.copy_(h_h, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            main.wait_event(ready)
+            i_c, h_c = (i_d, h_d) if along_b else (i_d.contiguous(), h_d.contiguous())
+            self.plan.forward(i_c, self.proj, self.weights, h_c, state if along_b else st, ws)
+            done = torch.cuda.Event()
+            done.record(main)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                h_h.copy_(h_c, non_blocking=True)
+                last_out = torch.cuda.Event()
+                last_out.record(s_out)
+        main.wait_event(last_out)                 # the host copy is complete when main's work is
+        return H

@@ -299,6 +299,30 @@ def test_streaming_bit_identical_across_gemm_tile_widths():
     assert_close(got, ref, "bf16", "sampled")
 
 
+@pytest.mark.parametrize("B,T,chunks", [(1, 333, 4), (6, 40, 4), (3, 50, 1)])
+def test_layer_pipelines_host_inputs_bit_exactly(B, T, chunks):
+    """EngramLayer with H in pinned host memory (pieces of the batch or of the one
+    sequence copied in, computed and copied back on three streams) equals one
+    device-resident forward bit for bit."""
+    from hashed_gram_embedding_engram_gb300 import EngramLayer
+    w = SMALL["small_bf16"].scaled(B=B, T=T)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    ref = H.clone()
+    plan.forward(torch.from_numpy(ids).cuda(), proj, weights, ref)
+    layer = EngramLayer(plan, weights, proj, chunks=chunks)
+    ids_h = torch.from_numpy(ids).pin_memory()
+    H_h = H.cpu().pin_memory()
+    for _ in range(2):                        # twice: buffers and streams are reused
+        out = H.cpu().pin_memory()
+        layer(ids_h, out)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
+    assert torch.equal(H_h.view(torch.int16), H.cpu().view(torch.int16))   # the caller's input untouched
+
+
 # --------------------------------------------------------------------------- #
 # UVA: host-resident tables
 # --------------------------------------------------------------------------- #
