@@ -19,7 +19,8 @@ F32, BF16, I8_ROWSCALE_F16 = 0, 1, 2
 EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes",
            "engram_hash", "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward",
            "engram_get_error", "engram_plan_set_timing", "engram_plan_kernel_times",
-           "engram_forward_static_scratch", "engram_stage_a")
+           "engram_forward_static_scratch", "engram_stage_a", "engram_cache_create", "engram_cache_destroy",
+           "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats")
 
 
 class Config(ctypes.Structure):
@@ -67,6 +68,13 @@ def _lib() -> ctypes.CDLL:
         lib.engram_gather.argtypes = [vp, vp, i64, vp, vp, vp, vp]
         lib.engram_kv_projection.argtypes = [vp, vp, i64, vp, vp, vp]
         lib.engram_stage_a.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
+        lib.engram_cache_create.argtypes = [vp, i64, vp, ctypes.POINTER(vp)]
+        lib.engram_cache_destroy.argtypes = [vp]
+        lib.engram_cache_observe.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
+        lib.engram_cache_build.argtypes = [vp, i32, vp, ctypes.POINTER(i64)]
+        lib.engram_stage_a_cached.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp]
+        lib.engram_cache_stats.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_uint64),
+                                           ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(i64)]
         lib.engram_stage_b.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.POINTER(Weights), vp,
                                        ctypes.POINTER(State), vp, sz, vp]
         lib.engram_forward.argtypes = [vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,

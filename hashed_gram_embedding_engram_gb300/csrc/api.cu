@@ -378,6 +378,114 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   return run_stage_b(plan, ws, ws.e, ids, proj, V, B, T, w, H, state, s);
 }
 
+}  // extern "C"
+
+struct engram_cache {
+  const engram_plan* plan;
+  int64_t capacity;
+  int row_bytes;
+  const void* table;                 // device view of the table
+  uint32_t* counts;                  // [total rows]
+  int32_t* slot;                     // [total rows]
+  void* rows;                        // [capacity, row_bytes]
+  unsigned long long* stats;         // [0] lookups, [1] hits, [2] slots used by the last build
+  int64_t cached;
+};
+
+extern "C" {
+
+engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity, const void* table,
+                                    engram_cache_t** out) {
+  if (!plan || !table || !out) return ENGRAM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (capacity <= 0 || capacity > plan->total_rows || capacity > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
+  const void* tab = nullptr;
+  if (engram_status_t s = device_view(table, &tab)) return s;
+  if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
+  engram_cache* c = new (std::nothrow) engram_cache();
+  if (!c) return ENGRAM_ERR_CUDA;
+  c->plan = plan;
+  c->capacity = capacity;
+  c->row_bytes = static_cast<int>(plan->cfg.row_dim * table_elem_bytes(plan->cfg.table_dtype));
+  c->table = tab;
+  const size_t n = static_cast<size_t>(plan->total_rows);
+  bool ok = cudaMalloc(&c->counts, n * sizeof(uint32_t)) == cudaSuccess &&
+            cudaMalloc(&c->slot, n * sizeof(int32_t)) == cudaSuccess &&
+            cudaMalloc(&c->rows, static_cast<size_t>(capacity) * c->row_bytes) == cudaSuccess &&
+            cudaMalloc(&c->stats, 4 * sizeof(unsigned long long)) == cudaSuccess;
+  ok = ok && cudaMemset(c->counts, 0, n * sizeof(uint32_t)) == cudaSuccess &&
+       cudaMemset(c->slot, 0xFF, n * sizeof(int32_t)) == cudaSuccess &&
+       cudaMemset(c->stats, 0, 4 * sizeof(unsigned long long)) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    engram_cache_destroy(c);
+    return ENGRAM_ERR_CUDA;
+  }
+  *out = c;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_cache_destroy(engram_cache_t* c) {
+  if (!c) return ENGRAM_OK;
+  cudaError_t e = cudaSuccess;
+  for (void* ptr : {static_cast<void*>(c->counts), static_cast<void*>(c->slot), c->rows, static_cast<void*>(c->stats)})
+    if (ptr && cudaFree(ptr) != cudaSuccess) e = cudaErrorUnknown;
+  delete c;
+  return cuda_status(e);
+}
+
+engram_status_t engram_cache_observe(engram_cache_t* c, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                                     const int32_t* prev_ids, engram_stream_t stream) {
+  if (!c) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_tokens(c->plan, B, T)) return s;
+  if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
+  if (!ids || !proj || V <= 0) return ENGRAM_ERR_INVALID_ARG;
+  return cuda_status(engram::cache_observe(c->plan, ids, B, T, proj, V, prev_ids, c->counts, (cudaStream_t)stream));
+}
+
+engram_status_t engram_cache_build(engram_cache_t* c, int decay, engram_stream_t stream, int64_t* cached_rows) {
+  if (!c) return ENGRAM_ERR_INVALID_ARG;
+  int64_t cached = 0;
+  if (engram::cache_build(c->plan, c->capacity, c->row_bytes, c->table, c->counts, c->slot, c->rows, c->stats + 2,
+                          decay, &cached, (cudaStream_t)stream) != cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  c->cached = cached;
+  if (cached_rows) *cached_rows = cached;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_stage_a_cached(const engram_cache_t* c, const int32_t* ids, int B, int T, const int32_t* proj,
+                                      int V, const int32_t* prev_ids, const uint16_t* scales, void* e_out,
+                                      engram_stream_t stream) {
+  if (!c) return ENGRAM_ERR_INVALID_ARG;
+  const engram_plan* plan = c->plan;
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
+  if (!ids || !proj || V <= 0 || !e_out || !aligned16(e_out)) return ENGRAM_ERR_INVALID_ARG;
+  const bool i8 = plan->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
+  if (i8 != (scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
+  const void* sc = nullptr;
+  if (i8) {
+    if (engram_status_t s = device_view(scales, &sc)) return s;
+  }
+  return cuda_status(engram::launch_hash_gather_cached(plan, ids, B, T, proj, V, prev_ids, c->table,
+                                                       static_cast<const uint16_t*>(sc), e_out, c->slot, c->rows,
+                                                       c->stats, (cudaStream_t)stream));
+}
+
+engram_status_t engram_cache_stats(const engram_cache_t* c, engram_stream_t stream, int reset,
+                                   uint64_t* rows_looked_up, uint64_t* rows_from_hbm, int64_t* cached_rows) {
+  if (!c) return ENGRAM_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  unsigned long long st[2] = {0, 0};
+  if (cudaMemcpy(st, c->stats, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (reset && cudaMemset(c->stats, 0, sizeof(st)) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (rows_looked_up) *rows_looked_up = st[0];
+  if (rows_from_hbm) *rows_from_hbm = st[1];
+  if (cached_rows) *cached_rows = c->cached;
+  return ENGRAM_OK;
+}
+
 engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable) {
   if (!plan) return ENGRAM_ERR_INVALID_ARG;
   if (enable && !plan->timing) {

@@ -101,6 +101,17 @@ cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok
 cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                                const int32_t* prev_ids, const void* table, const uint16_t* scales, void* e,
                                cudaStream_t s);
+// The same through the HBM hot-row cache (slot map, cached rows, [lookups, hits] counters).
+cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj,
+                                      int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,
+                                      void* e, const int32_t* slot, const void* rows, unsigned long long* stats,
+                                      cudaStream_t s);
+// Hot-row cache maintenance (cache.cu).
+cudaError_t cache_observe(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                          const int32_t* prev_ids, uint32_t* counts, cudaStream_t s);
+cudaError_t cache_build(const engram_plan* p, int64_t capacity, int row_bytes, const void* table, uint32_t* counts,
+                        int32_t* slot, void* rows, unsigned long long* used, int decay, int64_t* cached,
+                        cudaStream_t s);
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
                                  cudaStream_t s);
 // Floats per row of the per-token gate scalars: [s^(1..M), alpha^(1..M)] padded to 16 bytes.

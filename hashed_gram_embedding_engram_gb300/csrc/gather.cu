@@ -17,8 +17,8 @@
 // be read, Steps 1-3 -- the arithmetic of hashing.cuh -- so they never
 // travel through HBM).  There the warp first loads the token's n-gram window
 // (lane i holds x'_{t-i}) and broadcasts it by shuffle; each lane computes the
-// index of its chunk's row from per-row constants in shared memory (the lanes
-// of one row compute the same index in the same instructions).
+// index of its chunk's row from the per-row constants of the parameter block
+// (the lanes of one row compute the same index in the same instructions).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -63,13 +63,21 @@ __device__ __forceinline__ void dequant16(uint4 q, float s, uint4& o0, uint4& o1
   o1 = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
-template <int kCpr, bool kInt8, bool kHash>
+// Rows of a table in host memory that have a slot in the HBM hot-row cache
+// (cache.cu) are read from there instead; the bytes are the same.
+struct RowCache {
+  const int32_t* slot;               // [total rows]: slot or -1
+  const uint8_t* rows;               // [capacity, row bytes] in HBM
+  unsigned long long* stats;         // [2]: rows looked up, rows served from HBM
+};
+
+template <int kCpr, bool kInt8, bool kHash, bool kCache = false>
 __global__ void __launch_bounds__(kThreads, 8)
     row_gather_kernel(const __grid_constant__ PlanDev pd, uint32_t* __restrict__ err,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ ids, int T,
                       const int32_t* __restrict__ proj, int V, const int32_t* __restrict__ prev, int64_t ntok,
                       const uint8_t* __restrict__ table, const __half* __restrict__ scales,
-                      uint4* __restrict__ out) {
+                      uint4* __restrict__ out, const RowCache cache) {
   // The per-row constants are read from the parameter block itself (constant
   // bank): no shared memory, so blocks start at once and fit beside the K/V
   // GEMM's blocks on an SM (Stage A of a later layer prefetched on a side stream).
@@ -82,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 8)
   const int per_tok = R * kCpr;
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   bool bad = false;
+  uint32_t n_look = 0, n_hit = 0;                       // rows of this lane's chunks 0 (kCache)
   for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
        tok += n_warps) {
     uint64_t xp[kMaxN];
@@ -133,7 +142,16 @@ __global__ void __launch_bounds__(kThreads, 8)
           }
           if (z < pd.primes[r]) {
             const int64_t row = pd.offsets[r] + z;
-            v[j] = ld_stream_16(table + row * kRowBytes + c * 16);
+            const uint8_t* src = table + row * kRowBytes;
+            if constexpr (kCache) {
+              const int32_t sl = __ldg(cache.slot + row);
+              if (sl >= 0) src = cache.rows + static_cast<int64_t>(sl) * kRowBytes;
+              if (c == 0) {
+                ++n_look;
+                n_hit += sl >= 0;
+              }
+            }
+            v[j] = ld_stream_16(src + c * 16);
             if constexpr (kInt8) sc[j] = __half2float(scales[row]);
             ok[j] = true;
           } else {
@@ -158,6 +176,17 @@ __global__ void __launch_bounds__(kThreads, 8)
     }
   }
   if (bad) atomicOr(err, kErrIndexRange);
+  if constexpr (kCache) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n_look += __shfl_xor_sync(0xFFFFFFFFu, n_look, o);
+      n_hit += __shfl_xor_sync(0xFFFFFFFFu, n_hit, o);
+    }
+    if (lane == 0 && n_look) {
+      atomicAdd(cache.stats, static_cast<unsigned long long>(n_look));
+      atomicAdd(cache.stats + 1, static_cast<unsigned long long>(n_hit));
+    }
+  }
 }
 
 int grid_for_tokens(const engram_plan* p, int64_t ntok) {
@@ -175,7 +204,7 @@ cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, c
                     p->host, &p->dev->err, static_cast<const int32_t*>(idx), static_cast<const int32_t*>(nullptr), 1,
                     static_cast<const int32_t*>(nullptr), 0, static_cast<const int32_t*>(nullptr), ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
-                    static_cast<uint4*>(e));
+                    static_cast<uint4*>(e), RowCache{});
 }
 
 template <int kCpr, bool kInt8>
@@ -185,7 +214,18 @@ cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T,
   return launch_pdl(row_gather_kernel<kCpr, kInt8, true>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
                     p->host, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T, proj, V, prev, ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
-                    static_cast<uint4*>(e));
+                    static_cast<uint4*>(e), RowCache{});
+}
+
+template <int kCpr, bool kInt8>
+cudaError_t launch_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                          const int32_t* prev, const void* table, const uint16_t* scales, void* e,
+                          const RowCache& cache, cudaStream_t s) {
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  return launch_pdl(row_gather_kernel<kCpr, kInt8, true, true>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+                    p->host, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T, proj, V, prev, ntok,
+                    static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
+                    static_cast<uint4*>(e), cache);
 }
 
 int chunks_per_row(const engram_plan* p) {
@@ -218,6 +258,17 @@ cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, 
                                cudaStream_t s) {
   const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
 #define CALL(C, I) launch_fused<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, s)
+  ENGRAM_DISPATCH_CPR(CALL)
+#undef CALL
+}
+
+cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj,
+                                      int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,
+                                      void* e, const int32_t* slot, const void* rows, unsigned long long* stats,
+                                      cudaStream_t s) {
+  const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
+  const RowCache cache{slot, static_cast<const uint8_t*>(rows), stats};
+#define CALL(C, I) launch_cached<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, cache, s)
   ENGRAM_DISPATCH_CPR(CALL)
 #undef CALL
 }

@@ -266,6 +266,66 @@ class EngramPlan:
         return st, flags.value
 
 
+class EngramCache:
+    """HBM hot-row cache in front of a host-resident table (engram_cache_* in
+    include/engram.h): observe batches, build (LFU admission), then
+    ``stage_a`` reads cached rows from HBM and the others over the host link."""
+
+    def __init__(self, plan: "EngramPlan", capacity: int, table: torch.Tensor):
+        self.plan = plan
+        self._lib = _lib._lib()
+        self._table = table                      # kept alive: the cache reads it
+        tab = _dev_or_pinned(table, "table", _TABLE_DTYPES[plan.table_dtype][1])
+        h = ctypes.c_void_p()
+        _lib.check(self._lib.engram_cache_create(plan._h, int(capacity), tab, ctypes.byref(h)), "engram_cache_create")
+        self._h = h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            _lib.check(self._lib.engram_cache_destroy(self._h), "engram_cache_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def observe(self, ids: torch.Tensor, proj: torch.Tensor, prev_ids: Optional[torch.Tensor] = None) -> None:
+        B, T = ids.shape
+        prev = 0 if prev_ids is None else _dev(prev_ids, "prev_ids", torch.int32, (B, self.plan.N - 1))
+        _lib.check(self._lib.engram_cache_observe(self._h, _dev(ids, "ids", torch.int32), B, T,
+                                                  _dev(proj, "proj", torch.int32), proj.numel(), prev, _stream()),
+                   "engram_cache_observe")
+
+    def build(self, decay: bool = False) -> int:
+        n = ctypes.c_int64()
+        _lib.check(self._lib.engram_cache_build(self._h, int(bool(decay)), _stream(), ctypes.byref(n)),
+                   "engram_cache_build")
+        return n.value
+
+    def stage_a(self, ids: torch.Tensor, proj: torch.Tensor, scales: Optional[torch.Tensor] = None,
+                prev_ids: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        plan = self.plan
+        B, T = ids.shape
+        if out is None:
+            out = torch.empty(B * T, plan.d_mem, dtype=plan.act_torch_dtype, device=ids.device)
+        prev = 0 if prev_ids is None else _dev(prev_ids, "prev_ids", torch.int32, (B, plan.N - 1))
+        sc = 0 if scales is None else _dev_or_pinned(scales, "scales", torch.float16)
+        _lib.check(self._lib.engram_stage_a_cached(self._h, _dev(ids, "ids", torch.int32), B, T,
+                                                   _dev(proj, "proj", torch.int32), proj.numel(), prev, sc,
+                                                   _dev(out, "e_out", plan.act_torch_dtype, (B * T, plan.d_mem)),
+                                                   _stream()), "engram_stage_a_cached")
+        return out
+
+    def stats(self, reset: bool = False) -> Tuple[int, int, int]:
+        """(rows looked up, rows served from HBM, rows cached) since the last reset."""
+        a, b, c = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_int64()
+        _lib.check(self._lib.engram_cache_stats(self._h, _stream(), int(bool(reset)), ctypes.byref(a), ctypes.byref(b),
+                                                ctypes.byref(c)), "engram_cache_stats")
+        return a.value, b.value, c.value
+
+
 class EngramLayer:
     """A plan, its weights, the projection map and a reusable workspace.
 

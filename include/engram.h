@@ -223,6 +223,51 @@ engram_status_t engram_forward_static_scratch(const engram_plan_t* plan, const i
                                               const int32_t* proj, int V, const engram_weights_t* w,
                                               void* H, engram_state_t* state, engram_stream_t stream);
 
+/* HBM hot-row cache in front of a table held in host memory (the UVA path).
+ * The pages keep Engram tables in host DRAM and read rows over the host link
+ * ("Engram 嵌入扩展：面向高效 DRAM/SSD 卸载的协同设计", section "AgentX Engram
+ * DRAM卸载提升性能"), and keep Zipf-hot rows in device memory (the Ascend
+ * RecSDK Engram blog).  The cache holds up to `capacity` rows of `plan`'s
+ * table in HBM; which rows is decided by counting (LFU): engram_cache_observe
+ * counts the rows a batch will read, engram_cache_build admits the most-counted
+ * rows.  engram_stage_a_cached then reads cached rows from HBM and the rest
+ * from the host table; its output equals engram_stage_a's bit for bit.
+ * Device memory: 8 bytes per table row (counts and slot map) plus capacity
+ * rows.  A cache belongs to one plan and one table; calls on it are
+ * stream-ordered; engram_cache_build synchronises `stream`. */
+typedef struct engram_cache engram_cache_t;
+
+/* table: the plan's table in pinned or registered host memory (or on the
+ * device); capacity: rows, 0 < capacity <= total rows.  Starts empty, counts 0. */
+engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity, const void* table,
+                                    engram_cache_t** out);
+engram_status_t engram_cache_destroy(engram_cache_t* cache);
+
+/* Add one count to every table row the tokens read (ids/proj/V/prev_ids as
+ * in engram_hash). */
+engram_status_t engram_cache_observe(engram_cache_t* cache, const int32_t* ids, int B, int T,
+                                     const int32_t* proj, int V, const int32_t* prev_ids,
+                                     engram_stream_t stream);
+
+/* Re-admit: the rows with the highest counts (all rows above a count
+ * threshold, then rows one below it while slots remain) are copied into the
+ * cache; every other row is read from the host table.  decay != 0 halves all
+ * counts afterwards (aging).  cached_rows (optional): rows now cached. */
+engram_status_t engram_cache_build(engram_cache_t* cache, int decay, engram_stream_t stream,
+                                   int64_t* cached_rows);
+
+/* engram_stage_a with the cache's table, cached rows read from HBM.  scales:
+ * as in engram_gather (fp16 per row, HBM or mapped host memory; I8 only). */
+engram_status_t engram_stage_a_cached(const engram_cache_t* cache, const int32_t* ids, int B, int T,
+                                      const int32_t* proj, int V, const int32_t* prev_ids,
+                                      const uint16_t* scales, void* e_out, engram_stream_t stream);
+
+/* Synchronise `stream` and read the counters of engram_stage_a_cached since
+ * the last reset: table rows looked up and rows served from HBM; reset != 0
+ * zeroes them.  Any output pointer may be NULL. */
+engram_status_t engram_cache_stats(const engram_cache_t* cache, engram_stream_t stream, int reset,
+                                   uint64_t* rows_looked_up, uint64_t* rows_from_hbm, int64_t* cached_rows);
+
 /* Tracing.  With timing on, engram_forward / engram_stage_b record one of
  * the plan's CUDA events on `stream` before the first kernel and after every
  * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes", "engram_hash",
               "engram_gather", "engram_stage_a", "engram_kv_projection", "engram_stage_b", "engram_forward",
-              "engram_get_error",
+              "engram_get_error", "engram_cache_create", "engram_cache_observe", "engram_cache_build",
+              "engram_stage_a_cached", "engram_cache_stats", "engram_cache_destroy",
               "engram_status_string"):
         assert n in names
 

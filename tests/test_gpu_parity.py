@@ -340,3 +340,58 @@ def test_uva_gather_equals_hbm_gather():
     e_mix = plan.gather(idx, table_host, wd.scales)
     assert torch.equal(e_dev.view(torch.int16), e_host.view(torch.int16))
     assert torch.equal(e_dev.view(torch.int16), e_mix.view(torch.int16))
+
+
+# --------------------------------------------------------------------------- #
+# HBM hot-row cache in front of host tables
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("kind", ["small_i8", "small_bf16"])
+def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
+    """Rows read through the cache are the rows of the table: the cached Stage A
+    equals the plain one (host table over UVA, and the HBM copy) bit for bit,
+    before any build (nothing cached), after an LFU build, and with every row
+    cached; the counters see every row and the hits the build promised."""
+    from hashed_gram_embedding_engram_gb300 import EngramCache
+    w = SMALL[kind]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, wd, proj, H = make_layer(w, L, P, ids.size)
+    table_host = to_torch(L.table, w.table_dtype, "cpu", pin=True)
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = plan.stage_a(ids_d, proj, wd.table, wd.scales)
+    uva = plan.stage_a(ids_d, proj, table_host, wd.scales)
+    assert torch.equal(ref.view(torch.int16), uva.view(torch.int16))
+    n_rows = int(np.sum(L.primes))
+    cache = EngramCache(plan, max(1, n_rows // 50), table_host)
+    got = cache.stage_a(ids_d, proj, wd.scales)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    looked, hits, cached = cache.stats(reset=True)
+    assert looked == ids.size * w.R and hits == 0 and cached == 0
+    # LFU: observe a different sample of the same distribution, then serve this batch
+    warm = torch.from_numpy(W.token_stream(w, key="cache-warm")).cuda()
+    cache.observe(warm, proj)
+    cached = cache.build()
+    assert 0 < cached <= n_rows // 50
+    got = cache.stage_a(ids_d, proj, wd.scales)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    looked, hits, _ = cache.stats(reset=True)
+    assert looked == ids.size * w.R and 0 < hits < looked
+    # the most-counted rows of the warm sample are cached: their accesses in it are all hits
+    cache.stage_a(warm, proj, wd.scales)
+    looked_w, hits_w, _ = cache.stats(reset=True)
+    assert hits_w / looked_w >= hits / looked
+    full = EngramCache(plan, n_rows, table_host)
+    full.observe(ids_d, proj)
+    assert full.build() == len(np.unique(ref_rows(w, ids, P, L)))
+    got = full.stage_a(ids_d, proj, wd.scales)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    looked, hits, _ = full.stats()
+    assert hits == looked
+
+
+def ref_rows(w, ids, P, L):
+    """Global table rows a batch reads, from the oracle's indices."""
+    z = O.hash_heads(O.project(ids, P), L.multipliers, L.primes, w.N, w.K).reshape(-1, w.R)
+    offsets = np.concatenate([[0], np.cumsum(L.primes)[:-1]]).astype(np.int64)
+    return (z.astype(np.int64) + offsets[None, :]).ravel()
