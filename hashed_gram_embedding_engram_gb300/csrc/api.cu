@@ -314,11 +314,26 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
                                  &pstride, plan->num_sms, &plan->dev->err, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
     mark(plan, s);
+    if (T == 1) {
+      // one position per sequence (decode): gate, conv, residual and state in one launch
+      if (engram::launch_decode_tail(plan, ws.v32, d, nullptr, ws.part, n_sl, pstride, ws.sa, B, w->g_c, w->conv, H,
+                                     ids, proj, V, state, s) != cudaSuccess)
+        return ENGRAM_ERR_CUDA;
+      mark(plan, s);
+      return ENGRAM_OK;
+    }
     if (engram::launch_finalize(plan, ws.part, n_sl, pstride, ntok, ws.sa, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
     v = ws.v32;
     sv = d;
   }
   mark(plan, s);
+  if (T == 1) {
+    if (engram::launch_decode_tail(plan, v, sv, ws.sa, nullptr, 0, 0, nullptr, B, w->g_c, w->conv, H, ids, proj, V,
+                                   state, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    mark(plan, s);
+    return ENGRAM_OK;
+  }
   if (engram::launch_conv_residual(plan, v, sv, ws.sa, B, T, w->g_c, w->conv, H, state, s) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
   mark(plan, s);

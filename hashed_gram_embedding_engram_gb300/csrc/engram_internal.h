@@ -127,6 +127,13 @@ cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, i
 cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
                                  const float* g_c, const float* conv, void* H, const engram_state_t* state,
                                  cudaStream_t s);
+// Steps 6-8 and the state update for one position per sequence (decode) in one
+// launch: gate scalars from sa_in (fp32 layers) or the partials (bf16 layers,
+// also written to sa_out), conv from the ring, H += Y, ring/prev_ids/pos update.
+cudaError_t launch_decode_tail(const engram_plan* p, const float* v, int64_t sv, const float* sa_in, const float* part,
+                               int n_sl, int pstride, float* sa_out, int B, const float* g_c, const float* conv,
+                               void* H, const int32_t* ids, const int32_t* proj, int V, const engram_state_t* st,
+                               cudaStream_t s);
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,
                                 int64_t sv, const float* sa, int B, int T, const engram_state_t* state,
                                 cudaStream_t s);

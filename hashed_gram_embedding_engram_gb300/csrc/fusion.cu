@@ -89,6 +89,44 @@ __device__ __forceinline__ float pairwise_warp_sum(const float* p, int stride, i
 // One warp per token: part[0, n_sl) = sum v^2 nodes, part[n_sl + (m*n_sl + j)*3
 // + {0,1,2}] = (h.g_h.g_k.k, k^2, h^2) nodes of branch m -> the sa row.  Up to
 // 32 nodes (one per lane) the four sums of a branch are loaded together.
+// One token's gate scalars from its partials, by one warp (lane 0 writes out[]).
+__device__ __forceinline__ void gate_row(const float* p, int n_sl, int q, int M, float inv_d, float inv_sqrt_d,
+                                         float eps, int lane, float* out) {
+  if (q == 1) {
+    const bool has = lane < n_sl;
+    float sv = has ? __ldg(p + lane) : 0.f;
+    for (int m = 0; m < M; ++m) {
+      const float* pm = p + n_sl + (m * n_sl + lane) * 3;
+      float dot = has ? __ldg(pm) : 0.f;
+      float sk = has ? __ldg(pm + 1) : 0.f;
+      float sh = has ? __ldg(pm + 2) : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        if (m == 0) sv += __shfl_xor_sync(0xFFFFFFFFu, sv, o);
+        dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+        sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
+        sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
+      }
+      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
+    }
+  } else {
+    const float sv = pairwise_warp_sum(p, 1, n_sl, q, lane);
+    for (int m = 0; m < M; ++m) {
+      const float* pm = p + n_sl + m * n_sl * 3;
+      const float dot = pairwise_warp_sum(pm, 3, n_sl, q, lane);
+      const float sk = pairwise_warp_sum(pm + 1, 3, n_sl, q, lane);
+      const float sh = pairwise_warp_sum(pm + 2, 3, n_sl, q, lane);
+      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
+    }
+  }
+}
+
+__device__ __forceinline__ int nodes_per_lane(int n_sl) {
+  int q = 1;
+  while (q * 32 < n_sl) q <<= 1;
+  return q;
+}
+
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int n_sl, int pstride,
                                                        int64_t ntok, int M, int d, float eps, float* __restrict__ sa,
                                                        int saw) {
@@ -97,41 +135,11 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
   const int lane = threadIdx.x & 31;
   const float inv_d = 1.f / static_cast<float>(d);
   const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(d));
-  int q = 1;
-  while (q * 32 < n_sl) q <<= 1;
+  const int q = nodes_per_lane(n_sl);
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
-       tok += n_warps) {
-    const float* p = part + tok * pstride;
-    float* out = sa + tok * saw;
-    if (q == 1) {
-      const bool has = lane < n_sl;
-      float sv = has ? __ldg(p + lane) : 0.f;
-      for (int m = 0; m < M; ++m) {
-        const float* pm = p + n_sl + (m * n_sl + lane) * 3;
-        float dot = has ? __ldg(pm) : 0.f;
-        float sk = has ? __ldg(pm + 1) : 0.f;
-        float sh = has ? __ldg(pm + 2) : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          if (m == 0) sv += __shfl_xor_sync(0xFFFFFFFFu, sv, o);
-          dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-          sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
-          sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
-        }
-        if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
-      }
-    } else {
-      const float sv = pairwise_warp_sum(p, 1, n_sl, q, lane);
-      for (int m = 0; m < M; ++m) {
-        const float* pm = p + n_sl + m * n_sl * 3;
-        const float dot = pairwise_warp_sum(pm, 3, n_sl, q, lane);
-        const float sk = pairwise_warp_sum(pm + 1, 3, n_sl, q, lane);
-        const float sh = pairwise_warp_sum(pm + 2, 3, n_sl, q, lane);
-        if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
-      }
-    }
-  }
+       tok += n_warps)
+    gate_row(part + tok * pstride, n_sl, q, M, inv_d, inv_sqrt_d, eps, lane, sa + tok * saw);
 }
 
 // ------------------------------------------------------------------ gate (fp32 layers)
@@ -457,6 +465,125 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
   }
 }
 
+// ------------------------------------------------------------------ one-position decode step
+// Steps 6-8 and the streaming state for chunks of one position (decode), in
+// one launch: block b is sequence b.  Warp 0 turns the token's gate partials
+// into (s, alpha) (gate_row, the finalize kernel's arithmetic; fp32 layers
+// read the gate kernel's sa row); every thread forms its 4 channels' conv
+// from the caller's ring (the taps at lag > 0) and s * v (lag 0) with the
+// conv kernel's operation order, updates H, then writes s * v into the slot
+// of the new position -- the slot its own tap at lag (w-1)*dilation just read,
+// so no other thread touches it.  Thread 0 then rolls the projected ids and
+// advances pos.  The result equals finalize + conv + state bit for bit.
+template <typename TH, int W, bool kPart>
+__global__ void __launch_bounds__(256) decode_tail_kernel(
+    const float* __restrict__ gate_in, int n_sl, int pstride, int saw, float eps, const float* __restrict__ v,
+    int64_t sv, int M, int d, int dil, const float* __restrict__ g_c, const float* __restrict__ conv,
+    float* __restrict__ ring, int32_t* __restrict__ pos, int L, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ proj, int V, int32_t* __restrict__ prev, int N, float* __restrict__ sa_out,
+    uint32_t* __restrict__ err, TH* __restrict__ H) {
+  __shared__ float s_sa[2 * kMaxM];
+  __shared__ int s_p0;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    if constexpr (kPart) {
+      gate_row(gate_in + static_cast<int64_t>(b) * pstride, n_sl, nodes_per_lane(n_sl), M,
+               1.f / static_cast<float>(d), 1.f / sqrtf(static_cast<float>(d)), eps, lane, s_sa);
+    } else if (lane < 2 * M) {
+      s_sa[lane] = gate_in[static_cast<int64_t>(b) * saw + lane];
+    }
+    if (lane == 0) s_p0 = ring != nullptr ? pos[b] : 0;
+  }
+  __syncthreads();
+  if (sa_out != nullptr && threadIdx.x < 2 * M) sa_out[static_cast<int64_t>(b) * saw + threadIdx.x] = s_sa[threadIdx.x];
+  const int p0 = s_p0;
+  for (int g = threadIdx.x; g < d / 4; g += blockDim.x) {
+    const int c = 4 * g;
+    float wq[4][W];
+    {
+      float gc[4];
+      ld4(g_c + c, gc);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int j = 0; j < W; ++j) wq[i][j] = __ldg(conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
+      }
+    }
+    float vt[4];
+    ld4(v + static_cast<int64_t>(b) * sv + c, vt);
+    for (int m = 0; m < M; ++m) {
+      const float sm = s_sa[m];
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const int lag = (W - 1 - j) * dil;
+        if (lag == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sm * vt[i], acc[i]);
+        } else if (ring != nullptr && p0 - lag >= 0) {
+          float u[4];                                 // the ring holds RMSNorm(v~) before its weight
+          ld4(ring + ((static_cast<int64_t>(b) * L + (p0 - lag) % L) * M + m) * d + c, u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
+        }
+      }
+      TH* hp = H + (static_cast<int64_t>(b) * M + m) * d + c;
+      float h[4];
+      H4<TH>::load(hp, h);
+      const float at = s_sa[M + m];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = h[i] + (silu_fast(acc[i]) + at * vt[i]);
+      H4<TH>::store(hp, h);
+      if (ring != nullptr && L > 0) {
+        float* dst = ring + ((static_cast<int64_t>(b) * L + p0 % L) * M + m) * d + c;
+        *reinterpret_cast<float4*>(dst) = make_float4(sm * vt[0], sm * vt[1], sm * vt[2], sm * vt[3]);
+      }
+    }
+  }
+  if (ring == nullptr) return;
+  __syncthreads();                                    // every thread has read pos[b]
+  if (threadIdx.x == 0) {
+    int32_t old[kMaxN];
+    for (int j = 0; j < N - 1; ++j) old[j] = prev[static_cast<int64_t>(b) * (N - 1) + j];
+    int raw = ids[b];
+    bool bad = false;
+    if (static_cast<unsigned>(raw) >= static_cast<unsigned>(V)) {
+      bad = true;
+      raw = 0;
+    }
+    for (int j = 0; j + 1 < N - 1; ++j) prev[static_cast<int64_t>(b) * (N - 1) + j] = old[j + 1];
+    if (N > 1) prev[static_cast<int64_t>(b) * (N - 1) + N - 2] = proj[raw];
+    pos[b] = p0 + 1;
+    if (bad) atomicOr(err, kErrIndexRange);
+  }
+}
+
+template <typename TH, bool kPart>
+cudaError_t decode_tail_dispatch(int W, dim3 grid, cudaStream_t s, const float* gate_in, int n_sl, int pstride, int saw,
+                                 float eps, const float* v, int64_t sv, int M, int d, int dil, const float* g_c,
+                                 const float* conv, float* ring, int32_t* pos, int L, const int32_t* ids,
+                                 const int32_t* proj, int V, int32_t* prev, int N, float* sa_out, uint32_t* err,
+                                 void* H) {
+#define ENGRAM_TAIL(Wv)                                                                                               \
+  launch_pdl(decode_tail_kernel<TH, Wv, kPart>, grid, dim3(256), 0, s, gate_in, n_sl, pstride, saw, eps, v, sv, M, d, \
+             dil, g_c, conv, ring, pos, L, ids, proj, V, prev, N, sa_out, err, static_cast<TH*>(H))
+  switch (W) {
+    case 1: return ENGRAM_TAIL(1);
+    case 2: return ENGRAM_TAIL(2);
+    case 3: return ENGRAM_TAIL(3);
+    case 4: return ENGRAM_TAIL(4);
+    case 5: return ENGRAM_TAIL(5);
+    case 6: return ENGRAM_TAIL(6);
+    case 7: return ENGRAM_TAIL(7);
+    case 8: return ENGRAM_TAIL(8);
+    default: return cudaErrorInvalidValue;
+  }
+#undef ENGRAM_TAIL
+}
+
 // ------------------------------------------------------------------ streaming state
 __global__ void __launch_bounds__(256) state_kernel(const float* __restrict__ v_base, int64_t sv,
                                                     const float* __restrict__ sa, int saw, int Tn, int M, int d,
@@ -702,6 +829,25 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, p->num_sms));
   if (f32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, s);
   return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, s);
+}
+
+cudaError_t launch_decode_tail(const engram_plan* p, const float* v, int64_t sv, const float* sa_in, const float* part,
+                               int n_sl, int pstride, float* sa_out, int B, const float* g_c, const float* conv,
+                               void* H, const int32_t* ids, const int32_t* proj, int V, const engram_state_t* st,
+                               cudaStream_t s) {
+  const bool f32 = p->cfg.act_dtype == ENGRAM_F32;
+  float* ring = st ? st->u_ring : nullptr;
+  int32_t* pos = st ? st->pos : nullptr;
+  int32_t* prev = st ? st->prev_ids : nullptr;
+  const int saw = sa_row_floats(p->cfg.M);
+  const dim3 grid(static_cast<unsigned>(B));
+  if (f32)
+    return decode_tail_dispatch<float, false>(p->cfg.conv_w, grid, s, sa_in, 0, 0, saw, p->cfg.eps, v, sv, p->cfg.M,
+                                              p->cfg.d, p->cfg.conv_dilation, g_c, conv, ring, pos, p->L_ring, ids,
+                                              proj, V, prev, p->cfg.N, nullptr, &p->dev->err, H);
+  return decode_tail_dispatch<__nv_bfloat16, true>(p->cfg.conv_w, grid, s, part, n_sl, pstride, saw, p->cfg.eps, v,
+                                                   sv, p->cfg.M, p->cfg.d, p->cfg.conv_dilation, g_c, conv, ring, pos,
+                                                   p->L_ring, ids, proj, V, prev, p->cfg.N, sa_out, &p->dev->err, H);
 }
 
 cudaError_t launch_state_update(const engram_plan* p, const int32_t* ids, const int32_t* proj, int V, const float* v,

@@ -273,7 +273,9 @@ engram_status_t engram_cache_stats(const engram_cache_t* cache, engram_stream_t 
  * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps
  * 1-4 in one kernel), K/V projection with the gate reductions, gate
  * (finalize), conv + residual; on F32 layers: hash + gather, K/V projection,
- * gate, conv + residual; then the state update when a state is given.
+ * gate, conv + residual; then the state update when a state is given.  Chunks
+ * of one position (T = 1, decode) run the gate, conv, residual and state
+ * update as one kernel after the K/V projection.
  * engram_stage_b records the same list without the first kernel.  For use on
  * one stream at a time, outside CUDA-graph capture.  enable: 0 or 1. */
 engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable);
