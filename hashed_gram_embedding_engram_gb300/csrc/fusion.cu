@@ -58,6 +58,27 @@ __device__ __forceinline__ float warp_sum(float x) {
 // SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
+// Two fp32 lanes per instruction (sm_100 family): each lane is rounded exactly
+// as the scalar instruction would round it.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // ------------------------------------------------------------------ gate (bf16 layers: from partials)
 // Sum over a warp of the n values p[i * stride], i < n, as the adjacent
 // pairwise tree: lane l sums its aligned block [l*q, l*q + q) pairwise (zeros
@@ -196,7 +217,27 @@ constexpr int kConvStages = 3;
 constexpr uint64_t kConvWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
 constexpr int kConvMaxCS = 256;                    // channels per tile: one TMA box row (<= 256 elements)
 
+// n / d for 0 <= n < 2^31 as one widening multiply and a shift: with
+// 2^l >= d and s = 31 + l, m = ceil(2^s / d) fits in 32 bits and
+// floor(n * m / 2^s) = floor(n / d), since n * (m - 2^s/d) / 2^s < 2^-l <= 1/d
+// (the round-up method of Granlund & Montgomery, "Division by invariant
+// integers using multiplication", PLDI 1994).
+struct FastDiv {
+  uint32_t mul, sh;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return static_cast<uint32_t>((static_cast<uint64_t>(n) * mul) >> sh);
+  }
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint32_t sh = 31 + l;
+  return FastDiv{static_cast<uint32_t>(((1ull << sh) + d - 1) / d), sh};
+}
+
 struct ConvArgs {
+  FastDiv div_ct, div_tps;   // by n_ct and by tiles_per_seq
   int B, Tn, M, d, dil;
   int S;                 // positions per tile
   int CS;                // channels per tile
@@ -254,7 +295,7 @@ struct H4<float> {
 // (times g_c) in registers; SiLU, the skip and H += Y for every branch,
 // stored straight to H.
 // DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
-template <typename TH, int W, int DIL, int MC>
+template <typename TH, int W, int DIL, int MC, int CSC>
 __global__ void __launch_bounds__(kConvThreads + 32, 1)
     conv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
                 const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a, TH* __restrict__ H) {
@@ -269,9 +310,9 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
   const int tid = threadIdx.x;
 
   auto coords = [&](int tile, int& b, int& t0, int& c0) {
-    const int ct = tile % a.n_ct;
-    const int q = tile / a.n_ct;
-    b = q / a.tiles_per_seq;
+    const int q = static_cast<int>(a.div_ct.div(static_cast<uint32_t>(tile)));
+    const int ct = tile - q * a.n_ct;
+    b = static_cast<int>(a.div_tps.div(static_cast<uint32_t>(q)));
     t0 = (q - b * a.tiles_per_seq) * a.S;
     c0 = ct * a.CS;
   };
@@ -328,7 +369,9 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
 
   // -------------------------------------------------------------------- compute warps
   const int lane = tid & 31;
-  const int ng = a.CS >> 2;                        // channel groups of a tile
+  const int CS = CSC > 0 ? CSC : a.CS;            // channels per tile (compile-time on the common shape)
+  const int saw = MC == 1 ? 4 : a.saw;             // floats per sa row
+  const int ng = CS >> 2;                          // channel groups of a tile
   const int npar = kConvThreads / ng;              // chains processed side by side
   const int g = tid % ng, par0 = tid / ng;
   int c_cached = -1;
@@ -350,6 +393,7 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
     load_taps(c0 + 4 * g);
   }
   int k = 0;
+  int rot = par0;                                  // this tile's first chain: rotates by one per tile
   for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
     const int st = k % kConvStages;
     if (!ptx::mbar_wait_bounded(&full[st], static_cast<uint32_t>(k / kConvStages) & 1u, kConvWaitNs)) {
@@ -368,17 +412,19 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
       const int c = c0 + 4 * g;
       if (c != c_cached) load_taps(c);
       const int p0 = a.ring != nullptr ? a.pos[b] : 0;
-      const int rstride = dil * a.CS;                  // floats between tap rows in the staged v
+      const int rstride = dil * CS;                    // floats between tap rows in the staged v
+      const int64_t hrow = static_cast<int64_t>(M) * a.d;                 // elements per position of H
+      TH* const hbase = H + (static_cast<int64_t>(b) * a.Tn + t0) * hrow + c;   // position t0, branch 0
       // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
       const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
-      for (int ch = (par0 + k) % npar; ch < n_chains; ch += npar) {
+      for (int ch = rot; ch < n_chains; ch += npar) {
         const int tb = (ch / dil) * (kChain * dil) + ch % dil;
         if (tb >= nt) continue;
         if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
           // interior chain: every row staged, every output in the tile -- no branches, all loads first
           const int r0 = a.h0 + tb - (W - 1) * dil;
-          const float* vp = vs + r0 * a.CS + 4 * g;
-          const float* sp = ss + r0 * a.saw;
+          const float* vp = vs + r0 * CS + 4 * g;
+          const float* sp = ss + r0 * saw;
           float vr[kRows][4];
 #pragma unroll
           for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
@@ -386,28 +432,34 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
             float u[kRows][4], h[kChain][4], at[kChain];
 #pragma unroll
             for (int o = 0; o < kChain; ++o) {
-              H4<TH>::load(hs + ((tb + o * dil) * M + m) * a.CS + 4 * g, h[o]);
-              at[o] = sp[(o + W - 1) * dil * a.saw + M + m];
+              H4<TH>::load(hs + ((tb + o * dil) * M + m) * CS + 4 * g, h[o]);
+              at[o] = sp[(o + W - 1) * dil * saw + M + m];
             }
 #pragma unroll
             for (int j = 0; j < kRows; ++j) {
-              const float sj = sp[j * dil * a.saw + m];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
+              const float sj = sp[j * dil * saw + m];
+              mul2(u[j][0], u[j][1], sj, sj, vr[j][0], vr[j][1]);
+              mul2(u[j][2], u[j][3], sj, sj, vr[j][2], vr[j][3]);
             }
 #pragma unroll
             for (int o = 0; o < kChain; ++o) {
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
-                h[o][i] = h[o][i] + (silu_fast(acc) + at[o] * vr[o + W - 1][i]);
+              for (int j = 0; j < W; ++j) {
+                fma2(acc[0], acc[1], wq[0][j], wq[1][j], u[o + j][0], u[o + j][1], acc[0], acc[1]);
+                fma2(acc[2], acc[3], wq[2][j], wq[3][j], u[o + j][2], u[o + j][3], acc[2], acc[3]);
               }
-            }
-            TH* hp = H + ((static_cast<int64_t>(b) * a.Tn + t0 + tb) * M + m) * a.d + c;
+              float y[4];
 #pragma unroll
-            for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o) * dil * M * a.d, h[o]);
+              for (int i = 0; i < 4; ++i) y[i] = silu_fast(acc[i]);
+              fma2(y[0], y[1], at[o], at[o], vr[o + W - 1][0], vr[o + W - 1][1], y[0], y[1]);
+              fma2(y[2], y[3], at[o], at[o], vr[o + W - 1][2], vr[o + W - 1][3], y[2], y[3]);
+              add2(h[o][0], h[o][1], h[o][0], h[o][1], y[0], y[1]);
+              add2(h[o][2], h[o][3], h[o][2], h[o][3], y[2], y[3]);
+            }
+            TH* hp = hbase + static_cast<int64_t>(tb) * hrow + static_cast<int64_t>(m) * a.d;
+#pragma unroll
+            for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o * dil) * hrow, h[o]);
           }
           continue;
         }
@@ -416,7 +468,7 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
         for (int j = 0; j < kRows; ++j) {
           const int tr = tb + (j - (W - 1)) * dil;
           if (t0 + tr >= 0 && tr < nt) {
-            ld4(vs + (a.h0 + tr) * a.CS + 4 * g, vr[j]);
+            ld4(vs + (a.h0 + tr) * CS + 4 * g, vr[j]);
           } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
@@ -431,7 +483,7 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
 #pragma unroll
               for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
             } else if (t0 + tr >= 0) {
-              const float sj = ss[(a.h0 + tr) * a.saw + m];
+              const float sj = ss[(a.h0 + tr) * saw + m];
 #pragma unroll
               for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
             } else if (a.ring != nullptr && p0 + t0 + tr >= 0) {
@@ -446,14 +498,14 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
             const int tt = tb + o * dil;
             if (tt >= nt) break;
             float h[4];
-            H4<TH>::load(hs + (tt * M + m) * a.CS + 4 * g, h);
-            const float at = ss[(a.h0 + tt) * a.saw + M + m];
+            H4<TH>::load(hs + (tt * M + m) * CS + 4 * g, h);
+            const float at = ss[(a.h0 + tt) * saw + M + m];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               float acc = 0.f;
 #pragma unroll
               for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
-              h[i] = h[i] + (silu_fast(acc) + at * vr[o + W - 1][i]);
+              h[i] = h[i] + fmaf(at, vr[o + W - 1][i], silu_fast(acc));
             }
             H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t0 + tt) * M + m) * a.d + c, h);
           }
@@ -462,6 +514,7 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&empty[st]);    // this warp is done with the stage
+    if (++rot == npar) rot = 0;
   }
 }
 
@@ -535,7 +588,7 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
       H4<TH>::load(hp, h);
       const float at = s_sa[M + m];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) h[i] = h[i] + (silu_fast(acc[i]) + at * vt[i]);
+      for (int i = 0; i < 4; ++i) h[i] = h[i] + fmaf(at, vt[i], silu_fast(acc[i]));
       H4<TH>::store(hp, h);
       if (ring != nullptr && L > 0) {
         float* dst = ring + ((static_cast<int64_t>(b) * L + p0 % L) * M + m) * d + c;
@@ -642,26 +695,30 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-template <typename TH, int W, int DIL, int MC>
+template <typename TH, int W, int DIL, int MC, int CSC>
 cudaError_t conv_launch_m(const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts, const ConvArgs& a,
                           int grid, size_t smem, void* H, cudaStream_t s) {
   static size_t attr_bytes = 0;    // per template instance: the dynamic shared memory opted into so far
   if (smem > attr_bytes) {
-    const cudaError_t e = cudaFuncSetAttribute(conv_kernel<TH, W, DIL, MC>,
+    const cudaError_t e = cudaFuncSetAttribute(conv_kernel<TH, W, DIL, MC, CSC>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_bytes = smem;
   }
-  return launch_pdl(conv_kernel<TH, W, DIL, MC>, dim3(grid), dim3(kConvThreads + 32), smem, s, tv, th, ts, a,
+  return launch_pdl(conv_kernel<TH, W, DIL, MC, CSC>, dim3(grid), dim3(kConvThreads + 32), smem, s, tv, th, ts, a,
                     static_cast<TH*>(H));
 }
 
-// single-branch layers with a compile-time dilation get a compile-time M = 1
+// single-branch layers with a compile-time dilation get a compile-time M = 1,
+// and a compile-time tile width when it is the widest one
 template <typename TH, int W, int DIL>
 cudaError_t conv_launch(const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts, const ConvArgs& a,
                         int grid, size_t smem, void* H, cudaStream_t s) {
-  if (DIL > 0 && a.M == 1) return conv_launch_m<TH, W, DIL, 1>(tv, th, ts, a, grid, smem, H, s);
-  return conv_launch_m<TH, W, DIL, 0>(tv, th, ts, a, grid, smem, H, s);
+  if (DIL > 0 && a.M == 1) {
+    if (a.CS == kConvMaxCS) return conv_launch_m<TH, W, DIL, 1, kConvMaxCS>(tv, th, ts, a, grid, smem, H, s);
+    return conv_launch_m<TH, W, DIL, 1, 0>(tv, th, ts, a, grid, smem, H, s);
+  }
+  return conv_launch_m<TH, W, DIL, 0, 0>(tv, th, ts, a, grid, smem, H, s);
 }
 
 template <typename TH>
@@ -809,6 +866,8 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.S = S;
   a.tiles_per_seq = (T + S - 1) / S;
   a.h0 = a.tiles_per_seq > 1 ? halo : 0;
+  a.div_ct = make_fastdiv(static_cast<uint32_t>(a.n_ct));
+  a.div_tps = make_fastdiv(static_cast<uint32_t>(a.tiles_per_seq));
   const int64_t n_tiles = static_cast<int64_t>(B) * a.tiles_per_seq * a.n_ct;
   if (n_tiles > INT32_MAX) return cudaErrorInvalidValue;
   a.n_tiles = static_cast<int>(n_tiles);
