@@ -254,6 +254,9 @@ def run_ours(args) -> None:
             torch.cuda._sleep(400_000)   # keep the GPU behind the host: every launch is queued before it runs
             ly["plan"].forward(ids, ly["proj"], ly["weights"], ly["H"], None, ly["ws"])
             t = ly["plan"].kernel_times()
+            if len(t) == 3 and "finalize" in names:    # the conv computes the gate scalars itself
+                names.remove("finalize")
+                del dur["finalize"]
             assert len(t) == len(names), t
             for n, x in zip(names, t):
                 dur[n].append(x)

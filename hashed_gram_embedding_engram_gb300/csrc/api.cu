@@ -322,6 +322,19 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
       mark(plan, s);
       return ENGRAM_OK;
     }
+    if (engram::conv_fuses_gate(plan, n_sl, pstride)) {
+      // the conv computes the gate scalars from the partials itself
+      if (engram::launch_conv_residual(plan, ws.v32, d, nullptr, B, T, w->g_c, w->conv, H, state, s, ws.part,
+                                       state ? ws.sa : nullptr) != cudaSuccess)
+        return ENGRAM_ERR_CUDA;
+      mark(plan, s);
+      if (state) {
+        if (engram::launch_state_update(plan, ids, proj, V, ws.v32, d, ws.sa, B, T, state, s) != cudaSuccess)
+          return ENGRAM_ERR_CUDA;
+        mark(plan, s);
+      }
+      return ENGRAM_OK;
+    }
     if (engram::launch_finalize(plan, ws.part, n_sl, pstride, ntok, ws.sa, s) != cudaSuccess) return ENGRAM_ERR_CUDA;
     v = ws.v32;
     sv = d;

@@ -124,9 +124,15 @@ cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, i
                             cudaStream_t s);
 // Conv + SiLU + skip + residual over B sequences of T positions (v fp32 with
 // row stride sv; sa rows [s^(1..M), alpha^(1..M)] per token).
+// With `part` (bf16 layers where conv_fuses_gate holds) the conv computes the
+// gate scalars from the K/V epilogue's partials itself (sa_out: where to also
+// store them for the streaming state, or null) and sa is not read.
 cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
                                  const float* g_c, const float* conv, void* H, const engram_state_t* state,
-                                 cudaStream_t s);
+                                 cudaStream_t s, const float* part = nullptr, float* sa_out = nullptr);
+// Whether the conv can compute the gate scalars itself for this layer shape
+// (one branch, 8 slices per quantity: 32 partials per row).
+bool conv_fuses_gate(const engram_plan* p, int n_sl, int pstride);
 // Steps 6-8 and the state update for one position per sequence (decode) in one
 // launch: gate scalars from sa_in (fp32 layers) or the partials (bf16 layers,
 // also written to sa_out), conv from the ring, H += Y, ring/prev_ids/pos update.

@@ -244,7 +244,9 @@ struct ConvArgs {
   int h0;                // staged rows before a tile's first position: (w-1)*dil, or 0 if a sequence is one tile
   int tiles_per_seq, n_ct, n_tiles;
   int saw;               // floats per sa row
-  uint32_t v_off, h_off, sa_off, stage_bytes, tx_bytes;   // shared-memory layout of one stage
+  uint32_t v_off, h_off, sa_off, p_off, stage_bytes, tx_bytes;   // shared-memory layout of one stage
+  float* sa_out;         // gate scalars computed in-kernel (KFIN), for the streaming state; or null
+  float eps;
   const float* g_c;      // [d]
   const float* conv;     // [d, W]
   const float* ring;     // [B, L, M, d] or null
@@ -295,15 +297,21 @@ struct H4<float> {
 // (times g_c) in registers; SiLU, the skip and H += Y for every branch,
 // stored straight to H.
 // DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
-template <typename TH, int W, int DIL, int MC, int CSC>
-__global__ void __launch_bounds__(kConvThreads + 32, 1)
+// KFIN: the block also turns the K/V epilogue's gate partial sums into the
+// (s, alpha) rows itself (8 slices per quantity, one branch): the producer's
+// third copy brings each staged position's 32 partials (128-byte rows,
+// 128-byte swizzle) instead of an sa row, and a helper warp -- one row per
+// lane, the finalize kernel's tree and arithmetic -- writes the stage's sa
+// rows and releases them through sa_ready, one tile ahead of the compute warps.
+template <typename TH, int W, int DIL, int MC, int CSC, bool KFIN>
+__global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
     conv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
                 const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a, TH* __restrict__ H) {
   constexpr int kRows = kChain + W - 1;
   constexpr int kWarps = kConvThreads / 32;          // compute warps
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  __shared__ uint64_t full[kConvStages], empty[kConvStages];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kConvStages], empty[kConvStages], sa_ready[kConvStages];
   __shared__ int s_abort;
   const int dil = DIL > 0 ? DIL : a.dil;
   const int M = MC > 0 ? MC : a.M;
@@ -321,6 +329,7 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
     for (int st = 0; st < kConvStages; ++st) {
       ptx::mbar_init(&full[st], 1);
       ptx::mbar_init(&empty[st], kWarps);
+      ptx::mbar_init(&sa_ready[st], 1);
     }
     s_abort = 0;
     ptx::fence_mbar_init();
@@ -328,6 +337,70 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
   __syncthreads();
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
+
+  if constexpr (KFIN) {
+    if (tid >= kConvThreads + 32) {
+      // ---------------------------------------------------------------- helper warp: gate scalars
+      const int lane = tid & 31;
+      const float inv_d = 1.f / static_cast<float>(a.d);
+      const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(a.d));
+      const int rows = a.S + a.h0;
+      int k = 0;
+      for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+        const int st = k % kConvStages;
+        if (!ptx::mbar_wait_bounded(&full[st], static_cast<uint32_t>(k / kConvStages) & 1u, kConvWaitNs)) {
+          if (lane == 0) atomicOr(a.err, kErrTimeout);
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&s_abort)) break;
+        const uint8_t* pp = smem + st * a.stage_bytes + a.p_off;       // [rows][32 floats], 128-byte swizzle
+        float* sa_s = reinterpret_cast<float*>(smem + st * a.stage_bytes + a.sa_off);
+        int b, t0, c0;
+        coords(tile, b, t0, c0);
+        for (int r = lane; r < rows; r += 32) {
+          float x[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 q = *reinterpret_cast<const float4*>(pp + r * 128 + ((j ^ (r & 7)) << 4));
+            x[4 * j] = q.x;
+            x[4 * j + 1] = q.y;
+            x[4 * j + 2] = q.z;
+            x[4 * j + 3] = q.w;
+          }
+          float sv[8], dt[8], sk[8], sh[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            sv[i] = x[i];
+            dt[i] = x[8 + 3 * i];
+            sk[i] = x[9 + 3 * i];
+            sh[i] = x[10 + 3 * i];
+          }
+#pragma unroll
+          for (int w = 1; w < 8; w *= 2)
+#pragma unroll
+            for (int i = 0; i + w < 8; i += 2 * w) {
+              sv[i] = sv[i] + sv[i + w];
+              dt[i] = dt[i] + dt[i + w];
+              sk[i] = sk[i] + sk[i + w];
+              sh[i] = sh[i] + sh[i + w];
+            }
+          float out[2];
+          gate_scalars(sv[0], dt[0], sk[0], sh[0], inv_d, inv_sqrt_d, a.eps, out, 1, 0);
+          sa_s[r * 4] = out[0];
+          sa_s[r * 4 + 1] = out[1];
+          const int t = t0 - a.h0 + r;
+          if (a.sa_out != nullptr && c0 == 0 && r >= a.h0 && t < a.Tn) {
+            float* g = a.sa_out + (static_cast<int64_t>(b) * a.Tn + t) * 4;
+            g[0] = out[0];
+            g[1] = out[1];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sa_ready[st]);
+      }
+      return;
+    }
+  }
 
   if (tid >= kConvThreads) {
     // ---------------------------------------------------------------- producer warp
@@ -352,7 +425,7 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
         ptx::mbar_arrive_expect_tx(&full[st], a.tx_bytes);
         ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[st], c0, row0);
         ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[st], c0, (b * a.Tn + t0) * M);
-        ptx::tma_load_2d_nohint(base + a.sa_off, &tm_sa, &full[st], 0, row0);
+        ptx::tma_load_2d_nohint(base + (KFIN ? a.p_off : a.sa_off), &tm_sa, &full[st], 0, row0);
         armed |= 1u << st;
       }
       // copies still in flight land before the block may exit
@@ -399,6 +472,12 @@ __global__ void __launch_bounds__(kConvThreads + 32, 1)
     if (!ptx::mbar_wait_bounded(&full[st], static_cast<uint32_t>(k / kConvStages) & 1u, kConvWaitNs)) {
       if (lane == 0) atomicOr(a.err, kErrTimeout);
       break;
+    }
+    if constexpr (KFIN) {
+      if (!ptx::mbar_wait_bounded(&sa_ready[st], static_cast<uint32_t>(k / kConvStages) & 1u, kConvWaitNs)) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        break;
+      }
     }
     if (*reinterpret_cast<volatile int*>(&s_abort)) break;
     int b, t0, c0;
@@ -695,36 +774,40 @@ int grid_for(int64_t items, int threads, int num_sms) {
   return static_cast<int>(blocks);
 }
 
-template <typename TH, int W, int DIL, int MC, int CSC>
+template <typename TH, int W, int DIL, int MC, int CSC, bool KFIN>
 cudaError_t conv_launch_m(const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts, const ConvArgs& a,
                           int grid, size_t smem, void* H, cudaStream_t s) {
   static size_t attr_bytes = 0;    // per template instance: the dynamic shared memory opted into so far
   if (smem > attr_bytes) {
-    const cudaError_t e = cudaFuncSetAttribute(conv_kernel<TH, W, DIL, MC, CSC>,
+    const cudaError_t e = cudaFuncSetAttribute(conv_kernel<TH, W, DIL, MC, CSC, KFIN>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_bytes = smem;
   }
-  return launch_pdl(conv_kernel<TH, W, DIL, MC, CSC>, dim3(grid), dim3(kConvThreads + 32), smem, s, tv, th, ts, a,
-                    static_cast<TH*>(H));
+  return launch_pdl(conv_kernel<TH, W, DIL, MC, CSC, KFIN>, dim3(grid), dim3(kConvThreads + (KFIN ? 64 : 32)), smem,
+                    s, tv, th, ts, a, static_cast<TH*>(H));
 }
 
 // single-branch layers with a compile-time dilation get a compile-time M = 1,
-// and a compile-time tile width when it is the widest one
+// and a compile-time tile width when it is the widest one; the gate scalars
+// are computed in the conv (fin) only on that shape
 template <typename TH, int W, int DIL>
 cudaError_t conv_launch(const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts, const ConvArgs& a,
-                        int grid, size_t smem, void* H, cudaStream_t s) {
+                        int grid, size_t smem, void* H, bool fin, cudaStream_t s) {
   if (DIL > 0 && a.M == 1) {
-    if (a.CS == kConvMaxCS) return conv_launch_m<TH, W, DIL, 1, kConvMaxCS>(tv, th, ts, a, grid, smem, H, s);
-    return conv_launch_m<TH, W, DIL, 1, 0>(tv, th, ts, a, grid, smem, H, s);
+    if (a.CS == kConvMaxCS) {
+      if (fin) return conv_launch_m<TH, W, DIL, 1, kConvMaxCS, true>(tv, th, ts, a, grid, smem, H, s);
+      return conv_launch_m<TH, W, DIL, 1, kConvMaxCS, false>(tv, th, ts, a, grid, smem, H, s);
+    }
+    return conv_launch_m<TH, W, DIL, 1, 0, false>(tv, th, ts, a, grid, smem, H, s);
   }
-  return conv_launch_m<TH, W, DIL, 0, 0>(tv, th, ts, a, grid, smem, H, s);
+  return conv_launch_m<TH, W, DIL, 0, 0, false>(tv, th, ts, a, grid, smem, H, s);
 }
 
 template <typename TH>
 cudaError_t conv_dispatch(int conv_w, const CUtensorMap& tv, const CUtensorMap& th, const CUtensorMap& ts,
-                          const ConvArgs& a, int grid, size_t smem, void* H, cudaStream_t s) {
-#define ENGRAM_CONV(Wv, Dv) conv_launch<TH, Wv, Dv>(tv, th, ts, a, grid, smem, H, s)
+                          const ConvArgs& a, int grid, size_t smem, void* H, bool fin, cudaStream_t s) {
+#define ENGRAM_CONV(Wv, Dv) conv_launch<TH, Wv, Dv>(tv, th, ts, a, grid, smem, H, fin && (Dv) > 0 && (Wv) == 4, s)
   if (conv_w == 4) {
     switch (a.dil) {   // the pages' short conv: w = 4, dilation = max n-gram order
       case 1: return ENGRAM_CONV(4, 1);
@@ -755,7 +838,9 @@ cudaError_t conv_dispatch(int conv_w, const CUtensorMap& tv, const CUtensorMap& 
 uint32_t round128(uint32_t x) { return (x + 127u) & ~127u; }
 
 // Shared-memory layout of one stage for a tile of S positions and CS channels.
-void conv_layout(ConvArgs& a, size_t act_bytes) {
+// With fin, a 1024-byte aligned region of 128-byte partial rows follows (the
+// 128-byte swizzle pattern repeats every 1024 bytes) and sa is not copied.
+void conv_layout(ConvArgs& a, size_t act_bytes, bool fin) {
   const uint32_t rows = static_cast<uint32_t>(a.S + a.h0);
   const uint32_t vb = rows * a.CS * 4u;
   const uint32_t hb = static_cast<uint32_t>(a.S * a.M * a.CS) * static_cast<uint32_t>(act_bytes);
@@ -763,8 +848,15 @@ void conv_layout(ConvArgs& a, size_t act_bytes) {
   a.v_off = 0;
   a.h_off = round128(vb);
   a.sa_off = round128(a.h_off + hb);
-  a.stage_bytes = round128(a.sa_off + sb);
-  a.tx_bytes = vb + hb + sb;
+  if (fin) {
+    a.p_off = (a.sa_off + sb + 1023u) & ~1023u;
+    a.stage_bytes = (a.p_off + rows * 128u + 1023u) & ~1023u;
+    a.tx_bytes = vb + hb + rows * 128u;
+  } else {
+    a.p_off = 0;
+    a.stage_bytes = round128(a.sa_off + sb);
+    a.tx_bytes = vb + hb + sb;
+  }
 }
 
 }  // namespace
@@ -784,9 +876,14 @@ cudaError_t launch_gate_f32(const engram_plan* p, const float* kv, const float* 
   return cudaGetLastError();
 }
 
+bool conv_fuses_gate(const engram_plan* p, int n_sl, int pstride) {
+  return p->cfg.act_dtype == ENGRAM_BF16 && p->cfg.M == 1 && p->cfg.conv_w == 4 && p->cfg.conv_dilation >= 1 &&
+         p->cfg.conv_dilation <= 8 && n_sl == 8 && pstride == 32 && p->cfg.d % kConvMaxCS == 0;
+}
+
 cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
                                  const float* g_c, const float* conv, void* H, const engram_state_t* state,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, const float* part, float* sa_out) {
   ConvArgs a{};
   a.B = B;
   a.Tn = T;
@@ -812,12 +909,13 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   // if it fits.  Among multiples of 4 * dilation (whole chains) up to that
   // bound, S then minimises waves-of-tiles x (S + halo + 8): the staged rows
   // of the slowest block plus a per-tile overhead.
-  const int64_t budget = (227 * 1024 - 1024) / kConvStages - 3 * 128;
+  const bool fin = part != nullptr;
+  const int64_t budget = (227 * 1024 - 1024) / kConvStages - 3 * 128 - (fin ? 2048 : 0);
   int S = 0, smax_halo = 0;
   double best = -1.0;
-  for (int cs = kConvMaxCS; cs >= 4; cs >>= 1) {
+  for (int cs = kConvMaxCS; cs >= (fin ? kConvMaxCS : 4); cs >>= 1) {   // fin: the compile-time 256 only
     if (a.d % cs || (static_cast<size_t>(cs) * act) % 16) continue;
-    const int64_t per_row = static_cast<int64_t>(cs) * 4 + a.saw * 4;   // v and sa of one staged position
+    const int64_t per_row = static_cast<int64_t>(cs) * 4 + a.saw * 4 + (fin ? 128 : 0);   // v, sa (partials)
     const int64_t per_pos = per_row + static_cast<int64_t>(a.M) * cs * static_cast<int64_t>(act);
     const int64_t box_cap = std::min<int64_t>(256 / a.M, 256);
     const int64_t s_no_halo = std::min<int64_t>(budget / per_pos, box_cap);
@@ -871,8 +969,12 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   const int64_t n_tiles = static_cast<int64_t>(B) * a.tiles_per_seq * a.n_ct;
   if (n_tiles > INT32_MAX) return cudaErrorInvalidValue;
   a.n_tiles = static_cast<int>(n_tiles);
-  conv_layout(a, act);
-  const size_t smem = static_cast<size_t>(kConvStages) * a.stage_bytes + 128;
+  if (fin && a.CS != kConvMaxCS) return cudaErrorInvalidValue;   // the caller falls back to the finalize kernel
+  conv_layout(a, act, fin);
+  a.sa_out = sa_out;
+  a.eps = p->cfg.eps;
+  const size_t smem = static_cast<size_t>(kConvStages) * a.stage_bytes + 1024;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
 
   CUtensorMap tv, th, ts;
   if (!make_tensor_map_2d(&tv, v, true, static_cast<uint64_t>(a.d), static_cast<uint64_t>(ntok),
@@ -881,13 +983,15 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
       !make_tensor_map_2d(&th, H, f32, static_cast<uint64_t>(a.d), static_cast<uint64_t>(ntok * a.M),
                           static_cast<uint64_t>(a.d) * act, static_cast<uint32_t>(a.CS),
                           static_cast<uint32_t>(a.S * a.M), false) ||
-      !make_tensor_map_2d(&ts, sa, true, static_cast<uint64_t>(a.saw), static_cast<uint64_t>(ntok),
-                          static_cast<uint64_t>(a.saw) * 4, static_cast<uint32_t>(a.saw),
-                          static_cast<uint32_t>(a.S + a.h0), false))
+      !(fin ? make_tensor_map_2d(&ts, part, true, 32, static_cast<uint64_t>(ntok), 32 * 4, 32,
+                                 static_cast<uint32_t>(a.S + a.h0), true)
+            : make_tensor_map_2d(&ts, sa, true, static_cast<uint64_t>(a.saw), static_cast<uint64_t>(ntok),
+                                 static_cast<uint64_t>(a.saw) * 4, static_cast<uint32_t>(a.saw),
+                                 static_cast<uint32_t>(a.S + a.h0), false)))
     return cudaErrorInvalidValue;
   const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, p->num_sms));
-  if (f32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, s);
-  return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, s);
+  if (f32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, false, s);
+  return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, fin, s);
 }
 
 cudaError_t launch_decode_tail(const engram_plan* p, const float* v, int64_t sv, const float* sa_in, const float* part,
