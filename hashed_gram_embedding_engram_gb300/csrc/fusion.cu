@@ -34,6 +34,8 @@
 
 #include <algorithm>
 
+#include "conv_host.h"
+#include "conv_parts.cuh"
 #include "engram_internal.h"
 #include "gate.cuh"
 #include "ptx.cuh"
@@ -41,43 +43,7 @@
 namespace engram {
 namespace {
 
-__device__ __forceinline__ void ld4(const float* p, float* out) {
-  const float4 u = *reinterpret_cast<const float4*>(p);
-  out[0] = u.x;
-  out[1] = u.y;
-  out[2] = u.z;
-  out[3] = u.w;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-  return x;
-}
-
-// SiLU(x) = x * sigma(x) = x / (1 + e^-x), with the fast exponential and divide
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.f + __expf(-x)); }
-
-// Two fp32 lanes per instruction (sm_100 family): each lane is rounded exactly
-// as the scalar instruction would round it.
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
-  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
+using namespace cv;
 
 // ------------------------------------------------------------------ gate (bf16 layers: from partials)
 // Sum over a warp of the n values p[i * stride], i < n, as the adjacent
@@ -210,77 +176,6 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ kv,
   }
 }
 
-// ------------------------------------------------------------------ conv + SiLU + skip + residual
-constexpr int kConvThreads = 448;                 // compute threads (14 warps); one producer warp more
-constexpr int kChain = 4;                          // outputs per thread, a dilation apart
-constexpr int kConvStages = 3;
-constexpr uint64_t kConvWaitNs = 1000000000ull;   // 1 s: a healthy tile lands in microseconds
-constexpr int kConvMaxCS = 256;                    // channels per tile: one TMA box row (<= 256 elements)
-
-// n / d for 0 <= n < 2^31 as one widening multiply and a shift: with
-// 2^l >= d and s = 31 + l, m = ceil(2^s / d) fits in 32 bits and
-// floor(n * m / 2^s) = floor(n / d), since n * (m - 2^s/d) / 2^s < 2^-l <= 1/d
-// (the round-up method of Granlund & Montgomery, "Division by invariant
-// integers using multiplication", PLDI 1994).
-struct FastDiv {
-  uint32_t mul, sh;
-  __device__ __forceinline__ uint32_t div(uint32_t n) const {
-    return static_cast<uint32_t>((static_cast<uint64_t>(n) * mul) >> sh);
-  }
-};
-
-FastDiv make_fastdiv(uint32_t d) {
-  uint32_t l = 0;
-  while ((1ull << l) < d) ++l;
-  const uint32_t sh = 31 + l;
-  return FastDiv{static_cast<uint32_t>(((1ull << sh) + d - 1) / d), sh};
-}
-
-struct ConvArgs {
-  FastDiv div_ct, div_tps;   // by n_ct and by tiles_per_seq
-  int B, Tn, M, d, dil;
-  int S;                 // positions per tile
-  int CS;                // channels per tile
-  int h0;                // staged rows before a tile's first position: (w-1)*dil, or 0 if a sequence is one tile
-  int tiles_per_seq, n_ct, n_tiles;
-  int saw;               // floats per sa row
-  uint32_t v_off, h_off, sa_off, p_off, stage_bytes, tx_bytes;   // shared-memory layout of one stage
-  float* sa_out;         // gate scalars computed in-kernel (KFIN), for the streaming state; or null
-  float eps;
-  const float* g_c;      // [d]
-  const float* conv;     // [d, W]
-  const float* ring;     // [B, L, M, d] or null
-  const int32_t* pos;    // [B] (with a ring)
-  int L;
-  uint32_t* err;
-};
-
-// 4 channels of H as floats
-template <typename T>
-struct H4;
-template <>
-struct H4<__nv_bfloat16> {
-  __device__ static void load(const __nv_bfloat16* p, float* out) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    out[0] = __uint_as_float(u.x << 16);
-    out[1] = __uint_as_float(u.x & 0xFFFF0000u);
-    out[2] = __uint_as_float(u.y << 16);
-    out[3] = __uint_as_float(u.y & 0xFFFF0000u);
-  }
-  __device__ static void store(__nv_bfloat16* p, const float* in) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
-    __nv_bfloat162 b = __floats2bfloat162_rn(in[2], in[3]);
-    *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
-  }
-};
-template <>
-struct H4<float> {
-  __device__ static void load(const float* p, float* out) { ld4(p, out); }
-  __device__ static void store(float* p, const float* in) {
-    *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
-  }
-};
-
 // Persistent blocks over tiles of (S positions of one sequence, CS channels).
 // Each tile's inputs are staged in shared memory by three TMA copies -- the v
 // rows of its positions and of the (w-1)*dilation positions before them, the
@@ -296,34 +191,24 @@ struct H4<float> {
 // chain's taps cover are read from shared memory once and scaled once; taps
 // (times g_c) in registers; SiLU, the skip and H += Y for every branch,
 // stored straight to H.
-// DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
 // KFIN: the block also turns the K/V epilogue's gate partial sums into the
 // (s, alpha) rows itself (8 slices per quantity, one branch): the producer's
 // third copy brings each staged position's 32 partials (128-byte rows,
 // 128-byte swizzle) instead of an sa row, and a helper warp -- one row per
 // lane, the finalize kernel's tree and arithmetic -- writes the stage's sa
 // rows and releases them through sa_ready, one tile ahead of the compute warps.
+// DIL > 0: compile-time dilation (the pages' w = 4, dilation = N); DIL = 0: a.dil.
 template <typename TH, int W, int DIL, int MC, int CSC, bool KFIN>
 __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
     conv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_h,
                 const __grid_constant__ CUtensorMap tm_sa, const ConvArgs a, TH* __restrict__ H) {
-  constexpr int kRows = kChain + W - 1;
   constexpr int kWarps = kConvThreads / 32;          // compute warps
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full[kConvStages], empty[kConvStages], sa_ready[kConvStages];
   __shared__ int s_abort;
-  const int dil = DIL > 0 ? DIL : a.dil;
   const int M = MC > 0 ? MC : a.M;
   const int tid = threadIdx.x;
-
-  auto coords = [&](int tile, int& b, int& t0, int& c0) {
-    const int q = static_cast<int>(a.div_ct.div(static_cast<uint32_t>(tile)));
-    const int ct = tile - q * a.n_ct;
-    b = static_cast<int>(a.div_tps.div(static_cast<uint32_t>(q)));
-    t0 = (q - b * a.tiles_per_seq) * a.S;
-    c0 = ct * a.CS;
-  };
 
   if (tid == 0) {
     for (int st = 0; st < kConvStages; ++st) {
@@ -342,9 +227,6 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
     if (tid >= kConvThreads + 32) {
       // ---------------------------------------------------------------- helper warp: gate scalars
       const int lane = tid & 31;
-      const float inv_d = 1.f / static_cast<float>(a.d);
-      const float inv_sqrt_d = 1.f / sqrtf(static_cast<float>(a.d));
-      const int rows = a.S + a.h0;
       int k = 0;
       for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
         const int st = k % kConvStages;
@@ -353,48 +235,7 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
           break;
         }
         if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-        const uint8_t* pp = smem + st * a.stage_bytes + a.p_off;       // [rows][32 floats], 128-byte swizzle
-        float* sa_s = reinterpret_cast<float*>(smem + st * a.stage_bytes + a.sa_off);
-        int b, t0, c0;
-        coords(tile, b, t0, c0);
-        for (int r = lane; r < rows; r += 32) {
-          float x[32];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 q = *reinterpret_cast<const float4*>(pp + r * 128 + ((j ^ (r & 7)) << 4));
-            x[4 * j] = q.x;
-            x[4 * j + 1] = q.y;
-            x[4 * j + 2] = q.z;
-            x[4 * j + 3] = q.w;
-          }
-          float sv[8], dt[8], sk[8], sh[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            sv[i] = x[i];
-            dt[i] = x[8 + 3 * i];
-            sk[i] = x[9 + 3 * i];
-            sh[i] = x[10 + 3 * i];
-          }
-#pragma unroll
-          for (int w = 1; w < 8; w *= 2)
-#pragma unroll
-            for (int i = 0; i + w < 8; i += 2 * w) {
-              sv[i] = sv[i] + sv[i + w];
-              dt[i] = dt[i] + dt[i + w];
-              sk[i] = sk[i] + sk[i + w];
-              sh[i] = sh[i] + sh[i + w];
-            }
-          float out[2];
-          gate_scalars(sv[0], dt[0], sk[0], sh[0], inv_d, inv_sqrt_d, a.eps, out, 1, 0);
-          sa_s[r * 4] = out[0];
-          sa_s[r * 4 + 1] = out[1];
-          const int t = t0 - a.h0 + r;
-          if (a.sa_out != nullptr && c0 == 0 && r >= a.h0 && t < a.Tn) {
-            float* g = a.sa_out + (static_cast<int64_t>(b) * a.Tn + t) * 4;
-            g[0] = out[0];
-            g[1] = out[1];
-          }
-        }
+        conv_fin_rows(a, smem + st * a.stage_bytes, tile, lane);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sa_ready[st]);
       }
@@ -418,14 +259,7 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
           *reinterpret_cast<volatile int*>(&s_abort) = 1;
           break;
         }
-        int b, t0, c0;
-        coords(tile, b, t0, c0);
-        const int32_t row0 = b * a.Tn + t0 - a.h0;   // may be negative: zero fill
-        uint8_t* base = smem + st * a.stage_bytes;
-        ptx::mbar_arrive_expect_tx(&full[st], a.tx_bytes);
-        ptx::tma_load_2d_nohint(base + a.v_off, &tm_v, &full[st], c0, row0);
-        ptx::tma_load_2d_nohint(base + a.h_off, &tm_h, &full[st], c0, (b * a.Tn + t0) * M);
-        ptx::tma_load_2d_nohint(base + (KFIN ? a.p_off : a.sa_off), &tm_sa, &full[st], 0, row0);
+        conv_issue<KFIN>(a, &tm_v, &tm_h, &tm_sa, smem + st * a.stage_bytes, &full[st], tile, M);
         armed |= 1u << st;
       }
       // copies still in flight land before the block may exit
@@ -442,28 +276,18 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
 
   // -------------------------------------------------------------------- compute warps
   const int lane = tid & 31;
-  const int CS = CSC > 0 ? CSC : a.CS;            // channels per tile (compile-time on the common shape)
-  const int saw = MC == 1 ? 4 : a.saw;             // floats per sa row
+  const int CS = CSC > 0 ? CSC : a.CS;
   const int ng = CS >> 2;                          // channel groups of a tile
   const int npar = kConvThreads / ng;              // chains processed side by side
   const int g = tid % ng, par0 = tid / ng;
   int c_cached = -1;
   float wq[4][W];                                  // taps times g_c for channels c .. c+3
-  auto load_taps = [&](int c) {
-    float gc[4];
-    ld4(a.g_c + c, gc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int j = 0; j < W; ++j) wq[i][j] = __ldg(a.conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
-    }
-    c_cached = c;
-  };
   if (blockIdx.x < static_cast<unsigned>(a.n_tiles) && par0 < npar) {
     // the first tile's taps, while its copies are in flight
     int b, t0, c0;
-    coords(blockIdx.x, b, t0, c0);
-    load_taps(c0 + 4 * g);
+    conv_coords(a, blockIdx.x, b, t0, c0);
+    c_cached = c0 + 4 * g;
+    conv_load_taps<W>(a, c_cached, wq);
   }
   int k = 0;
   int rot = par0;                                  // this tile's first chain: rotates by one per tile
@@ -480,116 +304,14 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
       }
     }
     if (*reinterpret_cast<volatile int*>(&s_abort)) break;
-    int b, t0, c0;
-    coords(tile, b, t0, c0);
-    const int nt = min(a.S, a.Tn - t0);
-    const uint8_t* base = smem + st * a.stage_bytes;
-    const float* vs = reinterpret_cast<const float*>(base + a.v_off);    // [S + h0][CS], row r: position t0 - h0 + r
-    const TH* hs = reinterpret_cast<const TH*>(base + a.h_off);          // [S * M][CS]
-    const float* ss = reinterpret_cast<const float*>(base + a.sa_off);   // [S + h0][saw]
     if (par0 < npar) {
-      const int c = c0 + 4 * g;
-      if (c != c_cached) load_taps(c);
-      const int p0 = a.ring != nullptr ? a.pos[b] : 0;
-      const int rstride = dil * CS;                    // floats between tap rows in the staged v
-      const int64_t hrow = static_cast<int64_t>(M) * a.d;                 // elements per position of H
-      TH* const hbase = H + (static_cast<int64_t>(b) * a.Tn + t0) * hrow + c;   // position t0, branch 0
-      // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
-      const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
-      for (int ch = rot; ch < n_chains; ch += npar) {
-        const int tb = (ch / dil) * (kChain * dil) + ch % dil;
-        if (tb >= nt) continue;
-        if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
-          // interior chain: every row staged, every output in the tile -- no branches, all loads first
-          const int r0 = a.h0 + tb - (W - 1) * dil;
-          const float* vp = vs + r0 * CS + 4 * g;
-          const float* sp = ss + r0 * saw;
-          float vr[kRows][4];
-#pragma unroll
-          for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
-          for (int m = 0; m < M; ++m) {
-            float u[kRows][4], h[kChain][4], at[kChain];
-#pragma unroll
-            for (int o = 0; o < kChain; ++o) {
-              H4<TH>::load(hs + ((tb + o * dil) * M + m) * CS + 4 * g, h[o]);
-              at[o] = sp[(o + W - 1) * dil * saw + M + m];
-            }
-#pragma unroll
-            for (int j = 0; j < kRows; ++j) {
-              const float sj = sp[j * dil * saw + m];
-              mul2(u[j][0], u[j][1], sj, sj, vr[j][0], vr[j][1]);
-              mul2(u[j][2], u[j][3], sj, sj, vr[j][2], vr[j][3]);
-            }
-#pragma unroll
-            for (int o = 0; o < kChain; ++o) {
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int j = 0; j < W; ++j) {
-                fma2(acc[0], acc[1], wq[0][j], wq[1][j], u[o + j][0], u[o + j][1], acc[0], acc[1]);
-                fma2(acc[2], acc[3], wq[2][j], wq[3][j], u[o + j][2], u[o + j][3], acc[2], acc[3]);
-              }
-              float y[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) y[i] = silu_fast(acc[i]);
-              fma2(y[0], y[1], at[o], at[o], vr[o + W - 1][0], vr[o + W - 1][1], y[0], y[1]);
-              fma2(y[2], y[3], at[o], at[o], vr[o + W - 1][2], vr[o + W - 1][3], y[2], y[3]);
-              add2(h[o][0], h[o][1], h[o][0], h[o][1], y[0], y[1]);
-              add2(h[o][2], h[o][3], h[o][2], h[o][3], y[2], y[3]);
-            }
-            TH* hp = hbase + static_cast<int64_t>(tb) * hrow + static_cast<int64_t>(m) * a.d;
-#pragma unroll
-            for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o * dil) * hrow, h[o]);
-          }
-          continue;
-        }
-        float vr[kRows][4];                           // v of rows tb + (j - (W-1))*dil, tile-relative
-#pragma unroll
-        for (int j = 0; j < kRows; ++j) {
-          const int tr = tb + (j - (W - 1)) * dil;
-          if (t0 + tr >= 0 && tr < nt) {
-            ld4(vs + (a.h0 + tr) * CS + 4 * g, vr[j]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
-          }
-        }
-        for (int m = 0; m < M; ++m) {
-          float u[kRows][4];                          // conv input RMSNorm(v~) before g_c: s * v, or the ring
-#pragma unroll
-          for (int j = 0; j < kRows; ++j) {
-            const int tr = tb + (j - (W - 1)) * dil;
-            if (tr >= nt) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
-            } else if (t0 + tr >= 0) {
-              const float sj = ss[(a.h0 + tr) * saw + m];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
-            } else if (a.ring != nullptr && p0 + t0 + tr >= 0) {
-              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t0 + tr) % a.L) * M + m) * a.d + c, u[j]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
-            }
-          }
-#pragma unroll
-          for (int o = 0; o < kChain; ++o) {
-            const int tt = tb + o * dil;
-            if (tt >= nt) break;
-            float h[4];
-            H4<TH>::load(hs + (tt * M + m) * CS + 4 * g, h);
-            const float at = ss[(a.h0 + tt) * saw + M + m];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float acc = 0.f;
-#pragma unroll
-              for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
-              h[i] = h[i] + fmaf(at, vr[o + W - 1][i], silu_fast(acc));
-            }
-            H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t0 + tt) * M + m) * a.d + c, h);
-          }
-        }
+      int b, t0, c0;
+      conv_coords(a, tile, b, t0, c0);
+      if (c0 + 4 * g != c_cached) {
+        c_cached = c0 + 4 * g;
+        conv_load_taps<W>(a, c_cached, wq);
       }
+      conv_tile<TH, W, DIL, MC, CSC>(a, smem + st * a.stage_bytes, tile, g, rot, npar, wq, H);
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&empty[st]);    // this warp is done with the stage
@@ -881,9 +603,10 @@ bool conv_fuses_gate(const engram_plan* p, int n_sl, int pstride) {
          p->cfg.conv_dilation <= 8 && n_sl == 8 && pstride == 32 && p->cfg.d % kConvMaxCS == 0;
 }
 
-cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
-                                 const float* g_c, const float* conv, void* H, const engram_state_t* state,
-                                 cudaStream_t s, const float* part, float* sa_out) {
+cudaError_t conv_prepare(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
+                         const float* g_c, const float* conv, void* H, const engram_state_t* state, const float* part,
+                         float* sa_out, ConvArgs* out, CUtensorMap* tv_out, CUtensorMap* th_out, CUtensorMap* ts_out,
+                         size_t* smem_out, size_t smem_cap) {
   ConvArgs a{};
   a.B = B;
   a.Tn = T;
@@ -910,7 +633,7 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   // bound, S then minimises waves-of-tiles x (S + halo + 8): the staged rows
   // of the slowest block plus a per-tile overhead.
   const bool fin = part != nullptr;
-  const int64_t budget = (227 * 1024 - 1024) / kConvStages - 3 * 128 - (fin ? 2048 : 0);
+  const int64_t budget = (static_cast<int64_t>(smem_cap) - 1024) / kConvStages - 3 * 128 - (fin ? 2048 : 0);
   int S = 0, smax_halo = 0;
   double best = -1.0;
   for (int cs = kConvMaxCS; cs >= (fin ? kConvMaxCS : 4); cs >>= 1) {   // fin: the compile-time 256 only
@@ -974,9 +697,11 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   a.sa_out = sa_out;
   a.eps = p->cfg.eps;
   const size_t smem = static_cast<size_t>(kConvStages) * a.stage_bytes + 1024;
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  if (smem > smem_cap) return cudaErrorInvalidValue;
 
-  CUtensorMap tv, th, ts;
+  CUtensorMap& tv = *tv_out;
+  CUtensorMap& th = *th_out;
+  CUtensorMap& ts = *ts_out;
   if (!make_tensor_map_2d(&tv, v, true, static_cast<uint64_t>(a.d), static_cast<uint64_t>(ntok),
                           static_cast<uint64_t>(sv) * 4, static_cast<uint32_t>(a.CS),
                           static_cast<uint32_t>(a.S + a.h0), false) ||
@@ -989,9 +714,23 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
                                  static_cast<uint64_t>(a.saw) * 4, static_cast<uint32_t>(a.saw),
                                  static_cast<uint32_t>(a.S + a.h0), false)))
     return cudaErrorInvalidValue;
+  *out = a;
+  *smem_out = smem;
+  return cudaSuccess;
+}
+
+cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t sv, const float* sa, int B, int T,
+                                 const float* g_c, const float* conv, void* H, const engram_state_t* state,
+                                 cudaStream_t s, const float* part, float* sa_out) {
+  ConvArgs a;
+  CUtensorMap tv, th, ts;
+  size_t smem = 0;
+  const cudaError_t e =
+      conv_prepare(p, v, sv, sa, B, T, g_c, conv, H, state, part, sa_out, &a, &tv, &th, &ts, &smem, 227 * 1024);
+  if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, p->num_sms));
-  if (f32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, false, s);
-  return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, fin, s);
+  if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, false, s);
+  return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, part != nullptr, s);
 }
 
 cudaError_t launch_decode_tail(const engram_plan* p, const float* v, int64_t sv, const float* sa_in, const float* part,
