@@ -109,6 +109,7 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
     w.v32 = reinterpret_cast<float*>(take(n * d * 4));
     // widest case: 32-column slices, rows padded to 16 bytes
     w.part = reinterpret_cast<float*>(take(n * (((d / 32) * (1 + 3 * M) + 3) / 4 * 4) * 4));
+    w.sync = reinterpret_cast<uint32_t*>(take(engram::stage_b_sync_words(ntok) * 4));
   }
   w.sa = reinterpret_cast<float*>(take(n * engram::sa_row_floats(static_cast<int>(M)) * 4));
   w.bytes = off;
@@ -175,6 +176,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   p->max_tokens = max_tokens;
   p->device = dev;
   p->num_sms = sms;
+  p->fused_stage_b = false;
 
   PlanDev h{};
   h.R = R;
@@ -309,6 +311,26 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     v = ws.kv;
     sv = static_cast<int64_t>(M + 1) * d;
   } else {
+    cudaError_t fe = cudaErrorNotSupported;
+    if (plan->fused_stage_b && engram::stage_b_fused_applies(plan, ntok, T)) {
+      // projection and conv in one cooperative launch (after a one-block kernel zeroing its counters)
+      fe = engram::launch_stage_b_fused(plan, e, w->w_kv, B, T, H, w->g_h, w->g_k, w->g_c, w->conv, ws.v32, ws.part,
+                                        state ? ws.sa : nullptr, state, ws.sync, s);
+      if (fe == cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();     // fewer SMs than the plan saw (e.g. a partitioned device): two launches
+      } else if (fe != cudaSuccess) {
+        return ENGRAM_ERR_CUDA;
+      }
+    }
+    if (fe == cudaSuccess) {
+      mark(plan, s);
+      if (state) {
+        if (engram::launch_state_update(plan, ids, proj, V, ws.v32, d, ws.sa, B, T, state, s) != cudaSuccess)
+          return ENGRAM_ERR_CUDA;
+        mark(plan, s);
+      }
+      return ENGRAM_OK;
+    }
     int n_sl = 0, pstride = 0;
     if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part, &n_sl,
                                  &pstride, plan->num_sms, &plan->dev->err, s) != cudaSuccess)
@@ -511,6 +533,12 @@ engram_status_t engram_cache_stats(const engram_cache_t* c, engram_stream_t stre
   if (rows_looked_up) *rows_looked_up = st[0];
   if (rows_from_hbm) *rows_from_hbm = st[1];
   if (cached_rows) *cached_rows = c->cached;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable) {
+  if (!plan || (enable != 0 && enable != 1)) return ENGRAM_ERR_INVALID_ARG;
+  plan->fused_stage_b = enable != 0;
   return ENGRAM_OK;
 }
 

@@ -58,6 +58,7 @@ struct engram_plan {
   cudaEvent_t marks[kMaxMarks];
   bool timing;
   mutable int n_marks;
+  bool fused_stage_b;              // Stage B as one cooperative launch where launch_stage_b_fused applies
 };
 
 namespace engram {
@@ -88,6 +89,7 @@ struct Workspace {
   float* v32;        // bf16 layers: [ntok, d] v in fp32 (fused K/V epilogue)
   float* part;       // bf16 layers: gate partial sums, at most (d/32)(1+3M) per token (rows padded to 4)
   float* sa;         // [ntok, sa_row_floats(M)]: s^(1..M) = alpha/sqrt(mean(v~^2)+eps), then alpha^(1..M)
+  uint32_t* sync;    // bf16 layers: stage_b_sync_words(ntok) counters of the fused Stage-B kernel
   size_t bytes;
 };
 Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base);
@@ -162,6 +164,18 @@ bool make_tensor_map_2d(CUtensorMap* map, const void* base, bool is_f32, uint64_
 bool make_tensor_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                              uint32_t box2, bool swizzle128);
+// Stage B (Steps 5-8) of a bf16, one-branch, w = 4 layer with 128-column
+// projection slices (d = 1024) and T > 1, as one cooperative launch (stage_b.cu):
+// the K/V projection with its gate epilogue and the conv with the in-kernel
+// gate finalisation, the conv tiles starting as soon as their row blocks are
+// projected.  Bit-identical to gemm_bf16_engram + launch_conv_residual(part).
+// sync: stage_b_sync_words(B*T) words of device memory (any contents).
+bool stage_b_fused_applies(const engram_plan* p, int64_t ntok, int T);
+size_t stage_b_sync_words(int64_t ntok);
+cudaError_t launch_stage_b_fused(const engram_plan* p, const void* e, const void* w_kv, int B, int T, void* H,
+                                 const float* g_h, const float* g_k, const float* g_c, const float* conv, float* v32,
+                                 float* part, float* sa_out, const engram_state_t* state, uint32_t* sync,
+                                 cudaStream_t s);
 // fp32 GEMM on the CUDA cores, same shapes.
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);
 

@@ -248,6 +248,11 @@ class EngramPlan:
             _dev(ws, "workspace"), ws.numel(), _stream()), "engram_forward")
         return H
 
+    def set_fused_stage_b(self, enable: bool) -> None:
+        """Stage B as one cooperative launch, or as two launches (the default); same bits."""
+        _lib.check(self._lib.engram_plan_set_fused_stage_b(self._h, int(bool(enable))),
+                   "engram_plan_set_fused_stage_b")
+
     def set_timing(self, enable: bool) -> None:
         """Record CUDA events around each kernel of later forward / stage_b calls."""
         _lib.check(self._lib.engram_plan_set_timing(self._h, int(bool(enable))), "engram_plan_set_timing")

@@ -268,6 +268,18 @@ engram_status_t engram_stage_a_cached(const engram_cache_t* cache, const int32_t
 engram_status_t engram_cache_stats(const engram_cache_t* cache, engram_stream_t stream, int reset,
                                    uint64_t* rows_looked_up, uint64_t* rows_from_hbm, int64_t* cached_rows);
 
+/* Stage B of BF16 layers with one branch, conv_w = 4 and d = 1024 (eight
+ * 128-column slices per projection quantity), for chunks of T > 1 positions,
+ * can run as ONE cooperative launch (enable = 1): the K/V projection and the
+ * conv share the GPU, each conv tile starting as soon as the 128-row blocks
+ * it reads are projected (after a one-block kernel that zeroes the launch's
+ * counters in the workspace).  The default (enable = 0) is the two-launch
+ * form: projection, then the conv with the gate finalisation, which measures
+ * faster on GB300 at 4096 tokens.  Both give the same bits.  Other layer
+ * shapes always use separate launches.  enable: 0 or 1; applies to calls
+ * made after it. */
+engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable);
+
 /* Tracing.  With timing on, engram_forward / engram_stage_b record one of
  * the plan's CUDA events on `stream` before the first kernel and after every
  * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps
@@ -275,7 +287,10 @@ engram_status_t engram_cache_stats(const engram_cache_t* cache, engram_stream_t 
  * (finalize), conv + residual; on F32 layers: hash + gather, K/V projection,
  * gate, conv + residual; then the state update when a state is given.  Chunks
  * of one position (T = 1, decode) run the gate, conv, residual and state
- * update as one kernel after the K/V projection.
+ * update as one kernel after the K/V projection.  Where the conv computes the
+ * gate itself there is no finalize kernel; where Stage B is one cooperative
+ * launch (engram_plan_set_fused_stage_b), its events bracket the counter
+ * reset and that launch together.
  * engram_stage_b records the same list without the first kernel.  For use on
  * one stream at a time, outside CUDA-graph capture.  enable: 0 or 1. */
 engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable);

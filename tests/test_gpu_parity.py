@@ -271,10 +271,11 @@ def test_chunked_prefill_with_ragged_chunks():
 
 
 def test_streaming_bit_identical_across_gemm_tile_widths():
-    """2560 tokens at d = 1024 give the K/V GEMM 20 x 8 tiles of 128 x 256; chunks of
-    100 tokens run it with 128 x 64 tiles.  The gate's partial sums are combined as
-    one pairwise tree over 32-column chunks either way, so the outputs agree bit
-    for bit; the oracle checks a sample of positions."""
+    """2560 tokens at d = 1024 give the K/V projection 20 x 8 tiles of 128 x 256
+    (inside the one-launch Stage B); chunks of 100 tokens through the two-launch
+    form run it with 128 x 64 tiles.  The gate's partial sums are
+    combined as one pairwise tree over 32-column chunks either way, so the
+    outputs agree bit for bit; the oracle checks a sample of positions."""
     from hashed_gram_embedding_engram_gb300 import EngramState
     w = W.PREFILL_BF16.scaled(B=1, T=2560, V=5000, V_proj=3850, prime_target=4001)
     ids = W.token_stream(w)
@@ -283,7 +284,9 @@ def test_streaming_bit_identical_across_gemm_tile_widths():
     plan, weights, proj, H = make_layer(w, L, P, ids.size)
     ids_d = torch.from_numpy(ids).cuda()
     full = H.clone()
+    plan.set_fused_stage_b(True)
     plan.forward(ids_d, proj, weights, full)
+    plan.set_fused_stage_b(False)
     st = EngramState.zeros(plan, w.B)
     out = H.clone()
     for t0 in range(0, w.T, 100):
