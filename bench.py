@@ -144,6 +144,43 @@ def per_token_work(w, bn: int = 256) -> dict:
 
 
 # --------------------------------------------------------------------------- #
+# DRAM traffic per launch from the committed ncu summaries
+# --------------------------------------------------------------------------- #
+# The sources each kernel is compiled from; a summary's figure is used only
+# while they hash to what was profiled (otherwise the kernel changed: null).
+KERNEL_SOURCES = {
+    "kv_gemm": ["gemm.cu", "gemm_parts.cuh", "ptx.cuh"],
+    "conv": ["fusion.cu", "conv_parts.cuh", "gate.cuh", "ptx.cuh"],
+    "hash_gather": ["gather.cu", "hashing.cuh", "ptx.cuh"],
+}
+
+
+def sources_digest(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "hashed_gram_embedding_engram_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """dram read + write bytes per launch of `kernel` from profiles/*.md, if still current."""
+    import glob
+    import re
+    if kernel not in KERNEL_SOURCES:
+        return None
+    pat = re.compile(r"^traffic: (\w+) (\d+) bytes/launch, sources sha256 ([0-9a-f]+)\s*$")
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as fh:
+            for line in fh:
+                m = pat.match(line)
+                if m and m.group(1) == kernel:
+                    return int(m.group(2)) if m.group(3) == sources_digest(kernel) else None
+    return None
+
+
+# --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
 def run_ours(args) -> None:
@@ -291,7 +328,7 @@ def run_ours(args) -> None:
     top = max(names, key=lambda n: kernels[n]["ms"])
     kt = kernels[top]
     roofline = {"kernel": top, "bound": kt["bound"], "achieved": kt["achieved"], "peak": kt["peak"],
-                "unit": kt["unit"], "frac": kt["frac"], "traffic": None,
+                "unit": kt["unit"], "frac": kt["frac"], "traffic": profiled_traffic(top),
                 "peak_source": f"{peak_src} ({'bf16_tflops burst' if kt['bound'] == 'tensor' else 'hbm_gbs'})",
                 "algorithmic_per_token": work[top][1], "units_per_launch": w.ntok}
 
