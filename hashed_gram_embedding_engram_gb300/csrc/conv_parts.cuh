@@ -68,7 +68,7 @@ constexpr int kConvMaxCS = 256;                    // channels per tile: one TMA
 // integers using multiplication", PLDI 1994).
 struct FastDiv {
   uint32_t mul, sh;
-  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
     return static_cast<uint32_t>((static_cast<uint64_t>(n) * mul) >> sh);
   }
 };
@@ -157,44 +157,44 @@ __device__ __forceinline__ void conv_fin_rows(const ConvArgs& a, const uint8_t* 
   float* sa_s = reinterpret_cast<float*>(const_cast<uint8_t*>(base) + a.sa_off);
   int b, t0, c0;
   conv_coords(a, tile, b, t0, c0);
-        for (int r = lane; r < rows; r += 32) {
-          float x[32];
+  for (int r = lane; r < rows; r += 32) {
+    float x[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 q = *reinterpret_cast<const float4*>(pp + r * 128 + ((j ^ (r & 7)) << 4));
-            x[4 * j] = q.x;
-            x[4 * j + 1] = q.y;
-            x[4 * j + 2] = q.z;
-            x[4 * j + 3] = q.w;
-          }
-          float sv[8], dt[8], sk[8], sh[8];
+    for (int j = 0; j < 8; ++j) {
+      const float4 q = *reinterpret_cast<const float4*>(pp + r * 128 + ((j ^ (r & 7)) << 4));
+      x[4 * j] = q.x;
+      x[4 * j + 1] = q.y;
+      x[4 * j + 2] = q.z;
+      x[4 * j + 3] = q.w;
+    }
+    float sv[8], dt[8], sk[8], sh[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            sv[i] = x[i];
-            dt[i] = x[8 + 3 * i];
-            sk[i] = x[9 + 3 * i];
-            sh[i] = x[10 + 3 * i];
-          }
+    for (int i = 0; i < 8; ++i) {
+      sv[i] = x[i];
+      dt[i] = x[8 + 3 * i];
+      sk[i] = x[9 + 3 * i];
+      sh[i] = x[10 + 3 * i];
+    }
 #pragma unroll
-          for (int w = 1; w < 8; w *= 2)
+    for (int w = 1; w < 8; w *= 2)
 #pragma unroll
-            for (int i = 0; i + w < 8; i += 2 * w) {
-              sv[i] = sv[i] + sv[i + w];
-              dt[i] = dt[i] + dt[i + w];
-              sk[i] = sk[i] + sk[i + w];
-              sh[i] = sh[i] + sh[i + w];
-            }
-          float out[2];
-          gate_scalars(sv[0], dt[0], sk[0], sh[0], inv_d, inv_sqrt_d, a.eps, out, 1, 0);
-          sa_s[r * 4] = out[0];
-          sa_s[r * 4 + 1] = out[1];
-          const int t = t0 - a.h0 + r;
-          if (a.sa_out != nullptr && c0 == 0 && r >= a.h0 && t < a.Tn) {
-            float* g = a.sa_out + (static_cast<int64_t>(b) * a.Tn + t) * 4;
-            g[0] = out[0];
-            g[1] = out[1];
-          }
-        }
+      for (int i = 0; i + w < 8; i += 2 * w) {
+        sv[i] = sv[i] + sv[i + w];
+        dt[i] = dt[i] + dt[i + w];
+        sk[i] = sk[i] + sk[i + w];
+        sh[i] = sh[i] + sh[i + w];
+      }
+    float out[2];
+    gate_scalars(sv[0], dt[0], sk[0], sh[0], inv_d, inv_sqrt_d, a.eps, out, 1, 0);
+    sa_s[r * 4] = out[0];
+    sa_s[r * 4 + 1] = out[1];
+    const int t = t0 - a.h0 + r;
+    if (a.sa_out != nullptr && c0 == 0 && r >= a.h0 && t < a.Tn) {
+      float* g = a.sa_out + (static_cast<int64_t>(b) * a.Tn + t) * 4;
+      g[0] = out[0];
+      g[1] = out[1];
+    }
+  }
 }
 
 // Taps times g_c for channels c .. c+3.
@@ -226,106 +226,106 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
   const TH* hs = reinterpret_cast<const TH*>(base + a.h_off);          // [S * M][CS]
   const float* ss = reinterpret_cast<const float*>(base + a.sa_off);   // [S + h0][saw]
   const int c = c0 + 4 * g;
-      const int p0 = a.ring != nullptr ? a.pos[b] : 0;
-      const int rstride = dil * CS;                    // floats between tap rows in the staged v
-      const int64_t hrow = static_cast<int64_t>(M) * a.d;                 // elements per position of H
-      TH* const hbase = H + (static_cast<int64_t>(b) * a.Tn + t0) * hrow + c;   // position t0, branch 0
-      // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
-      const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
-      for (int ch = rot; ch < n_chains; ch += npar) {
-        const int tb = (ch / dil) * (kChain * dil) + ch % dil;
-        if (tb >= nt) continue;
-        if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
-          // interior chain: every row staged, every output in the tile -- no branches, all loads first
-          const int r0 = a.h0 + tb - (W - 1) * dil;
-          const float* vp = vs + r0 * CS + 4 * g;
-          const float* sp = ss + r0 * saw;
-          float vr[kRows][4];
+  const int p0 = a.ring != nullptr ? a.pos[b] : 0;
+  const int rstride = dil * CS;                    // floats between tap rows in the staged v
+  const int64_t hrow = static_cast<int64_t>(M) * a.d;                 // elements per position of H
+  TH* const hbase = H + (static_cast<int64_t>(b) * a.Tn + t0) * hrow + c;   // position t0, branch 0
+  // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
+  const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
+  for (int ch = rot; ch < n_chains; ch += npar) {
+    const int tb = (ch / dil) * (kChain * dil) + ch % dil;
+    if (tb >= nt) continue;
+    if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
+      // interior chain: every row staged, every output in the tile -- no branches, all loads first
+      const int r0 = a.h0 + tb - (W - 1) * dil;
+      const float* vp = vs + r0 * CS + 4 * g;
+      const float* sp = ss + r0 * saw;
+      float vr[kRows][4];
 #pragma unroll
-          for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
-          for (int m = 0; m < M; ++m) {
-            float u[kRows][4], h[kChain][4], at[kChain];
+      for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
+      for (int m = 0; m < M; ++m) {
+        float u[kRows][4], h[kChain][4], at[kChain];
 #pragma unroll
-            for (int o = 0; o < kChain; ++o) {
-              H4<TH>::load(hs + ((tb + o * dil) * M + m) * CS + 4 * g, h[o]);
-              at[o] = sp[(o + W - 1) * dil * saw + M + m];
-            }
-#pragma unroll
-            for (int j = 0; j < kRows; ++j) {
-              const float sj = sp[j * dil * saw + m];
-              mul2(u[j][0], u[j][1], sj, sj, vr[j][0], vr[j][1]);
-              mul2(u[j][2], u[j][3], sj, sj, vr[j][2], vr[j][3]);
-            }
-#pragma unroll
-            for (int o = 0; o < kChain; ++o) {
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-              for (int j = 0; j < W; ++j) {
-                fma2(acc[0], acc[1], wq[0][j], wq[1][j], u[o + j][0], u[o + j][1], acc[0], acc[1]);
-                fma2(acc[2], acc[3], wq[2][j], wq[3][j], u[o + j][2], u[o + j][3], acc[2], acc[3]);
-              }
-              float y[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) y[i] = silu_fast(acc[i]);
-              fma2(y[0], y[1], at[o], at[o], vr[o + W - 1][0], vr[o + W - 1][1], y[0], y[1]);
-              fma2(y[2], y[3], at[o], at[o], vr[o + W - 1][2], vr[o + W - 1][3], y[2], y[3]);
-              add2(h[o][0], h[o][1], h[o][0], h[o][1], y[0], y[1]);
-              add2(h[o][2], h[o][3], h[o][2], h[o][3], y[2], y[3]);
-            }
-            TH* hp = hbase + static_cast<int64_t>(tb) * hrow + static_cast<int64_t>(m) * a.d;
-#pragma unroll
-            for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o * dil) * hrow, h[o]);
-          }
-          continue;
+        for (int o = 0; o < kChain; ++o) {
+          H4<TH>::load(hs + ((tb + o * dil) * M + m) * CS + 4 * g, h[o]);
+          at[o] = sp[(o + W - 1) * dil * saw + M + m];
         }
-        float vr[kRows][4];                           // v of rows tb + (j - (W-1))*dil, tile-relative
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
-          const int tr = tb + (j - (W - 1)) * dil;
-          if (t0 + tr >= 0 && tr < nt) {
-            ld4(vs + (a.h0 + tr) * CS + 4 * g, vr[j]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
-          }
+          const float sj = sp[j * dil * saw + m];
+          mul2(u[j][0], u[j][1], sj, sj, vr[j][0], vr[j][1]);
+          mul2(u[j][2], u[j][3], sj, sj, vr[j][2], vr[j][3]);
         }
-        for (int m = 0; m < M; ++m) {
-          float u[kRows][4];                          // conv input RMSNorm(v~) before g_c: s * v, or the ring
 #pragma unroll
-          for (int j = 0; j < kRows; ++j) {
-            const int tr = tb + (j - (W - 1)) * dil;
-            if (tr >= nt) {
+        for (int o = 0; o < kChain; ++o) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
-            } else if (t0 + tr >= 0) {
-              const float sj = ss[(a.h0 + tr) * saw + m];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
-            } else if (a.ring != nullptr && p0 + t0 + tr >= 0) {
-              ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t0 + tr) % a.L) * M + m) * a.d + c, u[j]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
-            }
+          for (int j = 0; j < W; ++j) {
+            fma2(acc[0], acc[1], wq[0][j], wq[1][j], u[o + j][0], u[o + j][1], acc[0], acc[1]);
+            fma2(acc[2], acc[3], wq[2][j], wq[3][j], u[o + j][2], u[o + j][3], acc[2], acc[3]);
           }
+          float y[4];
 #pragma unroll
-          for (int o = 0; o < kChain; ++o) {
-            const int tt = tb + o * dil;
-            if (tt >= nt) break;
-            float h[4];
-            H4<TH>::load(hs + (tt * M + m) * CS + 4 * g, h);
-            const float at = ss[(a.h0 + tt) * saw + M + m];
+          for (int i = 0; i < 4; ++i) y[i] = silu_fast(acc[i]);
+          fma2(y[0], y[1], at[o], at[o], vr[o + W - 1][0], vr[o + W - 1][1], y[0], y[1]);
+          fma2(y[2], y[3], at[o], at[o], vr[o + W - 1][2], vr[o + W - 1][3], y[2], y[3]);
+          add2(h[o][0], h[o][1], h[o][0], h[o][1], y[0], y[1]);
+          add2(h[o][2], h[o][3], h[o][2], h[o][3], y[2], y[3]);
+        }
+        TH* hp = hbase + static_cast<int64_t>(tb) * hrow + static_cast<int64_t>(m) * a.d;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float acc = 0.f;
+        for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o * dil) * hrow, h[o]);
+      }
+      continue;
+    }
+    float vr[kRows][4];                           // v of rows tb + (j - (W-1))*dil, tile-relative
 #pragma unroll
-              for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
-              h[i] = h[i] + fmaf(at, vr[o + W - 1][i], silu_fast(acc));
-            }
-            H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t0 + tt) * M + m) * a.d + c, h);
-          }
+    for (int j = 0; j < kRows; ++j) {
+      const int tr = tb + (j - (W - 1)) * dil;
+      if (t0 + tr >= 0 && tr < nt) {
+        ld4(vs + (a.h0 + tr) * CS + 4 * g, vr[j]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
+      }
+    }
+    for (int m = 0; m < M; ++m) {
+      float u[kRows][4];                          // conv input RMSNorm(v~) before g_c: s * v, or the ring
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        const int tr = tb + (j - (W - 1)) * dil;
+        if (tr >= nt) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
+        } else if (t0 + tr >= 0) {
+          const float sj = ss[(a.h0 + tr) * saw + m];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) u[j][i] = sj * vr[j][i];
+        } else if (a.ring != nullptr && p0 + t0 + tr >= 0) {
+          ld4(a.ring + ((static_cast<int64_t>(b) * a.L + (p0 + t0 + tr) % a.L) * M + m) * a.d + c, u[j]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) u[j][i] = 0.f;
         }
       }
+#pragma unroll
+      for (int o = 0; o < kChain; ++o) {
+        const int tt = tb + o * dil;
+        if (tt >= nt) break;
+        float h[4];
+        H4<TH>::load(hs + (tt * M + m) * CS + 4 * g, h);
+        const float at = ss[(a.h0 + tt) * saw + M + m];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < W; ++j) acc = fmaf(wq[i][j], u[o + j][i], acc);
+          h[i] = h[i] + fmaf(at, vr[o + W - 1][i], silu_fast(acc));
+        }
+        H4<TH>::store(H + ((static_cast<int64_t>(b) * a.Tn + t0 + tt) * M + m) * a.d + c, h);
+      }
+    }
+  }
 }
 
 }  // namespace cv

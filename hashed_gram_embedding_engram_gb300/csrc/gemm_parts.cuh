@@ -260,36 +260,35 @@ __device__ __forceinline__ void gemm_producer(const GemmCtx& c, const CUtensorMa
   uint8_t* smem = c.smem;
   uint32_t* err = c.err;
   const int n_tiles = c.n_tiles, num_tiles = c.num_tiles, k_blocks = c.k_blocks;
-      // ------------------------------------------------ TMA producer
-      const uint64_t keep = ptx::policy_evict_last();    // W_kv is re-read by every row tile
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;               // per stage: armed at least once / parity
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles) * kBM;
-        const int n0 = (tile % n_tiles) * BN;
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!wait_or_abort(&bars->empty[stage], phase ^ 1, bars, err)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + stage * G::kStageBytes;
-          ptx::mbar_arrive_expect_tx(&bars->full[stage], G::kStageBytes);
-          ptx::tma_load_2d_nohint(sa, tmA, &bars->full[stage], kb * kBK, m0);
-          ptx::tma_load_2d(sa + G::kABytes, tmB, &bars->full[stage], kb * kBK, n0, keep);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == G::kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+  const uint64_t keep = ptx::policy_evict_last();    // W_kv is re-read by every row tile
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t armed = 0, armed_parity = 0;               // per stage: armed at least once / parity
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+    const int m0 = (tile / n_tiles) * kBM;
+    const int n0 = (tile % n_tiles) * BN;
+    for (int kb = 0; kb < k_blocks; ++kb) {
+      if (!wait_or_abort(&bars->empty[stage], phase ^ 1, bars, err)) {
+        ok = false;
+        break;
       }
-      // our own copies in flight must land before the CTA can exit
-      for (int s = 0; s < G::kStages; ++s)
-        if (armed & (1u << s)) ptx::mbar_wait_bounded(&bars->full[s], (armed_parity >> s) & 1u, kWaitLimitNs);
+      uint8_t* sa = smem + stage * G::kStageBytes;
+      ptx::mbar_arrive_expect_tx(&bars->full[stage], G::kStageBytes);
+      ptx::tma_load_2d_nohint(sa, tmA, &bars->full[stage], kb * kBK, m0);
+      ptx::tma_load_2d(sa + G::kABytes, tmB, &bars->full[stage], kb * kBK, n0, keep);
+      armed |= 1u << stage;
+      armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == G::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
     }
+  }
+  // our own copies in flight must land before the CTA can exit
+  for (int s = 0; s < G::kStages; ++s)
+    if (armed & (1u << s)) ptx::mbar_wait_bounded(&bars->full[s], (armed_parity >> s) & 1u, kWaitLimitNs);
+}
 
 // Warp 1, lane 0.
 template <int BN, bool kFused>
@@ -300,44 +299,43 @@ __device__ __forceinline__ void gemm_mma(const GemmCtx& c) {
   uint32_t* err = c.err;
   const uint32_t tmem = c.tmem;
   const int num_tiles = c.num_tiles, k_blocks = c.k_blocks;
-      // ------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        if (!wait_or_abort(&bars->tempty[acc], acc_phase ^ 1, bars, err)) break;
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!wait_or_abort(&bars->full[stage], phase, bars, err)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_u32(smem + stage * G::kStageBytes);
-          const uint32_t b_addr = a_addr + G::kABytes;
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + k * 32), ptx::sdesc_kmajor_sw128(b_addr + k * 32),
-                          G::kIdesc, (kb | k) != 0);
-          }
-          ptx::mma_commit(&bars->empty[stage]);
-          if (++stage == G::kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        ptx::mma_commit(&bars->tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+  int stage = 0;
+  uint32_t phase = 0;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+    if (!wait_or_abort(&bars->tempty[acc], acc_phase ^ 1, bars, err)) break;
+    ptx::tc_fence_after();
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+    for (int kb = 0; kb < k_blocks; ++kb) {
+      if (!wait_or_abort(&bars->full[stage], phase, bars, err)) {
+        ok = false;
+        break;
       }
-      // every MMA this thread issued has finished before TMEM is freed
-      ptx::mma_commit(&bars->drain);
-      ptx::mbar_wait_bounded(&bars->drain, 0, kWaitLimitNs);
+      ptx::tc_fence_after();
+      const uint32_t a_addr = ptx::smem_u32(smem + stage * G::kStageBytes);
+      const uint32_t b_addr = a_addr + G::kABytes;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + k * 32), ptx::sdesc_kmajor_sw128(b_addr + k * 32),
+                      G::kIdesc, (kb | k) != 0);
+      }
+      ptx::mma_commit(&bars->empty[stage]);
+      if (++stage == G::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
     }
+    if (!ok) break;
+    ptx::mma_commit(&bars->tfull[acc]);
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1;
+  }
+  // every MMA this thread issued has finished before TMEM is freed
+  ptx::mma_commit(&bars->drain);
+  ptx::mbar_wait_bounded(&bars->drain, 0, kWaitLimitNs);
+}
 
 // Warps 2..9.  kSignal: after each tile, the warp's global writes are made
 // visible device-wide (its TMA stores completed, proxy and memory fences) and
@@ -355,87 +353,86 @@ __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpil
   const int n_tiles = c.n_tiles, num_tiles = c.num_tiles, Mr = c.Mr, Nc = c.Nc;
   const CUtensorMap& tmV = *tmV_;
   const CUtensorMap& tmH = *tmH_;
-    // -------------------------------------------------- epilogue (warps 2..9)
-    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int ew = warp - 2;
-    const int c_lo = (ew >> 2) * (BN / 2);  // half of the tile's columns
-    uint8_t* eb = epi_smem + ew * kEpiWarpBytes;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    uint32_t h_phase = 0;
-    bool h_pending = false;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles) * kBM;
-      const int n0 = (tile % n_tiles) * BN;
-      const int row = m0 + q * 32 + lane;
-      const bool ktile = kFused && n0 >= epi.d;
-      if (ktile) {
-        // this warp's H slice (32 rows x BN/2 columns) lands while the tile's MMAs run
-        if (lane == 0) {
-          ptx::bulk_wait_read<0>();            // staged v of an earlier tile has left this buffer
-          ptx::fence_proxy_async_smem();
-          const int m = (n0 - epi.d) / epi.d;
-          const int col = n0 - epi.d - m * epi.d + c_lo;
-          ptx::mbar_arrive_expect_tx(&bars->hbar[ew], G::kHBoxes * 4096);
-#pragma unroll
-          for (int bx = 0; bx < G::kHBoxes; ++bx)
-            ptx::tma_load_3d(eb + bx * 4096, &tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32);
-        }
-        h_pending = true;
-      }
-      if (!wait_or_abort(&bars->tfull[acc], acc_phase, bars, err)) break;
-      ptx::tc_fence_after();
-      if (ktile) {
-        if (!wait_or_abort(&bars->hbar[ew], h_phase, bars, err)) break;
-        h_phase ^= 1;
-        h_pending = false;
-      }
-      const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if constexpr (!kFused) {
-#pragma unroll 1
-        for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c, r);
-          ptx::tmem_ld_wait();
-          if (row < Mr && n0 + c < Nc) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              packed[j] = *reinterpret_cast<uint32_t*>(&v);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(C + static_cast<int64_t>(row) * Nc + n0 + c);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-          }
-        }
-      } else {
-        fused_epilogue<BN>(epi, &tmV, eb, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->tempty[acc]);
-      if constexpr (kSignal) {
-        if (lane == 0) {
-          ptx::bulk_wait_all();                 // this tile's v stores are in global memory
-          ptx::fence_proxy_async_global();
-        }
-        __threadfence();                        // and every lane's partial sums
-        __syncwarp();
-        if (lane == 0) ptx::red_release_gpu_add(row_done + tile / n_tiles, 1u);
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
-    }
-    if constexpr (kFused) {
+  const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+  const int ew = warp - 2;
+  const int c_lo = (ew >> 2) * (BN / 2);  // half of the tile's columns
+  uint8_t* eb = epi_smem + ew * kEpiWarpBytes;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  uint32_t h_phase = 0;
+  bool h_pending = false;
+  for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    const int m0 = (tile / n_tiles) * kBM;
+    const int n0 = (tile % n_tiles) * BN;
+    const int row = m0 + q * 32 + lane;
+    const bool ktile = kFused && n0 >= epi.d;
+    if (ktile) {
+      // this warp's H slice (32 rows x BN/2 columns) lands while the tile's MMAs run
       if (lane == 0) {
-        // an H load that a timeout left in flight lands before the block exits; v stores complete
-        if (h_pending) ptx::mbar_wait_bounded(&bars->hbar[ew], h_phase, kWaitLimitNs);
-        ptx::bulk_wait_all();
+        ptx::bulk_wait_read<0>();            // staged v of an earlier tile has left this buffer
+        ptx::fence_proxy_async_smem();
+        const int m = (n0 - epi.d) / epi.d;
+        const int col = n0 - epi.d - m * epi.d + c_lo;
+        ptx::mbar_arrive_expect_tx(&bars->hbar[ew], G::kHBoxes * 4096);
+#pragma unroll
+        for (int bx = 0; bx < G::kHBoxes; ++bx)
+          ptx::tma_load_3d(eb + bx * 4096, &tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32);
       }
+      h_pending = true;
+    }
+    if (!wait_or_abort(&bars->tfull[acc], acc_phase, bars, err)) break;
+    ptx::tc_fence_after();
+    if (ktile) {
+      if (!wait_or_abort(&bars->hbar[ew], h_phase, bars, err)) break;
+      h_phase ^= 1;
+      h_pending = false;
+    }
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+    if constexpr (!kFused) {
+#pragma unroll 1
+      for (int c = c_lo; c < c_lo + BN / 2; c += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(t_row + c, r);
+        ptx::tmem_ld_wait();
+        if (row < Mr && n0 + c < Nc) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            packed[j] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(C + static_cast<int64_t>(row) * Nc + n0 + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        }
+      }
+    } else {
+      fused_epilogue<BN>(epi, &tmV, eb, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&bars->tempty[acc]);
+    if constexpr (kSignal) {
+      if (lane == 0) {
+        ptx::bulk_wait_all();                 // this tile's v stores are in global memory
+        ptx::fence_proxy_async_global();
+      }
+      __threadfence();                        // and every lane's partial sums
+      __syncwarp();
+      if (lane == 0) ptx::red_release_gpu_add(row_done + tile / n_tiles, 1u);
+    }
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1;
+  }
+  if constexpr (kFused) {
+    if (lane == 0) {
+      // an H load that a timeout left in flight lands before the block exits; v stores complete
+      if (h_pending) ptx::mbar_wait_bounded(&bars->hbar[ew], h_phase, kWaitLimitNs);
+      ptx::bulk_wait_all();
     }
   }
+}
 
 }  // namespace gk
 }  // namespace engram
