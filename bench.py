@@ -542,8 +542,8 @@ def run_workload(args) -> None:
             for ly in layers:
                 st = ly.get("state")
                 prev = None if st is None else st.prev_ids
-                if table_key == "cache":
-                    ly["cache"].stage_a(ids, ly["proj"], ly["weights"].scales, prev_ids=prev, out=ly["e"])
+                if table_key in ("cache", "dedup"):
+                    ly[table_key].stage_a(ids, ly["proj"], ly["weights"].scales, prev_ids=prev, out=ly["e"])
                 else:
                     table = ly[table_key] if table_key else ly["weights"].table
                     ly["plan"].stage_a(ids, ly["proj"], table, ly["weights"].scales, prev_ids=prev, out=ly["e"])
@@ -632,17 +632,62 @@ def run_workload(args) -> None:
             ly["cache_rows"] = ly["cache"].build()
             ly["cache"].stats(reset=True)
         ms_cache = timed("cache", K=min(args.steps, 50))
-        looked = hits = 0
+        looked = hits = link = 0
         for ly in layers:
-            a_, b_, _ = ly["cache"].stats(reset=True)
+            a_, b_, l_, _ = ly["cache"].stats(reset=True)
             looked += a_
             hits += b_
+            link += l_
+        # per-batch row dedup: each distinct row of a batch crosses the link once
+        # (alone, then together with the hot-row cache)
+        for ly in layers:
+            ly["dedup"] = EngramCache(ly["plan"], 0, ly["table_host"])
+            ly["dedup"].set_dedup(w.ntok * w.R)
+            ly["dedup"].stats(reset=True)
+        ms_dedup = timed("dedup", K=min(args.steps, 50))
+        d_looked = d_link = 0
+        for ly in layers:
+            a_, _, l_, _ = ly["dedup"].stats(reset=True)
+            d_looked += a_
+            d_link += l_
+        ly = layers[0]
+        for _ in range(3):
+            ly["dedup"].stage_a(ids, ly["proj"], ly["weights"].scales, out=ly["e"])
+        g0.record()
+        for _ in range(Kg):
+            ly["dedup"].stage_a(ids, ly["proj"], ly["weights"].scales, out=ly["e"])
+        g1.record()
+        g1.synchronize()
+        gd_ms = g0.elapsed_time(g1) / Kg
+        ly["dedup"].stats(reset=True)
+        for ly in layers:
+            ly["dedup"].close()
+            ly["cache"].set_dedup(w.ntok * w.R)
+            ly["cache"].stats(reset=True)
+        ms_both = timed("cache", K=min(args.steps, 50))
+        b_looked = b_link = 0
+        for ly in layers:
+            a_, _, l_, _ = ly["cache"].stats(reset=True)
+            b_looked += a_
+            b_link += l_
+        extra["dedup"] = {
+            "what": "per batch, each distinct table row crosses the host link once into an HBM region; "
+                    "every lookup is then served from HBM",
+            "rows_looked_up_per_step": w.ntok * w.R * len(layers),
+            "host_link_rows_per_step": int(round(d_link / max(1, d_looked) * w.ntok * w.R * len(layers))),
+            "host_link_bytes_per_step": int(round(d_link / max(1, d_looked) * w.ntok * w.R * len(layers))) * row_bytes,
+            "ms_per_step": round(ms_dedup, 5), "value": round(tokens_per_step / (ms_dedup / 1e3), 1),
+            "stage_a_ms": round(gd_ms, 5),
+            "with_hot_row_cache": {
+                "host_link_bytes_per_step": int(round(b_link / max(1, b_looked) * w.ntok * w.R * len(layers)))
+                * row_bytes,
+                "ms_per_step": round(ms_both, 5), "value": round(tokens_per_step / (ms_both / 1e3), 1)}}
         extra["hot_row_cache"] = {
             "capacity_rows": sum(int(frac * ly["plan"].total_rows) for ly in layers),
             "cached_rows": sum(ly["cache_rows"] for ly in layers),
             "admission": "LFU counts over a separate token sample of the same distribution",
             "hit_rate": round(hits / max(1, looked), 4),
-            "host_link_bytes_per_step": int((1 - hits / max(1, looked)) * w.ntok * w.R * len(layers) * row_bytes),
+            "host_link_bytes_per_step": int(link / max(1, looked) * w.ntok * w.R * len(layers) * row_bytes),
             "host_link_bytes_per_step_uncached": w.ntok * w.R * len(layers) * row_bytes,
             "ms_per_step": round(ms_cache, 5), "value": round(tokens_per_step / (ms_cache / 1e3), 1)}
         extra["uva"] = {"tables": "int8 rows in pinned host memory read over UVA (C2C), fp16 scales in HBM",

@@ -20,7 +20,8 @@ EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", 
            "engram_hash", "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward",
            "engram_get_error", "engram_plan_set_timing", "engram_plan_set_fused_stage_b", "engram_plan_kernel_times",
            "engram_forward_static_scratch", "engram_stage_a", "engram_cache_create", "engram_cache_destroy",
-           "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats")
+           "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats",
+           "engram_cache_set_dedup")
 
 
 class Config(ctypes.Structure):
@@ -73,8 +74,9 @@ def _lib() -> ctypes.CDLL:
         lib.engram_cache_observe.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]
         lib.engram_cache_build.argtypes = [vp, i32, vp, ctypes.POINTER(i64)]
         lib.engram_stage_a_cached.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp]
-        lib.engram_cache_stats.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_uint64),
+        lib.engram_cache_stats.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
                                            ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(i64)]
+        lib.engram_cache_set_dedup.argtypes = [vp, i64]
         lib.engram_stage_b.argtypes = [vp, vp, i32, i32, vp, i32, vp, ctypes.POINTER(Weights), vp,
                                        ctypes.POINTER(State), vp, sz, vp]
         lib.engram_forward.argtypes = [vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,

@@ -437,9 +437,12 @@ struct engram_cache {
   const void* table;                 // device view of the table
   uint32_t* counts;                  // [total rows]
   int32_t* slot;                     // [total rows]
-  void* rows;                        // [capacity, row_bytes]
-  unsigned long long* stats;         // [0] lookups, [1] hits, [2] slots used by the last build
+  void* rows;                        // [capacity + batch_cap, row_bytes]: cached rows, then the dedup region
+  unsigned long long* stats;         // [0] lookups, [1] served from HBM, [2] slots used by the last build,
+                                     // [3] rows fetched by the dedup
   int64_t cached;
+  int64_t batch_cap;                 // lookups the dedup region has a row for (0: no dedup)
+  uint32_t* batch_rows;              // [batch_cap] the table row each lookup claimed, or 0xFFFFFFFF
 };
 
 extern "C" {
@@ -448,7 +451,7 @@ engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity,
                                     engram_cache_t** out) {
   if (!plan || !table || !out) return ENGRAM_ERR_INVALID_ARG;
   *out = nullptr;
-  if (capacity <= 0 || capacity > plan->total_rows || capacity > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
+  if (capacity < 0 || capacity > plan->total_rows || capacity > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
   const void* tab = nullptr;
   if (engram_status_t s = device_view(table, &tab)) return s;
   if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
@@ -461,11 +464,11 @@ engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity,
   const size_t n = static_cast<size_t>(plan->total_rows);
   bool ok = cudaMalloc(&c->counts, n * sizeof(uint32_t)) == cudaSuccess &&
             cudaMalloc(&c->slot, n * sizeof(int32_t)) == cudaSuccess &&
-            cudaMalloc(&c->rows, static_cast<size_t>(capacity) * c->row_bytes) == cudaSuccess &&
-            cudaMalloc(&c->stats, 4 * sizeof(unsigned long long)) == cudaSuccess;
+            cudaMalloc(&c->rows, static_cast<size_t>(capacity > 0 ? capacity : 1) * c->row_bytes) == cudaSuccess &&
+            cudaMalloc(&c->stats, 8 * sizeof(unsigned long long)) == cudaSuccess;
   ok = ok && cudaMemset(c->counts, 0, n * sizeof(uint32_t)) == cudaSuccess &&
        cudaMemset(c->slot, 0xFF, n * sizeof(int32_t)) == cudaSuccess &&
-       cudaMemset(c->stats, 0, 4 * sizeof(unsigned long long)) == cudaSuccess;
+       cudaMemset(c->stats, 0, 8 * sizeof(unsigned long long)) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     engram_cache_destroy(c);
@@ -478,7 +481,8 @@ engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity,
 engram_status_t engram_cache_destroy(engram_cache_t* c) {
   if (!c) return ENGRAM_OK;
   cudaError_t e = cudaSuccess;
-  for (void* ptr : {static_cast<void*>(c->counts), static_cast<void*>(c->slot), c->rows, static_cast<void*>(c->stats)})
+  for (void* ptr : {static_cast<void*>(c->counts), static_cast<void*>(c->slot), c->rows, static_cast<void*>(c->stats),
+                    static_cast<void*>(c->batch_rows)})
     if (ptr && cudaFree(ptr) != cudaSuccess) e = cudaErrorUnknown;
   delete c;
   return cuda_status(e);
@@ -518,20 +522,62 @@ engram_status_t engram_stage_a_cached(const engram_cache_t* c, const int32_t* id
   if (i8) {
     if (engram_status_t s = device_view(scales, &sc)) return s;
   }
-  return cuda_status(engram::launch_hash_gather_cached(plan, ids, B, T, proj, V, prev_ids, c->table,
-                                                       static_cast<const uint16_t*>(sc), e_out, c->slot, c->rows,
-                                                       c->stats, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t lookups = static_cast<int64_t>(B) * T * plan->R;
+  const bool dedup = c->batch_cap > 0 && lookups <= c->batch_cap;
+  if (dedup) {
+    // distinct uncached rows of the batch: one fetch each over the host link, into the batch region
+    uint8_t* region = static_cast<uint8_t*>(c->rows) + static_cast<size_t>(c->capacity) * c->row_bytes;
+    if (engram::dedup_claim(plan, ids, B, T, proj, V, prev_ids, c->slot, static_cast<int32_t>(c->capacity),
+                            c->row_bytes, c->table, region, c->batch_rows, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+  }
+  if (engram::launch_hash_gather_cached(plan, ids, B, T, proj, V, prev_ids, c->table, static_cast<const uint16_t*>(sc),
+                                        e_out, c->slot, c->rows, c->stats, s) != cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  if (dedup && engram::dedup_release(plan, lookups, c->batch_rows, c->slot, c->stats + 3, s) != cudaSuccess)
+    return ENGRAM_ERR_CUDA;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_cache_set_dedup(engram_cache_t* c, int64_t batch_rows) {
+  if (!c || batch_rows < 0 || c->capacity + batch_rows > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
+  if (batch_rows == c->batch_cap) return ENGRAM_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ENGRAM_ERR_CUDA;
+  const size_t keep = static_cast<size_t>(c->capacity) * c->row_bytes;
+  const size_t total = keep + static_cast<size_t>(batch_rows) * c->row_bytes;
+  void* rows = nullptr;
+  uint32_t* br = nullptr;
+  bool ok = cudaMalloc(&rows, total > 0 ? total : c->row_bytes) == cudaSuccess &&
+            (batch_rows == 0 || cudaMalloc(&br, static_cast<size_t>(batch_rows) * sizeof(uint32_t)) == cudaSuccess);
+  ok = ok && (keep == 0 || cudaMemcpy(rows, c->rows, keep, cudaMemcpyDeviceToDevice) == cudaSuccess);
+  if (!ok) {
+    cudaGetLastError();
+    if (rows) cudaFree(rows);
+    if (br) cudaFree(br);
+    return ENGRAM_ERR_CUDA;
+  }
+  cudaFree(c->rows);
+  if (c->batch_rows) cudaFree(c->batch_rows);
+  c->rows = rows;
+  c->batch_rows = br;
+  c->batch_cap = batch_rows;
+  return ENGRAM_OK;
 }
 
 engram_status_t engram_cache_stats(const engram_cache_t* c, engram_stream_t stream, int reset,
-                                   uint64_t* rows_looked_up, uint64_t* rows_from_hbm, int64_t* cached_rows) {
+                                   uint64_t* rows_looked_up, uint64_t* rows_from_hbm, uint64_t* rows_over_link,
+                                   int64_t* cached_rows) {
   if (!c) return ENGRAM_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ENGRAM_ERR_CUDA;
-  unsigned long long st[2] = {0, 0};
+  unsigned long long st[4] = {0, 0, 0, 0};
   if (cudaMemcpy(st, c->stats, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return ENGRAM_ERR_CUDA;
-  if (reset && cudaMemset(c->stats, 0, sizeof(st)) != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (reset && (cudaMemset(c->stats, 0, 2 * sizeof(unsigned long long)) != cudaSuccess ||
+                cudaMemset(c->stats + 3, 0, sizeof(unsigned long long)) != cudaSuccess))
+    return ENGRAM_ERR_CUDA;
   if (rows_looked_up) *rows_looked_up = st[0];
   if (rows_from_hbm) *rows_from_hbm = st[1];
+  if (rows_over_link) *rows_over_link = (st[0] - st[1]) + st[3];
   if (cached_rows) *cached_rows = c->cached;
   return ENGRAM_OK;
 }

@@ -114,6 +114,16 @@ cudaError_t cache_observe(const engram_plan* p, const int32_t* ids, int B, int T
 cudaError_t cache_build(const engram_plan* p, int64_t capacity, int row_bytes, const void* table, uint32_t* counts,
                         int32_t* slot, void* rows, unsigned long long* used, int decay, int64_t* cached,
                         cudaStream_t s);
+// Per-batch row dedup through the cache's slot map (cache.cu): each distinct
+// row without a slot is claimed by one lookup f (slot first_slot + f; owner[f]
+// = its table row, else 0xFFFFFFFF) and copied into row f of the batch region;
+// after the gather the release returns the slots to -1 and adds the claims to
+// *fetched.
+cudaError_t dedup_claim(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                        const int32_t* prev_ids, int32_t* slot, int32_t first_slot, int row_bytes, const void* table,
+                        void* region, uint32_t* owner, cudaStream_t s);
+cudaError_t dedup_release(const engram_plan* p, int64_t total, const uint32_t* owner, int32_t* slot,
+                          unsigned long long* fetched, cudaStream_t s);
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
                                  cudaStream_t s);
 // Floats per row of the per-token gate scalars: [s^(1..M), alpha^(1..M)] padded to 16 bytes.

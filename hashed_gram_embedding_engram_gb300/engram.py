@@ -323,12 +323,18 @@ class EngramCache:
                                                    _stream()), "engram_stage_a_cached")
         return out
 
-    def stats(self, reset: bool = False) -> Tuple[int, int, int]:
-        """(rows looked up, rows served from HBM, rows cached) since the last reset."""
-        a, b, c = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_int64()
+    def set_dedup(self, batch_rows: int) -> None:
+        """Per-batch row dedup in ``stage_a``: each distinct uncached row of a
+        batch crosses the host link once (room for ``batch_rows`` of them; 0 = off)."""
+        _lib.check(self._lib.engram_cache_set_dedup(self._h, int(batch_rows)), "engram_cache_set_dedup")
+
+    def stats(self, reset: bool = False) -> Tuple[int, int, int, int]:
+        """(rows looked up, lookups served from HBM, rows read over the host link,
+        rows cached) since the last reset."""
+        a, b, l, c = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_int64()
         _lib.check(self._lib.engram_cache_stats(self._h, _stream(), int(bool(reset)), ctypes.byref(a), ctypes.byref(b),
-                                                ctypes.byref(c)), "engram_cache_stats")
-        return a.value, b.value, c.value
+                                                ctypes.byref(l), ctypes.byref(c)), "engram_cache_stats")
+        return a.value, b.value, l.value, c.value
 
 
 class EngramLayer:

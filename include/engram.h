@@ -233,12 +233,14 @@ engram_status_t engram_forward_static_scratch(const engram_plan_t* plan, const i
  * rows.  engram_stage_a_cached then reads cached rows from HBM and the rest
  * from the host table; its output equals engram_stage_a's bit for bit.
  * Device memory: 8 bytes per table row (counts and slot map) plus capacity
- * rows.  A cache belongs to one plan and one table; calls on it are
- * stream-ordered; engram_cache_build synchronises `stream`. */
+ * rows (plus the dedup region, below).  A cache belongs to one plan and one
+ * table; calls on it are stream-ordered (never in flight on two streams at
+ * once); engram_cache_build synchronises `stream`. */
 typedef struct engram_cache engram_cache_t;
 
 /* table: the plan's table in pinned or registered host memory (or on the
- * device); capacity: rows, 0 < capacity <= total rows.  Starts empty, counts 0. */
+ * device); capacity: rows, 0 <= capacity <= total rows (0: no hot rows, for
+ * the dedup alone).  Starts empty, counts 0, no dedup. */
 engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity, const void* table,
                                     engram_cache_t** out);
 engram_status_t engram_cache_destroy(engram_cache_t* cache);
@@ -256,17 +258,38 @@ engram_status_t engram_cache_observe(engram_cache_t* cache, const int32_t* ids, 
 engram_status_t engram_cache_build(engram_cache_t* cache, int decay, engram_stream_t stream,
                                    int64_t* cached_rows);
 
-/* engram_stage_a with the cache's table, cached rows read from HBM.  scales:
- * as in engram_gather (fp16 per row, HBM or mapped host memory; I8 only). */
+/* Per-batch row dedup.  Under the Zipf-skewed n-gram statistics of text many
+ * lookups of one batch read the same rows (about a quarter of them on the
+ * int8 host-table workload); "Engram 嵌入扩展：面向高效 DRAM/SSD 卸载的协同设计"
+ * names the host link as the cost.  With batch_rows > 0, every later
+ * engram_stage_a_cached whose batch has at most batch_rows lookups (B*T*R)
+ * first copies each distinct table row of the batch that is not cached over
+ * the host link once, into a per-batch HBM region with a row per lookup
+ * (after the cached rows, in the same slot map), serves every lookup of it
+ * from HBM, and frees the slots again (four launches instead of one;
+ * capturable).  Larger batches run without the dedup.  The output is
+ * unchanged, bit for bit.  batch_rows = 0 turns it off.  Synchronises the
+ * device and reallocates the cache's row buffer (cached rows are kept);
+ * capacity + batch_rows <= INT32_MAX.  Device memory: batch_rows x (row
+ * bytes + 4). */
+engram_status_t engram_cache_set_dedup(engram_cache_t* cache, int64_t batch_rows);
+
+/* engram_stage_a with the cache's table, cached rows read from HBM (and, with
+ * the dedup on, every row of the batch fetched once).  scales: as in
+ * engram_gather (fp16 per row, HBM or mapped host memory; I8 only). */
 engram_status_t engram_stage_a_cached(const engram_cache_t* cache, const int32_t* ids, int B, int T,
                                       const int32_t* proj, int V, const int32_t* prev_ids,
                                       const uint16_t* scales, void* e_out, engram_stream_t stream);
 
 /* Synchronise `stream` and read the counters of engram_stage_a_cached since
- * the last reset: table rows looked up and rows served from HBM; reset != 0
- * zeroes them.  Any output pointer may be NULL. */
+ * the last reset: table rows looked up, lookups served from HBM (cached rows
+ * and the dedup's batch region), and rows read over the host link (lookups
+ * read from the host table plus the dedup's one fetch per distinct row);
+ * reset != 0 zeroes them.  cached_rows: rows the last build cached.  Any
+ * output pointer may be NULL. */
 engram_status_t engram_cache_stats(const engram_cache_t* cache, engram_stream_t stream, int reset,
-                                   uint64_t* rows_looked_up, uint64_t* rows_from_hbm, int64_t* cached_rows);
+                                   uint64_t* rows_looked_up, uint64_t* rows_from_hbm, uint64_t* rows_over_link,
+                                   int64_t* cached_rows);
 
 /* Stage B of BF16 layers with one branch, conv_w = 4 and d = 1024 (eight
  * 128-column slices per projection quantity), for chunks of T > 1 positions,

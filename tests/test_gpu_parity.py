@@ -369,8 +369,8 @@ def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
     cache = EngramCache(plan, max(1, n_rows // 50), table_host)
     got = cache.stage_a(ids_d, proj, wd.scales)
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
-    looked, hits, cached = cache.stats(reset=True)
-    assert looked == ids.size * w.R and hits == 0 and cached == 0
+    looked, hits, link, cached = cache.stats(reset=True)
+    assert looked == ids.size * w.R and hits == 0 and cached == 0 and link == looked
     # LFU: observe a different sample of the same distribution, then serve this batch
     warm = torch.from_numpy(W.token_stream(w, key="cache-warm")).cuda()
     cache.observe(warm, proj)
@@ -378,19 +378,90 @@ def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
     assert 0 < cached <= n_rows // 50
     got = cache.stage_a(ids_d, proj, wd.scales)
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
-    looked, hits, _ = cache.stats(reset=True)
-    assert looked == ids.size * w.R and 0 < hits < looked
+    looked, hits, link, _ = cache.stats(reset=True)
+    assert looked == ids.size * w.R and 0 < hits < looked and link == looked - hits
     # the most-counted rows of the warm sample are cached: their accesses in it are all hits
     cache.stage_a(warm, proj, wd.scales)
-    looked_w, hits_w, _ = cache.stats(reset=True)
+    looked_w, hits_w, _, _ = cache.stats(reset=True)
     assert hits_w / looked_w >= hits / looked
     full = EngramCache(plan, n_rows, table_host)
     full.observe(ids_d, proj)
     assert full.build() == len(np.unique(ref_rows(w, ids, P, L)))
     got = full.stage_a(ids_d, proj, wd.scales)
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
-    looked, hits, _ = full.stats()
-    assert hits == looked
+    looked, hits, link, _ = full.stats()
+    assert hits == looked and link == 0
+
+
+@pytest.mark.parametrize("kind", ["small_i8", "small_bf16"])
+def test_dedup_stage_a_fetches_each_row_once(kind):
+    """Per-batch dedup: every distinct row of the batch crosses the host link
+    once (the oracle's count of distinct rows), every lookup is served from HBM,
+    and the output equals the plain gather bit for bit -- on two batches in a
+    row (the slots are released), with a batch region too small for the batch
+    (no dedup then), combined with an LFU cache, and replayed from a CUDA
+    graph."""
+    from hashed_gram_embedding_engram_gb300 import EngramCache
+    w = SMALL[kind]
+    ids = W.token_stream(w)
+    ids2 = W.token_stream(w, key="dedup-second")
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, wd, proj, H = make_layer(w, L, P, ids.size)
+    table_host = to_torch(L.table, w.table_dtype, "cpu", pin=True)
+    n = ids.size * w.R
+    for batch in (ids, ids2):
+        ids_d = torch.from_numpy(batch).cuda()
+        ref = plan.stage_a(ids_d, proj, wd.table, wd.scales)
+        uniq = len(np.unique(ref_rows(w, batch, P, L)))
+        assert uniq < n                                        # Zipf: some rows repeat
+        dd = EngramCache(plan, 0, table_host)
+        dd.set_dedup(n)
+        for _ in range(2):
+            got = dd.stage_a(ids_d, proj, wd.scales)
+            assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+            looked, from_hbm, link, cached = dd.stats(reset=True)
+            assert (looked, from_hbm, link, cached) == (n, n, uniq, 0)
+        # a region too small for the batch: no dedup, every lookup over the link
+        dd.set_dedup(n - 1)
+        got = dd.stage_a(ids_d, proj, wd.scales)
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        assert dd.stats(reset=True) == (n, 0, n, 0)
+        dd.close()
+    # with the LFU cache: cached rows never cross the link, the others once each
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = plan.stage_a(ids_d, proj, wd.table, wd.scales)
+    n_rows = int(np.sum(L.primes))
+    both = EngramCache(plan, max(1, n_rows // 50), table_host)
+    both.observe(torch.from_numpy(W.token_stream(w, key="cache-warm")).cuda(), proj)
+    assert both.build() > 0
+    both.set_dedup(n)
+    got = both.stage_a(ids_d, proj, wd.scales)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    looked, from_hbm, link, _ = both.stats(reset=True)
+    uniq = len(np.unique(ref_rows(w, ids, P, L)))
+    assert looked == n and from_hbm == n and 0 < link < uniq
+    # captured once, replayed twice: the claim, fetch, gather and release all replay
+    out = torch.empty_like(ref)
+    dd = EngramCache(plan, 0, table_host)
+    dd.set_dedup(n)
+    dd.stage_a(ids_d, proj, wd.scales, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            dd.stage_a(ids_d, proj, wd.scales, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    dd.stats(reset=True)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert dd.stats(reset=True)[2] == 2 * uniq
+    assert plan.get_error() == (0, 0)
 
 
 def ref_rows(w, ids, P, L):
