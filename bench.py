@@ -136,6 +136,9 @@ def per_token_work(w, bn: int = 256) -> dict:
         "kv_gemm": ("flops", 2 * w.d_mem * nc),
         # the K/V projection and the conv in one launch: bound by the projection's flops
         "stage_b": ("flops", 2 * w.d_mem * nc),
+        # FP8 projection: e read in bf16, its e4m3 codes and the token's scale written; the e4m3 GEMM
+        "quantize_e": ("bytes", 2 * w.d_mem + w.d_mem + 4),
+        "kv_gemm_fp8": ("flops", 2 * w.d_mem * nc),
         # gate partials in; the (scale, alpha) row out
         "finalize": ("bytes", 4 * n_part + 8 * w.M),
         # v (fp32), the (scale, alpha) row, H in; H out
@@ -197,6 +200,7 @@ def run_ours(args) -> None:
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
     w = W.PREFILL_BF16
+    fp8 = args.workload == "prefill_fp8"      # the same workload with the e4m3 K/V projection
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
@@ -209,6 +213,10 @@ def run_ours(args) -> None:
     for lid in w.layers:
         L = W.layer_inputs(w, lid)
         plan, weights, proj, H = make_layer(w, L, P, w.ntok)
+        if fp8:
+            import dataclasses
+            q, sc = plan.quantize_fp8(weights.w_kv)
+            weights = dataclasses.replace(weights, w_kv=None, w_kv_fp8=q, w_kv_scale=sc)
         layers.append({"plan": plan, "weights": weights, "proj": proj, "H0": H, "H": H.clone(),
                        "ws": plan.new_workspace(w.ntok), "H_host": to_torch(L.H, "bf16", "cpu", pin=True)})
         del L
@@ -286,6 +294,9 @@ def run_ours(args) -> None:
     # Stage B as one launch / projection + conv (gate in the conv) / + finalize
     name_sets = {2: ["hash_gather", "stage_b"], 3: ["hash_gather", "kv_gemm", "conv"],
                  4: ["hash_gather", "kv_gemm", "finalize", "conv"]}
+    if fp8:
+        name_sets = {4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
+                     5: ["hash_gather", "quantize_e", "kv_gemm_fp8", "finalize", "conv"]}
     names = None
     dur = {}
     for ly in layers:
@@ -316,8 +327,10 @@ def run_ours(args) -> None:
         amount = per_tok * w.ntok
         if kind == "flops":
             ach = amount / (ms / 1e3) / 1e12
+            # e4m3 runs at twice the bf16 rate on this part (nominal dense 4.5 vs 2.25 PFLOP/s)
+            pk = tc_peak * (2 if n.endswith("fp8") else 1)
             kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 2), "unit": "TFLOP/s",
-                          "peak": tc_peak, "frac": round(ach / tc_peak, 4), "bound": "tensor"}
+                          "peak": pk, "frac": round(ach / pk, 4), "bound": "tensor"}
         else:
             ach = amount / (ms / 1e3) / 1e9
             kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 1), "unit": "GB/s",
@@ -329,7 +342,7 @@ def run_ours(args) -> None:
     kt = kernels[top]
     roofline = {"kernel": top, "bound": kt["bound"], "achieved": kt["achieved"], "peak": kt["peak"],
                 "unit": kt["unit"], "frac": kt["frac"], "traffic": profiled_traffic(top),
-                "peak_source": f"{peak_src} ({'bf16_tflops burst' if kt['bound'] == 'tensor' else 'hbm_gbs'})",
+                "peak_source": f"{peak_src} ({'hbm_gbs' if kt['bound'] != 'tensor' else 'bf16_tflops burst x 2, the nominal e4m3/bf16 ratio' if top.endswith('fp8') else 'bf16_tflops burst'})",
                 "algorithmic_per_token": work[top][1], "units_per_launch": w.ntok}
 
     # ---- end to end through the public API: pinned host in, pinned host out ----
@@ -394,13 +407,15 @@ def run_ours(args) -> None:
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         cpu = cpu_baseline_subprocess(w)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        line = {"metric": METRIC if not fp8 else "Engram-layer tokens/s, prefill_fp8 workload (e4m3 K/V projection)",
+                "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if not fp8 else "e4m3 projection, bf16",
+                "data": "synthetic",
                 "config": dict(workload_desc(w), cuda_graph=True,
                                stage_a="every layer's hash+gather on a side stream, ahead of its Stage B"),
                 "roofline": roofline, "kernels": kernels,
@@ -506,7 +521,8 @@ def run_workload(args) -> None:
     from tests.gpu_helpers import make_layer, to_torch
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = W.BY_NAME[args.workload]
+    fp8 = args.workload.endswith("_fp8")           # the workload with the e4m3 K/V projection
+    w = W.BY_NAME[args.workload[:-4] if fp8 else args.workload]
     decode = w.prefix_len > 0
     T_all = w.prefix_len + w.T
     ids_np = W.token_stream(w, T=T_all) if decode else W.token_stream(w)
@@ -515,6 +531,10 @@ def run_workload(args) -> None:
     for lid in w.layers:
         L = W.layer_inputs(w, lid, T=T_all) if decode else W.layer_inputs(w, lid)
         plan, weights, proj, H = make_layer(w, L, P, w.B * T_all)
+        if fp8:
+            import dataclasses
+            q, sc = plan.quantize_fp8(weights.w_kv)
+            weights = dataclasses.replace(weights, w_kv=None, w_kv_fp8=q, w_kv_scale=sc)
         ly = {"plan": plan, "weights": weights, "proj": proj, "ws": plan.new_workspace(w.B * T_all),
               "e": torch.empty(w.ntok, w.d_mem, dtype=plan.act_torch_dtype, device=dev)}
         if w.table_in_host:
@@ -696,10 +716,11 @@ def run_workload(args) -> None:
                         "gather_ms": round(g_ms, 5),
                         "gather_host_link_gbs": round(w.ntok * w.R * row_bytes / (g_ms / 1e3) / 1e9, 1),
                         "h2d_copy_gbs": round(h2d, 1)}
-    line = {"metric": f"Engram-layer tokens/s, {w.name} workload", "value": round(value, 1), "unit": UNIT,
+    line = {"metric": f"Engram-layer tokens/s, {args.workload} workload" + (" (e4m3 K/V projection)" if fp8 else ""),
+            "value": round(value, 1), "unit": UNIT,
             "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.act_dtype, "data": "synthetic",
+            "vs_baseline": None, "dtype": "e4m3 projection, bf16" if fp8 else w.act_dtype, "data": "synthetic",
             "config": dict(workload_desc(w), cuda_graph=True,
                            stage_a="every layer's hash+gather on a side stream, ahead of its Stage B"),
             "clocks": clocks, **extra}
@@ -714,14 +735,14 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="prefill_bf16",
-                    help="prefill_bf16 (the headline line); decode_bf16, int8_host or multibranch_n4 print "
-                         "that workload's own line")
+                    help="prefill_bf16 (the headline line); prefill_fp8 (the same with the e4m3 K/V "
+                         "projection), decode_bf16, int8_host or multibranch_n4 print that workload's own line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload != "prefill_bf16":
+    elif args.workload not in ("prefill_bf16", "prefill_fp8"):
         run_workload(args)
     else:
         run_ours(args)

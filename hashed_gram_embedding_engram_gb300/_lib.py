@@ -21,7 +21,7 @@ EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", 
            "engram_get_error", "engram_plan_set_timing", "engram_plan_set_fused_stage_b", "engram_plan_kernel_times",
            "engram_forward_static_scratch", "engram_stage_a", "engram_cache_create", "engram_cache_destroy",
            "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats",
-           "engram_cache_set_dedup")
+           "engram_cache_set_dedup", "engram_quantize_fp8")
 
 
 class Config(ctypes.Structure):
@@ -34,7 +34,7 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("table", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("w_kv", ctypes.c_void_p),
                 ("g_h", ctypes.c_void_p), ("g_k", ctypes.c_void_p), ("g_c", ctypes.c_void_p),
-                ("conv", ctypes.c_void_p)]
+                ("conv", ctypes.c_void_p), ("w_kv_fp8", ctypes.c_void_p), ("w_kv_scale", ctypes.c_void_p)]
 
 
 class State(ctypes.Structure):
@@ -68,6 +68,7 @@ def _lib() -> ctypes.CDLL:
         lib.engram_hash.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp]
         lib.engram_gather.argtypes = [vp, vp, i64, vp, vp, vp, vp]
         lib.engram_kv_projection.argtypes = [vp, vp, i64, vp, vp, vp]
+        lib.engram_quantize_fp8.argtypes = [vp, vp, i64, i32, vp, vp, vp]
         lib.engram_stage_a.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
         lib.engram_cache_create.argtypes = [vp, i64, vp, ctypes.POINTER(vp)]
         lib.engram_cache_destroy.argtypes = [vp]

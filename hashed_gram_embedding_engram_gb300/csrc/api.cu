@@ -67,10 +67,16 @@ engram_status_t check_tokens(const engram_plan* p, int B, int T) {
 
 engram_status_t check_weights(const engram_plan* p, const engram_weights_t* w, bool need_table) {
   if (!w) return ENGRAM_ERR_INVALID_ARG;
-  if (!w->w_kv || !w->g_h || !w->g_k || !w->g_c || !w->conv) return ENGRAM_ERR_INVALID_ARG;
-  if (!aligned16(w->w_kv) || !aligned16(w->g_h) || !aligned16(w->g_k) || !aligned16(w->g_c) ||
-      !aligned16(w->conv))
+  if (!w->g_h || !w->g_k || !w->g_c || !w->conv) return ENGRAM_ERR_INVALID_ARG;
+  if (!aligned16(w->g_h) || !aligned16(w->g_k) || !aligned16(w->g_c) || !aligned16(w->conv))
     return ENGRAM_ERR_INVALID_ARG;
+  if ((w->w_kv_fp8 != nullptr) != (w->w_kv_scale != nullptr)) return ENGRAM_ERR_INVALID_ARG;
+  if (w->w_kv_fp8) {
+    if (p->cfg.act_dtype != ENGRAM_BF16 || p->d_mem % 128) return ENGRAM_ERR_UNSUPPORTED;
+    if (!aligned16(w->w_kv_fp8) || !aligned16(w->w_kv_scale)) return ENGRAM_ERR_INVALID_ARG;
+  } else if (!w->w_kv || !aligned16(w->w_kv)) {
+    return ENGRAM_ERR_INVALID_ARG;
+  }
   if (need_table) {
     if (!w->table) return ENGRAM_ERR_INVALID_ARG;
     if ((p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16) != (w->scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
@@ -110,6 +116,8 @@ Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base) {
     // widest case: 32-column slices, rows padded to 16 bytes
     w.part = reinterpret_cast<float*>(take(n * (((d / 32) * (1 + 3 * M) + 3) / 4 * 4) * 4));
     w.sync = reinterpret_cast<uint32_t*>(take(engram::stage_b_sync_words(ntok) * 4));
+    w.e8 = reinterpret_cast<uint8_t*>(take(n * p->d_mem));
+    w.e_scale = reinterpret_cast<float*>(take(n * 4));
   }
   w.sa = reinterpret_cast<float*>(take(n * engram::sa_row_floats(static_cast<int>(M)) * 4));
   w.bytes = off;
@@ -311,8 +319,9 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     v = ws.kv;
     sv = static_cast<int64_t>(M + 1) * d;
   } else {
+    const bool f8 = w->w_kv_fp8 != nullptr;
     cudaError_t fe = cudaErrorNotSupported;
-    if (plan->fused_stage_b && engram::stage_b_fused_applies(plan, ntok, T)) {
+    if (!f8 && plan->fused_stage_b && engram::stage_b_fused_applies(plan, ntok, T)) {
       // projection and conv in one cooperative launch (after a one-block kernel zeroing its counters)
       fe = engram::launch_stage_b_fused(plan, e, w->w_kv, B, T, H, w->g_h, w->g_k, w->g_c, w->conv, ws.v32, ws.part,
                                         state ? ws.sa : nullptr, state, ws.sync, s);
@@ -332,9 +341,20 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
       return ENGRAM_OK;
     }
     int n_sl = 0, pstride = 0;
-    if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part, &n_sl,
-                                 &pstride, plan->num_sms, &plan->dev->err, s) != cudaSuccess)
+    if (f8) {
+      // e4m3 projection: each token's row of e quantised, then the GEMM on the codes
+      if (engram::launch_quantize_rows_e4m3(e, ntok, plan->d_mem, ws.e8, ws.e_scale, plan->num_sms, s) !=
+          cudaSuccess)
+        return ENGRAM_ERR_CUDA;
+      mark(plan, s);
+      if (engram::gemm_e4m3_engram(ws.e8, ws.e_scale, w->w_kv_fp8, w->w_kv_scale, ntok, d, M, plan->d_mem, H, w->g_h,
+                                   w->g_k, ws.v32, ws.part, &n_sl, &pstride, plan->num_sms, &plan->dev->err, s) !=
+          cudaSuccess)
+        return ENGRAM_ERR_CUDA;
+    } else if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
+                                        &n_sl, &pstride, plan->num_sms, &plan->dev->err, s) != cudaSuccess) {
       return ENGRAM_ERR_CUDA;
+    }
     mark(plan, s);
     if (T == 1) {
       // one position per sequence (decode): gate, conv, residual and state in one launch
@@ -580,6 +600,14 @@ engram_status_t engram_cache_stats(const engram_cache_t* c, engram_stream_t stre
   if (rows_over_link) *rows_over_link = (st[0] - st[1]) + st[3];
   if (cached_rows) *cached_rows = c->cached;
   return ENGRAM_OK;
+}
+
+engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, int64_t rows, int cols, uint8_t* q,
+                                    float* scale, engram_stream_t stream) {
+  if (!plan || !x || !q || !scale || rows < 0 || cols <= 0 || cols % 16) return ENGRAM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return ENGRAM_ERR_INVALID_ARG;
+  if (rows == 0) return ENGRAM_OK;
+  return cuda_status(engram::launch_quantize_rows_e4m3(x, rows, cols, q, scale, plan->num_sms, (cudaStream_t)stream));
 }
 
 engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable) {

@@ -90,6 +90,8 @@ struct Workspace {
   float* part;       // bf16 layers: gate partial sums, at most (d/32)(1+3M) per token (rows padded to 4)
   float* sa;         // [ntok, sa_row_floats(M)]: s^(1..M) = alpha/sqrt(mean(v~^2)+eps), then alpha^(1..M)
   uint32_t* sync;    // bf16 layers: stage_b_sync_words(ntok) counters of the fused Stage-B kernel
+  uint8_t* e8;       // bf16 layers: [ntok, d_mem] e4m3 codes of e (FP8 projection)
+  float* e_scale;    // bf16 layers: [ntok] their per-token scales
   size_t bytes;
 };
 Workspace carve_workspace(const engram_plan* p, int64_t ntok, void* base);
@@ -165,10 +167,24 @@ cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr,
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
                              const float* g_h, const float* g_k, float* v32, float* part, int* n_sl, int* pstride,
                              int num_sms, uint32_t* err, cudaStream_t s);
+// The same projection on e4m3 operands: e8 [Mr, Kd] and w8 [(M+1)d, Kd]
+// quantised per row with scales s_e [Mr] and s_w [(M+1)d] (quant.cu); the
+// epilogue multiplies each accumulator by its two scales.  Kd % 128 == 0.
+cudaError_t gemm_e4m3_engram(const uint8_t* e8, const float* s_e, const uint8_t* w8, const float* s_w, int64_t Mr,
+                             int d, int M, int Kd, const void* H, const float* g_h, const float* g_k, float* v32,
+                             float* part, int* n_sl, int* pstride, int num_sms, uint32_t* err, cudaStream_t s);
+// Per-row e4m3 quantisation of a bf16 [rows, cols] array (quant.cu):
+// scale[i] = amax_i / 448 and q[i, j] = e4m3_satfinite(x[i, j] * (448 / amax_i)),
+// both quotients in binary32; an all-zero row gets scale 1 and zero codes.
+cudaError_t launch_quantize_rows_e4m3(const void* x, int64_t rows, int cols, uint8_t* q, float* scale, int num_sms,
+                                      cudaStream_t s);
 // 2-D tiled TMA descriptor of a row-major [rows, inner] array (fp32 or bf16),
 // rows row_stride_bytes apart, box of box_rows x box_inner elements.
 bool make_tensor_map_2d(CUtensorMap* map, const void* base, bool is_f32, uint64_t inner, uint64_t rows,
                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+// The same for a byte array (fp8 operands).
+bool make_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 // 3-D tiled TMA descriptor of a bf16 array with dims d0 (contiguous), d1, d2 and
 // byte strides stride1, stride2 between consecutive indices of d1 and d2.
 bool make_tensor_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,

@@ -74,6 +74,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The same persistent kernel on e4m3 operands: e and W_kv quantised per row
+// (one scale per token, one per output row of W_kv), kind::f8f6f4 MMAs with
+// K = 32 per instruction at twice the bf16 rate, and the Engram epilogue on
+// the rescaled accumulators.  The fused-projection suggestion of the page's
+// section "多分支 backbone 上的变体" names FP8 for this GEMM.
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_e4m3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmH, int Mr, int Nc,
+                     int Kd, uint32_t* __restrict__ err, const EngramEpilogue epi) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GemmCtx c = gemm_ctx<BN, true, true>(smem, Mr, Nc, Kd, err);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  gemm_setup<BN, true, true>(c, warp, lane);
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+    ptx::tma_prefetch_desc(&tmV);
+    ptx::tma_prefetch_desc(&tmH);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  c.tmem = c.bars->tmem_base;
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+
+  if (warp == 0) {
+    if (lane == 0) gemm_producer<BN, true, true>(c, &tmA, &tmB);
+  } else if (warp == 1) {
+    if (lane == 0) gemm_mma<BN, true, true>(c);
+  } else {
+    gemm_epilogue<BN, true, false, true>(c, epi, &tmV, &tmH, nullptr, warp, lane, nullptr);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(c.tmem, Cfg<BN, true, true>::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 // Row-major bf16 [rows, cols] -> 2D map with a box of box_rows x 64 elements, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int cols, int box_rows) {
@@ -114,6 +159,35 @@ cudaError_t run(const void* A, const void* B, void* C, int64_t Mr, int Nc, int K
   }
   return launch_pdl(gemm_bf16_kernel<BN, kFused>, dim3(grid), dim3(kThreads), G::kSmem, s, ta, tb, tv, th,
                     static_cast<__nv_bfloat16*>(C), static_cast<int>(Mr), Nc, Kd, err, epi);
+}
+
+template <int BN>
+cudaError_t run_e4m3(const uint8_t* A, const uint8_t* B, int64_t Mr, int Nc, int Kd, int num_sms, uint32_t* err,
+                     EngramEpilogue epi, cudaStream_t s) {
+  using G = Cfg<BN, true, true>;
+  CUtensorMap ta, tb, tv, th;
+  if (!make_tensor_map_2d_u8(&ta, A, static_cast<uint64_t>(Kd), static_cast<uint64_t>(Mr), static_cast<uint64_t>(Kd),
+                             128, kBM, true) ||
+      !make_tensor_map_2d_u8(&tb, B, static_cast<uint64_t>(Kd), static_cast<uint64_t>(Nc), static_cast<uint64_t>(Kd),
+                             128, BN, true) ||
+      !make_tensor_map_2d(&tv, epi.v32, true, static_cast<uint64_t>(epi.d), static_cast<uint64_t>(Mr),
+                          static_cast<uint64_t>(epi.d) * 4, 32, 32, true) ||
+      !make_tensor_map_3d_bf16(&th, epi.H, static_cast<uint64_t>(epi.d), static_cast<uint64_t>(epi.M),
+                               static_cast<uint64_t>(Mr), static_cast<uint64_t>(epi.d) * 2,
+                               static_cast<uint64_t>(epi.d) * epi.M * 2, 64, 1, 32, true))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;   // per template instance; idempotent if raced
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_e4m3_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t tiles = ((Mr + kBM - 1) / kBM) * ((Nc + BN - 1) / BN);
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  epi.n_sl = epi.d / (BN / 2);
+  epi.pstride = (epi.n_sl * (1 + 3 * epi.M) + 3) / 4 * 4;
+  return launch_pdl(gemm_e4m3_kernel<BN>, dim3(grid), dim3(kThreads), G::kSmem, s, ta, tb, tv, th,
+                    static_cast<int>(Mr), Nc, Kd, err, epi);
 }
 
 // Widest N tile (256, 128, 64) that divides `div` and still gives every SM a tile.
@@ -187,7 +261,7 @@ cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d,
                              int num_sms, uint32_t* err, cudaStream_t s) {
   const int Nc = (M + 1) * d;
   if (d % 64 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
-  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0, 0};
+  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0, 0, nullptr, nullptr};
   const int bn = pick_bn(Mr, Nc, d, num_sms);
   *n_sl = d / (bn / 2);
   *pstride = (*n_sl * (1 + 3 * M) + 3) / 4 * 4;
@@ -195,6 +269,22 @@ cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d,
     case 256: return run<256, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
     case 128: return run<128, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
     default: return run<64, true>(e, w_kv, nullptr, Mr, Nc, Kd, num_sms, err, epi, s);
+  }
+}
+
+cudaError_t gemm_e4m3_engram(const uint8_t* e8, const float* s_e, const uint8_t* w8, const float* s_w, int64_t Mr,
+                             int d, int M, int Kd, const void* H, const float* g_h, const float* g_k, float* v32,
+                             float* part, int* n_sl, int* pstride, int num_sms, uint32_t* err, cudaStream_t s) {
+  const int Nc = (M + 1) * d;
+  if (d % 64 || Kd % 128 || Mr <= 0) return cudaErrorInvalidValue;
+  EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0, 0, s_e, s_w};
+  const int bn = pick_bn(Mr, Nc, d, num_sms);
+  *n_sl = d / (bn / 2);
+  *pstride = (*n_sl * (1 + 3 * M) + 3) / 4 * 4;
+  switch (bn) {
+    case 256: return run_e4m3<256>(e8, w8, Mr, Nc, Kd, num_sms, err, epi, s);
+    case 128: return run_e4m3<128>(e8, w8, Mr, Nc, Kd, num_sms, err, epi, s);
+    default: return run_e4m3<64>(e8, w8, Mr, Nc, Kd, num_sms, err, epi, s);
   }
 }
 

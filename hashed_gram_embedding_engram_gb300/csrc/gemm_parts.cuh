@@ -16,23 +16,26 @@ namespace engram {
 namespace gk {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;                        // one 128-byte swizzle atom of bf16
+constexpr int kBK = 64;                        // bf16 elements per k-block: one 128-byte swizzle atom
 constexpr int kThreads = 320;                 // producer, MMA, 8 epilogue warps
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s: a healthy stage turns over in < 1 us
 
 constexpr int kEpiWarpBytes = 8192;            // fused epilogue: per-warp staging of v chunks / the H slice
 
-template <int BN, bool kFused>
+// kF8: e4m3 operands (128 elements per 128-byte k-block, kind::f8f6f4) with
+// per-row scales applied in the epilogue; else bf16 (64 per k-block, kind::f16).
+template <int BN, bool kFused, bool kF8 = false>
 struct Cfg {
   static constexpr int kStages = kFused ? (BN == 256 ? 3 : (BN == 128 ? 4 : 6)) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBKe = kF8 ? 128 : kBK;  // elements per k-block
+  static constexpr int kABytes = kBM * 128;
+  static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiBytes = kFused ? 8 * kEpiWarpBytes : 0;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
-  static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN);
+  static constexpr uint32_t kIdesc = kF8 ? ptx::idesc_e4m3_f32(kBM, BN) : ptx::idesc_bf16_f32(kBM, BN);
   static constexpr int kHBoxes = BN / 2 > 64 ? BN / 128 : 1;   // 64-column H boxes per warp slice
 };
 
@@ -46,6 +49,8 @@ struct EngramEpilogue {
   int M;
   int n_sl;                       // d / (BN / 2): column slices per row of v
   int pstride;                    // floats per row of part: n_sl * (1 + 3M) rounded up to 4
+  const float* s_row;             // e4m3 operands: [Mr] scale of each row of e
+  const float* s_col;             // e4m3 operands: [(M+1)d] scale of each row of W_kv
 };
 
 struct Bars {
@@ -95,10 +100,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 // row r at r*128 + 16*(j ^ (r % 8)), conflict-free for row-per-lane access):
 // v chunks of 32 x 32 fp32 leave by TMA tensor stores, and the warp's H slice
 // (32 rows x BN/2 columns) arrives by TMA while the tile's MMAs run.
-template <int BN>
+// e4m3 operands (kF8): the accumulator of row t, column n is the dot product
+// of the quantised codes; each is first multiplied by s_row[t] * s_col[n].
+template <bool kF8>
+__device__ __forceinline__ void dequant_chunk(const EngramEpilogue& epi, float srow, int n, uint32_t (&r)[32]) {
+  if constexpr (kF8) {
+    const float4* sc = reinterpret_cast<const float4*>(epi.s_col + n);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 c4 = __ldg(sc + q);
+      r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) * (srow * c4.x));
+      r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) * (srow * c4.y));
+      r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) * (srow * c4.z));
+      r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) * (srow * c4.w));
+    }
+  }
+}
+
+template <int BN, bool kF8 = false>
 __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const CUtensorMap* tmV, uint8_t* eb,
                                                uint32_t t_row, int row, int row0, int Mr, int n0, int c_lo, int lane) {
   constexpr int SW = BN / 2;
+  const float srow = kF8 && row < Mr ? __ldg(epi.s_row + row) : 0.f;
   constexpr int kChunks = SW / 32;          // 1, 2 or 4
   const int d = epi.d;
   const int P = epi.pstride;
@@ -112,6 +135,7 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
+      dequant_chunk<kF8>(epi, srow, n0 + c, r);
       float sv = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) sv = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), sv);
@@ -150,6 +174,7 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
+      dequant_chunk<kF8>(epi, srow, n0 + c, r);
       float dot = 0.f, sk = 0.f, sh = 0.f;
       const uint8_t* hb = eb + (ci >> 1) * 4096 + lane * 128;     // this row of the chunk's 64-column box
       const float4* gh4 = reinterpret_cast<const float4*>(gh + c);
@@ -204,10 +229,10 @@ struct GemmCtx {
 };
 
 // `bars`: where the barrier block lives; null = right after the epilogue staging.
-template <int BN, bool kFused>
+template <int BN, bool kFused, bool kF8 = false>
 __device__ __forceinline__ GemmCtx gemm_ctx(uint8_t* smem, int Mr, int Nc, int Kd, uint32_t* err,
                                             Bars* bars = nullptr) {
-  using G = Cfg<BN, kFused>;
+  using G = Cfg<BN, kFused, kF8>;
   GemmCtx c;
   c.smem = smem;
   c.epi_smem = smem + G::kStages * G::kStageBytes;
@@ -216,7 +241,7 @@ __device__ __forceinline__ GemmCtx gemm_ctx(uint8_t* smem, int Mr, int Nc, int K
   c.m_tiles = (Mr + kBM - 1) / kBM;
   c.n_tiles = (Nc + BN - 1) / BN;
   c.num_tiles = c.m_tiles * c.n_tiles;
-  c.k_blocks = (Kd + kBK - 1) / kBK;
+  c.k_blocks = (Kd + G::kBKe - 1) / G::kBKe;
   c.Mr = Mr;
   c.Nc = Nc;
   c.Kd = Kd;
@@ -227,9 +252,9 @@ __device__ __forceinline__ GemmCtx gemm_ctx(uint8_t* smem, int Mr, int Nc, int K
 // Barrier initialisation (thread 0) and TMEM allocation (warp 1); the caller
 // then synchronises the block with tcgen05 fences around the barrier and
 // reads the TMEM base from bars->tmem_base.
-template <int BN, bool kFused>
+template <int BN, bool kFused, bool kF8 = false>
 __device__ __forceinline__ void gemm_setup(const GemmCtx& c, int warp, int lane) {
-  using G = Cfg<BN, kFused>;
+  using G = Cfg<BN, kFused, kF8>;
   Bars* bars = c.bars;
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kStages; ++s) {
@@ -253,9 +278,9 @@ __device__ __forceinline__ void gemm_setup(const GemmCtx& c, int warp, int lane)
 }
 
 // Warp 0, lane 0.
-template <int BN, bool kFused>
+template <int BN, bool kFused, bool kF8 = false>
 __device__ __forceinline__ void gemm_producer(const GemmCtx& c, const CUtensorMap* tmA, const CUtensorMap* tmB) {
-  using G = Cfg<BN, kFused>;
+  using G = Cfg<BN, kFused, kF8>;
   Bars* bars = c.bars;
   uint8_t* smem = c.smem;
   uint32_t* err = c.err;
@@ -275,8 +300,8 @@ __device__ __forceinline__ void gemm_producer(const GemmCtx& c, const CUtensorMa
       }
       uint8_t* sa = smem + stage * G::kStageBytes;
       ptx::mbar_arrive_expect_tx(&bars->full[stage], G::kStageBytes);
-      ptx::tma_load_2d_nohint(sa, tmA, &bars->full[stage], kb * kBK, m0);
-      ptx::tma_load_2d(sa + G::kABytes, tmB, &bars->full[stage], kb * kBK, n0, keep);
+      ptx::tma_load_2d_nohint(sa, tmA, &bars->full[stage], kb * G::kBKe, m0);
+      ptx::tma_load_2d(sa + G::kABytes, tmB, &bars->full[stage], kb * G::kBKe, n0, keep);
       armed |= 1u << stage;
       armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == G::kStages) {
@@ -291,9 +316,9 @@ __device__ __forceinline__ void gemm_producer(const GemmCtx& c, const CUtensorMa
 }
 
 // Warp 1, lane 0.
-template <int BN, bool kFused>
+template <int BN, bool kFused, bool kF8 = false>
 __device__ __forceinline__ void gemm_mma(const GemmCtx& c) {
-  using G = Cfg<BN, kFused>;
+  using G = Cfg<BN, kFused, kF8>;
   Bars* bars = c.bars;
   uint8_t* smem = c.smem;
   uint32_t* err = c.err;
@@ -317,9 +342,13 @@ __device__ __forceinline__ void gemm_mma(const GemmCtx& c) {
       const uint32_t a_addr = ptx::smem_u32(smem + stage * G::kStageBytes);
       const uint32_t b_addr = a_addr + G::kABytes;
 #pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + k * 32), ptx::sdesc_kmajor_sw128(b_addr + k * 32),
-                      G::kIdesc, (kb | k) != 0);
+      for (int k = 0; k < 4; ++k) {            // 32 bytes of K per instruction: 16 bf16 or 32 e4m3
+        if constexpr (kF8)
+          ptx::mma_e4m3(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + k * 32), ptx::sdesc_kmajor_sw128(b_addr + k * 32),
+                        G::kIdesc, (kb | k) != 0);
+        else
+          ptx::mma_bf16(d_tmem, ptx::sdesc_kmajor_sw128(a_addr + k * 32), ptx::sdesc_kmajor_sw128(b_addr + k * 32),
+                        G::kIdesc, (kb | k) != 0);
       }
       ptx::mma_commit(&bars->empty[stage]);
       if (++stage == G::kStages) {
@@ -341,11 +370,12 @@ __device__ __forceinline__ void gemm_mma(const GemmCtx& c) {
 // visible device-wide (its TMA stores completed, proxy and memory fences) and
 // the warp adds one to row_done[tile's row block] with release semantics, so
 // a row block is complete once its counter reaches 8 x (column tiles).
-template <int BN, bool kFused, bool kSignal>
+template <int BN, bool kFused, bool kSignal, bool kF8 = false>
 __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpilogue& epi, const CUtensorMap* tmV_,
                                               const CUtensorMap* tmH_, __nv_bfloat16* C, int warp, int lane,
                                               uint32_t* row_done) {
-  using G = Cfg<BN, kFused>;
+  static_assert(kFused || !kF8, "e4m3 operands only with the Engram epilogue");
+  using G = Cfg<BN, kFused, kF8>;
   Bars* bars = c.bars;
   uint8_t* epi_smem = c.epi_smem;
   uint32_t* err = c.err;
@@ -408,7 +438,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpil
         }
       }
     } else {
-      fused_epilogue<BN>(epi, &tmV, eb, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
+      fused_epilogue<BN, kF8>(epi, &tmV, eb, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
     }
     ptx::tc_fence_before();
     __syncwarp();

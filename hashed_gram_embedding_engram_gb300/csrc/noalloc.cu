@@ -16,7 +16,7 @@
 
 namespace {
 
-// 32 MiB: the scratch of up to about 4900 tokens of a layer with d = 1024 and
+// 32 MiB: the scratch of up to about 4300 tokens of a layer with d = 1024 and
 // d_mem = 1024 (the prefill batch of 4096 tokens needs 26.6 MB).
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
 constexpr int kMaxDevices = 64;

@@ -300,7 +300,8 @@ cudaError_t launch_stage_b_fused(const engram_plan* p, const void* e, const void
   const int64_t ntok = static_cast<int64_t>(B) * T;
   const int d = p->cfg.d, Kd = p->d_mem, Nc = 2 * d;
   const int Mr = static_cast<int>(ntok);
-  gk::EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, 1, d / (kSbBN / 2), 0};
+  gk::EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, 1, d / (kSbBN / 2), 0,
+                         nullptr, nullptr};
   epi.pstride = (epi.n_sl * 4 + 3) / 4 * 4;
   if (epi.n_sl != 8 || epi.pstride != 32) return cudaErrorInvalidValue;
   CUtensorMap ta, tb, tv, th;

@@ -59,6 +59,10 @@ class EngramWeights:
     g_c: torch.Tensor              # float32 [d]
     conv: torch.Tensor             # float32 [d, w]
     scales: Optional[torch.Tensor] = None   # float16 [sum primes] for int8 tables
+    # FP8 projection: W_kv as e4m3 codes [(M+1)d, d_mem] (uint8) with float32
+    # row scales [(M+1)d], from EngramPlan.quantize_fp8(w_kv); w_kv is then unused
+    w_kv_fp8: Optional[torch.Tensor] = None
+    w_kv_scale: Optional[torch.Tensor] = None
 
     def struct(self, plan: "EngramPlan", need_table: bool = True) -> _lib.Weights:
         c = plan
@@ -73,7 +77,11 @@ class EngramWeights:
                 if self.scales is None:
                     raise ValueError("int8 tables need fp16 row scales")
                 w.scales = _dev_or_pinned(self.scales, "scales", torch.float16)
-        w.w_kv = _dev(self.w_kv, "w_kv", adt, ((c.M + 1) * c.d, c.d_mem))
+        if self.w_kv_fp8 is not None:
+            w.w_kv_fp8 = _dev(self.w_kv_fp8, "w_kv_fp8", torch.uint8, ((c.M + 1) * c.d, c.d_mem))
+            w.w_kv_scale = _dev(self.w_kv_scale, "w_kv_scale", torch.float32, ((c.M + 1) * c.d,))
+        if self.w_kv is not None:
+            w.w_kv = _dev(self.w_kv, "w_kv", adt, ((c.M + 1) * c.d, c.d_mem))
         w.g_h = _dev(self.g_h, "g_h", torch.float32, (c.M, c.d))
         w.g_k = _dev(self.g_k, "g_k", torch.float32, (c.M, c.d))
         w.g_c = _dev(self.g_c, "g_c", torch.float32, (c.d,))
@@ -204,6 +212,18 @@ class EngramPlan:
                                             _dev(out, "e_out", self.act_torch_dtype, (B * T, self.d_mem)),
                                             _stream()), "engram_stage_a")
         return out
+
+    def quantize_fp8(self, x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+        """Per-row e4m3 codes (uint8, same shape) and float32 scales of a bf16
+        [rows, cols] device tensor (engram_quantize_fp8)."""
+        if x.dim() != 2:
+            raise ValueError("x: expected a 2-D tensor")
+        rows, cols = x.shape
+        q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+        sc = torch.empty(rows, dtype=torch.float32, device=x.device)
+        _lib.check(self._lib.engram_quantize_fp8(self._h, _dev(x, "x", torch.bfloat16), rows, cols, _dev(q, "q"),
+                                                 _dev(sc, "scale"), _stream()), "engram_quantize_fp8")
+        return q, sc
 
     def kv_projection(self, e: torch.Tensor, w_kv: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Step 5: e [ntok, d_mem] -> kv [ntok, (M+1)d] = e . w_kv^T."""

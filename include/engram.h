@@ -105,6 +105,12 @@ typedef struct {
   const float* g_k;             /* [M, d] RMSNorm weight on k, per branch */
   const float* g_c;             /* [d]    RMSNorm weight on v~ before the conv (shared) */
   const float* conv;            /* [d, conv_w] depthwise taps (shared by branches) */
+  /* FP8 projection (BF16 layers, d_mem a multiple of 128), or both NULL.  With
+   * them, Step 5 runs on e4m3 operands: W_kv as quantised by
+   * engram_quantize_fp8 (one scale per output row), e quantised per token by
+   * the call itself; w_kv is then not read and may be NULL. */
+  const uint8_t* w_kv_fp8;      /* e4m3 [(M+1)*d, d_mem] */
+  const float* w_kv_scale;      /* [(M+1)*d] */
 } engram_weights_t;
 
 /* Streaming state of B sequences (decode, chunked prefill).  Owned by the
@@ -210,7 +216,7 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
  * that loads the library holds it until the process exits, and this call
  * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call).
  * Limit: engram_plan_workspace_bytes(plan, B*T) must not exceed 32 MiB (about
- * 4900 tokens of a d = 1024, d_mem = 1024 layer); larger calls return
+ * 4300 tokens of a d = 1024, d_mem = 1024 layer); larger calls return
  * ENGRAM_ERR_WORKSPACE before any launch.  The current device must be the
  * plan's.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
@@ -290,6 +296,19 @@ engram_status_t engram_stage_a_cached(const engram_cache_t* cache, const int32_t
 engram_status_t engram_cache_stats(const engram_cache_t* cache, engram_stream_t stream, int reset,
                                    uint64_t* rows_looked_up, uint64_t* rows_from_hbm, uint64_t* rows_over_link,
                                    int64_t* cached_rows);
+
+/* Per-row e4m3 quantisation of a bf16 array x [rows, cols] (device, 16-byte
+ * aligned, cols a multiple of 16), for the FP8 projection that "DeepSeek
+ * Engram 系列导读" (section "多分支 backbone 上的变体") suggests for the fused
+ * [W_V; W_K^(1..M)] GEMM; the page fixes no scaling.  For every row i:
+ *   scale[i] = amax_i / 448,  q[i, j] = e4m3(x[i, j] * (448 / amax_i))
+ * (448: the largest finite e4m3 value; both quotients IEEE binary32; the
+ * conversion rounds to nearest even and saturates to +-448); an all-zero row
+ * gets scale 1 and zero codes.  q: device uint8 [rows, cols]; scale: device
+ * float [rows].  Used once per layer for W_kv (rows = (M+1)*d, cols = d_mem);
+ * the forward applies the same rule to each token's row of e. */
+engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, int64_t rows, int cols, uint8_t* q,
+                                    float* scale, engram_stream_t stream);
 
 /* Stage B of BF16 layers with one branch, conv_w = 4 and d = 1024 (eight
  * 128-column slices per projection quantity), for chunks of T > 1 positions,

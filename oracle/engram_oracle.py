@@ -34,7 +34,14 @@ notes of the repository):
   * Conv1D is depthwise, causal, without bias, zero before the sequence start,
     PyTorch weight layout: tap j multiplies the input at lag (w-1-j)*dilation;
   * multi-branch: per-branch RMSNorm weights in the gate, shared W_V, conv
-    weights and conv RMSNorm; branch m gets H^(m) += Y^(m).
+    weights and conv RMSNorm; branch m gets H^(m) += Y^(m);
+  * FP8 projection (the section "多分支 backbone 上的变体" suggests one FP8 GEMM
+    for [W_V; W_K^(1..M)] and says nothing more): e4m3 operands, one scale
+    per row of e (per token) and per row of W_kv, s = amax/448, codes
+    e4m3(x * (448/amax)) rounded to nearest even and saturated to +-448, the
+    quotients and the product in binary32 (the codes are then a function of
+    the stored inputs alone); the dot products of the codes are exact, the
+    rest float64.
 """
 from __future__ import annotations
 
@@ -156,6 +163,53 @@ def kv_projection(e: np.ndarray, W_V: np.ndarray, W_K: Sequence[np.ndarray]):
     return k, v
 
 
+# --------------------------------------------------------------------------- #
+# FP8 (e4m3) projection
+# --------------------------------------------------------------------------- #
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Nearest e4m3 value (ties to even), saturating to +-448.
+
+    e4m3 (OCP 8-bit floating point, E4M3): sign, 4 exponent bits with bias 7,
+    3 mantissa bits.  Normal values 2^(E-7) (1 + m/8), E = 1..15, except
+    E = 15, m = 7 (NaN), so the largest finite value is 2^8 * 1.75 = 448;
+    subnormals 2^-6 (m/8) = m * 2^-9.  On [2^k, 2^(k+1)) with k >= -6 the
+    grid step is 2^(k-3); below 2^-6 it is 2^-9."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(a)                       # a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    step = np.where(a >= 2.0 ** -6, np.ldexp(1.0, ex - 1 - 3), 2.0 ** -9)
+    q = np.minimum(np.round(a / step) * step, E4M3_MAX)    # np.round: half to even
+    return np.copysign(q, x)
+
+
+def quantize_rows_e4m3(x: np.ndarray):
+    """Per-row e4m3 quantisation: (codes as float64 values, scales).
+
+    s = amax/448 and q = e4m3(x * (448/amax)), both quotients and the product
+    in binary32; an all-zero row gets s = 1 and zero codes."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1)).astype(np.float32)
+    inv = np.where(nz, np.float32(E4M3_MAX) / safe, np.float32(0)).astype(np.float32)
+    s = np.where(nz, safe / np.float32(E4M3_MAX), np.float32(1)).astype(np.float32)
+    y = (x32 * inv[..., None]).astype(np.float32)
+    return e4m3_round(y.astype(np.float64)), s.astype(np.float64)
+
+
+def kv_projection_fp8(e: np.ndarray, W: np.ndarray, d: int, M: int):
+    """Step 5 with e4m3 operands: kv = s_e s_w (q_e . q_w), then split into v and k^(1..M)."""
+    qe, se = quantize_rows_e4m3(e)
+    qw, sw = quantize_rows_e4m3(W)
+    kv = (qe @ qw.T) * se[..., None] * sw
+    v = kv[..., :d]
+    k = np.stack([kv[..., (1 + m) * d:(2 + m) * d] for m in range(M)], axis=-2)
+    return k, v
+
+
 def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     """x / sqrt(mean(x^2) + eps), times the weight g, over the last axis."""
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * g
@@ -213,7 +267,8 @@ def stage_a(ids, P, mults, primes, N, K, tables, table_kind, scales=None, prev=N
 
 
 def forward(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps: float,
-            table_kind: str, act_kind: str, state: Optional[Dict] = None) -> Dict[str, np.ndarray]:
+            table_kind: str, act_kind: str, state: Optional[Dict] = None,
+            projection: str = "exact") -> Dict[str, np.ndarray]:
     """One Engram layer over a batch of sequences, Steps 1-8.
 
     ``L`` carries the layer's inputs (multipliers, primes, tables, scales, W_kv,
@@ -221,7 +276,8 @@ def forward(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps: fl
     already saw tokens: {'prev': [B, N-1] projected ids (oldest first),
     'vt_hist': [B, (w-1)*dil, M, d] float64 gated values (oldest first)}.
     Returns H_new (float64 [B,T,M,d]) with the intermediates and the state
-    after the last position."""
+    after the last position.  projection="fp8": Step 5 on e4m3 operands
+    (kv_projection_fp8)."""
     B, T = ids.shape
     d = L.g_c.shape[0]
     M = L.g_h.shape[0]
@@ -232,7 +288,10 @@ def forward(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps: fl
     W = widen(L.W_kv, act_kind)
     W_V = W[:d]
     W_K = [W[(1 + m) * d:(2 + m) * d] for m in range(M)]
-    k, v = kv_projection(e, W_V, W_K)                     # k [B,T,M,d], v [B,T,d]
+    if projection == "fp8":
+        k, v = kv_projection_fp8(e, W, d, M)
+    else:
+        k, v = kv_projection(e, W_V, W_K)                 # k [B,T,M,d], v [B,T,d]
     H = widen(L.H, act_kind)                              # [B,T,M,d]
     alpha = gate(H, k, L.g_h, L.g_k, eps)                 # [B,T,M]
     w = L.conv.shape[1]
@@ -253,7 +312,7 @@ def forward(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps: fl
 
 
 def forward_at(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps: float,
-               table_kind: str, act_kind: str, positions: Sequence) -> np.ndarray:
+               table_kind: str, act_kind: str, positions: Sequence, projection: str = "exact") -> np.ndarray:
     """Windowed re-evaluation: H_new at selected (b, t) from local inputs only.
 
     For each requested (b, t) this touches only the raw tokens x_{t'-i} of the
@@ -284,7 +343,10 @@ def forward_at(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps:
                         h ^= np.uint64(x) * multiplier(L.multipliers, K, n, k, s)
                     zrows[i, (n - 2) * K + k] = int(h % np.uint64(L.primes[(n - 2) * K + k]))
     e = gather_concat(zrows, tabs, table_kind, scs)                    # [n_need, d_mem]
-    k, v = kv_projection(e, W_V, W_K)                                  # [n_need, M, d], [n_need, d]
+    if projection == "fp8":
+        k, v = kv_projection_fp8(e, W, d, M)
+    else:
+        k, v = kv_projection(e, W_V, W_K)                              # [n_need, M, d], [n_need, d]
     Hn = np.stack([widen(L.H[b, tp], act_kind) for (b, tp) in need])   # [n_need, M, d]
     alpha = gate(Hn, k, L.g_h, L.g_k, eps)                             # [n_need, M]
     vt = alpha[..., None] * v[:, None, :]                              # [n_need, M, d]
