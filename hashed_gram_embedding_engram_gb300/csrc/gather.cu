@@ -16,9 +16,9 @@
 // engram_forward (indices computed from the token ids for the rows about to
 // be read, Steps 1-3 -- the arithmetic of hashing.cuh -- so they never
 // travel through HBM).  There the warp first loads the token's n-gram window
-// (lane i holds x'_{t-i}) and broadcasts it by shuffle; each lane computes the
-// index of its chunk's row from the per-row constants of the parameter block
-// (the lanes of one row compute the same index in the same instructions).
+// (lane i holds x'_{t-i}) and broadcasts it by shuffle; lane r computes the
+// index of row r once, and the lanes reading that row's chunks get its
+// address by shuffle.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -71,33 +71,71 @@ struct RowCache {
   unsigned long long* stats;         // [2]: rows looked up, rows served from HBM
 };
 
-template <int kCpr, bool kInt8, bool kHash, bool kCache = false>
+// Per-lane table constants of one of the R rows a token reads: the lanes of a
+// warp own rows lane and lane + 32 (R <= 64).
+struct RowConst {
+  uint32_t prime;
+  uint64_t mu;
+  int64_t offset;
+  const uint64_t* mult;                // m_{n,k,0..n-1}
+  int n;
+};
+
+__device__ __forceinline__ RowConst row_const(const PlanDev* __restrict__ pdg, int K, int r) {
+  RowConst c;
+  c.prime = __ldg(&pdg->primes[r]);
+  c.mu = __ldg(&pdg->mu[r]);
+  c.offset = __ldg(&pdg->offsets[r]);
+  c.n = 2 + r / K;
+  c.mult = pdg->mults + __ldg(&pdg->mult_base[c.n]) + (r - (c.n - 2) * K) * c.n;
+  return c;
+}
+
+__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), src);
+  const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), src);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// One warp per token.  Row phase: lane r (and r + 32) owns row r of the
+// token -- its index (computed from the n-gram window, or read), its source
+// address (table, or the HBM cache) and its int8 scale -- so each row's index
+// is computed once.  Chunk phase: lane l takes the token's 16-byte chunks
+// l, l + 32, ... (chunk f = r * kCpr + c is also the output's slot f), gets
+// its row's address by shuffle and keeps kWarpItems independent loads in
+// flight before storing; consecutive lanes read consecutive chunks of a row
+// and write contiguous output.  The per-row constants come from the device
+// copy of the parameter block, read before the dependency wait (they are
+// written at plan creation only).
+// kWide: R > 32, two rows per lane.
+template <int kCpr, bool kInt8, bool kHash, bool kCache = false, bool kWide = false>
 __global__ void __launch_bounds__(kThreads, 8)
-    row_gather_kernel(const __grid_constant__ PlanDev pd, uint32_t* __restrict__ err,
+    row_gather_kernel(const PlanDev* __restrict__ pdg, int R, int N, int K, uint32_t* __restrict__ err,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ ids, int T,
                       const int32_t* __restrict__ proj, int V, const int32_t* __restrict__ prev, int64_t ntok,
                       const uint8_t* __restrict__ table, const __half* __restrict__ scales,
                       uint4* __restrict__ out, const RowCache cache) {
-  // The per-row constants are read from the parameter block itself (constant
-  // bank): no shared memory, so blocks start at once and fit beside the K/V
-  // GEMM's blocks on an SM (Stage A of a later layer prefetched on a side stream).
-  const int R = pd.R, N = pd.N, K = pd.K;
+  constexpr int kRowBytes = kCpr * 16;
+  const int lane = threadIdx.x & 31;
+  constexpr int kRows = kWide ? 2 : 1;
+  const bool has0 = lane < R, has1 = kWide && lane + 32 < R;
+  RowConst rc[kRows];
+  if (has0) rc[0] = row_const(pdg, K, lane);
+  if (kWide && has1) rc[kRows - 1] = row_const(pdg, K, lane + 32);
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
 
-  constexpr int kRowBytes = kCpr * 16;
-  const int lane = threadIdx.x & 31;
   const int per_tok = R * kCpr;
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   bool bad = false;
-  uint32_t n_look = 0, n_hit = 0;                       // rows of this lane's chunks 0 (kCache)
+  uint32_t n_look = 0, n_hit = 0;                       // this lane's rows (kCache)
   for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
        tok += n_warps) {
-    uint64_t xp[kMaxN];
+    uint32_t xp[kMaxN];                                // projected ids: non-negative int32
     if constexpr (kHash) {
       const int b = static_cast<int>(tok / T);
       const int t = static_cast<int>(tok - static_cast<int64_t>(b) * T);
-      int64_t x = 0;                                   // lane i: x'_{t-i}, pad 0 before the start
+      int32_t x = 0;                                   // lane i: x'_{t-i}, pad 0 before the start
       if (lane < N) {
         const int tt = t - lane;
         if (tt >= 0) {
@@ -112,52 +150,69 @@ __global__ void __launch_bounds__(kThreads, 8)
         }
       }
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) xp[i] = static_cast<uint64_t>(__shfl_sync(0xFFFFFFFFu, x, i));
+      for (int i = 0; i < kMaxN; ++i)
+        if (i < N) xp[i] = static_cast<uint32_t>(__shfl_sync(0xFFFFFFFFu, x, i));
     }
+    // ---- row phase: index, source and scale of rows lane and lane + 32
+    uint64_t src[kRows] = {};                          // 0: the row is out of range (zero output)
+    float sc[kRows] = {};
+#pragma unroll
+    for (int h = 0; h < kRows; ++h) {
+      const bool has = h == 0 ? has0 : has1;
+      if (!has) continue;
+      const RowConst& c = rc[h];
+      const int r = lane + 32 * h;
+      uint32_t z;
+      if constexpr (kHash) {
+        uint64_t hsh = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxN; ++i)
+          if (i < c.n) hsh ^= static_cast<uint64_t>(xp[i]) * __ldg(c.mult + i);
+        z = barrett_mod(hsh, c.prime, c.mu);
+      } else {
+        z = static_cast<uint32_t>(__ldg(idx + tok * R + r));
+        if (z >= c.prime) {
+          bad = true;
+          continue;
+        }
+      }
+      const int64_t row = c.offset + z;
+      const uint8_t* p = table + row * kRowBytes;
+      if constexpr (kCache) {
+        const int32_t sl = __ldg(cache.slot + row);
+        if (sl >= 0) p = cache.rows + static_cast<int64_t>(sl) * kRowBytes;
+        ++n_look;
+        n_hit += sl >= 0;
+      }
+      src[h] = reinterpret_cast<uint64_t>(p);
+      if constexpr (kInt8) sc[h] = __half2float(scales[row]);
+    }
+    // ---- chunk phase
     uint4* dst = out + (kInt8 ? 2 : 1) * tok * per_tok;
     for (int f0 = 0; f0 < per_tok; f0 += 32 * kWarpItems) {
       uint4 v[kWarpItems];
-      float sc[kWarpItems];
+      float s_[kWarpItems];
       bool ok[kWarpItems];
 #pragma unroll
       for (int j = 0; j < kWarpItems; ++j) {
         const int f = f0 + j * 32 + lane;
-        ok[j] = false;
-        v[j] = make_uint4(0, 0, 0, 0);
-        sc[j] = 0.f;
-        if (f < per_tok) {
-          const int r = f / kCpr;
-          const int c = f % kCpr;
-          uint32_t z;
-          const int n = 2 + r / K;
-          if constexpr (kHash) {
-            const uint64_t* m = pd.mults + pd.mult_base[n] + (r - (n - 2) * K) * n;
-            uint64_t h = 0;
-#pragma unroll
-            for (int i = 0; i < kMaxN; ++i)
-              if (i < n) h ^= xp[i] * m[i];
-            z = barrett_mod(h, pd.primes[r], pd.mu[r]);
-          } else {
-            z = static_cast<uint32_t>(__ldg(idx + tok * R + r));
-          }
-          if (z < pd.primes[r]) {
-            const int64_t row = pd.offsets[r] + z;
-            const uint8_t* src = table + row * kRowBytes;
-            if constexpr (kCache) {
-              const int32_t sl = __ldg(cache.slot + row);
-              if (sl >= 0) src = cache.rows + static_cast<int64_t>(sl) * kRowBytes;
-              if (c == 0) {
-                ++n_look;
-                n_hit += sl >= 0;
-              }
-            }
-            v[j] = ld_stream_16(src + c * 16);
-            if constexpr (kInt8) sc[j] = __half2float(scales[row]);
-            ok[j] = true;
-          } else {
-            bad = true;
+        const int r = f / kCpr;
+        const int c = f % kCpr;
+        // every lane takes part in the shuffles; lanes past the token's chunks discard theirs
+        const int rs = r < R ? r : 0;
+        uint64_t sp = shfl64(src[0], rs & 31);
+        float sj = kInt8 ? __shfl_sync(0xFFFFFFFFu, sc[0], rs & 31) : 0.f;
+        if constexpr (kWide) {
+          const uint64_t sp1 = shfl64(src[kRows - 1], rs & 31);
+          const float sj1 = kInt8 ? __shfl_sync(0xFFFFFFFFu, sc[kRows - 1], rs & 31) : 0.f;
+          if (rs >= 32) {
+            sp = sp1;
+            sj = sj1;
           }
         }
+        ok[j] = f < per_tok && sp != 0;
+        v[j] = ok[j] ? ld_stream_16(reinterpret_cast<const uint8_t*>(sp) + c * 16) : make_uint4(0, 0, 0, 0);
+        s_[j] = sj;
       }
 #pragma unroll
       for (int j = 0; j < kWarpItems; ++j) {
@@ -165,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 8)
         if (f < per_tok) {
           if constexpr (kInt8) {
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (ok[j]) dequant16(v[j], sc[j], o0, o1);
+            if (ok[j]) dequant16(v[j], s_[j], o0, o1);
             dst[2 * f] = o0;
             dst[2 * f + 1] = o1;
           } else {
@@ -200,8 +255,9 @@ int grid_for_tokens(const engram_plan* p, int64_t ntok) {
 template <int kCpr, bool kInt8>
 cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
                        const uint16_t* scales, void* e, cudaStream_t s) {
-  return launch_pdl(row_gather_kernel<kCpr, kInt8, false>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
-                    p->host, &p->dev->err, static_cast<const int32_t*>(idx), static_cast<const int32_t*>(nullptr), 1,
+  auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, false, false, true> : row_gather_kernel<kCpr, kInt8, false>;
+  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+                    p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(idx), static_cast<const int32_t*>(nullptr), 1,
                     static_cast<const int32_t*>(nullptr), 0, static_cast<const int32_t*>(nullptr), ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
                     static_cast<uint4*>(e), RowCache{});
@@ -211,8 +267,10 @@ template <int kCpr, bool kInt8>
 cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                          const int32_t* prev, const void* table, const uint16_t* scales, void* e, cudaStream_t s) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
-  return launch_pdl(row_gather_kernel<kCpr, kInt8, true>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
-                    p->host, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T, proj, V, prev, ntok,
+  auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, false, true> : row_gather_kernel<kCpr, kInt8, true>;
+  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+                    p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T,
+                    proj, V, prev, ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
                     static_cast<uint4*>(e), RowCache{});
 }
@@ -222,8 +280,10 @@ cudaError_t launch_cached(const engram_plan* p, const int32_t* ids, int B, int T
                           const int32_t* prev, const void* table, const uint16_t* scales, void* e,
                           const RowCache& cache, cudaStream_t s) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
-  return launch_pdl(row_gather_kernel<kCpr, kInt8, true, true>, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
-                    p->host, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T, proj, V, prev, ntok,
+  auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, true, true> : row_gather_kernel<kCpr, kInt8, true, true>;
+  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+                    p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T,
+                    proj, V, prev, ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
                     static_cast<uint4*>(e), cache);
 }
