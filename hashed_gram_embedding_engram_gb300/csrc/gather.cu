@@ -122,6 +122,11 @@ __global__ void __launch_bounds__(kThreads, 8)
   RowConst rc[kRows];
   if (has0) rc[0] = row_const(pdg, K, lane);
   if (kWide && has1) rc[kRows - 1] = row_const(pdg, K, lane + 32);
+  if constexpr (kHash) {
+    // P (read at random, written by no kernel) into L2 while the ids load: one 128-byte line per thread
+    const int64_t line = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (line * 32 < V) ptx::prefetch_l2(proj + line * 32);
+  }
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
 

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tma_prefetch_desc(&tmV);
       ptx::tma_prefetch_desc(&tmH);
     }
+    gemm_prefetch_b<BN, kFused>(c, &tmB);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmB);
     ptx::tma_prefetch_desc(&tmV);
     ptx::tma_prefetch_desc(&tmH);
+    gemm_prefetch_b<BN, true, true>(c, &tmB);
   }
   ptx::tc_fence_before();
   __syncthreads();

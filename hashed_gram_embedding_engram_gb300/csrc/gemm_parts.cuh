@@ -31,7 +31,9 @@ struct Cfg {
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kEpiBytes = kFused ? 8 * kEpiWarpBytes : 0;
+  // fused: 8 warps x (the warp's staging, then its columns' g_h and g_k: BN/2 floats each)
+  static constexpr int kGWarpBytes = kFused ? BN * 4 : 0;
+  static constexpr int kEpiBytes = kFused ? 8 * (kEpiWarpBytes + kGWarpBytes) : 0;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
@@ -117,9 +119,11 @@ __device__ __forceinline__ void dequant_chunk(const EngramEpilogue& epi, float s
   }
 }
 
+// gs: the warp's copy of g_h (then g_k) over its BN/2 columns of a k tile.
 template <int BN, bool kF8 = false>
 __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const CUtensorMap* tmV, uint8_t* eb,
-                                               uint32_t t_row, int row, int row0, int Mr, int n0, int c_lo, int lane) {
+                                               const float* gs, uint32_t t_row, int row, int row0, int Mr, int n0,
+                                               int c_lo, int lane) {
   constexpr int SW = BN / 2;
   const float srow = kF8 && row < Mr ? __ldg(epi.s_row + row) : 0.f;
   constexpr int kChunks = SW / 32;          // 1, 2 or 4
@@ -164,8 +168,7 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
     const int m = (n0 - d) / d;
     const int col = n0 - d - m * d;
     const int j = (col + c_lo) / SW;
-    const float* gh = epi.g_h + static_cast<int64_t>(m) * d + col;
-    const float* gk = epi.g_k + static_cast<int64_t>(m) * d + col;
+    (void)col;
     float s_dot[3], s_sk[3], s_sh[3];
     int top = 0;
 #pragma unroll
@@ -177,14 +180,14 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
       dequant_chunk<kF8>(epi, srow, n0 + c, r);
       float dot = 0.f, sk = 0.f, sh = 0.f;
       const uint8_t* hb = eb + (ci >> 1) * 4096 + lane * 128;     // this row of the chunk's 64-column box
-      const float4* gh4 = reinterpret_cast<const float4*>(gh + c);
-      const float4* gk4 = reinterpret_cast<const float4*>(gk + c);
+      const float4* gh4 = reinterpret_cast<const float4*>(gs + ci * 32);        // shared: broadcast reads
+      const float4* gk4 = reinterpret_cast<const float4*>(gs + SW + ci * 32);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const uint4 hv = *reinterpret_cast<const uint4*>(hb + ((((ci & 1) * 4 + q4) ^ swz) << 4));
         const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
-        const float4 ga = __ldg(gh4 + 2 * q4), gb = __ldg(gh4 + 2 * q4 + 1);
-        const float4 ka = __ldg(gk4 + 2 * q4), kb = __ldg(gk4 + 2 * q4 + 1);
+        const float4 ga = gh4[2 * q4], gb = gh4[2 * q4 + 1];
+        const float4 ka = gk4[2 * q4], kb = gk4[2 * q4 + 1];
         const float g[8] = {ga.x * ka.x, ga.y * ka.y, ga.z * ka.z, ga.w * ka.w,
                             gb.x * kb.x, gb.y * kb.y, gb.z * kb.z, gb.w * kb.w};
 #pragma unroll
@@ -275,6 +278,18 @@ __device__ __forceinline__ void gemm_setup(const GemmCtx& c, int warp, int lane)
     ptx::tmem_alloc(&bars->tmem_base, G::kTmemCols);
     ptx::tmem_relinquish();
   }
+}
+
+// Warp 0, lane 0, before the dependency wait: W_kv into L2, each column
+// panel by one block (the blocks of the first row block).  W_kv is not
+// written by the kernel before, and a prefetch changes no data, so it may
+// overlap that kernel.
+template <int BN, bool kFused, bool kF8 = false>
+__device__ __forceinline__ void gemm_prefetch_b(const GemmCtx& c, const CUtensorMap* tmB) {
+  using G = Cfg<BN, kFused, kF8>;
+  if (static_cast<int>(blockIdx.x) >= c.n_tiles || static_cast<int>(blockIdx.x) >= c.num_tiles) return;
+  const int n0 = (static_cast<int>(blockIdx.x) % c.n_tiles) * BN;
+  for (int kb = 0; kb < c.k_blocks; ++kb) ptx::tma_prefetch_l2_2d(tmB, kb * G::kBKe, n0);
 }
 
 // Warp 0, lane 0.
@@ -387,6 +402,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpil
   const int ew = warp - 2;
   const int c_lo = (ew >> 2) * (BN / 2);  // half of the tile's columns
   uint8_t* eb = epi_smem + ew * kEpiWarpBytes;
+  float* gs = reinterpret_cast<float*>(epi_smem + 8 * kEpiWarpBytes + ew * G::kGWarpBytes);
   int acc = 0;
   uint32_t acc_phase = 0;
   uint32_t h_phase = 0;
@@ -403,7 +419,11 @@ __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpil
         ptx::fence_proxy_async_smem();
         const int m = (n0 - epi.d) / epi.d;
         const int col = n0 - epi.d - m * epi.d + c_lo;
-        ptx::mbar_arrive_expect_tx(&bars->hbar[ew], G::kHBoxes * 4096);
+        ptx::mbar_arrive_expect_tx(&bars->hbar[ew], G::kHBoxes * 4096 + G::kGWarpBytes);
+        // the slice's RMSNorm weights, read by every lane of every row: one copy into shared memory
+        const int64_t go = static_cast<int64_t>(m) * epi.d + col;
+        ptx::bulk_load(gs, epi.g_h + go, G::kGWarpBytes / 2, &bars->hbar[ew]);
+        ptx::bulk_load(gs + BN / 2, epi.g_k + go, G::kGWarpBytes / 2, &bars->hbar[ew]);
 #pragma unroll
         for (int bx = 0; bx < G::kHBoxes; ++bx)
           ptx::tma_load_3d(eb + bx * 4096, &tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32);
@@ -438,7 +458,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpil
         }
       }
     } else {
-      fused_epilogue<BN, kF8>(epi, &tmV, eb, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
+      fused_epilogue<BN, kF8>(epi, &tmV, eb, gs, t_row, row, m0 + q * 32, Mr, n0, c_lo, lane);
     }
     ptx::tc_fence_before();
     __syncwarp();

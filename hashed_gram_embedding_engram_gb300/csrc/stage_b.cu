@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kSbThreads, 1)
     ptx::tma_prefetch_desc(&tmB);
     ptx::tma_prefetch_desc(&tmV);
     ptx::tma_prefetch_desc(&tmH);
+    gk::gemm_prefetch_b<kSbBN, true>(c, &tmB);
   }
   if (warp == 10 && lane == 0) {
     ptx::tma_prefetch_desc(&cv_v);
