@@ -357,6 +357,18 @@ class EngramCache:
         return a.value, b.value, l.value, c.value
 
 
+_COPY_STREAMS = {}
+
+
+def _copy_streams(dev):
+    """The host-to-device and device-to-host copy streams of a device, shared by
+    every EngramLayer on it so that their transfers cross the link in order."""
+    key = torch.device(dev).index
+    if key not in _COPY_STREAMS:
+        _COPY_STREAMS[key] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    return _COPY_STREAMS[key]
+
+
 class EngramLayer:
     """A plan, its weights, the projection map and a reusable workspace.
 
@@ -367,14 +379,29 @@ class EngramLayer:
     overlap (use pinned host tensors, or the copies serialise).  Pieces split
     the batch when B >= chunks (sequences are independent), else the
     positions of a single-sequence batch with a streaming state carried from
-    piece to piece; both give the bits of one whole-batch call."""
+    piece to piece; both give the bits of one whole-batch call.
+
+    The copy streams are shared by all layers on a device.  A call's input
+    copies wait for the work already queued on the current stream, or, given
+    ``after`` (an event recorded on the current stream), only for that event
+    and the same layer's previous call (whose device buffers they reuse): so
+    independent layers called one after another with the same ``after``
+    overlap, the next layer's inputs crossing while this one computes.  With
+    ``join=False`` the current stream does not wait for this call's copy back
+    to the host; ``join()`` makes it wait (call it before reading H on the
+    host, and before the end of a CUDA-graph capture)."""
 
     def __init__(self, plan: EngramPlan, weights: EngramWeights, proj: torch.Tensor, chunks: int = 4):
         self.plan, self.weights, self.proj = plan, weights, proj
         self.chunks = max(1, int(chunks))
         self._ws = None
         self._dev_buf = None
-        self._streams = None
+        # (event, recorded during a graph capture): the previous call is done with the device
+        # buffers; its copy back to the host completed.  An event is waited on only in the mode
+        # it was recorded in: a capture may not wait on eager work (which a capture follows
+        # anyway, from a synchronised device), nor eager work on a captured event.
+        self._free = None
+        self._last_out = None
 
     def workspace(self, ntok: int, device) -> torch.Tensor:
         need = self.plan.workspace_bytes(ntok)
@@ -387,11 +414,15 @@ class EngramLayer:
         if self._dev_buf is None or self._dev_buf[0] != key:
             self._dev_buf = (key, torch.empty(ids.shape, dtype=ids.dtype, device=dev),
                              torch.empty(H.shape, dtype=H.dtype, device=dev))
-        if self._streams is None:
-            self._streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
         return self._dev_buf[1], self._dev_buf[2]
 
-    def __call__(self, ids: torch.Tensor, H: torch.Tensor, state: Optional[EngramState] = None) -> torch.Tensor:
+    def join(self) -> None:
+        """Make the current stream wait for the last call's copy back to the host."""
+        if self._last_out is not None and self._last_out[1] == torch.cuda.is_current_stream_capturing():
+            torch.cuda.current_stream(self.proj.device).wait_event(self._last_out[0])
+
+    def __call__(self, ids: torch.Tensor, H: torch.Tensor, state: Optional[EngramState] = None,
+                 join: bool = True, after: Optional[torch.cuda.Event] = None) -> torch.Tensor:
         dev = self.proj.device
         if H.is_cuda:
             ids_d = ids if ids.is_cuda else ids.to(dev, non_blocking=True)
@@ -409,9 +440,15 @@ class EngramLayer:
             along_b = True
         ids_h = ids if not ids.is_cuda else ids.cpu()
         ids_d, H_d = self._buffers(ids_h, H, dev)
-        s_in, s_out = self._streams
+        s_in, s_out = _copy_streams(dev)
         main = torch.cuda.current_stream(dev)
-        s_in.wait_stream(main)                    # device buffers free: the previous call joined main
+        if after is None:
+            after = torch.cuda.Event()
+            after.record(main)                    # work the caller queued before this call comes first
+        s_in.wait_event(after)
+        capturing = torch.cuda.is_current_stream_capturing()
+        if self._free is not None and self._free[1] == capturing:
+            s_in.wait_event(self._free[0])        # this layer's device buffers are free again
         st = None if along_b else EngramState.zeros(self.plan, 1, dev)
         ws = self.workspace(max(hi - lo for lo, hi in cuts) * (T if along_b else 1), dev)
         last_out = None
@@ -434,5 +471,8 @@ class EngramLayer:
                 h_h.copy_(h_c, non_blocking=True)
                 last_out = torch.cuda.Event()
                 last_out.record(s_out)
-        main.wait_event(last_out)                 # the host copy is complete when main's work is
+        self._free = (last_out, capturing)        # the last reader of the device buffers
+        self._last_out = (last_out, capturing)
+        if join:
+            main.wait_event(last_out)             # the host copy is complete when main's work is
         return H

@@ -326,6 +326,55 @@ def test_layer_pipelines_host_inputs_bit_exactly(B, T, chunks):
     assert torch.equal(H_h.view(torch.int16), H.cpu().view(torch.int16))   # the caller's input untouched
 
 
+def test_independent_layers_overlap_and_stay_bit_exact():
+    """Two independent layers with host-resident H, called with one fork event
+    and joined afterwards (so each one's copies overlap the other's compute),
+    eagerly and replayed from a CUDA graph, three times on the same buffers:
+    each equals its own device-resident forward bit for bit."""
+    from hashed_gram_embedding_engram_gb300 import EngramLayer
+    w = SMALL["small_bf16"].scaled(B=1, T=300)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    ids_h = torch.from_numpy(ids).pin_memory()
+    lays, refs, outs, inputs = [], [], [], []
+    for lid in (1, 15):
+        L = W.layer_inputs(w, lid)
+        plan, weights, proj, H = make_layer(w, L, P, ids.size)
+        ref = H.clone()
+        plan.forward(torch.from_numpy(ids).cuda(), proj, weights, ref)
+        lays.append(EngramLayer(plan, weights, proj, chunks=2))
+        refs.append(ref.cpu())
+        inputs.append(H.cpu().pin_memory())
+        outs.append(H.cpu().pin_memory())
+
+    def step():
+        fork = torch.cuda.Event()
+        fork.record(torch.cuda.current_stream())
+        for lay, out in zip(lays, outs):
+            lay(ids_h, out, join=False, after=fork)
+        for lay in lays:
+            lay.join()
+
+    def check():
+        torch.cuda.synchronize()
+        for out, ref in zip(outs, refs):
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+    for _ in range(3):
+        for out, inp in zip(outs, inputs):
+            out.copy_(inp)
+        step()
+        check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        step()
+    for _ in range(3):
+        for out, inp in zip(outs, inputs):
+            out.copy_(inp)
+        g.replay()
+        check()
+
+
 # --------------------------------------------------------------------------- #
 # UVA: host-resident tables
 # --------------------------------------------------------------------------- #
