@@ -114,6 +114,10 @@ class EngramState:
     def clone(self) -> "EngramState":
         return EngramState(self.prev_ids.clone(), self.u_ring.clone(), self.pos.clone())
 
+    def rows(self, lo: int, hi: int) -> "EngramState":
+        """The state of sequences lo..hi-1 (views: updates land in this state)."""
+        return EngramState(self.prev_ids[lo:hi], self.u_ring[lo:hi], self.pos[lo:hi])
+
 
 class EngramPlan:
     """A validated layer configuration bound to the current CUDA device."""
@@ -379,7 +383,8 @@ class EngramLayer:
     overlap (use pinned host tensors, or the copies serialise).  Pieces split
     the batch when B >= chunks (sequences are independent), else the
     positions of a single-sequence batch with a streaming state carried from
-    piece to piece; both give the bits of one whole-batch call.
+    piece to piece; both give the bits of one whole-batch call.  A state
+    given with a batch split continues each piece's own sequences.
 
     The copy streams are shared by all layers on a device.  A call's input
     copies wait for the work already queued on the current stream, or, given
@@ -463,7 +468,8 @@ class EngramLayer:
                 ready.record(s_in)
             main.wait_event(ready)
             i_c, h_c = (i_d, h_d) if along_b else (i_d.contiguous(), h_d.contiguous())
-            self.plan.forward(i_c, self.proj, self.weights, h_c, state if along_b else st, ws)
+            pst = (None if state is None else state.rows(lo, hi)) if along_b else st
+            self.plan.forward(i_c, self.proj, self.weights, h_c, pst, ws)
             done = torch.cuda.Event()
             done.record(main)
             with torch.cuda.stream(s_out):

@@ -326,6 +326,32 @@ def test_layer_pipelines_host_inputs_bit_exactly(B, T, chunks):
     assert torch.equal(H_h.view(torch.int16), H.cpu().view(torch.int16))   # the caller's input untouched
 
 
+def test_layer_with_state_split_along_the_batch():
+    """A host-resident decode-style call split along the batch with a streaming
+    state: each piece continues its own sequences' state; the result and the
+    state equal one device-resident call's, bit for bit."""
+    from hashed_gram_embedding_engram_gb300 import EngramLayer, EngramState
+    w = SMALL["small_bf16"].scaled(B=6, T=40)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    st_ref, st = EngramState.zeros(plan, w.B), EngramState.zeros(plan, w.B)
+    pre = H[:, :30].contiguous()
+    plan.forward(ids_d[:, :30].contiguous(), proj, weights, pre.clone(), st_ref)
+    plan.forward(ids_d[:, :30].contiguous(), proj, weights, pre.clone(), st)
+    ref = H[:, 30:].contiguous()
+    plan.forward(ids_d[:, 30:].contiguous(), proj, weights, ref, st_ref)
+    layer = EngramLayer(plan, weights, proj, chunks=3)
+    out = H[:, 30:].contiguous().cpu().pin_memory()
+    layer(torch.from_numpy(ids[:, 30:].copy()).pin_memory(), out, st)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
+    for a, b in ((st.prev_ids, st_ref.prev_ids), (st.u_ring, st_ref.u_ring), (st.pos, st_ref.pos)):
+        assert torch.equal(a, b)
+
+
 def test_independent_layers_overlap_and_stay_bit_exact():
     """Two independent layers with host-resident H, called with one fork event
     and joined afterwards (so each one's copies overlap the other's compute),
