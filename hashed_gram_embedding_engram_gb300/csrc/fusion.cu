@@ -328,7 +328,9 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
 // conv kernel's operation order, updates H, then writes s * v into the slot
 // of the new position -- the slot its own tap at lag (w-1)*dilation just read,
 // so no other thread touches it.  Thread 0 then rolls the projected ids and
-// advances pos.  The result equals finalize + conv + state bit for bit.
+// advances pos.  The result equals finalize + conv + state bit for bit.  Each
+// thread loads its first channel group's taps, v, ring rows and H before the
+// barrier that publishes the gate, so those loads overlap warp 0's gate.
 template <typename TH, int W, bool kPart>
 __global__ void __launch_bounds__(256) decode_tail_kernel(
     const float* __restrict__ gate_in, int n_sl, int pstride, int saw, float eps, const float* __restrict__ v,
@@ -337,11 +339,34 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
     const int32_t* __restrict__ proj, int V, int32_t* __restrict__ prev, int N, float* __restrict__ sa_out,
     uint32_t* __restrict__ err, TH* __restrict__ H) {
   __shared__ float s_sa[2 * kMaxM];
-  __shared__ int s_p0;
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31;
+  const int p0 = ring != nullptr ? pos[b] : 0;     // written by thread 0 at the end, after the barrier below
+  // This thread's first channel group, branch 0: its taps, v, ring rows and H are loaded before
+  // the gate is known (they do not depend on it), so their latency overlaps warp 0's gate.
+  const int g0 = threadIdx.x;
+  const bool pre = g0 < d / 4;
+  float wq0[4][W], vt0[4], u0[W][4], h0[4];
+  if (pre) {
+    const int c = 4 * g0;
+    float gc[4];
+    ld4(g_c + c, gc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) wq0[i][j] = __ldg(conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
+    }
+    ld4(v + static_cast<int64_t>(b) * sv + c, vt0);
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      const int lag = (W - 1 - j) * dil;
+      if (lag > 0 && ring != nullptr && p0 - lag >= 0)
+        ld4(ring + ((static_cast<int64_t>(b) * L + (p0 - lag) % L) * M) * d + c, u0[j]);
+    }
+    H4<TH>::load(H + static_cast<int64_t>(b) * M * d + c, h0);
+  }
   if (threadIdx.x < 32) {
     if constexpr (kPart) {
       gate_row(gate_in + static_cast<int64_t>(b) * pstride, n_sl, nodes_per_lane(n_sl), M,
@@ -349,15 +374,22 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
     } else if (lane < 2 * M) {
       s_sa[lane] = gate_in[static_cast<int64_t>(b) * saw + lane];
     }
-    if (lane == 0) s_p0 = ring != nullptr ? pos[b] : 0;
   }
   __syncthreads();
   if (sa_out != nullptr && threadIdx.x < 2 * M) sa_out[static_cast<int64_t>(b) * saw + threadIdx.x] = s_sa[threadIdx.x];
-  const int p0 = s_p0;
   for (int g = threadIdx.x; g < d / 4; g += blockDim.x) {
     const int c = 4 * g;
+    const bool first = g == g0;                    // its inputs of branch 0 are already in registers
     float wq[4][W];
-    {
+    float vt[4];
+    if (first) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        vt[i] = vt0[i];
+#pragma unroll
+        for (int j = 0; j < W; ++j) wq[i][j] = wq0[i][j];
+      }
+    } else {
       float gc[4];
       ld4(g_c + c, gc);
 #pragma unroll
@@ -365,11 +397,11 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
 #pragma unroll
         for (int j = 0; j < W; ++j) wq[i][j] = __ldg(conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
       }
+      ld4(v + static_cast<int64_t>(b) * sv + c, vt);
     }
-    float vt[4];
-    ld4(v + static_cast<int64_t>(b) * sv + c, vt);
     for (int m = 0; m < M; ++m) {
       const float sm = s_sa[m];
+      const bool have = first && m == 0;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < W; ++j) {
@@ -379,14 +411,24 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
           for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sm * vt[i], acc[i]);
         } else if (ring != nullptr && p0 - lag >= 0) {
           float u[4];                                 // the ring holds RMSNorm(v~) before its weight
-          ld4(ring + ((static_cast<int64_t>(b) * L + (p0 - lag) % L) * M + m) * d + c, u);
+          if (have) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[i] = u0[j][i];
+          } else {
+            ld4(ring + ((static_cast<int64_t>(b) * L + (p0 - lag) % L) * M + m) * d + c, u);
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
         }
       }
       TH* hp = H + (static_cast<int64_t>(b) * M + m) * d + c;
       float h[4];
-      H4<TH>::load(hp, h);
+      if (have) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = h0[i];
+      } else {
+        H4<TH>::load(hp, h);
+      }
       const float at = s_sa[M + m];
 #pragma unroll
       for (int i = 0; i < 4; ++i) h[i] = h[i] + fmaf(at, vt[i], silu_fast(acc[i]));
