@@ -463,6 +463,11 @@ struct engram_cache {
   int64_t cached;
   int64_t batch_cap;                 // lookups the dedup region has a row for (0: no dedup)
   uint32_t* batch_rows;              // [batch_cap] the table row each lookup claimed, or 0xFFFFFFFF
+  // dedup pipeline over pieces of the batch: claims on the caller's stream, fetches over the
+  // host link on `fetch`, gathers from HBM on `gather`
+  static constexpr int kChunks = 4;
+  cudaStream_t fetch = nullptr, gather = nullptr;
+  cudaEvent_t claimed[kChunks] = {}, fetched[kChunks] = {}, fork = nullptr, join = nullptr;
 };
 
 extern "C" {
@@ -504,6 +509,13 @@ engram_status_t engram_cache_destroy(engram_cache_t* c) {
   for (void* ptr : {static_cast<void*>(c->counts), static_cast<void*>(c->slot), c->rows, static_cast<void*>(c->stats),
                     static_cast<void*>(c->batch_rows)})
     if (ptr && cudaFree(ptr) != cudaSuccess) e = cudaErrorUnknown;
+  for (int i = 0; i < engram_cache::kChunks; ++i)
+    for (cudaEvent_t ev : {c->claimed[i], c->fetched[i]})
+      if (ev && cudaEventDestroy(ev) != cudaSuccess) e = cudaErrorUnknown;
+  for (cudaEvent_t ev : {c->fork, c->join})
+    if (ev && cudaEventDestroy(ev) != cudaSuccess) e = cudaErrorUnknown;
+  for (cudaStream_t st : {c->fetch, c->gather})
+    if (st && cudaStreamDestroy(st) != cudaSuccess) e = cudaErrorUnknown;
   delete c;
   return cuda_status(e);
 }
@@ -545,11 +557,49 @@ engram_status_t engram_stage_a_cached(const engram_cache_t* c, const int32_t* id
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t lookups = static_cast<int64_t>(B) * T * plan->R;
   const bool dedup = c->batch_cap > 0 && lookups <= c->batch_cap;
+  const int chunks = dedup && c->gather ? (B < engram_cache::kChunks ? B : engram_cache::kChunks) : 1;
+  if (chunks > 1) {
+    // pieces of whole sequences: piece i+1 is claimed while piece i's claimed rows cross the host
+    // link and piece i-1 is gathered from HBM.  A row claimed by an earlier piece is served from its
+    // slot and not fetched again; every claim is released after the last gather.
+    const int R = plan->R, Nm1 = plan->cfg.N - 1;
+    const size_t e_row = static_cast<size_t>(plan->d_mem) * act_bytes(plan->cfg.act_dtype);
+    uint8_t* region = static_cast<uint8_t*>(c->rows) + static_cast<size_t>(c->capacity) * c->row_bytes;
+    if (cudaEventRecord(c->fork, s) != cudaSuccess || cudaStreamWaitEvent(c->fetch, c->fork, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(c->gather, c->fork, 0) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    for (int k = 0; k < chunks; ++k) {
+      const int b0 = static_cast<int>(static_cast<int64_t>(B) * k / chunks);
+      const int b1 = static_cast<int>(static_cast<int64_t>(B) * (k + 1) / chunks);
+      const int64_t f0 = static_cast<int64_t>(b0) * T * R;
+      const int64_t n = static_cast<int64_t>(b1 - b0) * T * R;
+      const int32_t* ids_k = ids + static_cast<int64_t>(b0) * T;
+      const int32_t* prev_k = prev_ids ? prev_ids + static_cast<int64_t>(b0) * Nm1 : nullptr;
+      if (engram::dedup_claim(plan, ids_k, b1 - b0, T, proj, V, prev_k, c->slot,
+                              static_cast<int32_t>(c->capacity + f0), c->batch_rows + f0, s) != cudaSuccess ||
+          cudaEventRecord(c->claimed[k], s) != cudaSuccess ||
+          cudaStreamWaitEvent(c->fetch, c->claimed[k], 0) != cudaSuccess ||
+          engram::dedup_fetch(plan, n, c->batch_rows + f0, c->row_bytes, c->table,
+                              region + static_cast<size_t>(f0) * c->row_bytes, c->fetch) != cudaSuccess ||
+          cudaEventRecord(c->fetched[k], c->fetch) != cudaSuccess ||
+          cudaStreamWaitEvent(c->gather, c->fetched[k], 0) != cudaSuccess ||
+          engram::launch_hash_gather_cached(plan, ids_k, b1 - b0, T, proj, V, prev_k, c->table,
+                                            static_cast<const uint16_t*>(sc),
+                                            static_cast<uint8_t*>(e_out) + static_cast<size_t>(b0) * T * e_row,
+                                            c->slot, c->rows, c->stats, c->gather) != cudaSuccess)
+        return ENGRAM_ERR_CUDA;
+    }
+    if (cudaEventRecord(c->join, c->gather) != cudaSuccess || cudaStreamWaitEvent(s, c->join, 0) != cudaSuccess ||
+        engram::dedup_release(plan, lookups, c->batch_rows, c->slot, c->stats + 3, s) != cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    return ENGRAM_OK;
+  }
   if (dedup) {
     // distinct uncached rows of the batch: one fetch each over the host link, into the batch region
     uint8_t* region = static_cast<uint8_t*>(c->rows) + static_cast<size_t>(c->capacity) * c->row_bytes;
     if (engram::dedup_claim(plan, ids, B, T, proj, V, prev_ids, c->slot, static_cast<int32_t>(c->capacity),
-                            c->row_bytes, c->table, region, c->batch_rows, s) != cudaSuccess)
+                            c->batch_rows, s) != cudaSuccess ||
+        engram::dedup_fetch(plan, lookups, c->batch_rows, c->row_bytes, c->table, region, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
   }
   if (engram::launch_hash_gather_cached(plan, ids, B, T, proj, V, prev_ids, c->table, static_cast<const uint16_t*>(sc),
@@ -582,6 +632,33 @@ engram_status_t engram_cache_set_dedup(engram_cache_t* c, int64_t batch_rows) {
   c->rows = rows;
   c->batch_rows = br;
   c->batch_cap = batch_rows;
+  if (batch_rows > 0 && !c->gather) {
+    // the pipeline's streams and events (its fork/join are stream-ordered and capturable)
+    auto ev = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+    bool made = cudaStreamCreateWithFlags(&c->fetch, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaStreamCreateWithFlags(&c->gather, cudaStreamNonBlocking) == cudaSuccess && ev(&c->fork) &&
+                ev(&c->join);
+    for (int i = 0; made && i < engram_cache::kChunks; ++i) made = ev(&c->claimed[i]) && ev(&c->fetched[i]);
+    if (!made) {
+      cudaGetLastError();
+      for (int i = 0; i < engram_cache::kChunks; ++i)
+        for (cudaEvent_t* e : {&c->claimed[i], &c->fetched[i]})
+          if (*e) {
+            cudaEventDestroy(*e);
+            *e = nullptr;
+          }
+      for (cudaEvent_t* e : {&c->fork, &c->join})
+        if (*e) {
+          cudaEventDestroy(*e);
+          *e = nullptr;
+        }
+      for (cudaStream_t* st : {&c->fetch, &c->gather})
+        if (*st) {
+          cudaStreamDestroy(*st);
+          *st = nullptr;
+        }                                 // the dedup then runs unpipelined
+    }
+  }
   return ENGRAM_OK;
 }
 

@@ -164,11 +164,15 @@ int grid_rows(const engram_plan* p, int64_t n) {
 }  // namespace
 
 cudaError_t dedup_claim(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                        const int32_t* prev_ids, int32_t* slot, int32_t first_slot, int row_bytes, const void* table,
-                        void* region, uint32_t* owner, cudaStream_t s) {
+                        const int32_t* prev_ids, int32_t* slot, int32_t first_slot, uint32_t* owner, cudaStream_t s) {
   const int64_t total = static_cast<int64_t>(B) * T * p->R;
   dedup_claim_kernel<<<grid_rows(p, total), 256, 0, s>>>(p->host, &p->dev->err, ids, B, T, proj, V, prev_ids, slot,
                                                          first_slot, owner);
+  return cudaGetLastError();
+}
+
+cudaError_t dedup_fetch(const engram_plan* p, int64_t total, const uint32_t* owner, int row_bytes, const void* table,
+                        void* region, cudaStream_t s) {
   dedup_fetch_kernel<<<grid_rows(p, total * (row_bytes / 16)), 256, 0, s>>>(
       total, owner, row_bytes, static_cast<const uint8_t*>(table), static_cast<uint8_t*>(region));
   return cudaGetLastError();

@@ -122,8 +122,9 @@ cudaError_t cache_build(const engram_plan* p, int64_t capacity, int row_bytes, c
 // after the gather the release returns the slots to -1 and adds the claims to
 // *fetched.
 cudaError_t dedup_claim(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                        const int32_t* prev_ids, int32_t* slot, int32_t first_slot, int row_bytes, const void* table,
-                        void* region, uint32_t* owner, cudaStream_t s);
+                        const int32_t* prev_ids, int32_t* slot, int32_t first_slot, uint32_t* owner, cudaStream_t s);
+cudaError_t dedup_fetch(const engram_plan* p, int64_t total, const uint32_t* owner, int row_bytes, const void* table,
+                        void* region, cudaStream_t s);
 cudaError_t dedup_release(const engram_plan* p, int64_t total, const uint32_t* owner, int32_t* slot,
                           unsigned long long* fetched, cudaStream_t s);
 cudaError_t launch_kv_projection(const engram_plan* p, const void* e, int64_t ntok, const void* w_kv, void* kv,
