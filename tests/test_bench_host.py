@@ -24,3 +24,27 @@ def test_per_token_work_of_the_prefill_workload():
     assert work["stage_b"] == work["kv_gemm"]
     # v fp32, the (s, alpha) row, H read and written in bf16
     assert work["conv"] == ("bytes", 4 * 1024 + 8 + 2 * 2 * 1024)
+
+
+def test_reference_arm_generates_its_inputs_once(monkeypatch, capsys):
+    """The reference arm times the oracle on a sample per step; the layers'
+    tables are generated once per process, not once per step, so the run's
+    length follows the step count through the oracle's own work only."""
+    import argparse
+    import json
+    import workloads as W
+    calls = []
+    real = W.layer_inputs
+
+    def counted(*a, **k):
+        calls.append(a[1] if len(a) > 1 else k.get("layer"))
+        return real(*a, **k)
+
+    monkeypatch.setattr(W, "layer_inputs", counted)
+    monkeypatch.setattr(bench, "_ORACLE_INPUTS", None)
+    bench.run_reference(argparse.Namespace(steps=4, warmup=1, gpus=1))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 4 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert len(calls) == len(W.PREFILL_BF16.layers)

@@ -122,3 +122,119 @@ def test_multibranch_n4_full():
     plan.forward(torch.from_numpy(ids).cuda(), proj, weights, H)
     assert plan.get_error() == (0, 0)
     check_sampled(w, ids, P, L, H, sample_positions(w, n_random=48))
+
+
+def test_prefill_graph_step_full():
+    """The prefill step in the launch configuration the benchmark times: both
+    layers' Stage A on a side stream, each layer's Stage B on the main stream
+    once its rows are in, the whole step captured in a CUDA graph and replayed
+    with H restored in between.  Every replay equals the layer-by-layer forward
+    bit for bit, and the oracle at sampled positions."""
+    w = W.PREFILL_BF16
+    ids, P = W.token_stream(w), W.projection_map(w)
+    Ls = [W.layer_inputs(w, lid) for lid in w.layers]
+    built = [make_layer(w, L, P, ids.size) for L in Ls]
+    ids_d = torch.from_numpy(ids).cuda()
+    want = []
+    for plan, weights, proj, H in built:
+        Hr = H.clone()
+        plan.forward(ids_d, proj, weights, Hr)
+        want.append(Hr)
+    H0 = [H.clone() for *_, H in built]
+    es = [torch.empty(ids.size, w.d_mem, dtype=torch.bfloat16, device="cuda") for _ in built]
+    wss = [plan.new_workspace(ids.size, torch.device("cuda")) for plan, *_ in built]
+    side = torch.cuda.Stream()
+
+    def step():
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)
+        ready = []
+        with torch.cuda.stream(side):
+            for (plan, weights, proj, _), e in zip(built, es):
+                plan.stage_a(ids_d, proj, weights.table, weights.scales, out=e)
+                ev = torch.cuda.Event()
+                ev.record(side)
+                ready.append(ev)
+        for (plan, weights, _, H), e, ev, ws in zip(built, es, ready, wss):
+            main.wait_event(ev)
+            plan.stage_b(e, weights, H, workspace=ws)
+
+    def restore():
+        for (*_, H), h0 in zip(built, H0):
+            H.copy_(h0)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        restore()
+        g.replay()
+        torch.cuda.synchronize()
+        for (plan, *_, H), Hr in zip(built, want):
+            assert plan.get_error() == (0, 0)
+            assert torch.equal(H.view(torch.int16), Hr.view(torch.int16))
+    for L, (*_, H) in zip(Ls, built):
+        check_sampled(w, ids, P, L, H, sample_positions(w))
+
+
+@pytest.mark.parametrize("wname", ["prefill_bf16", "multibranch_n4"])
+def test_fp8_projection_full(wname):
+    """The e4m3 projection at full size: the weight codes and scales equal the
+    oracle's byte for byte, and the layer output matches the oracle's FP8
+    evaluation at sampled positions."""
+    import dataclasses
+    w = W.PREFILL_BF16 if wname == "prefill_bf16" else W.MULTIBRANCH_N4
+    ids, P, L = W.token_stream(w), W.projection_map(w), W.layer_inputs(w, w.layers[0])
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    q, sc = plan.quantize_fp8(weights.w_kv)
+    q_ref, s_ref = O.quantize_rows_e4m3(O.widen(L.W_kv, "bf16"))
+    assert np.array_equal(q.view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy(), q_ref)
+    assert np.array_equal(sc.cpu().numpy().astype(np.float64), s_ref)
+    w8 = dataclasses.replace(weights, w_kv=None, w_kv_fp8=q, w_kv_scale=sc)
+    plan.forward(torch.from_numpy(ids).cuda(), proj, w8, H)
+    assert plan.get_error() == (0, 0)
+    pos = sample_positions(w, n_random=48)
+    ref = O.forward_at(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype, pos, projection="fp8")
+    got = np.stack([act_to_f64(H[b, t]) for b, t in pos])
+    assert_close(got, ref, "bf16", f"{wname} fp8")
+
+
+def test_int8_host_cache_and_dedup_full():
+    """Stage A over the host link at full size with the HBM hot-row cache, the
+    per-batch dedup and both: the rows equal the plain UVA gather bit for bit;
+    with the dedup every lookup is served from HBM and each distinct uncached
+    row (the oracle's count when nothing is cached) crosses the link once."""
+    from hashed_gram_embedding_engram_gb300 import EngramCache
+    w = W.INT8_HOST
+    ids, P, L = W.token_stream(w), W.projection_map(w), W.layer_inputs(w, w.layers[0])
+    plan, weights, proj, H = make_layer(w, L, P, ids.size)
+    table_host = to_torch(L.table, "i8", "cpu", pin=True)
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = plan.stage_a(ids_d, proj, table_host, weights.scales)
+    z = O.hash_heads(O.project(ids, P), L.multipliers, L.primes, w.N, w.K).reshape(-1, w.R)
+    offsets = np.concatenate([[0], np.cumsum(np.asarray(L.primes, dtype=np.int64))[:-1]])
+    uniq = len(np.unique(z.astype(np.int64) + offsets[None, :]))
+    n = ids.size * w.R
+    warm = torch.from_numpy(W.token_stream(w, key="cache-warm")).cuda()
+    for capacity, dedup in ((0, True), (int(0.05 * plan.total_rows), False), (int(0.05 * plan.total_rows), True)):
+        c = EngramCache(plan, capacity, table_host)
+        if capacity:
+            c.observe(warm, proj)
+            assert c.build() > 0
+        if dedup:
+            c.set_dedup(n)
+        c.stats(reset=True)
+        got = c.stage_a(ids_d, proj, weights.scales)
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (capacity, dedup)
+        looked, from_hbm, link, _ = c.stats(reset=True)
+        assert looked == n
+        if dedup:
+            assert from_hbm == n
+            assert link == uniq if capacity == 0 else 0 < link < uniq
+        else:
+            assert 0 < from_hbm < n and link == n - from_hbm
+        c.close()
+    assert plan.get_error() == (0, 0)
