@@ -272,8 +272,14 @@ engram_status_t engram_cache_build(engram_cache_t* cache, int decay, engram_stre
  * first copies each distinct table row of the batch that is not cached over
  * the host link once, into a per-batch HBM region with a row per lookup
  * (after the cached rows, in the same slot map), serves every lookup of it
- * from HBM, and frees the slots again (four launches instead of one;
- * capturable).  Larger batches run without the dedup.  The output is
+ * from HBM, and frees the slots again.  A batch of B >= 2 sequences runs in
+ * up to four pieces of whole sequences so that the host-link copies of one
+ * piece overlap the claims of the next and the HBM gather of the one before:
+ * claims and the final release on the caller's stream, copies and gathers on
+ * two streams the cache owns (made here), which the caller's stream waits for
+ * before the call's work on it ends; stream-ordered and capturable.  A row
+ * claimed by an earlier piece is not fetched again.  Larger batches run
+ * without the dedup.  The output is
  * unchanged, bit for bit.  batch_rows = 0 turns it off.  Synchronises the
  * device and reallocates the cache's row buffer (cached rows are kept);
  * capacity + batch_rows <= INT32_MAX.  Device memory: batch_rows x (row
