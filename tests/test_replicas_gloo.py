@@ -49,3 +49,22 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(2.0, 1) == 2.0
     bench.barrier(1)
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Launched like the GPU arm with two ranks, the reference arm (the oracle
+    on the host cores) runs on rank 0 alone: one JSON line, every rank exits 0."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="2"))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["n_gpus"] == 2 and line["value"] > 0
