@@ -192,7 +192,7 @@ def run_ours(args) -> None:
     import torch
     import workloads as W
     from hashed_gram_embedding_engram_gb300 import EngramLayer
-    from tests.gpu_helpers import make_layer, to_torch
+    from workloads.torch_layer import make_layer, to_torch
 
     world, rank, local = dist_env()
     if world > 1:
@@ -660,7 +660,7 @@ def run_workload(args) -> None:
     import torch
     import workloads as W
     from hashed_gram_embedding_engram_gb300 import EngramState
-    from tests.gpu_helpers import make_layer, to_torch
+    from workloads.torch_layer import make_layer, to_torch
 
     dev = torch.device("cuda", torch.cuda.current_device())
     fp8 = args.workload.endswith("_fp8")           # the workload with the e4m3 K/V projection

@@ -220,7 +220,10 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
  * ENGRAM_ERR_WORKSPACE before any launch.  The current device must be the
  * plan's.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture.  All calls in the process share the one array and it keeps
+ * stream capture.  The cached address belongs to the device's context of that
+ * first call: after cudaDeviceReset (or anything else that destroys and
+ * re-creates the primary context) this entry point must not be called again
+ * in the same process.  All calls in the process share the one array and it keeps
  * the last call's contents (nothing in it needs to start at zero: the forward
  * writes every scratch byte before reading it), so calls that overlap on the
  * GPU -- on different streams, or from different threads -- race; serialise

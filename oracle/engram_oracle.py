@@ -259,13 +259,6 @@ def conv_branch(vt: np.ndarray, g_c: np.ndarray, conv: np.ndarray, dil: int, eps
 # --------------------------------------------------------------------------- #
 # the whole layer
 # --------------------------------------------------------------------------- #
-def stage_a(ids, P, mults, primes, N, K, tables, table_kind, scales=None, prev=None):
-    """Steps 1-4: raw ids [B, T] -> (z [B,T,R], e [B,T,d_mem] float64)."""
-    xp = project(ids, P)
-    z = hash_heads(xp, mults, primes, N, K, prev)
-    return z, gather_concat(z, tables, table_kind, scales)
-
-
 def forward(ids: np.ndarray, P: np.ndarray, L, N: int, K: int, dil: int, eps: float,
             table_kind: str, act_kind: str, state: Optional[Dict] = None,
             projection: str = "exact") -> Dict[str, np.ndarray]:

@@ -4,47 +4,11 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from hashed_gram_embedding_engram_gb300 import EngramPlan, EngramWeights
-
-
-def to_torch(a: np.ndarray, kind: str, device="cuda", pin: bool = False) -> torch.Tensor:
-    """numpy array as stored by the generators -> torch tensor of the stored dtype."""
-    if kind == "bf16":
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
-    else:
-        t = torch.from_numpy(np.ascontiguousarray(a))
-    if device == "cpu":
-        return t.pin_memory() if pin else t
-    return t.to(device)
+from workloads.torch_layer import make_layer, make_plan, make_weights, to_torch  # noqa: F401
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-
-
-def make_plan(w, L, max_tokens: int) -> EngramPlan:
-    return EngramPlan(N=w.N, K=w.K, row_dim=w.row_dim, d=w.d, M=w.M, conv_w=w.conv_w, conv_dilation=w.conv_dil,
-                      table_dtype=w.table_dtype, act_dtype=w.act_dtype, eps=w.eps, primes=L.primes.tolist(),
-                      multipliers=[int(m) for m in L.multipliers], max_tokens=max_tokens)
-
-
-def make_weights(w, L, table_on_host: bool = False) -> EngramWeights:
-    dev = "cpu" if table_on_host else "cuda"
-    table = to_torch(L.table, w.table_dtype, dev, pin=table_on_host)
-    scales = None
-    if L.scales is not None:
-        scales = to_torch(L.scales, "f16", "cuda")
-    return EngramWeights(table=table, w_kv=to_torch(L.W_kv, w.act_dtype), g_h=to_torch(L.g_h, "f32"),
-                         g_k=to_torch(L.g_k, "f32"), g_c=to_torch(L.g_c, "f32"), conv=to_torch(L.conv, "f32"),
-                         scales=scales)
-
-
-def make_layer(w, L, P, max_tokens: int, table_on_host: bool = False):
-    plan = make_plan(w, L, max_tokens)
-    weights = make_weights(w, L, table_on_host)
-    proj = torch.from_numpy(P).cuda()
-    H = to_torch(L.H, w.act_dtype)
-    return plan, weights, proj, H
 
 
 def act_to_f64(t: torch.Tensor) -> np.ndarray:
@@ -71,12 +35,16 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
 def assert_close(got: np.ndarray, ref: np.ndarray, kind: str, what: str = "") -> None:
     """got (as stored: bf16 or fp32, widened) vs the float64 oracle.
 
-    For bf16 the max-abs bound is 2e-2 except where |ref| >= 8: there one bf16
-    ulp is 0.0625 and no bf16 value lies within 2e-2 of every real, so the bound
-    there is one bf16 ulp.  The relative-L2 bound applies unchanged."""
+    For bf16 the max-abs bound is 2e-2 except where |ref| >= 8: there the
+    spacing of bf16 numbers is 0.0625, so no bf16 value lies within 2e-2 of
+    every real.  A stored output is the fp32 result (within 2e-2 of the real
+    one) rounded once to bf16, which moves it by at most half a bf16 ulp at
+    its own magnitude (at most |ref| + 2e-2), so the bound there is
+    2e-2 + ulp/2 (0.05125 on [8, 16 - 2e-2)).  The relative-L2 bound applies
+    unchanged."""
     tol_abs, tol_rel = TOL[kind]
     mx, rel = errors(got, ref)
     diff = np.abs(got - ref)
-    bound = np.where(np.abs(ref) < 8, tol_abs, bf16_ulp(ref)) if kind == "bf16" else tol_abs
+    bound = np.where(np.abs(ref) < 8, tol_abs, tol_abs + 0.5 * bf16_ulp(np.abs(ref) + tol_abs)) if kind == "bf16" else tol_abs
     worst = float((diff - bound).max())
     assert worst <= 0.0 and rel <= tol_rel, f"{what}: max-abs {mx:.4g}, rel-L2 {rel:.4g}, worst excess {worst:.3g}"

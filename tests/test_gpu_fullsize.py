@@ -31,12 +31,25 @@ def check_indices_and_rows(w, ids, P, L, plan, weights, proj):
     xp = O.project(ids, P)
     z = O.hash_heads(xp, L.multipliers, L.primes, w.N, w.K).reshape(-1, w.R)
     assert np.array_equal(idx.cpu().numpy(), z)
+    assert_rows_equal_oracle(w, z, L, e)
+    return idx, e
+
+
+def oracle_rows_bits(w, z, L):
+    """The oracle's gathered rows (Step 4) of indices z as bf16 bits, built in blocks."""
+    out = np.empty((z.shape[0], w.d_mem), dtype=np.uint16)
+    for lo in range(0, z.shape[0], CHUNK):
+        hi = min(z.shape[0], lo + CHUNK)
+        out[lo:hi] = O.f64_to_bf16_bits(O.gather_concat(z[lo:hi], L.tables(), w.table_dtype, L.table_scales()))
+    return out
+
+
+def assert_rows_equal_oracle(w, z, L, e):
+    """e (the GPU's gathered rows of indices z) equals the oracle's, bit for bit, in blocks."""
     for lo in range(0, z.shape[0], CHUNK):
         hi = min(z.shape[0], lo + CHUNK)
         ref = O.gather_concat(z[lo:hi], L.tables(), w.table_dtype, L.table_scales())
-        got = bf16_bits(e[lo:hi])
-        assert np.array_equal(got, O.f64_to_bf16_bits(ref)), lo
-    return idx, e
+        assert np.array_equal(bf16_bits(e[lo:hi]), O.f64_to_bf16_bits(ref)), lo
 
 
 def sample_positions(w, n_random=64, seed=0):
@@ -204,8 +217,8 @@ def test_fp8_projection_full(wname):
 
 def test_int8_host_cache_and_dedup_full():
     """Stage A over the host link at full size with the HBM hot-row cache, the
-    per-batch dedup and both: the rows equal the plain UVA gather bit for bit;
-    with the dedup every lookup is served from HBM and each distinct uncached
+    per-batch dedup and both: every output equals the oracle's gathered rows
+    (Steps 1-4) bit for bit, in full; with the dedup every lookup is served from HBM and each distinct uncached
     row (the oracle's count when nothing is cached) crosses the link once."""
     from hashed_gram_embedding_engram_gb300 import EngramCache
     w = W.INT8_HOST
@@ -215,6 +228,8 @@ def test_int8_host_cache_and_dedup_full():
     ids_d = torch.from_numpy(ids).cuda()
     ref = plan.stage_a(ids_d, proj, table_host, weights.scales)
     z = O.hash_heads(O.project(ids, P), L.multipliers, L.primes, w.N, w.K).reshape(-1, w.R)
+    oracle_bits = oracle_rows_bits(w, z, L)
+    assert np.array_equal(bf16_bits(ref), oracle_bits)
     offsets = np.concatenate([[0], np.cumsum(np.asarray(L.primes, dtype=np.int64))[:-1]])
     uniq = len(np.unique(z.astype(np.int64) + offsets[None, :]))
     n = ids.size * w.R
@@ -228,7 +243,7 @@ def test_int8_host_cache_and_dedup_full():
             c.set_dedup(n)
         c.stats(reset=True)
         got = c.stage_a(ids_d, proj, weights.scales)
-        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (capacity, dedup)
+        assert np.array_equal(bf16_bits(got), oracle_bits), (capacity, dedup)
         looked, from_hbm, link, _ = c.stats(reset=True)
         assert looked == n
         if dedup:

@@ -426,9 +426,10 @@ def test_uva_gather_equals_hbm_gather():
 @pytest.mark.parametrize("kind", ["small_i8", "small_bf16"])
 def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
     """Rows read through the cache are the rows of the table: the cached Stage A
-    equals the plain one (host table over UVA, and the HBM copy) bit for bit,
-    before any build (nothing cached), after an LFU build, and with every row
-    cached; the counters see every row and the hits the build promised."""
+    equals the oracle's gathered rows (Steps 1-4) bit for bit, before any build
+    (nothing cached), after an LFU build, and with every row cached, as do the
+    plain Stage A over the HBM table and over UVA; the counters see every row
+    and the hits the build promised."""
     from hashed_gram_embedding_engram_gb300 import EngramCache
     w = SMALL[kind]
     ids = W.token_stream(w)
@@ -437,13 +438,15 @@ def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
     plan, wd, proj, H = make_layer(w, L, P, ids.size)
     table_host = to_torch(L.table, w.table_dtype, "cpu", pin=True)
     ids_d = torch.from_numpy(ids).cuda()
+    oracle_bits = oracle_rows_bits(w, ids, P, L)
     ref = plan.stage_a(ids_d, proj, wd.table, wd.scales)
+    assert np.array_equal(bf16_bits(ref), oracle_bits.reshape(ref.shape))
     uva = plan.stage_a(ids_d, proj, table_host, wd.scales)
     assert torch.equal(ref.view(torch.int16), uva.view(torch.int16))
     n_rows = int(np.sum(L.primes))
     cache = EngramCache(plan, max(1, n_rows // 50), table_host)
     got = cache.stage_a(ids_d, proj, wd.scales)
-    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert np.array_equal(bf16_bits(got), oracle_bits.reshape(got.shape))
     looked, hits, link, cached = cache.stats(reset=True)
     assert looked == ids.size * w.R and hits == 0 and cached == 0 and link == looked
     # LFU: observe a different sample of the same distribution, then serve this batch
@@ -452,7 +455,7 @@ def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
     cached = cache.build()
     assert 0 < cached <= n_rows // 50
     got = cache.stage_a(ids_d, proj, wd.scales)
-    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert np.array_equal(bf16_bits(got), oracle_bits.reshape(got.shape))
     looked, hits, link, _ = cache.stats(reset=True)
     assert looked == ids.size * w.R and 0 < hits < looked and link == looked - hits
     # the most-counted rows of the warm sample are cached: their accesses in it are all hits
@@ -463,7 +466,7 @@ def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
     full.observe(ids_d, proj)
     assert full.build() == len(np.unique(ref_rows(w, ids, P, L)))
     got = full.stage_a(ids_d, proj, wd.scales)
-    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert np.array_equal(bf16_bits(got), oracle_bits.reshape(got.shape))
     looked, hits, link, _ = full.stats()
     assert hits == looked and link == 0
 
@@ -472,7 +475,7 @@ def test_cached_stage_a_equals_uva_and_hbm_gathers(kind):
 def test_dedup_stage_a_fetches_each_row_once(kind):
     """Per-batch dedup: every distinct row of the batch crosses the host link
     once (the oracle's count of distinct rows), every lookup is served from HBM,
-    and the output equals the plain gather bit for bit -- on two batches in a
+    and the output equals the oracle's gathered rows bit for bit -- on two batches in a
     row (the slots are released), with a batch region too small for the batch
     (no dedup then), combined with an LFU cache, and replayed from a CUDA
     graph."""
@@ -487,24 +490,27 @@ def test_dedup_stage_a_fetches_each_row_once(kind):
     n = ids.size * w.R
     for batch in (ids, ids2):
         ids_d = torch.from_numpy(batch).cuda()
+        oracle_bits = oracle_rows_bits(w, batch, P, L)
         ref = plan.stage_a(ids_d, proj, wd.table, wd.scales)
+        assert np.array_equal(bf16_bits(ref), oracle_bits.reshape(ref.shape))
         uniq = len(np.unique(ref_rows(w, batch, P, L)))
         assert uniq < n                                        # Zipf: some rows repeat
         dd = EngramCache(plan, 0, table_host)
         dd.set_dedup(n)
         for _ in range(2):
             got = dd.stage_a(ids_d, proj, wd.scales)
-            assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+            assert np.array_equal(bf16_bits(got), oracle_bits.reshape(got.shape))
             looked, from_hbm, link, cached = dd.stats(reset=True)
             assert (looked, from_hbm, link, cached) == (n, n, uniq, 0)
         # a region too small for the batch: no dedup, every lookup over the link
         dd.set_dedup(n - 1)
         got = dd.stage_a(ids_d, proj, wd.scales)
-        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        assert np.array_equal(bf16_bits(got), oracle_bits.reshape(got.shape))
         assert dd.stats(reset=True) == (n, 0, n, 0)
         dd.close()
     # with the LFU cache: cached rows never cross the link, the others once each
     ids_d = torch.from_numpy(ids).cuda()
+    oracle_bits = oracle_rows_bits(w, ids, P, L)
     ref = plan.stage_a(ids_d, proj, wd.table, wd.scales)
     n_rows = int(np.sum(L.primes))
     both = EngramCache(plan, max(1, n_rows // 50), table_host)
@@ -512,7 +518,7 @@ def test_dedup_stage_a_fetches_each_row_once(kind):
     assert both.build() > 0
     both.set_dedup(n)
     got = both.stage_a(ids_d, proj, wd.scales)
-    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert np.array_equal(bf16_bits(got), oracle_bits.reshape(got.shape))
     looked, from_hbm, link, _ = both.stats(reset=True)
     uniq = len(np.unique(ref_rows(w, ids, P, L)))
     assert looked == n and from_hbm == n and 0 < link < uniq
@@ -534,9 +540,15 @@ def test_dedup_stage_a_fetches_each_row_once(kind):
         out.zero_()
         g.replay()
         torch.cuda.synchronize()
-        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert np.array_equal(bf16_bits(out), oracle_bits.reshape(out.shape))
     assert dd.stats(reset=True)[2] == 2 * uniq
     assert plan.get_error() == (0, 0)
+
+
+def oracle_rows_bits(w, ids, P, L):
+    """The batch's gathered rows as the oracle defines them (Steps 1-4), as bf16 bits."""
+    z = O.hash_heads(O.project(ids, P), L.multipliers, L.primes, w.N, w.K).reshape(-1, w.R)
+    return expected_e_bits(w, z, L)
 
 
 def ref_rows(w, ids, P, L):
