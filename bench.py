@@ -152,7 +152,7 @@ def per_token_work(w, bn: int = 256) -> dict:
 # The sources each kernel is compiled from; a summary's figure is used only
 # while they hash to what was profiled (otherwise the kernel changed: null).
 KERNEL_SOURCES = {
-    "kv_gemm": ["gemm.cu", "gemm_parts.cuh", "ptx.cuh"],
+    "kv_gemm": ["gemm.cu", "gemm_pair.cu", "gemm_parts.cuh", "ptx.cuh"],
     "kv_gemm_fp8": ["gemm.cu", "gemm_parts.cuh", "ptx.cuh"],
     "conv": ["fusion.cu", "conv_parts.cuh", "gate.cuh", "ptx.cuh"],
     "hash_gather": ["gather.cu", "hashing.cuh", "ptx.cuh"],

@@ -185,6 +185,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   p->device = dev;
   p->num_sms = sms;
   p->fused_stage_b = false;
+  p->cta_pairs = false;
 
   PlanDev h{};
   h.R = R;
@@ -352,7 +353,8 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
           cudaSuccess)
         return ENGRAM_ERR_CUDA;
     } else if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
-                                        &n_sl, &pstride, plan->num_sms, &plan->dev->err, s) != cudaSuccess) {
+                                        &n_sl, &pstride, plan->num_sms, &plan->dev->err, s, plan->cta_pairs) !=
+               cudaSuccess) {
       return ENGRAM_ERR_CUDA;
     }
     mark(plan, s);
@@ -690,6 +692,12 @@ engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, in
 engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable) {
   if (!plan || (enable != 0 && enable != 1)) return ENGRAM_ERR_INVALID_ARG;
   plan->fused_stage_b = enable != 0;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_plan_set_cta_pairs(engram_plan_t* plan, int enable) {
+  if (!plan || (enable != 0 && enable != 1)) return ENGRAM_ERR_INVALID_ARG;
+  plan->cta_pairs = enable != 0;
   return ENGRAM_OK;
 }
 

@@ -59,6 +59,7 @@ struct engram_plan {
   bool timing;
   mutable int n_marks;
   bool fused_stage_b;              // Stage B as one cooperative launch where launch_stage_b_fused applies
+  bool cta_pairs;                  // the K/V projection's 256-column tiles on CTA pairs (gemm_pair.cu)
 };
 
 namespace engram {
@@ -165,9 +166,18 @@ cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr,
 // The same GEMM with the Engram epilogue: v (columns [0,d)) to v32 in fp32,
 // gate partial sums of every tile to part (n_sl nodes per quantity, rows
 // pstride floats apart; both returned); k is never stored.
+// cta_pairs: where the tiles are 256 columns wide, run them on CTA pairs
+// (gemm_bf16_engram_pair); the same bits either way.
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
                              const float* g_h, const float* g_k, float* v32, float* part, int* n_sl, int* pstride,
-                             int num_sms, uint32_t* err, cudaStream_t s);
+                             int num_sms, uint32_t* err, cudaStream_t s, bool cta_pairs = false);
+// The same GEMM and epilogue on CTA pairs (tcgen05.mma.cta_group::2, 256 x 256
+// tiles per pair of SMs; gemm_pair.cu): bit-identical results, 256-column
+// slices (n_sl = d / 128).  Applies when Mr >= 256, d % 256 == 0, Kd % 64 == 0.
+bool gemm_pair_applies(int64_t Mr, int d, int Kd);
+cudaError_t gemm_bf16_engram_pair(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
+                                  const float* g_h, const float* g_k, float* v32, float* part, int* n_sl,
+                                  int* pstride, int num_sms, uint32_t* err, cudaStream_t s);
 // The same projection on e4m3 operands: e8 [Mr, Kd] and w8 [(M+1)d, Kd]
 // quantised per row with scales s_e [Mr] and s_w [(M+1)d] (quant.cu); the
 // epilogue multiplies each accumulator by its two scales.  Kd % 128 == 0.

@@ -260,11 +260,14 @@ cudaError_t gemm_bf16_tcgen05(const void* A, const void* B, void* C, int64_t Mr,
 
 cudaError_t gemm_bf16_engram(const void* e, const void* w_kv, int64_t Mr, int d, int M, int Kd, const void* H,
                              const float* g_h, const float* g_k, float* v32, float* part, int* n_sl, int* pstride,
-                             int num_sms, uint32_t* err, cudaStream_t s) {
+                             int num_sms, uint32_t* err, cudaStream_t s, bool cta_pairs) {
   const int Nc = (M + 1) * d;
   if (d % 64 || Kd % 64 || Mr <= 0) return cudaErrorInvalidValue;
   EngramEpilogue epi{v32, part, static_cast<const __nv_bfloat16*>(H), g_h, g_k, d, M, 0, 0, nullptr, nullptr};
   const int bn = pick_bn(Mr, Nc, d, num_sms);
+  // on request, the widest tiles run on CTA pairs: half of B per SM, same bits
+  if (cta_pairs && bn == 256 && gemm_pair_applies(Mr, d, Kd))
+    return gemm_bf16_engram_pair(e, w_kv, Mr, d, M, Kd, H, g_h, g_k, v32, part, n_sl, pstride, num_sms, err, s);
   *n_sl = d / (bn / 2);
   *pstride = (*n_sl * (1 + 3 * M) + 3) / 4 * 4;
   switch (bn) {

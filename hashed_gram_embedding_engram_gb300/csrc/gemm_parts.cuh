@@ -90,8 +90,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 // n_sl = d / (BN/2) slices per row of v (and of each k^(m)), token t has
 // part[t*P + j] = sum v^2 of v slice j, and
 // part[t*P + n_sl + (m*n_sl + j)*3 + {0,1,2}] = (dot, sk, sh) of k^(m) slice j.
-// Rows of part are pstride floats apart (padded to 16 bytes).  Each sum is a
-// sequential fmaf chain over the 32 columns of one tcgen05.ld chunk; a
+// Rows of part are pstride floats apart (padded to 16 bytes).  Within one
+// 32-column tcgen05.ld chunk each sum is four interleaved fmaf chains (column
+// j of the chunk in chain j % 4, so the dependent chains are 8 deep, not 32),
+// combined as (c0 + c1) + (c2 + c3); a
 // slice's chunks are combined as an adjacent pairwise tree, which the gate
 // finalisation continues over the slices (fusion.cu), so the gate's sums have
 // the same bits for every tile width BN.
@@ -140,9 +142,10 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
       dequant_chunk<kF8>(epi, srow, n0 + c, r);
-      float sv = 0.f;
+      float a[4] = {0.f, 0.f, 0.f, 0.f};       // column j of the chunk goes to chain j % 4
 #pragma unroll
-      for (int j = 0; j < 32; ++j) sv = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), sv);
+      for (int j = 0; j < 32; ++j) a[j & 3] = fmaf(__uint_as_float(r[j]), __uint_as_float(r[j]), a[j & 3]);
+      float sv = (a[0] + a[1]) + (a[2] + a[3]);
 #pragma unroll
       for (int k = ci; k & 1; k >>= 1) sv = stk[--top] + sv;
       stk[top++] = sv;
@@ -178,7 +181,7 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
       ptx::tmem_ld_32x32b_x32(t_row + c, r);
       ptx::tmem_ld_wait();
       dequant_chunk<kF8>(epi, srow, n0 + c, r);
-      float dot = 0.f, sk = 0.f, sh = 0.f;
+      float d4[4] = {0.f, 0.f, 0.f, 0.f}, k4[4] = {0.f, 0.f, 0.f, 0.f}, h4[4] = {0.f, 0.f, 0.f, 0.f};
       const uint8_t* hb = eb + (ci >> 1) * 4096 + lane * 128;     // this row of the chunk's 64-column box
       const float4* gh4 = reinterpret_cast<const float4*>(gs + ci * 32);        // shared: broadcast reads
       const float4* gk4 = reinterpret_cast<const float4*>(gs + SW + ci * 32);
@@ -194,11 +197,14 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
         for (int i = 0; i < 8; ++i) {
           const float h = __uint_as_float(i & 1 ? (hw[i >> 1] & 0xFFFF0000u) : (hw[i >> 1] << 16));
           const float k = __uint_as_float(r[q4 * 8 + i]);
-          dot = fmaf(h * g[i], k, dot);
-          sk = fmaf(k, k, sk);
-          sh = fmaf(h, h, sh);
+          d4[i & 3] = fmaf(h * g[i], k, d4[i & 3]);
+          k4[i & 3] = fmaf(k, k, k4[i & 3]);
+          h4[i & 3] = fmaf(h, h, h4[i & 3]);
         }
       }
+      float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+      float sk = (k4[0] + k4[1]) + (k4[2] + k4[3]);
+      float sh = (h4[0] + h4[1]) + (h4[2] + h4[3]);
 #pragma unroll
       for (int k = ci; k & 1; k >>= 1) {
         --top;

@@ -331,6 +331,17 @@ engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, in
  * made after it. */
 engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable);
 
+/* The K/V projection (Step 5, bf16 layers) in 256 x 256 output tiles on CTA
+ * pairs (enable = 1): two SMs of a thread-block cluster share one
+ * tcgen05.mma.cta_group::2 tile, each staging its 128 rows of e and half of
+ * the tile's rows of W_kv, so each SM loads a third less operand data per
+ * FLOP.  Applies where the projection would use 256-column tiles on one SM
+ * (enough tokens to give every SM such a tile: about 2400 or more at
+ * d = 1024) and d is a multiple of 256; the results are the same bits.  The
+ * default (enable = 0) keeps one SM per 128 x 256 tile, which measures faster
+ * on GB300 at 4096 tokens.  enable: 0 or 1; applies to calls made after it. */
+engram_status_t engram_plan_set_cta_pairs(engram_plan_t* plan, int enable);
+
 /* Tracing.  With timing on, engram_forward / engram_stage_b record one of
  * the plan's CUDA events on `stream` before the first kernel and after every
  * kernel they launch.  engram_forward on BF16 layers: hash + gather (Steps

@@ -30,9 +30,10 @@ def layer(w):
     return ids, P, L
 
 
-def forward(w, ids, P, L, fused, timing=False):
+def forward(w, ids, P, L, fused, timing=False, pairs=False):
     plan, weights, proj, H = make_layer(w, L, P, ids.size)
     plan.set_fused_stage_b(fused)
+    plan.set_cta_pairs(pairs)
     if timing:
         plan.set_timing(True)
     plan.forward(torch.from_numpy(ids).cuda(), proj, weights, H)
@@ -48,13 +49,20 @@ def sample_positions(B, T):
 
 # ordered by growing shared memory per block (longer tiles), so a launch that
 # needs more than an earlier shape of the same dilation is covered
-@pytest.mark.parametrize("B,T,dil", [(5, 2, 3), (7, 37, 5), (2, 129, 1), (3, 700, 3), (1, 1000, 8), (1, 4096, 3),
-                                     (16, 2048, 3)])
+# (1, 2600, 3), (3, 900, 3), (1, 4096, 3) and (16, 2048, 3) give the two-launch form's
+# projection 256-column tiles, which can also run on CTA pairs (gemm_pair.cu);
+# 2600 and 2700 rows leave a ragged last pair tile whose second CTA holds no
+# valid row.  The pair form is compared with the same bits.
+@pytest.mark.parametrize("B,T,dil", [(5, 2, 3), (7, 37, 5), (2, 129, 1), (3, 700, 3), (1, 1000, 8), (1, 2600, 3),
+                                     (3, 900, 3), (1, 4096, 3), (16, 2048, 3)])
 def test_fused_stage_b_equals_two_launches_and_oracle(B, T, dil):
     w = BASE.scaled(B=B, T=T, conv_dil=dil)
     ids, P, L = layer(w)
     H_fused, n_fused = forward(w, ids, P, L, True, timing=True)
     H_split, n_split = forward(w, ids, P, L, False, timing=True)
+    H_pairs, n_pairs = forward(w, ids, P, L, False, timing=True, pairs=True)
+    assert n_pairs == n_split
+    assert torch.equal(H_pairs.view(torch.int16), H_split.view(torch.int16))
     # the fused form ran: one traced interval for Stage B; the two-launch form
     # has two, or three with the finalize kernel where its projection tiles are
     # narrower than 256 columns (fewer than one tile of that width per SM)
