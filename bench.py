@@ -38,7 +38,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Engram-layer tokens/s at B=1,T=4096; gather HBM GB/s and % of peak"
-UNIT = "tokens/s"
+# tokens x layers per second: every token passes through each Engram layer of
+# the step; "tokens_per_s" beside it counts each token once per step
+UNIT = "token-layers/s"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -143,6 +145,9 @@ def per_token_work(w, bn: int = 256) -> dict:
         "finalize": ("bytes", 4 * n_part + 8 * w.M),
         # v (fp32), the (scale, alpha) row, H in; H out
         "conv": ("bytes", 4 * w.d + 8 * w.M + 2 * act * w.M * w.d),
+        # one position per sequence: v (fp32) and the gate partials in; H in and out; the ring's
+        # taps at lag > 0 read and the new position's slot written (fp32, per branch)
+        "decode_tail": ("bytes", 4 * w.d + 4 * n_part + 2 * act * w.M * w.d + 4 * w.conv_w * w.M * w.d),
     }
 
 
@@ -182,6 +187,83 @@ def profiled_traffic(kernel: str):
                 if m and m.group(1) == kernel:
                     return int(m.group(2)) if m.group(3) == sources_digest(kernel) else None
     return None
+
+
+# --------------------------------------------------------------------------- #
+# per-kernel device times from the plan's tracing events
+# --------------------------------------------------------------------------- #
+# kernel lists of one engram_forward by the number of traced intervals
+NAME_SETS = {2: ["hash_gather", "stage_b"], 3: ["hash_gather", "kv_gemm", "conv"],
+             4: ["hash_gather", "kv_gemm", "finalize", "conv"]}
+NAME_SETS_FP8 = {4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
+                 5: ["hash_gather", "quantize_e", "kv_gemm_fp8", "finalize", "conv"]}
+NAME_SETS_DECODE = {3: ["hash_gather", "kv_gemm", "decode_tail"]}
+
+
+def trace_kernels(layers, ids, flush, reps: int, w, peaks: dict, fp8: bool = False, decode: bool = False,
+                  table_key=None, sustained: bool = False, bn: int = 256):
+    """Mean device time of each kernel of one engram_forward per layer, over
+    `reps` calls after three untimed ones, each after an L2 flush and behind a
+    GPU sleep (so that every launch is queued before it runs), with the
+    achieved rate against the measured peaks.  Layers with a streaming state
+    run on a copy of it."""
+    import torch
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    tc_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
+    name_sets = NAME_SETS_DECODE if decode else (NAME_SETS_FP8 if fp8 else NAME_SETS)
+    names, dur = None, {}
+    for ly in layers:
+        ly["plan"].set_timing(True)
+    warm = 3                                       # untimed: first launches of each instance, allocations
+    for rep in range(warm + reps):
+        for ly in layers:
+            ly["H"].copy_(ly["H0"])
+            st = ly["state"].clone() if ly.get("state") is not None else None
+            table = ly[table_key] if table_key else ly["weights"].table
+            wts = ly["weights"] if table is ly["weights"].table else dataclass_replace(ly["weights"], table=table)
+            flush.zero_()
+            torch.cuda._sleep(400_000)
+            ly["plan"].forward(ids, ly["proj"], wts, ly["H"], st, ly["ws"])
+            t = ly["plan"].kernel_times()
+            if rep < warm:
+                continue
+            if names is None:
+                names = name_sets[len(t)]
+                dur = {n: [] for n in names}
+            assert len(t) == len(names), t
+            for n, x in zip(names, t):
+                dur[n].append(x)
+    for ly in layers:
+        ly["plan"].set_timing(False)
+    work = per_token_work(w, bn)
+    ntok = ids.numel()
+    kernels = {}
+    for n in names:
+        ms = sum(dur[n]) / len(dur[n])
+        kind, per_tok = work[n]
+        amount = per_tok * ntok
+        if kind == "flops":
+            ach = amount / (ms / 1e3) / 1e12
+            # e4m3 runs at twice the bf16 rate on this part (nominal dense 4.5 vs 2.25 PFLOP/s)
+            pk = tc_peak * (2 if n.endswith("fp8") else 1)
+            kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 2), "unit": "TFLOP/s",
+                          "peak": pk, "frac": round(ach / pk, 4), "bound": "tensor"}
+        else:
+            ach = amount / (ms / 1e3) / 1e9
+            kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 1), "unit": "GB/s",
+                          "peak": hbm_peak, "frac": round(ach / hbm_peak, 4), "bound": "hbm"}
+    total_k = sum(kernels[n]["ms"] for n in names)
+    for n in names:
+        kernels[n]["share"] = round(kernels[n]["ms"] / total_k, 4)
+        # against the nominal figures too: 7.9 TB/s HBM3e, 2.25 PFLOP/s dense bf16 (4.5 e4m3)
+        nominal = 7900.0 if kernels[n]["bound"] == "hbm" else (4500.0 if n.endswith("fp8") else 2250.0)
+        kernels[n]["frac_of_nominal"] = round(kernels[n]["achieved"] / nominal, 4)
+    return kernels, names
+
+
+def dataclass_replace(obj, **kw):
+    import dataclasses
+    return dataclasses.replace(obj, **kw)
 
 
 # --------------------------------------------------------------------------- #
@@ -290,59 +372,11 @@ def run_ours(args) -> None:
         assert st == 0, f"device error flags {flags}"
 
     # ---- per-kernel durations: the plan's tracing events around each kernel of engram_forward ----
-    Kb = min(K, 200)
-    # kernel lists of engram_forward by the number of traced intervals:
-    # Stage B as one launch / projection + conv (gate in the conv) / + finalize
-    name_sets = {2: ["hash_gather", "stage_b"], 3: ["hash_gather", "kv_gemm", "conv"],
-                 4: ["hash_gather", "kv_gemm", "finalize", "conv"]}
-    if fp8:
-        name_sets = {4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
-                     5: ["hash_gather", "quantize_e", "kv_gemm_fp8", "finalize", "conv"]}
-    names = None
-    dur = {}
-    for ly in layers:
-        ly["plan"].set_timing(True)
-    for i in range(Kb):
-        restore()
-        for ly in layers:
-            flush.zero_()
-            torch.cuda._sleep(400_000)   # keep the GPU behind the host: every launch is queued before it runs
-            ly["plan"].forward(ids, ly["proj"], ly["weights"], ly["H"], None, ly["ws"])
-            t = ly["plan"].kernel_times()
-            if names is None:
-                names = name_sets[len(t)]
-                dur = {n: [] for n in names}
-            assert len(t) == len(names), t
-            for n, x in zip(names, t):
-                dur[n].append(x)
-    for ly in layers:
-        ly["plan"].set_timing(False)
+    kernels, names = trace_kernels(layers, ids, flush, min(K, 200), w, peaks, fp8=fp8)
     # kernels per layer in the timed step: Stage A, then Stage B's (the one-launch
     # form is preceded by a one-block kernel that zeroes its counters)
     launches_per_layer = len(names) + (1 if names[-1] == "stage_b" else 0)
     work = per_token_work(w)
-    kernels = {}
-    for n in names:
-        ms = sum(dur[n]) / len(dur[n])
-        kind, per_tok = work[n]
-        amount = per_tok * w.ntok
-        if kind == "flops":
-            ach = amount / (ms / 1e3) / 1e12
-            # e4m3 runs at twice the bf16 rate on this part (nominal dense 4.5 vs 2.25 PFLOP/s)
-            pk = tc_peak * (2 if n.endswith("fp8") else 1)
-            kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 2), "unit": "TFLOP/s",
-                          "peak": pk, "frac": round(ach / pk, 4), "bound": "tensor"}
-        else:
-            ach = amount / (ms / 1e3) / 1e9
-            kernels[n] = {"ms": round(ms, 5), "achieved": round(ach, 1), "unit": "GB/s",
-                          "peak": hbm_peak, "frac": round(ach / hbm_peak, 4), "bound": "hbm"}
-    total_k = sum(kernels[n]["ms"] for n in names)
-    for n in names:
-        kernels[n]["share"] = round(kernels[n]["ms"] / total_k, 4)
-        # against the nominal figures too: 7.9 TB/s HBM3e, 2.25 PFLOP/s dense bf16 (4.5 e4m3)
-        nominal = 7900.0 if kernels[n]["bound"] == "hbm" else (4500.0 if n.endswith("fp8") else 2250.0)
-        kernels[n]["frac_of_nominal"] = round(kernels[n]["achieved"] / nominal, 4)
-
     # ---- the same projection shape through torch.matmul (cuBLAS), for comparison ----
     # e [ntok, d_mem] . W_kv^T in bf16 with a bf16 result (no epilogue), warm and with
     # the L2 flushed before each call, CUDA events on the current stream, each call
@@ -451,10 +485,17 @@ def run_ours(args) -> None:
     except Exception as exc:  # a side measurement: it must never sink the line
         prefetch = {"error": str(exc)[:200]}
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only), on every
+    # core and single-threaded (a 1024-token sample) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         cpu = cpu_baseline_subprocess(w)
+        cpu["single_thread"] = cpu_baseline_subprocess(w, threads=1, T_sample=1024, min_seconds=10.0)
+
+    # ---- the other workloads' lines (N = 1 only) ----
+    others = None
+    if rank == 0 and world == 1 and not args.no_other_workloads and not fp8:
+        others = other_workloads(args)
 
     if rank == 0:
         line = {"metric": METRIC if not fp8 else "Engram-layer tokens/s, prefill_fp8 workload (e4m3 K/V projection)",
@@ -466,14 +507,16 @@ def run_ours(args) -> None:
                                stage_a="every layer's hash+gather on a side stream, ahead of its Stage B"),
                 "roofline": roofline, "kernels": kernels, "torch_matmul_same_shape": torch_matmul,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * launches_per_layer * len(layers), "clocks": clocks,
-                "prefetch": prefetch}
+                "prefetch": prefetch, "tokens_per_s": round(value / len(w.layers), 1)}
+        if others is not None:
+            line["other_workloads"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def prefetch_hiding(ly, ids, e, side, flush, reps: int = 50) -> dict:
+def prefetch_hiding(ly, ids, e, side, flush, reps: int = 50, lookup_fn=None) -> dict:
     """How much of one layer's lookup (Stage A) the work before the layer hides
     when Stage A runs on a side stream beside it.  The stand-in for the layers
     before the Engram layer is one FFN block of the hidden size (x [ntok, d] .
@@ -482,7 +525,8 @@ def prefetch_hiding(ly, ids, e, side, flush, reps: int = 50) -> dict:
     the three interleaved: stand-in, Stage A, Stage B on one stream (serial);
     Stage A on the side stream beside the stand-in, then Stage B (prefetched);
     stand-in then Stage B with the rows already gathered (no lookup).  The
-    hidden fraction is (serial - prefetched) / (serial - no lookup)."""
+    hidden fraction is (serial - prefetched) / (serial - no lookup).
+    ``lookup_fn`` replaces the lookup (e.g. Stage A over the host link)."""
     import statistics
     import torch
     plan, weights, proj = ly["plan"], ly["weights"], ly["proj"]
@@ -499,7 +543,10 @@ def prefetch_hiding(ly, ids, e, side, flush, reps: int = 50) -> dict:
         torch.matmul(torch.matmul(x, w1), w2)
 
     def lookup():
-        plan.stage_a(ids, proj, weights.table, weights.scales, out=e)
+        if lookup_fn is not None:
+            lookup_fn()
+        else:
+            plan.stage_a(ids, proj, weights.table, weights.scales, out=e)
 
     def rest():
         plan.stage_b(e, weights, ly["H"], workspace=ly["ws"])
@@ -597,13 +644,18 @@ def oracle_sample_seconds(T_sample: int, repeats: int = 1, min_seconds: float = 
     return times, T_sample * len(w.layers)
 
 
-def cpu_baseline_subprocess(w) -> dict:
-    """Run the oracle in a child process with a known BLAS thread count."""
-    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+def cpu_baseline_subprocess(w, threads: int = 0, T_sample: int = 0, min_seconds: float = 12.0) -> dict:
+    """Run the oracle in a child process with a known BLAS thread count
+    (0: every core this process may run on) on the first T_sample tokens
+    (0: the whole workload)."""
+    if threads <= 0:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    T_s = T_sample or w.T
     env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
                MKL_NUM_THREADS=str(threads), CUDA_VISIBLE_DEVICES="")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "t, n = bench.oracle_sample_seconds(%d, 3, 12.0); print(json.dumps({'t': t, 'n': n}))") % (ROOT, w.T)
+            "t, n = bench.oracle_sample_seconds(%d, 1, %r); print(json.dumps({'t': t, 'n': n}))") % (
+                ROOT, T_s, min_seconds)
     try:
         r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
         res = json.loads(r.stdout.strip().splitlines()[-1])
@@ -611,10 +663,27 @@ def cpu_baseline_subprocess(w) -> dict:
         return {"value": None, "unit": UNIT, "cores": threads, "kind": "oracle", "error": str(exc)[:200]}
     total = sum(res["t"])
     passes = len(res["t"])
+    what = "full workload" if T_s == w.T else f"first {T_s} tokens of the workload"
     return {"value": round(res["n"] * passes / total, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"full workload ({w.T} tokens x {len(w.layers)} layers) repeated {passes} times "
+            "sample": f"{what} ({T_s} tokens x {len(w.layers)} layers) repeated {passes} times "
                       f"({total:.1f} s of CPU time, mean rate), float64 numpy oracle, BLAS threads = {threads}, "
                       f"input generation excluded"}
+
+
+def other_workloads(args) -> dict:
+    """The other workloads' own lines (decode, int8 host tables, multi-branch),
+    each from a child process on the same GPU with its own step count."""
+    out = {}
+    for name, steps in (("decode_bf16", 300), ("int8_host", 30), ("multibranch_n4", 20)):
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", name, "--steps", str(steps), "--warmup", "3"]
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=1200)
+            lines = [x for x in r.stdout.strip().splitlines() if x.startswith("{")]
+            out[name] = json.loads(lines[-1]) if r.returncode == 0 and lines else {
+                "error": f"exit {r.returncode}: {r.stderr.strip()[-300:]}"}
+        except Exception as exc:  # a side measurement: it must never sink the line
+            out[name] = {"error": str(exc)[:300]}
+    return out
 
 
 def run_reference(args) -> None:
@@ -752,12 +821,34 @@ def run_workload(args) -> None:
     tokens_per_step = w.ntok * len(w.layers)
     value = tokens_per_step / (ms / 1e3)
     extra = {}
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    # per-kernel device times (tables in HBM; the multi-branch projection sits inside a
+    # milliseconds-long step, so it is compared with the sustained bf16 peak)
+    big = w.name == "multibranch_n4"
+    kern, knames = trace_kernels(layers, ids, flush, min(args.steps, 20 if big else 100), w, peaks, fp8=fp8,
+                                 decode=decode, table_key="table_dev" if w.table_in_host else None,
+                                 sustained=big, bn=64 if decode else 256)
+    extra["kernels"] = kern
+    extra["peaks"] = {"hbm_gbs": peaks.get("hbm_gbs"), "bf16_tflops": peaks.get("bf16_tflops"),
+                      "bf16_tflops_sustained": peaks.get("bf16_tflops_sustained"),
+                      "source": "MEASURED_PEAKS.json" if peaks else "fallback"}
     if decode:
         rows = w.B * w.R * len(w.layers)
+        # the bytes a decode step must move: per layer W_kv once, the table rows, H in and out,
+        # the ring's taps and the new slot, v and the gate partials through the tail
+        wt = per_token_work(w, 64)
+        w_bytes = (w.M + 1) * w.d * w.d_mem * 2
+        step_bytes = len(w.layers) * (w_bytes + w.B * (wt["hash_gather"][1] + wt["decode_tail"][1]))
+        hbm = peaks.get("hbm_gbs", 6800.0)
         extra["decode"] = {"us_per_step": round(ms * 1e3, 2), "table_rows_per_step": rows,
                            "table_rows_per_s": round(rows / (ms / 1e3), 1),
+                           "bytes_per_step": step_bytes,
+                           "hbm_roofline_us": round(step_bytes / (hbm * 1e9) * 1e6, 3),
+                           "frac_of_hbm_roofline": round(step_bytes / (hbm * 1e9) / (ms / 1e3), 4),
                            "note": f"{w.B} sequences, one new token each after a {w.prefix_len}-token prefix, "
-                                   f"state carried between steps"}
+                                   f"state carried between steps; the roofline counts W_kv ({w_bytes} B per "
+                                   f"layer), the table rows, H in and out and the conv ring"}
     if w.table_in_host:
         ms_hbm = timed("table_dev")
         # the gather alone over UVA: the host link carries the rows, the scales stay in HBM
@@ -783,6 +874,16 @@ def run_workload(args) -> None:
         c1.record()
         c1.synchronize()
         h2d = 5 * (1 << 28) / (c0.elapsed_time(c1) / 1e3) / 1e9
+        del host, devb
+        # per-kernel times with the rows read over the host link: the gather's bytes over the
+        # link (the int8 rows; scales, ids and P stay in HBM) against the pinned copy rate
+        kern_uva, _ = trace_kernels(layers, ids, flush, min(args.steps, 50), w, peaks, table_key="table_host")
+        link_bytes = w.ntok * w.R * w.row_dim
+        g_uva = kern_uva["hash_gather"]
+        g_uva["host_link_bytes"] = link_bytes
+        g_uva["host_link_gbs"] = round(link_bytes / (g_uva["ms"] / 1e3) / 1e9, 1)
+        g_uva["frac_of_h2d_copy"] = round(g_uva["host_link_gbs"] / h2d, 4)
+        extra["kernels_uva"] = kern_uva
         # HBM hot-row cache: LFU over a different sample of the same token distribution
         from hashed_gram_embedding_engram_gb300 import EngramCache
         from workloads import token_stream
@@ -800,6 +901,25 @@ def run_workload(args) -> None:
             looked += a_
             hits += b_
             link += l_
+        # the lookup that Stage A prefetch is meant to hide: over the host link, plain and
+        # through the hot-row cache, beside a stand-in for the layers before the Engram layer
+        ly0 = layers[0]
+        side_pf = torch.cuda.Stream()
+        pf = {}
+        for name, look in (("uva", lambda ly=ly0: ly["plan"].stage_a(ids, ly["proj"], ly["table_host"],
+                                                                      ly["weights"].scales, out=ly["e"])),
+                           ("uva_hot_row_cache", lambda ly=ly0: ly["cache"].stage_a(ids, ly["proj"],
+                                                                                    ly["weights"].scales,
+                                                                                    out=ly["e"])),
+                           ("hbm", lambda ly=ly0: ly["plan"].stage_a(ids, ly["proj"], ly["table_dev"],
+                                                                      ly["weights"].scales, out=ly["e"]))):
+            try:
+                pf[name] = prefetch_hiding(ly0, ids, ly0["e"], side_pf, flush, reps=20, lookup_fn=look)
+            except Exception as exc:  # a side measurement: it must never sink the line
+                pf[name] = {"error": str(exc)[:200]}
+        for ly in layers:
+            ly["cache"].stats(reset=True)
+        extra["prefetch"] = pf
         # per-batch row dedup: each distinct row of a batch crosses the link once
         # (alone, then together with the hot-row cache)
         for ly in layers:
@@ -876,6 +996,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the decode, int8 host-table and multi-branch lines embedded in the default run")
     ap.add_argument("--workload", default="prefill_bf16",
                     help="prefill_bf16 (the headline line); prefill_fp8 (the same with the e4m3 K/V "
                          "projection), decode_bf16, int8_host or multibranch_n4 print that workload's own line")

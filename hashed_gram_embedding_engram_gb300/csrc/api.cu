@@ -33,7 +33,8 @@ engram_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ENGRAM_OK
 // Resolve a pointer the kernels will dereference.  Device and managed memory
 // are used as is; pinned or registered host memory through its device alias;
 // pageable host memory is refused.
-engram_status_t device_view(const void* ptr, const void** out) {
+engram_status_t device_view(const void* ptr, const void** out, bool* on_host = nullptr) {
+  if (on_host) *on_host = false;
   cudaPointerAttributes a;
   cudaError_t e = cudaPointerGetAttributes(&a, ptr);
   if (e != cudaSuccess) {
@@ -48,6 +49,7 @@ engram_status_t device_view(const void* ptr, const void** out) {
     case cudaMemoryTypeHost:
       if (a.devicePointer == nullptr) return ENGRAM_ERR_NOT_MAPPED;
       *out = a.devicePointer;
+      if (on_host) *on_host = true;
       return ENGRAM_OK;
     default:
       return ENGRAM_ERR_NOT_MAPPED;
@@ -281,14 +283,16 @@ engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, in
   const bool i8 = plan->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
   if (i8 != (scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
   const void* tab = nullptr;
-  if (engram_status_t s = device_view(table, &tab)) return s;
+  bool host = false;
+  if (engram_status_t s = device_view(table, &tab, &host)) return s;
   if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
   const void* sc = nullptr;
   if (i8) {
     if (engram_status_t s = device_view(scales, &sc)) return s;
   }
   return cuda_status(engram::launch_hash_gather(plan, ids, B, T, proj, V, prev_ids, tab,
-                                                static_cast<const uint16_t*>(sc), e_out, (cudaStream_t)stream));
+                                                static_cast<const uint16_t*>(sc), e_out, (cudaStream_t)stream,
+                                                host));
 }
 
 engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok, const void* w_kv,
@@ -434,7 +438,8 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return ENGRAM_ERR_WORKSPACE;
   const void* tab = nullptr;
-  if (engram_status_t s = device_view(w->table, &tab)) return s;
+  bool host = false;
+  if (engram_status_t s = device_view(w->table, &tab, &host)) return s;
   if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
   const void* sc = nullptr;
   if (w->scales) {
@@ -444,8 +449,8 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   const int32_t* prev = state ? state->prev_ids : nullptr;
   plan->n_marks = 0;
   mark(plan, s);
-  if (engram::launch_hash_gather(plan, ids, B, T, proj, V, prev, tab, static_cast<const uint16_t*>(sc), ws.e, s) !=
-      cudaSuccess)
+  if (engram::launch_hash_gather(plan, ids, B, T, proj, V, prev, tab, static_cast<const uint16_t*>(sc), ws.e, s,
+                                 host) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
   return run_stage_b(plan, ws, ws.e, ids, proj, V, B, T, w, H, state, s);
 }
@@ -457,6 +462,7 @@ struct engram_cache {
   int64_t capacity;
   int row_bytes;
   const void* table;                 // device view of the table
+  bool table_on_host = false;        // pinned or registered host memory (rows cross the host link)
   uint32_t* counts;                  // [total rows]
   int32_t* slot;                     // [total rows]
   void* rows;                        // [capacity + batch_cap, row_bytes]: cached rows, then the dedup region
@@ -480,11 +486,13 @@ engram_status_t engram_cache_create(const engram_plan_t* plan, int64_t capacity,
   *out = nullptr;
   if (capacity < 0 || capacity > plan->total_rows || capacity > INT32_MAX) return ENGRAM_ERR_INVALID_ARG;
   const void* tab = nullptr;
-  if (engram_status_t s = device_view(table, &tab)) return s;
+  bool host = false;
+  if (engram_status_t s = device_view(table, &tab, &host)) return s;
   if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
   engram_cache* c = new (std::nothrow) engram_cache();
   if (!c) return ENGRAM_ERR_CUDA;
   c->plan = plan;
+  c->table_on_host = host;
   c->capacity = capacity;
   c->row_bytes = static_cast<int>(plan->cfg.row_dim * table_elem_bytes(plan->cfg.table_dtype));
   c->table = tab;
@@ -604,8 +612,10 @@ engram_status_t engram_stage_a_cached(const engram_cache_t* c, const int32_t* id
         engram::dedup_fetch(plan, lookups, c->batch_rows, c->row_bytes, c->table, region, s) != cudaSuccess)
       return ENGRAM_ERR_CUDA;
   }
+  // with the dedup every lookup is served from HBM; otherwise the misses cross the host link
   if (engram::launch_hash_gather_cached(plan, ids, B, T, proj, V, prev_ids, c->table, static_cast<const uint16_t*>(sc),
-                                        e_out, c->slot, c->rows, c->stats, s) != cudaSuccess)
+                                        e_out, c->slot, c->rows, c->stats, s, c->table_on_host && !dedup) !=
+      cudaSuccess)
     return ENGRAM_ERR_CUDA;
   if (dedup && engram::dedup_release(plan, lookups, c->batch_rows, c->slot, c->stats + 3, s) != cudaSuccess)
     return ENGRAM_ERR_CUDA;

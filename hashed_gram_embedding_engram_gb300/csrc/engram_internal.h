@@ -103,14 +103,18 @@ cudaError_t launch_hash(const engram_plan* p, const int32_t* ids, int B, int T, 
 cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
                           const uint16_t* scales, void* e, cudaStream_t s);
 // Steps 1-4 fused: indices computed per row inside the gather, never stored.
+// host_table: the rows are read from pinned host memory over the host link;
+// the grid then holds a share of the SMs sized for the link (one 1024-thread
+// block on each of hostgrid_sms SMs), leaving the rest to concurrent work (the
+// Stage-A prefetch beside earlier layers).
 cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                                const int32_t* prev_ids, const void* table, const uint16_t* scales, void* e,
-                               cudaStream_t s);
+                               cudaStream_t s, bool host_table = false);
 // The same through the HBM hot-row cache (slot map, cached rows, [lookups, hits] counters).
 cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj,
                                       int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,
                                       void* e, const int32_t* slot, const void* rows, unsigned long long* stats,
-                                      cudaStream_t s);
+                                      cudaStream_t s, bool host_table = false);
 // Hot-row cache maintenance (cache.cu).
 cudaError_t cache_observe(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                           const int32_t* prev_ids, uint32_t* counts, cudaStream_t s);

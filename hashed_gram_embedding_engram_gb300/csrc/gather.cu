@@ -97,7 +97,55 @@ __device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
-// One warp per token.  Row phase: lane r (and r + 32) owns row r of the
+// 32-bit loads through the non-coherent path, kept in program order with the
+// row loads (asm volatile), so the next token's id and projection loads are
+// issued exactly where the pipeline below places them.
+__device__ __forceinline__ int32_t ld_nc_s32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// The warp's view of one token's n-gram window, in two memory hops: the raw
+// id (or the projected id from `prev`, or the pad), then its projection.
+struct WindowHop {
+  int32_t v;        // raw id (need_proj) or the projected id itself
+  bool need_proj;
+};
+
+__device__ __forceinline__ WindowHop window_hop1(const int32_t* __restrict__ ids, const int32_t* __restrict__ prev,
+                                                 int64_t tok, int T, int N, int V, int lane, bool& bad) {
+  WindowHop h{0, false};
+  if (lane < N) {
+    const int b = static_cast<int>(tok / T);
+    const int t = static_cast<int>(tok - static_cast<int64_t>(b) * T);
+    const int tt = t - lane;                           // lane i: x'_{t-i}, pad 0 before the start
+    if (tt >= 0) {
+      int raw = ld_nc_s32(ids + static_cast<int64_t>(b) * T + tt);
+      if (static_cast<unsigned>(raw) >= static_cast<unsigned>(V)) {
+        bad = true;
+        raw = 0;
+      }
+      h.v = raw;
+      h.need_proj = true;
+    } else if (prev != nullptr) {
+      h.v = ld_nc_s32(prev + static_cast<int64_t>(b) * (N - 1) + (N - 1) + tt);
+    }
+  }
+  return h;
+}
+
+__device__ __forceinline__ int32_t window_hop2(const WindowHop& h, const int32_t* __restrict__ proj) {
+  return h.need_proj ? ld_nc_s32(proj + h.v) : h.v;
+}
+
+// Each warp walks its tokens tok, tok + n_warps, ... as a two-stage software
+// pipeline: while one token's table rows are in flight, the next token's
+// n-gram window is fetched (its raw ids before the row loads are issued, their
+// projections right after), so a warp's consecutive tokens overlap their
+// dependent memory round trips instead of paying them one after another.
+//
+// Per token (one warp).  Row phase: lane r (and r + 32) owns row r of the
 // token -- its index (computed from the n-gram window, or read), its source
 // address (table, or the HBM cache) and its int8 scale -- so each row's index
 // is computed once.  Chunk phase: lane l takes the token's 16-byte chunks
@@ -108,8 +156,11 @@ __device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
 // copy of the parameter block, read before the dependency wait (they are
 // written at plan creation only).
 // kWide: R > 32, two rows per lane.
-template <int kCpr, bool kInt8, bool kHash, bool kCache = false, bool kWide = false>
-__global__ void __launch_bounds__(kThreads, 8)
+// kBlk: threads per block -- 128 (eight blocks per SM), or 1024 for tables in
+// host memory, so that a grid of hostgrid_sms blocks holds that many whole SMs
+// and leaves the others to the work running beside the lookup.
+template <int kCpr, bool kInt8, bool kHash, bool kCache = false, bool kWide = false, int kBlk = kThreads>
+__global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
     row_gather_kernel(const PlanDev* __restrict__ pdg, int R, int N, int K, uint32_t* __restrict__ err,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ ids, int T,
                       const int32_t* __restrict__ proj, int V, const int32_t* __restrict__ prev, int64_t ntok,
@@ -134,29 +185,37 @@ __global__ void __launch_bounds__(kThreads, 8)
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   bool bad = false;
   uint32_t n_look = 0, n_hit = 0;                       // this lane's rows (kCache)
-  for (int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < ntok;
-       tok += n_warps) {
+  int64_t tok = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // pipeline state: the current token's projected window id (kHash) or row index (read)
+  int32_t x_cur = 0;
+  int32_t z_cur[kRows] = {};
+  if (tok < ntok) {
+    if constexpr (kHash) {
+      x_cur = window_hop2(window_hop1(ids, prev, tok, T, N, V, lane, bad), proj);
+    } else {
+      if (has0) z_cur[0] = ld_nc_s32(idx + tok * R + lane);
+      if (kWide && has1) z_cur[kRows - 1] = ld_nc_s32(idx + tok * R + lane + 32);
+    }
+  }
+  for (; tok < ntok; tok += n_warps) {
+    const int64_t tn = tok + n_warps;
+    const bool more = tn < ntok;
+    // next token, first hop (raw ids, or its row indices)
+    WindowHop hop{0, false};
+    int32_t z_next[kRows] = {};
+    if (more) {
+      if constexpr (kHash) {
+        hop = window_hop1(ids, prev, tn, T, N, V, lane, bad);
+      } else {
+        if (has0) z_next[0] = ld_nc_s32(idx + tn * R + lane);
+        if (kWide && has1) z_next[kRows - 1] = ld_nc_s32(idx + tn * R + lane + 32);
+      }
+    }
     uint32_t xp[kMaxN];                                // projected ids: non-negative int32
     if constexpr (kHash) {
-      const int b = static_cast<int>(tok / T);
-      const int t = static_cast<int>(tok - static_cast<int64_t>(b) * T);
-      int32_t x = 0;                                   // lane i: x'_{t-i}, pad 0 before the start
-      if (lane < N) {
-        const int tt = t - lane;
-        if (tt >= 0) {
-          int raw = __ldg(ids + static_cast<int64_t>(b) * T + tt);
-          if (static_cast<unsigned>(raw) >= static_cast<unsigned>(V)) {
-            bad = true;
-            raw = 0;
-          }
-          x = __ldg(proj + raw);
-        } else if (prev != nullptr) {
-          x = __ldg(prev + static_cast<int64_t>(b) * (N - 1) + (N - 1) + tt);
-        }
-      }
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i)
-        if (i < N) xp[i] = static_cast<uint32_t>(__shfl_sync(0xFFFFFFFFu, x, i));
+        if (i < N) xp[i] = static_cast<uint32_t>(__shfl_sync(0xFFFFFFFFu, x_cur, i));
     }
     // ---- row phase: index, source and scale of rows lane and lane + 32
     uint64_t src[kRows] = {};                          // 0: the row is out of range (zero output)
@@ -166,7 +225,6 @@ __global__ void __launch_bounds__(kThreads, 8)
       const bool has = h == 0 ? has0 : has1;
       if (!has) continue;
       const RowConst& c = rc[h];
-      const int r = lane + 32 * h;
       uint32_t z;
       if constexpr (kHash) {
         uint64_t hsh = 0;
@@ -175,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 8)
           if (i < c.n) hsh ^= static_cast<uint64_t>(xp[i]) * __ldg(c.mult + i);
         z = barrett_mod(hsh, c.prime, c.mu);
       } else {
-        z = static_cast<uint32_t>(__ldg(idx + tok * R + r));
+        z = static_cast<uint32_t>(z_cur[h]);
         if (z >= c.prime) {
           bad = true;
           continue;
@@ -219,6 +277,12 @@ __global__ void __launch_bounds__(kThreads, 8)
         v[j] = ok[j] ? ld_stream_16(reinterpret_cast<const uint8_t*>(sp) + c * 16) : make_uint4(0, 0, 0, 0);
         s_[j] = sj;
       }
+      if (f0 == 0) {
+        // next token, second hop, while this token's rows are in flight
+        if constexpr (kHash) {
+          if (more) x_cur = window_hop2(hop, proj);
+        }
+      }
 #pragma unroll
       for (int j = 0; j < kWarpItems; ++j) {
         const int f = f0 + j * 32 + lane;
@@ -233,6 +297,10 @@ __global__ void __launch_bounds__(kThreads, 8)
           }
         }
       }
+    }
+    if constexpr (!kHash) {
+#pragma unroll
+      for (int h = 0; h < kRows; ++h) z_cur[h] = z_next[h];
     }
   }
   if (bad) atomicOr(err, kErrIndexRange);
@@ -249,10 +317,18 @@ __global__ void __launch_bounds__(kThreads, 8)
   }
 }
 
-int grid_for_tokens(const engram_plan* p, int64_t ntok) {
-  const int64_t warps_per_block = kThreads / 32;
+// SMs a gather over the host link occupies: one 1024-thread block each.  An
+// SM keeps 32 warps' row loads in flight (a token's rows each, the next
+// token's window behind them), so a quarter of the SMs already carries the
+// ~200 GB/s the link delivers (NVLink-C2C, as measured with pinned copies);
+// the rest stay free for work that runs beside the lookup.
+constexpr int kHostBlk = 1024;
+int hostgrid_sms(int num_sms) { return num_sms / 4 > 0 ? num_sms / 4 : 1; }
+
+int grid_for_tokens(const engram_plan* p, int64_t ntok, bool host_table = false) {
+  const int64_t warps_per_block = (host_table ? kHostBlk : kThreads) / 32;
   int64_t blocks = (ntok + warps_per_block - 1) / warps_per_block;
-  const int64_t cap = static_cast<int64_t>(p->num_sms) * 8;
+  const int64_t cap = host_table ? hostgrid_sms(p->num_sms) : static_cast<int64_t>(p->num_sms) * 8;
   if (blocks > cap) blocks = cap;
   return static_cast<int>(blocks);
 }
@@ -270,10 +346,14 @@ cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, c
 
 template <int kCpr, bool kInt8>
 cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                         const int32_t* prev, const void* table, const uint16_t* scales, void* e, cudaStream_t s) {
+                         const int32_t* prev, const void* table, const uint16_t* scales, void* e, cudaStream_t s,
+                         bool host_table) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
   auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, false, true> : row_gather_kernel<kCpr, kInt8, true>;
-  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+  if (host_table)
+    k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, false, true, kHostBlk>
+                  : row_gather_kernel<kCpr, kInt8, true, false, false, kHostBlk>;
+  return launch_pdl(k, dim3(grid_for_tokens(p, ntok, host_table)), dim3(host_table ? kHostBlk : kThreads), 0, s,
                     p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T,
                     proj, V, prev, ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
@@ -283,10 +363,13 @@ cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T,
 template <int kCpr, bool kInt8>
 cudaError_t launch_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                           const int32_t* prev, const void* table, const uint16_t* scales, void* e,
-                          const RowCache& cache, cudaStream_t s) {
+                          const RowCache& cache, cudaStream_t s, bool host_table) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
   auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, true, true> : row_gather_kernel<kCpr, kInt8, true, true>;
-  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
+  if (host_table)
+    k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, true, true, kHostBlk>
+                  : row_gather_kernel<kCpr, kInt8, true, true, false, kHostBlk>;
+  return launch_pdl(k, dim3(grid_for_tokens(p, ntok, host_table)), dim3(host_table ? kHostBlk : kThreads), 0, s,
                     p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T,
                     proj, V, prev, ntok,
                     static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
@@ -320,9 +403,9 @@ cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok
 
 cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                                const int32_t* prev_ids, const void* table, const uint16_t* scales, void* e,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool host_table) {
   const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
-#define CALL(C, I) launch_fused<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, s)
+#define CALL(C, I) launch_fused<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, s, host_table)
   ENGRAM_DISPATCH_CPR(CALL)
 #undef CALL
 }
@@ -330,10 +413,10 @@ cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, 
 cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj,
                                       int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,
                                       void* e, const int32_t* slot, const void* rows, unsigned long long* stats,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, bool host_table) {
   const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
   const RowCache cache{slot, static_cast<const uint8_t*>(rows), stats};
-#define CALL(C, I) launch_cached<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, cache, s)
+#define CALL(C, I) launch_cached<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, cache, s, host_table)
   ENGRAM_DISPATCH_CPR(CALL)
 #undef CALL
 }
