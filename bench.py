@@ -127,6 +127,15 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 def per_token_work(w, bn: int = 256) -> dict:
     """Algorithmic bytes (or flops) per token per layer of each kernel engram_forward launches."""
+    work = _per_token_work(w, bn)
+    # the one-launch decode step (T = 1): the gather's and the tail's bytes, and W_kv once per
+    # step shared by the batch's B tokens
+    w_kv_bytes = (w.M + 1) * w.d * w.d_mem * (2 if w.act_dtype == "bf16" else 4)
+    work["decode_step"] = ("bytes", work["hash_gather"][1] + work["decode_tail"][1] + w_kv_bytes // max(1, w.B))
+    return work
+
+
+def _per_token_work(w, bn: int) -> dict:
     act = 2 if w.act_dtype == "bf16" else 4
     row_bytes = w.row_dim * {"f32": 4, "bf16": 2, "i8": 1}[w.table_dtype]
     nc = (w.M + 1) * w.d
@@ -197,7 +206,7 @@ NAME_SETS = {2: ["hash_gather", "stage_b"], 3: ["hash_gather", "kv_gemm", "conv"
              4: ["hash_gather", "kv_gemm", "finalize", "conv"]}
 NAME_SETS_FP8 = {4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
                  5: ["hash_gather", "quantize_e", "kv_gemm_fp8", "finalize", "conv"]}
-NAME_SETS_DECODE = {3: ["hash_gather", "kv_gemm", "decode_tail"]}
+NAME_SETS_DECODE = {1: ["decode_step"], 3: ["hash_gather", "kv_gemm", "decode_tail"]}
 
 
 def trace_kernels(layers, ids, flush, reps: int, w, peaks: dict, fp8: bool = False, decode: bool = False,
@@ -766,6 +775,11 @@ def run_workload(args) -> None:
     side = torch.cuda.Stream()
 
     def step(table_key=None):
+        if table_key == "fused_decode":
+            # one new token per sequence: each layer's whole step (gather, projection, tail) as one launch
+            for ly in layers:
+                ly["plan"].forward(ids, ly["proj"], ly["weights"], ly["H"], ly["state"], ly["ws"])
+            return
         main = torch.cuda.current_stream()
         side.wait_stream(main)
         ready = []
@@ -849,6 +863,16 @@ def run_workload(args) -> None:
                            "note": f"{w.B} sequences, one new token each after a {w.prefix_len}-token prefix, "
                                    f"state carried between steps; the roofline counts W_kv ({w_bytes} B per "
                                    f"layer), the table rows, H in and out and the conv ring"}
+        # the same step with each layer as one cooperative launch (gather, projection, tail)
+        for ly in layers:
+            ly["plan"].set_fused_decode(True)
+        ms_fused = timed("fused_decode", K=min(args.steps, 200))
+        kern_fused, _ = trace_kernels(layers, ids, flush, min(args.steps, 100), w, peaks, decode=True, bn=64)
+        for ly in layers:
+            ly["plan"].set_fused_decode(False)
+        extra["decode"]["one_launch_per_layer"] = {
+            "us_per_step": round(ms_fused * 1e3, 2), "kernels": kern_fused,
+            "what": "engram_plan_set_fused_decode(1): each layer's step one cooperative launch, Stage A inside it"}
     if w.table_in_host:
         ms_hbm = timed("table_dev")
         # the gather alone over UVA: the host link carries the rows, the scales stay in HBM

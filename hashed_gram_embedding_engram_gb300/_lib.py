@@ -19,7 +19,7 @@ F32, BF16, I8_ROWSCALE_F16 = 0, 1, 2
 EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", "engram_plan_workspace_bytes",
            "engram_hash", "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward",
            "engram_get_error", "engram_plan_set_timing", "engram_plan_set_fused_stage_b", "engram_plan_set_cta_pairs",
-           "engram_plan_kernel_times",
+           "engram_plan_set_fused_decode", "engram_plan_kernel_times",
            "engram_forward_static_scratch", "engram_stage_a", "engram_cache_create", "engram_cache_destroy",
            "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats",
            "engram_cache_set_dedup", "engram_quantize_fp8")
@@ -89,6 +89,7 @@ def _lib() -> ctypes.CDLL:
         lib.engram_plan_set_timing.argtypes = [vp, i32]
         lib.engram_plan_set_fused_stage_b.argtypes = [vp, i32]
         lib.engram_plan_set_cta_pairs.argtypes = [vp, i32]
+        lib.engram_plan_set_fused_decode.argtypes = [vp, i32]
         lib.engram_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
         for name in EXPORTS:
             if name != "engram_status_string":

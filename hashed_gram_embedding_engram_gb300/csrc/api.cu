@@ -188,6 +188,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   p->num_sms = sms;
   p->fused_stage_b = false;
   p->cta_pairs = false;
+  p->fused_decode = false;
 
   PlanDev h{};
   h.R = R;
@@ -325,6 +326,17 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     sv = static_cast<int64_t>(M + 1) * d;
   } else {
     const bool f8 = w->w_kv_fp8 != nullptr;
+    if (!f8 && plan->fused_decode && engram::decode_fused_applies(plan, T)) {
+      // one position per sequence, rows already gathered: projection and tail as one cooperative launch
+      const cudaError_t de =
+          engram::launch_decode_fused(plan, ids, B, proj, V, nullptr, nullptr, e, false, w, H, state, ws, s);
+      if (de == cudaSuccess) {
+        mark(plan, s);
+        return ENGRAM_OK;
+      }
+      if (de != cudaErrorCooperativeLaunchTooLarge) return ENGRAM_ERR_CUDA;
+      (void)cudaGetLastError();
+    }
     cudaError_t fe = cudaErrorNotSupported;
     if (!f8 && plan->fused_stage_b && engram::stage_b_fused_applies(plan, ntok, T)) {
       // projection and conv in one cooperative launch (after a one-block kernel zeroing its counters)
@@ -449,6 +461,17 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   const int32_t* prev = state ? state->prev_ids : nullptr;
   plan->n_marks = 0;
   mark(plan, s);
+  if (plan->fused_decode && w->w_kv_fp8 == nullptr && engram::decode_fused_applies(plan, T)) {
+    // one position per sequence: the whole layer as one cooperative launch
+    const cudaError_t de = engram::launch_decode_fused(plan, ids, B, proj, V, tab, static_cast<const uint16_t*>(sc),
+                                                       ws.e, true, w, H, state, ws, s);
+    if (de == cudaSuccess) {
+      mark(plan, s);
+      return ENGRAM_OK;
+    }
+    if (de != cudaErrorCooperativeLaunchTooLarge) return ENGRAM_ERR_CUDA;
+    (void)cudaGetLastError();     // fewer co-resident blocks than SMs (e.g. a partitioned device): three launches
+  }
   if (engram::launch_hash_gather(plan, ids, B, T, proj, V, prev, tab, static_cast<const uint16_t*>(sc), ws.e, s,
                                  host) != cudaSuccess)
     return ENGRAM_ERR_CUDA;
@@ -702,6 +725,12 @@ engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, in
 engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable) {
   if (!plan || (enable != 0 && enable != 1)) return ENGRAM_ERR_INVALID_ARG;
   plan->fused_stage_b = enable != 0;
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_plan_set_fused_decode(engram_plan_t* plan, int enable) {
+  if (!plan || (enable != 0 && enable != 1)) return ENGRAM_ERR_INVALID_ARG;
+  plan->fused_decode = enable != 0;
   return ENGRAM_OK;
 }
 

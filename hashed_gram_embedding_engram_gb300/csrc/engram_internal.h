@@ -60,6 +60,7 @@ struct engram_plan {
   mutable int n_marks;
   bool fused_stage_b;              // Stage B as one cooperative launch where launch_stage_b_fused applies
   bool cta_pairs;                  // the K/V projection's 256-column tiles on CTA pairs (gemm_pair.cu)
+  bool fused_decode;               // chunks of one position as one cooperative launch (decode.cu)
 };
 
 namespace engram {
@@ -217,6 +218,20 @@ cudaError_t launch_stage_b_fused(const engram_plan* p, const void* e, const void
                                  const float* g_h, const float* g_k, const float* g_c, const float* conv, float* v32,
                                  float* part, float* sa_out, const engram_state_t* state, uint32_t* sync,
                                  cudaStream_t s);
+// Zero n words of device memory (one block, stream-ordered, programmatic
+// dependent launch: it waits for the previous kernel before writing).
+cudaError_t launch_zero_words(uint32_t* p, int n, cudaStream_t s);
+// A whole decode step (chunks of one position, T = 1) of a bf16 layer with
+// R <= 32 and conv_w = 4 as one cooperative launch (decode.cu): the gather
+// (unless do_gather is false and e already holds the rows), the K/V
+// projection in 128 x 64 tiles with its gate epilogue, and the decode tail,
+// linked by counters in ws.sync.  Bit-identical to the gather + projection +
+// decode tail launches.
+bool decode_fused_applies(const engram_plan* p, int T);
+cudaError_t launch_decode_fused(const engram_plan* p, const int32_t* ids, int B, const int32_t* proj, int V,
+                                const void* table, const uint16_t* scales, const void* e, bool do_gather,
+                                const engram_weights_t* w, void* H, const engram_state_t* state,
+                                const Workspace& ws, cudaStream_t s);
 // fp32 GEMM on the CUDA cores, same shapes.
 cudaError_t gemm_f32_simt(const float* A, const float* B, float* C, int64_t Mr, int Nc, int Kd, cudaStream_t s);
 

@@ -39,80 +39,12 @@
 #include "engram_internal.h"
 #include "gate.cuh"
 #include "ptx.cuh"
+#include "tail_parts.cuh"
 
 namespace engram {
 namespace {
 
 using namespace cv;
-
-// ------------------------------------------------------------------ gate (bf16 layers: from partials)
-// Sum over a warp of the n values p[i * stride], i < n, as the adjacent
-// pairwise tree: lane l sums its aligned block [l*q, l*q + q) pairwise (zeros
-// past n), then the butterfly pairs lanes at distances 1, 2, ..., 16.  With
-// q a power of two the result is the tree sum over the values zero-padded to
-// a power of two, whatever q is -- so slices that are themselves pairwise
-// sums of aligned 32-column chunks (gemm.cu) give the same bits for every
-// GEMM tile width.  Every lane returns the same value.
-__device__ __forceinline__ float pairwise_warp_sum(const float* p, int stride, int n, int q, int lane) {
-  float x;
-  if (q == 1) {
-    x = lane < n ? __ldg(p + static_cast<int64_t>(lane) * stride) : 0.f;
-  } else {
-    float stk[12];
-    int top = 0;
-    for (int i = 0; i < q; ++i) {
-      const int j = lane * q + i;
-      float y = j < n ? __ldg(p + static_cast<int64_t>(j) * stride) : 0.f;
-      for (int k = i; k & 1; k >>= 1) y = stk[--top] + y;
-      stk[top++] = y;
-    }
-    x = stk[0];
-  }
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-  return x;
-}
-
-// One warp per token: part[0, n_sl) = sum v^2 nodes, part[n_sl + (m*n_sl + j)*3
-// + {0,1,2}] = (h.g_h.g_k.k, k^2, h^2) nodes of branch m -> the sa row.  Up to
-// 32 nodes (one per lane) the four sums of a branch are loaded together.
-// One token's gate scalars from its partials, by one warp (lane 0 writes out[]).
-__device__ __forceinline__ void gate_row(const float* p, int n_sl, int q, int M, float inv_d, float inv_sqrt_d,
-                                         float eps, int lane, float* out) {
-  if (q == 1) {
-    const bool has = lane < n_sl;
-    float sv = has ? __ldg(p + lane) : 0.f;
-    for (int m = 0; m < M; ++m) {
-      const float* pm = p + n_sl + (m * n_sl + lane) * 3;
-      float dot = has ? __ldg(pm) : 0.f;
-      float sk = has ? __ldg(pm + 1) : 0.f;
-      float sh = has ? __ldg(pm + 2) : 0.f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        if (m == 0) sv += __shfl_xor_sync(0xFFFFFFFFu, sv, o);
-        dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-        sk += __shfl_xor_sync(0xFFFFFFFFu, sk, o);
-        sh += __shfl_xor_sync(0xFFFFFFFFu, sh, o);
-      }
-      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
-    }
-  } else {
-    const float sv = pairwise_warp_sum(p, 1, n_sl, q, lane);
-    for (int m = 0; m < M; ++m) {
-      const float* pm = p + n_sl + m * n_sl * 3;
-      const float dot = pairwise_warp_sum(pm, 3, n_sl, q, lane);
-      const float sk = pairwise_warp_sum(pm + 1, 3, n_sl, q, lane);
-      const float sh = pairwise_warp_sum(pm + 2, 3, n_sl, q, lane);
-      if (lane == 0) gate_scalars(sv, dot, sk, sh, inv_d, inv_sqrt_d, eps, out, M, m);
-    }
-  }
-}
-
-__device__ __forceinline__ int nodes_per_lane(int n_sl) {
-  int q = 1;
-  while (q * 32 < n_sl) q <<= 1;
-  return q;
-}
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ part, int n_sl, int pstride,
                                                        int64_t ntok, int M, int d, float eps, float* __restrict__ sa,
@@ -341,120 +273,9 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
   __shared__ float s_sa[2 * kMaxM];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  const int p0 = ring != nullptr ? pos[b] : 0;     // written by thread 0 at the end, after the barrier below
-  // This thread's first channel group, branch 0: its taps, v, ring rows and H are loaded before
-  // the gate is known (they do not depend on it), so their latency overlaps warp 0's gate.
-  const int g0 = threadIdx.x;
-  const bool pre = g0 < d / 4;
-  float wq0[4][W], vt0[4], u0[W][4], h0[4];
-  if (pre) {
-    const int c = 4 * g0;
-    float gc[4];
-    ld4(g_c + c, gc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int j = 0; j < W; ++j) wq0[i][j] = __ldg(conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
-    }
-    ld4(v + static_cast<int64_t>(b) * sv + c, vt0);
-#pragma unroll
-    for (int j = 0; j < W; ++j) {
-      const int lag = (W - 1 - j) * dil;
-      if (lag > 0 && ring != nullptr && p0 - lag >= 0)
-        ld4(ring + ((static_cast<int64_t>(b) * L + (p0 - lag) % L) * M) * d + c, u0[j]);
-    }
-    H4<TH>::load(H + static_cast<int64_t>(b) * M * d + c, h0);
-  }
-  if (threadIdx.x < 32) {
-    if constexpr (kPart) {
-      gate_row(gate_in + static_cast<int64_t>(b) * pstride, n_sl, nodes_per_lane(n_sl), M,
-               1.f / static_cast<float>(d), 1.f / sqrtf(static_cast<float>(d)), eps, lane, s_sa);
-    } else if (lane < 2 * M) {
-      s_sa[lane] = gate_in[static_cast<int64_t>(b) * saw + lane];
-    }
-  }
-  __syncthreads();
-  if (sa_out != nullptr && threadIdx.x < 2 * M) sa_out[static_cast<int64_t>(b) * saw + threadIdx.x] = s_sa[threadIdx.x];
-  for (int g = threadIdx.x; g < d / 4; g += blockDim.x) {
-    const int c = 4 * g;
-    const bool first = g == g0;                    // its inputs of branch 0 are already in registers
-    float wq[4][W];
-    float vt[4];
-    if (first) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        vt[i] = vt0[i];
-#pragma unroll
-        for (int j = 0; j < W; ++j) wq[i][j] = wq0[i][j];
-      }
-    } else {
-      float gc[4];
-      ld4(g_c + c, gc);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int j = 0; j < W; ++j) wq[i][j] = __ldg(conv + static_cast<int64_t>(c + i) * W + j) * gc[i];
-      }
-      ld4(v + static_cast<int64_t>(b) * sv + c, vt);
-    }
-    for (int m = 0; m < M; ++m) {
-      const float sm = s_sa[m];
-      const bool have = first && m == 0;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < W; ++j) {
-        const int lag = (W - 1 - j) * dil;
-        if (lag == 0) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], sm * vt[i], acc[i]);
-        } else if (ring != nullptr && p0 - lag >= 0) {
-          float u[4];                                 // the ring holds RMSNorm(v~) before its weight
-          if (have) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) u[i] = u0[j][i];
-          } else {
-            ld4(ring + ((static_cast<int64_t>(b) * L + (p0 - lag) % L) * M + m) * d + c, u);
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = fmaf(wq[i][j], u[i], acc[i]);
-        }
-      }
-      TH* hp = H + (static_cast<int64_t>(b) * M + m) * d + c;
-      float h[4];
-      if (have) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = h0[i];
-      } else {
-        H4<TH>::load(hp, h);
-      }
-      const float at = s_sa[M + m];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) h[i] = h[i] + fmaf(at, vt[i], silu_fast(acc[i]));
-      H4<TH>::store(hp, h);
-      if (ring != nullptr && L > 0) {
-        float* dst = ring + ((static_cast<int64_t>(b) * L + p0 % L) * M + m) * d + c;
-        *reinterpret_cast<float4*>(dst) = make_float4(sm * vt[0], sm * vt[1], sm * vt[2], sm * vt[3]);
-      }
-    }
-  }
-  if (ring == nullptr) return;
-  __syncthreads();                                    // every thread has read pos[b]
-  if (threadIdx.x == 0) {
-    int32_t old[kMaxN];
-    for (int j = 0; j < N - 1; ++j) old[j] = prev[static_cast<int64_t>(b) * (N - 1) + j];
-    int raw = ids[b];
-    bool bad = false;
-    if (static_cast<unsigned>(raw) >= static_cast<unsigned>(V)) {
-      bad = true;
-      raw = 0;
-    }
-    for (int j = 0; j + 1 < N - 1; ++j) prev[static_cast<int64_t>(b) * (N - 1) + j] = old[j + 1];
-    if (N > 1) prev[static_cast<int64_t>(b) * (N - 1) + N - 2] = proj[raw];
-    pos[b] = p0 + 1;
-    if (bad) atomicOr(err, kErrIndexRange);
-  }
+  decode_tail_seq<TH, W, kPart, true>(blockIdx.x, threadIdx.x, blockDim.x, s_sa, gate_in, n_sl, pstride, saw, eps,
+                                      v, sv, M, d, dil, g_c, conv, ring, pos, L, ids, proj, V, prev, N, sa_out, err,
+                                      H, [] { __syncthreads(); });
 }
 
 template <typename TH, bool kPart>

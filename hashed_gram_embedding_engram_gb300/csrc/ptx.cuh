@@ -46,6 +46,11 @@ __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
 
 __device__ __forceinline__ void nanosleep(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
+// Named barrier `id` (1..15; 0 is the block barrier) over `count` threads (whole warps).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Pull one 128-byte line of global memory into L2 (no register result).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -284,6 +284,10 @@ cudaError_t sb_launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 
 }  // namespace
 
+cudaError_t launch_zero_words(uint32_t* p, int n, cudaStream_t s) {
+  return launch_pdl(sync_zero_kernel, dim3(1), dim3(256), 0, s, p, n);
+}
+
 size_t stage_b_sync_words(int64_t ntok) { return static_cast<size_t>((ntok + gk::kBM - 1) / gk::kBM) + 1; }
 
 bool stage_b_fused_applies(const engram_plan* p, int64_t ntok, int T) {

@@ -277,6 +277,10 @@ class EngramPlan:
         _lib.check(self._lib.engram_plan_set_fused_stage_b(self._h, int(bool(enable))),
                    "engram_plan_set_fused_stage_b")
 
+    def set_fused_decode(self, enable: bool) -> None:
+        """Chunks of one position as one cooperative launch, or as separate launches (default); same bits."""
+        _lib.check(self._lib.engram_plan_set_fused_decode(self._h, int(bool(enable))), "engram_plan_set_fused_decode")
+
     def set_cta_pairs(self, enable: bool) -> None:
         """The K/V projection's 256-column tiles on CTA pairs (cta_group::2), or one SM each; same bits."""
         _lib.check(self._lib.engram_plan_set_cta_pairs(self._h, int(bool(enable))), "engram_plan_set_cta_pairs")

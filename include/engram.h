@@ -331,6 +331,22 @@ engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, in
  * made after it. */
 engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable);
 
+/* Chunks of one position per sequence (decode, T = 1) of BF16 layers with
+ * (N-1)*K <= 32 table rows per token, conv_w = 4 and e4m3-free weights can run
+ * as ONE cooperative launch (enable = 1): engram_forward's gather (Steps
+ * 1-4), the K/V projection on the tensor cores with its gate epilogue (Steps
+ * 5-6) and the gate, conv, residual and state update of every sequence
+ * (Steps 6-8), phases linked by counters in the workspace; engram_stage_b
+ * runs the same launch without the gather.  The indices of Stage A depend on
+ * the tokens only ("DeepSeek Engram 系列导读", section "Engram 工作原理"), so
+ * nothing between them needs the host.  The default (enable = 0) is separate
+ * launches (gather, projection, decode tail), which measure faster on GB300
+ * for 256 sequences: they overlap the next layer's gather and each other's
+ * launch, where the one launch runs its phases back to back.  Both give the
+ * same bits.  A device that cannot hold one block per SM of the launch falls
+ * back to separate launches.  enable: 0 or 1; applies to calls made after it. */
+engram_status_t engram_plan_set_fused_decode(engram_plan_t* plan, int enable);
+
 /* The K/V projection (Step 5, bf16 layers) in 256 x 256 output tiles on CTA
  * pairs (enable = 1): two SMs of a thread-block cluster share one
  * tcgen05.mma.cta_group::2 tile, each staging its 128 rows of e and half of
@@ -349,7 +365,9 @@ engram_status_t engram_plan_set_cta_pairs(engram_plan_t* plan, int enable);
  * (finalize), conv + residual; on F32 layers: hash + gather, K/V projection,
  * gate, conv + residual; then the state update when a state is given.  Chunks
  * of one position (T = 1, decode) run the gate, conv, residual and state
- * update as one kernel after the K/V projection.  Where the conv computes the
+ * update as one kernel after the K/V projection, or, with the one-launch
+ * decode (engram_plan_set_fused_decode, the default where it applies), the
+ * whole step is one traced interval.  Where the conv computes the
  * gate itself there is no finalize kernel; where Stage B is one cooperative
  * launch (engram_plan_set_fused_stage_b), its events bracket the counter
  * reset and that launch together.

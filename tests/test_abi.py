@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
               "engram_gather", "engram_stage_a", "engram_kv_projection", "engram_stage_b", "engram_forward",
               "engram_get_error", "engram_cache_create", "engram_cache_observe", "engram_cache_build",
               "engram_stage_a_cached", "engram_cache_stats", "engram_cache_destroy",
-              "engram_status_string", "engram_plan_set_fused_stage_b", "engram_plan_set_cta_pairs", "engram_cache_set_dedup", "engram_quantize_fp8"):
+              "engram_status_string", "engram_plan_set_fused_stage_b", "engram_plan_set_cta_pairs", "engram_plan_set_fused_decode", "engram_cache_set_dedup", "engram_quantize_fp8"):
         assert n in names
 
 
