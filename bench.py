@@ -168,8 +168,8 @@ def _per_token_work(w, bn: int) -> dict:
 KERNEL_SOURCES = {
     "kv_gemm": ["gemm.cu", "gemm_pair.cu", "gemm_parts.cuh", "ptx.cuh"],
     "kv_gemm_fp8": ["gemm.cu", "gemm_parts.cuh", "ptx.cuh"],
-    "conv": ["fusion.cu", "conv_parts.cuh", "gate.cuh", "ptx.cuh"],
-    "hash_gather": ["gather.cu", "hashing.cuh", "ptx.cuh"],
+    "conv": ["fusion.cu", "conv_parts.cuh", "gate.cuh", "tail_parts.cuh", "ptx.cuh"],
+    "hash_gather": ["gather.cu", "gather_parts.cuh", "hashing.cuh", "ptx.cuh"],
 }
 
 
@@ -366,9 +366,11 @@ def run_ours(args) -> None:
     for i in range(K):
         restore()
         flush.zero_()
+        torch.cuda.nvtx.range_push(f"engram step {i}")      # tracing: one NVTX range per timed step
         ev[i][0].record(stream)
         graph.replay()
         ev[i][1].record(stream)
+        torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
@@ -1013,6 +1015,54 @@ def run_workload(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- #
+# small cases for single-kernel profiler captures (no timing, a few launches)
+# --------------------------------------------------------------------------- #
+PROFILE_CASES = {
+    # the headline workload, one layer: hash+gather, K/V GEMM and conv, each launched 4 times
+    "prefill": "prefill_bf16 layer 1 (B=1, T=4096), engram_forward x4",
+    # the UVA gather: int8 rows of the int8-host tables (~40M rows, 2.6 GB) in pinned host
+    # memory, 32768 tokens (B=16, T=2048), engram_stage_a x4
+    "uva_gather": "int8_host tables in pinned host memory, B=16 T=2048, engram_stage_a x4",
+    # the multi-branch projection (d=4096, M=4, d_mem=1536: 20480 output columns) on 32768 tokens
+    # (B=4, T=8192) with small tables, engram_forward x2
+    "multibranch": "multibranch_n4 with 4 x 8192 tokens and small tables, engram_forward x2",
+}
+
+
+def run_profile_case(name: str) -> None:
+    import torch
+    import workloads as W
+    from workloads.torch_layer import make_layer, to_torch
+    if name == "prefill":
+        w, reps = W.PREFILL_BF16, 4
+    elif name == "uva_gather":
+        w, reps = W.INT8_HOST.scaled(B=16), 4
+    elif name == "multibranch":
+        w, reps = W.MULTIBRANCH_N4.scaled(B=4, prime_target=40000), 2
+    else:
+        raise SystemExit(f"unknown profile case {name}: {sorted(PROFILE_CASES)}")
+    ids_np, P = W.token_stream(w), W.projection_map(w)
+    L = W.layer_inputs(w, w.layers[0])
+    plan, weights, proj, H = make_layer(w, L, P, w.ntok)
+    ids = torch.from_numpy(ids_np).cuda()
+    if name == "uva_gather":
+        table_host = to_torch(L.table, w.table_dtype, "cpu", pin=True)
+        e = torch.empty(w.ntok, w.d_mem, dtype=torch.bfloat16, device="cuda")
+        for _ in range(reps):
+            plan.stage_a(ids, proj, table_host, weights.scales, out=e)
+    else:
+        ws = plan.new_workspace(w.ntok)
+        H0 = H.clone()
+        for _ in range(reps):
+            H.copy_(H0)
+            plan.forward(ids, proj, weights, H, None, ws)
+    torch.cuda.synchronize()
+    st, flags = plan.get_error()
+    assert st == 0, flags
+    print(f"profile case {name}: {PROFILE_CASES[name]}: ok", flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1025,7 +1075,12 @@ def main() -> None:
     ap.add_argument("--workload", default="prefill_bf16",
                     help="prefill_bf16 (the headline line); prefill_fp8 (the same with the e4m3 K/V "
                          "projection), decode_bf16, int8_host or multibranch_n4 print that workload's own line")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="run a small case for a profiler capture (no timing, no JSON line)")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

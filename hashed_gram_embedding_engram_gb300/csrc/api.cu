@@ -6,6 +6,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "engram_internal.h"
 
 using engram::PlanDev;
@@ -13,6 +15,16 @@ using engram::PlanDev;
 namespace {
 
 constexpr uint64_t kU64Max = ~0ull;
+
+// Tracing: an NVTX range over each entry point that enqueues work (host side:
+// the enqueue itself; a profiler shows the GPU work it launched beneath it).
+// NVTX is header-only and inert unless a profiler is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -249,6 +261,7 @@ engram_status_t engram_plan_workspace_bytes(const engram_plan_t* plan, int64_t n
 
 engram_status_t engram_hash(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
                             int V, const int32_t* prev_ids, int32_t* idx_out, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_hash");
   if (!plan) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_tokens(plan, B, T)) return s;
   if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
@@ -258,6 +271,7 @@ engram_status_t engram_hash(const engram_plan_t* plan, const int32_t* ids, int B
 
 engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int64_t ntok, const void* table,
                               const uint16_t* scales, void* e_out, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_gather");
   if (!plan || ntok < 0 || ntok > plan->max_tokens) return ENGRAM_ERR_INVALID_ARG;
   if (ntok == 0) return ENGRAM_OK;
   if (!idx || !table || !e_out || !aligned16(e_out)) return ENGRAM_ERR_INVALID_ARG;
@@ -277,6 +291,7 @@ engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int
 engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
                                int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,
                                void* e_out, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_stage_a");
   if (!plan) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_tokens(plan, B, T)) return s;
   if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
@@ -298,6 +313,7 @@ engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, in
 
 engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok, const void* w_kv,
                                      void* kv_out, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_kv_projection");
   if (!plan || ntok < 0 || ntok > plan->max_tokens) return ENGRAM_ERR_INVALID_ARG;
   if (ntok == 0) return ENGRAM_OK;
   if (!e || !w_kv || !kv_out || !aligned16(e) || !aligned16(w_kv) || !aligned16(kv_out))
@@ -421,6 +437,7 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
 engram_status_t engram_stage_b(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
                                int V, const void* e, const engram_weights_t* w, void* H, engram_state_t* state,
                                void* workspace, size_t workspace_bytes, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_stage_b");
   if (!plan) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_tokens(plan, B, T)) return s;
   const int64_t ntok = static_cast<int64_t>(B) * T;
@@ -439,6 +456,7 @@ engram_status_t engram_stage_b(const engram_plan_t* plan, const int32_t* ids, in
 engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
                                int V, const engram_weights_t* w, void* H, engram_state_t* state, void* workspace,
                                size_t workspace_bytes, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_forward");
   if (!plan) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_tokens(plan, B, T)) return s;
   const int64_t ntok = static_cast<int64_t>(B) * T;
@@ -555,6 +573,7 @@ engram_status_t engram_cache_destroy(engram_cache_t* c) {
 
 engram_status_t engram_cache_observe(engram_cache_t* c, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                                      const int32_t* prev_ids, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_cache_observe");
   if (!c) return ENGRAM_ERR_INVALID_ARG;
   if (engram_status_t s = check_tokens(c->plan, B, T)) return s;
   if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
@@ -563,6 +582,7 @@ engram_status_t engram_cache_observe(engram_cache_t* c, const int32_t* ids, int 
 }
 
 engram_status_t engram_cache_build(engram_cache_t* c, int decay, engram_stream_t stream, int64_t* cached_rows) {
+  NvtxRange nvtx_range("engram_cache_build");
   if (!c) return ENGRAM_ERR_INVALID_ARG;
   int64_t cached = 0;
   if (engram::cache_build(c->plan, c->capacity, c->row_bytes, c->table, c->counts, c->slot, c->rows, c->stats + 2,
@@ -576,6 +596,7 @@ engram_status_t engram_cache_build(engram_cache_t* c, int decay, engram_stream_t
 engram_status_t engram_stage_a_cached(const engram_cache_t* c, const int32_t* ids, int B, int T, const int32_t* proj,
                                       int V, const int32_t* prev_ids, const uint16_t* scales, void* e_out,
                                       engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_stage_a_cached");
   if (!c) return ENGRAM_ERR_INVALID_ARG;
   const engram_plan* plan = c->plan;
   if (engram_status_t s = check_tokens(plan, B, T)) return s;
@@ -716,6 +737,7 @@ engram_status_t engram_cache_stats(const engram_cache_t* c, engram_stream_t stre
 
 engram_status_t engram_quantize_fp8(const engram_plan_t* plan, const void* x, int64_t rows, int cols, uint8_t* q,
                                     float* scale, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_quantize_fp8");
   if (!plan || !x || !q || !scale || rows < 0 || cols <= 0 || cols % 16) return ENGRAM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q) || !aligned16(scale)) return ENGRAM_ERR_INVALID_ARG;
   if (rows == 0) return ENGRAM_OK;
