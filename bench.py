@@ -927,25 +927,6 @@ def run_workload(args) -> None:
             looked += a_
             hits += b_
             link += l_
-        # the lookup that Stage A prefetch is meant to hide: over the host link, plain and
-        # through the hot-row cache, beside a stand-in for the layers before the Engram layer
-        ly0 = layers[0]
-        side_pf = torch.cuda.Stream()
-        pf = {}
-        for name, look in (("uva", lambda ly=ly0: ly["plan"].stage_a(ids, ly["proj"], ly["table_host"],
-                                                                      ly["weights"].scales, out=ly["e"])),
-                           ("uva_hot_row_cache", lambda ly=ly0: ly["cache"].stage_a(ids, ly["proj"],
-                                                                                    ly["weights"].scales,
-                                                                                    out=ly["e"])),
-                           ("hbm", lambda ly=ly0: ly["plan"].stage_a(ids, ly["proj"], ly["table_dev"],
-                                                                      ly["weights"].scales, out=ly["e"]))):
-            try:
-                pf[name] = prefetch_hiding(ly0, ids, ly0["e"], side_pf, flush, reps=20, lookup_fn=look)
-            except Exception as exc:  # a side measurement: it must never sink the line
-                pf[name] = {"error": str(exc)[:200]}
-        for ly in layers:
-            ly["cache"].stats(reset=True)
-        extra["prefetch"] = pf
         # per-batch row dedup: each distinct row of a batch crosses the link once
         # (alone, then together with the hot-row cache)
         for ly in layers:
@@ -998,6 +979,28 @@ def run_workload(args) -> None:
             "host_link_bytes_per_step": int(link / max(1, looked) * w.ntok * w.R * len(layers) * row_bytes),
             "host_link_bytes_per_step_uncached": w.ntok * w.R * len(layers) * row_bytes,
             "ms_per_step": round(ms_cache, 5), "value": round(tokens_per_step / (ms_cache / 1e3), 1)}
+        # the lookup that Stage A prefetch is meant to hide: over the host link, plain and
+        # through the hot-row cache, beside a stand-in for the layers before the Engram layer
+        # (measured last: the stand-in's allocations slowed the dedup step measured after them)
+        for ly in layers:
+            ly["cache"].set_dedup(0)
+        ly0 = layers[0]
+        side_pf = torch.cuda.Stream()
+        pf = {}
+        for name, look in (("uva", lambda ly=ly0: ly["plan"].stage_a(ids, ly["proj"], ly["table_host"],
+                                                                      ly["weights"].scales, out=ly["e"])),
+                           ("uva_hot_row_cache", lambda ly=ly0: ly["cache"].stage_a(ids, ly["proj"],
+                                                                                    ly["weights"].scales,
+                                                                                    out=ly["e"])),
+                           ("hbm", lambda ly=ly0: ly["plan"].stage_a(ids, ly["proj"], ly["table_dev"],
+                                                                      ly["weights"].scales, out=ly["e"]))):
+            try:
+                pf[name] = prefetch_hiding(ly0, ids, ly0["e"], side_pf, flush, reps=20, lookup_fn=look)
+            except Exception as exc:  # a side measurement: it must never sink the line
+                pf[name] = {"error": str(exc)[:200]}
+        for ly in layers:
+            ly["cache"].stats(reset=True)
+        extra["prefetch"] = pf
         extra["uva"] = {"tables": "int8 rows in pinned host memory read over UVA (C2C), fp16 scales in HBM",
                         "ms_per_step": round(ms, 5), "hbm_table_ms_per_step": round(ms_hbm, 5),
                         "hbm_table_value": round(tokens_per_step / (ms_hbm / 1e3), 1),
@@ -1027,6 +1030,8 @@ PROFILE_CASES = {
     # the multi-branch projection (d=4096, M=4, d_mem=1536: 20480 output columns) on 32768 tokens
     # (B=4, T=8192) with small tables, engram_forward x2
     "multibranch": "multibranch_n4 with 4 x 8192 tokens and small tables, engram_forward x2",
+    # the prefill workload with the e4m3 projection (W_kv quantised once), engram_forward x4
+    "prefill_fp8": "prefill_bf16 layer 1 with e4m3 W_kv and per-token e4m3 e, engram_forward x4",
 }
 
 
@@ -1034,7 +1039,7 @@ def run_profile_case(name: str) -> None:
     import torch
     import workloads as W
     from workloads.torch_layer import make_layer, to_torch
-    if name == "prefill":
+    if name in ("prefill", "prefill_fp8"):
         w, reps = W.PREFILL_BF16, 4
     elif name == "uva_gather":
         w, reps = W.INT8_HOST.scaled(B=16), 4
@@ -1045,6 +1050,9 @@ def run_profile_case(name: str) -> None:
     ids_np, P = W.token_stream(w), W.projection_map(w)
     L = W.layer_inputs(w, w.layers[0])
     plan, weights, proj, H = make_layer(w, L, P, w.ntok)
+    if name == "prefill_fp8":
+        q, sc = plan.quantize_fp8(weights.w_kv)
+        weights = dataclass_replace(weights, w_kv=None, w_kv_fp8=q, w_kv_scale=sc)
     ids = torch.from_numpy(ids_np).cuda()
     if name == "uva_gather":
         table_host = to_torch(L.table, w.table_dtype, "cpu", pin=True)

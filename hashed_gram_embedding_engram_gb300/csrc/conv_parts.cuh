@@ -243,6 +243,7 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
       float vr[kRows][4];
 #pragma unroll
       for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
+#pragma unroll 1
       for (int m = 0; m < M; ++m) {
         float u[kRows][4], h[kChain][4], at[kChain];
 #pragma unroll
@@ -289,6 +290,7 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
         for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
       }
     }
+#pragma unroll 1
     for (int m = 0; m < M; ++m) {
       float u[kRows][4];                          // conv input RMSNorm(v~) before g_c: s * v, or the ring
 #pragma unroll

@@ -386,6 +386,8 @@ cudaError_t conv_launch(const CUtensorMap& tv, const CUtensorMap& th, const CUte
     }
     return conv_launch_m<TH, W, DIL, 1, 0, false>(tv, th, ts, a, grid, smem, H, s);
   }
+  // four hyper-connection branches (the pages' multi-branch variant) at the pages' w = 4
+  if (DIL > 0 && W == 4 && a.M == 4) return conv_launch_m<TH, W, DIL, 4, 0, false>(tv, th, ts, a, grid, smem, H, s);
   return conv_launch_m<TH, W, DIL, 0, 0, false>(tv, th, ts, a, grid, smem, H, s);
 }
 
