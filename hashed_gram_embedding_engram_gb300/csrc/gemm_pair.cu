@@ -219,10 +219,9 @@ __device__ __forceinline__ void pair_epilogue(const PairCtx& c, uint32_t tmem, c
         const int64_t go = static_cast<int64_t>(m) * epi.d + col;
         ptx::bulk_load(gs, epi.g_h + go, EpiCfg::kGWarpBytes / 2, &bars->hbar[ew]);
         ptx::bulk_load(gs + kPairBN / 2, epi.g_k + go, EpiCfg::kGWarpBytes / 2, &bars->hbar[ew]);
-        const uint64_t stream = ptx::policy_evict_first();     // H streams through L2: evicted before W_kv
 #pragma unroll
         for (int bx = 0; bx < EpiCfg::kHBoxes; ++bx)
-          ptx::tma_load_3d_hint(eb + bx * 4096, tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32, stream);
+          ptx::tma_load_3d(eb + bx * 4096, tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32);
       }
       h_pending = true;
     }

@@ -162,8 +162,7 @@ __device__ __forceinline__ void fused_epilogue(const EngramEpilogue& epi, const 
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        // v streams through L2 (the conv reads it next): it goes before W_kv, which every row tile re-reads
-        ptx::tma_store_2d_hint(tmV, sb, n0 + c, row0, ptx::policy_evict_first());
+        ptx::tma_store_2d(tmV, sb, n0 + c, row0);
         ptx::bulk_commit();
       }
     }
@@ -431,11 +430,9 @@ __device__ __forceinline__ void gemm_epilogue(const GemmCtx& c, const EngramEpil
         const int64_t go = static_cast<int64_t>(m) * epi.d + col;
         ptx::bulk_load(gs, epi.g_h + go, G::kGWarpBytes / 2, &bars->hbar[ew]);
         ptx::bulk_load(gs + BN / 2, epi.g_k + go, G::kGWarpBytes / 2, &bars->hbar[ew]);
-        // H streams through L2 as well: evicted before W_kv
-        const uint64_t stream = ptx::policy_evict_first();
 #pragma unroll
         for (int bx = 0; bx < G::kHBoxes; ++bx)
-          ptx::tma_load_3d_hint(eb + bx * 4096, &tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32, stream);
+          ptx::tma_load_3d(eb + bx * 4096, &tmH, &bars->hbar[ew], col + bx * 64, m, m0 + q * 32);
       }
       h_pending = true;
     }

@@ -197,30 +197,12 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* desc, ui
       : "memory");
 }
 
-// The same with an L2 eviction-priority policy for the loaded lines.
-__device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* desc, uint64_t* bar, int32_t c0,
-                                                 int32_t c1, int32_t c2, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(desc)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(cache_hint)
-      : "memory");
-}
-
 // 2D tiled bulk tensor store shared -> global (rows past the tensor are not
 // written).  The coordinates must not be negative.
 __device__ __forceinline__ void tma_store_2d(const void* desc, const void* smem_src, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(desc)),
                "r"(c0), "r"(c1), "r"(smem_u32(smem_src))
-               : "memory");
-}
-// The same with an L2 eviction-priority policy for the stored lines.
-__device__ __forceinline__ void tma_store_2d_hint(const void* desc, const void* smem_src, int32_t c0, int32_t c1,
-                                                  uint64_t cache_hint) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
-                   reinterpret_cast<uint64_t>(desc)),
-               "r"(c0), "r"(c1), "r"(smem_u32(smem_src)), "l"(cache_hint)
                : "memory");
 }
 // Pull a tile of a tensor map into L2 (no shared memory, no completion to wait for).
