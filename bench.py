@@ -282,7 +282,7 @@ def run_ours(args) -> None:
     import numpy as np
     import torch
     import workloads as W
-    from hashed_gram_embedding_engram_gb300 import EngramLayer
+    from hashed_gram_embedding_engram_gb300 import EngramLayer, stage_a_layers
     from workloads.torch_layer import make_layer, to_torch
 
     world, rank, local = dist_env()
@@ -321,19 +321,19 @@ def run_ours(args) -> None:
 
     def step():
         # Stage A (hash + gather) depends on the token ids only: every layer's
-        # runs on a side stream, so a later layer's rows arrive while an
-        # earlier layer's Stage B computes; each Stage B waits for its own rows.
+        # rows come from one launch (engram_stage_a_layers) on a side stream,
+        # and the Stage Bs follow it on the main stream after one event wait,
+        # so that each Stage B's kernels overlap the previous kernel's tail
+        # (programmatic launch) with no other dependency in between.
         main = torch.cuda.current_stream()
         side.wait_stream(main)
-        ready = []
         with torch.cuda.stream(side):
-            for ly, e in zip(layers, e_bufs):
-                ly["plan"].stage_a(ids, ly["proj"], ly["weights"].table, ly["weights"].scales, out=e)
-                ev = torch.cuda.Event()
-                ev.record(side)
-                ready.append(ev)
-        for ly, e, ev in zip(layers, e_bufs, ready):
-            main.wait_event(ev)
+            stage_a_layers([ly["plan"] for ly in layers], ids, layers[0]["proj"],
+                           [ly["weights"].table for ly in layers], outs=e_bufs)
+            ready = torch.cuda.Event()
+            ready.record(side)
+        main.wait_event(ready)
+        for ly, e in zip(layers, e_bufs):
             ly["plan"].stage_b(e, ly["weights"], ly["H"], workspace=ly["ws"])
 
     def restore():
@@ -384,9 +384,10 @@ def run_ours(args) -> None:
 
     # ---- per-kernel durations: the plan's tracing events around each kernel of engram_forward ----
     kernels, names = trace_kernels(layers, ids, flush, min(K, 200), w, peaks, fp8=fp8)
-    # kernels per layer in the timed step: Stage A, then Stage B's (the one-launch
-    # form is preceded by a one-block kernel that zeroes its counters)
-    launches_per_layer = len(names) + (1 if names[-1] == "stage_b" else 0)
+    # kernels in the timed step: one Stage A for all layers, then each layer's
+    # Stage B kernels (the one-launch form is preceded by a one-block kernel
+    # that zeroes its counters)
+    launches_per_step = 1 + len(layers) * (len(names) - 1 + (1 if names[-1] == "stage_b" else 0))
     work = per_token_work(w)
     # ---- the same projection shape through torch.matmul (cuBLAS), for comparison ----
     # e [ntok, d_mem] . W_kv^T in bf16 with a bf16 result (no epilogue), warm and with
@@ -517,7 +518,7 @@ def run_ours(args) -> None:
                 "config": dict(workload_desc(w), cuda_graph=True,
                                stage_a="every layer's hash+gather on a side stream, ahead of its Stage B"),
                 "roofline": roofline, "kernels": kernels, "torch_matmul_same_shape": torch_matmul,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * launches_per_layer * len(layers), "clocks": clocks,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K * launches_per_step, "clocks": clocks,
                 "prefetch": prefetch, "tokens_per_s": round(value / len(w.layers), 1)}
         if others is not None:
             line["other_workloads"] = others
@@ -739,7 +740,7 @@ def run_workload(args) -> None:
     pinned-host-to-device copy rate measured in the same run."""
     import torch
     import workloads as W
-    from hashed_gram_embedding_engram_gb300 import EngramState
+    from hashed_gram_embedding_engram_gb300 import EngramState, stage_a_layers
     from workloads.torch_layer import make_layer, to_torch
 
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -784,21 +785,25 @@ def run_workload(args) -> None:
             return
         main = torch.cuda.current_stream()
         side.wait_stream(main)
-        ready = []
         with torch.cuda.stream(side):
-            for ly in layers:
-                st = ly.get("state")
-                prev = None if st is None else st.prev_ids
-                if table_key in ("cache", "dedup"):
-                    ly[table_key].stage_a(ids, ly["proj"], ly["weights"].scales, prev_ids=prev, out=ly["e"])
-                else:
-                    table = ly[table_key] if table_key else ly["weights"].table
-                    ly["plan"].stage_a(ids, ly["proj"], table, ly["weights"].scales, prev_ids=prev, out=ly["e"])
-                ev = torch.cuda.Event()
-                ev.record(side)
-                ready.append(ev)
-        for ly, ev in zip(layers, ready):
-            main.wait_event(ev)
+            if table_key in ("cache", "dedup"):
+                for ly in layers:
+                    st = ly.get("state")
+                    ly[table_key].stage_a(ids, ly["proj"], ly["weights"].scales,
+                                          prev_ids=None if st is None else st.prev_ids, out=ly["e"])
+            else:
+                # every layer's Stage A in one launch
+                stage_a_layers([ly["plan"] for ly in layers], ids, layers[0]["proj"],
+                               [ly[table_key] if table_key else ly["weights"].table for ly in layers],
+                               scales=None if layers[0]["weights"].scales is None else
+                               [ly["weights"].scales for ly in layers],
+                               prev_ids=None if layers[0].get("state") is None else
+                               [ly["state"].prev_ids for ly in layers],
+                               outs=[ly["e"] for ly in layers])
+            ready = torch.cuda.Event()
+            ready.record(side)
+        main.wait_event(ready)
+        for ly in layers:
             ly["plan"].stage_b(ly["e"], ly["weights"], ly["H"], ly.get("state"), ids=ids, proj=ly["proj"],
                                workspace=ly["ws"])
 

@@ -20,7 +20,7 @@ EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", 
            "engram_hash", "engram_gather", "engram_kv_projection", "engram_stage_b", "engram_forward",
            "engram_get_error", "engram_plan_set_timing", "engram_plan_set_fused_stage_b", "engram_plan_set_cta_pairs",
            "engram_plan_set_fused_decode", "engram_plan_kernel_times",
-           "engram_forward_static_scratch", "engram_stage_a", "engram_cache_create", "engram_cache_destroy",
+           "engram_forward_static_scratch", "engram_stage_a", "engram_stage_a_layers", "engram_cache_create", "engram_cache_destroy",
            "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats",
            "engram_cache_set_dedup", "engram_quantize_fp8")
 
@@ -71,6 +71,7 @@ def _lib() -> ctypes.CDLL:
         lib.engram_kv_projection.argtypes = [vp, vp, i64, vp, vp, vp]
         lib.engram_quantize_fp8.argtypes = [vp, vp, i64, i32, vp, vp, vp]
         lib.engram_stage_a.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
+        lib.engram_stage_a_layers.argtypes = [i32, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
         lib.engram_cache_create.argtypes = [vp, i64, vp, ctypes.POINTER(vp)]
         lib.engram_cache_destroy.argtypes = [vp]
         lib.engram_cache_observe.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp]

@@ -311,6 +311,48 @@ engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, in
                                                 host));
 }
 
+engram_status_t engram_stage_a_layers(int n_layers, const engram_plan_t* const* plans, const int32_t* ids, int B,
+                                      int T, const int32_t* proj, int V, const int32_t* const* prev_ids,
+                                      const void* const* tables, const uint16_t* const* scales, void* const* e_out,
+                                      engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_stage_a_layers");
+  if (n_layers < 1 || n_layers > engram::kMaxGatherLayers || !plans || !tables || !e_out)
+    return ENGRAM_ERR_INVALID_ARG;
+  const engram_plan_t* p0 = plans[0];
+  if (!p0) return ENGRAM_ERR_INVALID_ARG;
+  const bool i8 = p0->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
+  if (i8 != (scales != nullptr)) return ENGRAM_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const engram_plan_t* p = plans[l];
+    if (!p || p->device != p0->device || p->cfg.N != p0->cfg.N || p->cfg.K != p0->cfg.K ||
+        p->cfg.row_dim != p0->cfg.row_dim || p->cfg.table_dtype != p0->cfg.table_dtype ||
+        p->cfg.act_dtype != p0->cfg.act_dtype)
+      return ENGRAM_ERR_INVALID_ARG;
+    if (engram_status_t s = check_tokens(p, B, T)) return s;
+  }
+  if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
+  if (!ids || !proj || V <= 0) return ENGRAM_ERR_INVALID_ARG;
+  const void* tab[engram::kMaxGatherLayers] = {};
+  const uint16_t* sc[engram::kMaxGatherLayers] = {};
+  bool host0 = false;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!tables[l] || !e_out[l] || !aligned16(e_out[l])) return ENGRAM_ERR_INVALID_ARG;
+    bool host = false;
+    if (engram_status_t s = device_view(tables[l], &tab[l], &host)) return s;
+    if (!aligned16(tab[l])) return ENGRAM_ERR_INVALID_ARG;
+    if (l == 0) host0 = host;
+    if (host != host0) return ENGRAM_ERR_INVALID_ARG;
+    if (i8) {
+      const void* v = nullptr;
+      if (!scales[l]) return ENGRAM_ERR_INVALID_ARG;
+      if (engram_status_t s = device_view(scales[l], &v)) return s;
+      sc[l] = static_cast<const uint16_t*>(v);
+    }
+  }
+  return cuda_status(engram::launch_hash_gather_layers(plans, n_layers, ids, B, T, proj, V, prev_ids, tab,
+                                                       i8 ? sc : nullptr, e_out, (cudaStream_t)stream, host0));
+}
+
 engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok, const void* w_kv,
                                      void* kv_out, engram_stream_t stream) {
   NvtxRange nvtx_range("engram_kv_projection");

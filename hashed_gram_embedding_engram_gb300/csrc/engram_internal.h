@@ -17,6 +17,7 @@ constexpr int kMaxMults = 320;     // sum_{n=2..N} K*n with (N-1)*K <= 64, N <= 
 constexpr int kMaxN = 8;
 constexpr int kMaxConvW = 8;
 constexpr int kMaxM = 8;
+constexpr int kMaxGatherLayers = 8;   // layers one engram_stage_a_layers launch gathers for
 
 // bits of the device error word
 constexpr uint32_t kErrIndexRange = 1u;
@@ -111,6 +112,12 @@ cudaError_t launch_gather(const engram_plan* p, const int32_t* idx, int64_t ntok
 cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
                                const int32_t* prev_ids, const void* table, const uint16_t* scales, void* e,
                                cudaStream_t s, bool host_table = false);
+// Steps 1-4 of n_layers layers in one launch (the layers share ids, P and the
+// table shape; each has its own plan, tables, state ids and output).
+cudaError_t launch_hash_gather_layers(const engram_plan* const* plans, int n_layers, const int32_t* ids, int B, int T,
+                                      const int32_t* proj, int V, const int32_t* const* prev_ids,
+                                      const void* const* tables, const uint16_t* const* scales, void* const* e,
+                                      cudaStream_t s, bool host_table = false);
 // The same through the HBM hot-row cache (slot map, cached rows, [lookups, hits] counters).
 cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj,
                                       int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,

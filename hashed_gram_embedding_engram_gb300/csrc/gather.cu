@@ -58,13 +58,19 @@ constexpr int kThreads = 128;
 // and ga::chunk_phase as in decode.cu: this form measured 7 % faster.)
 template <int kCpr, bool kInt8, bool kHash, bool kCache = false, bool kWide = false, int kBlk = kThreads>
 __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
-    row_gather_kernel(const PlanDev* __restrict__ pdg, int R, int N, int K, uint32_t* __restrict__ err,
-                      const int32_t* __restrict__ idx, const int32_t* __restrict__ ids, int T,
-                      const int32_t* __restrict__ proj, int V, const int32_t* __restrict__ prev, int64_t ntok,
-                      const uint8_t* __restrict__ table, const __half* __restrict__ scales,
-                      uint4* __restrict__ out, const RowCache cache) {
+    row_gather_kernel(const GatherLayers ls, int R, int N, int K, const int32_t* __restrict__ idx,
+                      const int32_t* __restrict__ ids, int T, const int32_t* __restrict__ proj, int V, int64_t ntok,
+                      const RowCache cache) {
   constexpr int kRowBytes = kCpr * 16;
   const int lane = threadIdx.x & 31;
+  // this block's layer: blockIdx.y (the layers share ids, proj and the table shape)
+  const int ly = static_cast<int>(blockIdx.y);
+  const PlanDev* __restrict__ pdg = ls.pdg[ly];
+  uint32_t* __restrict__ err = ls.err[ly];
+  const int32_t* __restrict__ prev = ls.prev[ly];
+  const uint8_t* __restrict__ table = ls.table[ly];
+  const __half* __restrict__ scales = ls.scales[ly];
+  uint4* __restrict__ out = ls.out[ly];
   constexpr int kRows = kWide ? 2 : 1;
   const bool has0 = lane < R, has1 = kWide && lane + 32 < R;
   RowConst rc[kRows];
@@ -73,7 +79,7 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
   if constexpr (kHash) {
     // P (read at random, written by no kernel) into L2 while the ids load: one 128-byte line per thread
     const int64_t line = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (line * 32 < V) ptx::prefetch_l2(proj + line * 32);
+    if (ly == 0 && line * 32 < V) ptx::prefetch_l2(proj + line * 32);
   }
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
@@ -230,47 +236,53 @@ int grid_for_tokens(const engram_plan* p, int64_t ntok, bool host_table = false)
   return static_cast<int>(blocks);
 }
 
+GatherLayers one_layer(const engram_plan* p, const int32_t* prev, const void* table, const uint16_t* scales,
+                       void* e) {
+  GatherLayers ls{};
+  ls.pdg[0] = p->dev;
+  ls.err[0] = &p->dev->err;
+  ls.prev[0] = prev;
+  ls.table[0] = static_cast<const uint8_t*>(table);
+  ls.scales[0] = reinterpret_cast<const __half*>(scales);
+  ls.out[0] = static_cast<uint4*>(e);
+  return ls;
+}
+
 template <int kCpr, bool kInt8>
 cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, const void* table,
                        const uint16_t* scales, void* e, cudaStream_t s) {
   auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, false, false, true> : row_gather_kernel<kCpr, kInt8, false>;
-  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s,
-                    p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(idx), static_cast<const int32_t*>(nullptr), 1,
-                    static_cast<const int32_t*>(nullptr), 0, static_cast<const int32_t*>(nullptr), ntok,
-                    static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
-                    static_cast<uint4*>(e), RowCache{});
+  return launch_pdl(k, dim3(grid_for_tokens(p, ntok)), dim3(kThreads), 0, s, one_layer(p, nullptr, table, scales, e),
+                    p->R, p->cfg.N, p->cfg.K, idx, static_cast<const int32_t*>(nullptr), 1,
+                    static_cast<const int32_t*>(nullptr), 0, ntok, RowCache{});
 }
 
+// Steps 1-4 for n_layers layers of one shape in one launch (grid.y = layer);
+// with tables in host memory, the grid's share of the SMs is split among them.
 template <int kCpr, bool kInt8>
-cudaError_t launch_fused(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                         const int32_t* prev, const void* table, const uint16_t* scales, void* e, cudaStream_t s,
-                         bool host_table) {
+cudaError_t launch_fused(const engram_plan* p, int n_layers, const GatherLayers& ls, const int32_t* ids, int B, int T,
+                         const int32_t* proj, int V, cudaStream_t s, bool host_table, const RowCache* cache) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
-  auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, false, true> : row_gather_kernel<kCpr, kInt8, true>;
+  int gx = grid_for_tokens(p, ntok, host_table);
+  const int cap = host_table ? hostgrid_sms(p->num_sms) : p->num_sms * 8;   // one wave over all layers
+  if (static_cast<int64_t>(gx) * n_layers > cap) gx = cap / n_layers > 0 ? cap / n_layers : 1;
+  const dim3 grid(gx, n_layers);
+  const dim3 block(host_table ? kHostBlk : kThreads);
+  const bool wide = p->R > 32;
+  if (cache != nullptr) {
+    auto k = wide ? row_gather_kernel<kCpr, kInt8, true, true, true> : row_gather_kernel<kCpr, kInt8, true, true>;
+    if (host_table)
+      k = wide ? row_gather_kernel<kCpr, kInt8, true, true, true, kHostBlk>
+               : row_gather_kernel<kCpr, kInt8, true, true, false, kHostBlk>;
+    return launch_pdl(k, grid, block, 0, s, ls, p->R, p->cfg.N, p->cfg.K, static_cast<const int32_t*>(nullptr), ids,
+                      T, proj, V, ntok, *cache);
+  }
+  auto k = wide ? row_gather_kernel<kCpr, kInt8, true, false, true> : row_gather_kernel<kCpr, kInt8, true>;
   if (host_table)
-    k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, false, true, kHostBlk>
-                  : row_gather_kernel<kCpr, kInt8, true, false, false, kHostBlk>;
-  return launch_pdl(k, dim3(grid_for_tokens(p, ntok, host_table)), dim3(host_table ? kHostBlk : kThreads), 0, s,
-                    p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T,
-                    proj, V, prev, ntok,
-                    static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
-                    static_cast<uint4*>(e), RowCache{});
-}
-
-template <int kCpr, bool kInt8>
-cudaError_t launch_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                          const int32_t* prev, const void* table, const uint16_t* scales, void* e,
-                          const RowCache& cache, cudaStream_t s, bool host_table) {
-  const int64_t ntok = static_cast<int64_t>(B) * T;
-  auto k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, true, true> : row_gather_kernel<kCpr, kInt8, true, true>;
-  if (host_table)
-    k = p->R > 32 ? row_gather_kernel<kCpr, kInt8, true, true, true, kHostBlk>
-                  : row_gather_kernel<kCpr, kInt8, true, true, false, kHostBlk>;
-  return launch_pdl(k, dim3(grid_for_tokens(p, ntok, host_table)), dim3(host_table ? kHostBlk : kThreads), 0, s,
-                    p->dev, p->R, p->cfg.N, p->cfg.K, &p->dev->err, static_cast<const int32_t*>(nullptr), ids, T,
-                    proj, V, prev, ntok,
-                    static_cast<const uint8_t*>(table), reinterpret_cast<const __half*>(scales),
-                    static_cast<uint4*>(e), cache);
+    k = wide ? row_gather_kernel<kCpr, kInt8, true, false, true, kHostBlk>
+             : row_gather_kernel<kCpr, kInt8, true, false, false, kHostBlk>;
+  return launch_pdl(k, grid, block, 0, s, ls, p->R, p->cfg.N, p->cfg.K, static_cast<const int32_t*>(nullptr), ids, T,
+                    proj, V, ntok, RowCache{});
 }
 
 int chunks_per_row(const engram_plan* p) {
@@ -302,7 +314,8 @@ cudaError_t launch_hash_gather(const engram_plan* p, const int32_t* ids, int B, 
                                const int32_t* prev_ids, const void* table, const uint16_t* scales, void* e,
                                cudaStream_t s, bool host_table) {
   const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
-#define CALL(C, I) launch_fused<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, s, host_table)
+  const GatherLayers ls = one_layer(p, prev_ids, table, scales, e);
+#define CALL(C, I) launch_fused<C, I>(p, 1, ls, ids, B, T, proj, V, s, host_table, nullptr)
   ENGRAM_DISPATCH_CPR(CALL)
 #undef CALL
 }
@@ -313,7 +326,29 @@ cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, 
                                       cudaStream_t s, bool host_table) {
   const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
   const RowCache cache{slot, static_cast<const uint8_t*>(rows), stats};
-#define CALL(C, I) launch_cached<C, I>(p, ids, B, T, proj, V, prev_ids, table, scales, e, cache, s, host_table)
+  const GatherLayers ls = one_layer(p, prev_ids, table, scales, e);
+#define CALL(C, I) launch_fused<C, I>(p, 1, ls, ids, B, T, proj, V, s, host_table, &cache)
+  ENGRAM_DISPATCH_CPR(CALL)
+#undef CALL
+}
+
+cudaError_t launch_hash_gather_layers(const engram_plan* const* plans, int n_layers, const int32_t* ids, int B, int T,
+                                      const int32_t* proj, int V, const int32_t* const* prev_ids,
+                                      const void* const* tables, const uint16_t* const* scales, void* const* e,
+                                      cudaStream_t s, bool host_table) {
+  if (n_layers < 1 || n_layers > kMaxGatherLayers) return cudaErrorInvalidValue;
+  const engram_plan* p = plans[0];
+  GatherLayers ls{};
+  for (int l = 0; l < n_layers; ++l) {
+    ls.pdg[l] = plans[l]->dev;
+    ls.err[l] = &plans[l]->dev->err;
+    ls.prev[l] = prev_ids != nullptr ? prev_ids[l] : nullptr;
+    ls.table[l] = static_cast<const uint8_t*>(tables[l]);
+    ls.scales[l] = scales != nullptr ? reinterpret_cast<const __half*>(scales[l]) : nullptr;
+    ls.out[l] = static_cast<uint4*>(e[l]);
+  }
+  const bool i8 = p->cfg.table_dtype == ENGRAM_I8_ROWSCALE_F16;
+#define CALL(C, I) launch_fused<C, I>(p, n_layers, ls, ids, B, T, proj, V, s, host_table, nullptr)
   ENGRAM_DISPATCH_CPR(CALL)
 #undef CALL
 }

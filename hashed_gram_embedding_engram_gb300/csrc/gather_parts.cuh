@@ -58,6 +58,18 @@ struct RowCache {
   unsigned long long* stats;         // [2]: rows looked up, rows served from HBM
 };
 
+// The per-layer operands of one gather launch; blockIdx.y selects the layer.
+// Layers of one launch share the token ids, P and the table shape (N, K, row
+// size and type); each has its own parameter block, tables, state and output.
+struct GatherLayers {
+  const PlanDev* pdg[kMaxGatherLayers];
+  uint32_t* err[kMaxGatherLayers];
+  const int32_t* prev[kMaxGatherLayers];
+  const uint8_t* table[kMaxGatherLayers];
+  const __half* scales[kMaxGatherLayers];
+  uint4* out[kMaxGatherLayers];
+};
+
 // Per-lane table constants of one of the R rows a token reads: the lanes of a
 // warp own rows lane and lane + 32 (R <= 64).
 struct RowConst {

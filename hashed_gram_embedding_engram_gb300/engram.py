@@ -372,6 +372,33 @@ class EngramCache:
 _COPY_STREAMS = {}
 
 
+def stage_a_layers(plans: Sequence["EngramPlan"], ids: torch.Tensor, proj: torch.Tensor,
+                   tables: Sequence[torch.Tensor], scales: Optional[Sequence[torch.Tensor]] = None,
+                   prev_ids: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                   outs: Optional[Sequence[torch.Tensor]] = None) -> list:
+    """Stage A of several layers of one shape in one launch (engram_stage_a_layers):
+    int32 ids [B, T] -> one e [B*T, d_mem] per plan, the bits of per-layer stage_a."""
+    n = len(plans)
+    if n == 0 or len(tables) != n or (scales is not None and len(scales) != n) or \
+            (prev_ids is not None and len(prev_ids) != n) or (outs is not None and len(outs) != n):
+        raise ValueError("stage_a_layers: plans, tables, scales, prev_ids and outs must have one entry per layer")
+    B, T = ids.shape
+    p0 = plans[0]
+    if outs is None:
+        outs = [torch.empty(B * T, p.d_mem, dtype=p.act_torch_dtype, device=ids.device) for p in plans]
+    arr = lambda vals: (ctypes.c_void_p * n)(*vals)  # noqa: E731
+    h = arr([p._h.value for p in plans])
+    tab = arr([_dev_or_pinned(t, "table", _TABLE_DTYPES[p.table_dtype][1]) for p, t in zip(plans, tables)])
+    sc = 0 if scales is None else arr([_dev_or_pinned(s, "scales", torch.float16) for s in scales])
+    prev = 0 if prev_ids is None else arr(
+        [0 if x is None else _dev(x, "prev_ids", torch.int32, (B, p.N - 1)) for p, x in zip(plans, prev_ids)])
+    out = arr([_dev(o, "e_out", p.act_torch_dtype, (B * T, p.d_mem)) for p, o in zip(plans, outs)])
+    _lib.check(p0._lib.engram_stage_a_layers(n, h, _dev(ids, "ids", torch.int32), B, T,
+                                             _dev(proj, "proj", torch.int32), proj.numel(), prev, tab, sc, out,
+                                             _stream()), "engram_stage_a_layers")
+    return list(outs)
+
+
 def _copy_streams(dev):
     """The host-to-device and device-to-host copy streams of a device, shared by
     every EngramLayer on it so that their transfers cross the link in order."""

@@ -173,6 +173,26 @@ engram_status_t engram_stage_a(const engram_plan_t* plan, const int32_t* ids, in
                                const void* table, const uint16_t* scales, void* e_out,
                                engram_stream_t stream);
 
+/* Stage A of several layers in one launch: engram_stage_a for layer l =
+ * 0..n_layers-1 with plans[l], tables[l], scales[l] (or scales == NULL for
+ * tables without scales), prev_ids[l] (or prev_ids == NULL: fresh sequences in
+ * every layer) and e_out[l], all of one shape: the plans share N, K, row_dim,
+ * table_dtype, act_dtype and the device, and the tables are either all in
+ * device memory or all in pinned host memory.  ids, proj and V are common to
+ * the layers (the token stream and P).  Indices depend on the tokens only
+ * ("DeepSeek Engram 系列导读", section "Engram 工作原理", Stage A), so every
+ * layer's lookups can be issued together: one grid (grid.y = layer) in place
+ * of n_layers launches, which lets a step start its first Stage B sooner than
+ * a chain of per-layer gathers that occupy the SMs in turn.  Writes exactly
+ * what n_layers engram_stage_a calls write.  1 <= n_layers <= 8; plans that
+ * differ in shape, or n_layers out of range: ENGRAM_ERR_INVALID_ARG.  Errors
+ * found by the kernel go to each layer's own plan. */
+engram_status_t engram_stage_a_layers(int n_layers, const engram_plan_t* const* plans,
+                                      const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                                      const int32_t* const* prev_ids, const void* const* tables,
+                                      const uint16_t* const* scales, void* const* e_out,
+                                      engram_stream_t stream);
+
 /* Step 5 alone (inspection / reuse of k and v).  e: [ntok, d_mem] act_dtype;
  * w_kv as in engram_weights_t; kv_out: [ntok, (M+1)*d] act_dtype =
  * e . w_kv^T (fp32 accumulation, one rounding to act_dtype), columns [0,d) = v,
