@@ -386,8 +386,8 @@ engram_status_t engram_plan_set_cta_pairs(engram_plan_t* plan, int enable);
  * gate, conv + residual; then the state update when a state is given.  Chunks
  * of one position (T = 1, decode) run the gate, conv, residual and state
  * update as one kernel after the K/V projection, or, with the one-launch
- * decode (engram_plan_set_fused_decode, the default where it applies), the
- * whole step is one traced interval.  Where the conv computes the
+ * decode (engram_plan_set_fused_decode, off by default), the whole step is
+ * one traced interval.  Where the conv computes the
  * gate itself there is no finalize kernel; where Stage B is one cooperative
  * launch (engram_plan_set_fused_stage_b), its events bracket the counter
  * reset and that launch together.
