@@ -1037,6 +1037,8 @@ PROFILE_CASES = {
     "multibranch": "multibranch_n4 with 4 x 8192 tokens and small tables, engram_forward x2",
     # the prefill workload with the e4m3 projection (W_kv quantised once), engram_forward x4
     "prefill_fp8": "prefill_bf16 layer 1 with e4m3 W_kv and per-token e4m3 e, engram_forward x4",
+    # the timed step's Stage A: both prefill layers (2 x 1.32 GB of tables) in one launch, x4
+    "prefill_stage_a_layers": "prefill_bf16 layers 1 and 15 (B=1, T=4096), engram_stage_a_layers x4",
 }
 
 
@@ -1044,7 +1046,7 @@ def run_profile_case(name: str) -> None:
     import torch
     import workloads as W
     from workloads.torch_layer import make_layer, to_torch
-    if name in ("prefill", "prefill_fp8"):
+    if name in ("prefill", "prefill_fp8", "prefill_stage_a_layers"):
         w, reps = W.PREFILL_BF16, 4
     elif name == "uva_gather":
         w, reps = W.INT8_HOST.scaled(B=16), 4
@@ -1059,7 +1061,17 @@ def run_profile_case(name: str) -> None:
         q, sc = plan.quantize_fp8(weights.w_kv)
         weights = dataclass_replace(weights, w_kv=None, w_kv_fp8=q, w_kv_scale=sc)
     ids = torch.from_numpy(ids_np).cuda()
-    if name == "uva_gather":
+    if name == "prefill_stage_a_layers":
+        from hashed_gram_embedding_engram_gb300 import stage_a_layers
+        L2 = W.layer_inputs(w, w.layers[1])
+        plan2, weights2, _, _ = make_layer(w, L2, P, w.ntok)
+        del L2
+        outs = [torch.empty(w.ntok, w.d_mem, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        for _ in range(reps):
+            stage_a_layers([plan, plan2], ids, proj, [weights.table, weights2.table], outs=outs)
+        torch.cuda.synchronize()
+        assert plan2.get_error()[0] == 0
+    elif name == "uva_gather":
         table_host = to_torch(L.table, w.table_dtype, "cpu", pin=True)
         e = torch.empty(w.ntok, w.d_mem, dtype=torch.bfloat16, device="cuda")
         for _ in range(reps):

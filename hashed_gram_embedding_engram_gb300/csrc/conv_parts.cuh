@@ -134,17 +134,37 @@ __device__ __forceinline__ void conv_coords(const ConvArgs& a, int tile, int& b,
   c0 = ct * a.CS;
 }
 
+// One thread: the first of a tile's three TMA copies into the stage at
+// `base` -- its H rows -- after arming the stage's barrier for all three.  H
+// is written by no kernel between the previous Stage B and this conv (the
+// K/V projection and the gate only read it), so this copy may be issued
+// before the dependency wait.
+__device__ __forceinline__ void conv_issue_h(const ConvArgs& a, const CUtensorMap* tm_h, uint8_t* base,
+                                             uint64_t* full, int tile, int M) {
+  int b, t0, c0;
+  conv_coords(a, tile, b, t0, c0);
+  ptx::mbar_arrive_expect_tx(full, a.tx_bytes);
+  ptx::tma_load_2d_nohint(base + a.h_off, tm_h, full, c0, (b * a.Tn + t0) * M);
+}
+
+// The other two: v rows with the causal halo and the gate partials (KFIN) or
+// sa rows, both written by the kernels just before the conv.
+template <bool KFIN>
+__device__ __forceinline__ void conv_issue_rest(const ConvArgs& a, const CUtensorMap* tm_v, const CUtensorMap* tm_sa,
+                                                uint8_t* base, uint64_t* full, int tile) {
+  int b, t0, c0;
+  conv_coords(a, tile, b, t0, c0);
+  const int32_t row0 = b * a.Tn + t0 - a.h0;       // may be negative: zero fill
+  ptx::tma_load_2d_nohint(base + a.v_off, tm_v, full, c0, row0);
+  ptx::tma_load_2d_nohint(base + (KFIN ? a.p_off : a.sa_off), tm_sa, full, 0, row0);
+}
+
 // One thread: the three TMA copies of a tile into the stage at `base`.
 template <bool KFIN>
 __device__ __forceinline__ void conv_issue(const ConvArgs& a, const CUtensorMap* tm_v, const CUtensorMap* tm_h,
                                            const CUtensorMap* tm_sa, uint8_t* base, uint64_t* full, int tile, int M) {
-  int b, t0, c0;
-  conv_coords(a, tile, b, t0, c0);
-  const int32_t row0 = b * a.Tn + t0 - a.h0;       // may be negative: zero fill
-  ptx::mbar_arrive_expect_tx(full, a.tx_bytes);
-  ptx::tma_load_2d_nohint(base + a.v_off, tm_v, full, c0, row0);
-  ptx::tma_load_2d_nohint(base + a.h_off, tm_h, full, c0, (b * a.Tn + t0) * M);
-  ptx::tma_load_2d_nohint(base + (KFIN ? a.p_off : a.sa_off), tm_sa, full, 0, row0);
+  conv_issue_h(a, tm_h, base, full, tile, M);
+  conv_issue_rest<KFIN>(a, tm_v, tm_sa, base, full, tile);
 }
 
 // One warp: the (s, alpha) rows of a staged tile from its partials (8 slices

@@ -152,7 +152,11 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
     ptx::fence_mbar_init();
   }
   __syncthreads();
-  ptx::grid_dep_wait();
+  // Only the producer waits for the kernels before this one: every copy of
+  // their results (v, the gate partials or sa rows) is issued after its wait,
+  // and the other warps read those results, and write H, only after a stage
+  // they wait for has landed.  H itself, the state and the weights are
+  // written by no kernel of this Stage B.
   ptx::grid_dep_launch();
 
   if constexpr (KFIN) {
@@ -182,10 +186,21 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
       ptx::tma_prefetch_desc(&tm_h);
       ptx::tma_prefetch_desc(&tm_sa);
       uint32_t armed = 0;                            // stages with a copy issued and not yet seen complete
+      // the H rows of the first tiles (one per stage) while the previous kernel finishes
+      int n_pre = 0;
+      for (int tile = blockIdx.x; tile < a.n_tiles && n_pre < kConvStages; tile += gridDim.x, ++n_pre) {
+        conv_issue_h(a, &tm_h, smem + n_pre * a.stage_bytes, &full[n_pre], tile, M);
+        armed |= 1u << n_pre;
+      }
+      ptx::grid_dep_wait();
       int k = 0;
       for (int tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
         const int st = k % kConvStages;
         const uint32_t round = static_cast<uint32_t>(k / kConvStages);
+        if (k < n_pre) {
+          conv_issue_rest<KFIN>(a, &tm_v, &tm_sa, smem + st * a.stage_bytes, &full[st], tile);
+          continue;
+        }
         if (round > 0 && !ptx::mbar_wait_bounded(&empty[st], (round - 1) & 1u, kConvWaitNs)) {
           atomicOr(a.err, kErrTimeout);
           *reinterpret_cast<volatile int*>(&s_abort) = 1;
@@ -261,8 +276,10 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
 // of the new position -- the slot its own tap at lag (w-1)*dilation just read,
 // so no other thread touches it.  Thread 0 then rolls the projected ids and
 // advances pos.  The result equals finalize + conv + state bit for bit.  Each
-// thread loads its first channel group's taps, v, ring rows and H before the
-// barrier that publishes the gate, so those loads overlap warp 0's gate.
+// thread loads its first channel group's taps, ring rows and H before the
+// dependency wait (none of them comes from the K/V projection) and its v
+// before the barrier that publishes the gate, so those loads overlap the
+// projection's tail and warp 0's gate.
 template <typename TH, int W, bool kPart>
 __global__ void __launch_bounds__(256) decode_tail_kernel(
     const float* __restrict__ gate_in, int n_sl, int pstride, int saw, float eps, const float* __restrict__ v,
@@ -271,11 +288,18 @@ __global__ void __launch_bounds__(256) decode_tail_kernel(
     const int32_t* __restrict__ proj, int V, int32_t* __restrict__ prev, int N, float* __restrict__ sa_out,
     uint32_t* __restrict__ err, TH* __restrict__ H) {
   __shared__ float s_sa[2 * kMaxM];
+  // the state, taps and H: written by no kernel of this call (the previous
+  // kernel, the K/V projection, writes only v and the partials), so they load
+  // while the projection finishes
+  TailPre<W> t;
+  int32_t roll[kMaxN];
+  decode_tail_pre<TH, W>(t, roll, blockIdx.x, threadIdx.x, M, d, dil, g_c, conv, ring, pos, L, ids, proj, V, prev, N,
+                         H);
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  decode_tail_seq<TH, W, kPart, true>(blockIdx.x, threadIdx.x, blockDim.x, s_sa, gate_in, n_sl, pstride, saw, eps,
-                                      v, sv, M, d, dil, g_c, conv, ring, pos, L, ids, proj, V, prev, N, sa_out, err,
-                                      H, [] { __syncthreads(); });
+  decode_tail_main<TH, W, kPart, true>(t, roll, blockIdx.x, threadIdx.x, blockDim.x, s_sa, gate_in, n_sl, pstride, saw, eps,
+                                       v, sv, M, d, dil, g_c, conv, ring, pos, L, prev, N, sa_out, err, H,
+                                       [] { __syncthreads(); });
 }
 
 template <typename TH, bool kPart>
