@@ -229,8 +229,11 @@ __device__ __forceinline__ void conv_load_taps(const ConvArgs& a, int c, float (
   }
 }
 
-// One thread: the chains rot, rot + npar, ... of the staged tile at `base`,
-// channels c = c0 + 4g .. c+3 (taps in wq).
+// One thread: the work items rot, rot + npar, ... of the staged tile at
+// `base`, channels c = c0 + 4g .. c+3 (taps in wq).  An item is one chain of
+// one branch (item = chain * M + branch), so with several branches the chains
+// of a tile spread over more threads; a thread reads its chain's v rows from
+// shared memory for each item it takes.
 template <typename TH, int W, int DIL, int MC, int CSC>
 __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base, int tile, int g, int rot, int npar,
                                           const float (&wq)[4][W], TH* __restrict__ H) {
@@ -252,7 +255,9 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
   TH* const hbase = H + (static_cast<int64_t>(b) * a.Tn + t0) * hrow + c;   // position t0, branch 0
   // chains of kChain outputs a dilation apart: first output tb = q*kChain*dil + rr
   const int n_chains = (nt + kChain * dil - 1) / (kChain * dil) * dil;
-  for (int ch = rot; ch < n_chains; ch += npar) {
+  for (int it = rot; it < n_chains * M; it += npar) {
+    const int ch = MC == 1 ? it : it / M;
+    const int m = MC == 1 ? 0 : it - ch * M;
     const int tb = (ch / dil) * (kChain * dil) + ch % dil;
     if (tb >= nt) continue;
     if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
@@ -263,8 +268,7 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
       float vr[kRows][4];
 #pragma unroll
       for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
-#pragma unroll 1
-      for (int m = 0; m < M; ++m) {
+      {
         float u[kRows][4], h[kChain][4], at[kChain];
 #pragma unroll
         for (int o = 0; o < kChain; ++o) {
@@ -310,8 +314,7 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
         for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
       }
     }
-#pragma unroll 1
-    for (int m = 0; m < M; ++m) {
+    {
       float u[kRows][4];                          // conv input RMSNorm(v~) before g_c: s * v, or the ring
 #pragma unroll
       for (int j = 0; j < kRows; ++j) {
