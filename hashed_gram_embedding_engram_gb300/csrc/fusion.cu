@@ -279,9 +279,11 @@ __global__ void __launch_bounds__(kConvThreads + (KFIN ? 64 : 32), 1)
 // thread loads its first channel group's taps, ring rows and H before the
 // dependency wait (none of them comes from the K/V projection) and its v
 // before the barrier that publishes the gate, so those loads overlap the
-// projection's tail and warp 0's gate.
+// projection's tail and warp 0's gate.  Three blocks fit an SM (80 registers
+// a thread): 256 sequences' blocks are all resident beside the projection's
+// blocks (64 SMs at decode sizes), so all of them load ahead of the wait.
 template <typename TH, int W, bool kPart>
-__global__ void __launch_bounds__(256) decode_tail_kernel(
+__global__ void __launch_bounds__(256, 3) decode_tail_kernel(
     const float* __restrict__ gate_in, int n_sl, int pstride, int saw, float eps, const float* __restrict__ v,
     int64_t sv, int M, int d, int dil, const float* __restrict__ g_c, const float* __restrict__ conv,
     float* __restrict__ ring, int32_t* __restrict__ pos, int L, const int32_t* __restrict__ ids,
