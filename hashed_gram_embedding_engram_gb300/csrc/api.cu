@@ -69,8 +69,15 @@ engram_status_t device_view(const void* ptr, const void** out, bool* on_host = n
 }
 
 // Tracing: record the plan's next event on `s` (no-op unless timing is on).
+// Under stream capture the event becomes an event-record node of the graph
+// (cudaEventRecordExternal), so every replay records it again.
 void mark(const engram_plan* p, cudaStream_t s) {
-  if (p->timing && p->n_marks < engram_plan::kMaxMarks) cudaEventRecord(p->marks[p->n_marks++], s);
+  if (!p->timing || p->n_marks >= engram_plan::kMaxMarks) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(p->marks[p->n_marks++], s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(p->marks[p->n_marks++], s);
 }
 
 engram_status_t check_tokens(const engram_plan* p, int B, int T) {

@@ -392,7 +392,9 @@ engram_status_t engram_plan_set_cta_pairs(engram_plan_t* plan, int enable);
  * launch (engram_plan_set_fused_stage_b), its events bracket the counter
  * reset and that launch together.
  * engram_stage_b records the same list without the first kernel.  For use on
- * one stream at a time, outside CUDA-graph capture.  enable: 0 or 1. */
+ * one stream at a time.  A call captured into a CUDA graph records its events
+ * as event-record nodes: after each replay, engram_plan_kernel_times reads
+ * that replay's times (until the plan's next call).  enable: 0 or 1. */
 engram_status_t engram_plan_set_timing(engram_plan_t* plan, int enable);
 
 /* Wait for the last call's events and write the device time of each kernel it

@@ -128,3 +128,31 @@ def test_fused_stage_b_repeats_and_reuses_its_workspace():
         torch.cuda.synchronize()
         assert torch.equal(H.view(torch.int16), ref.view(torch.int16))
     assert plan.get_error() == (0, 0)
+
+
+def test_tracing_inside_a_graph():
+    """A traced call captured into a CUDA graph records its events as graph
+    nodes: every replay gives one interval per kernel, and the same bits."""
+    w = BASE.scaled(B=2, T=900)
+    ids, P, L = layer(w)
+    ref, _ = forward(w, ids, P, L, False)
+    plan, weights, proj, H0 = make_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    ws = plan.new_workspace(ids.size)
+    H = H0.clone()
+    plan.set_timing(True)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            plan.forward(ids_d, proj, weights, H, None, ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        H.copy_(H0)
+        g.replay()
+        torch.cuda.synchronize()
+        t = plan.kernel_times()
+        assert len(t) in (3, 4) and all(x > 0 for x in t)
+        assert torch.equal(H.view(torch.int16), ref.view(torch.int16))
+    assert plan.get_error() == (0, 0)
