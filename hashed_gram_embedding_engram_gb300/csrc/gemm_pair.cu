@@ -11,12 +11,15 @@
 // instruction reads A from each SM's shared memory and B from both; each SM's
 // TMEM receives its 128 rows x 256 columns.  Operand traffic per FLOP, into
 // and out of each SM's shared memory, drops by a third.
-// Measured on GB300 (4096 x 2048 x 1024, warm): both forms run the mainloop
-// at the tensor rate (about 0.35 us per k-block of 128 x 256 per SM), and the
-// pair form takes 24.2 us against 22.2 us: its set-up (cluster barrier,
-// paired TMEM allocation) and a stall of a pair's second tile while the first
-// tile's epilogue runs outweigh the smaller loads.  It is selectable
-// (engram_plan_set_cta_pairs) and gives the same bits.
+// Measured on GB300 (4096 x 2048 x 1024, event-timed): 24.2 us against
+// 22.2 us for the one-SM form.  A globaltimer timeline of both (L2 flushed, e
+// just written) shows why: the pair's first tile runs its mainloop at 94 % of
+// the MMA rate (5.6 us against 6.1 us on one SM: the 4-stage ring covers the
+// refill latency), but the cluster barrier and the paired TMEM allocation
+// start it 1.3 us later, and its second tile's mainloop takes 6.9-7.2 us while
+// the first wave's epilogues -- all v tiles, 128 KB of stores per SM -- go out
+// through the same TMA unit.  It is selectable (engram_plan_set_cta_pairs)
+// and gives the same bits.
 //
 // Roles (320 threads per CTA, one CTA per SM, persistent over pair tiles):
 //   warp 0      both CTAs: TMA producer of the CTA's own A rows and B half into
