@@ -415,7 +415,10 @@ class EngramLayer:
     engram_forward.  With H (and ids) in host memory the layer is pipelined
     in ``chunks`` pieces over three streams: the copy of piece i+1 to the
     device, the layer on piece i and the copy of piece i-1 back to the host
-    overlap (use pinned host tensors, or the copies serialise).  Pieces split
+    overlap (use pinned host tensors, or the copies serialise).  A piece's
+    token ids cross first, and its Stage A (engram_stage_a: Steps 1-4, which
+    need the ids only) runs while its H still crosses the link; its Stage B
+    (engram_stage_b) follows once H has arrived.  Pieces split
     the batch when B >= chunks (sequences are independent), else the
     positions of a single-sequence batch with a streaming state carried from
     piece to piece; both give the bits of one whole-batch call.  A state
@@ -436,6 +439,7 @@ class EngramLayer:
         self.chunks = max(1, int(chunks))
         self._ws = None
         self._dev_buf = None
+        self._e_buf = None
         # (event, recorded during a graph capture): the previous call is done with the device
         # buffers; its copy back to the host completed.  An event is waited on only in the mode
         # it was recorded in: a capture may not wait on eager work (which a capture follows
@@ -448,6 +452,13 @@ class EngramLayer:
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(max(1, need), dtype=torch.uint8, device=device)
         return self._ws
+
+    def _rows_buffer(self, ntok: int, dev) -> torch.Tensor:
+        """Gathered rows e [ntok, d_mem] for Stage A of one piece (reused)."""
+        p = self.plan
+        if self._e_buf is None or self._e_buf.shape[0] < ntok:
+            self._e_buf = torch.empty(max(1, ntok), p.d_mem, dtype=p.act_torch_dtype, device=dev)
+        return self._e_buf[:ntok]
 
     def _buffers(self, ids: torch.Tensor, H: torch.Tensor, dev):
         key = (tuple(ids.shape), tuple(H.shape), H.dtype)
@@ -498,13 +509,21 @@ class EngramLayer:
             h_h, h_d = H[sl], H_d[sl]
             with torch.cuda.stream(s_in):
                 i_d.copy_(i_h, non_blocking=True)
+                ids_ready = torch.cuda.Event()
+                ids_ready.record(s_in)
                 h_d.copy_(h_h, non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(s_in)
-            main.wait_event(ready)
-            i_c, h_c = (i_d, h_d) if along_b else (i_d.contiguous(), h_d.contiguous())
+            main.wait_event(ids_ready)
+            i_c = i_d if along_b else i_d.contiguous()
             pst = (None if state is None else state.rows(lo, hi)) if along_b else st
-            self.plan.forward(i_c, self.proj, self.weights, h_c, pst, ws)
+            # Stage A needs the ids only: it runs while this piece's H still crosses the link
+            e = self.plan.stage_a(i_c, self.proj, self.weights.table, self.weights.scales,
+                                  prev_ids=None if pst is None else pst.prev_ids,
+                                  out=self._rows_buffer(i_c.numel(), dev))
+            main.wait_event(ready)
+            h_c = h_d if along_b else h_d.contiguous()
+            self.plan.stage_b(e, self.weights, h_c, pst, ids=i_c, proj=self.proj, workspace=ws)
             done = torch.cuda.Event()
             done.record(main)
             with torch.cuda.stream(s_out):
