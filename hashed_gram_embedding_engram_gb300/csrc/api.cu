@@ -208,6 +208,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   p->fused_stage_b = false;
   p->cta_pairs = false;
   p->fused_decode = false;
+  p->sm_limit = 0;
 
   PlanDev h{};
   h.R = R;
@@ -425,16 +426,18 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     int n_sl = 0, pstride = 0;
     if (f8) {
       // e4m3 projection: each token's row of e quantised, then the GEMM on the codes
-      if (engram::launch_quantize_rows_e4m3(e, ntok, plan->d_mem, ws.e8, ws.e_scale, plan->num_sms, s) !=
+      if (engram::launch_quantize_rows_e4m3(e, ntok, plan->d_mem, ws.e8, ws.e_scale, engram::stage_b_sms(plan), s) !=
           cudaSuccess)
         return ENGRAM_ERR_CUDA;
       mark(plan, s);
       if (engram::gemm_e4m3_engram(ws.e8, ws.e_scale, w->w_kv_fp8, w->w_kv_scale, ntok, d, M, plan->d_mem, H, w->g_h,
-                                   w->g_k, ws.v32, ws.part, &n_sl, &pstride, plan->num_sms, &plan->dev->err, s) !=
+                                   w->g_k, ws.v32, ws.part, &n_sl, &pstride, engram::stage_b_sms(plan),
+                                   &plan->dev->err, s) !=
           cudaSuccess)
         return ENGRAM_ERR_CUDA;
     } else if (engram::gemm_bf16_engram(e, w->w_kv, ntok, d, M, plan->d_mem, H, w->g_h, w->g_k, ws.v32, ws.part,
-                                        &n_sl, &pstride, plan->num_sms, &plan->dev->err, s, plan->cta_pairs) !=
+                                        &n_sl, &pstride, engram::stage_b_sms(plan), &plan->dev->err, s,
+                                        plan->cta_pairs) !=
                cudaSuccess) {
       return ENGRAM_ERR_CUDA;
     }
@@ -797,6 +800,16 @@ engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable) {
   if (!plan || (enable != 0 && enable != 1)) return ENGRAM_ERR_INVALID_ARG;
   plan->fused_stage_b = enable != 0;
   return ENGRAM_OK;
+}
+
+engram_status_t engram_plan_set_sm_limit(engram_plan_t* plan, int n_sms) {
+  if (!plan || n_sms < 0) return ENGRAM_ERR_INVALID_ARG;
+  plan->sm_limit = n_sms;
+  return ENGRAM_OK;
+}
+
+int engram_plan_host_gather_sms(const engram_plan_t* plan) {
+  return plan ? engram::hostgrid_sms(plan->num_sms) : 0;
 }
 
 engram_status_t engram_plan_set_fused_decode(engram_plan_t* plan, int enable) {

@@ -62,9 +62,18 @@ struct engram_plan {
   bool fused_stage_b;              // Stage B as one cooperative launch where launch_stage_b_fused applies
   bool cta_pairs;                  // the K/V projection's 256-column tiles on CTA pairs (gemm_pair.cu)
   bool fused_decode;               // chunks of one position as one cooperative launch (decode.cu)
+  int sm_limit;                    // SMs Stage B's persistent kernels may use (0: all)
 };
 
 namespace engram {
+
+// SMs a Stage A over tables in host memory occupies (gather.cu): one 1024-thread block each.
+int hostgrid_sms(int num_sms);
+
+// SMs the persistent Stage B kernels (K/V projection, conv) size their grids and tiles for.
+inline int stage_b_sms(const engram_plan* p) {
+  return p->sm_limit > 0 && p->sm_limit < p->num_sms ? p->sm_limit : p->num_sms;
+}
 
 // Launch `k` with programmatic stream serialisation: its blocks may be
 // scheduled while the previous kernel on `s` drains; the kernel itself waits

@@ -478,7 +478,7 @@ int sa_row_floats(int M) { return (2 * M + 3) / 4 * 4; }
 
 cudaError_t launch_finalize(const engram_plan* p, const float* part, int n_sl, int pstride, int64_t ntok, float* sa,
                             cudaStream_t s) {
-  return launch_pdl(finalize_kernel, dim3(grid_for(ntok * 32, 256, p->num_sms)), dim3(256), 0, s, part, n_sl, pstride,
+  return launch_pdl(finalize_kernel, dim3(grid_for(ntok * 32, 256, stage_b_sms(p))), dim3(256), 0, s, part, n_sl, pstride,
                     ntok, p->cfg.M, p->cfg.d, p->cfg.eps, sa, sa_row_floats(p->cfg.M));
 }
 
@@ -560,7 +560,7 @@ cudaError_t conv_prepare(const engram_plan* p, const float* v, int64_t sv, const
     const int64_t lanes = static_cast<int64_t>(B) * a.n_ct;
     auto cost = [&](int sc) {
       const int64_t tiles = lanes * ((T + sc - 1) / sc);
-      const int64_t waves = (tiles + p->num_sms - 1) / p->num_sms;
+      const int64_t waves = (tiles + stage_b_sms(p) - 1) / stage_b_sms(p);
       return waves * (sc + (sc < T ? halo : 0) + 8);
     };
     int best_s = S;
@@ -619,7 +619,7 @@ cudaError_t launch_conv_residual(const engram_plan* p, const float* v, int64_t s
   const cudaError_t e =
       conv_prepare(p, v, sv, sa, B, T, g_c, conv, H, state, part, sa_out, &a, &tv, &th, &ts, &smem, 227 * 1024);
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, p->num_sms));
+  const int grid = static_cast<int>(std::min<int64_t>(a.n_tiles, stage_b_sms(p)));
   if (p->cfg.act_dtype == ENGRAM_F32) return conv_dispatch<float>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, false, s);
   return conv_dispatch<__nv_bfloat16>(p->cfg.conv_w, tv, th, ts, a, grid, smem, H, part != nullptr, s);
 }

@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
 // ~200 GB/s the link delivers (NVLink-C2C, as measured with pinned copies);
 // the rest stay free for work that runs beside the lookup.
 constexpr int kHostBlk = 1024;
-int hostgrid_sms(int num_sms) { return num_sms / 4 > 0 ? num_sms / 4 : 1; }
+}  // namespace
+int hostgrid_sms(int num_sms);
+namespace {
 
 int grid_for_tokens(const engram_plan* p, int64_t ntok, bool host_table = false) {
   const int64_t warps_per_block = (host_table ? kHostBlk : kThreads) / 32;
@@ -291,6 +293,8 @@ int chunks_per_row(const engram_plan* p) {
 }
 
 }  // namespace
+
+int hostgrid_sms(int num_sms) { return num_sms / 4 > 0 ? num_sms / 4 : 1; }
 
 #define ENGRAM_DISPATCH_CPR(CALL)                                                  \
   switch (chunks_per_row(p)) {                                                     \

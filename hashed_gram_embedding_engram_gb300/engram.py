@@ -285,6 +285,14 @@ class EngramPlan:
         """The K/V projection's 256-column tiles on CTA pairs (cta_group::2), or one SM each; same bits."""
         _lib.check(self._lib.engram_plan_set_cta_pairs(self._h, int(bool(enable))), "engram_plan_set_cta_pairs")
 
+    def set_sm_limit(self, n_sms: int) -> None:
+        """At most n_sms SMs for Stage B's persistent kernels (0: all); the results do not depend on it."""
+        _lib.check(self._lib.engram_plan_set_sm_limit(self._h, int(n_sms)), "engram_plan_set_sm_limit")
+
+    def host_gather_sms(self) -> int:
+        """SMs a Stage A over tables in pinned host memory occupies."""
+        return int(self._lib.engram_plan_host_gather_sms(self._h))
+
     def set_timing(self, enable: bool) -> None:
         """Record CUDA events around each kernel of later forward / stage_b calls."""
         _lib.check(self._lib.engram_plan_set_timing(self._h, int(bool(enable))), "engram_plan_set_timing")

@@ -367,6 +367,22 @@ engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable);
  * back to separate launches.  enable: 0 or 1; applies to calls made after it. */
 engram_status_t engram_plan_set_fused_decode(engram_plan_t* plan, int enable);
 
+/* At most n_sms SMs for Stage B's persistent kernels (the K/V projection,
+ * the conv, their tile shapes chosen for that many SMs); 0 (the default): all
+ * of them.  For running Stage B beside other work that holds the remaining
+ * SMs: chiefly the Stage A of the next piece of a batch over tables in pinned
+ * host memory, whose gather occupies engram_plan_host_gather_sms(plan) whole
+ * SMs while the host link sets its pace ("DeepSeek Engram 系列导读", section
+ * "Engram 工作原理": the lookup depends on the tokens only and can run ahead).
+ * The results do not depend on it.  n_sms >= 0; applies to calls made after it. */
+engram_status_t engram_plan_set_sm_limit(engram_plan_t* plan, int n_sms);
+
+/* The number of SMs a Stage A (engram_stage_a, engram_stage_a_layers,
+ * engram_forward's gather) over tables in pinned host memory occupies: its
+ * gather runs as one 1024-thread block per SM on that many SMs, leaving the
+ * others to concurrent work.  0 for a null plan. */
+int engram_plan_host_gather_sms(const engram_plan_t* plan);
+
 /* The K/V projection (Step 5, bf16 layers) in 256 x 256 output tiles on CTA
  * pairs (enable = 1): two SMs of a thread-block cluster share one
  * tcgen05.mma.cta_group::2 tile, each staging its 128 rows of e and half of
