@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libengram_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
-SOURCES = ["api.cu", "hash.cu", "gather.cu", "gemm.cu", "gemm_pair.cu", "fusion.cu", "tma.cu", "noalloc.cu", "cache.cu", "stage_b.cu", "decode.cu", "quant.cu"]
+SOURCES = ["api.cu", "hash.cu", "gather.cu", "gemm.cu", "gemm_pair.cu", "fusion.cu", "tma.cu", "noalloc.cu", "cache.cu", "stage_b.cu", "decode.cu", "quant.cu", "smsplit.cu"]
 
 
 def nvcc() -> str:

@@ -209,6 +209,7 @@ engram_status_t engram_plan_create(const engram_config_t* cfg, int64_t max_token
   p->cta_pairs = false;
   p->fused_decode = false;
   p->sm_limit = 0;
+  p->host_sms = 0;
 
   PlanDev h{};
   h.R = R;
@@ -809,7 +810,13 @@ engram_status_t engram_plan_set_sm_limit(engram_plan_t* plan, int n_sms) {
 }
 
 int engram_plan_host_gather_sms(const engram_plan_t* plan) {
-  return plan ? engram::hostgrid_sms(plan->num_sms) : 0;
+  return plan ? engram::hostgrid_sms(plan) : 0;
+}
+
+engram_status_t engram_plan_set_host_gather_sms(engram_plan_t* plan, int n_sms) {
+  if (!plan || n_sms < 0) return ENGRAM_ERR_INVALID_ARG;
+  plan->host_sms = n_sms;
+  return ENGRAM_OK;
 }
 
 engram_status_t engram_plan_set_fused_decode(engram_plan_t* plan, int enable) {

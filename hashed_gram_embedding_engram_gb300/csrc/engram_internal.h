@@ -63,12 +63,16 @@ struct engram_plan {
   bool cta_pairs;                  // the K/V projection's 256-column tiles on CTA pairs (gemm_pair.cu)
   bool fused_decode;               // chunks of one position as one cooperative launch (decode.cu)
   int sm_limit;                    // SMs Stage B's persistent kernels may use (0: all)
+  int host_sms;                    // blocks of a Stage A over host-memory tables (0: a quarter of the SMs)
 };
 
 namespace engram {
 
 // SMs a Stage A over tables in host memory occupies (gather.cu): one 1024-thread block each.
-int hostgrid_sms(int num_sms);
+inline int hostgrid_sms(const engram_plan* p) {
+  if (p->host_sms > 0) return p->host_sms < p->num_sms ? p->host_sms : p->num_sms;
+  return p->num_sms / 4 > 0 ? p->num_sms / 4 : 1;
+}
 
 // SMs the persistent Stage B kernels (K/V projection, conv) size their grids and tiles for.
 inline int stage_b_sms(const engram_plan* p) {

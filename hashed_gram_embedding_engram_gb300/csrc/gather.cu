@@ -226,14 +226,11 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
 // ~200 GB/s the link delivers (NVLink-C2C, as measured with pinned copies);
 // the rest stay free for work that runs beside the lookup.
 constexpr int kHostBlk = 1024;
-}  // namespace
-int hostgrid_sms(int num_sms);
-namespace {
 
 int grid_for_tokens(const engram_plan* p, int64_t ntok, bool host_table = false) {
   const int64_t warps_per_block = (host_table ? kHostBlk : kThreads) / 32;
   int64_t blocks = (ntok + warps_per_block - 1) / warps_per_block;
-  const int64_t cap = host_table ? hostgrid_sms(p->num_sms) : static_cast<int64_t>(p->num_sms) * 8;
+  const int64_t cap = host_table ? hostgrid_sms(p) : static_cast<int64_t>(p->num_sms) * 8;
   if (blocks > cap) blocks = cap;
   return static_cast<int>(blocks);
 }
@@ -266,7 +263,7 @@ cudaError_t launch_fused(const engram_plan* p, int n_layers, const GatherLayers&
                          const int32_t* proj, int V, cudaStream_t s, bool host_table, const RowCache* cache) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
   int gx = grid_for_tokens(p, ntok, host_table);
-  const int cap = host_table ? hostgrid_sms(p->num_sms) : p->num_sms * 8;   // one wave over all layers
+  const int cap = host_table ? hostgrid_sms(p) : p->num_sms * 8;   // one wave over all layers
   if (static_cast<int64_t>(gx) * n_layers > cap) gx = cap / n_layers > 0 ? cap / n_layers : 1;
   const dim3 grid(gx, n_layers);
   const dim3 block(host_table ? kHostBlk : kThreads);
@@ -293,8 +290,6 @@ int chunks_per_row(const engram_plan* p) {
 }
 
 }  // namespace
-
-int hostgrid_sms(int num_sms) { return num_sms / 4 > 0 ? num_sms / 4 : 1; }
 
 #define ENGRAM_DISPATCH_CPR(CALL)                                                  \
   switch (chunks_per_row(p)) {                                                     \

@@ -400,6 +400,7 @@ cudaError_t gemm_bf16_engram_pair(const void* e, const void* w_kv, int64_t Mr, i
   const int64_t tiles = ((Mr + kPairBM - 1) / kPairBM) * (Nc / kPairBN);
   int pairs = max_pairs(num_sms);
   if (pairs <= 0) return cudaErrorInvalidConfiguration;
+  if (pairs > num_sms / 2) pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;   // the SMs granted to this launch
   if (tiles < pairs) pairs = static_cast<int>(tiles);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));

@@ -293,6 +293,10 @@ class EngramPlan:
         """SMs a Stage A over tables in pinned host memory occupies."""
         return int(self._lib.engram_plan_host_gather_sms(self._h))
 
+    def set_host_gather_sms(self, n_sms: int) -> None:
+        """SMs a Stage A over tables in pinned host memory runs on (0: a quarter of them); same bits."""
+        _lib.check(self._lib.engram_plan_set_host_gather_sms(self._h, int(n_sms)), "engram_plan_set_host_gather_sms")
+
     def set_timing(self, enable: bool) -> None:
         """Record CUDA events around each kernel of later forward / stage_b calls."""
         _lib.check(self._lib.engram_plan_set_timing(self._h, int(bool(enable))), "engram_plan_set_timing")
@@ -309,6 +313,41 @@ class EngramPlan:
         flags = ctypes.c_uint32()
         st = self._lib.engram_get_error(self._h, _stream(), ctypes.byref(flags))
         return st, flags.value
+
+
+class SmSplit:
+    """The device's SMs in two disjoint sets, each with one stream whose kernels
+    run on that set only (engram_sm_split_* in include/engram.h).  Group 0 has
+    at least ``n_sms`` SMs (rounded up by the driver), group 1 the rest;
+    ``stream(g)`` is a torch stream over group g's stream."""
+
+    def __init__(self, n_sms: int, device: Optional[int] = None):
+        self._lib = _lib._lib()
+        dev = torch.cuda.current_device() if device is None else int(device)
+        h = ctypes.c_void_p()
+        _lib.check(self._lib.engram_sm_split_create(dev, int(n_sms), ctypes.byref(h)), "engram_sm_split_create")
+        self._h = h
+        self.device = dev
+        self.sms = tuple(int(self._lib.engram_sm_split_sms(h, g)) for g in (0, 1))
+        self._streams = tuple(torch.cuda.ExternalStream(int(self._lib.engram_sm_split_stream(h, g)), device=dev)
+                              for g in (0, 1))
+
+    def stream(self, group: int) -> torch.cuda.Stream:
+        return self._streams[group]
+
+    def close(self) -> None:
+        """Destroys both streams: call after the work on them has completed."""
+        if getattr(self, "_h", None):
+            torch.cuda.synchronize(self.device)
+            self._streams = ()
+            _lib.check(self._lib.engram_sm_split_destroy(self._h), "engram_sm_split_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class EngramCache:

@@ -368,8 +368,9 @@ engram_status_t engram_plan_set_fused_stage_b(engram_plan_t* plan, int enable);
 engram_status_t engram_plan_set_fused_decode(engram_plan_t* plan, int enable);
 
 /* At most n_sms SMs for Stage B's persistent kernels (the K/V projection,
- * the conv, their tile shapes chosen for that many SMs); 0 (the default): all
- * of them.  For running Stage B beside other work that holds the remaining
+ * the conv, their tile shapes chosen for that many SMs) in its two-launch
+ * form, the default; the one-launch cooperative form (set_fused_stage_b)
+ * keeps one block per SM.  0 (the default): all of them.  For running Stage B beside other work that holds the remaining
  * SMs: chiefly the Stage A of the next piece of a batch over tables in pinned
  * host memory, whose gather occupies engram_plan_host_gather_sms(plan) whole
  * SMs while the host link sets its pace ("DeepSeek Engram 系列导读", section
@@ -382,6 +383,40 @@ engram_status_t engram_plan_set_sm_limit(engram_plan_t* plan, int n_sms);
  * gather runs as one 1024-thread block per SM on that many SMs, leaving the
  * others to concurrent work.  0 for a null plan. */
 int engram_plan_host_gather_sms(const engram_plan_t* plan);
+
+/* The number of SMs (one 1024-thread block each) a Stage A over tables in
+ * pinned host memory runs on: n_sms > 0 (capped at the device's SM count),
+ * or 0 for the default, a quarter of the SMs.  For an SM split, set it to
+ * the lookup group's SM count.  The results do not depend on it; n_sms >= 0;
+ * applies to calls made after it. */
+engram_status_t engram_plan_set_host_gather_sms(engram_plan_t* plan, int n_sms);
+
+/* An SM split: the device's SMs in two disjoint sets, each with one
+ * non-blocking stream whose kernels run on that set's SMs only (green
+ * contexts of the driver).  For a batch in pieces over tables in pinned host
+ * memory: each piece's Stage A on group 0's stream, sized to the host gather
+ * (engram_plan_host_gather_sms), and the previous piece's Stage B on group 1's
+ * stream with engram_plan_set_sm_limit(plan, engram_sm_split_sms(split, 1)),
+ * so neither stage's blocks wait for SMs the other holds ("DeepSeek Engram
+ * 系列导读", section "Engram 工作原理": the lookup depends on the tokens only
+ * and can run ahead of the layers that use it).
+ *
+ * engram_sm_split_create: device ordinal; n_sms > 0, below the device's SM
+ * count, is group 0's minimum (the driver rounds it up to its partition
+ * granularity: 8 SMs on this architecture); group 1 holds the rest.  The
+ * streams use the device's primary context, so memory allocated there (by
+ * the CUDA runtime, or PyTorch) is used as is, and events order them against
+ * any other stream.  A driver without green contexts, or a split the driver
+ * refuses: ENGRAM_ERR_UNSUPPORTED.  The split owns both streams; destroy it
+ * after the work on them has completed.
+ * engram_sm_split_sms: the SMs of group 0 or 1 (0 for a null split or
+ * another group).  engram_sm_split_stream: that group's stream (a
+ * cudaStream_t; null for a null split or another group). */
+typedef struct engram_sm_split engram_sm_split_t;
+engram_status_t engram_sm_split_create(int device, int n_sms, engram_sm_split_t** out);
+int engram_sm_split_sms(const engram_sm_split_t* split, int group);
+void* engram_sm_split_stream(const engram_sm_split_t* split, int group);
+engram_status_t engram_sm_split_destroy(engram_sm_split_t* split);
 
 /* The K/V projection (Step 5, bf16 layers) in 256 x 256 output tiles on CTA
  * pairs (enable = 1): two SMs of a thread-block cluster share one

@@ -1,7 +1,9 @@
 """Stage B's persistent kernels limited to fewer SMs (engram_plan_set_sm_limit)
-give the same bits as on all SMs, and a batch in pieces -- each piece's Stage A
-over host-memory tables on a side stream, beside the previous piece's Stage B
-limited to the SMs the lookup leaves free -- equals one call."""
+and a host-table gather on a chosen number of SMs (engram_plan_set_host_gather_sms)
+give the same bits as the defaults; a batch in pieces -- each piece's Stage A
+over host-memory tables on one stream, beside the previous piece's Stage B on
+another -- equals one call, on plain streams and on the two groups of an SM
+split (engram_sm_split_*)."""
 import pytest
 import torch
 
@@ -12,6 +14,7 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # pragma: no cover
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
+from hashed_gram_embedding_engram_gb300 import EngramError, SmSplit  # noqa: E402
 from tests.gpu_helpers import make_layer, to_torch  # noqa: E402
 
 BF16 = W.PREFILL_BF16.scaled(V=5000, V_proj=3850, prime_target=4001)
@@ -22,8 +25,9 @@ def bits(t):
     return t.contiguous().view(torch.int16)
 
 
-@pytest.mark.parametrize("B,T,limit", [(1, 4096, 114), (2, 1300, 37), (3, 500, 1), (1, 2600, 0)])
-def test_sm_limit_keeps_the_bits(B, T, limit):
+@pytest.mark.parametrize("B,T,limit,pairs", [(1, 4096, 114, False), (2, 1300, 37, False), (3, 500, 1, False),
+                                             (1, 2600, 0, False), (2, 2048, 37, True), (1, 1024, 1, True)])
+def test_sm_limit_keeps_the_bits(B, T, limit, pairs):
     w = BF16.scaled(B=B, T=T)
     ids = W.token_stream(w)
     P = W.projection_map(w)
@@ -32,6 +36,7 @@ def test_sm_limit_keeps_the_bits(B, T, limit):
     ids_d = torch.from_numpy(ids).cuda()
     ref = H0.clone()
     plan.forward(ids_d, proj, weights, ref)
+    plan.set_cta_pairs(pairs)
     plan.set_sm_limit(limit)
     got = H0.clone()
     plan.forward(ids_d, proj, weights, got)
@@ -39,7 +44,29 @@ def test_sm_limit_keeps_the_bits(B, T, limit):
     assert torch.equal(bits(got), bits(ref))
 
 
-def test_pieces_beside_a_host_table_lookup_equal_one_call():
+def run_pieces(plan, weights, proj, ids_d, table_host, H, pieces, sa, sb, T, d_mem):
+    es = [torch.empty((hi - lo) * T, d_mem, dtype=torch.bfloat16, device="cuda") for lo, hi in pieces]
+    cur = torch.cuda.current_stream()
+    sa.wait_stream(cur)
+    sb.wait_stream(cur)
+    ready = []
+    with torch.cuda.stream(sa):
+        for (lo, hi), ep in zip(pieces, es):
+            plan.stage_a(ids_d[lo:hi], proj, table_host, weights.scales, out=ep)
+            ev = torch.cuda.Event()
+            ev.record(sa)
+            ready.append(ev)
+    with torch.cuda.stream(sb):
+        for (lo, hi), ep, ev in zip(pieces, es, ready):
+            sb.wait_event(ev)
+            plan.stage_b(ep, weights, H[lo:hi])
+    cur.wait_stream(sa)
+    cur.wait_stream(sb)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_pieces_beside_a_host_table_lookup_equal_one_call(split):
     w = I8
     ids = W.token_stream(w)
     P = W.projection_map(w)
@@ -50,23 +77,55 @@ def test_pieces_beside_a_host_table_lookup_equal_one_call():
     ref = H0.clone()
     e = plan.stage_a(ids_d, proj, table_host, weights.scales)
     plan.stage_b(e, weights, ref)
-    assert 0 < plan.host_gather_sms() < torch.cuda.get_device_properties(0).multi_processor_count
-    plan.set_sm_limit(torch.cuda.get_device_properties(0).multi_processor_count - plan.host_gather_sms())
+    n_dev = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan.host_gather_sms() == n_dev // 4
     pieces = [(0, 3), (3, 5), (5, 8)]
-    es = [torch.empty((hi - lo) * w.T, w.d_mem, dtype=torch.bfloat16, device="cuda") for lo, hi in pieces]
     H = H0.clone()
-    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
-    side.wait_stream(main)
-    ready = []
-    with torch.cuda.stream(side):
-        for (lo, hi), ep in zip(pieces, es):
-            plan.stage_a(ids_d[lo:hi], proj, table_host, weights.scales, out=ep)
-            ev = torch.cuda.Event()
-            ev.record(side)
-            ready.append(ev)
-    for (lo, hi), ep, ev in zip(pieces, es, ready):
-        main.wait_event(ev)
-        plan.stage_b(ep, weights, H[lo:hi])
-    torch.cuda.synchronize()
+    if split:
+        sp = SmSplit(16)
+        assert sp.sms[0] >= 16 and sp.sms[0] + sp.sms[1] <= n_dev and sp.sms[1] > 0
+        plan.set_host_gather_sms(sp.sms[0])
+        plan.set_sm_limit(sp.sms[1])
+        assert plan.host_gather_sms() == sp.sms[0]
+        run_pieces(plan, weights, proj, ids_d, table_host, H, pieces, sp.stream(0), sp.stream(1), w.T, w.d_mem)
+        sp.close()
+    else:
+        plan.set_sm_limit(n_dev - plan.host_gather_sms())
+        run_pieces(plan, weights, proj, ids_d, table_host, H, pieces, torch.cuda.Stream(),
+                   torch.cuda.current_stream(), w.T, w.d_mem)
     assert plan.get_error() == (0, 0)
     assert torch.equal(bits(H), bits(ref))
+
+
+@pytest.mark.parametrize("n", [1, 8, 37, 500])
+def test_host_gather_sms_keeps_the_bits(n):
+    w = I8
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, _ = make_layer(w, L, P, ids.size)
+    table_host = to_torch(L.table, "i8", "cpu", pin=True)
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = plan.stage_a(ids_d, proj, table_host, weights.scales)
+    plan.set_host_gather_sms(n)
+    n_dev = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan.host_gather_sms() == min(n, n_dev)
+    got = plan.stage_a(ids_d, proj, table_host, weights.scales)
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(bits(got), bits(ref))
+    plan.set_host_gather_sms(0)
+    assert plan.host_gather_sms() == n_dev // 4
+
+
+def test_split_argument_errors():
+    n_dev = torch.cuda.get_device_properties(0).multi_processor_count
+    for n in (0, -3, n_dev, n_dev + 8):
+        with pytest.raises(EngramError):
+            SmSplit(n)
+    w = BF16
+    L = W.layer_inputs(w, 1)
+    plan, *_ = make_layer(w, L, W.projection_map(w), 64)
+    with pytest.raises(EngramError):
+        plan.set_sm_limit(-1)
+    with pytest.raises(EngramError):
+        plan.set_host_gather_sms(-1)
