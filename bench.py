@@ -943,15 +943,16 @@ def run_workload(args) -> None:
         g_uva["host_link_gbs"] = round(link_bytes / (g_uva["ms"] / 1e3) / 1e9, 1)
         g_uva["frac_of_h2d_copy"] = round(g_uva["host_link_gbs"] / h2d, 4)
         extra["kernels_uva"] = kern_uva
-        # the batch in pieces of whole sequences on an SM split (green contexts): every piece's Stage A over
-        # the host link on group 0's stream, its gather on group 0's SMs; piece i's Stage B on group 1's
-        # stream, its persistent kernels sized for group 1's SMs, as soon as piece i's rows are in -- so
-        # the lookup of piece i+1 runs beside the projection and conv of piece i.  Swept over the lookup
-        # group's size and the piece count; every point is checked bit for bit against the one-call step.
+        # the batch in pieces of whole sequences on an SM split (green contexts), engram_forward_split:
+        # every piece's Stage A over the host link on group 0's SMs, piece i's Stage B on group 1's SMs as
+        # soon as piece i's rows are in -- so the lookup of piece i+1 runs beside the projection and conv of
+        # piece i.  Swept over the lookup group's size and the piece count; every point is checked bit for
+        # bit against the one-call step.
         from hashed_gram_embedding_engram_gb300 import SmSplit
         restore()
         step("table_host")
         ref_h = [ly["H"].clone() for ly in layers]
+        w_host = [dataclass_replace(ly["weights"], table=ly["table_host"]) for ly in layers]
         Kp = min(args.steps, 30)
         sweep = []
         for n0 in (16, 24, 32):
@@ -960,34 +961,10 @@ def run_workload(args) -> None:
             except Exception as exc:  # a driver without green contexts: report and go on
                 sweep.append({"lookup_sms": n0, "error": str(exc)[:200]})
                 continue
-            s0, s1 = sp.stream(0), sp.stream(1)
-            for ly in layers:
-                ly["plan"].set_host_gather_sms(sp.sms[0])
-                ly["plan"].set_sm_limit(sp.sms[1])
             for n_pieces in (4, 8):
-                pcs = [(w.B * i // n_pieces, w.B * (i + 1) // n_pieces) for i in range(n_pieces)]
-                e_pcs = [[torch.empty((hi - lo) * w.T, w.d_mem, dtype=torch.bfloat16, device=dev) for lo, hi in pcs]
-                         for _ in layers]
-
                 def pieces_step():
-                    cur = torch.cuda.current_stream()
-                    s0.wait_stream(cur)
-                    s1.wait_stream(cur)
-                    for ly, es in zip(layers, e_pcs):
-                        ready = []
-                        with torch.cuda.stream(s0):
-                            for (lo, hi), e in zip(pcs, es):
-                                ly["plan"].stage_a(ids[lo:hi], ly["proj"], ly["table_host"], ly["weights"].scales,
-                                                   out=e)
-                                ev_ = torch.cuda.Event()
-                                ev_.record(s0)
-                                ready.append(ev_)
-                        with torch.cuda.stream(s1):
-                            for (lo, hi), e, ev_ in zip(pcs, es, ready):
-                                s1.wait_event(ev_)
-                                ly["plan"].stage_b(e, ly["weights"], ly["H"][lo:hi], workspace=ly["ws"])
-                    cur.wait_stream(s0)
-                    cur.wait_stream(s1)
+                    for ly, wh in zip(layers, w_host):
+                        ly["plan"].forward_split(sp, n_pieces, ids, ly["proj"], wh, ly["H"], workspace=ly["ws"])
 
                 for _ in range(3):
                     restore()
@@ -1013,22 +990,21 @@ def run_workload(args) -> None:
                     gp.replay()
                     evp[i][1].record()
                 torch.cuda.synchronize()
-                ms_p = sum(a.elapsed_time(b) for a, b in evp) / Kp
-                del gp, e_pcs
+                ms_p = sorted(a.elapsed_time(b) for a, b in evp)
+                del gp
                 sweep.append({"lookup_sms": sp.sms[0], "stage_b_sms": sp.sms[1], "pieces": n_pieces,
-                              "ms_per_step": round(ms_p, 5), "value": round(tokens_per_step / (ms_p / 1e3), 1),
+                              "ms_per_step": round(sum(ms_p) / Kp, 5), "ms_per_step_median": round(ms_p[Kp // 2], 5),
+                              "value": round(tokens_per_step / (sum(ms_p) / Kp / 1e3), 1),
                               "bit_identical_to_one_call": bool(same)})
             torch.cuda.synchronize()
             sp.close()
             for ly in layers:
-                ly["plan"].set_host_gather_sms(0)
-                ly["plan"].set_sm_limit(0)
                 st_, flags = ly["plan"].get_error()
                 assert st_ == 0, f"device error flags {flags}"
         ok_pts = [p_ for p_ in sweep if p_.get("bit_identical_to_one_call")]
         extra["uva_pieces"] = {
-            "what": "pieces of whole sequences on an SM split: each piece's Stage A over the host link on the "
-                    "lookup group's SMs, beside the previous piece's Stage B on the other SMs",
+            "what": "engram_forward_split: pieces of whole sequences on an SM split, each piece's Stage A over the "
+                    "host link on the lookup group's SMs beside the previous piece's Stage B on the other SMs",
             "best": min(ok_pts, key=lambda p_: p_["ms_per_step"]) if ok_pts else None,
             "one_call_ms_per_step": round(ms, 5), "sweep": sweep, "cuda_graph": True,
             "l2": "flushed between timed steps"}

@@ -23,7 +23,8 @@ EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", 
            "engram_forward_static_scratch", "engram_stage_a", "engram_stage_a_layers", "engram_cache_create", "engram_cache_destroy",
            "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats",
            "engram_cache_set_dedup", "engram_quantize_fp8", "engram_plan_set_sm_limit", "engram_plan_host_gather_sms", "engram_plan_set_host_gather_sms",
-           "engram_sm_split_create", "engram_sm_split_sms", "engram_sm_split_stream", "engram_sm_split_destroy")
+           "engram_sm_split_create", "engram_sm_split_sms", "engram_sm_split_stream", "engram_sm_split_destroy",
+           "engram_forward_split")
 
 
 class Config(ctypes.Structure):
@@ -101,10 +102,12 @@ def _lib() -> ctypes.CDLL:
         lib.engram_sm_split_stream.argtypes = [vp, i32]
         lib.engram_sm_split_stream.restype = vp
         lib.engram_sm_split_destroy.argtypes = [vp]
+        lib.engram_forward_split.argtypes = [vp, vp, i32, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
+                                             ctypes.POINTER(State), vp, sz, vp]
         lib.engram_plan_set_fused_decode.argtypes = [vp, i32]
         lib.engram_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
         for name in EXPORTS:
-            if name != "engram_status_string":
+            if name not in ("engram_status_string", "engram_sm_split_stream"):   # those two return pointers
                 getattr(lib, name).restype = i32
         _LIB = lib
     return _LIB

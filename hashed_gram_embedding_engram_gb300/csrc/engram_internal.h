@@ -68,6 +68,14 @@ struct engram_plan {
 
 namespace engram {
 
+// An SM split (smsplit.cu): each group's stream and SM count, and events for
+// ordering the two streams (kSplitEvents of them, created with the split).
+constexpr int kMaxPieces = 64;
+constexpr int kSplitEvents = kMaxPieces + 3;
+cudaStream_t split_stream(const engram_sm_split* sp, int group);
+int split_sms(const engram_sm_split* sp, int group);
+cudaEvent_t split_event(const engram_sm_split* sp, int i);
+
 // SMs a Stage A over tables in host memory occupies (gather.cu): one 1024-thread block each.
 inline int hostgrid_sms(const engram_plan* p) {
   if (p->host_sms > 0) return p->host_sms < p->num_sms ? p->host_sms : p->num_sms;

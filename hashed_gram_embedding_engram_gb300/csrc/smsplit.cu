@@ -12,11 +12,13 @@
 #include <new>
 
 #include "engram.h"
+#include "engram_internal.h"
 
 struct engram_sm_split {
   CUgreenCtx ctx[2];
   CUstream stream[2];
   int sms[2];
+  cudaEvent_t ev[engram::kSplitEvents];   // ordering events for engram_forward_split
 };
 
 namespace {
@@ -58,6 +60,8 @@ const GreenFns& green_fns() {
 }
 
 void release(const GreenFns& f, engram_sm_split* sp) {
+  for (cudaEvent_t& e : sp->ev)
+    if (e) cudaEventDestroy(e);
   for (int g = 0; g < 2; ++g) {
     if (sp->stream[g]) f.stream_destroy(sp->stream[g]);
     if (sp->ctx[g]) f.ctx_destroy(sp->ctx[g]);
@@ -66,6 +70,12 @@ void release(const GreenFns& f, engram_sm_split* sp) {
 }
 
 }  // namespace
+
+namespace engram {
+cudaStream_t split_stream(const engram_sm_split* sp, int group) { return sp->stream[group]; }
+int split_sms(const engram_sm_split* sp, int group) { return sp->sms[group]; }
+cudaEvent_t split_event(const engram_sm_split* sp, int i) { return sp->ev[i]; }
+}  // namespace engram
 
 extern "C" {
 
@@ -97,6 +107,13 @@ engram_status_t engram_sm_split_create(int device, int n_sms, engram_sm_split_t*
       return ENGRAM_ERR_CUDA;
     }
     sp->sms[g] = static_cast<int>(part[g].sm.smCount);
+  }
+  for (cudaEvent_t& e : sp->ev) {
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      e = nullptr;
+      release(f, sp);
+      return ENGRAM_ERR_CUDA;
+    }
   }
   *out = sp;
   return ENGRAM_OK;

@@ -418,6 +418,27 @@ int engram_sm_split_sms(const engram_sm_split_t* split, int group);
 void* engram_sm_split_stream(const engram_sm_split_t* split, int group);
 engram_status_t engram_sm_split_destroy(engram_sm_split_t* split);
 
+/* engram_forward (Steps 1-8) of B sequences in n_pieces pieces of whole
+ * sequences (piece i: sequences [B*i/n_pieces, B*(i+1)/n_pieces)) on an SM
+ * split: every piece's Stage A on group 0's stream, each piece's Stage B on
+ * group 1's stream as soon as its rows are in, so the lookup of piece i+1
+ * runs beside the projection and conv of piece i ("DeepSeek Engram 系列导读",
+ * section "Engram 工作原理": the lookup depends on the tokens only).  Made for
+ * tables in pinned host memory, whose lookup is paced by the host link; any
+ * table works.  Same arguments, layouts and results (bit for bit) as
+ * engram_forward; the state, when given, is updated per piece.
+ * The work is ordered after what `stream` holds before the call, and `stream`
+ * waits for all of it (graph capture of `stream` captures both groups).
+ * During the call the plan's SM limit and host-gather SMs are the split's
+ * groups (1 and 0), and the call uses the two-launch Stage B on one SM per
+ * CTA and records no tracing events; the plan's settings are restored before
+ * it returns.  Not for concurrent calls on one split.  1 <= n_pieces <= B and
+ * n_pieces <= 64, else ENGRAM_ERR_INVALID_ARG; other errors as engram_forward. */
+engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_t* split, int n_pieces,
+                                     const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                                     const engram_weights_t* w, void* H, engram_state_t* state, void* workspace,
+                                     size_t workspace_bytes, engram_stream_t stream);
+
 /* The K/V projection (Step 5, bf16 layers) in 256 x 256 output tiles on CTA
  * pairs (enable = 1): two SMs of a thread-block cluster share one
  * tcgen05.mma.cta_group::2 tile, each staging its 128 rows of e and half of

@@ -43,6 +43,22 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, n), n
 
 
+def test_binding_return_types_match_the_header(lib):
+    """A function the header declares returning a pointer gets a pointer restype,
+    one returning engram_status_t or int an int (a truncated pointer would pass
+    unnoticed until an address above 2^31)."""
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", f)).read(), flags=re.S)
+        for ret, name in re.findall(r"^\s*((?:const\s+)?\w+\s*\**)\s*(engram_\w+)\s*\(", src, flags=re.M):
+            rt = getattr(lib, name).restype
+            if "*" in ret:
+                assert rt in (ctypes.c_void_p, ctypes.c_char_p), (name, ret, rt)
+            elif ret.strip() in ("engram_status_t", "int"):
+                assert rt is ctypes.c_int, (name, ret, rt)
+
+
 def test_status_strings(lib):
     from hashed_gram_embedding_engram_gb300 import _lib
     for s in range(8):

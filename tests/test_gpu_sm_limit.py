@@ -129,3 +129,85 @@ def test_split_argument_errors():
         plan.set_sm_limit(-1)
     with pytest.raises(EngramError):
         plan.set_host_gather_sms(-1)
+
+
+# ---------------------------------------------------------------- engram_forward_split
+def _layer(w, host):
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H0 = make_layer(w, L, P, ids.size, table_on_host=host)
+    return plan, weights, proj, H0, torch.from_numpy(ids).cuda()
+
+
+@pytest.fixture(scope="module")
+def split():
+    sp = SmSplit(16)
+    yield sp
+    sp.close()
+
+
+@pytest.mark.parametrize("host,n_pieces", [(True, 1), (True, 3), (True, 8), (False, 2)])
+def test_forward_split_equals_forward(split, host, n_pieces):
+    w = I8 if host else BF16.scaled(B=4, T=700)
+    plan, weights, proj, H0, ids_d = _layer(w, host)
+    ref = H0.clone()
+    plan.forward(ids_d, proj, weights, ref)
+    plan.set_sm_limit(100)
+    plan.set_host_gather_sms(5)
+    got = H0.clone()
+    plan.forward_split(split, n_pieces, ids_d, proj, weights, got)
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(bits(got), bits(ref))
+    assert plan.host_gather_sms() == 5               # the plan's own settings are back
+
+
+def test_forward_split_continues_sequences_with_state(split):
+    """Two chunks of every sequence: the second through the split with the state
+    the first left, against two plain forwards (H and the whole state, bit for bit)."""
+    w = I8.scaled(B=6, T=400)
+    plan, weights, proj, H0, ids_d = _layer(w, True)
+    from hashed_gram_embedding_engram_gb300 import EngramState
+    st_ref, st = EngramState.zeros(plan, w.B), EngramState.zeros(plan, w.B)
+    ref, got = H0.clone(), H0.clone()
+    plan.forward(ids_d, proj, weights, ref, st_ref)
+    plan.forward(ids_d, proj, weights, got, st)
+    ids2 = torch.flip(ids_d, dims=[1]).contiguous()
+    ref2, got2 = H0.clone(), H0.clone()
+    plan.forward(ids2, proj, weights, ref2, st_ref)
+    plan.forward_split(split, 4, ids2, proj, weights, got2, st)
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(bits(got2), bits(ref2))
+    for a, b in ((st.prev_ids, st_ref.prev_ids), (st.u_ring, st_ref.u_ring), (st.pos, st_ref.pos)):
+        assert torch.equal(a, b)
+
+
+def test_forward_split_in_a_cuda_graph(split):
+    w = I8
+    plan, weights, proj, H0, ids_d = _layer(w, True)
+    ref = H0.clone()
+    plan.forward(ids_d, proj, weights, ref)
+    H = H0.clone()
+    ws = plan.new_workspace(ids_d.numel(), "cuda")
+    plan.forward_split(split, 4, ids_d, proj, weights, H, workspace=ws)     # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.forward_split(split, 4, ids_d, proj, weights, H, workspace=ws)
+    for _ in range(2):
+        H.copy_(H0)
+        g.replay()
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(bits(H), bits(ref))
+
+
+def test_forward_split_argument_errors(split):
+    w = I8.scaled(B=3, T=64)
+    plan, weights, proj, H0, ids_d = _layer(w, True)
+    for n in (0, 4, 65):
+        with pytest.raises(EngramError):
+            plan.forward_split(split, n, ids_d, proj, weights, H0.clone())
+    assert plan.get_error() == (0, 0)
