@@ -954,58 +954,68 @@ def run_workload(args) -> None:
         ref_h = [ly["H"].clone() for ly in layers]
         w_host = [dataclass_replace(ly["weights"], table=ly["table_host"]) for ly in layers]
         Kp = min(args.steps, 30)
-        sweep = []
-        for n0 in (16, 24, 32):
-            try:
-                sp = SmSplit(n0, dev.index or 0)
-            except Exception as exc:  # a driver without green contexts: report and go on
-                sweep.append({"lookup_sms": n0, "error": str(exc)[:200]})
-                continue
-            for n_pieces in (4, 8):
-                def pieces_step():
-                    for ly, wh in zip(layers, w_host):
-                        ly["plan"].forward_split(sp, n_pieces, ids, ly["proj"], wh, ly["H"], workspace=ly["ws"])
 
-                for _ in range(3):
+        def split_sweep(use_cache: bool):
+            sweep = []
+            for n0 in (16, 24, 32):
+                try:
+                    sp = SmSplit(n0, dev.index or 0)
+                except Exception as exc:  # a driver without green contexts: report and go on
+                    sweep.append({"lookup_sms": n0, "error": str(exc)[:200]})
+                    continue
+                for n_pieces in (4, 8):
+                    def pieces_step():
+                        for ly, wh in zip(layers, w_host):
+                            ly["plan"].forward_split(sp, n_pieces, ids, ly["proj"], wh, ly["H"], workspace=ly["ws"],
+                                                     cache=ly["cache"] if use_cache else None)
+
+                    for _ in range(3):
+                        restore()
+                        pieces_step()
+                    torch.cuda.synchronize()
+                    same = all(torch.equal(ly["H"].view(torch.int16), r.view(torch.int16))
+                               for ly, r in zip(layers, ref_h))
+                    gp = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gp, capture_error_mode="relaxed"):
+                        pieces_step()
+                    torch.cuda.synchronize()
                     restore()
-                    pieces_step()
-                torch.cuda.synchronize()
-                same = all(torch.equal(ly["H"].view(torch.int16), r.view(torch.int16))
-                           for ly, r in zip(layers, ref_h))
-                gp = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gp, capture_error_mode="relaxed"):
-                    pieces_step()
-                torch.cuda.synchronize()
-                restore()
-                gp.replay()
-                torch.cuda.synchronize()
-                same = same and all(torch.equal(ly["H"].view(torch.int16), r.view(torch.int16))
-                                    for ly, r in zip(layers, ref_h))
-                evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                       for _ in range(Kp)]
-                for i in range(Kp):
-                    restore()
-                    flush.zero_()
-                    evp[i][0].record()
                     gp.replay()
-                    evp[i][1].record()
+                    torch.cuda.synchronize()
+                    same = same and all(torch.equal(ly["H"].view(torch.int16), r.view(torch.int16))
+                                        for ly, r in zip(layers, ref_h))
+                    evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                           for _ in range(Kp)]
+                    for i in range(Kp):
+                        restore()
+                        flush.zero_()
+                        evp[i][0].record()
+                        gp.replay()
+                        evp[i][1].record()
+                    torch.cuda.synchronize()
+                    ms_p = sorted(a.elapsed_time(b) for a, b in evp)
+                    del gp
+                    sweep.append({"lookup_sms": sp.sms[0], "stage_b_sms": sp.sms[1], "pieces": n_pieces,
+                                  "ms_per_step": round(sum(ms_p) / Kp, 5),
+                                  "ms_per_step_median": round(ms_p[Kp // 2], 5),
+                                  "value": round(tokens_per_step / (sum(ms_p) / Kp / 1e3), 1),
+                                  "bit_identical_to_one_call": bool(same)})
                 torch.cuda.synchronize()
-                ms_p = sorted(a.elapsed_time(b) for a, b in evp)
-                del gp
-                sweep.append({"lookup_sms": sp.sms[0], "stage_b_sms": sp.sms[1], "pieces": n_pieces,
-                              "ms_per_step": round(sum(ms_p) / Kp, 5), "ms_per_step_median": round(ms_p[Kp // 2], 5),
-                              "value": round(tokens_per_step / (sum(ms_p) / Kp / 1e3), 1),
-                              "bit_identical_to_one_call": bool(same)})
-            torch.cuda.synchronize()
-            sp.close()
-            for ly in layers:
-                st_, flags = ly["plan"].get_error()
-                assert st_ == 0, f"device error flags {flags}"
-        ok_pts = [p_ for p_ in sweep if p_.get("bit_identical_to_one_call")]
+                sp.close()
+                for ly in layers:
+                    st_, flags = ly["plan"].get_error()
+                    assert st_ == 0, f"device error flags {flags}"
+            return sweep
+
+        def best_of(sweep):
+            ok_pts = [p_ for p_ in sweep if p_.get("bit_identical_to_one_call")]
+            return min(ok_pts, key=lambda p_: p_["ms_per_step"]) if ok_pts else None
+
+        sweep = split_sweep(False)
         extra["uva_pieces"] = {
             "what": "engram_forward_split: pieces of whole sequences on an SM split, each piece's Stage A over the "
                     "host link on the lookup group's SMs beside the previous piece's Stage B on the other SMs",
-            "best": min(ok_pts, key=lambda p_: p_["ms_per_step"]) if ok_pts else None,
+            "best": best_of(sweep),
             "one_call_ms_per_step": round(ms, 5), "sweep": sweep, "cuda_graph": True,
             "l2": "flushed between timed steps"}
         # HBM hot-row cache: LFU over a different sample of the same token distribution
@@ -1025,6 +1035,11 @@ def run_workload(args) -> None:
             looked += a_
             hits += b_
             link += l_
+        # the split pipeline with every piece's lookup through the hot-row cache
+        sweep_c = split_sweep(True)
+        extra["uva_pieces"]["hot_row_cache"] = {"best": best_of(sweep_c), "sweep": sweep_c}
+        for ly in layers:
+            ly["cache"].stats(reset=True)
         # per-batch row dedup: each distinct row of a batch crosses the link once
         # (alone, then together with the hot-row cache)
         for ly in layers:

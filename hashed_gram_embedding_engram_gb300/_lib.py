@@ -102,7 +102,7 @@ def _lib() -> ctypes.CDLL:
         lib.engram_sm_split_stream.argtypes = [vp, i32]
         lib.engram_sm_split_stream.restype = vp
         lib.engram_sm_split_destroy.argtypes = [vp]
-        lib.engram_forward_split.argtypes = [vp, vp, i32, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
+        lib.engram_forward_split.argtypes = [vp, vp, i32, vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
                                              ctypes.POINTER(State), vp, sz, vp]
         lib.engram_plan_set_fused_decode.argtypes = [vp, i32]
         lib.engram_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]

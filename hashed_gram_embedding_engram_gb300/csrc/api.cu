@@ -549,88 +549,6 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
   return run_stage_b(plan, ws, ws.e, ids, proj, V, B, T, w, H, state, s);
 }
 
-engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_t* split, int n_pieces,
-                                     const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                                     const engram_weights_t* w, void* H, engram_state_t* state, void* workspace,
-                                     size_t workspace_bytes, engram_stream_t stream) {
-  NvtxRange nvtx_range("engram_forward_split");
-  if (!plan || !split) return ENGRAM_ERR_INVALID_ARG;
-  if (engram_status_t s = check_tokens(plan, B, T)) return s;
-  const int64_t ntok = static_cast<int64_t>(B) * T;
-  if (ntok == 0) return ENGRAM_OK;
-  if (n_pieces < 1 || n_pieces > B || n_pieces > engram::kMaxPieces) return ENGRAM_ERR_INVALID_ARG;
-  if (!ids || !proj || V <= 0 || !H || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
-  if (engram_status_t s = check_weights(plan, w, true)) return s;
-  if (engram_status_t s = check_state(plan, state)) return s;
-  engram::Workspace ws = engram::carve_workspace(plan, ntok, workspace);
-  if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return ENGRAM_ERR_WORKSPACE;
-  const void* tab = nullptr;
-  bool host = false;
-  if (engram_status_t s = device_view(w->table, &tab, &host)) return s;
-  if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
-  const void* sc = nullptr;
-  if (w->scales) {
-    if (engram_status_t s = device_view(w->scales, &sc)) return s;
-  }
-  const cudaStream_t s = (cudaStream_t)stream;
-  const cudaStream_t sa = engram::split_stream(split, 0), sb = engram::split_stream(split, 1);
-  const size_t ab = act_bytes(plan->cfg.act_dtype);
-  const int64_t e_row = static_cast<int64_t>(plan->d_mem) * ab;                    // bytes of e per token
-  const int64_t h_row = static_cast<int64_t>(plan->cfg.M) * plan->cfg.d * ab;      // bytes of H per token
-  const int L = plan->L_ring, N = plan->cfg.N, Md = plan->cfg.M * plan->cfg.d;
-  // each group's grids sized for its SMs; the two-launch Stage B on one SM per CTA (its
-  // one-launch and CTA-pair forms need every SM or clusters): the same bits in every form
-  struct Saved {
-    engram_plan* p;
-    int sm_limit, host_sms;
-    bool timing, fused_stage_b, cta_pairs;
-    ~Saved() {
-      p->sm_limit = sm_limit;
-      p->host_sms = host_sms;
-      p->timing = timing;
-      p->fused_stage_b = fused_stage_b;
-      p->cta_pairs = cta_pairs;
-    }
-  } saved{plan, plan->sm_limit, plan->host_sms, plan->timing, plan->fused_stage_b, plan->cta_pairs};
-  plan->sm_limit = engram::split_sms(split, 1);
-  plan->host_sms = engram::split_sms(split, 0);
-  plan->timing = false;
-  plan->fused_stage_b = false;
-  plan->cta_pairs = false;
-  plan->n_marks = 0;
-  auto order = [](cudaStream_t before, cudaStream_t after, cudaEvent_t ev) {
-    return cudaEventRecord(ev, before) == cudaSuccess && cudaStreamWaitEvent(after, ev, 0) == cudaSuccess;
-  };
-  // both groups' streams start after the work already on `stream`
-  if (!order(s, sa, engram::split_event(split, 0)) || cudaStreamWaitEvent(sb, engram::split_event(split, 0), 0))
-    return ENGRAM_ERR_CUDA;
-  for (int i = 0; i < n_pieces; ++i) {
-    const int lo = static_cast<int>(static_cast<int64_t>(B) * i / n_pieces);
-    const int hi = static_cast<int>(static_cast<int64_t>(B) * (i + 1) / n_pieces);
-    const int nb = hi - lo;
-    const int64_t t0 = static_cast<int64_t>(lo) * T;
-    void* e_i = static_cast<char*>(ws.e) + t0 * e_row;
-    engram_state_t st_i{};
-    if (state) {
-      st_i.prev_ids = state->prev_ids + static_cast<int64_t>(lo) * (N - 1);
-      st_i.u_ring = state->u_ring + static_cast<int64_t>(lo) * L * Md;
-      st_i.pos = state->pos + lo;
-    }
-    if (engram::launch_hash_gather(plan, ids + t0, nb, T, proj, V, state ? st_i.prev_ids : nullptr, tab,
-                                   static_cast<const uint16_t*>(sc), e_i, sa, host) != cudaSuccess)
-      return ENGRAM_ERR_CUDA;
-    if (!order(sa, sb, engram::split_event(split, 1 + i))) return ENGRAM_ERR_CUDA;
-    if (engram_status_t r = run_stage_b(plan, ws, e_i, ids + t0, proj, V, nb, T, w, static_cast<char*>(H) + t0 * h_row,
-                                        state ? &st_i : nullptr, sb))
-      return r;
-  }
-  // `stream` waits for both groups
-  if (!order(sa, s, engram::split_event(split, n_pieces + 1)) || !order(sb, s, engram::split_event(split, n_pieces + 2)))
-    return ENGRAM_ERR_CUDA;
-  return ENGRAM_OK;
-}
-
 }  // extern "C"
 
 struct engram_cache {
@@ -850,6 +768,96 @@ engram_status_t engram_cache_set_dedup(engram_cache_t* c, int64_t batch_rows) {
         }                                 // the dedup then runs unpipelined
     }
   }
+  return ENGRAM_OK;
+}
+
+engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_t* split, int n_pieces,
+                                     const engram_cache_t* cache, const int32_t* ids, int B, int T,
+                                     const int32_t* proj, int V, const engram_weights_t* w, void* H,
+                                     engram_state_t* state, void* workspace, size_t workspace_bytes,
+                                     engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_forward_split");
+  if (!plan || !split) return ENGRAM_ERR_INVALID_ARG;
+  if (cache && cache->plan != plan) return ENGRAM_ERR_INVALID_ARG;
+  if (cache && cache->batch_cap > 0) return ENGRAM_ERR_UNSUPPORTED;      // the dedup runs its own pipeline
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  if (ntok == 0) return ENGRAM_OK;
+  if (n_pieces < 1 || n_pieces > B || n_pieces > engram::kMaxPieces) return ENGRAM_ERR_INVALID_ARG;
+  if (!ids || !proj || V <= 0 || !H || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_weights(plan, w, true)) return s;
+  if (engram_status_t s = check_state(plan, state)) return s;
+  engram::Workspace ws = engram::carve_workspace(plan, ntok, workspace);
+  if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ENGRAM_ERR_WORKSPACE;
+  const void* tab = nullptr;
+  bool host = false;
+  if (engram_status_t s = device_view(w->table, &tab, &host)) return s;
+  if (!aligned16(tab)) return ENGRAM_ERR_INVALID_ARG;
+  const void* sc = nullptr;
+  if (w->scales) {
+    if (engram_status_t s = device_view(w->scales, &sc)) return s;
+  }
+  const cudaStream_t s = (cudaStream_t)stream;
+  const cudaStream_t sa = engram::split_stream(split, 0), sb = engram::split_stream(split, 1);
+  const size_t ab = act_bytes(plan->cfg.act_dtype);
+  const int64_t e_row = static_cast<int64_t>(plan->d_mem) * ab;                    // bytes of e per token
+  const int64_t h_row = static_cast<int64_t>(plan->cfg.M) * plan->cfg.d * ab;      // bytes of H per token
+  const int L = plan->L_ring, N = plan->cfg.N, Md = plan->cfg.M * plan->cfg.d;
+  // each group's grids sized for its SMs; the two-launch Stage B on one SM per CTA (its
+  // one-launch and CTA-pair forms need every SM or clusters): the same bits in every form
+  struct Saved {
+    engram_plan* p;
+    int sm_limit, host_sms;
+    bool timing, fused_stage_b, cta_pairs;
+    ~Saved() {
+      p->sm_limit = sm_limit;
+      p->host_sms = host_sms;
+      p->timing = timing;
+      p->fused_stage_b = fused_stage_b;
+      p->cta_pairs = cta_pairs;
+    }
+  } saved{plan, plan->sm_limit, plan->host_sms, plan->timing, plan->fused_stage_b, plan->cta_pairs};
+  plan->sm_limit = engram::split_sms(split, 1);
+  plan->host_sms = engram::split_sms(split, 0);
+  plan->timing = false;
+  plan->fused_stage_b = false;
+  plan->cta_pairs = false;
+  plan->n_marks = 0;
+  auto order = [](cudaStream_t before, cudaStream_t after, cudaEvent_t ev) {
+    return cudaEventRecord(ev, before) == cudaSuccess && cudaStreamWaitEvent(after, ev, 0) == cudaSuccess;
+  };
+  // both groups' streams start after the work already on `stream`
+  if (!order(s, sa, engram::split_event(split, 0)) || cudaStreamWaitEvent(sb, engram::split_event(split, 0), 0))
+    return ENGRAM_ERR_CUDA;
+  for (int i = 0; i < n_pieces; ++i) {
+    const int lo = static_cast<int>(static_cast<int64_t>(B) * i / n_pieces);
+    const int hi = static_cast<int>(static_cast<int64_t>(B) * (i + 1) / n_pieces);
+    const int nb = hi - lo;
+    const int64_t t0 = static_cast<int64_t>(lo) * T;
+    void* e_i = static_cast<char*>(ws.e) + t0 * e_row;
+    engram_state_t st_i{};
+    if (state) {
+      st_i.prev_ids = state->prev_ids + static_cast<int64_t>(lo) * (N - 1);
+      st_i.u_ring = state->u_ring + static_cast<int64_t>(lo) * L * Md;
+      st_i.pos = state->pos + lo;
+    }
+    const int32_t* prev_i = state ? st_i.prev_ids : nullptr;
+    const cudaError_t ga =
+        cache ? engram::launch_hash_gather_cached(plan, ids + t0, nb, T, proj, V, prev_i, cache->table,
+                                                  static_cast<const uint16_t*>(sc), e_i, cache->slot, cache->rows,
+                                                  cache->stats, sa, cache->table_on_host)
+              : engram::launch_hash_gather(plan, ids + t0, nb, T, proj, V, prev_i, tab,
+                                           static_cast<const uint16_t*>(sc), e_i, sa, host);
+    if (ga != cudaSuccess) return ENGRAM_ERR_CUDA;
+    if (!order(sa, sb, engram::split_event(split, 1 + i))) return ENGRAM_ERR_CUDA;
+    if (engram_status_t r = run_stage_b(plan, ws, e_i, ids + t0, proj, V, nb, T, w, static_cast<char*>(H) + t0 * h_row,
+                                        state ? &st_i : nullptr, sb))
+      return r;
+  }
+  // `stream` waits for both groups
+  if (!order(sa, s, engram::split_event(split, n_pieces + 1)) || !order(sb, s, engram::split_event(split, n_pieces + 2)))
+    return ENGRAM_ERR_CUDA;
   return ENGRAM_OK;
 }
 

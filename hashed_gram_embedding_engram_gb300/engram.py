@@ -274,16 +274,18 @@ class EngramPlan:
 
     def forward_split(self, split: "SmSplit", n_pieces: int, ids: torch.Tensor, proj: torch.Tensor,
                       weights: EngramWeights, H: torch.Tensor, state: Optional[EngramState] = None,
-                      workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+                      workspace: Optional[torch.Tensor] = None, cache: Optional["EngramCache"] = None) -> torch.Tensor:
         """``forward`` in ``n_pieces`` pieces of whole sequences on an SM split: each
-        piece's Stage A on group 0, its Stage B on group 1 once its rows are in
-        (engram_forward_split); the same bits as ``forward``."""
+        piece's Stage A on group 0 (through ``cache`` if given), its Stage B on
+        group 1 once its rows are in (engram_forward_split); the same bits as
+        ``forward``."""
         B, T = ids.shape
         ws = self.new_workspace(B * T, H.device) if workspace is None else workspace
         w = weights.struct(self)
         st = None if state is None else ctypes.byref(state.struct(self, B))
         _lib.check(self._lib.engram_forward_split(
-            self._h, split._h, int(n_pieces), _dev(ids, "ids", torch.int32), B, T, _dev(proj, "proj", torch.int32),
+            self._h, split._h, int(n_pieces), None if cache is None else cache._h, _dev(ids, "ids", torch.int32), B, T,
+            _dev(proj, "proj", torch.int32),
             proj.numel(), ctypes.byref(w), _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), st,
             _dev(ws, "workspace"), ws.numel(), _stream()), "engram_forward_split")
         return H

@@ -433,11 +433,16 @@ engram_status_t engram_sm_split_destroy(engram_sm_split_t* split);
  * groups (1 and 0), and the call uses the two-launch Stage B on one SM per
  * CTA and records no tracing events; the plan's settings are restored before
  * it returns.  Not for concurrent calls on one split.  1 <= n_pieces <= B and
- * n_pieces <= 64, else ENGRAM_ERR_INVALID_ARG; other errors as engram_forward. */
+ * n_pieces <= 64, else ENGRAM_ERR_INVALID_ARG; other errors as engram_forward.
+ * cache: NULL, or an HBM hot-row cache of this plan's table (engram_cache_*),
+ * through which every piece's Stage A then reads (engram_stage_a_cached, the
+ * same bits); a cache of another plan: ENGRAM_ERR_INVALID_ARG; a cache with
+ * the per-batch dedup on (it runs its own pipeline): ENGRAM_ERR_UNSUPPORTED. */
 engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_t* split, int n_pieces,
-                                     const int32_t* ids, int B, int T, const int32_t* proj, int V,
-                                     const engram_weights_t* w, void* H, engram_state_t* state, void* workspace,
-                                     size_t workspace_bytes, engram_stream_t stream);
+                                     const engram_cache_t* cache, const int32_t* ids, int B, int T,
+                                     const int32_t* proj, int V, const engram_weights_t* w, void* H,
+                                     engram_state_t* state, void* workspace, size_t workspace_bytes,
+                                     engram_stream_t stream);
 
 /* The K/V projection (Step 5, bf16 layers) in 256 x 256 output tiles on CTA
  * pairs (enable = 1): two SMs of a thread-block cluster share one

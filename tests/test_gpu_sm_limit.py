@@ -211,3 +211,33 @@ def test_forward_split_argument_errors(split):
         with pytest.raises(EngramError):
             plan.forward_split(split, n, ids_d, proj, weights, H0.clone())
     assert plan.get_error() == (0, 0)
+
+
+def test_forward_split_through_the_hot_row_cache(split):
+    """Every piece's Stage A through an LFU-built HBM cache of the host table:
+    the bits of the plain forward, and the cache's counters see every lookup."""
+    from hashed_gram_embedding_engram_gb300 import EngramCache
+    w = I8
+    plan, weights, proj, H0, ids_d = _layer(w, True)
+    ref = H0.clone()
+    plan.forward(ids_d, proj, weights, ref)
+    cache = EngramCache(plan, max(1, plan.total_rows // 20), weights.table)
+    cache.observe(torch.from_numpy(W.token_stream(w, key="cache-warm")).cuda(), proj)
+    assert cache.build() > 0
+    cache.stats(reset=True)
+    got = H0.clone()
+    plan.forward_split(split, 4, ids_d, proj, weights, got, cache=cache)
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(bits(got), bits(ref))
+    looked, hits, link, _ = cache.stats()
+    assert looked == ids_d.numel() * plan.R and 0 < hits < looked and link == looked - hits
+    # the per-batch dedup runs its own pipeline; a cache of another plan is refused
+    cache.set_dedup(ids_d.numel() * plan.R)
+    with pytest.raises(EngramError):
+        plan.forward_split(split, 4, ids_d, proj, weights, H0.clone(), cache=cache)
+    cache.set_dedup(0)
+    other, *_ = _layer(w, True)
+    with pytest.raises(EngramError):
+        other.forward_split(split, 4, ids_d, proj, weights, H0.clone(), cache=cache)
+    cache.close()
