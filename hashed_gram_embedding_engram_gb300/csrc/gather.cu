@@ -220,6 +220,121 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
   }
 }
 
+// Steps 1-4 for tokens of at most 16 rows and 64 chunks (int8 rows of 64
+// bytes at R = 16): one token's chunk phase would fill only half of a warp's
+// load slots, so each half-warp owns a token -- two tokens per warp pass,
+// twice a warp's rows in flight with the same registers.  Lane h*16 + i holds
+// row i, and window entry i, of half h's token; otherwise the row kernel's
+// pipeline, phases and arithmetic, per half.
+template <int kCpr, bool kInt8, bool kCache, int kBlk>
+__global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
+    row_gather_half_kernel(const GatherLayers ls, int R, int N, int K, const int32_t* __restrict__ ids, int T,
+                           const int32_t* __restrict__ proj, int V, int64_t ntok, const RowCache cache) {
+  constexpr int kRowBytes = kCpr * 16;
+  const int lane = threadIdx.x & 31;
+  const int hl = lane & 15, hb = lane & 16;            // lane within the half; the half's first lane
+  const int ly = static_cast<int>(blockIdx.y);
+  const PlanDev* __restrict__ pdg = ls.pdg[ly];
+  uint32_t* __restrict__ err = ls.err[ly];
+  const int32_t* __restrict__ prev = ls.prev[ly];
+  const uint8_t* __restrict__ table = ls.table[ly];
+  const __half* __restrict__ scales = ls.scales[ly];
+  uint4* __restrict__ out = ls.out[ly];
+  const bool has = hl < R;
+  RowConst rc{};
+  if (has) rc = row_const(pdg, K, hl);
+  {
+    const int64_t line = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (ly == 0 && line * 32 < V) ptx::prefetch_l2(proj + line * 32);
+  }
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+
+  const int per_tok = R * kCpr;                          // <= 64: four chunks per lane of a half
+  const int64_t stride = 2 * static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  bool bad = false;
+  uint32_t n_look = 0, n_hit = 0;
+  // a warp's pair of tokens: base (lanes 0-15) and base + 1 (lanes 16-31); base is warp-uniform
+  int64_t base = 2 * (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5));
+  int32_t x_cur = 0;
+  if (base + (hb >> 4) < ntok) x_cur = window_hop2(window_hop1(ids, prev, base + (hb >> 4), T, N, V, hl, bad), proj);
+  for (; base < ntok; base += stride) {
+    const int64_t tok = base + (hb >> 4);
+    const bool live = tok < ntok;
+    const int64_t tn = tok + stride;
+    const bool more = tn < ntok;
+    WindowHop hop{0, false};
+    if (more) hop = window_hop1(ids, prev, tn, T, N, V, hl, bad);
+    uint32_t xp[kMaxN];
+#pragma unroll
+    for (int i = 0; i < kMaxN; ++i)
+      if (i < N) xp[i] = static_cast<uint32_t>(__shfl_sync(0xFFFFFFFFu, x_cur, hb + i));
+    // ---- row phase: lane hl < R of each half, row hl of the half's token
+    uint64_t src = 0;
+    float sc = 0.f;
+    if (has && live) {
+      uint64_t hsh = 0;
+#pragma unroll
+      for (int i = 0; i < kMaxN; ++i)
+        if (i < rc.n) hsh ^= static_cast<uint64_t>(xp[i]) * __ldg(rc.mult + i);
+      const int64_t row = rc.offset + barrett_mod(hsh, rc.prime, rc.mu);
+      const uint8_t* p = table + row * kRowBytes;
+      if constexpr (kCache) {
+        const int32_t sl = __ldg(cache.slot + row);
+        if (sl >= 0) p = cache.rows + static_cast<int64_t>(sl) * kRowBytes;
+        ++n_look;
+        n_hit += sl >= 0;
+      }
+      src = reinterpret_cast<uint64_t>(p);
+      if constexpr (kInt8) sc = __half2float(scales[row]);
+    }
+    // ---- chunk phase: chunk f = j * 16 + hl of the half's token
+    uint4* dst = out + (kInt8 ? 2 : 1) * tok * per_tok;
+    uint4 v[kWarpItems];
+    float s_[kWarpItems];
+    bool ok[kWarpItems];
+#pragma unroll
+    for (int j = 0; j < kWarpItems; ++j) {
+      const int f = j * 16 + hl;
+      const int r = f / kCpr;
+      const int c = f % kCpr;
+      const int rs = r < R ? r : 0;
+      const uint64_t sp = shfl64(src, hb + rs);
+      s_[j] = kInt8 ? __shfl_sync(0xFFFFFFFFu, sc, hb + rs) : 0.f;
+      ok[j] = live && f < per_tok && sp != 0;
+      v[j] = ok[j] ? ld_stream_16(reinterpret_cast<const uint8_t*>(sp) + c * 16) : make_uint4(0, 0, 0, 0);
+    }
+    // next pair's second hop while these rows are in flight
+    if (more) x_cur = window_hop2(hop, proj);
+#pragma unroll
+    for (int j = 0; j < kWarpItems; ++j) {
+      const int f = j * 16 + hl;
+      if (live && f < per_tok) {
+        if constexpr (kInt8) {
+          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+          if (ok[j]) dequant16(v[j], s_[j], o0, o1);
+          dst[2 * f] = o0;
+          dst[2 * f + 1] = o1;
+        } else {
+          dst[f] = v[j];
+        }
+      }
+    }
+  }
+  if (bad) atomicOr(err, kErrIndexRange);
+  if constexpr (kCache) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      n_look += __shfl_xor_sync(0xFFFFFFFFu, n_look, o);
+      n_hit += __shfl_xor_sync(0xFFFFFFFFu, n_hit, o);
+    }
+    if (lane == 0 && n_look) {
+      atomicAdd(cache.stats, static_cast<unsigned long long>(n_look));
+      atomicAdd(cache.stats + 1, static_cast<unsigned long long>(n_hit));
+    }
+  }
+}
+
 // SMs a gather over the host link occupies: one 1024-thread block each.  An
 // SM keeps 32 warps' row loads in flight (a token's rows each, the next
 // token's window behind them), so a quarter of the SMs already carries the
@@ -268,6 +383,18 @@ cudaError_t launch_fused(const engram_plan* p, int n_layers, const GatherLayers&
   const dim3 grid(gx, n_layers);
   const dim3 block(host_table ? kHostBlk : kThreads);
   const bool wide = p->R > 32;
+  if constexpr (kCpr <= 4) {
+    if (p->R <= 16 && kCpr * p->R <= 64) {
+      // half a warp per token
+      const RowCache rcache = cache != nullptr ? *cache : RowCache{};
+      auto k = cache != nullptr ? row_gather_half_kernel<kCpr, kInt8, true, kThreads>
+                                : row_gather_half_kernel<kCpr, kInt8, false, kThreads>;
+      if (host_table)
+        k = cache != nullptr ? row_gather_half_kernel<kCpr, kInt8, true, kHostBlk>
+                             : row_gather_half_kernel<kCpr, kInt8, false, kHostBlk>;
+      return launch_pdl(k, grid, block, 0, s, ls, p->R, p->cfg.N, p->cfg.K, ids, T, proj, V, ntok, rcache);
+    }
+  }
   if (cache != nullptr) {
     auto k = wide ? row_gather_kernel<kCpr, kInt8, true, true, true> : row_gather_kernel<kCpr, kInt8, true, true>;
     if (host_table)
