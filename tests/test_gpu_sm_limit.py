@@ -241,3 +241,25 @@ def test_forward_split_through_the_hot_row_cache(split):
     with pytest.raises(EngramError):
         other.forward_split(split, 4, ids_d, proj, weights, H0.clone(), cache=cache)
     cache.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_multibranch"])
+def test_forward_split_other_shapes(split, name):
+    """fp32 layers (SIMT projection, gate kernel) and four branches (M = 4, the
+    finalize kernel): the split form equals the plain forward bit for bit."""
+    w = {"tiny_f32": W.TINY_F32.scaled(B=3),
+         "small_multibranch": W.MULTIBRANCH_N4.scaled(B=3, T=129, V=5000, V_proj=3850, prime_target=2003, d=256,
+                                                      span_copies=3)}[name]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, w.layers[0])
+    plan, weights, proj, H0 = make_layer(w, L, P, ids.size, table_on_host=True)
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = H0.clone()
+    plan.forward(ids_d, proj, weights, ref)
+    got = H0.clone()
+    plan.forward_split(split, min(2, w.B), ids_d, proj, weights, got)
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    view = (lambda t: t.contiguous().view(torch.int32)) if w.act_dtype == "f32" else bits
+    assert torch.equal(view(got), view(ref))

@@ -137,3 +137,31 @@ def test_argument_errors():
         stage_a_layers(plans, ids_d, built[0][2], tables[:1])
     for p in plans:
         assert p.get_error() == (0, 0)
+
+
+@pytest.mark.parametrize("N,K,row_dim,dtype,B,T", [
+    (3, 8, 64, "i8", 3, 101),      # 16 rows of 64 bytes: 64 chunks, both halves full
+    (4, 4, 32, "i8", 2, 77),       # 12 rows of 32 bytes: 24 chunks per token
+    (3, 4, 16, "bf16", 5, 33),     # 8 rows of 32 bytes: 16 chunks
+    (2, 3, 16, "f32", 1, 7),       # 3 rows of 64 bytes, 7 tokens: the last pair has one token
+])
+def test_half_warp_gather_shapes(N, K, row_dim, dtype, B, T):
+    """Stage A where a token has at most 16 rows and 64 chunks (half a warp per
+    token) against the oracle's gathered rows, odd token counts included, from
+    HBM and from pinned host memory."""
+    w = W.INT8_HOST.scaled(B=B, T=T, V=5000, V_proj=3850, prime_target=2003, d=256, span_copies=2, N=N, K=K,
+                           row_dim=row_dim, table_dtype=dtype, act_dtype="f32" if dtype == "f32" else "bf16")
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, _ = make_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    z = O.hash_heads(O.project(ids, P), L.multipliers, L.primes, w.N, w.K, None)
+    want = O.gather_concat(z.reshape(-1, w.R), L.tables(), w.table_dtype, L.table_scales())
+    for host in (False, True):
+        tab = to_torch(L.table, dtype, "cpu", pin=True) if host else weights.table
+        e = plan.stage_a(ids_d, proj, tab, weights.scales)
+        got = e.cpu().numpy() if dtype == "f32" else bf16_bits(e)
+        exp = want.astype(np.float32) if dtype == "f32" else O.f64_to_bf16_bits(want)
+        assert np.array_equal(got, exp.reshape(got.shape)), (dtype, host)
+        assert plan.get_error() == (0, 0)
