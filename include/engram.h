@@ -153,7 +153,10 @@ engram_status_t engram_hash(const engram_plan_t* plan, const int32_t* ids, int B
  * bf16(q * scale) with one rounding (the product is exact in binary32).
  * An index >= p_r writes a zero row and flags ENGRAM_ERR_INDEX_RANGE.
  * Host tables must be cudaHostAlloc'd or cudaHostRegister'd: otherwise
- * ENGRAM_ERR_NOT_MAPPED. */
+ * ENGRAM_ERR_NOT_MAPPED.  The first read of a newly pinned host table pays for
+ * the GPU's first translation of its pages (measured: 50-70 ms for a 2.6 GB
+ * int8 table); later reads run at the host link's rate whatever the tokens,
+ * so a server warms a table with one call before it takes traffic. */
 engram_status_t engram_gather(const engram_plan_t* plan, const int32_t* idx, int64_t ntok,
                               const void* table, const uint16_t* scales, void* e_out,
                               engram_stream_t stream);
