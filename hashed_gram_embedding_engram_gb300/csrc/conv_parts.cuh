@@ -229,6 +229,68 @@ __device__ __forceinline__ void conv_load_taps(const ConvArgs& a, int c, float (
   }
 }
 
+// One chain of kChain outputs a dilation apart, every row a position of the
+// sequence: v rows vp + j * rstride (j = 0 .. kChain + W - 2, lag (W-1-j) * dil
+// before the first output), their gate scalars sp + j * sstride (s at m, alpha
+// at M + m), H rows hp_s + o * hstride_s in shared memory and hp + o * hstride
+// in global memory.  kFull: all kChain outputs; else the first n_out, and the
+// rows only the others read are neither loaded nor used.  All loads first.
+template <typename TH, int W, bool kFull>
+__device__ __forceinline__ void conv_chain(const float* vp, int rstride, const float* sp, int sstride, int saw, int M,
+                                           int m, const TH* hp_s, int hstride_s, const float (&wq)[4][W], TH* hp,
+                                           int64_t hstride, int n_out) {
+  constexpr int kRows = kChain + W - 1;
+  (void)saw;
+  float vr[kRows][4];
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    if (kFull || j < n_out + W - 1) {
+      ld4(vp + j * rstride, vr[j]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vr[j][i] = 0.f;
+    }
+  }
+  float u[kRows][4], h[kChain][4], at[kChain];
+#pragma unroll
+  for (int o = 0; o < kChain; ++o) {
+    if (kFull || o < n_out) {
+      H4<TH>::load(hp_s + o * hstride_s, h[o]);
+      at[o] = sp[(o + W - 1) * sstride + M + m];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[o][i] = 0.f;
+      at[o] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const float sj = (kFull || j < n_out + W - 1) ? sp[j * sstride + m] : 0.f;
+    mul2(u[j][0], u[j][1], sj, sj, vr[j][0], vr[j][1]);
+    mul2(u[j][2], u[j][3], sj, sj, vr[j][2], vr[j][3]);
+  }
+#pragma unroll
+  for (int o = 0; o < kChain; ++o) {
+    if (!kFull && o >= n_out) break;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      fma2(acc[0], acc[1], wq[0][j], wq[1][j], u[o + j][0], u[o + j][1], acc[0], acc[1]);
+      fma2(acc[2], acc[3], wq[2][j], wq[3][j], u[o + j][2], u[o + j][3], acc[2], acc[3]);
+    }
+    float y[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = silu_fast(acc[i]);
+    fma2(y[0], y[1], at[o], at[o], vr[o + W - 1][0], vr[o + W - 1][1], y[0], y[1]);
+    fma2(y[2], y[3], at[o], at[o], vr[o + W - 1][2], vr[o + W - 1][3], y[2], y[3]);
+    add2(h[o][0], h[o][1], h[o][0], h[o][1], y[0], y[1]);
+    add2(h[o][2], h[o][3], h[o][2], h[o][3], y[2], y[3]);
+  }
+#pragma unroll
+  for (int o = 0; o < kChain; ++o)
+    if (kFull || o < n_out) H4<TH>::store(hp + o * hstride, h[o]);
+}
+
 // One thread: the work items rot, rot + npar, ... of the staged tile at
 // `base`, channels c = c0 + 4g .. c+3 (taps in wq).  An item is one chain of
 // one branch (item = chain * M + branch), so with several branches the chains
@@ -260,47 +322,20 @@ __device__ __forceinline__ void conv_tile(const ConvArgs& a, const uint8_t* base
     const int m = MC == 1 ? 0 : it - ch * M;
     const int tb = (ch / dil) * (kChain * dil) + ch % dil;
     if (tb >= nt) continue;
-    if (t0 + tb - (W - 1) * dil >= 0 && tb + (kChain - 1) * dil < nt) {
-      // interior chain: every row staged, every output in the tile -- no branches, all loads first
+    // every row the chain reads is a position of the sequence (no ring, no zero rows).  With several
+    // branches, whose tiles end inside a chain, a chain that runs past the tile's end also takes
+    // this path and computes only its first n_out outputs (same arithmetic); single-branch tiles
+    // hold whole chains but for a sequence's last tile, and keep the full-chain form alone.
+    const int n_out = min(kChain, (nt - 1 - tb) / dil + 1);
+    if (t0 + tb - (W - 1) * dil >= 0 && (MC != 1 || n_out == kChain)) {
       const int r0 = a.h0 + tb - (W - 1) * dil;
-      const float* vp = vs + r0 * CS + 4 * g;
-      const float* sp = ss + r0 * saw;
-      float vr[kRows][4];
-#pragma unroll
-      for (int j = 0; j < kRows; ++j) ld4(vp + j * rstride, vr[j]);
-      {
-        float u[kRows][4], h[kChain][4], at[kChain];
-#pragma unroll
-        for (int o = 0; o < kChain; ++o) {
-          H4<TH>::load(hs + ((tb + o * dil) * M + m) * CS + 4 * g, h[o]);
-          at[o] = sp[(o + W - 1) * dil * saw + M + m];
-        }
-#pragma unroll
-        for (int j = 0; j < kRows; ++j) {
-          const float sj = sp[j * dil * saw + m];
-          mul2(u[j][0], u[j][1], sj, sj, vr[j][0], vr[j][1]);
-          mul2(u[j][2], u[j][3], sj, sj, vr[j][2], vr[j][3]);
-        }
-#pragma unroll
-        for (int o = 0; o < kChain; ++o) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < W; ++j) {
-            fma2(acc[0], acc[1], wq[0][j], wq[1][j], u[o + j][0], u[o + j][1], acc[0], acc[1]);
-            fma2(acc[2], acc[3], wq[2][j], wq[3][j], u[o + j][2], u[o + j][3], acc[2], acc[3]);
-          }
-          float y[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) y[i] = silu_fast(acc[i]);
-          fma2(y[0], y[1], at[o], at[o], vr[o + W - 1][0], vr[o + W - 1][1], y[0], y[1]);
-          fma2(y[2], y[3], at[o], at[o], vr[o + W - 1][2], vr[o + W - 1][3], y[2], y[3]);
-          add2(h[o][0], h[o][1], h[o][0], h[o][1], y[0], y[1]);
-          add2(h[o][2], h[o][3], h[o][2], h[o][3], y[2], y[3]);
-        }
-        TH* hp = hbase + static_cast<int64_t>(tb) * hrow + static_cast<int64_t>(m) * a.d;
-#pragma unroll
-        for (int o = 0; o < kChain; ++o) H4<TH>::store(hp + static_cast<int64_t>(o * dil) * hrow, h[o]);
-      }
+      TH* hp = hbase + static_cast<int64_t>(tb) * hrow + static_cast<int64_t>(m) * a.d;
+      if (MC == 1 || n_out == kChain)
+        conv_chain<TH, W, true>(vs + r0 * CS + 4 * g, rstride, ss + r0 * saw, dil * saw, saw, M, m,
+                                hs + (tb * M + m) * CS + 4 * g, dil * M * CS, wq, hp, dil * hrow, kChain);
+      else if constexpr (MC != 1)
+        conv_chain<TH, W, false>(vs + r0 * CS + 4 * g, rstride, ss + r0 * saw, dil * saw, saw, M, m,
+                                 hs + (tb * M + m) * CS + 4 * g, dil * M * CS, wq, hp, dil * hrow, n_out);
       continue;
     }
     float vr[kRows][4];                           // v of rows tb + (j - (W-1))*dil, tile-relative
