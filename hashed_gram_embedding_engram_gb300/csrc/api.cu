@@ -830,7 +830,8 @@ engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_
   // both groups' streams start after the work already on `stream`
   if (!order(s, sa, engram::split_event(split, 0)) || cudaStreamWaitEvent(sb, engram::split_event(split, 0), 0))
     return ENGRAM_ERR_CUDA;
-  for (int i = 0; i < n_pieces; ++i) {
+  engram_status_t status = ENGRAM_OK;
+  for (int i = 0; i < n_pieces && status == ENGRAM_OK; ++i) {
     const int lo = static_cast<int>(static_cast<int64_t>(B) * i / n_pieces);
     const int hi = static_cast<int>(static_cast<int64_t>(B) * (i + 1) / n_pieces);
     const int nb = hi - lo;
@@ -849,16 +850,17 @@ engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_
                                                   cache->stats, sa, cache->table_on_host)
               : engram::launch_hash_gather(plan, ids + t0, nb, T, proj, V, prev_i, tab,
                                            static_cast<const uint16_t*>(sc), e_i, sa, host);
-    if (ga != cudaSuccess) return ENGRAM_ERR_CUDA;
-    if (!order(sa, sb, engram::split_event(split, 1 + i))) return ENGRAM_ERR_CUDA;
-    if (engram_status_t r = run_stage_b(plan, ws, e_i, ids + t0, proj, V, nb, T, w, static_cast<char*>(H) + t0 * h_row,
-                                        state ? &st_i : nullptr, sb))
-      return r;
+    if (ga != cudaSuccess || !order(sa, sb, engram::split_event(split, 1 + i))) {
+      status = ENGRAM_ERR_CUDA;
+      break;
+    }
+    status = run_stage_b(plan, ws, e_i, ids + t0, proj, V, nb, T, w, static_cast<char*>(H) + t0 * h_row,
+                         state ? &st_i : nullptr, sb);
   }
-  // `stream` waits for both groups
+  // `stream` waits for both groups, also after an error, so that no work of this call is left unordered
   if (!order(sa, s, engram::split_event(split, n_pieces + 1)) || !order(sb, s, engram::split_event(split, n_pieces + 2)))
     return ENGRAM_ERR_CUDA;
-  return ENGRAM_OK;
+  return status;
 }
 
 engram_status_t engram_cache_stats(const engram_cache_t* c, engram_stream_t stream, int reset,
