@@ -263,3 +263,22 @@ def test_forward_split_other_shapes(split, name):
     assert plan.get_error() == (0, 0)
     view = (lambda t: t.contiguous().view(torch.int32)) if w.act_dtype == "f32" else bits
     assert torch.equal(view(got), view(ref))
+
+
+@pytest.mark.parametrize("name", ["small_i8", "small_multibranch"])
+def test_forward_split_matches_oracle(split, name):
+    """engram_forward_split's H against the float64 oracle (Steps 1-8), element by
+    element, within the bf16 tolerance."""
+    from oracle import engram_oracle as O
+    from tests.gpu_helpers import act_to_f64, assert_close
+    from tests.test_gpu_parity import SMALL
+    w = SMALL[name]
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, w.layers[0])
+    ref = O.forward(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype, None)
+    plan, weights, proj, H = make_layer(w, L, P, ids.size, table_on_host=True)
+    plan.forward_split(split, w.B, torch.from_numpy(ids).cuda(), proj, weights, H)
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    assert_close(act_to_f64(H), ref["H_new"], w.act_dtype, name)
