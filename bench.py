@@ -149,6 +149,8 @@ def _per_token_work(w, bn: int) -> dict:
         "stage_b": ("flops", 2 * w.d_mem * nc),
         # FP8 projection: e read in bf16, its e4m3 codes and the token's scale written; the e4m3 GEMM
         "quantize_e": ("bytes", 2 * w.d_mem + w.d_mem + 4),
+        # the gather writing e's e4m3 codes and the token's scale instead of e
+        "hash_gather_e4m3": ("bytes", 4 + 4 + w.R * row_bytes + w.d_mem + 4),
         "kv_gemm_fp8": ("flops", 2 * w.d_mem * nc),
         # gate partials in; the (scale, alpha) row out
         "finalize": ("bytes", 4 * n_part + 8 * w.M),
@@ -204,7 +206,8 @@ def profiled_traffic(kernel: str):
 # kernel lists of one engram_forward by the number of traced intervals
 NAME_SETS = {2: ["hash_gather", "stage_b"], 3: ["hash_gather", "kv_gemm", "conv"],
              4: ["hash_gather", "kv_gemm", "finalize", "conv"]}
-NAME_SETS_FP8 = {4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
+NAME_SETS_FP8 = {3: ["hash_gather_e4m3", "kv_gemm_fp8", "conv"],
+                 4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
                  5: ["hash_gather", "quantize_e", "kv_gemm_fp8", "finalize", "conv"]}
 NAME_SETS_DECODE = {1: ["decode_step"], 3: ["hash_gather", "kv_gemm", "decode_tail"]}
 
@@ -282,7 +285,7 @@ def run_ours(args) -> None:
     import numpy as np
     import torch
     import workloads as W
-    from hashed_gram_embedding_engram_gb300 import EngramLayer, stage_a_layers
+    from hashed_gram_embedding_engram_gb300 import EngramLayer, stage_a_layers, stage_a_layers_e4m3
     from workloads.torch_layer import make_layer, to_torch
 
     world, rank, local = dist_env()
@@ -318,6 +321,9 @@ def run_ours(args) -> None:
 
     side = torch.cuda.Stream()
     e_bufs = [torch.empty(w.ntok, w.d_mem, dtype=torch.bfloat16, device=dev) for _ in layers]
+    # with the e4m3 projection the gather writes e's codes and scales itself
+    q_bufs = [(torch.empty(w.ntok, w.d_mem, dtype=torch.uint8, device=dev),
+               torch.empty(w.ntok, dtype=torch.float32, device=dev)) for _ in layers] if fp8 else None
 
     def step():
         # Stage A (hash + gather) depends on the token ids only: every layer's
@@ -328,13 +334,21 @@ def run_ours(args) -> None:
         main = torch.cuda.current_stream()
         side.wait_stream(main)
         with torch.cuda.stream(side):
-            stage_a_layers([ly["plan"] for ly in layers], ids, layers[0]["proj"],
-                           [ly["weights"].table for ly in layers], outs=e_bufs)
+            if fp8:
+                stage_a_layers_e4m3([ly["plan"] for ly in layers], ids, layers[0]["proj"],
+                                    [ly["weights"].table for ly in layers], outs=q_bufs)
+            else:
+                stage_a_layers([ly["plan"] for ly in layers], ids, layers[0]["proj"],
+                               [ly["weights"].table for ly in layers], outs=e_bufs)
             ready = torch.cuda.Event()
             ready.record(side)
         main.wait_event(ready)
-        for ly, e in zip(layers, e_bufs):
-            ly["plan"].stage_b(e, ly["weights"], ly["H"], workspace=ly["ws"])
+        if fp8:
+            for ly, (q, sc) in zip(layers, q_bufs):
+                ly["plan"].stage_b_e4m3(q, sc, ly["weights"], ly["H"], workspace=ly["ws"])
+        else:
+            for ly, e in zip(layers, e_bufs):
+                ly["plan"].stage_b(e, ly["weights"], ly["H"], workspace=ly["ws"])
 
     def restore():
         for ly in layers:
@@ -765,7 +779,7 @@ def run_workload(args) -> None:
     pinned-host-to-device copy rate measured in the same run."""
     import torch
     import workloads as W
-    from hashed_gram_embedding_engram_gb300 import EngramState, stage_a_layers
+    from hashed_gram_embedding_engram_gb300 import EngramState, stage_a_layers, stage_a_layers_e4m3
     from workloads.torch_layer import make_layer, to_torch
 
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -801,6 +815,12 @@ def run_workload(args) -> None:
     ids = torch.from_numpy(ids_np[:, w.prefix_len:].copy()).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     side = torch.cuda.Stream()
+    # e4m3 projection on bf16 rows of at most 128 chunks per token: the gather writes e's codes itself
+    codes = fp8 and w.table_dtype == "bf16" and w.act_dtype == "bf16" and w.R <= 32 and w.R * w.row_dim * 2 <= 2048
+    if codes:
+        for ly in layers:
+            ly["q8"] = (torch.empty(w.ntok, w.d_mem, dtype=torch.uint8, device=dev),
+                        torch.empty(w.ntok, dtype=torch.float32, device=dev))
 
     def step(table_key=None):
         if table_key == "fused_decode":
@@ -816,6 +836,13 @@ def run_workload(args) -> None:
                     st = ly.get("state")
                     ly[table_key].stage_a(ids, ly["proj"], ly["weights"].scales,
                                           prev_ids=None if st is None else st.prev_ids, out=ly["e"])
+            elif codes and table_key is None:
+                # every layer's Stage A in one launch, writing e's e4m3 codes and scales
+                stage_a_layers_e4m3([ly["plan"] for ly in layers], ids, layers[0]["proj"],
+                                    [ly["weights"].table for ly in layers],
+                                    prev_ids=None if layers[0].get("state") is None else
+                                    [ly["state"].prev_ids for ly in layers],
+                                    outs=[ly["q8"] for ly in layers])
             else:
                 # every layer's Stage A in one launch
                 stage_a_layers([ly["plan"] for ly in layers], ids, layers[0]["proj"],
@@ -829,8 +856,12 @@ def run_workload(args) -> None:
             ready.record(side)
         main.wait_event(ready)
         for ly in layers:
-            ly["plan"].stage_b(ly["e"], ly["weights"], ly["H"], ly.get("state"), ids=ids, proj=ly["proj"],
-                               workspace=ly["ws"])
+            if codes and table_key is None:
+                ly["plan"].stage_b_e4m3(ly["q8"][0], ly["q8"][1], ly["weights"], ly["H"], ly.get("state"), ids=ids,
+                                        proj=ly["proj"], workspace=ly["ws"])
+            else:
+                ly["plan"].stage_b(ly["e"], ly["weights"], ly["H"], ly.get("state"), ids=ids, proj=ly["proj"],
+                                   workspace=ly["ws"])
 
     def restore():
         for ly in layers:

@@ -24,7 +24,7 @@ EXPORTS = ("engram_status_string", "engram_plan_create", "engram_plan_destroy", 
            "engram_cache_observe", "engram_cache_build", "engram_stage_a_cached", "engram_cache_stats",
            "engram_cache_set_dedup", "engram_quantize_fp8", "engram_plan_set_sm_limit", "engram_plan_host_gather_sms", "engram_plan_set_host_gather_sms",
            "engram_sm_split_create", "engram_sm_split_sms", "engram_sm_split_stream", "engram_sm_split_destroy",
-           "engram_forward_split")
+           "engram_forward_split", "engram_stage_a_e4m3", "engram_stage_a_layers_e4m3", "engram_stage_b_e4m3")
 
 
 class Config(ctypes.Structure):
@@ -104,6 +104,10 @@ def _lib() -> ctypes.CDLL:
         lib.engram_sm_split_destroy.argtypes = [vp]
         lib.engram_forward_split.argtypes = [vp, vp, i32, vp, vp, i32, i32, vp, i32, ctypes.POINTER(Weights), vp,
                                              ctypes.POINTER(State), vp, sz, vp]
+        lib.engram_stage_a_e4m3.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
+        lib.engram_stage_a_layers_e4m3.argtypes = [i32, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
+        lib.engram_stage_b_e4m3.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, ctypes.POINTER(Weights), vp,
+                                            ctypes.POINTER(State), vp, sz, vp]
         lib.engram_plan_set_fused_decode.argtypes = [vp, i32]
         lib.engram_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]
         for name in EXPORTS:

@@ -362,6 +362,48 @@ engram_status_t engram_stage_a_layers(int n_layers, const engram_plan_t* const* 
                                                        i8 ? sc : nullptr, e_out, (cudaStream_t)stream, host0));
 }
 
+engram_status_t engram_stage_a_layers_e4m3(int n_layers, const engram_plan_t* const* plans, const int32_t* ids,
+                                           int B, int T, const int32_t* proj, int V, const int32_t* const* prev_ids,
+                                           const void* const* tables, uint8_t* const* e8_out,
+                                           float* const* e_scale_out, engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_stage_a_layers_e4m3");
+  if (n_layers < 1 || n_layers > engram::kMaxGatherLayers || !plans || !tables || !e8_out || !e_scale_out)
+    return ENGRAM_ERR_INVALID_ARG;
+  const engram_plan_t* p0 = plans[0];
+  if (!p0) return ENGRAM_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const engram_plan_t* p = plans[l];
+    if (!p || p->device != p0->device || p->cfg.N != p0->cfg.N || p->cfg.K != p0->cfg.K ||
+        p->cfg.row_dim != p0->cfg.row_dim || p->cfg.table_dtype != p0->cfg.table_dtype ||
+        p->cfg.act_dtype != p0->cfg.act_dtype)
+      return ENGRAM_ERR_INVALID_ARG;
+    if (engram_status_t s = check_tokens(p, B, T)) return s;
+  }
+  if (!engram::gather_e4m3_applies(p0)) return ENGRAM_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * T == 0) return ENGRAM_OK;
+  if (!ids || !proj || V <= 0) return ENGRAM_ERR_INVALID_ARG;
+  const void* tab[engram::kMaxGatherLayers] = {};
+  bool host0 = false;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!tables[l] || !e8_out[l] || !e_scale_out[l] || !aligned16(e8_out[l]) || !aligned16(e_scale_out[l]))
+      return ENGRAM_ERR_INVALID_ARG;
+    bool host = false;
+    if (engram_status_t s = device_view(tables[l], &tab[l], &host)) return s;
+    if (!aligned16(tab[l])) return ENGRAM_ERR_INVALID_ARG;
+    if (l == 0) host0 = host;
+    if (host != host0) return ENGRAM_ERR_INVALID_ARG;
+  }
+  return cuda_status(engram::launch_hash_gather_layers_e4m3(plans, n_layers, ids, B, T, proj, V, prev_ids, tab,
+                                                            e8_out, e_scale_out, (cudaStream_t)stream, host0));
+}
+
+engram_status_t engram_stage_a_e4m3(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
+                                    int V, const int32_t* prev_ids, const void* table, uint8_t* e8_out,
+                                    float* e_scale_out, engram_stream_t stream) {
+  return engram_stage_a_layers_e4m3(1, &plan, ids, B, T, proj, V, prev_ids ? &prev_ids : nullptr, &table, &e8_out,
+                                    &e_scale_out, stream);
+}
+
 engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, int64_t ntok, const void* w_kv,
                                      void* kv_out, engram_stream_t stream) {
   NvtxRange nvtx_range("engram_kv_projection");
@@ -373,9 +415,12 @@ engram_status_t engram_kv_projection(const engram_plan_t* plan, const void* e, i
 }
 
 // Steps 5-8 from e (already gathered into ws.e or the caller's buffer).
+// e8 / e_scale: e's e4m3 codes and scales from the codes gather (FP8 weights only), used instead of
+// quantising e (which may then be null)
 static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Workspace& ws, const void* e,
                                    const int32_t* ids, const int32_t* proj, int V, int B, int T,
-                                   const engram_weights_t* w, void* H, engram_state_t* state, cudaStream_t s) {
+                                   const engram_weights_t* w, void* H, engram_state_t* state, cudaStream_t s,
+                                   const uint8_t* e8 = nullptr, const float* e_scale = nullptr) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
   const int d = plan->cfg.d, M = plan->cfg.M;
   const float* v = nullptr;
@@ -426,12 +471,16 @@ static engram_status_t run_stage_b(const engram_plan_t* plan, const engram::Work
     }
     int n_sl = 0, pstride = 0;
     if (f8) {
-      // e4m3 projection: each token's row of e quantised, then the GEMM on the codes
-      if (engram::launch_quantize_rows_e4m3(e, ntok, plan->d_mem, ws.e8, ws.e_scale, engram::stage_b_sms(plan), s) !=
-          cudaSuccess)
-        return ENGRAM_ERR_CUDA;
-      mark(plan, s);
-      if (engram::gemm_e4m3_engram(ws.e8, ws.e_scale, w->w_kv_fp8, w->w_kv_scale, ntok, d, M, plan->d_mem, H, w->g_h,
+      // e4m3 projection: each token's row of e quantised (unless the gather wrote the codes), then the GEMM on them
+      if (e8 == nullptr) {
+        if (engram::launch_quantize_rows_e4m3(e, ntok, plan->d_mem, ws.e8, ws.e_scale, engram::stage_b_sms(plan),
+                                              s) != cudaSuccess)
+          return ENGRAM_ERR_CUDA;
+        mark(plan, s);
+        e8 = ws.e8;
+        e_scale = ws.e_scale;
+      }
+      if (engram::gemm_e4m3_engram(e8, e_scale, w->w_kv_fp8, w->w_kv_scale, ntok, d, M, plan->d_mem, H, w->g_h,
                                    w->g_k, ws.v32, ws.part, &n_sl, &pstride, engram::stage_b_sms(plan),
                                    &plan->dev->err, s) !=
           cudaSuccess)
@@ -506,6 +555,27 @@ engram_status_t engram_stage_b(const engram_plan_t* plan, const int32_t* ids, in
   return run_stage_b(plan, ws, e, ids, proj, V, B, T, w, H, state, (cudaStream_t)stream);
 }
 
+engram_status_t engram_stage_b_e4m3(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
+                                    int V, const uint8_t* e8, const float* e_scale, const engram_weights_t* w, void* H,
+                                    engram_state_t* state, void* workspace, size_t workspace_bytes,
+                                    engram_stream_t stream) {
+  NvtxRange nvtx_range("engram_stage_b_e4m3");
+  if (!plan) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_tokens(plan, B, T)) return s;
+  const int64_t ntok = static_cast<int64_t>(B) * T;
+  if (ntok == 0) return ENGRAM_OK;
+  if (!e8 || !e_scale || !H || !aligned16(e8) || !aligned16(e_scale) || !aligned16(H)) return ENGRAM_ERR_INVALID_ARG;
+  if (!w || !w->w_kv_fp8) return ENGRAM_ERR_INVALID_ARG;
+  if (state && (!ids || !proj || V <= 0)) return ENGRAM_ERR_INVALID_ARG;
+  if (engram_status_t s = check_weights(plan, w, false)) return s;
+  if (engram_status_t s = check_state(plan, state)) return s;
+  engram::Workspace ws = engram::carve_workspace(plan, ntok, workspace);
+  if (!workspace || workspace_bytes < ws.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ENGRAM_ERR_WORKSPACE;
+  plan->n_marks = 0;
+  return run_stage_b(plan, ws, nullptr, ids, proj, V, B, T, w, H, state, (cudaStream_t)stream, e8, e_scale);
+}
+
 engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, int B, int T, const int32_t* proj,
                                int V, const engram_weights_t* w, void* H, engram_state_t* state, void* workspace,
                                size_t workspace_bytes, engram_stream_t stream) {
@@ -542,6 +612,13 @@ engram_status_t engram_forward(const engram_plan_t* plan, const int32_t* ids, in
     }
     if (de != cudaErrorCooperativeLaunchTooLarge) return ENGRAM_ERR_CUDA;
     (void)cudaGetLastError();     // fewer co-resident blocks than SMs (e.g. a partitioned device): three launches
+  }
+  if (w->w_kv_fp8 != nullptr && engram::gather_e4m3_applies(plan)) {
+    // FP8 projection: the gather writes e's codes and scales itself (no e, no quantisation launch)
+    if (engram::launch_hash_gather_e4m3(plan, ids, B, T, proj, V, prev, tab, ws.e8, ws.e_scale, s, host) !=
+        cudaSuccess)
+      return ENGRAM_ERR_CUDA;
+    return run_stage_b(plan, ws, nullptr, ids, proj, V, B, T, w, H, state, s, ws.e8, ws.e_scale);
   }
   if (engram::launch_hash_gather(plan, ids, B, T, proj, V, prev, tab, static_cast<const uint16_t*>(sc), ws.e, s,
                                  host) != cudaSuccess)

@@ -139,6 +139,17 @@ cudaError_t launch_hash_gather_layers(const engram_plan* const* plans, int n_lay
                                       const int32_t* proj, int V, const int32_t* const* prev_ids,
                                       const void* const* tables, const uint16_t* const* scales, void* const* e,
                                       cudaStream_t s, bool host_table = false);
+// Steps 1-4 writing e's e4m3 codes and per-token scales instead of e (the FP8
+// projection's input), for bf16 tables of at most 32 rows and 128 chunks per
+// token (gather_e4m3_applies); else cudaErrorInvalidValue.
+bool gather_e4m3_applies(const engram_plan* p);
+cudaError_t launch_hash_gather_e4m3(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                                    const int32_t* prev_ids, const void* table, uint8_t* e8, float* e_scale,
+                                    cudaStream_t s, bool host_table);
+cudaError_t launch_hash_gather_layers_e4m3(const engram_plan* const* plans, int n_layers, const int32_t* ids, int B,
+                                           int T, const int32_t* proj, int V, const int32_t* const* prev_ids,
+                                           const void* const* tables, uint8_t* const* e8, float* const* e_scale,
+                                           cudaStream_t s, bool host_table);
 // The same through the HBM hot-row cache (slot map, cached rows, [lookups, hits] counters).
 cudaError_t launch_hash_gather_cached(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj,
                                       int V, const int32_t* prev_ids, const void* table, const uint16_t* scales,

@@ -23,6 +23,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "e4m3.cuh"
 #include "engram_internal.h"
 #include "gather_parts.cuh"
 #include "ptx.cuh"
@@ -56,7 +57,12 @@ constexpr int kThreads = 128;
 // and leaves the others to the work running beside the lookup.
 // (The row and chunk phases are written out here, not through ga::row_phase
 // and ga::chunk_phase as in decode.cu: this form measured 7 % faster.)
-template <int kCpr, bool kInt8, bool kHash, bool kCache = false, bool kWide = false, int kBlk = kThreads>
+// kQ8 (bf16 rows, a token's chunks within one round of loads): instead of
+// e, the token's e4m3 codes and scale for the FP8 projection, from the row
+// the warp holds in registers (the arithmetic of e4m3.cuh, so the bytes of
+// the quantisation kernel run on e).
+template <int kCpr, bool kInt8, bool kHash, bool kCache = false, bool kWide = false, int kBlk = kThreads,
+          bool kQ8 = false>
 __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
     row_gather_kernel(const GatherLayers ls, int R, int N, int K, const int32_t* __restrict__ idx,
                       const int32_t* __restrict__ ids, int T, const int32_t* __restrict__ proj, int V, int64_t ntok,
@@ -71,6 +77,8 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
   const uint8_t* __restrict__ table = ls.table[ly];
   const __half* __restrict__ scales = ls.scales[ly];
   uint4* __restrict__ out = ls.out[ly];
+  uint8_t* __restrict__ q8 = ls.q8[ly];
+  float* __restrict__ qscale = ls.qscale[ly];
   constexpr int kRows = kWide ? 2 : 1;
   const bool has0 = lane < R, has1 = kWide && lane + 32 < R;
   RowConst rc[kRows];
@@ -185,6 +193,24 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
         if constexpr (kHash) {
           if (more) x_cur = window_hop2(hop, proj);
         }
+      }
+      if constexpr (kQ8) {
+        // the token's whole row is in this round's registers: its amax, scale and codes
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < kWarpItems; ++j)
+          if (f0 + j * 32 + lane < per_tok) amax = e4m3::amax8(v[j], amax);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float inv = e4m3::inv_of(amax);
+        if (lane == 0) qscale[tok] = e4m3::scale_of(amax);
+        uint2* qd = reinterpret_cast<uint2*>(q8 + tok * per_tok * 8);
+#pragma unroll
+        for (int j = 0; j < kWarpItems; ++j) {
+          const int f = f0 + j * 32 + lane;
+          if (f < per_tok) qd[f] = e4m3::quant8(v[j], inv);
+        }
+        continue;
       }
 #pragma unroll
       for (int j = 0; j < kWarpItems; ++j) {
@@ -375,7 +401,8 @@ cudaError_t launch_idx(const engram_plan* p, const int32_t* idx, int64_t ntok, c
 // with tables in host memory, the grid's share of the SMs is split among them.
 template <int kCpr, bool kInt8>
 cudaError_t launch_fused(const engram_plan* p, int n_layers, const GatherLayers& ls, const int32_t* ids, int B, int T,
-                         const int32_t* proj, int V, cudaStream_t s, bool host_table, const RowCache* cache) {
+                         const int32_t* proj, int V, cudaStream_t s, bool host_table, const RowCache* cache,
+                         bool q8 = false) {
   const int64_t ntok = static_cast<int64_t>(B) * T;
   int gx = grid_for_tokens(p, ntok, host_table);
   const int cap = host_table ? hostgrid_sms(p) : p->num_sms * 8;   // one wave over all layers
@@ -383,6 +410,18 @@ cudaError_t launch_fused(const engram_plan* p, int n_layers, const GatherLayers&
   const dim3 grid(gx, n_layers);
   const dim3 block(host_table ? kHostBlk : kThreads);
   const bool wide = p->R > 32;
+  if (q8) {
+    if constexpr (!kInt8) {
+      // e4m3 codes of bf16 rows: the token's chunks within one round of loads
+      if (cache != nullptr || wide || p->R * kCpr > 32 * kWarpItems || p->cfg.table_dtype != ENGRAM_BF16)
+        return cudaErrorInvalidValue;
+      auto k = host_table ? row_gather_kernel<kCpr, false, true, false, false, kHostBlk, true>
+                          : row_gather_kernel<kCpr, false, true, false, false, kThreads, true>;
+      return launch_pdl(k, grid, block, 0, s, ls, p->R, p->cfg.N, p->cfg.K, static_cast<const int32_t*>(nullptr), ids,
+                        T, proj, V, ntok, RowCache{});
+    }
+    return cudaErrorInvalidValue;
+  }
   if constexpr (kCpr <= 4) {
     if (p->R <= 16 && kCpr * p->R <= 64) {
       // half a warp per token
@@ -477,6 +516,39 @@ cudaError_t launch_hash_gather_layers(const engram_plan* const* plans, int n_lay
 #define CALL(C, I) launch_fused<C, I>(p, n_layers, ls, ids, B, T, proj, V, s, host_table, nullptr)
   ENGRAM_DISPATCH_CPR(CALL)
 #undef CALL
+}
+
+bool gather_e4m3_applies(const engram_plan* p) {
+  return p->cfg.table_dtype == ENGRAM_BF16 && p->cfg.act_dtype == ENGRAM_BF16 && p->R <= 32 &&
+         p->R * chunks_per_row(p) <= 32 * kWarpItems;
+}
+
+cudaError_t launch_hash_gather_layers_e4m3(const engram_plan* const* plans, int n_layers, const int32_t* ids, int B,
+                                           int T, const int32_t* proj, int V, const int32_t* const* prev_ids,
+                                           const void* const* tables, uint8_t* const* e8, float* const* e_scale,
+                                           cudaStream_t s, bool host_table) {
+  if (n_layers < 1 || n_layers > kMaxGatherLayers || !gather_e4m3_applies(plans[0])) return cudaErrorInvalidValue;
+  const engram_plan* p = plans[0];
+  GatherLayers ls{};
+  for (int l = 0; l < n_layers; ++l) {
+    ls.pdg[l] = plans[l]->dev;
+    ls.err[l] = &plans[l]->dev->err;
+    ls.prev[l] = prev_ids != nullptr ? prev_ids[l] : nullptr;
+    ls.table[l] = static_cast<const uint8_t*>(tables[l]);
+    ls.q8[l] = e8[l];
+    ls.qscale[l] = e_scale[l];
+  }
+  const bool i8 = false;
+#define CALL(C, I) launch_fused<C, I>(p, n_layers, ls, ids, B, T, proj, V, s, host_table, nullptr, true)
+  ENGRAM_DISPATCH_CPR(CALL)
+#undef CALL
+}
+
+cudaError_t launch_hash_gather_e4m3(const engram_plan* p, const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                                    const int32_t* prev_ids, const void* table, uint8_t* e8, float* e_scale,
+                                    cudaStream_t s, bool host_table) {
+  return launch_hash_gather_layers_e4m3(&p, 1, ids, B, T, proj, V, prev_ids ? &prev_ids : nullptr, &table, &e8,
+                                        &e_scale, s, host_table);
 }
 
 #undef ENGRAM_DISPATCH_CPR

@@ -68,6 +68,8 @@ struct GatherLayers {
   const uint8_t* table[kMaxGatherLayers];
   const __half* scales[kMaxGatherLayers];
   uint4* out[kMaxGatherLayers];
+  uint8_t* q8[kMaxGatherLayers];       // e4m3 codes of e [ntok, d_mem] instead of e (the codes kernel)
+  float* qscale[kMaxGatherLayers];     // and each token's scale [ntok]
 };
 
 // Per-lane table constants of one of the R rows a token reads: the lanes of a

@@ -15,33 +15,15 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include "e4m3.cuh"
 #include "engram_internal.h"
 #include "ptx.cuh"
 
 namespace engram {
 namespace {
 
-constexpr float kE4M3Max = 448.f;
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t e4m3_byte(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-// four bf16 pairs (8 values) times inv -> 8 e4m3 codes, element j in byte j
-__device__ __forceinline__ uint2 quant8(uint4 v, float inv) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[2] = {0u, 0u};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t lo = e4m3_byte(bf16_lo(w[j]) * inv);
-    const uint32_t hi = e4m3_byte(bf16_hi(w[j]) * inv);
-    out[j >> 1] |= (lo | (hi << 8)) << ((j & 1) * 16);
-  }
-  return make_uint2(out[0], out[1]);
-}
+using e4m3::amax8;
+using e4m3::quant8;
 
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows, int cols,
                                                             uint8_t* __restrict__ q, float* __restrict__ scale) {
@@ -54,16 +36,11 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
        row += n_warps) {
     const uint4* xr = reinterpret_cast<const uint4*>(x + row * cols);
     float amax = 0.f;
-    for (int i = lane; i < n8; i += 32) {
-      const uint4 v = xr[i];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-    }
+    for (int i = lane; i < n8; i += 32) amax = amax8(xr[i], amax);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const float inv = amax > 0.f ? kE4M3Max / amax : 0.f;
-    if (lane == 0) scale[row] = amax > 0.f ? amax / kE4M3Max : 1.f;
+    const float inv = e4m3::inv_of(amax);
+    if (lane == 0) scale[row] = e4m3::scale_of(amax);
     uint4* qr = reinterpret_cast<uint4*>(q + row * cols);
     for (int i = lane; i < n8 / 2; i += 32) {
       const uint2 a = quant8(xr[2 * i], inv);

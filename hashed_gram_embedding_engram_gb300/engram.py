@@ -259,6 +259,31 @@ class EngramPlan:
             _dev(ws, "workspace"), ws.numel(), _stream()), "engram_stage_b")
         return H
 
+    def stage_a_e4m3(self, ids: torch.Tensor, proj: torch.Tensor, table: torch.Tensor,
+                     prev_ids: Optional[torch.Tensor] = None,
+                     out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+        """Steps 1-4 writing e's e4m3 codes [B*T, d_mem] and scales [B*T] instead of e
+        (engram_stage_a_e4m3; bf16 layers)."""
+        return stage_a_layers_e4m3([self], ids, proj, [table], None if prev_ids is None else [prev_ids],
+                                   None if out is None else [out])[0]
+
+    def stage_b_e4m3(self, e8: torch.Tensor, e_scale: torch.Tensor, weights: EngramWeights, H: torch.Tensor,
+                     state: Optional[EngramState] = None, ids: Optional[torch.Tensor] = None,
+                     proj: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Steps 5-8 from e's e4m3 codes and scales (engram_stage_b_e4m3); the weights carry W_kv in e4m3."""
+        B, T = H.shape[0], H.shape[1]
+        ws = self.new_workspace(B * T, H.device) if workspace is None else workspace
+        w = weights.struct(self, need_table=False)
+        st = None if state is None else ctypes.byref(state.struct(self, B))
+        ids_p = 0 if ids is None else _dev(ids, "ids", torch.int32, (B, T))
+        proj_p, V = (0, 0) if proj is None else (_dev(proj, "proj", torch.int32), proj.numel())
+        _lib.check(self._lib.engram_stage_b_e4m3(
+            self._h, ids_p, B, T, proj_p, V, _dev(e8, "e8", torch.uint8, (B * T, self.d_mem)),
+            _dev(e_scale, "e_scale", torch.float32, (B * T,)), ctypes.byref(w),
+            _dev(H, "H", self.act_torch_dtype, (B, T, self.M, self.d)), st, _dev(ws, "workspace"), ws.numel(),
+            _stream()), "engram_stage_b_e4m3")
+        return H
+
     def forward(self, ids: torch.Tensor, proj: torch.Tensor, weights: EngramWeights, H: torch.Tensor,
                 state: Optional[EngramState] = None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Steps 1-8 in place on H [B, T, M, d]; ``state`` continues sequences."""
@@ -461,6 +486,34 @@ def stage_a_layers(plans: Sequence["EngramPlan"], ids: torch.Tensor, proj: torch
     _lib.check(p0._lib.engram_stage_a_layers(n, h, _dev(ids, "ids", torch.int32), B, T,
                                              _dev(proj, "proj", torch.int32), proj.numel(), prev, tab, sc, out,
                                              _stream()), "engram_stage_a_layers")
+    return list(outs)
+
+
+def stage_a_layers_e4m3(plans: Sequence["EngramPlan"], ids: torch.Tensor, proj: torch.Tensor,
+                        tables: Sequence[torch.Tensor], prev_ids: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                        outs: Optional[Sequence[Tuple[torch.Tensor, torch.Tensor]]] = None) -> list:
+    """Stage A of several bf16 layers in one launch, writing each layer's e4m3
+    codes [B*T, d_mem] (uint8) and per-token scales [B*T] (float32) instead of e
+    (engram_stage_a_layers_e4m3): the bytes quantize_fp8 makes of stage_a's rows."""
+    n = len(plans)
+    if n == 0 or len(tables) != n or (prev_ids is not None and len(prev_ids) != n) or \
+            (outs is not None and len(outs) != n):
+        raise ValueError("stage_a_layers_e4m3: plans, tables, prev_ids and outs must have one entry per layer")
+    B, T = ids.shape
+    p0 = plans[0]
+    if outs is None:
+        outs = [(torch.empty(B * T, p.d_mem, dtype=torch.uint8, device=ids.device),
+                 torch.empty(B * T, dtype=torch.float32, device=ids.device)) for p in plans]
+    arr = lambda vals: (ctypes.c_void_p * n)(*vals)  # noqa: E731
+    h = arr([p._h.value for p in plans])
+    tab = arr([_dev_or_pinned(t, "table", _TABLE_DTYPES[p.table_dtype][1]) for p, t in zip(plans, tables)])
+    prev = 0 if prev_ids is None else arr(
+        [0 if x is None else _dev(x, "prev_ids", torch.int32, (B, p.N - 1)) for p, x in zip(plans, prev_ids)])
+    q = arr([_dev(o[0], "e8_out", torch.uint8, (B * T, p.d_mem)) for p, o in zip(plans, outs)])
+    sc = arr([_dev(o[1], "e_scale_out", torch.float32, (B * T,)) for p, o in zip(plans, outs)])
+    _lib.check(p0._lib.engram_stage_a_layers_e4m3(n, h, _dev(ids, "ids", torch.int32), B, T,
+                                                  _dev(proj, "proj", torch.int32), proj.numel(), prev, tab, q, sc,
+                                                  _stream()), "engram_stage_a_layers_e4m3")
     return list(outs)
 
 

@@ -108,7 +108,8 @@ typedef struct {
   /* FP8 projection (BF16 layers, d_mem a multiple of 128), or both NULL.  With
    * them, Step 5 runs on e4m3 operands: W_kv as quantised by
    * engram_quantize_fp8 (one scale per output row), e quantised per token by
-   * the call itself; w_kv is then not read and may be NULL. */
+   * the call itself (engram_forward: by its gather, where engram_stage_a_e4m3
+   * applies); w_kv is then not read and may be NULL. */
   const uint8_t* w_kv_fp8;      /* e4m3 [(M+1)*d, d_mem] */
   const float* w_kv_scale;      /* [(M+1)*d] */
 } engram_weights_t;
@@ -218,6 +219,35 @@ engram_status_t engram_stage_b(const engram_plan_t* plan, const int32_t* ids, in
                                const int32_t* proj, int V, const void* e,
                                const engram_weights_t* w, void* H, engram_state_t* state,
                                void* workspace, size_t workspace_bytes, engram_stream_t stream);
+
+/* Stage A for the FP8 projection: Steps 1-4 writing, instead of e, its e4m3
+ * codes and per-token scales -- exactly what engram_quantize_fp8 would make of
+ * the rows engram_stage_a writes (same rule, same bytes; see there) -- from
+ * the row each warp holds in registers, so e never reaches memory and no
+ * quantisation launch follows.  For BF16 tables and activations with at most
+ * 32 rows and 128 16-byte chunks per token (R * row_dim * 2 <= 2048 bytes),
+ * else ENGRAM_ERR_UNSUPPORTED.  e8_out: device uint8 [B*T, d_mem]; e_scale_out:
+ * device float [B*T]; both 16-byte aligned.  Other arguments, errors and the
+ * several-layer form as engram_stage_a and engram_stage_a_layers (there:
+ * e8_out[l], e_scale_out[l] per layer). */
+engram_status_t engram_stage_a_e4m3(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                                    const int32_t* proj, int V, const int32_t* prev_ids, const void* table,
+                                    uint8_t* e8_out, float* e_scale_out, engram_stream_t stream);
+engram_status_t engram_stage_a_layers_e4m3(int n_layers, const engram_plan_t* const* plans,
+                                           const int32_t* ids, int B, int T, const int32_t* proj, int V,
+                                           const int32_t* const* prev_ids, const void* const* tables,
+                                           uint8_t* const* e8_out, float* const* e_scale_out,
+                                           engram_stream_t stream);
+
+/* Stage B from the codes of engram_stage_a_e4m3: engram_stage_b with e given
+ * as e4m3 codes e8 [B*T, d_mem] and scales e_scale [B*T] (device, 16-byte
+ * aligned) instead of bf16 rows; the weights must carry the FP8 projection
+ * (w_kv_fp8, w_kv_scale), else ENGRAM_ERR_INVALID_ARG.  The same bits as
+ * engram_stage_b on the rows the codes were made from. */
+engram_status_t engram_stage_b_e4m3(const engram_plan_t* plan, const int32_t* ids, int B, int T,
+                                    const int32_t* proj, int V, const uint8_t* e8, const float* e_scale,
+                                    const engram_weights_t* w, void* H, engram_state_t* state,
+                                    void* workspace, size_t workspace_bytes, engram_stream_t stream);
 
 /* Steps 1-8: the whole layer for B sequences of T new tokens each.
  * ids/proj/V as in engram_hash; w as in engram_weights_t; H: [B, T, M, d]

@@ -104,3 +104,83 @@ def test_fp8_streaming_and_decode_are_bit_identical_to_prefill():
     ref = O.forward_at(ids, P, L, w.N, w.K, w.conv_dil, w.eps, w.table_dtype, w.act_dtype, pos, projection="fp8")
     got = np.stack([act_to_f64(full[b, t]) for b, t in pos])
     assert_close(got, ref, "bf16", "fp8 sampled")
+
+
+# ---------------------------------------------------------------- codes written by the gather
+def _codes_ref(w, ids, P, L, prev=None):
+    """The oracle's e4m3 codes and scales of the oracle's gathered rows."""
+    from tests.test_gpu_parity import expected_e_bits
+    z = O.hash_heads(O.project(ids, P), L.multipliers, L.primes, w.N, w.K, prev)
+    e_bits = expected_e_bits(w, z.reshape(-1, w.R), L)
+    return O.quantize_rows_e4m3(O.bf16_to_f64(e_bits.reshape(-1, w.d_mem)))
+
+
+@pytest.mark.parametrize("host", [False, True])
+def test_stage_a_e4m3_is_the_quantised_stage_a(host):
+    """engram_stage_a_e4m3's codes and scales: byte for byte what quantize_fp8
+    makes of stage_a's rows, and the oracle's quantisation of its rows; two
+    layers in one launch, with state ids, give each layer's."""
+    from hashed_gram_embedding_engram_gb300 import stage_a_layers_e4m3
+    from tests.gpu_helpers import to_torch
+    w = SMALL_BF16.scaled(B=5, T=91)
+    ids, P = W.token_stream(w), W.projection_map(w)
+    Ls = [W.layer_inputs(w, lid) for lid in (1, 15)]
+    built = [make_layer(w, L, P, ids.size) for L in Ls]
+    ids_d = torch.from_numpy(ids).cuda()
+    rng = np.random.default_rng(3)
+    prev = [rng.integers(0, w.V_proj, size=(w.B, w.N - 1)).astype(np.int32) for _ in Ls]
+    prev_d = [torch.from_numpy(p).cuda() for p in prev]
+    tables = [to_torch(L.table, "bf16", "cpu", pin=True) if host else b[1].table for L, b in zip(Ls, built)]
+    outs = stage_a_layers_e4m3([b[0] for b in built], ids_d, built[0][2], tables, prev_ids=prev_d)
+    for (plan, weights, proj, _), L, (q, sc), tab, pv, pvd in zip(built, Ls, outs, tables, prev, prev_d):
+        e = plan.stage_a(ids_d, proj, tab, prev_ids=pvd)
+        q_ref, sc_ref = plan.quantize_fp8(e)
+        assert torch.equal(q, q_ref) and torch.equal(sc, sc_ref)
+        q_o, s_o = _codes_ref(w, ids, P, L, pv)
+        assert np.array_equal(q.view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy(), q_o)
+        assert np.array_equal(sc.cpu().numpy().astype(np.float64), s_o)
+        assert plan.get_error() == (0, 0)
+
+
+def test_stage_b_e4m3_and_forward_equal_the_quantising_stage_b():
+    """Stage B from the gather's codes, and engram_forward (whose gather now
+    writes the codes), give the bits of stage_a + stage_b with the separate
+    quantisation launch."""
+    w = SMALL_BF16
+    ids, P, L = W.token_stream(w), W.projection_map(w), W.layer_inputs(w, 1)
+    plan, w8, _, proj, H0 = fp8_layer(w, L, P, ids.size)
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = H0.clone()
+    plan.stage_b(plan.stage_a(ids_d, proj, w8.table), w8, ref)
+    got_b = H0.clone()
+    q, sc = plan.stage_a_e4m3(ids_d, proj, w8.table)
+    plan.stage_b_e4m3(q, sc, w8, got_b)
+    got_f = H0.clone()
+    plan.forward(ids_d, proj, w8, got_f)
+    assert plan.get_error() == (0, 0)
+    for got in (got_b, got_f):
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+def test_e4m3_gather_refuses_what_it_does_not_cover():
+    from hashed_gram_embedding_engram_gb300 import EngramError
+    # 24 rows of 128 bytes: 192 chunks per token, more than one round of loads
+    w = SMALL_MB
+    ids, P, L = W.token_stream(w), W.projection_map(w), W.layer_inputs(w, 1)
+    plan, w8, _, proj, H0 = fp8_layer(w, L, P, ids.size)
+    with pytest.raises(EngramError):
+        plan.stage_a_e4m3(torch.from_numpy(ids).cuda(), proj, w8.table)
+    # int8 tables
+    wi = W.INT8_HOST.scaled(B=2, T=50, V=5000, V_proj=3850, prime_target=3001, d=256, span_copies=2)
+    idi, Pi, Li = W.token_stream(wi), W.projection_map(wi), W.layer_inputs(wi, 1)
+    pi, wti, proji, _ = make_layer(wi, Li, Pi, idi.size)
+    with pytest.raises(EngramError):
+        pi.stage_a_e4m3(torch.from_numpy(idi).cuda(), proji, wti.table)
+    # Stage B from codes needs the FP8 weights
+    w = SMALL_BF16
+    ids, P, L = W.token_stream(w), W.projection_map(w), W.layer_inputs(w, 1)
+    plan, weights, proj, H0 = make_layer(w, L, P, ids.size)
+    q, sc = plan.stage_a_e4m3(torch.from_numpy(ids).cuda(), proj, weights.table)
+    with pytest.raises(EngramError):
+        plan.stage_b_e4m3(q, sc, weights, H0.clone())
+    assert plan.get_error() == (0, 0)
