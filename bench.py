@@ -210,6 +210,8 @@ NAME_SETS_FP8 = {3: ["hash_gather_e4m3", "kv_gemm_fp8", "conv"],
                  4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "conv"],
                  5: ["hash_gather", "quantize_e", "kv_gemm_fp8", "finalize", "conv"]}
 NAME_SETS_DECODE = {1: ["decode_step"], 3: ["hash_gather", "kv_gemm", "decode_tail"]}
+NAME_SETS_DECODE_FP8 = {3: ["hash_gather_e4m3", "kv_gemm_fp8", "decode_tail"],
+                        4: ["hash_gather", "quantize_e", "kv_gemm_fp8", "decode_tail"]}
 
 
 def trace_kernels(layers, ids, flush, reps: int, w, peaks: dict, fp8: bool = False, decode: bool = False,
@@ -222,7 +224,7 @@ def trace_kernels(layers, ids, flush, reps: int, w, peaks: dict, fp8: bool = Fal
     import torch
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     tc_peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops", 1900.0)
-    name_sets = NAME_SETS_DECODE if decode else (NAME_SETS_FP8 if fp8 else NAME_SETS)
+    name_sets = (NAME_SETS_DECODE_FP8 if fp8 else NAME_SETS_DECODE) if decode else (NAME_SETS_FP8 if fp8 else NAME_SETS)
     names, dur = None, {}
     for ly in layers:
         ly["plan"].set_timing(True)
