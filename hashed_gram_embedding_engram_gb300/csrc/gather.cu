@@ -210,19 +210,19 @@ __global__ void __launch_bounds__(kBlk, kThreads * 8 / kBlk)
           const int f = f0 + j * 32 + lane;
           if (f < per_tok) qd[f] = e4m3::quant8(v[j], inv);
         }
-        continue;
-      }
+      } else {
 #pragma unroll
-      for (int j = 0; j < kWarpItems; ++j) {
-        const int f = f0 + j * 32 + lane;
-        if (f < per_tok) {
-          if constexpr (kInt8) {
-            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (ok[j]) dequant16(v[j], s_[j], o0, o1);
-            dst[2 * f] = o0;
-            dst[2 * f + 1] = o1;
-          } else {
-            dst[f] = v[j];
+        for (int j = 0; j < kWarpItems; ++j) {
+          const int f = f0 + j * 32 + lane;
+          if (f < per_tok) {
+            if constexpr (kInt8) {
+              uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+              if (ok[j]) dequant16(v[j], s_[j], o0, o1);
+              dst[2 * f] = o0;
+              dst[2 * f + 1] = o1;
+            } else {
+              dst[f] = v[j];
+            }
           }
         }
       }
