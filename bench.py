@@ -724,10 +724,11 @@ def cpu_baseline_subprocess(w, threads: int = 0, T_sample: int = 0, min_seconds:
 
 
 def other_workloads(args) -> dict:
-    """The other workloads' own lines (decode, int8 host tables, multi-branch),
-    each from a child process on the same GPU with its own step count."""
+    """The other workloads' own lines (decode, int8 host tables, multi-branch, the
+    prefill workload with the e4m3 projection), each from a child process on the
+    same GPU with its own step count."""
     out = {}
-    for name, steps in (("decode_bf16", 300), ("int8_host", 30), ("multibranch_n4", 20)):
+    for name, steps in (("decode_bf16", 300), ("int8_host", 30), ("multibranch_n4", 20), ("prefill_fp8", 300)):
         cmd = [sys.executable, os.path.abspath(__file__), "--workload", name, "--steps", str(steps), "--warmup", "3"]
         try:
             r = subprocess.run(cmd, capture_output=True, text=True, timeout=1200)
