@@ -881,6 +881,7 @@ engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_
   const int64_t e_row = static_cast<int64_t>(plan->d_mem) * ab;                    // bytes of e per token
   const int64_t h_row = static_cast<int64_t>(plan->cfg.M) * plan->cfg.d * ab;      // bytes of H per token
   const int L = plan->L_ring, N = plan->cfg.N, Md = plan->cfg.M * plan->cfg.d;
+  const bool codes = w->w_kv_fp8 != nullptr && !cache && engram::gather_e4m3_applies(plan);
   // each group's grids sized for its SMs; the two-launch Stage B on one SM per CTA (its
   // one-launch and CTA-pair forms need every SM or clusters): the same bits in every form
   struct Saved {
@@ -921,18 +922,22 @@ engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_
       st_i.pos = state->pos + lo;
     }
     const int32_t* prev_i = state ? st_i.prev_ids : nullptr;
+    // with e4m3 weights the gather writes the piece's codes and scales where it can (as engram_forward)
+    uint8_t* e8_i = codes ? ws.e8 + t0 * plan->d_mem : nullptr;
+    float* es_i = codes ? ws.e_scale + t0 : nullptr;
     const cudaError_t ga =
-        cache ? engram::launch_hash_gather_cached(plan, ids + t0, nb, T, proj, V, prev_i, cache->table,
-                                                  static_cast<const uint16_t*>(sc), e_i, cache->slot, cache->rows,
-                                                  cache->stats, sa, cache->table_on_host)
-              : engram::launch_hash_gather(plan, ids + t0, nb, T, proj, V, prev_i, tab,
-                                           static_cast<const uint16_t*>(sc), e_i, sa, host);
+        codes ? engram::launch_hash_gather_e4m3(plan, ids + t0, nb, T, proj, V, prev_i, tab, e8_i, es_i, sa, host)
+        : cache ? engram::launch_hash_gather_cached(plan, ids + t0, nb, T, proj, V, prev_i, cache->table,
+                                                    static_cast<const uint16_t*>(sc), e_i, cache->slot, cache->rows,
+                                                    cache->stats, sa, cache->table_on_host)
+                : engram::launch_hash_gather(plan, ids + t0, nb, T, proj, V, prev_i, tab,
+                                             static_cast<const uint16_t*>(sc), e_i, sa, host);
     if (ga != cudaSuccess || !order(sa, sb, engram::split_event(split, 1 + i))) {
       status = ENGRAM_ERR_CUDA;
       break;
     }
-    status = run_stage_b(plan, ws, e_i, ids + t0, proj, V, nb, T, w, static_cast<char*>(H) + t0 * h_row,
-                         state ? &st_i : nullptr, sb);
+    status = run_stage_b(plan, ws, codes ? nullptr : e_i, ids + t0, proj, V, nb, T, w,
+                         static_cast<char*>(H) + t0 * h_row, state ? &st_i : nullptr, sb, e8_i, es_i);
   }
   // `stream` waits for both groups, also after an error, so that no work of this call is left unordered
   if (!order(sa, s, engram::split_event(split, n_pieces + 1)) || !order(sb, s, engram::split_event(split, n_pieces + 2)))

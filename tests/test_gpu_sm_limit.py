@@ -282,3 +282,24 @@ def test_forward_split_matches_oracle(split, name):
     torch.cuda.synchronize()
     assert plan.get_error() == (0, 0)
     assert_close(act_to_f64(H), ref["H_new"], w.act_dtype, name)
+
+
+def test_forward_split_with_the_e4m3_projection(split):
+    """e4m3 weights: every piece's gather writes its codes (as engram_forward's
+    does); the same bits as the plain forward."""
+    import dataclasses
+    w = BF16.scaled(B=4, T=333)
+    ids = W.token_stream(w)
+    P = W.projection_map(w)
+    L = W.layer_inputs(w, 1)
+    plan, weights, proj, H0 = make_layer(w, L, P, ids.size, table_on_host=True)
+    q, sc = plan.quantize_fp8(weights.w_kv)
+    w8 = dataclasses.replace(weights, w_kv=None, w_kv_fp8=q, w_kv_scale=sc)
+    ids_d = torch.from_numpy(ids).cuda()
+    ref = H0.clone()
+    plan.forward(ids_d, proj, w8, ref)
+    got = H0.clone()
+    plan.forward_split(split, 3, ids_d, proj, w8, got)
+    torch.cuda.synchronize()
+    assert plan.get_error() == (0, 0)
+    assert torch.equal(bits(got), bits(ref))
