@@ -441,7 +441,8 @@ engram_status_t engram_plan_set_host_gather_sms(engram_plan_t* plan, int n_sms);
  * the CUDA runtime, or PyTorch) is used as is, and events order them against
  * any other stream.  A driver without green contexts, or a split the driver
  * refuses: ENGRAM_ERR_UNSUPPORTED.  The split owns both streams; destroy it
- * after the work on them has completed.
+ * after the work on them has completed, and after any CUDA graph captured
+ * from them (engram_forward_split inside a capture) has been destroyed.
  * engram_sm_split_sms: the SMs of group 0 or 1 (0 for a null split or
  * another group).  engram_sm_split_stream: that group's stream (a
  * cudaStream_t; null for a null split or another group). */
