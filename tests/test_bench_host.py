@@ -26,6 +26,22 @@ def test_per_token_work_of_the_prefill_workload():
     assert work["conv"] == ("bytes", 4 * 1024 + 8 + 2 * 2 * 1024)
 
 
+def test_every_traced_kernel_name_has_its_work():
+    """Each name the per-kernel tracing can assign has an algorithmic amount, so a
+    traced interval is never reported without a roofline denominator; the codes
+    gather moves the rows in and the codes and scale out (no bf16 e)."""
+    import workloads as W
+    for w in W.ALL:
+        work = bench.per_token_work(w)
+        for sets in (bench.NAME_SETS, bench.NAME_SETS_FP8, bench.NAME_SETS_DECODE, bench.NAME_SETS_DECODE_FP8):
+            for names in sets.values():
+                for n in names:
+                    assert n in work, (w.name, n)
+    w = W.PREFILL_BF16
+    work = bench.per_token_work(w)
+    assert work["hash_gather_e4m3"] == ("bytes", 8 + 16 * 128 + 1024 + 4)
+
+
 def test_reference_arm_generates_its_inputs_once(monkeypatch, capsys):
     """The reference arm times the oracle on a sample per step; the layers'
     tables are generated once per process, not once per step, so the run's
