@@ -908,11 +908,19 @@ engram_status_t engram_forward_split(engram_plan_t* plan, const engram_sm_split_
   // both groups' streams start after the work already on `stream`
   if (!order(s, sa, engram::split_event(split, 0)) || cudaStreamWaitEvent(sb, engram::split_event(split, 0), 0))
     return ENGRAM_ERR_CUDA;
+  // piece boundaries: with three pieces or more, the first and the last are half the size of the others,
+  // so that the pipeline's fill (the first lookup) and drain (the last Stage B) are short
+  auto piece_start = [&](int i) -> int {
+    if (i <= 0) return 0;
+    if (i >= n_pieces) return B;
+    if (n_pieces <= 2) return static_cast<int>(static_cast<int64_t>(B) * i / n_pieces);
+    return static_cast<int>((static_cast<int64_t>(B) * (2 * i - 1) + (n_pieces - 1)) / (2 * (n_pieces - 1)));
+  };
   engram_status_t status = ENGRAM_OK;
   for (int i = 0; i < n_pieces && status == ENGRAM_OK; ++i) {
-    const int lo = static_cast<int>(static_cast<int64_t>(B) * i / n_pieces);
-    const int hi = static_cast<int>(static_cast<int64_t>(B) * (i + 1) / n_pieces);
+    const int lo = piece_start(i), hi = piece_start(i + 1);
     const int nb = hi - lo;
+    if (nb == 0) continue;
     const int64_t t0 = static_cast<int64_t>(lo) * T;
     void* e_i = static_cast<char*>(ws.e) + t0 * e_row;
     engram_state_t st_i{};

@@ -453,7 +453,9 @@ void* engram_sm_split_stream(const engram_sm_split_t* split, int group);
 engram_status_t engram_sm_split_destroy(engram_sm_split_t* split);
 
 /* engram_forward (Steps 1-8) of B sequences in n_pieces pieces of whole
- * sequences (piece i: sequences [B*i/n_pieces, B*(i+1)/n_pieces)) on an SM
+ * sequences (with n_pieces >= 3 the first and the last piece hold half as
+ * many sequences as the others, so that the pipeline fills and drains fast;
+ * with 1 or 2, equal pieces) on an SM
  * split: every piece's Stage A on group 0's stream, each piece's Stage B on
  * group 1's stream as soon as its rows are in, so the lookup of piece i+1
  * runs beside the projection and conv of piece i ("DeepSeek Engram 系列导读",
