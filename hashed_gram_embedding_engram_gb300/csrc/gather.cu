@@ -19,6 +19,11 @@
 // (lane i holds x'_{t-i}) and broadcasts it by shuffle; lane r computes the
 // index of row r once, and the lanes reading that row's chunks get its
 // address by shuffle.
+//
+// Variants: tokens of at most 16 rows and 64 chunks (int8 rows of 64 bytes)
+// take half a warp each (row_gather_half_kernel), so a warp carries two
+// tokens' rows at once; for the FP8 projection the row kernel can write the
+// token's e4m3 codes and scale instead of e (kQ8, the rule of e4m3.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
