@@ -118,6 +118,32 @@ def test_null_plan_is_refused_everywhere(lib):
     assert lib.engram_get_error(None, None, None) == _lib.ERR_INVALID_ARG
 
 
+def test_newer_entry_points_refuse_null_and_bad_sizes_before_cuda(lib):
+    """The several-layer, FP8, split and option entry points check their handles
+    and sizes on the host: no CUDA call is needed to refuse these."""
+    from hashed_gram_embedding_engram_gb300 import _lib
+    bad = _lib.ERR_INVALID_ARG
+    assert lib.engram_stage_a(None, None, 1, 1, None, 1, None, None, None, None, None) == bad
+    assert lib.engram_stage_a_layers(0, None, None, 1, 1, None, 1, None, None, None, None, None) == bad
+    assert lib.engram_stage_a_layers(9, None, None, 1, 1, None, 1, None, None, None, None, None) == bad
+    assert lib.engram_stage_a_e4m3(None, None, 1, 1, None, 1, None, None, None, None, None) == bad
+    assert lib.engram_stage_a_layers_e4m3(0, None, None, 1, 1, None, 1, None, None, None, None, None) == bad
+    assert lib.engram_stage_b_e4m3(None, None, 1, 1, None, 1, None, None, None, None, None, None, 0, None) == bad
+    assert lib.engram_forward_split(None, None, 1, None, None, 1, 1, None, 1, None, None, None, None, 0,
+                                    None) == bad
+    assert lib.engram_plan_set_sm_limit(None, 1) == bad
+    assert lib.engram_plan_set_host_gather_sms(None, 1) == bad
+    assert lib.engram_plan_host_gather_sms(None) == 0
+    out = ctypes.c_void_p()
+    for n in (0, -1):
+        assert lib.engram_sm_split_create(0, n, ctypes.byref(out)) == bad
+        assert not out.value
+    assert lib.engram_sm_split_create(0, 8, None) == bad
+    assert lib.engram_sm_split_sms(None, 0) == 0
+    assert lib.engram_sm_split_stream(None, 1) is None
+    assert lib.engram_sm_split_destroy(None) == _lib.OK
+
+
 def test_front_end_fails_loudly_without_library(monkeypatch, tmp_path):
     from hashed_gram_embedding_engram_gb300 import _lib
     monkeypatch.setattr(_lib, "_LIB", None)
