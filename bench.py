@@ -1250,10 +1250,11 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
-                    help="skip the decode, int8 host-table and multi-branch lines embedded in the default run")
+                    help="skip the decode, int8 host-table, multi-branch and FP8-prefill lines embedded in the default run")
     ap.add_argument("--workload", default="prefill_bf16",
                     help="prefill_bf16 (the headline line); prefill_fp8 (the same with the e4m3 K/V "
-                         "projection), decode_bf16, int8_host or multibranch_n4 print that workload's own line")
+                         "projection), decode_bf16, int8_host or multibranch_n4 (any of them with _fp8 appended: "
+                         "the e4m3 projection) print that workload's own line")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                     help="run a small case for a profiler capture (no timing, no JSON line)")
     args = ap.parse_args()
